@@ -1,0 +1,211 @@
+/*
+ * kvinc.h -- C ABI of a GB300 (sm_103a) library for incremental decoding
+ * against a preallocated per-row KV cache.
+ *
+ * The caller owns a model; per layer and step it hands the library the new
+ * tokens' pre-RoPE queries, keys and values.  The library rotates them (RoPE
+ * at each row's absolute positions), appends keys and values to the layer's
+ * cache, and returns the attention output of every new token.
+ *
+ * Sources (web pages, by title and section):
+ *  [G]  tiny_agent/generate.py -- `KVCache` (global cache with a scratch
+ *       slot, per-layer W-slot ring with a scratch slot, lens mirrored on the
+ *       host), `reset`, `append` (right-padded chunk, n_new per row, optional
+ *       rows, "KV cache full" raised before any write, sub-chunks of CHUNK=64),
+ *       `_append_chunk` (pos = lens + i, pads to the scratch slot, keep the
+ *       last W real tokens, ring slot pos % W, grouped queries read the cache
+ *       directly), `_rope_pos` (half-split RoPE).
+ *  [T]  tinyllm/kv_cache.py -- `SlotKVCache` (per-slot lengths; the device
+ *       half of end_step adds the active mask; begin/update/end protocol).
+ *  [P]  pycraft-1 model/kv_cache.py -- `KVCache.update` (does NOT advance;
+ *       overflow, batch and dtype guards), `advance`, `reset` (no memset),
+ *       `memory_bytes`; pre-expansion (n_kv_heads) post-RoPE storage.
+ *  [I]  "inkling: ring-buffer KV cache for sliding-window layers" -- "How it
+ *       works": ring rows = window when 0 < window < max_t else max_t; the
+ *       current batch is read from scratch before the ring append; the append
+ *       skips rows the batch would overwrite; a fail-fast bound check.
+ *  [L]  Lab 07 -- KV cache and sampling -- section 2 (query i sees key
+ *       j <= pos + i), section 3 (chunked prefill equals one pass), the note
+ *       that the model advances the cache once after all layers updated.
+ *
+ * Conventions for every entry point:
+ *  - Return value: KV_OK or a kv_status code; kv_strerror() names it.
+ *  - Every argument is validated on the host before any work is enqueued; a
+ *    call that returns an error has changed no state (host or device).
+ *  - Device work runs asynchronously on the caller's CUDA stream (`stream`,
+ *    a cudaStream_t passed as void*, NULL = legacy default stream).  No entry
+ *    point synchronises the device unless its comment says so.
+ *  - Not thread-safe: one cache is driven from one host thread and one
+ *    stream at a time.
+ *  - Tensors are bfloat16, row-major, contiguous, 16-byte aligned.
+ */
+#ifndef KVINC_H
+#define KVINC_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct kv_cache kv_cache; /* opaque; the library owns all cache memory */
+
+/* Layer kinds of the layer layout. */
+enum kv_layer_kind {
+    KV_GLOBAL = 0,  /* full-length cache, every past key visible ([G] global K/V) */
+    KV_SLIDING = 1  /* ring of W slots, keys p-W+1..p visible ([I], [G] local K/V) */
+};
+
+enum kv_status {
+    KV_OK = 0,
+    KV_ERR_ARG = 1,    /* invalid argument: sizes, layer, rows, n_new, pointers */
+    KV_ERR_FULL = 2,   /* lens[row] + n_new > max_len for some row ([G] append, [P] update) */
+    KV_ERR_DTYPE = 3,  /* tensor dtype is not bfloat16 (raised by language bindings; [P]) */
+    KV_ERR_CUDA = 4,   /* a CUDA runtime call failed */
+    KV_ERR_OOM = 5,    /* device memory allocation failed at create */
+    KV_ERR_DEVICE = 6  /* a kernel reported a timed-out wait (see kv_device_error) */
+};
+
+/*
+ * Create a cache for B rows on CUDA device `device`.  [G] KVCache, [P] KVCache,
+ * [I] kv_ring_rows.
+ *
+ *  max_len     positions per row (>= 1, <= 2^20)
+ *  Hq, Hk      query heads and key/value heads; Hq % Hk == 0, Hq/Hk <= 16
+ *  D           head dimension: 64 or 128
+ *  W           sliding window in tokens (>= 1) when any layer is KV_SLIDING,
+ *              else ignored.  A sliding layer stores R = W < max_len ? W :
+ *              max_len ring slots per (row, kv head) plus one scratch slot.
+ *  layer_kind  host array [n_layers] of kv_layer_kind
+ *  rope_theta  RoPE base (e.g. 10000); frequencies theta^(-2i/D), i < D/2
+ *
+ * Device memory, allocated here with cudaMalloc and freed by
+ * kv_cache_destroy (per layer, K and V):
+ *    global layer   [B][Hk][max_len + 1][D] bf16   (slot max_len = scratch)
+ *    sliding layer  [B][Hk][R + 1][D] bf16         (slot R = scratch)
+ * plus lens [B] and lpos [B][R] (int32), a chunk scratch [B][Hk][64][D] for K
+ * and V, the RoPE table [max_len][D/2] of (cos, sin) float pairs computed on
+ * the host in double, and split-K partials.  All lens start at 0.
+ * On success *out holds the cache; on failure *out is NULL.
+ */
+int kv_cache_create(kv_cache **out, int B, int max_len, int Hq, int Hk, int D, int W,
+                    int n_layers, const int32_t *layer_kind, double rope_theta, int device);
+
+/* Free all device and host memory of the cache (NULL is a no-op).  Waits for
+ * the device to finish work that uses the cache. */
+void kv_cache_destroy(kv_cache *c);
+
+/*
+ * Empty rows so new sequences can start there.  [G] reset, [P] reset.
+ *  rows  host int32 [n_rows], distinct, in [0, B)
+ * Sets lens[row] = 0 (host mirror and device) and lpos[row][*] = -1.  Cached
+ * K/V are not cleared: stale slots are never read, because every key a
+ * query can see was written after the reset.
+ */
+int kv_reset(kv_cache *c, const int32_t *rows, int n_rows, void *stream);
+
+/*
+ * Append one layer's new tokens and return their attention outputs.
+ * [G] append / _append_chunk, [P] update, [I], [L] sections 2-3.
+ *
+ *  layer   0 <= layer < n_layers
+ *  q       device bf16 [Bs][C][Hq][D]   pre-RoPE queries
+ *  k, v    device bf16 [Bs][C][Hk][D]   pre-RoPE keys, values
+ *  Hq      must equal the cache's Hq (checked)
+ *  C       chunk width (>= 1); row i carries n_new[i] real tokens at
+ *          t = 0..n_new[i]-1, the rest of the row is padding
+ *  n_new   host int32 [Bs], each in [0, C]; 0 leaves the row untouched
+ *  rows    host int32 [Bs] cache rows (distinct, in [0, B)), or NULL for
+ *          rows 0..Bs-1
+ *  out     device bf16 [Bs][C][Hq][D]; for every real token t of row i,
+ *          out[i][t][h] = softmax over the visible keys of
+ *          (rope(q,p) . K_j) / sqrt(D), times V_j, at p = lens[row] + t,
+ *          with head h reading kv head h / (Hq/Hk).  Visible keys: j <= p
+ *          (global) or p-W < j <= p (sliding), the chunk's own earlier
+ *          tokens included.  Padding positions of `out` are not written.
+ *
+ * Effects on layer `layer`: rope(k, p) and v are stored at position p of
+ * every real token (global: cache slot p; sliding: ring slot p % R for the
+ * last min(n_new, W) tokens of the row only -- [G] keep rule, [I] skip
+ * rule).  lens is NOT advanced: every layer of a step sees the same
+ * positions, and the caller ends the step with kv_advance ([P] update/
+ * advance, [L]).  Tokens are processed in sub-chunks of 64 per row.
+ * Errors: KV_ERR_FULL if lens[row] + n_new[i] > max_len for any row,
+ * KV_ERR_ARG for bad sizes, rows, counts or pointers.
+ */
+int kv_append(kv_cache *c, int layer, const void *q, const void *k, const void *v, int Hq,
+              int C, const int32_t *n_new, const int32_t *rows, int Bs, void *out,
+              void *stream);
+
+/*
+ * Same as kv_append, but q, k, v and out are HOST buffers (pinned memory
+ * gives asynchronous copies).  The library copies the inputs into device
+ * staging buffers it owns, runs kv_append on them and copies the outputs
+ * back, all on `stream`; the call returns before the copies finish, so the
+ * caller synchronises the stream before reading `out`.  Staging buffers are
+ * allocated on the first call and grown when a larger call arrives.
+ */
+int kv_append_host(kv_cache *c, int layer, const void *q, const void *k, const void *v,
+                   int Hq, int C, const int32_t *n_new, const int32_t *rows, int Bs,
+                   void *out, void *stream);
+
+/*
+ * End a step: lens[row] += n_new[i] (host mirror and device) and record the
+ * ring-slot positions lpos[row][p % R] = p of the kept tokens.  Call once per
+ * step, after every layer has been appended with the same n_new and rows.
+ * [P] advance, [T] end_step, [L] "who advances the cache".
+ * Errors: as kv_append (KV_ERR_FULL, KV_ERR_ARG); nothing changes on error.
+ */
+int kv_advance(kv_cache *c, const int32_t *n_new, const int32_t *rows, int Bs, void *stream);
+
+/* Bytes of K and V storage of all layers, scratch slots included ([G] nbytes,
+ * [P] memory_bytes).  -1 for a NULL cache. */
+int64_t kv_nbytes(const kv_cache *c);
+
+/* Copy the host mirror of lens into lens_out (host int32 [B]).  No device sync. */
+int kv_get_lens(const kv_cache *c, int32_t *lens_out);
+
+/* Device pointers of a layer's K and V storage and of lpos ([B][R] int32, or
+ * NULL without sliding layers), for inspection and tests.  Layouts as in
+ * kv_cache_create.  The pointers stay owned by the cache. */
+int kv_debug_ptrs(const kv_cache *c, int layer, void **K, void **V, int32_t **lpos);
+
+/* Shape query: fills any non-NULL output with the cache's parameters. */
+int kv_get_config(const kv_cache *c, int *B, int *max_len, int *Hq, int *Hk, int *D, int *W,
+                  int *R, int *n_layers);
+
+/* Read and clear the device error word (0 = no kernel reported a timed-out
+ * wait).  SYNCHRONISES the device.  Returns KV_ERR_DEVICE when the word was
+ * non-zero, else KV_OK. */
+int kv_device_error(kv_cache *c, int32_t *code_out);
+
+/*
+ * Kernel timing for measurement.  kv_profile_enable(c, 1) makes the library
+ * record a CUDA event pair around each kernel launch it makes, on the stream
+ * of the launch; kv_profile_read sums, per kernel kind, the launches, the
+ * event-timed milliseconds (it SYNCHRONISES the device) and the algorithmic
+ * bytes the host counted for those launches; kv_profile_enable(c, 0) or a read
+ * with reset=1 clears the record.  Kinds: KV_KERNEL_APPEND, KV_KERNEL_DECODE,
+ * KV_KERNEL_COMBINE, KV_KERNEL_PREFILL, KV_KERNEL_COMMIT, KV_KERNEL_STATE.
+ */
+enum kv_kernel_kind {
+    KV_KERNEL_APPEND = 0,
+    KV_KERNEL_DECODE = 1,
+    KV_KERNEL_COMBINE = 2,
+    KV_KERNEL_PREFILL = 3,
+    KV_KERNEL_COMMIT = 4,
+    KV_KERNEL_STATE = 5,
+    KV_KERNEL_NKINDS = 6
+};
+int kv_profile_enable(kv_cache *c, int enable);
+int kv_profile_read(kv_cache *c, int kind, int reset, int64_t *launches, double *total_ms,
+                    double *alg_bytes, double *alg_flops);
+
+/* Static name of a status code. */
+const char *kv_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVINC_H */

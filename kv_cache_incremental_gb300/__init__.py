@@ -1,0 +1,187 @@
+"""Python binding of libkvinc: a preallocated per-row KV cache for incremental decoding
+on one GB300.
+
+Argument marshalling only: every step of the path (RoPE, append, attention, ring
+commit, state updates) runs in the library's CUDA kernels.  PyTorch provides device
+memory and streams.  Importing this package loads ``libkvinc.so`` (building it
+in-tree when absent) and raises if that fails -- there is no CPU fallback.
+
+    cache = KVCache(B=64, max_len=8192, Hq=32, Hk=8, D=128)
+    out = cache.append(0, q, k, v, n_new)     # per layer; does not advance
+    cache.advance(n_new)                      # once per step, after all layers
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional, Sequence
+
+from ._lib import (KERNELS, KV_GLOBAL, KV_SLIDING, KVCacheFull, KVError, check, load)
+
+__all__ = ["KVCache", "KVError", "KVCacheFull", "KV_GLOBAL", "KV_SLIDING", "load"]
+
+_clib = load()
+
+
+def _i32_array(values) -> Optional[ctypes.Array]:
+    if values is None:
+        return None
+    vals = [int(x) for x in values]
+    return (ctypes.c_int32 * max(1, len(vals)))(*vals)
+
+
+def _stream_ptr(stream, device):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+class _DevArray:
+    """Zero-copy __cuda_array_interface__ view of library-owned device memory."""
+
+    def __init__(self, ptr: int, shape, typestr: str):
+        self.__cuda_array_interface__ = {"shape": tuple(shape), "typestr": typestr,
+                                         "data": (ptr, False), "version": 3, "strides": None}
+
+
+class KVCache:
+    """A cache of B rows; see include/kvinc.h for the full contract."""
+
+    def __init__(self, B: int, max_len: int, Hq: int, Hk: int, D: int, W: int = 0,
+                 layer_kinds: Sequence[int] = (KV_GLOBAL,), rope_theta: float = 1e4,
+                 device: int = 0):
+        kinds = _i32_array(layer_kinds)
+        h = ctypes.c_void_p()
+        check(_clib.kv_cache_create(ctypes.byref(h), B, max_len, Hq, Hk, D, W, len(layer_kinds),
+                                   kinds, float(rope_theta), device), "kv_cache_create")
+        self._h = h
+        self.B, self.max_len, self.Hq, self.Hk, self.D, self.W = B, max_len, Hq, Hk, D, W
+        self.layer_kinds = list(layer_kinds)
+        self.device = device
+        r = ctypes.c_int()
+        _clib.kv_get_config(h, None, None, None, None, None, None, ctypes.byref(r), None)
+        self.R = r.value
+
+    # ------------------------------------------------------------------ lifecycle
+    def close(self) -> None:
+        if getattr(self, "_h", None):
+            _clib.kv_cache_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # ------------------------------------------------------------------ checks
+    def _check_tensor(self, x, name, heads, C=None, Bs=None):
+        import torch
+        if x.dtype != torch.bfloat16:
+            raise TypeError(f"{name}: cache dtype bfloat16 != incoming dtype {x.dtype}")
+        if not x.is_cuda or x.device.index != self.device:
+            raise ValueError(f"{name} must live on cuda:{self.device}")
+        if x.dim() != 4 or x.shape[2] != heads or x.shape[3] != self.D:
+            raise ValueError(f"{name}: expected (Bs, C, {heads}, {self.D}), got {tuple(x.shape)}")
+        if C is not None and (x.shape[1] != C or x.shape[0] != Bs):
+            raise ValueError(f"{name}: shape {tuple(x.shape)} does not match q")
+        if not x.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+
+    # ------------------------------------------------------------------ the path
+    def append(self, layer: int, q, k, v, n_new, rows=None, out=None, stream=None):
+        """Rotate, append and attend one layer's right-padded chunk; returns out (Bs,C,Hq,D)."""
+        import torch
+        self._check_tensor(q, "q", self.Hq)
+        Bs, C = q.shape[0], q.shape[1]
+        self._check_tensor(k, "k", self.Hk, C, Bs)
+        self._check_tensor(v, "v", self.Hk, C, Bs)
+        if out is None:
+            out = torch.empty_like(q)
+        else:
+            self._check_tensor(out, "out", self.Hq, C, Bs)
+        n = _i32_array(n_new)
+        if len(n_new) != Bs or (rows is not None and len(rows) != Bs):
+            raise ValueError("n_new and rows must have one entry per row of q")
+        check(_clib.kv_append(self._h, layer, q.data_ptr(), k.data_ptr(), v.data_ptr(), self.Hq, C,
+                             n, _i32_array(rows), Bs, out.data_ptr(),
+                             _stream_ptr(stream, q.device)), "kv_append")
+        return out
+
+    def append_host(self, layer: int, q, k, v, n_new, rows=None, out=None, stream=None):
+        """append() for CPU tensors (pinned for asynchronous copies); synchronise the stream
+        before reading `out`."""
+        import torch
+        for x, name in ((q, "q"), (k, "k"), (v, "v")):
+            if x.dtype != torch.bfloat16:
+                raise TypeError(f"{name}: cache dtype bfloat16 != incoming dtype {x.dtype}")
+            if x.is_cuda or not x.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous CPU tensor")
+        Bs, C = q.shape[0], q.shape[1]
+        if out is None:
+            out = torch.empty_like(q)
+        check(_clib.kv_append_host(self._h, layer, q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                  self.Hq, C, _i32_array(n_new), _i32_array(rows), Bs,
+                                  out.data_ptr(), _stream_ptr(stream, self.device)),
+              "kv_append_host")
+        return out
+
+    def advance(self, n_new, rows=None, stream=None) -> None:
+        """End the step: lens[row] += n_new (call once, after every layer was appended)."""
+        Bs = len(n_new)
+        check(_clib.kv_advance(self._h, _i32_array(n_new), _i32_array(rows), Bs,
+                              _stream_ptr(stream, self.device)), "kv_advance")
+
+    def reset(self, rows, stream=None) -> None:
+        rows = list(rows)
+        check(_clib.kv_reset(self._h, _i32_array(rows), len(rows),
+                            _stream_ptr(stream, self.device)), "kv_reset")
+
+    # ------------------------------------------------------------------ inspection
+    @property
+    def lens(self):
+        arr = (ctypes.c_int32 * self.B)()
+        check(_clib.kv_get_lens(self._h, arr))
+        return list(arr)
+
+    def nbytes(self) -> int:
+        return int(_clib.kv_nbytes(self._h))
+
+    def storage(self, layer: int):
+        """Zero-copy torch views (K, V) of a layer's storage, [B, Hk, rows, D] bf16;
+        rows = max_len + 1 (global) or R + 1 (sliding).  Valid while the cache lives."""
+        import torch
+        kp, vp, lp = ctypes.c_void_p(), ctypes.c_void_p(), ctypes.c_void_p()
+        check(_clib.kv_debug_ptrs(self._h, layer, ctypes.byref(kp), ctypes.byref(vp),
+                                 ctypes.byref(lp)))
+        rows = self.R + 1 if self.layer_kinds[layer] == KV_SLIDING else self.max_len + 1
+        shape = (self.B, self.Hk, rows, self.D)
+        dev = f"cuda:{self.device}"
+        K = torch.as_tensor(_DevArray(kp.value, shape, "<i2"), device=dev).view(torch.bfloat16)
+        V = torch.as_tensor(_DevArray(vp.value, shape, "<i2"), device=dev).view(torch.bfloat16)
+        return K, V
+
+    def lpos(self):
+        """Zero-copy view of lpos [B, R] int32 (position held by each ring slot, -1 empty)."""
+        import torch
+        lp = ctypes.c_void_p()
+        check(_clib.kv_debug_ptrs(self._h, 0, None, None, ctypes.byref(lp)))
+        if not lp.value:
+            return None
+        return torch.as_tensor(_DevArray(lp.value, (self.B, self.R), "<i4"),
+                               device=f"cuda:{self.device}")
+
+    def device_error(self) -> int:
+        code = ctypes.c_int32()
+        _clib.kv_device_error(self._h, ctypes.byref(code))
+        return code.value
+
+    # ------------------------------------------------------------------ profiling
+    def profile(self, enable: bool = True) -> None:
+        check(_clib.kv_profile_enable(self._h, 1 if enable else 0))
+
+    def profile_read(self, kernel: str, reset: bool = False) -> dict:
+        n, ms, by, fl = ctypes.c_int64(), ctypes.c_double(), ctypes.c_double(), ctypes.c_double()
+        check(_clib.kv_profile_read(self._h, KERNELS[kernel], 1 if reset else 0, ctypes.byref(n),
+                                   ctypes.byref(ms), ctypes.byref(by), ctypes.byref(fl)))
+        return {"launches": n.value, "ms": ms.value, "bytes": by.value, "flops": fl.value}

@@ -1,0 +1,734 @@
+// host.cu -- the C ABI: cache creation, argument validation, the per-call
+// plan (sub-chunks, decode / chunk rows, split-K schedule) and kernel launches.
+//
+// The plan uses only host data: n_new and rows arrive in host memory and lens
+// is mirrored on the host (tiny_agent/generate.py keeps `lens_cpu` for the same
+// reason), so no call reads device memory back.  Every check runs before the
+// first enqueue, so a rejected call changes nothing (pycraft-1 `update` guards;
+// "KV cache full" is raised before any write in tiny_agent/generate.py
+// `append`).
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <vector>
+
+#include "../../include/kvinc.h"
+#include "kvinc_internal.h"
+
+namespace kvinc {
+cudaError_t configure_decode();
+cudaError_t configure_prefill();
+}  // namespace kvinc
+
+using namespace kvinc;
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 2-D bf16 view [rows][D] with 64-column x kTileKeys-row boxes, 128-byte swizzle.
+bool make_tmap(CUtensorMap *m, void *base, int64_t rows, int D) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)kTileKeys};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct DeviceGuard {
+  int prev = -1;
+  bool changed = false;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) == cudaSuccess && prev != dev) {
+      changed = cudaSetDevice(dev) == cudaSuccess;
+    }
+  }
+  ~DeviceGuard() {
+    if (changed) cudaSetDevice(prev);
+  }
+};
+
+struct ProfRec {
+  cudaEvent_t a, b;
+  int kind;
+  double bytes, flops;
+};
+
+constexpr size_t kMaxProfRecs = 1 << 16;
+
+}  // namespace
+
+struct kv_cache {
+  int B, max_len, Hq, Hk, D, W, R, n_layers, device, num_sms;
+  double theta;
+  std::vector<int32_t> kind;
+  std::vector<int32_t> lens;  // host mirror
+  std::vector<void *> K, V;
+  std::vector<int> seg_rows;
+  std::vector<CUtensorMap> tmK, tmV;
+  CUtensorMap tmSK, tmSV;
+  void *scrK = nullptr, *scrV = nullptr;
+  float2 *rope = nullptr;
+  int32_t *lens_dev = nullptr, *lpos = nullptr, *err = nullptr;
+  float *part_o = nullptr;
+  float2 *part_ml = nullptr;
+  // host-buffer entry point staging
+  void *stage = nullptr;
+  size_t stage_bytes = 0;
+  // profiling
+  bool prof = false;
+  std::vector<ProfRec> recs;
+  std::vector<cudaEvent_t> free_events;
+};
+
+namespace {
+
+int set_err(cudaError_t e) { return e == cudaSuccess ? KV_OK : KV_ERR_CUDA; }
+
+cudaEvent_t take_event(kv_cache *c) {
+  if (!c->free_events.empty()) {
+    cudaEvent_t e = c->free_events.back();
+    c->free_events.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+// Launch `fn` with an optional event pair around it.
+template <class F>
+cudaError_t timed(kv_cache *c, int kind, double bytes, double flops, cudaStream_t s, F fn) {
+  if (!c->prof || c->recs.size() >= kMaxProfRecs) return fn();
+  ProfRec r{take_event(c), take_event(c), kind, bytes, flops};
+  if (!r.a || !r.b) return fn();
+  cudaEventRecord(r.a, s);
+  cudaError_t e = fn();
+  cudaEventRecord(r.b, s);
+  c->recs.push_back(r);
+  return e;
+}
+
+// Validate (n_new, rows) against the cache; fills the effective cache rows.
+int check_rows(const kv_cache *c, const int32_t *n_new, const int32_t *rows, int Bs, int C,
+               std::vector<int32_t> &cache_rows) {
+  if (Bs < 0 || Bs > c->B) return KV_ERR_ARG;
+  if (Bs > 0 && !n_new) return KV_ERR_ARG;
+  cache_rows.resize(Bs);
+  std::vector<char> seen(c->B, 0);
+  for (int i = 0; i < Bs; ++i) {
+    const int r = rows ? rows[i] : i;
+    if (r < 0 || r >= c->B || seen[r]) return KV_ERR_ARG;
+    seen[r] = 1;
+    cache_rows[i] = r;
+    if (n_new[i] < 0 || n_new[i] > C) return KV_ERR_ARG;
+  }
+  for (int i = 0; i < Bs; ++i)
+    if ((int64_t)c->lens[cache_rows[i]] + n_new[i] > c->max_len) return KV_ERR_FULL;
+  return KV_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct DecodeIn {
+  int cache_row, call_row, pos;
+};
+
+// Split-K schedule for one batch of decode rows (<= kMaxRowsPerLaunch).
+void plan_decode(const kv_cache *c, bool sliding, const std::vector<DecodeIn> &in,
+                 DecodeParams &p, int &n_multi, CombineParams &cp, double &kv_bytes,
+                 double &flops) {
+  int64_t total_tiles = 0;
+  std::vector<int> nk(in.size());
+  for (size_t i = 0; i < in.size(); ++i) {
+    nk[i] = sliding ? std::min(in[i].pos + 1, c->R) : in[i].pos + 1;
+    total_tiles += (nk[i] + kTileKeys - 1) / kTileKeys;
+  }
+  // Aim for about four waves of two CTAs per SM; splits of at least four tiles.
+  const int64_t target = (int64_t)c->num_sms * 2 * 4;
+  int64_t per = (total_tiles * c->Hk + target - 1) / target;
+  if (per < 4) per = 4;
+  int item = 0, part = 0;
+  n_multi = 0;
+  kv_bytes = 0;
+  flops = 0;
+  for (size_t i = 0; i < in.size(); ++i) {
+    const int tiles = (nk[i] + kTileKeys - 1) / kTileKeys;
+    int ns = (int)std::min<int64_t>(kMaxSplits, (tiles + per - 1) / per);
+    if (ns < 1) ns = 1;
+    const int st = (tiles + ns - 1) / ns;
+    ns = (tiles + st - 1) / st;
+    DecodeRow &r = p.rows[i];
+    r.cache_row = in[i].cache_row;
+    r.call_row = in[i].call_row;
+    r.pos = in[i].pos;
+    r.nk = nk[i];
+    r.item0 = item;
+    r.split_len = st * kTileKeys;
+    r.n_splits = ns;
+    r.part0 = ns > 1 ? part : 0;
+    if (ns > 1) {
+      cp.call_row[n_multi] = in[i].call_row;
+      cp.part0[n_multi] = part;
+      cp.n_splits[n_multi] = ns;
+      ++n_multi;
+      part += ns;
+    }
+    item += ns;
+    kv_bytes += 2.0 * nk[i] * c->Hk * c->D * 2.0;
+    flops += 4.0 * nk[i] * c->Hq * c->D;
+  }
+  p.n_rows = (int)in.size();
+  p.n_items = item;
+  cp.n_rows = n_multi;
+}
+
+int append_device(kv_cache *c, int layer, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
+                  const __nv_bfloat16 *v, int C, const int32_t *n_new,
+                  const std::vector<int32_t> &cache_rows, int Bs, __nv_bfloat16 *out,
+                  cudaStream_t s) {
+  const bool sliding = c->kind[layer] == KV_SLIDING;
+  const int Hq = c->Hq, Hk = c->Hk, D = c->D, rep = Hq / Hk;
+  int max_n = 0;
+  for (int i = 0; i < Bs; ++i) max_n = std::max(max_n, (int)n_new[i]);
+  if (max_n == 0) return KV_OK;
+
+  const int64_t q_row = (int64_t)C * Hq * D, kv_row = (int64_t)C * Hk * D;
+  static thread_local AppendParams ap;
+  static thread_local DecodeParams dp;
+  static thread_local CombineParams cp;
+  static thread_local PrefillParams pp;
+  static thread_local CommitParams mp;
+  const float scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
+
+  for (int off = 0; off < max_n; off += kChunk) {
+    std::vector<AppendRow> arows;
+    std::vector<DecodeIn> drows;
+    std::vector<PrefillRow> prows;
+    for (int i = 0; i < Bs; ++i) {
+      const int n = n_new[i];
+      const int b = cache_rows[i];
+      if (n == 1 && off == 0) {
+        arows.push_back({b, i, c->lens[b], 1, sliding ? kDestRing : kDestGlobal, 0});
+        drows.push_back({b, i, c->lens[b]});
+      } else if (n >= 2 && n - off >= 1) {
+        const int ns = std::min(kChunk, n - off);
+        arows.push_back({b, i, c->lens[b] + off, ns, sliding ? kDestScratch : kDestGlobal, 0});
+        prows.push_back({b, i, c->lens[b] + off, ns, 0});
+      }
+    }
+
+    // ---- RoPE + append (decode rows and chunk rows of this sub-chunk)
+    for (size_t r0 = 0; r0 < arows.size(); r0 += kMaxRowsPerLaunch) {
+      const size_t r1 = std::min(arows.size(), r0 + kMaxRowsPerLaunch);
+      ap.k = k + (int64_t)off * Hk * D;
+      ap.v = v + (int64_t)off * Hk * D;
+      ap.kv_row_stride = kv_row;
+      ap.cache_k = (__nv_bfloat16 *)c->K[layer];
+      ap.cache_v = (__nv_bfloat16 *)c->V[layer];
+      ap.scr_k = (__nv_bfloat16 *)c->scrK;
+      ap.scr_v = (__nv_bfloat16 *)c->scrV;
+      ap.rope = c->rope;
+      ap.Hk = Hk;
+      ap.D = D;
+      ap.seg_rows = c->seg_rows[layer];
+      ap.ring_R = c->R;
+      ap.max_len = c->max_len;
+      ap.c_avail = C - off;
+      int blk = 0;
+      double bytes = 0;
+      for (size_t j = r0; j < r1; ++j) {
+        AppendRow r = arows[j];
+        r.blk0 = blk;
+        blk += (r.n + 7) / 8;
+        ap.rows[j - r0] = r;
+        bytes += 4.0 * r.n * Hk * D * 2.0;
+      }
+      ap.n_rows = (int)(r1 - r0);
+      ap.n_blocks = blk;
+      cudaError_t e = timed(c, KV_KERNEL_APPEND, bytes, 0, s, [&] { return launch_append(ap, s); });
+      if (e != cudaSuccess) return KV_ERR_CUDA;
+    }
+
+    // ---- split-K decode + combine for single-token rows
+    for (size_t r0 = 0; r0 < drows.size(); r0 += kMaxRowsPerLaunch) {
+      const size_t r1 = std::min(drows.size(), r0 + kMaxRowsPerLaunch);
+      std::vector<DecodeIn> batch(drows.begin() + r0, drows.begin() + r1);
+      dp.tmap_k = c->tmK[layer];
+      dp.tmap_v = c->tmV[layer];
+      dp.q = q;
+      dp.q_row_stride = q_row;
+      dp.out = out;
+      dp.out_row_stride = q_row;
+      dp.rope = c->rope;
+      dp.part_o = c->part_o;
+      dp.part_ml = c->part_ml;
+      dp.err = c->err;
+      dp.Hq = Hq;
+      dp.Hk = Hk;
+      dp.rep = rep;
+      dp.seg_rows = c->seg_rows[layer];
+      dp.scale_log2 = scale_log2;
+      int n_multi = 0;
+      double kvb = 0, fl = 0;
+      plan_decode(c, sliding, batch, dp, n_multi, cp, kvb, fl);
+      const double io = (double)batch.size() * Hq * D * 2.0 * 2.0;  // q in, out
+      const int nt = rep <= 8 ? 1 : 2;
+      cudaError_t e = timed(c, KV_KERNEL_DECODE, kvb + io, fl, s,
+                            [&] { return launch_decode(dp, D, nt, s); });
+      if (e != cudaSuccess) return KV_ERR_CUDA;
+      if (n_multi > 0) {
+        cp.part_o = c->part_o;
+        cp.part_ml = c->part_ml;
+        cp.out = out;
+        cp.out_row_stride = q_row;
+        cp.Hq = Hq;
+        cp.D = D;
+        double pb = 0;
+        for (int j = 0; j < n_multi; ++j) pb += (double)cp.n_splits[j] * Hq * (D + 2) * 4.0;
+        e = timed(c, KV_KERNEL_COMBINE, pb, 0, s, [&] { return launch_combine(cp, s); });
+        if (e != cudaSuccess) return KV_ERR_CUDA;
+      }
+    }
+
+    // ---- chunked prefill (+ ring commit on sliding layers)
+    for (size_t r0 = 0; r0 < prows.size(); r0 += kMaxRowsPerLaunch) {
+      const size_t r1 = std::min(prows.size(), r0 + kMaxRowsPerLaunch);
+      pp.tmap_k = c->tmK[layer];
+      pp.tmap_v = c->tmV[layer];
+      pp.tmap_sk = c->tmSK;
+      pp.tmap_sv = c->tmSV;
+      pp.q = q + (int64_t)off * Hq * D;
+      pp.q_row_stride = q_row;
+      pp.out = out + (int64_t)off * Hq * D;
+      pp.out_row_stride = q_row;
+      pp.rope = c->rope;
+      pp.err = c->err;
+      pp.Hq = Hq;
+      pp.Hk = Hk;
+      pp.rep = rep;
+      pp.seg_rows = c->seg_rows[layer];
+      pp.sliding = sliding ? 1 : 0;
+      pp.ring_R = c->R;
+      pp.window = c->W;
+      pp.scale_log2 = scale_log2;
+      int cta = 0;
+      double bytes = 0, fl = 0;
+      for (size_t j = r0; j < r1; ++j) {
+        PrefillRow r = prows[j];
+        r.cta0 = cta;
+        cta += (r.n * rep + 63) / 64;
+        pp.rows[j - r0] = r;
+        const int keys = sliding ? std::min(r.lens, c->R) + r.n : r.lens + r.n;
+        bytes += 2.0 * keys * Hk * D * 2.0 + 2.0 * r.n * Hq * D * 2.0;
+        for (int t = 0; t < r.n; ++t) {
+          const int p = r.lens + t;
+          const int vis = sliding ? std::min(p + 1, c->W) : p + 1;
+          fl += 4.0 * vis * Hq * D;
+        }
+      }
+      pp.n_rows = (int)(r1 - r0);
+      pp.n_ctas = cta;
+      cudaError_t e = timed(c, KV_KERNEL_PREFILL, bytes, fl, s, [&] { return launch_prefill(pp, D, s); });
+      if (e != cudaSuccess) return KV_ERR_CUDA;
+      if (sliding) {
+        mp.scr_k = (const __nv_bfloat16 *)c->scrK;
+        mp.scr_v = (const __nv_bfloat16 *)c->scrV;
+        mp.ring_k = (__nv_bfloat16 *)c->K[layer];
+        mp.ring_v = (__nv_bfloat16 *)c->V[layer];
+        mp.Hk = Hk;
+        mp.D = D;
+        mp.ring_R = c->R;
+        mp.window = c->W;
+        mp.seg_rows = c->seg_rows[layer];
+        double cb = 0;
+        for (size_t j = r0; j < r1; ++j) {
+          mp.cache_row[j - r0] = prows[j].cache_row;
+          mp.lens[j - r0] = prows[j].lens;
+          mp.n[j - r0] = prows[j].n;
+          cb += 4.0 * std::min(prows[j].n, c->W) * Hk * D * 2.0;
+        }
+        mp.n_rows = (int)(r1 - r0);
+        e = timed(c, KV_KERNEL_COMMIT, cb, 0, s, [&] { return launch_commit(mp, s); });
+        if (e != cudaSuccess) return KV_ERR_CUDA;
+      }
+    }
+  }
+  return KV_OK;
+}
+
+int state_update(kv_cache *c, const std::vector<int32_t> &rows, const int32_t *n_new, bool reset,
+                 cudaStream_t s) {
+  static thread_local StateParams sp;
+  for (size_t r0 = 0; r0 < rows.size(); r0 += kMaxRowsPerLaunch) {
+    const size_t r1 = std::min(rows.size(), r0 + kMaxRowsPerLaunch);
+    sp.lens_dev = c->lens_dev;
+    sp.lpos = c->lpos;
+    sp.ring_R = c->R;
+    sp.window = c->W;
+    sp.reset = reset ? 1 : 0;
+    int n = 0;
+    for (size_t j = r0; j < r1; ++j) {
+      if (!reset && n_new[j] == 0) continue;
+      sp.cache_row[n] = rows[j];
+      sp.lens[n] = c->lens[rows[j]];
+      sp.n[n] = reset ? 0 : n_new[j];
+      ++n;
+    }
+    sp.n_rows = n;
+    cudaError_t e = timed(c, KV_KERNEL_STATE, 0, 0, s, [&] { return launch_state(sp, s); });
+    if (e != cudaSuccess) return KV_ERR_CUDA;
+  }
+  return KV_OK;
+}
+
+void free_all(kv_cache *c) {
+  for (void *p : c->K) cudaFree(p);
+  for (void *p : c->V) cudaFree(p);
+  cudaFree(c->scrK);
+  cudaFree(c->scrV);
+  cudaFree(c->rope);
+  cudaFree(c->lens_dev);
+  cudaFree(c->lpos);
+  cudaFree(c->err);
+  cudaFree(c->part_o);
+  cudaFree(c->part_ml);
+  cudaFree(c->stage);
+  for (auto &r : c->recs) {
+    cudaEventDestroy(r.a);
+    cudaEventDestroy(r.b);
+  }
+  for (auto e : c->free_events) cudaEventDestroy(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+int kv_cache_create(kv_cache **out, int B, int max_len, int Hq, int Hk, int D, int W,
+                    int n_layers, const int32_t *layer_kind, double rope_theta, int device) {
+  if (!out) return KV_ERR_ARG;
+  *out = nullptr;
+  if (B < 1 || max_len < 1 || max_len > (1 << 20) || Hk < 1 || Hq < 1 || Hq % Hk != 0 ||
+      Hq / Hk > kMaxRep || (D != 64 && D != 128) || n_layers < 1 || !layer_kind ||
+      !(rope_theta > 0.0) || device < 0)
+    return KV_ERR_ARG;
+  bool any_sliding = false;
+  for (int l = 0; l < n_layers; ++l) {
+    if (layer_kind[l] != KV_GLOBAL && layer_kind[l] != KV_SLIDING) return KV_ERR_ARG;
+    any_sliding |= layer_kind[l] == KV_SLIDING;
+  }
+  if (any_sliding && W < 1) return KV_ERR_ARG;
+  const int R = any_sliding ? (W < max_len ? W : max_len) : 0;
+  if ((int64_t)B * Hk * (max_len + 1) >= (1LL << 31)) return KV_ERR_ARG;  // TMA coordinates
+
+  int n_dev = 0;
+  if (cudaGetDeviceCount(&n_dev) != cudaSuccess || device >= n_dev) return KV_ERR_CUDA;
+  DeviceGuard guard(device);
+  if (!get_encode_fn()) return KV_ERR_CUDA;
+  if (configure_decode() != cudaSuccess || configure_prefill() != cudaSuccess) return KV_ERR_CUDA;
+
+  kv_cache *c = new kv_cache();
+  c->B = B;
+  c->max_len = max_len;
+  c->Hq = Hq;
+  c->Hk = Hk;
+  c->D = D;
+  c->W = any_sliding ? W : 0;
+  c->R = R;
+  c->n_layers = n_layers;
+  c->device = device;
+  c->theta = rope_theta;
+  c->kind.assign(layer_kind, layer_kind + n_layers);
+  c->lens.assign(B, 0);
+  cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, device);
+  if (c->num_sms < 1) c->num_sms = 1;
+
+  auto fail = [&](int code) {
+    free_all(c);
+    delete c;
+    return code;
+  };
+  auto alloc = [&](void **p, size_t bytes) {
+    if (cudaMalloc(p, bytes) != cudaSuccess) return false;
+    return cudaMemset(*p, 0, bytes) == cudaSuccess;  // stale slots stay finite
+  };
+
+  for (int l = 0; l < n_layers; ++l) {
+    const int rows = c->kind[l] == KV_SLIDING ? R + 1 : max_len + 1;
+    const size_t bytes = (size_t)B * Hk * rows * D * 2;
+    void *k = nullptr, *v = nullptr;
+    if (!alloc(&k, bytes)) return fail(KV_ERR_OOM);
+    c->K.push_back(k);
+    if (!alloc(&v, bytes)) return fail(KV_ERR_OOM);
+    c->V.push_back(v);
+    c->seg_rows.push_back(rows);
+    CUtensorMap mk, mv;
+    if (!make_tmap(&mk, k, (int64_t)B * Hk * rows, D) || !make_tmap(&mv, v, (int64_t)B * Hk * rows, D))
+      return fail(KV_ERR_CUDA);
+    c->tmK.push_back(mk);
+    c->tmV.push_back(mv);
+  }
+  const size_t scr = (size_t)B * Hk * kChunk * D * 2;
+  if (!alloc(&c->scrK, scr) || !alloc(&c->scrV, scr)) return fail(KV_ERR_OOM);
+  if (!make_tmap(&c->tmSK, c->scrK, (int64_t)B * Hk * kChunk, D) ||
+      !make_tmap(&c->tmSV, c->scrV, (int64_t)B * Hk * kChunk, D))
+    return fail(KV_ERR_CUDA);
+
+  // RoPE table: theta^(-2i/D) with the exponent as the double quotient (-2i)/D,
+  // angle p * theta_i in double, cos/sin rounded once to float.
+  {
+    const int half = D / 2;
+    std::vector<double> inv(half);
+    for (int i = 0; i < half; ++i) inv[i] = std::pow(rope_theta, (double)(-2 * i) / (double)D);
+    std::vector<float2> tab((size_t)max_len * half);
+    for (int p = 0; p < max_len; ++p)
+      for (int i = 0; i < half; ++i) {
+        const double a = (double)p * inv[i];
+        tab[(size_t)p * half + i] = make_float2((float)std::cos(a), (float)std::sin(a));
+      }
+    if (cudaMalloc((void **)&c->rope, tab.size() * sizeof(float2)) != cudaSuccess)
+      return fail(KV_ERR_OOM);
+    if (cudaMemcpy(c->rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice) !=
+        cudaSuccess)
+      return fail(KV_ERR_CUDA);
+  }
+  if (!alloc((void **)&c->lens_dev, (size_t)B * 4) || !alloc((void **)&c->err, 16))
+    return fail(KV_ERR_OOM);
+  if (R > 0) {
+    if (cudaMalloc((void **)&c->lpos, (size_t)B * R * 4) != cudaSuccess) return fail(KV_ERR_OOM);
+    if (cudaMemset(c->lpos, 0xFF, (size_t)B * R * 4) != cudaSuccess) return fail(KV_ERR_CUDA);
+  }
+  const size_t parts = (size_t)B * kMaxSplits * Hq;
+  if (!alloc((void **)&c->part_o, parts * D * 4) || !alloc((void **)&c->part_ml, parts * 8))
+    return fail(KV_ERR_OOM);
+  if (cudaDeviceSynchronize() != cudaSuccess) return fail(KV_ERR_CUDA);
+  if (const char *log = std::getenv("KVINC_LOG")) {
+    if (log[0] == '1')
+      std::fprintf(stderr, "[kv] %.1f MiB K/V (%d layers, B=%d, Hk=%d, D=%d, max_len=%d, R=%d)\n",
+                   kv_nbytes(c) / 1048576.0, n_layers, B, Hk, D, max_len, R);
+  }
+  *out = c;
+  return KV_OK;
+}
+
+void kv_cache_destroy(kv_cache *c) {
+  if (!c) return;
+  DeviceGuard guard(c->device);
+  cudaDeviceSynchronize();
+  free_all(c);
+  delete c;
+}
+
+int kv_reset(kv_cache *c, const int32_t *rows, int n_rows, void *stream) {
+  if (!c || n_rows < 0 || (n_rows > 0 && !rows)) return KV_ERR_ARG;
+  std::vector<char> seen(c->B, 0);
+  std::vector<int32_t> rv(rows, rows + n_rows);
+  for (int r : rv) {
+    if (r < 0 || r >= c->B || seen[r]) return KV_ERR_ARG;
+    seen[r] = 1;
+  }
+  if (n_rows == 0) return KV_OK;
+  DeviceGuard guard(c->device);
+  const int rc = state_update(c, rv, nullptr, true, (cudaStream_t)stream);
+  if (rc != KV_OK) return rc;
+  for (int r : rv) c->lens[r] = 0;
+  return KV_OK;
+}
+
+int kv_append(kv_cache *c, int layer, const void *q, const void *k, const void *v, int Hq, int C,
+              const int32_t *n_new, const int32_t *rows, int Bs, void *out, void *stream) {
+  if (!c || layer < 0 || layer >= c->n_layers || Hq != c->Hq || C < 1) return KV_ERR_ARG;
+  std::vector<int32_t> cache_rows;
+  const int rc = check_rows(c, n_new, rows, Bs, C, cache_rows);
+  if (rc != KV_OK) return rc;
+  bool any = false;
+  for (int i = 0; i < Bs; ++i) any |= n_new[i] > 0;
+  if (!any) return KV_OK;
+  if (!q || !k || !v || !out || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+    return KV_ERR_ARG;
+  DeviceGuard guard(c->device);
+  return append_device(c, layer, (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)k,
+                       (const __nv_bfloat16 *)v, C, n_new, cache_rows, Bs, (__nv_bfloat16 *)out,
+                       (cudaStream_t)stream);
+}
+
+int kv_append_host(kv_cache *c, int layer, const void *q, const void *k, const void *v, int Hq,
+                   int C, const int32_t *n_new, const int32_t *rows, int Bs, void *out,
+                   void *stream) {
+  if (!c || layer < 0 || layer >= c->n_layers || Hq != c->Hq || C < 1) return KV_ERR_ARG;
+  std::vector<int32_t> cache_rows;
+  const int rc = check_rows(c, n_new, rows, Bs, C, cache_rows);
+  if (rc != KV_OK) return rc;
+  bool any = false;
+  for (int i = 0; i < Bs; ++i) any |= n_new[i] > 0;
+  if (!any) return KV_OK;
+  if (!q || !k || !v || !out) return KV_ERR_ARG;
+  DeviceGuard guard(c->device);
+  cudaStream_t s = (cudaStream_t)stream;
+  const size_t qb = (size_t)Bs * C * c->Hq * c->D * 2, kb = (size_t)Bs * C * c->Hk * c->D * 2;
+  const size_t need = 2 * qb + 2 * kb + 64;
+  if (need > c->stage_bytes) {
+    // The old buffer may still be in use by queued work on this stream.
+    if (c->stage && cudaStreamSynchronize(s) != cudaSuccess) return KV_ERR_CUDA;
+    cudaFree(c->stage);
+    c->stage = nullptr;
+    c->stage_bytes = 0;
+    if (cudaMalloc(&c->stage, need) != cudaSuccess) return KV_ERR_OOM;
+    c->stage_bytes = need;
+  }
+  auto al = [](size_t x) { return (x + 15) & ~size_t(15); };
+  char *base = (char *)c->stage;
+  char *dq = base, *dk = dq + al(qb), *dv = dk + al(kb), *dout = dv + al(kb);
+  if (cudaMemcpyAsync(dq, q, qb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(dk, k, kb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(dv, v, kb, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return KV_ERR_CUDA;
+  const int r = append_device(c, layer, (const __nv_bfloat16 *)dq, (const __nv_bfloat16 *)dk,
+                              (const __nv_bfloat16 *)dv, C, n_new, cache_rows, Bs,
+                              (__nv_bfloat16 *)dout, s);
+  if (r != KV_OK) return r;
+  return set_err(cudaMemcpyAsync(out, dout, qb, cudaMemcpyDeviceToHost, s));
+}
+
+int kv_advance(kv_cache *c, const int32_t *n_new, const int32_t *rows, int Bs, void *stream) {
+  if (!c) return KV_ERR_ARG;
+  std::vector<int32_t> cache_rows;
+  const int rc = check_rows(c, n_new, rows, Bs, c->max_len, cache_rows);
+  if (rc != KV_OK) return rc;
+  DeviceGuard guard(c->device);
+  const int r = state_update(c, cache_rows, n_new, false, (cudaStream_t)stream);
+  if (r != KV_OK) return r;
+  for (int i = 0; i < Bs; ++i) c->lens[cache_rows[i]] += n_new[i];
+  return KV_OK;
+}
+
+int64_t kv_nbytes(const kv_cache *c) {
+  if (!c) return -1;
+  int64_t total = 0;
+  for (int l = 0; l < c->n_layers; ++l)
+    total += 2LL * c->B * c->Hk * c->seg_rows[l] * c->D * 2;
+  return total;
+}
+
+int kv_get_lens(const kv_cache *c, int32_t *lens_out) {
+  if (!c || !lens_out) return KV_ERR_ARG;
+  std::memcpy(lens_out, c->lens.data(), sizeof(int32_t) * c->B);
+  return KV_OK;
+}
+
+int kv_debug_ptrs(const kv_cache *c, int layer, void **K, void **V, int32_t **lpos) {
+  if (!c || layer < 0 || layer >= c->n_layers) return KV_ERR_ARG;
+  if (K) *K = c->K[layer];
+  if (V) *V = c->V[layer];
+  if (lpos) *lpos = c->lpos;
+  return KV_OK;
+}
+
+int kv_get_config(const kv_cache *c, int *B, int *max_len, int *Hq, int *Hk, int *D, int *W,
+                  int *R, int *n_layers) {
+  if (!c) return KV_ERR_ARG;
+  if (B) *B = c->B;
+  if (max_len) *max_len = c->max_len;
+  if (Hq) *Hq = c->Hq;
+  if (Hk) *Hk = c->Hk;
+  if (D) *D = c->D;
+  if (W) *W = c->W;
+  if (R) *R = c->R;
+  if (n_layers) *n_layers = c->n_layers;
+  return KV_OK;
+}
+
+int kv_device_error(kv_cache *c, int32_t *code_out) {
+  if (!c) return KV_ERR_ARG;
+  DeviceGuard guard(c->device);
+  int32_t v = 0;
+  if (cudaMemcpy(&v, c->err, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return KV_ERR_CUDA;
+  if (cudaMemset(c->err, 0, 4) != cudaSuccess) return KV_ERR_CUDA;
+  if (code_out) *code_out = v;
+  return v ? KV_ERR_DEVICE : KV_OK;
+}
+
+int kv_profile_enable(kv_cache *c, int enable) {
+  if (!c) return KV_ERR_ARG;
+  if (!enable) {
+    for (auto &r : c->recs) {
+      c->free_events.push_back(r.a);
+      c->free_events.push_back(r.b);
+    }
+    c->recs.clear();
+  }
+  c->prof = enable != 0;
+  return KV_OK;
+}
+
+int kv_profile_read(kv_cache *c, int kind, int reset, int64_t *launches, double *total_ms,
+                    double *alg_bytes, double *alg_flops) {
+  if (!c || kind < 0 || kind >= KV_KERNEL_NKINDS) return KV_ERR_ARG;
+  DeviceGuard guard(c->device);
+  int64_t n = 0;
+  double ms = 0, by = 0, fl = 0;
+  for (auto &r : c->recs) {
+    if (r.kind != kind) continue;
+    if (cudaEventSynchronize(r.b) != cudaSuccess) return KV_ERR_CUDA;
+    float t = 0;
+    if (cudaEventElapsedTime(&t, r.a, r.b) != cudaSuccess) return KV_ERR_CUDA;
+    ++n;
+    ms += t;
+    by += r.bytes;
+    fl += r.flops;
+  }
+  if (launches) *launches = n;
+  if (total_ms) *total_ms = ms;
+  if (alg_bytes) *alg_bytes = by;
+  if (alg_flops) *alg_flops = fl;
+  if (reset) {
+    std::vector<ProfRec> keep;
+    for (auto &r : c->recs) {
+      if (r.kind == kind) {
+        c->free_events.push_back(r.a);
+        c->free_events.push_back(r.b);
+      } else {
+        keep.push_back(r);
+      }
+    }
+    c->recs.swap(keep);
+  }
+  return KV_OK;
+}
+
+const char *kv_strerror(int code) {
+  switch (code) {
+    case KV_OK: return "KV_OK";
+    case KV_ERR_ARG: return "KV_ERR_ARG: invalid argument";
+    case KV_ERR_FULL: return "KV_ERR_FULL: KV cache full (lens + n_new > max_len)";
+    case KV_ERR_DTYPE: return "KV_ERR_DTYPE: tensors must be bfloat16";
+    case KV_ERR_CUDA: return "KV_ERR_CUDA: CUDA runtime error";
+    case KV_ERR_OOM: return "KV_ERR_OOM: device allocation failed";
+    case KV_ERR_DEVICE: return "KV_ERR_DEVICE: a kernel reported a timed-out wait";
+    default: return "unknown kv status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,164 @@
+// kvinc_internal.h -- structures shared by the host planner (host.cu) and the
+// kernels.  Nothing here is part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace kvinc {
+
+// Sub-chunk width: a row's new tokens are processed 64 at a time
+// (tiny_agent/generate.py, CHUNK = 64).
+constexpr int kChunk = 64;
+// Keys per shared-memory tile (one TMA box height).
+constexpr int kTileKeys = 64;
+// Upper bound of key splits per (row, kv head) in split-K decode.
+constexpr int kMaxSplits = 32;
+// Row records carried in kernel parameters per launch.
+constexpr int kMaxRowsPerLaunch = 512;
+// Largest GQA group (query heads per kv head).
+constexpr int kMaxRep = 16;
+// Spin limit of every mbarrier wait (each try_wait may also suspend briefly);
+// reaching it sets the device error word and abandons the work item.
+constexpr uint32_t kWaitLimit = 1u << 24;
+
+enum DestMode : int32_t {
+  kDestGlobal = 0,   // cache slot lens + t (pads: scratch slot max_len)
+  kDestRing = 1,     // ring slot (lens + t) % R (pads: scratch slot R)
+  kDestScratch = 2,  // chunk scratch row t of [B][Hk][64][D]
+};
+
+// ---------------------------------------------------------------- append
+struct AppendRow {
+  int32_t cache_row;
+  int32_t call_row;
+  int32_t lens;   // position of token t = 0 of this sub-chunk
+  int32_t n;      // real tokens in this sub-chunk
+  int32_t mode;   // DestMode
+  int32_t blk0;   // first token block (8 tokens each) of this row in the grid
+};
+
+struct AppendParams {
+  const __nv_bfloat16 *k;  // call tensor [Bs][C][Hk][D], already offset to the sub-chunk
+  const __nv_bfloat16 *v;
+  int64_t kv_row_stride;   // elements between call rows (C*Hk*D)
+  __nv_bfloat16 *cache_k;  // layer storage [B][Hk][seg_rows][D]
+  __nv_bfloat16 *cache_v;
+  __nv_bfloat16 *scr_k;    // chunk scratch [B][Hk][64][D]
+  __nv_bfloat16 *scr_v;
+  const float2 *rope;      // [max_len][D/2] (cos, sin)
+  int Hk, D;
+  int seg_rows;            // rows per (row, kv head) of the layer storage
+  int ring_R;              // ring slots (sliding) -- scratch slot index R
+  int max_len;             // global scratch slot index
+  int c_avail;             // tokens per call row present in the tensors from the sub-chunk on
+  int n_rows;
+  int n_blocks;            // token blocks in the grid
+  AppendRow rows[kMaxRowsPerLaunch];
+};
+
+// ---------------------------------------------------------------- decode
+struct DecodeRow {
+  int32_t cache_row;
+  int32_t call_row;
+  int32_t pos;        // absolute position of the new token
+  int32_t nk;         // keys to scan: storage slots [0, nk)
+  int32_t item0;      // first work item of this row
+  int32_t split_len;  // keys per split (multiple of kTileKeys)
+  int32_t n_splits;
+  int32_t part0;      // first partial slot of this row (items of multi-split rows)
+};
+
+struct DecodeParams {  // 64-byte aligned through its CUtensorMap members
+  CUtensorMap tmap_k;       // layer K storage as 2-D [B*Hk*seg_rows][D], box 64 x kTileKeys
+  CUtensorMap tmap_v;
+  const __nv_bfloat16 *q;   // [Bs][C][Hq][D] (token 0 of each row is the decode token)
+  int64_t q_row_stride;
+  __nv_bfloat16 *out;       // [Bs][C][Hq][D]
+  int64_t out_row_stride;
+  const float2 *rope;
+  float *part_o;            // [part][Hq][D] unnormalised partial outputs
+  float2 *part_ml;          // [part][Hq] (running max in log2 units, sum of weights)
+  int32_t *err;
+  int Hq, Hk, rep, seg_rows;
+  int n_rows, n_items;
+  float scale_log2;         // log2(e) / sqrt(D)
+  DecodeRow rows[kMaxRowsPerLaunch];
+};
+
+struct CombineParams {
+  const float *part_o;
+  const float2 *part_ml;
+  __nv_bfloat16 *out;
+  int64_t out_row_stride;
+  int Hq, D;
+  int n_rows;
+  int32_t call_row[kMaxRowsPerLaunch];
+  int32_t part0[kMaxRowsPerLaunch];
+  int32_t n_splits[kMaxRowsPerLaunch];
+};
+
+// ---------------------------------------------------------------- prefill
+struct PrefillRow {
+  int32_t cache_row;
+  int32_t call_row;
+  int32_t lens;   // position of token 0 of the sub-chunk
+  int32_t n;      // tokens of the sub-chunk
+  int32_t cta0;   // first CTA (query tile) of this row
+};
+
+struct PrefillParams {  // 64-byte aligned through its CUtensorMap members
+  CUtensorMap tmap_k;       // layer storage (global cache or ring)
+  CUtensorMap tmap_v;
+  CUtensorMap tmap_sk;      // chunk scratch [B*Hk*64][D] (sliding only)
+  CUtensorMap tmap_sv;
+  const __nv_bfloat16 *q;   // [Bs][C][Hq][D], offset to the sub-chunk
+  int64_t q_row_stride;
+  __nv_bfloat16 *out;       // offset to the sub-chunk
+  int64_t out_row_stride;
+  const float2 *rope;
+  int32_t *err;
+  int Hq, Hk, rep, seg_rows;
+  int sliding;              // 0: keys from the global cache; 1: ring + chunk scratch
+  int ring_R, window;
+  int n_rows, n_ctas;
+  float scale_log2;
+  PrefillRow rows[kMaxRowsPerLaunch];
+};
+
+// ---------------------------------------------------------------- ring commit / state
+struct CommitParams {
+  const __nv_bfloat16 *scr_k, *scr_v;
+  __nv_bfloat16 *ring_k, *ring_v;
+  int Hk, D, ring_R, window, seg_rows;
+  int n_rows;
+  int32_t cache_row[kMaxRowsPerLaunch];
+  int32_t lens[kMaxRowsPerLaunch];
+  int32_t n[kMaxRowsPerLaunch];
+};
+
+struct StateParams {
+  int32_t *lens_dev;   // [B]
+  int32_t *lpos;       // [B][R] or nullptr
+  int ring_R, window;
+  int reset;           // 1: lens = 0, lpos = -1; 0: lens += n, record kept positions
+  int n_rows;
+  int32_t cache_row[kMaxRowsPerLaunch];
+  int32_t lens[kMaxRowsPerLaunch];   // lens before the advance
+  int32_t n[kMaxRowsPerLaunch];
+};
+
+// ---------------------------------------------------------------- launchers
+cudaError_t launch_append(const AppendParams &p, cudaStream_t s);
+cudaError_t launch_decode(const DecodeParams &p, int D, int n_tiles_heads, cudaStream_t s);
+cudaError_t launch_combine(const CombineParams &p, cudaStream_t s);
+cudaError_t launch_prefill(const PrefillParams &p, int D, cudaStream_t s);
+cudaError_t launch_commit(const CommitParams &p, cudaStream_t s);
+cudaError_t launch_state(const StateParams &p, cudaStream_t s);
+// Opt kernels into their dynamic shared memory sizes (once per process and device).
+cudaError_t configure_kernels();
+
+}  // namespace kvinc

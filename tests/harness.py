@@ -1,0 +1,161 @@
+"""Drive a KV-cache scenario through the C-ABI binding and check it against the oracle.
+
+Inputs come from the counter-based generator (synth): the value of q/k/v at
+(layer, row, seq, position, head, d) is fixed by the seed, so the oracle can
+regenerate any row's whole history when it checks an output.  `seq` counts the
+sequences a row has held (it advances on every reset).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+import oracle
+import synth
+
+TOL_ABS, TOL_REL = 2e-3, 1e-2  # |err| <= 2e-3 + 1e-2 |ref|, elementwise
+
+
+def bf16_bits_to_torch(bits, device):
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16))
+    return t.view(torch.bfloat16).to(device)
+
+
+def torch_to_bits(t):
+    import torch
+    return t.detach().to("cpu").contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def check_close(got_bits, ref, what=""):
+    got = oracle.bf16_to_f32(got_bits).astype(np.float64)
+    err = np.abs(got - ref)
+    bound = TOL_ABS + TOL_REL * np.abs(ref)
+    bad = ~(err <= bound)
+    if bad.any():
+        i = np.argwhere(bad)[0]
+        raise AssertionError(
+            f"{what}: {int(bad.sum())} of {bad.size} elements out of tolerance; first at "
+            f"{tuple(i)} got {got[tuple(i)]!r} ref {ref[tuple(i)]!r}; max err/bound "
+            f"{float((err / bound).max()):.3f}")
+    return float((err / bound).max()) if err.size else 0.0
+
+
+class Scenario:
+    """One cache plus the bookkeeping needed to regenerate every row's history."""
+
+    def __init__(self, B, max_len, Hq, Hk, D, W=0, kinds=(0,), theta=1e4, seed=0, device=0,
+                 pad_value=None):
+        import kv_cache_incremental_gb300 as kvi
+        self.kvi = kvi
+        self.cache = kvi.KVCache(B, max_len, Hq, Hk, D, W, list(kinds), theta, device)
+        self.B, self.max_len, self.Hq, self.Hk, self.D, self.W = B, max_len, Hq, Hk, D, W
+        self.kinds = list(kinds)
+        self.theta, self.seed = theta, seed
+        self.dev = f"cuda:{device}"
+        self.lens = [0] * B
+        self.seq = [0] * B
+        self.pad_value = pad_value  # None: generator values at pad positions; else a constant
+        self.max_ratio = 0.0
+
+    # ------------------------------------------------------------------ inputs
+    def gen(self, tensor, layer, row, positions, H):
+        return synth.normal_bf16(self.seed, tensor, layer, row, self.seq[row], positions, H,
+                                 self.D)
+
+    def chunk_inputs(self, layer, rows, n_new, C):
+        Bs = len(rows)
+        q = np.zeros((Bs, C, self.Hq, self.D), np.uint16)
+        k = np.zeros((Bs, C, self.Hk, self.D), np.uint16)
+        v = np.zeros((Bs, C, self.Hk, self.D), np.uint16)
+        for i, (b, n) in enumerate(zip(rows, n_new)):
+            pos = np.arange(self.lens[b], self.lens[b] + C)
+            q[i] = self.gen(synth.Q, layer, b, pos, self.Hq)
+            k[i] = self.gen(synth.K, layer, b, pos, self.Hk)
+            v[i] = self.gen(synth.V, layer, b, pos, self.Hk)
+            if self.pad_value is not None and n < C:
+                pad = np.uint16(self.pad_value)
+                q[i, n:], k[i, n:], v[i, n:] = pad, pad, pad
+        return q, k, v
+
+    # ------------------------------------------------------------------ one step
+    def step(self, n_new, rows=None, C=None, resets=(), check=True, check_state=False):
+        import torch
+        rows_eff = list(range(len(n_new))) if rows is None else list(rows)
+        if resets:
+            self.cache.reset(list(resets))
+            for b in resets:
+                self.lens[b] = 0
+                self.seq[b] += 1
+        C = C or max(1, max(n_new))
+        outs = []
+        for layer in range(len(self.kinds)):
+            q, k, v = self.chunk_inputs(layer, rows_eff, n_new, C)
+            qt, kt, vt = (bf16_bits_to_torch(x, self.dev) for x in (q, k, v))
+            sentinel = torch.full_like(qt, 12345.0)
+            out = self.cache.append(layer, qt, kt, vt, list(n_new), rows, out=sentinel.clone())
+            outs.append((q, out))
+        torch.cuda.synchronize()
+        if check:
+            for layer, (q, out) in enumerate(outs):
+                self.check_outputs(layer, rows_eff, n_new, q, torch_to_bits(out))
+        self.cache.advance(list(n_new), rows)
+        for b, n in zip(rows_eff, n_new):
+            self.lens[b] += n
+        if check_state:
+            self.check_state()
+        return outs
+
+    # ------------------------------------------------------------------ checks
+    def check_outputs(self, layer, rows, n_new, q, out_bits):
+        sliding = self.kinds[layer] == 1
+        W = self.W if sliding else 0
+        sentinel = np.uint16(0x4641)  # bf16(12345.0) rounds to 0x4641 (12352)
+        for i, (b, n) in enumerate(zip(rows, n_new)):
+            C = out_bits.shape[1]
+            # padding positions and untouched rows keep the sentinel
+            assert np.all(out_bits[i, n:] == sentinel), f"layer {layer} row {b}: pad written"
+            if n == 0:
+                continue
+            L = self.lens[b]
+            last = L + n - 1
+            lo = max(0, L - (W - 1)) if W else 0
+            hist = np.arange(lo, last + 1)
+            kh = self.gen(synth.K, layer, b, hist, self.Hk)
+            vh = self.gen(synth.V, layer, b, hist, self.Hk)
+            ref = oracle.attend(q[i, :n], np.arange(L, L + n), kh, vh, lo, self.Hq, self.Hk, W=W,
+                                theta=self.theta)
+            r = check_close(out_bits[i, :n], ref, f"layer {layer} row {b} lens {L} n {n}")
+            self.max_ratio = max(self.max_ratio, r)
+
+    def check_state(self):
+        """Cache contents, ring slots, lpos and lens against the oracle, bit for bit."""
+        import torch
+        assert self.cache.lens == self.lens
+        R = self.cache.R
+        for layer, kind in enumerate(self.kinds):
+            K, V = self.cache.storage(layer)
+            Kb, Vb = torch_to_bits(K), torch_to_bits(V)
+            for b in range(self.B):
+                L = self.lens[b]
+                if L == 0:
+                    continue
+                if kind == 0:
+                    pos = np.arange(L)
+                    slots = pos
+                else:
+                    ring = oracle.ring_positions(L, R)
+                    slots = np.nonzero(ring >= 0)[0]
+                    pos = ring[slots]
+                kr = oracle.rope_bf16(self.gen(synth.K, layer, b, pos, self.Hk), pos[:, None],
+                                      self.theta)
+                vv = self.gen(synth.V, layer, b, pos, self.Hk)
+                got_k = Kb[b][:, slots].transpose(1, 0, 2)
+                got_v = Vb[b][:, slots].transpose(1, 0, 2)
+                assert np.array_equal(got_k, kr), f"layer {layer} row {b}: K differs"
+                assert np.array_equal(got_v, vv), f"layer {layer} row {b}: V differs"
+        lp = self.cache.lpos()
+        if lp is not None:
+            lpos = lp.cpu().numpy()
+            for b in range(self.B):
+                assert np.array_equal(lpos[b], oracle.ring_positions(self.lens[b], R)), \
+                    f"row {b}: lpos differs"
