@@ -63,7 +63,8 @@ enum kv_status {
     KV_ERR_DTYPE = 3,  /* tensor dtype is not bfloat16 (raised by language bindings; [P]) */
     KV_ERR_CUDA = 4,   /* a CUDA runtime call failed */
     KV_ERR_OOM = 5,    /* device memory allocation failed at create */
-    KV_ERR_DEVICE = 6  /* a kernel reported a timed-out wait (see kv_device_error) */
+    KV_ERR_DEVICE = 6, /* a kernel reported a timed-out wait (see kv_device_error) */
+    KV_ERR_SCRATCH = 7 /* request too large for kv_decode_noalloc's fixed scratch */
 };
 
 /*
@@ -200,6 +201,48 @@ enum kv_kernel_kind {
 int kv_profile_enable(kv_cache *c, int enable);
 int kv_profile_read(kv_cache *c, int kind, int reset, int64_t *launches, double *total_ms,
                     double *alg_bytes, double *alg_flops);
+
+/*
+ * Decode attention that allocates nothing.  The pages have no counterpart: this
+ * entry point exists for callers that cannot call cudaMalloc -- for example a
+ * process whose device memory is owned by another allocator (a framework's
+ * caching pool or a fixed arena that forbids allocations from outside it), or a
+ * latency-critical loop that must never allocate.  Such a caller cannot create a
+ * kv_cache, so it passes its own memory: the cache storage, the queries, the
+ * RoPE table and the output.  The call runs the same split-K decode and combine
+ * kernels as kv_append; their split partials live in one file-scope device
+ * array of 18 MiB + 256 bytes that every GPU which loads the library holds
+ * until the process exits.
+ *
+ *  K, V        device bf16 [n_cache_rows][Hk][seg_rows][D] (one layer's storage in
+ *              the kv_cache layout, e.g. from kv_debug_ptrs, or the caller's own)
+ *  q           device bf16 [Bs][Hq][D], pre-RoPE query of each row's decode token
+ *  rope        device float2 [rope_positions][D/2]: (cos, sin) of position p,
+ *              pair i, as kv_cache_create computes them
+ *  cache_rows  host int32 [Bs], row of K/V for each query, in [0, n_cache_rows)
+ *  pos         host int32 [Bs], the query's absolute position (for RoPE),
+ *              in [0, rope_positions)
+ *  n_keys      host int32 [Bs], keys in storage slots [0, n_keys) are visible
+ *              (1 <= n_keys <= seg_rows); the new token's key must already be
+ *              stored (global layer: n_keys = pos + 1; ring: min(pos + 1, R))
+ *  out         device bf16 [Bs][Hq][D]
+ *  D is 64 or 128, Hq % Hk == 0, Hq / Hk <= 16.
+ *
+ * Limits: Bs <= 512, and the call's split partials must fit the fixed scratch
+ * (16 MiB of float partial outputs, 2 MiB of (max, sum) pairs); a request
+ * beyond either limit returns KV_ERR_SCRATCH before any work is enqueued.
+ * Set-up: the first call on each device (made with that device current)
+ * resolves the scratch array's device address with cudaGetSymbolAddress and
+ * opts the kernels into their shared-memory size, so make that first call
+ * before any stream capture.  All calls share the scratch and it keeps the
+ * last call's contents: calls whose work overlaps on the GPU (different
+ * streams or host threads) race on it and must be ordered by the caller.
+ * Each call clears the scratch's error word on `stream` before its kernels.
+ */
+int kv_decode_noalloc(const void *K, const void *V, int n_cache_rows, int seg_rows, int Hq,
+                      int Hk, int D, const void *q, const void *rope, int rope_positions,
+                      const int32_t *cache_rows, const int32_t *pos, const int32_t *n_keys,
+                      int Bs, void *out, void *stream);
 
 /* Static name of a status code. */
 const char *kv_strerror(int code);

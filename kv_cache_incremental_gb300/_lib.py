@@ -15,7 +15,8 @@ c_int, c_int32, c_int64, c_double, c_void_p = (ctypes.c_int, ctypes.c_int32, cty
 P_i32 = ctypes.POINTER(ctypes.c_int32)
 
 KV_GLOBAL, KV_SLIDING = 0, 1
-KV_OK, KV_ERR_ARG, KV_ERR_FULL, KV_ERR_DTYPE, KV_ERR_CUDA, KV_ERR_OOM, KV_ERR_DEVICE = range(7)
+(KV_OK, KV_ERR_ARG, KV_ERR_FULL, KV_ERR_DTYPE, KV_ERR_CUDA, KV_ERR_OOM, KV_ERR_DEVICE,
+ KV_ERR_SCRATCH) = range(8)
 KERNELS = {"append": 0, "decode": 1, "combine": 2, "prefill": 3, "commit": 4, "state": 5}
 
 # name -> (restype, argtypes); mirrors include/kvinc.h
@@ -39,6 +40,9 @@ SIGNATURES = {
     "kv_profile_read": (c_int, [c_void_p, c_int, c_int, ctypes.POINTER(c_int64),
                                 ctypes.POINTER(c_double), ctypes.POINTER(c_double),
                                 ctypes.POINTER(c_double)]),
+    "kv_decode_noalloc": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_void_p,
+                                  c_void_p, c_int, P_i32, P_i32, P_i32, c_int, c_void_p,
+                                  c_void_p]),
     "kv_strerror": (ctypes.c_char_p, [c_int]),
 }
 

@@ -727,6 +727,7 @@ const char *kv_strerror(int code) {
     case KV_ERR_CUDA: return "KV_ERR_CUDA: CUDA runtime error";
     case KV_ERR_OOM: return "KV_ERR_OOM: device allocation failed";
     case KV_ERR_DEVICE: return "KV_ERR_DEVICE: a kernel reported a timed-out wait";
+    case KV_ERR_SCRATCH: return "KV_ERR_SCRATCH: request exceeds the fixed no-allocation scratch";
     default: return "unknown kv status";
   }
 }

@@ -1,0 +1,192 @@
+// noalloc.cu -- kv_decode_noalloc: split-K decode attention that allocates nothing.
+//
+// Some callers cannot call cudaMalloc at all: processes whose device memory is
+// owned by another allocator (a framework's caching pool or a fixed arena that
+// forbids allocations from outside it), or latency-critical loops that must not
+// allocate.  Such a caller owns the K/V storage, the queries, the RoPE table and
+// the output; this entry point runs the same split-K decode and combine kernels
+// as kv_append, with their split partials in the file-scope device array below
+// instead of memory from kv_cache_create.
+//
+// The array is fixed at kNoallocScratchBytes; every GPU that loads the library
+// holds it until the process exits.  All calls share it and it keeps the last
+// call's contents, so calls whose work overlaps on the GPU (two streams, or two
+// host threads) race on it; only the error word must start at zero, and each
+// call clears it on its stream before the kernels run.
+#include <algorithm>
+#include <cmath>
+#include <mutex>
+
+#include "../../include/kvinc.h"
+#include "kvinc_internal.h"
+
+namespace kvinc {
+cudaError_t configure_decode();
+}  // namespace kvinc
+
+using namespace kvinc;
+
+namespace {
+
+constexpr size_t kPartOBytes = size_t(16) << 20;   // float partial outputs: 4 Mi floats
+constexpr size_t kPartMLBytes = size_t(2) << 20;   // float2 (m, l): 256 Ki entries
+constexpr size_t kErrBytes = 256;                  // device error word
+constexpr size_t kNoallocScratchBytes = kPartOBytes + kPartMLBytes + kErrBytes;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_setup_mu;
+unsigned char *g_scratch_ptr[kMaxDevices] = {};
+int g_num_sms[kMaxDevices] = {};
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// Per-device set-up on the first call with that device current: the device
+// address of the scratch array (host code only sees a host-side stand-in for
+// the symbol), the SM count, and the decode kernels' shared-memory opt-in.
+int setup_device(int dev, unsigned char **scratch, int *num_sms) {
+  if (dev < 0 || dev >= kMaxDevices) return KV_ERR_ARG;
+  std::lock_guard<std::mutex> lock(g_setup_mu);
+  if (!g_scratch_ptr[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return KV_ERR_CUDA;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return KV_ERR_CUDA;
+    if (configure_decode() != cudaSuccess) return KV_ERR_CUDA;
+    g_num_sms[dev] = sms > 0 ? sms : 1;
+    g_scratch_ptr[dev] = static_cast<unsigned char *>(p);
+  }
+  *scratch = g_scratch_ptr[dev];
+  *num_sms = g_num_sms[dev];
+  return KV_OK;
+}
+
+bool encode(CUtensorMap *m, const void *base, int64_t rows, int D) {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return false;
+    fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)kTileKeys};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" int kv_decode_noalloc(const void *K, const void *V, int n_cache_rows, int seg_rows,
+                                 int Hq, int Hk, int D, const void *q, const void *rope,
+                                 int rope_positions, const int32_t *cache_rows,
+                                 const int32_t *pos, const int32_t *n_keys, int Bs, void *out,
+                                 void *stream) {
+  if (!K || !V || !q || !rope || !out || !cache_rows || !pos || !n_keys) return KV_ERR_ARG;
+  if (n_cache_rows < 1 || seg_rows < 1 || Hk < 1 || Hq < 1 || Hq % Hk != 0 ||
+      Hq / Hk > kMaxRep || (D != 64 && D != 128) || rope_positions < 1 || Bs < 1)
+    return KV_ERR_ARG;
+  if ((int64_t)n_cache_rows * Hk * seg_rows >= (1LL << 31)) return KV_ERR_ARG;
+  if (!aligned16(K) || !aligned16(V) || !aligned16(q) || !aligned16(out) || !aligned16(rope))
+    return KV_ERR_ARG;
+  if (Bs > kMaxRowsPerLaunch) return KV_ERR_SCRATCH;
+  for (int i = 0; i < Bs; ++i) {
+    if (cache_rows[i] < 0 || cache_rows[i] >= n_cache_rows || pos[i] < 0 ||
+        pos[i] >= rope_positions || n_keys[i] < 1 || n_keys[i] > seg_rows)
+      return KV_ERR_ARG;
+  }
+
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KV_ERR_CUDA;
+  unsigned char *scratch = nullptr;
+  int num_sms = 1;
+  const int rc = setup_device(dev, &scratch, &num_sms);
+  if (rc != KV_OK) return rc;
+
+  static thread_local DecodeParams dp;
+  static thread_local CombineParams cp;
+  if (!encode(&dp.tmap_k, K, (int64_t)n_cache_rows * Hk * seg_rows, D) ||
+      !encode(&dp.tmap_v, V, (int64_t)n_cache_rows * Hk * seg_rows, D))
+    return KV_ERR_CUDA;
+
+  // Split schedule as in kv_append: about four waves of two CTAs per SM.
+  int64_t total_tiles = 0;
+  for (int i = 0; i < Bs; ++i) total_tiles += (n_keys[i] + kTileKeys - 1) / kTileKeys;
+  const int64_t target = (int64_t)num_sms * 2 * 4;
+  int64_t per = (total_tiles * Hk + target - 1) / target;
+  if (per < 4) per = 4;
+  int item = 0, part = 0, n_multi = 0;
+  for (int i = 0; i < Bs; ++i) {
+    const int tiles = (n_keys[i] + kTileKeys - 1) / kTileKeys;
+    int ns = (int)std::min<int64_t>(kMaxSplits, (tiles + per - 1) / per);
+    if (ns < 1) ns = 1;
+    const int st = (tiles + ns - 1) / ns;
+    ns = (tiles + st - 1) / st;
+    DecodeRow &r = dp.rows[i];
+    r.cache_row = cache_rows[i];
+    r.call_row = i;
+    r.pos = pos[i];
+    r.nk = n_keys[i];
+    r.item0 = item;
+    r.split_len = st * kTileKeys;
+    r.n_splits = ns;
+    r.part0 = ns > 1 ? part : 0;
+    if (ns > 1) {
+      cp.call_row[n_multi] = i;
+      cp.part0[n_multi] = part;
+      cp.n_splits[n_multi] = ns;
+      ++n_multi;
+      part += ns;
+    }
+    item += ns;
+  }
+  // The partials of this call must fit the fixed scratch.
+  if ((size_t)part * Hq * D * sizeof(float) > kPartOBytes ||
+      (size_t)part * Hq * sizeof(float2) > kPartMLBytes)
+    return KV_ERR_SCRATCH;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t *err = reinterpret_cast<int32_t *>(scratch + kPartOBytes + kPartMLBytes);
+  if (cudaMemsetAsync(err, 0, sizeof(int32_t), s) != cudaSuccess) return KV_ERR_CUDA;
+
+  dp.q = static_cast<const __nv_bfloat16 *>(q);
+  dp.q_row_stride = (int64_t)Hq * D;
+  dp.out = static_cast<__nv_bfloat16 *>(out);
+  dp.out_row_stride = (int64_t)Hq * D;
+  dp.rope = static_cast<const float2 *>(rope);
+  dp.part_o = reinterpret_cast<float *>(scratch);
+  dp.part_ml = reinterpret_cast<float2 *>(scratch + kPartOBytes);
+  dp.err = err;
+  dp.Hq = Hq;
+  dp.Hk = Hk;
+  dp.rep = Hq / Hk;
+  dp.seg_rows = seg_rows;
+  dp.n_rows = Bs;
+  dp.n_items = item;
+  dp.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
+  if (launch_decode(dp, D, dp.rep <= 8 ? 1 : 2, s) != cudaSuccess) return KV_ERR_CUDA;
+  if (n_multi > 0) {
+    cp.part_o = dp.part_o;
+    cp.part_ml = dp.part_ml;
+    cp.out = dp.out;
+    cp.out_row_stride = dp.out_row_stride;
+    cp.Hq = Hq;
+    cp.D = D;
+    cp.n_rows = n_multi;
+    if (launch_combine(cp, s) != cudaSuccess) return KV_ERR_CUDA;
+  }
+  return KV_OK;
+}
