@@ -222,6 +222,18 @@ def traffic_record(kernel_file, workload):
         return None
 
 
+def reduce_over_ranks(times, units, device):
+    """Max over ranks of each time, sum over ranks of each unit count (replicas: the slowest
+    rank bounds the whole job; every rank's work counts)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x) for x in times], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    u = torch.tensor([float(x) for x in units], dtype=torch.float64, device=device)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return t.tolist(), u.tolist()
+
+
 # ---------------------------------------------------------------------------- CPU oracle leg
 
 def oracle_sample(cfg, lens, seed, budget_s=20.0, max_rows=None):
@@ -466,13 +478,8 @@ def run_ours(args):
 
     # ---- max over ranks
     if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms, ms_e2e], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, ms_e2e = float(t[0]), float(t[1])
-        tb = torch.tensor([alg_bytes, e_bytes], dtype=torch.float64, device=dev)
-        dist.all_reduce(tb, op=dist.ReduceOp.SUM)
-        alg_bytes, e_bytes = float(tb[0]), float(tb[1])
+        (ms, ms_e2e), (alg_bytes, e_bytes) = reduce_over_ranks([ms, ms_e2e],
+                                                               [alg_bytes, e_bytes], dev)
     if rank != 0:
         return
     value = alg_bytes / (ms / 1e3) / 1e9
