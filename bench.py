@@ -72,6 +72,14 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def peak_tflops():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops_sustained"])
+    except Exception:
+        return 1700.0
+
+
 def initial_lens(cfg, total_steps, seed):
     rng = np.random.default_rng(seed)
     hi = cfg["max_len"] - total_steps - 1
@@ -368,11 +376,16 @@ def run_ours(args):
 
     caches, lens0 = [], []
     t_fill = time.perf_counter()
+    pre = {"launches": 0, "ms": 0.0, "bytes": 0.0, "flops": 0.0}
     for r in range(rounds):
         seed_r = args.seed + 7919 * rank + 104729 * r
         c = kvi.KVCache(B, cfg["max_len"], Hq, Hk, D, cfg["W"], cfg["kinds"], 1e4, local_rank)
         l0 = initial_lens(cfg, reserve, seed_r)
+        c.profile(r == 0)  # the chunked-prefill kernel, timed on the first fill
         fill_cache(c, cfg, l0, seed_r, stream)
+        if r == 0:
+            pre = c.profile_read("prefill", reset=True)
+            c.profile(False)
         caches.append((c, seed_r))
         lens0.append(l0)
     t_fill = time.perf_counter() - t_fill
@@ -520,6 +533,12 @@ def run_ours(args):
         "kernels": {k: {"launches": p["launches"], "ms": p["ms"]} for k, p in prof.items()},
         "clocks": clk,
         "fill_s": t_fill,
+        "prefill": {"kernel": "prefill_kernel (chunked prefill, 64-token chunks, cache fill)",
+                    "launches": pre["launches"], "ms": pre["ms"],
+                    "tflops": pre["flops"] / (pre["ms"] / 1e3) / 1e12 if pre["ms"] else None,
+                    "frac_of_bf16_sustained": (pre["flops"] / (pre["ms"] / 1e3) / 1e12
+                                               / peak_tflops()) if pre["ms"] else None,
+                    "flops_counted": "4*Hq*D per visible (query, key) pair, causal only"},
     }
     if world == 1 and not args.no_cpu_baseline:
         gbs, tps, nr, thr, t = oracle_sample(cfg, lens0[0] + Wm + per_round, caches[0][1],

@@ -139,12 +139,16 @@ int kv_append(kv_cache *c, int layer, const void *q, const void *k, const void *
               void *stream);
 
 /*
- * Same as kv_append, but q, k, v and out are HOST buffers (pinned memory
- * gives asynchronous copies).  The library copies the inputs into device
- * staging buffers it owns, runs kv_append on them and copies the outputs
- * back, all on `stream`; the call returns before the copies finish, so the
- * caller synchronises the stream before reading `out`.  Staging buffers are
- * allocated on the first call and grown when a larger call arrives.
+ * Same as kv_append, but q, k, v and out are HOST buffers.  Page-locked buffers
+ * (cudaHostAlloc / cudaHostRegister, e.g. torch pin_memory) are read and written
+ * by the kernels directly through their device addresses: on GB300 host memory
+ * is coherent over NVLink-C2C, so the inputs and outputs cross the link inside
+ * the kernels with no copy-engine operation.  Pageable buffers are staged
+ * through device buffers the cache owns (allocated on the first such call and
+ * grown when a larger call arrives) with cudaMemcpyAsync.  Either way the work
+ * is queued on `stream` and the call returns before it finishes: synchronise the
+ * stream before reading `out`.  Padding positions of `out` are not written with
+ * page-locked buffers and are unspecified with pageable ones.
  */
 int kv_append_host(kv_cache *c, int layer, const void *q, const void *k, const void *v,
                    int Hq, int C, const int32_t *n_new, const int32_t *rows, int Bs,
@@ -209,10 +213,10 @@ int kv_profile_read(kv_cache *c, int kind, int reset, int64_t *launches, double 
  * caching pool or a fixed arena that forbids allocations from outside it), or a
  * latency-critical loop that must never allocate.  Such a caller cannot create a
  * kv_cache, so it passes its own memory: the cache storage, the queries, the
- * RoPE table and the output.  The call runs the same split-K decode and combine
- * kernels as kv_append; their split partials live in one file-scope device
- * array of 18 MiB + 256 bytes that every GPU which loads the library holds
- * until the process exits.
+ * RoPE table and the output.  The call runs the same split-K decode kernel as
+ * kv_append; its split partials and merge tickets live in one file-scope device
+ * array of 18 MiB + 128 KiB + 256 bytes that every GPU which loads the library
+ * holds until the process exits.
  *
  *  K, V        device bf16 [n_cache_rows][Hk][seg_rows][D] (one layer's storage in
  *              the kv_cache layout, e.g. from kv_debug_ptrs, or the caller's own)
@@ -228,16 +232,17 @@ int kv_profile_read(kv_cache *c, int kind, int reset, int64_t *launches, double 
  *  out         device bf16 [Bs][Hq][D]
  *  D is 64 or 128, Hq % Hk == 0, Hq / Hk <= 16.
  *
- * Limits: Bs <= 512, and the call's split partials must fit the fixed scratch
- * (16 MiB of float partial outputs, 2 MiB of (max, sum) pairs); a request
- * beyond either limit returns KV_ERR_SCRATCH before any work is enqueued.
+ * Limits: Bs <= 512, Hk <= 64, and the call's split partials must fit the fixed
+ * scratch (16 MiB of float partial outputs, 2 MiB of (max, sum) pairs); a
+ * request beyond any limit returns KV_ERR_SCRATCH before any work is enqueued.
  * Set-up: the first call on each device (made with that device current)
  * resolves the scratch array's device address with cudaGetSymbolAddress and
  * opts the kernels into their shared-memory size, so make that first call
  * before any stream capture.  All calls share the scratch and it keeps the
  * last call's contents: calls whose work overlaps on the GPU (different
  * streams or host threads) race on it and must be ordered by the caller.
- * Each call clears the scratch's error word on `stream` before its kernels.
+ * Each call clears the merge tickets it uses and the error word on `stream`
+ * before its kernel.
  */
 int kv_decode_noalloc(const void *K, const void *V, int n_cache_rows, int seg_rows, int Hq,
                       int Hk, int D, const void *q, const void *rope, int rope_positions,

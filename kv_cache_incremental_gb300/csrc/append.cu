@@ -1,4 +1,4 @@
-// append.cu -- RoPE-and-append, ring commit and lens/lpos state kernels.
+// append.cu -- RoPE-and-append (chunk rows), ring commit and lpos state kernels.
 //
 // RoPE follows tiny_agent/generate.py `_rope_pos` (half-split pairing,
 // (x1 c - x2 s, x1 s + x2 c)) at each row's absolute position; the cos/sin
@@ -113,22 +113,19 @@ __global__ void __launch_bounds__(128) commit_kernel(const __grid_constant__ Com
   }
 }
 
+// lpos (tiny_agent/generate.py keeps the position held by every ring slot): -1 on
+// reset; on advance, the kept tokens' positions at their slots.
 __global__ void __launch_bounds__(128) state_kernel(const __grid_constant__ StateParams p) {
   const int r = blockIdx.x;
   const int b = p.cache_row[r];
   if (p.reset) {
-    if (threadIdx.x == 0) p.lens_dev[b] = 0;
-    if (p.lpos)
-      for (int s = threadIdx.x; s < p.ring_R; s += blockDim.x) p.lpos[(int64_t)b * p.ring_R + s] = -1;
+    for (int s = threadIdx.x; s < p.ring_R; s += blockDim.x) p.lpos[(int64_t)b * p.ring_R + s] = -1;
     return;
   }
   const int lens = p.lens[r], n = p.n[r];
-  if (threadIdx.x == 0) p.lens_dev[b] = lens + n;
-  if (p.lpos) {
-    const int first = n - p.window > 0 ? n - p.window : 0;
-    for (int t = first + threadIdx.x; t < n; t += blockDim.x)
-      p.lpos[(int64_t)b * p.ring_R + (lens + t) % p.ring_R] = lens + t;
-  }
+  const int first = n - p.window > 0 ? n - p.window : 0;
+  for (int t = first + threadIdx.x; t < n; t += blockDim.x)
+    p.lpos[(int64_t)b * p.ring_R + (lens + t) % p.ring_R] = lens + t;
 }
 
 }  // namespace

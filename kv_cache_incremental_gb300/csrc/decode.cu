@@ -1,23 +1,34 @@
-// decode.cu -- split-K grouped-query decode attention against the cache.
+// decode.cu -- split-K grouped-query decode attention against the cache, with the
+// decode token's append and the split merge fused in.
 //
 // One CTA owns one (row, kv head, key split).  A producer warp streams the
 // split's K and V rows through a multi-stage shared-memory ring with TMA 2-D
-// tile loads (128-byte swizzle, one mbarrier per stage); four consumer warps
-// each take 16 keys of every 64-key tile.  For the whole GQA group at once a
-// warp computes S^T = K Q^T on the tensor cores (keys on the MMA's M side,
-// the group's query heads on N), keeps a per-warp online softmax in float,
-// and accumulates O^T = V^T P^T with P split into a bf16 high and low part so
-// that the probabilities keep ~16 significant bits.  Warps merge at the end;
-// a split either writes the normalised bf16 output (single split) or a float
-// partial (m, l, O) for the combine pass.
+// tile loads (128-byte swizzle, one mbarrier pair per stage); four consumer
+// warps each take 16 keys of every 64-key tile.  For the whole GQA group at
+// once a warp computes S^T = K Q^T on the tensor cores (keys on the MMA's M
+// side, the group's query heads on N), keeps a per-warp online softmax in
+// float, and accumulates O^T = V^T P^T with P split into a bf16 high and low
+// part so that the probabilities keep ~16 significant bits.
+//
+// Append fused in (kv_append's decode rows): the CTA whose key range holds the
+// new token's storage slot rotates the new key itself (tiny_agent/generate.py
+// `_rope_pos`), masks the slot's stale content in its tiles, scores the new key
+// from a 16-row shared-memory mini-tile after its main loop, and stores the
+// rotated key and the value to the cache once all of its loads have landed.  No
+// other CTA reads that slot, and later launches see the stored key.
+//
+// Split merge fused in: a split writes its float partial (m, l, O); the last
+// CTA of a (row, kv head) to finish -- found with an atomic ticket -- merges
+// all splits (log-sum-exp) and writes the bf16 output, then re-arms the ticket.
+// A row with a single split writes its output directly.
 //
 // What is computed follows tiny_agent/generate.py `_append_chunk` (grouped
 // queries straight against the cache, scale 1/sqrt(D), float softmax) and the
 // inkling ring-buffer pull request (the sliding scan covers the last W
 // positions): for a decode token at position p the visible keys are storage
-// slots [0, nk) with nk = p + 1 (global) or min(p + 1, R) (sliding ring, where
-// the ring holds exactly positions max(0, p - W + 1) .. p once the new key is
-// written).  The order of keys does not change a softmax, so slots are read in
+// slots [0, nk) with nk = p + 1 (global) or min(p + 1, R) (sliding ring, which
+// holds exactly positions max(0, p - W + 1) .. p once the new key is in).  A
+// softmax does not depend on the order of its keys, so slots are read in
 // storage order.
 #include "kvinc_internal.h"
 #include "ptx.cuh"
@@ -27,6 +38,7 @@ namespace {
 
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kMiniRows = 16;  // rows of the new-key mini-tile
 
 template <int D>
 struct DecodeCfg {
@@ -34,13 +46,15 @@ struct DecodeCfg {
   static constexpr int kTileBytes = kPanels * kTileKeys * 128;  // one K or V tile
   static constexpr int kStages = D == 128 ? 3 : 6;
   static constexpr int kStageBytes = 2 * kTileBytes;
+  static constexpr int kMiniBytes = kPanels * kMiniRows * 128;  // one K or V mini-tile
 };
 
 template <int D, int NT>
 constexpr int decode_smem_bytes() {
   using C = DecodeCfg<D>;
-  return 1024 /*alignment slack*/ + C::kStages * C::kStageBytes + NT * 8 * D * 2 /*Q*/ +
-         2 * C::kStages * 8 /*barriers*/ + 16 /*flags*/;
+  return 1024 /*alignment slack*/ + C::kStages * C::kStageBytes + 2 * C::kMiniBytes +
+         NT * 8 * D * 2 /*Q*/ + 2 * D * 2 /*new K, V*/ + 2 * C::kStages * 8 /*barriers*/ +
+         16 /*flags*/;
 }
 
 __device__ __forceinline__ int find_item_row(const DecodeParams &p, int item) {
@@ -58,18 +72,139 @@ __device__ __forceinline__ void consumer_sync() {
 }
 
 template <int D, int NT>
+struct WarpAcc {
+  float o[D / 16][NT][4];  // O^T fragments: (head dim, head)
+  float m[NT][2];          // running max (log2 units) of the lane's two heads
+  float l[NT][2];          // lane-partial sum of weights
+};
+
+// One warp, 16 keys at smem rows [row0, row0 + 16) of a K tile `kt` and V tile `vt`
+// whose 128-byte panels are `pstride` bytes apart.  Keys r < n_valid, r != skip are
+// visible; the V rows of the others must already be zero.
+template <int D, int NT>
+__device__ __forceinline__ void attend16(WarpAcc<D, NT> &acc, const uint32_t (&qb)[NT][D / 16][2],
+                                         const uint8_t *kt, const uint8_t *vt, int pstride,
+                                         int row0, int n_valid, int skip, float scale_log2,
+                                         int lane) {
+  const int gq = lane >> 2;
+  float sacc[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
+  {
+    const int mrow = row0 + (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const int ch = 2 * (kk % 4) + (lane >> 4);
+      uint32_t a0, a1, a2, a3;
+      ptx::ldsm_x4(ptx::smem_u32(kt + (kk / 4) * pstride) + ptx::swz128(mrow, ch), a0, a1, a2,
+                   a3);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+        ptx::mma_bf16(sacc[nt], a0, a1, a2, a3, qb[nt][kk][0], qb[nt][kk][1]);
+    }
+  }
+  const bool va = gq < n_valid && gq != skip;
+  const bool vb = gq + 8 < n_valid && gq + 8 != skip;
+  uint32_t bh[NT][2], bl[NT][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const float t0 = va ? sacc[nt][0] * scale_log2 : -INFINITY;
+    const float t1 = va ? sacc[nt][1] * scale_log2 : -INFINITY;
+    const float t2 = vb ? sacc[nt][2] * scale_log2 : -INFINITY;
+    const float t3 = vb ? sacc[nt][3] * scale_log2 : -INFINITY;
+    float mx0 = fmaxf(t0, t2), mx1 = fmaxf(t1, t3);
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+    }
+    const float mn0 = fmaxf(acc.m[nt][0], mx0), mn1 = fmaxf(acc.m[nt][1], mx1);
+    const float b0 = mn0 == -INFINITY ? 0.f : mn0;
+    const float b1 = mn1 == -INFINITY ? 0.f : mn1;
+    const float al0 = exp2f(acc.m[nt][0] - b0), al1 = exp2f(acc.m[nt][1] - b1);
+    const float p0 = exp2f(t0 - b0), p1 = exp2f(t1 - b1);
+    const float p2 = exp2f(t2 - b0), p3 = exp2f(t3 - b1);
+    acc.m[nt][0] = mn0;
+    acc.m[nt][1] = mn1;
+    acc.l[nt][0] = acc.l[nt][0] * al0 + (p0 + p2);
+    acc.l[nt][1] = acc.l[nt][1] * al1 + (p1 + p3);
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) {
+      acc.o[mt][nt][0] *= al0;
+      acc.o[mt][nt][1] *= al1;
+      acc.o[mt][nt][2] *= al0;
+      acc.o[mt][nt][3] *= al1;
+    }
+    uint32_t h01, l01, h23, l23;
+    ptx::split_bf16(p0, p1, h01, l01);
+    ptx::split_bf16(p2, p3, h23, l23);
+    // (key, head) fragments -> (head, key) fragments: the B operand of O^T = V^T P^T
+    bh[nt][0] = ptx::movm_t(h01);
+    bh[nt][1] = ptx::movm_t(h23);
+    bl[nt][0] = ptx::movm_t(l01);
+    bl[nt][1] = ptx::movm_t(l23);
+  }
+  {
+    const int mi = lane >> 3;
+    const int vrow = row0 + (lane & 7) + (mi >> 1) * 8;
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) {
+      const int ch = 2 * (mt % 4) + (mi & 1);
+      uint32_t a0, a1, a2, a3;
+      ptx::ldsm_x4_t(ptx::smem_u32(vt + (mt / 4) * pstride) + ptx::swz128(vrow, ch), a0, a1, a2,
+                     a3);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        ptx::mma_bf16(acc.o[mt][nt], a0, a1, a2, a3, bh[nt][0], bh[nt][1]);
+        ptx::mma_bf16(acc.o[mt][nt], a0, a1, a2, a3, bl[nt][0], bl[nt][1]);
+      }
+    }
+  }
+}
+
+// Half-split RoPE of 8 pairs: lo = x1 c - x2 s, hi = x1 s + x2 c in float without
+// contraction, each rounded once to bf16.
+__device__ __forceinline__ void rope8(const uint4 &x1v, const uint4 &x2v, const float2 *cs,
+                                      uint4 &lo, uint4 &hi) {
+  const __nv_bfloat16 *x1 = reinterpret_cast<const __nv_bfloat16 *>(&x1v);
+  const __nv_bfloat16 *x2 = reinterpret_cast<const __nv_bfloat16 *>(&x2v);
+  __nv_bfloat16 *o1 = reinterpret_cast<__nv_bfloat16 *>(&lo);
+  __nv_bfloat16 *o2 = reinterpret_cast<__nv_bfloat16 *>(&hi);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float a = __bfloat162float(x1[j]), b = __bfloat162float(x2[j]);
+    const float2 c = cs[j];
+    o1[j] = __float2bfloat16_rn(__fsub_rn(__fmul_rn(a, c.x), __fmul_rn(b, c.y)));
+    o2[j] = __float2bfloat16_rn(__fadd_rn(__fmul_rn(a, c.y), __fmul_rn(b, c.x)));
+  }
+}
+
+// Zero one 16-byte chunk of V row `r` of a swizzled tile.
+__device__ __forceinline__ void zero_v_chunk(uint8_t *vt, int pstride, int r, int ch) {
+  *reinterpret_cast<uint4 *>(vt + (ch / 8) * pstride + ptx::swz128(r, ch % 8)) =
+      make_uint4(0, 0, 0, 0);
+}
+
+template <int D, int NT>
 __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant__ DecodeParams p) {
   using Cfg = DecodeCfg<D>;
   constexpr int kStages = Cfg::kStages;
+  constexpr int kHalf = D / 2;
+  static_assert(kHalf % 8 == 0, "head dim must be a multiple of 16");
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t *tiles = smem;                                       // [stage][K tile | V tile]
-  __nv_bfloat16 *qs = reinterpret_cast<__nv_bfloat16 *>(smem + kStages * Cfg::kStageBytes);
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + kStages * Cfg::kStageBytes + NT * 8 * D * 2);
+  uint8_t *tiles = smem;                                     // [stage][K tile | V tile]
+  uint8_t *mini_k = smem + kStages * Cfg::kStageBytes;       // new-key mini-tiles
+  uint8_t *mini_v = mini_k + Cfg::kMiniBytes;
+  __nv_bfloat16 *qs = reinterpret_cast<__nv_bfloat16 *>(mini_v + Cfg::kMiniBytes);
+  __nv_bfloat16 *knew = qs + NT * 8 * D;                     // rotated new key, then value
+  __nv_bfloat16 *vnew = knew + D;
+  uint64_t *full = reinterpret_cast<uint64_t *>(vnew + D);
   uint64_t *empty = full + kStages;
-  volatile int *fail = reinterpret_cast<volatile int *>(empty + kStages);  // any wait gave up
+  volatile int *fail = reinterpret_cast<volatile int *>(empty + kStages);  // a wait gave up
   volatile int *issued = fail + 1;                                          // tiles loaded
+  volatile int *last = fail + 2;                                            // merging CTA
 
   const int item = blockIdx.x;
   const int g = blockIdx.y;
@@ -78,6 +213,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
   const int k0 = split * row.split_len;
   const int k1 = min(row.nk, k0 + row.split_len);
   const int n_tiles = (k1 - k0 + kTileKeys - 1) / kTileKeys;
+  const bool owner = p.fuse_append && row.slot >= k0 && row.slot < k1;  // holds the new key
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
@@ -90,29 +226,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
     *issued = 0;
     ptx::fence_barrier_init();
   }
-  if (warp < kConsumerWarps) {
-    // Rotate this row's decode query for the group's heads into shared memory
-    // (tiny_agent/generate.py `_rope_pos`; float ops without contraction).
-    constexpr int kHalf = D / 2;
-    const __nv_bfloat16 *q = p.q + (int64_t)row.call_row * p.q_row_stride +
-                             (int64_t)g * p.rep * D;
-    const float2 *cs = p.rope + (int64_t)row.pos * kHalf;
-    for (int u = threadIdx.x; u < NT * 8 * kHalf; u += kConsumerWarps * 32) {
-      const int h = u / kHalf, i = u % kHalf;
-      __nv_bfloat16 lo = __float2bfloat16_rn(0.f), hi = lo;
-      if (h < p.rep) {
-        const float a = __bfloat162float(q[h * D + i]);
-        const float b = __bfloat162float(q[h * D + i + kHalf]);
-        const float2 c = cs[i];
-        lo = __float2bfloat16_rn(__fsub_rn(__fmul_rn(a, c.x), __fmul_rn(b, c.y)));
-        hi = __float2bfloat16_rn(__fadd_rn(__fmul_rn(a, c.y), __fmul_rn(b, c.x)));
-      }
-      qs[h * D + i] = lo;
-      qs[h * D + i + kHalf] = hi;
-    }
-  }
-  __syncthreads();
-
+  __syncthreads();  // barriers ready: the producer streams while consumers set up
   const int64_t row0 = ((int64_t)row.cache_row * p.Hk + g) * p.seg_rows + k0;
 
   if (warp == kConsumerWarps) {
@@ -144,6 +258,55 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
   }
 
   // -------------------------------------------------------------- consumers
+  {
+    // Rotate the decode query for the group's heads into shared memory
+    // (tiny_agent/generate.py `_rope_pos`; float ops without contraction), 8 pairs
+    // per thread with 16-byte loads.
+    const __nv_bfloat16 *q = p.q + (int64_t)row.call_row * p.q_row_stride +
+                             (int64_t)g * p.rep * D;
+    const float2 *cs = p.rope + (int64_t)row.pos * kHalf;
+    constexpr int kVec = kHalf / 8;  // 8-pair groups per head
+    for (int u = threadIdx.x; u < NT * 8 * kVec; u += kConsumerWarps * 32) {
+      const int h = u / kVec, c = u % kVec;
+      uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
+      if (h < p.rep)
+        rope8(*reinterpret_cast<const uint4 *>(q + h * D + 8 * c),
+              *reinterpret_cast<const uint4 *>(q + h * D + kHalf + 8 * c), cs + 8 * c, lo, hi);
+      *reinterpret_cast<uint4 *>(qs + h * D + 8 * c) = lo;
+      *reinterpret_cast<uint4 *>(qs + h * D + kHalf + 8 * c) = hi;
+    }
+    if (owner) {
+      // The new key (rotated) and value, kept plainly for the store to the cache,
+      // and as row 0 of the mini-tiles (rows 1..15 zero).
+      const __nv_bfloat16 *k = p.k_new + (int64_t)row.call_row * p.kv_row_stride + (int64_t)g * D;
+      const __nv_bfloat16 *v = p.v_new + (int64_t)row.call_row * p.kv_row_stride + (int64_t)g * D;
+      for (int c = threadIdx.x; c < kVec; c += kConsumerWarps * 32) {
+        uint4 lo, hi;
+        rope8(*reinterpret_cast<const uint4 *>(k + 8 * c),
+              *reinterpret_cast<const uint4 *>(k + kHalf + 8 * c), cs + 8 * c, lo, hi);
+        *reinterpret_cast<uint4 *>(knew + 8 * c) = lo;
+        *reinterpret_cast<uint4 *>(knew + kHalf + 8 * c) = hi;
+        *reinterpret_cast<uint4 *>(vnew + 8 * c) = *reinterpret_cast<const uint4 *>(v + 8 * c);
+        *reinterpret_cast<uint4 *>(vnew + kHalf + 8 * c) =
+            *reinterpret_cast<const uint4 *>(v + kHalf + 8 * c);
+      }
+    }
+    consumer_sync();
+    if (owner) {
+      for (int u = threadIdx.x; u < kMiniRows * (D / 8); u += kConsumerWarps * 32) {
+        const int r = u / (D / 8), ch = u % (D / 8);
+        uint4 kv = make_uint4(0, 0, 0, 0), vv = kv;
+        if (r == 0) {
+          kv = *reinterpret_cast<const uint4 *>(knew + 8 * ch);
+          vv = *reinterpret_cast<const uint4 *>(vnew + 8 * ch);
+        }
+        const uint32_t off = (ch / 8) * (kMiniRows * 128) + ptx::swz128(r, ch % 8);
+        *reinterpret_cast<uint4 *>(mini_k + off) = kv;
+        *reinterpret_cast<uint4 *>(mini_v + off) = vv;
+      }
+      consumer_sync();  // the mini-tiles are complete before warp 0 reads them
+    }
+  }
   const int gq = lane >> 2;  // fragment row group
   const int qq = lane & 3;   // fragment column pair
 
@@ -158,128 +321,52 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
       qb[nt][kk][1] = *reinterpret_cast<const uint32_t *>(qr + 8);
     }
 
-  float o[D / 16][NT][4];
+  WarpAcc<D, NT> acc;
 #pragma unroll
   for (int mt = 0; mt < D / 16; ++mt)
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) o[mt][nt][j] = 0.f;
-  float m_run[NT][2], l_run[NT][2];
+      for (int j = 0; j < 4; ++j) acc.o[mt][nt][j] = 0.f;
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    m_run[nt][0] = m_run[nt][1] = -INFINITY;
-    l_run[nt][0] = l_run[nt][1] = 0.f;
+    acc.m[nt][0] = acc.m[nt][1] = -INFINITY;
+    acc.l[nt][0] = acc.l[nt][1] = 0.f;
   }
 
-  bool ok = true;
   for (int it = 0; it < n_tiles; ++it) {
     const int s = it % kStages;
     if (*fail || !ptx::mbar_wait(&full[s], (it / kStages) & 1, kWaitLimit)) {
       atomicExch(p.err, 1);
       *fail = 1;
-      ok = false;
       break;
     }
     uint8_t *kt = tiles + s * Cfg::kStageBytes;
     uint8_t *vt = kt + Cfg::kTileBytes;
     const int key_base = k0 + it * kTileKeys + 16 * warp;  // first key of this warp
     const int n_valid = k1 - key_base;                      // may be <= 0 or >= 16
+    const int skip = owner ? row.slot - key_base : -1;      // stale slot of the new key
+    const bool skip_here = skip >= 0 && skip < 16;
 
-    if (n_valid < 16) {
+    if (n_valid < 16 || skip_here) {
       // Masked keys may hold anything (stale rows, another row's data, padding):
       // zero their V rows so that 0 * V stays 0 in the PV product.
-      const int first = n_valid > 0 ? n_valid : 0;
-      for (int u = lane; u < (16 - first) * (D / 8); u += 32) {
-        const int r = 16 * warp + first + u / (D / 8);
-        const int ch = u % (D / 8);
-        *reinterpret_cast<uint4 *>(vt + (ch / 8) * kTileKeys * 128 + ptx::swz128(r, ch % 8)) =
-            make_uint4(0, 0, 0, 0);
-      }
+      const int first = n_valid > 0 ? (n_valid < 16 ? n_valid : 16) : 0;
+      for (int u = lane; u < (16 - first) * (D / 8); u += 32)
+        zero_v_chunk(vt, kTileKeys * 128, 16 * warp + first + u / (D / 8), u % (D / 8));
+      if (skip_here && skip < first)
+        for (int ch = lane; ch < D / 8; ch += 32)
+          zero_v_chunk(vt, kTileKeys * 128, 16 * warp + skip, ch);
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
     }
-
-    // S^T (16 keys x 8 heads per n-tile) = K Q^T
-    float sacc[NT][4];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
-    {
-      const int mrow = 16 * warp + (lane & 7) + ((lane >> 3) & 1) * 8;
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const int ch = 2 * (kk % 4) + (lane >> 4);
-        uint32_t a0, a1, a2, a3;
-        ptx::ldsm_x4(ptx::smem_u32(kt + (kk / 4) * kTileKeys * 128) + ptx::swz128(mrow, ch), a0,
-                     a1, a2, a3);
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-          ptx::mma_bf16(sacc[nt], a0, a1, a2, a3, qb[nt][kk][0], qb[nt][kk][1]);
-      }
-    }
-
-    // Online softmax for the lane's two heads (columns 2qq, 2qq+1 of each n-tile).
-    const bool va = gq < n_valid, vb = gq + 8 < n_valid;
-    uint32_t bh[NT][2], bl[NT][2];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      float t0 = va ? sacc[nt][0] * p.scale_log2 : -INFINITY;
-      float t1 = va ? sacc[nt][1] * p.scale_log2 : -INFINITY;
-      float t2 = vb ? sacc[nt][2] * p.scale_log2 : -INFINITY;
-      float t3 = vb ? sacc[nt][3] * p.scale_log2 : -INFINITY;
-      float mx0 = fmaxf(t0, t2), mx1 = fmaxf(t1, t3);
-#pragma unroll
-      for (int off = 4; off < 32; off <<= 1) {
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-      }
-      const float mn0 = fmaxf(m_run[nt][0], mx0), mn1 = fmaxf(m_run[nt][1], mx1);
-      const float b0 = mn0 == -INFINITY ? 0.f : mn0;
-      const float b1 = mn1 == -INFINITY ? 0.f : mn1;
-      const float al0 = exp2f(m_run[nt][0] - b0), al1 = exp2f(m_run[nt][1] - b1);
-      const float p0 = exp2f(t0 - b0), p1 = exp2f(t1 - b1);
-      const float p2 = exp2f(t2 - b0), p3 = exp2f(t3 - b1);
-      m_run[nt][0] = mn0;
-      m_run[nt][1] = mn1;
-      l_run[nt][0] = l_run[nt][0] * al0 + (p0 + p2);
-      l_run[nt][1] = l_run[nt][1] * al1 + (p1 + p3);
-#pragma unroll
-      for (int mt = 0; mt < D / 16; ++mt) {
-        o[mt][nt][0] *= al0;
-        o[mt][nt][1] *= al1;
-        o[mt][nt][2] *= al0;
-        o[mt][nt][3] *= al1;
-      }
-      uint32_t h01, l01, h23, l23;
-      ptx::split_bf16(p0, p1, h01, l01);
-      ptx::split_bf16(p2, p3, h23, l23);
-      // (key, head) fragments -> (head, key) fragments: the B operand of O^T = V^T P^T
-      bh[nt][0] = ptx::movm_t(h01);
-      bh[nt][1] = ptx::movm_t(h23);
-      bl[nt][0] = ptx::movm_t(l01);
-      bl[nt][1] = ptx::movm_t(l23);
-    }
-
-    // O^T (head dim x heads) += V^T P^T
-    {
-      const int mi = lane >> 3;
-      const int vrow = 16 * warp + (lane & 7) + (mi >> 1) * 8;
-#pragma unroll
-      for (int mt = 0; mt < D / 16; ++mt) {
-        const int ch = 2 * (mt % 4) + (mi & 1);
-        uint32_t a0, a1, a2, a3;
-        ptx::ldsm_x4_t(ptx::smem_u32(vt + (mt / 4) * kTileKeys * 128) + ptx::swz128(vrow, ch),
-                       a0, a1, a2, a3);
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          ptx::mma_bf16(o[mt][nt], a0, a1, a2, a3, bh[nt][0], bh[nt][1]);
-          ptx::mma_bf16(o[mt][nt], a0, a1, a2, a3, bl[nt][0], bl[nt][1]);
-        }
-      }
-    }
+    attend16<D, NT>(acc, qb, kt, vt, kTileKeys * 128, 16 * warp, n_valid, skip_here ? skip : -1,
+                    p.scale_log2, lane);
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(&empty[s]);
   }
+  if (owner && warp == 0 && !*fail)  // the new key, from the mini-tile (row 0 only)
+    attend16<D, NT>(acc, qb, mini_k, mini_v, kMiniRows * 128, 0, 1, -1, p.scale_log2, lane);
 
   // ---------------------------------------------------------------- merge warps
   // All consumers are past their last tile before the stage memory is reused.
@@ -290,20 +377,29 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
     if (threadIdx.x == 0) {
       const int n_issued = *issued;
       for (int s = 0; s < kStages && s < n_issued; ++s) {
-        const int last = s + ((n_issued - 1 - s) / kStages) * kStages;
-        ptx::mbar_wait(&full[s], (last / kStages) & 1, kWaitLimit);
+        const int lst = s + ((n_issued - 1 - s) / kStages) * kStages;
+        ptx::mbar_wait(&full[s], (lst / kStages) & 1, kWaitLimit);
       }
     }
     return;
   }
-  (void)ok;
+  if (owner) {
+    // Every load of this CTA has landed: store the new key and value in the cache.
+    const int64_t dst = (((int64_t)row.cache_row * p.Hk + g) * p.seg_rows + row.slot) * D;
+    for (int ch = threadIdx.x; ch < D / 8; ch += kConsumerWarps * 32) {
+      *reinterpret_cast<uint4 *>(p.cache_k + dst + 8 * ch) =
+          *reinterpret_cast<const uint4 *>(knew + 8 * ch);
+      *reinterpret_cast<uint4 *>(p.cache_v + dst + 8 * ch) =
+          *reinterpret_cast<const uint4 *>(vnew + 8 * ch);
+    }
+  }
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
     for (int j = 0; j < 2; ++j)
 #pragma unroll
       for (int off = 4; off < 32; off <<= 1)
-        l_run[nt][j] += __shfl_xor_sync(0xffffffffu, l_run[nt][j], off);
+        acc.l[nt][j] += __shfl_xor_sync(0xffffffffu, acc.l[nt][j], off);
 
   constexpr int kH = NT * 8;
   float *mw = reinterpret_cast<float *>(tiles);  // [warp][kH]
@@ -312,10 +408,10 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
   if (gq == 0) {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      mw[warp * kH + nt * 8 + 2 * qq] = m_run[nt][0];
-      mw[warp * kH + nt * 8 + 2 * qq + 1] = m_run[nt][1];
-      lw[warp * kH + nt * 8 + 2 * qq] = l_run[nt][0];
-      lw[warp * kH + nt * 8 + 2 * qq + 1] = l_run[nt][1];
+      mw[warp * kH + nt * 8 + 2 * qq] = acc.m[nt][0];
+      mw[warp * kH + nt * 8 + 2 * qq + 1] = acc.m[nt][1];
+      lw[warp * kH + nt * 8 + 2 * qq] = acc.l[nt][0];
+      lw[warp * kH + nt * 8 + 2 * qq + 1] = acc.l[nt][1];
     }
   }
 #pragma unroll
@@ -324,57 +420,88 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
     for (int nt = 0; nt < NT; ++nt) {
       const int h0 = nt * 8 + 2 * qq;
       float *base = ow + (int64_t)warp * kH * D;
-      base[h0 * D + 16 * mt + gq] = o[mt][nt][0];
-      base[(h0 + 1) * D + 16 * mt + gq] = o[mt][nt][1];
-      base[h0 * D + 16 * mt + gq + 8] = o[mt][nt][2];
-      base[(h0 + 1) * D + 16 * mt + gq + 8] = o[mt][nt][3];
+      base[h0 * D + 16 * mt + gq] = acc.o[mt][nt][0];
+      base[(h0 + 1) * D + 16 * mt + gq] = acc.o[mt][nt][1];
+      base[h0 * D + 16 * mt + gq + 8] = acc.o[mt][nt][2];
+      base[(h0 + 1) * D + 16 * mt + gq + 8] = acc.o[mt][nt][3];
     }
   consumer_sync();
 
   const bool single = row.n_splits == 1;
+  const int64_t part = (int64_t)row.part0 + split;
   for (int u = threadIdx.x; u < p.rep * D; u += kConsumerWarps * 32) {
     const int h = u / D, d = u % D;
     float m = -INFINITY;
 #pragma unroll
     for (int w = 0; w < kConsumerWarps; ++w) m = fmaxf(m, mw[w * kH + h]);
-    float l = 0.f, acc = 0.f;
+    float l = 0.f, a = 0.f;
 #pragma unroll
     for (int w = 0; w < kConsumerWarps; ++w) {
       const float f = exp2f(mw[w * kH + h] - m);  // warps without keys: exp2(-inf) = 0
       l += f * lw[w * kH + h];
-      acc += f * ow[((int64_t)w * kH + h) * D + d];
+      a += f * ow[((int64_t)w * kH + h) * D + d];
     }
     const int hq = g * p.rep + h;
     if (single) {
       p.out[(int64_t)row.call_row * p.out_row_stride + (int64_t)hq * D + d] =
-          __float2bfloat16_rn(acc / l);
+          __float2bfloat16_rn(a / l);
     } else {
-      const int64_t part = (int64_t)row.part0 + split;
-      p.part_o[(part * p.Hq + hq) * D + d] = acc;
+      p.part_o[(part * p.Hq + hq) * D + d] = a;
       if (d == 0) p.part_ml[part * p.Hq + hq] = make_float2(m, l);
     }
   }
-}
+  if (single) return;
 
-// Merge the splits of each multi-split row: weights 2^(m_s - max m), output
-// sum_s w_s O_s / sum_s w_s l_s (the log-sum-exp merge of partial softmaxes).
-__global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ CombineParams p) {
-  const int r = blockIdx.x, h = blockIdx.y;
-  const int n = p.n_splits[r];
-  const int64_t base = p.part0[r];
-  float m = -INFINITY;
-  for (int s = 0; s < n; ++s) m = fmaxf(m, p.part_ml[(base + s) * p.Hq + h].x);
-  for (int d = threadIdx.x; d < p.D; d += blockDim.x) {
-    float l = 0.f, acc = 0.f;
-    for (int s = 0; s < n; ++s) {
-      const float2 ml = p.part_ml[(base + s) * p.Hq + h];
-      const float f = exp2f(ml.x - m);
-      l += f * ml.y;
-      acc += f * p.part_o[((base + s) * p.Hq + h) * p.D + d];
-    }
-    p.out[(int64_t)p.call_row[r] * p.out_row_stride + (int64_t)h * p.D + d] =
-        __float2bfloat16_rn(acc / l);
+  // ---------------------------------------------------------------- split merge
+  // Publish this split's partial and take a ticket; the last split of the (row, kv
+  // head) to arrive merges all of them: weights 2^(m_s - max m),
+  // out = sum_s w_s O_s / sum_s w_s l_s (log-sum-exp merge of partial softmaxes).
+  __threadfence();
+  consumer_sync();
+  int32_t *ticket = p.counters + (int64_t)row.ctr * p.Hk + g;
+  if (threadIdx.x == 0) *last = atomicAdd(ticket, 1) == row.n_splits - 1;
+  consumer_sync();
+  if (!*last) return;
+  __threadfence();
+  // Stage every split's (m, l) of the group's heads, turn them into merge weights
+  // 2^(m_s - max m) / sum_s 2^(m_s - max m) l_s, then sum the weighted partials with
+  // all loads of an element in flight at once.
+  const int ns = row.n_splits;
+  const int64_t base = row.part0;
+  float2 *wml = reinterpret_cast<float2 *>(tiles);            // [split][rep] (m, l) -> weight
+  for (int u = threadIdx.x; u < ns * p.rep; u += kConsumerWarps * 32) {
+    const int sp = u / p.rep, h = u % p.rep;
+    wml[u] = __ldcg(&p.part_ml[(base + sp) * p.Hq + g * p.rep + h]);
   }
+  consumer_sync();
+  if (threadIdx.x < p.rep) {
+    const int h = threadIdx.x;
+    float m = -INFINITY;
+    for (int sp = 0; sp < ns; ++sp) m = fmaxf(m, wml[sp * p.rep + h].x);
+    float l = 0.f;
+    for (int sp = 0; sp < ns; ++sp) l += exp2f(wml[sp * p.rep + h].x - m) * wml[sp * p.rep + h].y;
+    const float inv = 1.f / l;
+    for (int sp = 0; sp < ns; ++sp)
+      wml[sp * p.rep + h].x = exp2f(wml[sp * p.rep + h].x - m) * inv;
+  }
+  consumer_sync();
+  for (int u = threadIdx.x; u < p.rep * D; u += kConsumerWarps * 32) {
+    const int h = u / D, d = u % D;
+    const int hq = g * p.rep + h;
+    const float *src = p.part_o + (base * p.Hq + hq) * D + d;
+    const int64_t stride = (int64_t)p.Hq * D;
+    float a = 0.f;
+    int sp = 0;
+    for (; sp + 4 <= ns; sp += 4) {
+      const float x0 = __ldcg(src + (sp + 0) * stride), x1 = __ldcg(src + (sp + 1) * stride);
+      const float x2 = __ldcg(src + (sp + 2) * stride), x3 = __ldcg(src + (sp + 3) * stride);
+      a += wml[(sp + 0) * p.rep + h].x * x0 + wml[(sp + 1) * p.rep + h].x * x1 +
+           wml[(sp + 2) * p.rep + h].x * x2 + wml[(sp + 3) * p.rep + h].x * x3;
+    }
+    for (; sp < ns; ++sp) a += wml[sp * p.rep + h].x * __ldcg(src + sp * stride);
+    p.out[(int64_t)row.call_row * p.out_row_stride + (int64_t)hq * D + d] = __float2bfloat16_rn(a);
+  }
+  if (threadIdx.x == 0) *ticket = 0;  // re-armed for the next launch on the stream
 }
 
 template <int D, int NT>
@@ -398,12 +525,6 @@ cudaError_t launch_decode(const DecodeParams &p, int D, int n_tiles_heads, cudaS
   if (D == 128) return n_tiles_heads == 1 ? launch_decode_t<128, 1>(p, s) : launch_decode_t<128, 2>(p, s);
   if (D == 64) return n_tiles_heads == 1 ? launch_decode_t<64, 1>(p, s) : launch_decode_t<64, 2>(p, s);
   return cudaErrorInvalidValue;
-}
-
-cudaError_t launch_combine(const CombineParams &p, cudaStream_t s) {
-  if (p.n_rows <= 0) return cudaSuccess;
-  combine_kernel<<<dim3(p.n_rows, p.Hq), 128, 0, s>>>(p);
-  return cudaGetLastError();
 }
 
 cudaError_t configure_decode() {

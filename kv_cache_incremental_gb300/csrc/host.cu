@@ -90,7 +90,7 @@ struct kv_cache {
   CUtensorMap tmSK, tmSV;
   void *scrK = nullptr, *scrV = nullptr;
   float2 *rope = nullptr;
-  int32_t *lens_dev = nullptr, *lpos = nullptr, *err = nullptr;
+  int32_t *lpos = nullptr, *err = nullptr, *counters = nullptr;
   float *part_o = nullptr;
   float2 *part_ml = nullptr;
   // host-buffer entry point staging
@@ -157,8 +157,7 @@ struct DecodeIn {
 
 // Split-K schedule for one batch of decode rows (<= kMaxRowsPerLaunch).
 void plan_decode(const kv_cache *c, bool sliding, const std::vector<DecodeIn> &in,
-                 DecodeParams &p, int &n_multi, CombineParams &cp, double &kv_bytes,
-                 double &flops) {
+                 DecodeParams &p, double &kv_bytes, double &flops) {
   int64_t total_tiles = 0;
   std::vector<int> nk(in.size());
   for (size_t i = 0; i < in.size(); ++i) {
@@ -170,7 +169,6 @@ void plan_decode(const kv_cache *c, bool sliding, const std::vector<DecodeIn> &i
   int64_t per = (total_tiles * c->Hk + target - 1) / target;
   if (per < 4) per = 4;
   int item = 0, part = 0;
-  n_multi = 0;
   kv_bytes = 0;
   flops = 0;
   for (size_t i = 0; i < in.size(); ++i) {
@@ -188,20 +186,15 @@ void plan_decode(const kv_cache *c, bool sliding, const std::vector<DecodeIn> &i
     r.split_len = st * kTileKeys;
     r.n_splits = ns;
     r.part0 = ns > 1 ? part : 0;
-    if (ns > 1) {
-      cp.call_row[n_multi] = in[i].call_row;
-      cp.part0[n_multi] = part;
-      cp.n_splits[n_multi] = ns;
-      ++n_multi;
-      part += ns;
-    }
+    r.slot = sliding ? in[i].pos % c->R : in[i].pos;
+    r.ctr = in[i].cache_row;
+    if (ns > 1) part += ns;
     item += ns;
     kv_bytes += 2.0 * nk[i] * c->Hk * c->D * 2.0;
     flops += 4.0 * nk[i] * c->Hq * c->D;
   }
   p.n_rows = (int)in.size();
   p.n_items = item;
-  cp.n_rows = n_multi;
 }
 
 int append_device(kv_cache *c, int layer, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
@@ -217,7 +210,6 @@ int append_device(kv_cache *c, int layer, const __nv_bfloat16 *q, const __nv_bfl
   const int64_t q_row = (int64_t)C * Hq * D, kv_row = (int64_t)C * Hk * D;
   static thread_local AppendParams ap;
   static thread_local DecodeParams dp;
-  static thread_local CombineParams cp;
   static thread_local PrefillParams pp;
   static thread_local CommitParams mp;
   const float scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
@@ -230,8 +222,7 @@ int append_device(kv_cache *c, int layer, const __nv_bfloat16 *q, const __nv_bfl
       const int n = n_new[i];
       const int b = cache_rows[i];
       if (n == 1 && off == 0) {
-        arows.push_back({b, i, c->lens[b], 1, sliding ? kDestRing : kDestGlobal, 0});
-        drows.push_back({b, i, c->lens[b]});
+        drows.push_back({b, i, c->lens[b]});  // appended inside the decode kernel
       } else if (n >= 2 && n - off >= 1) {
         const int ns = std::min(kChunk, n - off);
         arows.push_back({b, i, c->lens[b] + off, ns, sliding ? kDestScratch : kDestGlobal, 0});
@@ -271,7 +262,7 @@ int append_device(kv_cache *c, int layer, const __nv_bfloat16 *q, const __nv_bfl
       if (e != cudaSuccess) return KV_ERR_CUDA;
     }
 
-    // ---- split-K decode + combine for single-token rows
+    // ---- split-K decode for single-token rows (append and split merge fused in)
     for (size_t r0 = 0; r0 < drows.size(); r0 += kMaxRowsPerLaunch) {
       const size_t r1 = std::min(drows.size(), r0 + kMaxRowsPerLaunch);
       std::vector<DecodeIn> batch(drows.begin() + r0, drows.begin() + r1);
@@ -284,32 +275,27 @@ int append_device(kv_cache *c, int layer, const __nv_bfloat16 *q, const __nv_bfl
       dp.rope = c->rope;
       dp.part_o = c->part_o;
       dp.part_ml = c->part_ml;
+      dp.counters = c->counters;
       dp.err = c->err;
+      dp.k_new = k;
+      dp.v_new = v;
+      dp.kv_row_stride = kv_row;
+      dp.cache_k = (__nv_bfloat16 *)c->K[layer];
+      dp.cache_v = (__nv_bfloat16 *)c->V[layer];
+      dp.fuse_append = 1;
       dp.Hq = Hq;
       dp.Hk = Hk;
       dp.rep = rep;
       dp.seg_rows = c->seg_rows[layer];
       dp.scale_log2 = scale_log2;
-      int n_multi = 0;
       double kvb = 0, fl = 0;
-      plan_decode(c, sliding, batch, dp, n_multi, cp, kvb, fl);
-      const double io = (double)batch.size() * Hq * D * 2.0 * 2.0;  // q in, out
+      plan_decode(c, sliding, batch, dp, kvb, fl);
+      // q, k, v in; new K and V and the output out
+      const double io = (double)batch.size() * (Hq + 2 * Hk) * D * 2.0 * 2.0;
       const int nt = rep <= 8 ? 1 : 2;
       cudaError_t e = timed(c, KV_KERNEL_DECODE, kvb + io, fl, s,
                             [&] { return launch_decode(dp, D, nt, s); });
       if (e != cudaSuccess) return KV_ERR_CUDA;
-      if (n_multi > 0) {
-        cp.part_o = c->part_o;
-        cp.part_ml = c->part_ml;
-        cp.out = out;
-        cp.out_row_stride = q_row;
-        cp.Hq = Hq;
-        cp.D = D;
-        double pb = 0;
-        for (int j = 0; j < n_multi; ++j) pb += (double)cp.n_splits[j] * Hq * (D + 2) * 4.0;
-        e = timed(c, KV_KERNEL_COMBINE, pb, 0, s, [&] { return launch_combine(cp, s); });
-        if (e != cudaSuccess) return KV_ERR_CUDA;
-      }
     }
 
     // ---- chunked prefill (+ ring commit on sliding layers)
@@ -380,10 +366,10 @@ int append_device(kv_cache *c, int layer, const __nv_bfloat16 *q, const __nv_bfl
 
 int state_update(kv_cache *c, const std::vector<int32_t> &rows, const int32_t *n_new, bool reset,
                  cudaStream_t s) {
+  if (!c->lpos) return KV_OK;  // lens lives on the host; lpos exists with sliding layers only
   static thread_local StateParams sp;
   for (size_t r0 = 0; r0 < rows.size(); r0 += kMaxRowsPerLaunch) {
     const size_t r1 = std::min(rows.size(), r0 + kMaxRowsPerLaunch);
-    sp.lens_dev = c->lens_dev;
     sp.lpos = c->lpos;
     sp.ring_R = c->R;
     sp.window = c->W;
@@ -409,7 +395,7 @@ void free_all(kv_cache *c) {
   cudaFree(c->scrK);
   cudaFree(c->scrV);
   cudaFree(c->rope);
-  cudaFree(c->lens_dev);
+  cudaFree(c->counters);
   cudaFree(c->lpos);
   cudaFree(c->err);
   cudaFree(c->part_o);
@@ -514,7 +500,7 @@ int kv_cache_create(kv_cache **out, int B, int max_len, int Hq, int Hk, int D, i
         cudaSuccess)
       return fail(KV_ERR_CUDA);
   }
-  if (!alloc((void **)&c->lens_dev, (size_t)B * 4) || !alloc((void **)&c->err, 16))
+  if (!alloc((void **)&c->counters, (size_t)B * Hk * 4) || !alloc((void **)&c->err, 16))
     return fail(KV_ERR_OOM);
   if (R > 0) {
     if (cudaMalloc((void **)&c->lpos, (size_t)B * R * 4) != cudaSuccess) return fail(KV_ERR_OOM);
@@ -574,6 +560,18 @@ int kv_append(kv_cache *c, int layer, const void *q, const void *k, const void *
                        (cudaStream_t)stream);
 }
 
+// Device address of a page-locked host buffer the GPU can reach directly (on GB300
+// pinned host memory is coherent over NVLink-C2C), or nullptr.
+static const void *mapped_host(const void *p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();  // clear the error of a plain pageable pointer
+    return nullptr;
+  }
+  if (a.type == cudaMemoryTypeHost && a.devicePointer) return a.devicePointer;
+  return nullptr;
+}
+
 int kv_append_host(kv_cache *c, int layer, const void *q, const void *k, const void *v, int Hq,
                    int C, const int32_t *n_new, const int32_t *rows, int Bs, void *out,
                    void *stream) {
@@ -587,6 +585,15 @@ int kv_append_host(kv_cache *c, int layer, const void *q, const void *k, const v
   if (!q || !k || !v || !out) return KV_ERR_ARG;
   DeviceGuard guard(c->device);
   cudaStream_t s = (cudaStream_t)stream;
+  // Page-locked buffers: the kernels read the inputs and write the outputs in host
+  // memory directly; the bytes cross NVLink-C2C inside the kernels.
+  const void *mq = mapped_host(q), *mk = mapped_host(k), *mv = mapped_host(v);
+  void *mo = const_cast<void *>(mapped_host(out));
+  if (mq && mk && mv && mo && aligned16(mq) && aligned16(mk) && aligned16(mv) && aligned16(mo))
+    return append_device(c, layer, (const __nv_bfloat16 *)mq, (const __nv_bfloat16 *)mk,
+                         (const __nv_bfloat16 *)mv, C, n_new, cache_rows, Bs,
+                         (__nv_bfloat16 *)mo, s);
+  // Pageable buffers: stage through device buffers owned by the cache.
   const size_t qb = (size_t)Bs * C * c->Hq * c->D * 2, kb = (size_t)Bs * C * c->Hk * c->D * 2;
   const size_t need = 2 * qb + 2 * kb + 64;
   if (need > c->stage_bytes) {

@@ -70,6 +70,8 @@ struct DecodeRow {
   int32_t split_len;  // keys per split (multiple of kTileKeys)
   int32_t n_splits;
   int32_t part0;      // first partial slot of this row (items of multi-split rows)
+  int32_t slot;       // storage slot of the new token's key (fused append)
+  int32_t ctr;        // row index of this row's merge tickets
 };
 
 struct DecodeParams {  // 64-byte aligned through its CUtensorMap members
@@ -82,23 +84,19 @@ struct DecodeParams {  // 64-byte aligned through its CUtensorMap members
   const float2 *rope;
   float *part_o;            // [part][Hq][D] unnormalised partial outputs
   float2 *part_ml;          // [part][Hq] (running max in log2 units, sum of weights)
+  int32_t *counters;        // [ctr][Hk] merge tickets, zero between launches
   int32_t *err;
+  // fused append of the decode token (fuse_append = 1): its pre-RoPE k and v
+  const __nv_bfloat16 *k_new;  // [Bs][C][Hk][D], token 0
+  const __nv_bfloat16 *v_new;
+  int64_t kv_row_stride;
+  __nv_bfloat16 *cache_k;      // layer storage [B][Hk][seg_rows][D]
+  __nv_bfloat16 *cache_v;
+  int fuse_append;
   int Hq, Hk, rep, seg_rows;
   int n_rows, n_items;
   float scale_log2;         // log2(e) / sqrt(D)
   DecodeRow rows[kMaxRowsPerLaunch];
-};
-
-struct CombineParams {
-  const float *part_o;
-  const float2 *part_ml;
-  __nv_bfloat16 *out;
-  int64_t out_row_stride;
-  int Hq, D;
-  int n_rows;
-  int32_t call_row[kMaxRowsPerLaunch];
-  int32_t part0[kMaxRowsPerLaunch];
-  int32_t n_splits[kMaxRowsPerLaunch];
 };
 
 // ---------------------------------------------------------------- prefill
@@ -141,10 +139,9 @@ struct CommitParams {
 };
 
 struct StateParams {
-  int32_t *lens_dev;   // [B]
-  int32_t *lpos;       // [B][R] or nullptr
+  int32_t *lpos;       // [B][R]
   int ring_R, window;
-  int reset;           // 1: lens = 0, lpos = -1; 0: lens += n, record kept positions
+  int reset;           // 1: lpos = -1; 0: record the kept positions of the advance
   int n_rows;
   int32_t cache_row[kMaxRowsPerLaunch];
   int32_t lens[kMaxRowsPerLaunch];   // lens before the advance
@@ -154,7 +151,6 @@ struct StateParams {
 // ---------------------------------------------------------------- launchers
 cudaError_t launch_append(const AppendParams &p, cudaStream_t s);
 cudaError_t launch_decode(const DecodeParams &p, int D, int n_tiles_heads, cudaStream_t s);
-cudaError_t launch_combine(const CombineParams &p, cudaStream_t s);
 cudaError_t launch_prefill(const PrefillParams &p, int D, cudaStream_t s);
 cudaError_t launch_commit(const CommitParams &p, cudaStream_t s);
 cudaError_t launch_state(const StateParams &p, cudaStream_t s);

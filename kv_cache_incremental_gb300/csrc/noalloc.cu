@@ -4,15 +4,15 @@
 // owned by another allocator (a framework's caching pool or a fixed arena that
 // forbids allocations from outside it), or latency-critical loops that must not
 // allocate.  Such a caller owns the K/V storage, the queries, the RoPE table and
-// the output; this entry point runs the same split-K decode and combine kernels
-// as kv_append, with their split partials in the file-scope device array below
+// the output; this entry point runs the same split-K decode kernel as kv_append,
+// with its split partials and merge tickets in the file-scope device array below
 // instead of memory from kv_cache_create.
 //
 // The array is fixed at kNoallocScratchBytes; every GPU that loads the library
 // holds it until the process exits.  All calls share it and it keeps the last
 // call's contents, so calls whose work overlaps on the GPU (two streams, or two
-// host threads) race on it; only the error word must start at zero, and each
-// call clears it on its stream before the kernels run.
+// host threads) race on it.  The merge tickets and the error word must start at
+// zero: each call clears the ones it uses on its stream before the kernel runs.
 #include <algorithm>
 #include <cmath>
 #include <mutex>
@@ -28,10 +28,12 @@ using namespace kvinc;
 
 namespace {
 
+constexpr int kNoallocMaxHk = 64;                  // kv heads per call
 constexpr size_t kPartOBytes = size_t(16) << 20;   // float partial outputs: 4 Mi floats
 constexpr size_t kPartMLBytes = size_t(2) << 20;   // float2 (m, l): 256 Ki entries
+constexpr size_t kTicketBytes = size_t(kMaxRowsPerLaunch) * kNoallocMaxHk * 4;  // 128 KiB
 constexpr size_t kErrBytes = 256;                  // device error word
-constexpr size_t kNoallocScratchBytes = kPartOBytes + kPartMLBytes + kErrBytes;
+constexpr size_t kNoallocScratchBytes = kPartOBytes + kPartMLBytes + kTicketBytes + kErrBytes;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
@@ -99,6 +101,7 @@ extern "C" int kv_decode_noalloc(const void *K, const void *V, int n_cache_rows,
   if (n_cache_rows < 1 || seg_rows < 1 || Hk < 1 || Hq < 1 || Hq % Hk != 0 ||
       Hq / Hk > kMaxRep || (D != 64 && D != 128) || rope_positions < 1 || Bs < 1)
     return KV_ERR_ARG;
+  if (Hk > kNoallocMaxHk) return KV_ERR_SCRATCH;
   if ((int64_t)n_cache_rows * Hk * seg_rows >= (1LL << 31)) return KV_ERR_ARG;
   if (!aligned16(K) || !aligned16(V) || !aligned16(q) || !aligned16(out) || !aligned16(rope))
     return KV_ERR_ARG;
@@ -117,7 +120,6 @@ extern "C" int kv_decode_noalloc(const void *K, const void *V, int n_cache_rows,
   if (rc != KV_OK) return rc;
 
   static thread_local DecodeParams dp;
-  static thread_local CombineParams cp;
   if (!encode(&dp.tmap_k, K, (int64_t)n_cache_rows * Hk * seg_rows, D) ||
       !encode(&dp.tmap_v, V, (int64_t)n_cache_rows * Hk * seg_rows, D))
     return KV_ERR_CUDA;
@@ -128,7 +130,7 @@ extern "C" int kv_decode_noalloc(const void *K, const void *V, int n_cache_rows,
   const int64_t target = (int64_t)num_sms * 2 * 4;
   int64_t per = (total_tiles * Hk + target - 1) / target;
   if (per < 4) per = 4;
-  int item = 0, part = 0, n_multi = 0;
+  int item = 0, part = 0;
   for (int i = 0; i < Bs; ++i) {
     const int tiles = (n_keys[i] + kTileKeys - 1) / kTileKeys;
     int ns = (int)std::min<int64_t>(kMaxSplits, (tiles + per - 1) / per);
@@ -144,13 +146,9 @@ extern "C" int kv_decode_noalloc(const void *K, const void *V, int n_cache_rows,
     r.split_len = st * kTileKeys;
     r.n_splits = ns;
     r.part0 = ns > 1 ? part : 0;
-    if (ns > 1) {
-      cp.call_row[n_multi] = i;
-      cp.part0[n_multi] = part;
-      cp.n_splits[n_multi] = ns;
-      ++n_multi;
-      part += ns;
-    }
+    r.slot = -1;  // the caller has stored the new key already
+    r.ctr = i;
+    if (ns > 1) part += ns;
     item += ns;
   }
   // The partials of this call must fit the fixed scratch.
@@ -159,8 +157,11 @@ extern "C" int kv_decode_noalloc(const void *K, const void *V, int n_cache_rows,
     return KV_ERR_SCRATCH;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  int32_t *err = reinterpret_cast<int32_t *>(scratch + kPartOBytes + kPartMLBytes);
-  if (cudaMemsetAsync(err, 0, sizeof(int32_t), s) != cudaSuccess) return KV_ERR_CUDA;
+  int32_t *tickets = reinterpret_cast<int32_t *>(scratch + kPartOBytes + kPartMLBytes);
+  int32_t *err = reinterpret_cast<int32_t *>(scratch + kPartOBytes + kPartMLBytes + kTicketBytes);
+  if (cudaMemsetAsync(tickets, 0, (size_t)Bs * Hk * sizeof(int32_t), s) != cudaSuccess ||
+      cudaMemsetAsync(err, 0, sizeof(int32_t), s) != cudaSuccess)
+    return KV_ERR_CUDA;
 
   dp.q = static_cast<const __nv_bfloat16 *>(q);
   dp.q_row_stride = (int64_t)Hq * D;
@@ -169,7 +170,14 @@ extern "C" int kv_decode_noalloc(const void *K, const void *V, int n_cache_rows,
   dp.rope = static_cast<const float2 *>(rope);
   dp.part_o = reinterpret_cast<float *>(scratch);
   dp.part_ml = reinterpret_cast<float2 *>(scratch + kPartOBytes);
+  dp.counters = tickets;
   dp.err = err;
+  dp.k_new = nullptr;
+  dp.v_new = nullptr;
+  dp.kv_row_stride = 0;
+  dp.cache_k = nullptr;
+  dp.cache_v = nullptr;
+  dp.fuse_append = 0;
   dp.Hq = Hq;
   dp.Hk = Hk;
   dp.rep = Hq / Hk;
@@ -178,15 +186,5 @@ extern "C" int kv_decode_noalloc(const void *K, const void *V, int n_cache_rows,
   dp.n_items = item;
   dp.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
   if (launch_decode(dp, D, dp.rep <= 8 ? 1 : 2, s) != cudaSuccess) return KV_ERR_CUDA;
-  if (n_multi > 0) {
-    cp.part_o = dp.part_o;
-    cp.part_ml = dp.part_ml;
-    cp.out = dp.out;
-    cp.out_row_stride = dp.out_row_stride;
-    cp.Hq = Hq;
-    cp.D = D;
-    cp.n_rows = n_multi;
-    if (launch_combine(cp, s) != cudaSuccess) return KV_ERR_CUDA;
-  }
   return KV_OK;
 }

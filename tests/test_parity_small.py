@@ -141,19 +141,33 @@ def test_fill_to_max_len_and_full_rejection_changes_nothing():
     assert sc.lens == [70, 12]
 
 
-def test_host_buffer_entry_point_matches_device_entry_point():
+@pytest.mark.parametrize("pinned", [True, False])
+def test_host_buffer_entry_point_matches_device_entry_point(pinned):
+    """kv_append_host with page-locked buffers (read and written by the kernels over the
+    host link) and with pageable buffers (staged copies) gives kv_append's outputs."""
     import torch
     a = Scenario(B=2, max_len=100, Hq=8, Hk=2, D=128, W=10, kinds=[1, 0], seed=11)
-    q, k, v = a.chunk_inputs(0, [0, 1], [20, 1], 20)
-    out_dev = a.cache.append(0, *(bf16_bits_to_torch(x, "cuda") for x in (q, k, v)), [20, 1])
     b = Scenario(B=2, max_len=100, Hq=8, Hk=2, D=128, W=10, kinds=[1, 0], seed=11)
-    cpu = [torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory() for x in (q, k, v)]
-    out_host = torch.empty(cpu[0].shape, dtype=torch.bfloat16).pin_memory()
-    b.cache.append_host(0, *cpu, [20, 1], out=out_host)
-    torch.cuda.synchronize()
-    d = torch_to_bits(out_dev)
-    h = out_host.view(torch.int16).numpy().view(np.uint16)
-    assert np.array_equal(d[0, :20], h[0, :20]) and np.array_equal(d[1, :1], h[1, :1])
+    for n_new, C in (([20, 1], 20), ([1, 1], 1), ([3, 0], 4)):
+        for layer in (0, 1):
+            q, k, v = a.chunk_inputs(layer, [0, 1], n_new, C)
+            out_dev = a.cache.append(layer, *(bf16_bits_to_torch(x, "cuda") for x in (q, k, v)),
+                                     n_new)
+            cpu = [torch.from_numpy(x.view(np.int16)).view(torch.bfloat16) for x in (q, k, v)]
+            out_host = torch.empty(cpu[0].shape, dtype=torch.bfloat16)
+            if pinned:
+                cpu = [x.pin_memory() for x in cpu]
+                out_host = out_host.pin_memory()
+            b.cache.append_host(layer, *cpu, n_new, out=out_host)
+            torch.cuda.synchronize()
+            d = torch_to_bits(out_dev)
+            h = out_host.view(torch.int16).numpy().view(np.uint16)
+            for i, n in enumerate(n_new):
+                assert np.array_equal(d[i, :n], h[i, :n])
+        for sc in (a, b):
+            sc.cache.advance(n_new)
+            sc.lens = [l + n for l, n in zip(sc.lens, n_new)]
+    b.check_state()
 
 
 def test_determinism_two_runs_bit_equal():
