@@ -54,6 +54,11 @@ def parse():
     ap.add_argument("--workload", default="decode_bw", choices=sorted(WORKLOADS))
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fill-only", action="store_true",
+                    help="time only the chunked-prefill cache fill of one cache (TFLOP/s)")
+    ap.add_argument("--fill-to", type=int, default=0,
+                    help="with --fill-only: fill every row to this length (default: the "
+                         "workload's length draw)")
     return ap.parse_args()
 
 
@@ -306,27 +311,7 @@ def run_reference(args):
 def fill_cache(cache, cfg, lens_target, seed, stream):
     """Prefill every row to its target length through the library, 64 tokens per call."""
     import torch
-    import synth
-    B, Hq, Hk, D = cfg["B"], cfg["Hq"], cfg["Hk"], cfg["D"]
-    C = 64
-    dev = torch.device("cuda", torch.cuda.current_device())
-    q = torch.empty((B, C, Hq, D), dtype=torch.bfloat16, device=dev)
-    k = torch.empty((B, C, Hk, D), dtype=torch.bfloat16, device=dev)
-    v = torch.empty_like(k)
-    out = torch.empty_like(q)
-    rows = torch.arange(B, dtype=torch.int32, device=dev)
-    seqs = torch.zeros(B, dtype=torch.int32, device=dev)
-    lens = np.zeros(B, dtype=np.int64)
-    while (lens < lens_target).any():
-        n = np.minimum(C, lens_target - lens).astype(np.int32)
-        pos0 = torch.from_numpy(lens.astype(np.int32)).to(dev)
-        for layer in range(len(cfg["kinds"])):
-            for t, (x, H) in zip((synth.Q, synth.K, synth.V), ((q, Hq), (k, Hk), (v, Hk))):
-                synth.fill_device(x.data_ptr(), seed, t, layer, rows.data_ptr(), seqs.data_ptr(),
-                                  pos0.data_ptr(), B, C, H, D, stream.cuda_stream)
-            cache.append(layer, q, k, v, n.tolist(), out=out, stream=stream)
-        cache.advance(n.tolist(), stream=stream)
-        lens += n
+    fill_cache_from(cache, cfg, np.zeros(cfg["B"], dtype=np.int64), lens_target, seed, stream)
     torch.cuda.synchronize()
 
 
@@ -350,6 +335,69 @@ def make_inputs(cfg, lens, n_steps, seed, dev, stream):
                                   seqs.data_ptr(), pos0.data_ptr(), B, 1, H, D,
                                   stream.cuda_stream)
     return qs, ks, vs
+
+
+def run_fill_only(args):
+    """Chunked-prefill throughput: fill one cache of the workload through kv_append in
+    64-token chunks; the profiler range covers the last chunk call (all layers)."""
+    import torch
+    import kv_cache_incremental_gb300 as kvi
+    cfg = WORKLOADS[args.workload]
+    torch.cuda.set_device(0)
+    stream = torch.cuda.current_stream()
+    B, Hq, Hk, D = cfg["B"], cfg["Hq"], cfg["Hk"], cfg["D"]
+    c = kvi.KVCache(B, cfg["max_len"], Hq, Hk, D, cfg["W"], cfg["kinds"], 1e4, 0)
+    if args.fill_to:
+        target = np.full(B, args.fill_to, dtype=np.int64)
+    else:
+        target = initial_lens(cfg, 2 * (args.warmup + cfg["per_round"]), args.seed)
+    c.profile(True)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    fill_cache(c, cfg, np.maximum(target - 64, 0), args.seed, stream)
+    torch.cuda.profiler.start()
+    fill_cache_from(c, cfg, np.maximum(target - 64, 0), target, args.seed, stream)
+    torch.cuda.synchronize()
+    torch.cuda.profiler.stop()
+    wall = time.perf_counter() - t0
+    pre = c.profile_read("prefill", reset=True)
+    app = c.profile_read("append", reset=True)
+    com = c.profile_read("commit", reset=True)
+    tflops = pre["flops"] / (pre["ms"] / 1e3) / 1e12 if pre["ms"] else None
+    print(json.dumps({
+        "metric": "chunked-prefill TFLOP/s (cache fill, 64-token chunks)", "value": tflops,
+        "unit": "TFLOP/s", "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "B": B, "Hq": Hq, "Hk": Hk, "D": D,
+                   "layers": len(cfg["kinds"]), "fill_to": int(target.max())},
+        "frac_of_bf16_sustained": tflops / peak_tflops() if tflops else None,
+        "kernels": {"prefill": pre, "append": app, "commit": com}, "wall_s": wall,
+        "flops_counted": "4*Hq*D per visible (query, key) pair, causal only"}), flush=True)
+
+
+def fill_cache_from(cache, cfg, lens_from, lens_target, seed, stream):
+    """Continue a fill from lens_from (the cache's current lengths) to lens_target."""
+    import torch
+    import synth
+    B, Hq, Hk, D = cfg["B"], cfg["Hq"], cfg["Hk"], cfg["D"]
+    C = 64
+    dev = torch.device("cuda", torch.cuda.current_device())
+    q = torch.empty((B, C, Hq, D), dtype=torch.bfloat16, device=dev)
+    k = torch.empty((B, C, Hk, D), dtype=torch.bfloat16, device=dev)
+    v = torch.empty_like(k)
+    out = torch.empty_like(q)
+    rows = torch.arange(B, dtype=torch.int32, device=dev)
+    seqs = torch.zeros(B, dtype=torch.int32, device=dev)
+    lens = lens_from.astype(np.int64).copy()
+    while (lens < lens_target).any():
+        n = np.minimum(C, lens_target - lens).astype(np.int32)
+        pos0 = torch.from_numpy(lens.astype(np.int32)).to(dev)
+        for layer in range(len(cfg["kinds"])):
+            for t, (x, H) in zip((synth.Q, synth.K, synth.V), ((q, Hq), (k, Hk), (v, Hk))):
+                synth.fill_device(x.data_ptr(), seed, t, layer, rows.data_ptr(), seqs.data_ptr(),
+                                  pos0.data_ptr(), B, C, H, D, stream.cuda_stream)
+            cache.append(layer, q, k, v, n.tolist(), out=out, stream=stream)
+        cache.advance(n.tolist(), stream=stream)
+        lens += n
 
 
 def run_ours(args):
@@ -555,6 +603,8 @@ def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.fill_only:
+        run_fill_only(args)
     else:
         run_ours(args)
 

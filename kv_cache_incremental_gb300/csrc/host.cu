@@ -19,6 +19,8 @@
 namespace kvinc {
 cudaError_t configure_decode();
 cudaError_t configure_prefill();
+cudaError_t configure_prefill_tc();
+cudaError_t launch_prefill_tc(const PrefillParams &p, int D, cudaStream_t s);
 }  // namespace kvinc
 
 using namespace kvinc;
@@ -76,6 +78,9 @@ struct ProfRec {
 };
 
 constexpr size_t kMaxProfRecs = 1 << 16;
+// Chunk rows with at least this many query rows (tokens x GQA group) use the tcgen05
+// prefill kernel.
+constexpr int kTcMinRows = 64;
 
 }  // namespace
 
@@ -298,47 +303,60 @@ int append_device(kv_cache *c, int layer, const __nv_bfloat16 *q, const __nv_bfl
       if (e != cudaSuccess) return KV_ERR_CUDA;
     }
 
-    // ---- chunked prefill (+ ring commit on sliding layers)
-    for (size_t r0 = 0; r0 < prows.size(); r0 += kMaxRowsPerLaunch) {
-      const size_t r1 = std::min(prows.size(), r0 + kMaxRowsPerLaunch);
-      pp.tmap_k = c->tmK[layer];
-      pp.tmap_v = c->tmV[layer];
-      pp.tmap_sk = c->tmSK;
-      pp.tmap_sv = c->tmSV;
-      pp.q = q + (int64_t)off * Hq * D;
-      pp.q_row_stride = q_row;
-      pp.out = out + (int64_t)off * Hq * D;
-      pp.out_row_stride = q_row;
-      pp.rope = c->rope;
-      pp.err = c->err;
-      pp.Hq = Hq;
-      pp.Hk = Hk;
-      pp.rep = rep;
-      pp.seg_rows = c->seg_rows[layer];
-      pp.sliding = sliding ? 1 : 0;
-      pp.ring_R = c->R;
-      pp.window = c->W;
-      pp.scale_log2 = scale_log2;
-      int cta = 0;
-      double bytes = 0, fl = 0;
-      for (size_t j = r0; j < r1; ++j) {
-        PrefillRow r = prows[j];
-        r.cta0 = cta;
-        cta += (r.n * rep + 63) / 64;
-        pp.rows[j - r0] = r;
-        const int keys = sliding ? std::min(r.lens, c->R) + r.n : r.lens + r.n;
-        bytes += 2.0 * keys * Hk * D * 2.0 + 2.0 * r.n * Hq * D * 2.0;
-        for (int t = 0; t < r.n; ++t) {
-          const int p = r.lens + t;
-          const int vis = sliding ? std::min(p + 1, c->W) : p + 1;
-          fl += 4.0 * vis * Hq * D;
+    // ---- chunked prefill (+ ring commit on sliding layers).  Rows whose GQA group x
+    // chunk gives at least 64 query rows go to the tcgen05 kernel (128-row tiles);
+    // smaller ones to the mma.sync kernel (16-row warp tiles).
+    for (int kind = 0; kind < 2; ++kind) {
+      std::vector<PrefillRow> sel;
+      for (const PrefillRow &r : prows)
+        if ((r.n * rep >= kTcMinRows) == (kind == 1)) sel.push_back(r);
+      const int rows_per_cta = kind == 1 ? 128 : 64;
+      for (size_t r0 = 0; r0 < sel.size(); r0 += kMaxRowsPerLaunch) {
+        const size_t r1 = std::min(sel.size(), r0 + kMaxRowsPerLaunch);
+        pp.tmap_k = c->tmK[layer];
+        pp.tmap_v = c->tmV[layer];
+        pp.tmap_sk = c->tmSK;
+        pp.tmap_sv = c->tmSV;
+        pp.q = q + (int64_t)off * Hq * D;
+        pp.q_row_stride = q_row;
+        pp.out = out + (int64_t)off * Hq * D;
+        pp.out_row_stride = q_row;
+        pp.rope = c->rope;
+        pp.err = c->err;
+        pp.Hq = Hq;
+        pp.Hk = Hk;
+        pp.rep = rep;
+        pp.seg_rows = c->seg_rows[layer];
+        pp.sliding = sliding ? 1 : 0;
+        pp.ring_R = c->R;
+        pp.window = c->W;
+        pp.scale_log2 = scale_log2;
+        int cta = 0;
+        double bytes = 0, fl = 0;
+        for (size_t j = r0; j < r1; ++j) {
+          PrefillRow r = sel[j];
+          r.cta0 = cta;
+          cta += (r.n * rep + rows_per_cta - 1) / rows_per_cta;
+          pp.rows[j - r0] = r;
+          const int keys = sliding ? std::min(r.lens, c->R) + r.n : r.lens + r.n;
+          bytes += 2.0 * keys * Hk * D * 2.0 + 2.0 * r.n * Hq * D * 2.0;
+          for (int t = 0; t < r.n; ++t) {
+            const int pz = r.lens + t;
+            const int vis = sliding ? std::min(pz + 1, c->W) : pz + 1;
+            fl += 4.0 * vis * Hq * D;
+          }
         }
+        pp.n_rows = (int)(r1 - r0);
+        pp.n_ctas = cta;
+        cudaError_t e = timed(c, KV_KERNEL_PREFILL, bytes, fl, s, [&] {
+          return kind == 1 ? launch_prefill_tc(pp, D, s) : launch_prefill(pp, D, s);
+        });
+        if (e != cudaSuccess) return KV_ERR_CUDA;
       }
-      pp.n_rows = (int)(r1 - r0);
-      pp.n_ctas = cta;
-      cudaError_t e = timed(c, KV_KERNEL_PREFILL, bytes, fl, s, [&] { return launch_prefill(pp, D, s); });
-      if (e != cudaSuccess) return KV_ERR_CUDA;
-      if (sliding) {
+    }
+    if (sliding) {
+      for (size_t r0 = 0; r0 < prows.size(); r0 += kMaxRowsPerLaunch) {
+        const size_t r1 = std::min(prows.size(), r0 + kMaxRowsPerLaunch);
         mp.scr_k = (const __nv_bfloat16 *)c->scrK;
         mp.scr_v = (const __nv_bfloat16 *)c->scrV;
         mp.ring_k = (__nv_bfloat16 *)c->K[layer];
@@ -356,7 +374,7 @@ int append_device(kv_cache *c, int layer, const __nv_bfloat16 *q, const __nv_bfl
           cb += 4.0 * std::min(prows[j].n, c->W) * Hk * D * 2.0;
         }
         mp.n_rows = (int)(r1 - r0);
-        e = timed(c, KV_KERNEL_COMMIT, cb, 0, s, [&] { return launch_commit(mp, s); });
+        cudaError_t e = timed(c, KV_KERNEL_COMMIT, cb, 0, s, [&] { return launch_commit(mp, s); });
         if (e != cudaSuccess) return KV_ERR_CUDA;
       }
     }
@@ -433,7 +451,9 @@ int kv_cache_create(kv_cache **out, int B, int max_len, int Hq, int Hk, int D, i
   if (cudaGetDeviceCount(&n_dev) != cudaSuccess || device >= n_dev) return KV_ERR_CUDA;
   DeviceGuard guard(device);
   if (!get_encode_fn()) return KV_ERR_CUDA;
-  if (configure_decode() != cudaSuccess || configure_prefill() != cudaSuccess) return KV_ERR_CUDA;
+  if (configure_decode() != cudaSuccess || configure_prefill() != cudaSuccess ||
+      configure_prefill_tc() != cudaSuccess)
+    return KV_ERR_CUDA;
 
   kv_cache *c = new kv_cache();
   c->B = B;

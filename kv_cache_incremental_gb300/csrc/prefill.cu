@@ -78,6 +78,10 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(const __grid_constant
   const int rho_last = min(n_rho, rho0 + kRowsPerCta) - 1;
   const int t_max = rho_last / p.rep;  // last token any row of this CTA needs
   const int lens = row.lens;
+  // Ring slot s holds position s + ring_base, less R when s > ring_rem: the largest
+  // position below lens congruent to s modulo R (every slot is occupied once lens >= R).
+  const int ring_base = (lens > p.ring_R && p.ring_R > 0) ? ((lens - 1) / p.ring_R) * p.ring_R : 0;
+  const int ring_rem = (lens > p.ring_R && p.ring_R > 0) ? (lens - 1) % p.ring_R : 0x7fffffff;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
@@ -252,8 +256,7 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(const __grid_constant
           int kpos;
           if (!p.sliding) kpos = kidx;
           else if (!in_a) kpos = lens + kidx;
-          else kpos = lens <= p.ring_R ? kidx
-                                       : kidx + p.ring_R * ((lens - 1 - kidx) / p.ring_R);
+          else kpos = kidx + ring_base - (kidx > ring_rem ? p.ring_R : 0);
           vis = kpos <= qpos[rj] && (!p.sliding || qpos[rj] - kpos < p.window);
         }
         sc[j][e] = vis ? sc[j][e] * p.scale_log2 : -INFINITY;

@@ -1,0 +1,469 @@
+// prefill_tc.cu -- chunked prefill on the 5th-generation tensor cores (tcgen05, TMEM).
+//
+// What is computed is the same as prefill.cu: query row rho of a (row, kv head) is
+// token t = rho / rep, head h = rho % rep of the GQA group at absolute position
+// p = lens + t; it attends to the visible keys of the layer storage (global: slots
+// [0, lens + t], sliding: the ring's occupied slots, whose positions follow from
+// lens) and of the chunk scratch (sliding layers), reading the ring before this
+// chunk is committed to it ("inkling: ring-buffer KV cache for sliding-window
+// layers", How it works; Lab 07 section 3; tiny_agent/generate.py `_append_chunk`).
+//
+// One CTA owns 128 query rows (the MMA's M) of one (row, kv head).  Warp roles:
+//   warps 0-3  softmax: thread i owns query row i = TMEM lane i.  They rotate the
+//              queries into shared memory, read S from TMEM, mask, run the online
+//              softmax (lazy rescaling: O in TMEM is rescaled only when a row's
+//              maximum grows by more than 2^8), write P as bf16 high and low parts
+//              into shared memory, and finally read O from TMEM and normalise.
+//   warp 4     TMA producer of 64-key K and V tiles (128-byte swizzle).
+//   warp 5     TMEM owner and MMA issuer (one thread): S = Q K^T (M=128, N=64)
+//              into one of two TMEM S buffers, O += P_hi V + P_lo V (M=128, N=D),
+//              with V read in place as an MN-major operand (keys are its K).
+// Every mbarrier wait is bounded; on a timeout the CTA records the error, lets its
+// own TMA loads and MMAs finish (bounded), frees its TMEM and returns.
+#include "kvinc_internal.h"
+#include "ptx.cuh"
+
+namespace kvinc {
+namespace {
+
+constexpr int kRows = 128;        // query rows per CTA (MMA M)
+constexpr int kKeys = kTileKeys;  // keys per tile (MMA N of S, K of PV)
+constexpr int kThreads = 6 * 32;
+constexpr int kSoftmaxWarps = 4;
+constexpr int kProducerWarp = 4, kMmaWarp = 5;
+constexpr int kStages = 3;
+constexpr float kRescaleLog2 = 8.f;  // lazy rescale threshold (log2 units)
+
+template <int D>
+struct TcCfg {
+  static constexpr int kPanels = D / 64;
+  static constexpr int kQBytes = kPanels * kRows * 128;   // Q, K-major, 128-byte swizzle
+  static constexpr int kKVTile = kPanels * kKeys * 128;    // one K or V tile (TMA layout)
+  static constexpr int kStageBytes = 2 * kKVTile;
+  static constexpr int kPBytes = kRows * 128;              // P: 128 rows x 64 keys bf16
+  static constexpr int kTmemCols = 256;                    // S0 | S1 | O
+  static constexpr int kOff_Q = 0;
+  static constexpr int kOff_KV = kOff_Q + kQBytes;
+  static constexpr int kOff_P = kOff_KV + kStages * kStageBytes;  // [buf][hi | lo]
+  static constexpr int kOff_Bar = kOff_P + 2 * 2 * kPBytes;
+  static constexpr int kBars = 2 * kStages + 4 * 2 + 1;
+  static constexpr int kSmem = 1024 + kOff_Bar + kBars * 8 + 32;
+};
+
+__device__ __forceinline__ int find_cta_row(const PrefillParams &p, int b) {
+  int lo = 0, hi = p.n_rows - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.rows[mid].cta0 <= b) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+// 2^x with the hardware approximation (relative error ~2^-22), denormals flushed.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ void stsm_x4(uint32_t addr, uint32_t r0, uint32_t r1, uint32_t r2,
+                                        uint32_t r3) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};" ::"r"(addr),
+               "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+               : "memory");
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
+  using Cfg = TcCfg<D>;
+  constexpr int kHalf = D / 2;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t *qsm = smem + Cfg::kOff_Q;
+  uint8_t *kv = smem + Cfg::kOff_KV;
+  uint8_t *pbuf = smem + Cfg::kOff_P;  // P tile b: hi at b * 2 * kPBytes, lo kPBytes later
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::kOff_Bar);
+  uint64_t *kv_full = bars;                 // [kStages] TMA -> MMA and softmax
+  uint64_t *kv_empty = kv_full + kStages;   // [kStages] QK and PV of the stage done
+  uint64_t *s_full = kv_empty + kStages;    // [2] QK done -> softmax
+  uint64_t *s_free = s_full + 2;            // [2] softmax read S -> MMA
+  uint64_t *p_full = s_free + 2;            // [2] softmax wrote P buffer -> MMA
+  uint64_t *o_done = p_full + 2;            // [2] PV that read P buffer b done -> softmax
+  uint64_t *drain = o_done + 2;             // [1] every MMA done (teardown)
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + Cfg::kBars);
+  volatile int *fail = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  volatile int *issued = fail + 1;
+
+  const PrefillRow &row = p.rows[find_cta_row(p, blockIdx.x)];
+  const int g = blockIdx.y;
+  const int rho0 = (blockIdx.x - row.cta0) * kRows;
+  const int n_rho = row.n * p.rep;
+  const int rho_last = min(n_rho, rho0 + kRows) - 1;
+  const int t_max = rho_last / p.rep;
+  const int lens = row.lens;
+  // Ring slot s holds position s + ring_base, less R when s > ring_rem: the largest
+  // position below lens congruent to s modulo R (every slot is occupied once lens >= R).
+  const int ring_base = (lens > p.ring_R && p.ring_R > 0) ? ((lens - 1) / p.ring_R) * p.ring_R : 0;
+  const int ring_rem = (lens > p.ring_R && p.ring_R > 0) ? (lens - 1) % p.ring_R : 0x7fffffff;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  const int len_a = p.sliding ? min(lens, p.ring_R) : lens + t_max + 1;
+  const int len_b = p.sliding ? t_max + 1 : 0;
+  const int tiles_a = (len_a + kKeys - 1) / kKeys;
+  const int n_tiles = tiles_a + (len_b + kKeys - 1) / kKeys;
+  const int64_t base_a = ((int64_t)row.cache_row * p.Hk + g) * p.seg_rows;
+  const int64_t base_b = ((int64_t)row.cache_row * p.Hk + g) * kChunk;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(&kv_full[s], 1);
+      ptx::mbar_init(&kv_empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(&s_full[b], 1);
+      ptx::mbar_init(&s_free[b], kSoftmaxWarps);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(&p_full[b], kSoftmaxWarps);
+      ptx::mbar_init(&o_done[b], 1);
+    }
+    ptx::mbar_init(drain, 1);
+    *fail = 0;
+    *issued = 0;
+    ptx::fence_barrier_init();
+  }
+  if (warp == kMmaWarp) tc::alloc(tmem_slot, Cfg::kTmemCols);
+  if (warp < kSoftmaxWarps) {
+    // Rotated query of this thread's row into the 128-byte-swizzled Q tile.
+    const int r = threadIdx.x;
+    const int rho = rho0 + r;
+    const bool valid = rho < n_rho;
+    const int t = valid ? rho / p.rep : 0, h = valid ? rho % p.rep : 0;
+    const __nv_bfloat16 *q = p.q + (int64_t)row.call_row * p.q_row_stride +
+                             ((int64_t)t * p.Hq + g * p.rep + h) * D;
+    const float2 *cs = p.rope + (int64_t)(lens + t) * kHalf;
+#pragma unroll 2
+    for (int c = 0; c < kHalf / 8; ++c) {
+      uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
+      if (valid) {
+        const uint4 x1v = *reinterpret_cast<const uint4 *>(q + 8 * c);
+        const uint4 x2v = *reinterpret_cast<const uint4 *>(q + kHalf + 8 * c);
+        const __nv_bfloat16 *x1 = reinterpret_cast<const __nv_bfloat16 *>(&x1v);
+        const __nv_bfloat16 *x2 = reinterpret_cast<const __nv_bfloat16 *>(&x2v);
+        __nv_bfloat16 *o1 = reinterpret_cast<__nv_bfloat16 *>(&lo);
+        __nv_bfloat16 *o2 = reinterpret_cast<__nv_bfloat16 *>(&hi);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float a = __bfloat162float(x1[j]), b = __bfloat162float(x2[j]);
+          const float2 e = cs[8 * c + j];
+          o1[j] = __float2bfloat16_rn(__fsub_rn(__fmul_rn(a, e.x), __fmul_rn(b, e.y)));
+          o2[j] = __float2bfloat16_rn(__fadd_rn(__fmul_rn(a, e.y), __fmul_rn(b, e.x)));
+        }
+      }
+      const int c_lo = c, c_hi = kHalf / 8 + c;  // 16-byte chunk index along D
+      *reinterpret_cast<uint4 *>(qsm + (c_lo / 8) * kRows * 128 + ptx::swz128(r, c_lo % 8)) = lo;
+      *reinterpret_cast<uint4 *>(qsm + (c_hi / 8) * kRows * 128 + ptx::swz128(r, c_hi % 8)) = hi;
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // Q -> tensor core
+  }
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tS[2] = {tmem, tmem + kKeys};
+  const uint32_t tO = tmem + 2 * kKeys;
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      ptx::prefetch_tmap(&p.tmap_k);
+      ptx::prefetch_tmap(&p.tmap_v);
+      for (int it = 0; it < n_tiles && !*fail; ++it) {
+        const int s = it % kStages;
+        if (it >= kStages &&
+            !ptx::mbar_wait(&kv_empty[s], ((it / kStages) - 1) & 1, kWaitLimit)) {
+          atomicExch(p.err, 1);
+          *fail = 1;
+          break;
+        }
+        uint8_t *kt = kv + s * Cfg::kStageBytes;
+        uint8_t *vtile = kt + Cfg::kKVTile;
+        const bool in_a = it < tiles_a;
+        const CUtensorMap *mk = in_a ? &p.tmap_k : &p.tmap_sk;
+        const CUtensorMap *mv = in_a ? &p.tmap_v : &p.tmap_sv;
+        const int y = static_cast<int>(in_a ? base_a + (int64_t)it * kKeys
+                                            : base_b + (int64_t)(it - tiles_a) * kKeys);
+        ptx::mbar_arrive_expect_tx(&kv_full[s], Cfg::kStageBytes);
+#pragma unroll
+        for (int pn = 0; pn < Cfg::kPanels; ++pn) {
+          ptx::tma_load_2d(kt + pn * kKeys * 128, mk, pn * 64, y, &kv_full[s]);
+          ptx::tma_load_2d(vtile + pn * kKeys * 128, mv, pn * 64, y, &kv_full[s]);
+        }
+        *issued = it + 1;
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdQK = tc::idesc_bf16_f32(kRows, kKeys);
+      constexpr uint32_t kIdPV = tc::idesc_bf16_f32(kRows, D, /*b_mn_major=*/true);
+      const uint32_t q_addr = ptx::smem_u32(qsm);
+      auto issue_pv = [&](int i) -> bool {
+        const int b = i & 1;
+        if (!ptx::mbar_wait(&p_full[b], (i >> 1) & 1, kWaitLimit)) return false;
+        tc::fence_after();
+        // B = V as stored by TMA: rows = keys (K), 64-dim panels (MN) kKeys*128 bytes apart
+        const uint32_t v_addr = ptx::smem_u32(kv + (i % kStages) * Cfg::kStageBytes + Cfg::kKVTile);
+        const uint32_t ph = ptx::smem_u32(pbuf + b * 2 * Cfg::kPBytes);
+        const uint32_t pl = ph + Cfg::kPBytes;
+#pragma unroll
+        for (int ks = 0; ks < kKeys / 16; ++ks) {
+          const uint64_t bd = tc::desc_sw128_mn(v_addr + ks * 16 * 128, kKeys * 128, 1024);
+          tc::mma(tO, tc::desc_sw128(ph + 32 * ks), bd, kIdPV, i > 0 || ks > 0);
+          tc::mma(tO, tc::desc_sw128(pl + 32 * ks), bd, kIdPV, true);
+        }
+        tc::commit(&kv_empty[i % kStages]);  // V of this stage is consumed
+        tc::commit(&o_done[b]);
+        return true;
+      };
+      bool ok = true;
+      for (int j = 0; j < n_tiles && ok && !*fail; ++j) {
+        const int s = j % kStages, sb = j & 1;
+        if (!ptx::mbar_wait(&kv_full[s], (j / kStages) & 1, kWaitLimit) ||
+            (j >= 2 && !ptx::mbar_wait(&s_free[sb], ((j - 2) >> 1) & 1, kWaitLimit))) {
+          ok = false;
+          break;
+        }
+        tc::fence_after();
+        const uint32_t k_addr = ptx::smem_u32(kv + s * Cfg::kStageBytes);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off_q = (kk / 4) * (kRows * 128) + 32 * (kk % 4);
+          const uint32_t off_k = (kk / 4) * (kKeys * 128) + 32 * (kk % 4);
+          tc::mma(tS[sb], tc::desc_sw128(q_addr + off_q), tc::desc_sw128(k_addr + off_k), kIdQK,
+                  kk > 0);
+        }
+        tc::commit(&s_full[sb]);
+        if (j >= 1 && !issue_pv(j - 1)) ok = false;
+      }
+      if (ok && !*fail && n_tiles > 0 && !issue_pv(n_tiles - 1)) ok = false;
+      if (!ok) {
+        atomicExch(p.err, 1);
+        *fail = 1;
+      }
+      // Every MMA issued has completed before TMEM can be released.
+      tc::commit(drain);
+      ptx::mbar_wait(drain, 0, kWaitLimit);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax warps
+    const int r = threadIdx.x;  // query row of this thread = TMEM lane
+    const int rho = rho0 + r;
+    const bool qvalid = rho < n_rho;
+    const int qpos = lens + (qvalid ? rho / p.rep : 0);
+    const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
+    float m_used = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_tiles && ok; ++j) {
+      const int sb = j & 1;
+      // warp-uniform decisions: tcgen05.ld / st are warp-collective
+      const bool good = !*fail && ptx::mbar_wait(&s_full[sb], (j >> 1) & 1, kWaitLimit);
+      if (!__all_sync(0xffffffffu, good)) {
+        ok = false;
+        break;
+      }
+      tc::fence_after();
+      float sv[kKeys];
+#pragma unroll
+      for (int c = 0; c < kKeys / 16; ++c) {
+        float t16[16];
+        tc::ld16(tS[sb] + lane_off + 16 * c, t16);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) sv[16 * c + i] = t16[i];
+      }
+      tc::wait_ld();
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&s_free[sb]);
+
+      // mask and scale (log2 units)
+      const bool in_a = j < tiles_a;
+      const int kb = (in_a ? j : j - tiles_a) * kKeys;
+      const int seg_len = in_a ? len_a : len_b;
+      float mt = -INFINITY;
+      if (qvalid && !p.sliding && kb + kKeys - 1 <= qpos) {
+        // every key of the tile is at or before this row's position
+#pragma unroll
+        for (int i = 0; i < kKeys; ++i) {
+          sv[i] *= p.scale_log2;
+          mt = fmaxf(mt, sv[i]);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < kKeys; ++i) {
+          const int kidx = kb + i;
+          bool vis = qvalid && kidx < seg_len;
+          if (vis) {
+            int kpos;
+            if (!p.sliding) kpos = kidx;
+            else if (!in_a) kpos = lens + kidx;
+            else kpos = kidx + ring_base - (kidx > ring_rem ? p.ring_R : 0);
+            vis = kpos <= qpos && (!p.sliding || qpos - kpos < p.window);
+          }
+          sv[i] = vis ? sv[i] * p.scale_log2 : -INFINITY;
+          mt = fmaxf(mt, sv[i]);
+        }
+      }
+      // The P buffer of this tile was last read by PV(j-2).
+      const int pb = j & 1;
+      const bool buf_free = j < 2 || ptx::mbar_wait(&o_done[pb], ((j - 2) >> 1) & 1, kWaitLimit);
+      if (!__all_sync(0xffffffffu, buf_free)) {
+        ok = false;
+        break;
+      }
+      float alpha = 1.f;
+      bool rescale = false;
+      if (m_used == -INFINITY) {
+        m_used = mt;  // O and l of this row are still zero
+      } else if (mt > m_used + kRescaleLog2) {
+        alpha = exp2f(m_used - mt);
+        m_used = mt;
+        rescale = true;
+      }
+      if (__any_sync(0xffffffffu, rescale)) {
+        // O may be rescaled only once PV(j-1), the last MMA to write it, is complete.
+        const bool pv_done =
+            j < 1 || ptx::mbar_wait(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, kWaitLimit);
+        if (!__all_sync(0xffffffffu, pv_done)) {
+          ok = false;
+          break;
+        }
+        tc::fence_after();
+#pragma unroll
+        for (int c = 0; c < D / 16; ++c) {
+          float o16[16];
+          tc::ld16(tO + lane_off + 16 * c, o16);
+          tc::wait_ld();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) o16[i] *= alpha;
+          tc::st16(tO + lane_off + 16 * c, o16);
+        }
+        tc::wait_st();
+      }
+      l_run *= alpha;
+      const float base = m_used == -INFINITY ? 0.f : m_used;
+      if (seg_len - kb < kKeys) {
+        // Keys past the segment may hold anything: zero their V rows so that 0 * V
+        // stays 0 in the PV product (the MMA reads V only after P is published).
+        uint8_t *vtile = kv + (j % kStages) * Cfg::kStageBytes + Cfg::kKVTile;
+        const int first = seg_len - kb > 0 ? seg_len - kb : 0;
+        for (int u = r; u < (kKeys - first) * (D / 8); u += kSoftmaxWarps * 32) {
+          const int vr = first + u / (D / 8), ch = u % (D / 8);
+          *reinterpret_cast<uint4 *>(vtile + (ch / 8) * (kKeys * 128) + ptx::swz128(vr, ch % 8)) =
+              make_uint4(0, 0, 0, 0);
+        }
+      }
+      uint8_t *p_hi = pbuf + pb * 2 * Cfg::kPBytes;
+      uint8_t *p_lo = p_hi + Cfg::kPBytes;
+      // P = 2^(s - m) as bf16 high + low parts, row r of the swizzled P tiles
+#pragma unroll
+      for (int c = 0; c < kKeys / 8; ++c) {
+        uint32_t hv[4], lv[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float e0 = fast_exp2(sv[8 * c + 2 * i] - base);
+          const float e1 = fast_exp2(sv[8 * c + 2 * i + 1] - base);
+          l_run += e0 + e1;
+          ptx::split_bf16(e0, e1, hv[i], lv[i]);
+        }
+        const uint32_t off = ptx::swz128(r, c);
+        *reinterpret_cast<uint4 *>(p_hi + off) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+        *reinterpret_cast<uint4 *>(p_lo + off) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // P -> tensor core
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&p_full[pb]);
+    }
+    const bool last_done = ok && n_tiles > 0 &&
+                           ptx::mbar_wait(&o_done[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1,
+                                          kWaitLimit);
+    if (!ok) {
+      atomicExch(p.err, 1);
+      *fail = 1;
+    } else if (__all_sync(0xffffffffu, last_done)) {
+      tc::fence_after();
+      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+      const int t = qvalid ? rho / p.rep : 0, h = qvalid ? rho % p.rep : 0;
+      __nv_bfloat16 *dst = p.out + (int64_t)row.call_row * p.out_row_stride +
+                           ((int64_t)t * p.Hq + g * p.rep + h) * D;
+#pragma unroll
+      for (int c = 0; c < D / 16; ++c) {
+        float o16[16];
+        tc::ld16(tO + lane_off + 16 * c, o16);
+        tc::wait_ld();
+        uint4 w0, w1;
+        w0.x = ptx::pack_bf16(o16[0] * inv, o16[1] * inv);
+        w0.y = ptx::pack_bf16(o16[2] * inv, o16[3] * inv);
+        w0.z = ptx::pack_bf16(o16[4] * inv, o16[5] * inv);
+        w0.w = ptx::pack_bf16(o16[6] * inv, o16[7] * inv);
+        w1.x = ptx::pack_bf16(o16[8] * inv, o16[9] * inv);
+        w1.y = ptx::pack_bf16(o16[10] * inv, o16[11] * inv);
+        w1.z = ptx::pack_bf16(o16[12] * inv, o16[13] * inv);
+        w1.w = ptx::pack_bf16(o16[14] * inv, o16[15] * inv);
+        if (qvalid) {
+          *reinterpret_cast<uint4 *>(dst + 16 * c) = w0;
+          *reinterpret_cast<uint4 *>(dst + 16 * c + 8) = w1;
+        }
+      }
+    } else if (n_tiles > 0) {
+      atomicExch(p.err, 1);
+      *fail = 1;
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  tc::fence_before();
+  __syncthreads();
+  if (*fail && threadIdx.x == 0) {
+    // Let every TMA load this CTA issued land before its shared memory is released.
+    const int n_issued = *issued;
+    for (int s = 0; s < kStages && s < n_issued; ++s) {
+      const int lst = s + ((n_issued - 1 - s) / kStages) * kStages;
+      ptx::mbar_wait(&kv_full[s], (lst / kStages) & 1, kWaitLimit);
+    }
+  }
+  if (warp == kMmaWarp) {
+    tc::fence_after();
+    tc::dealloc(tmem, Cfg::kTmemCols);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_tc(const PrefillParams &p, int D, cudaStream_t s) {
+  if (p.n_ctas <= 0) return cudaSuccess;
+  if (D == 128) {
+    prefill_tc_kernel<128><<<dim3(p.n_ctas, p.Hk), kThreads, TcCfg<128>::kSmem, s>>>(p);
+  } else if (D == 64) {
+    prefill_tc_kernel<64><<<dim3(p.n_ctas, p.Hk), kThreads, TcCfg<64>::kSmem, s>>>(p);
+  } else {
+    return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t configure_prefill_tc() {
+  cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<128>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       TcCfg<128>::kSmem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(prefill_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              TcCfg<64>::kSmem);
+}
+
+}  // namespace kvinc
