@@ -60,6 +60,39 @@ __device__ __forceinline__ int find_cta_row(const PrefillParams &p, int b) {
   return lo;
 }
 
+// Visible key indices of one query row within a key segment, as two inclusive ranges
+// (an empty range has lo > hi).  Global layer: cache slots 0..p.  Sliding layer, ring
+// segment: slot s holds position s + base (s <= rem) or s + base - R (s > rem), or just s
+// while lens <= R; it is visible iff that position is >= p - W + 1.  Sliding layer, chunk
+// scratch: token j sits at lens + j and is visible iff p - W + 1 <= lens + j <= p.
+__device__ __forceinline__ void row_ranges(bool ring_or_cache, bool qvalid, int qpos, int lens,
+                                           const PrefillParams &p, int (&rg)[4]) {
+  rg[0] = 1; rg[1] = 0; rg[2] = 1; rg[3] = 0;
+  if (!qvalid) return;
+  if (!p.sliding) {  // the global cache holds this chunk too: slots 0..qpos
+    rg[0] = 0;
+    rg[1] = qpos;
+    return;
+  }
+  const int thr = qpos - p.window + 1;  // first visible position
+  if (!ring_or_cache) {                 // chunk scratch
+    rg[0] = max(0, thr - lens);
+    rg[1] = qpos - lens;
+    return;
+  }
+  const int R = p.ring_R;
+  if (lens <= R) {
+    rg[0] = max(0, thr);
+    rg[1] = lens - 1;
+    return;
+  }
+  const int base = ((lens - 1) / R) * R, rem = (lens - 1) % R;
+  rg[0] = max(0, thr - base);
+  rg[1] = rem;
+  rg[2] = max(rem + 1, thr - base + R);
+  rg[3] = R - 1;
+}
+
 // 2^x with the hardware approximation (relative error ~2^-22), denormals flushed.
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
@@ -104,10 +137,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int rho_last = min(n_rho, rho0 + kRows) - 1;
   const int t_max = rho_last / p.rep;
   const int lens = row.lens;
-  // Ring slot s holds position s + ring_base, less R when s > ring_rem: the largest
-  // position below lens congruent to s modulo R (every slot is occupied once lens >= R).
-  const int ring_base = (lens > p.ring_R && p.ring_R > 0) ? ((lens - 1) / p.ring_R) * p.ring_R : 0;
-  const int ring_rem = (lens > p.ring_R && p.ring_R > 0) ? (lens - 1) % p.ring_R : 0x7fffffff;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
@@ -267,6 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int qpos = lens + (qvalid ? rho / p.rep : 0);
     const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
     float m_used = -INFINITY, l_run = 0.f;
+    int rg[4];  // visible key-index ranges [rg0, rg1] and [rg2, rg3] of the current segment
     bool ok = true;
     for (int j = 0; j < n_tiles && ok; ++j) {
       const int sb = j & 1;
@@ -290,13 +320,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&s_free[sb]);
 
-      // mask and scale (log2 units)
+      // mask and scale (log2 units): the visible keys of a segment are at most two
+      // index ranges per row (computed when the segment starts)
       const bool in_a = j < tiles_a;
       const int kb = (in_a ? j : j - tiles_a) * kKeys;
       const int seg_len = in_a ? len_a : len_b;
+      if (j == 0 || j == tiles_a) row_ranges(in_a, qvalid, qpos, lens, p, rg);
       float mt = -INFINITY;
-      if (qvalid && !p.sliding && kb + kKeys - 1 <= qpos) {
-        // every key of the tile is at or before this row's position
+      const bool all_vis = (kb >= rg[0] && kb + kKeys - 1 <= rg[1]) ||
+                           (kb >= rg[2] && kb + kKeys - 1 <= rg[3]);
+      if (all_vis) {
 #pragma unroll
         for (int i = 0; i < kKeys; ++i) {
           sv[i] *= p.scale_log2;
@@ -306,14 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < kKeys; ++i) {
           const int kidx = kb + i;
-          bool vis = qvalid && kidx < seg_len;
-          if (vis) {
-            int kpos;
-            if (!p.sliding) kpos = kidx;
-            else if (!in_a) kpos = lens + kidx;
-            else kpos = kidx + ring_base - (kidx > ring_rem ? p.ring_R : 0);
-            vis = kpos <= qpos && (!p.sliding || qpos - kpos < p.window);
-          }
+          const bool vis = (kidx >= rg[0] && kidx <= rg[1]) || (kidx >= rg[2] && kidx <= rg[3]);
           sv[i] = vis ? sv[i] * p.scale_log2 : -INFINITY;
           mt = fmaxf(mt, sv[i]);
         }
