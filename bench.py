@@ -57,8 +57,8 @@ def parse():
     ap.add_argument("--fill-only", action="store_true",
                     help="time only the chunked-prefill cache fill of one cache (TFLOP/s)")
     ap.add_argument("--fill-to", type=int, default=0,
-                    help="with --fill-only: fill every row to this length (default: the "
-                         "workload's length draw)")
+                    help="fill every row to this length instead of the workload's length "
+                         "draw (small cases for profiling)")
     return ap.parse_args()
 
 
@@ -429,6 +429,8 @@ def run_ours(args):
         seed_r = args.seed + 7919 * rank + 104729 * r
         c = kvi.KVCache(B, cfg["max_len"], Hq, Hk, D, cfg["W"], cfg["kinds"], 1e4, local_rank)
         l0 = initial_lens(cfg, reserve, seed_r)
+        if args.fill_to:  # small-case profiling: every row at the same, shorter length
+            l0 = np.full(B, min(args.fill_to, cfg["max_len"] - reserve - 1), dtype=np.int64)
         c.profile(r == 0)  # the chunked-prefill kernel, timed on the first fill
         fill_cache(c, cfg, l0, seed_r, stream)
         if r == 0:

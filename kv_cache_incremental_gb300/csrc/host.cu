@@ -169,10 +169,11 @@ void plan_decode(const kv_cache *c, bool sliding, const std::vector<DecodeIn> &i
     nk[i] = sliding ? std::min(in[i].pos + 1, c->R) : in[i].pos + 1;
     total_tiles += (nk[i] + kTileKeys - 1) / kTileKeys;
   }
-  // Aim for about four waves of two CTAs per SM; splits of at least four tiles.
+  // Aim for about four waves of two CTAs per SM; splits of at least eight tiles (512 keys):
+  // a shorter row is one CTA with no split merge, which is what small (ring) layers want.
   const int64_t target = (int64_t)c->num_sms * 2 * 4;
   int64_t per = (total_tiles * c->Hk + target - 1) / target;
-  if (per < 4) per = 4;
+  if (per < 8) per = 8;
   int item = 0, part = 0;
   kv_bytes = 0;
   flops = 0;
