@@ -21,6 +21,7 @@ cudaError_t configure_decode();
 cudaError_t configure_prefill();
 cudaError_t configure_prefill_tc();
 cudaError_t launch_prefill_tc(const PrefillParams &p, int D, cudaStream_t s);
+int prefill_tc_rows_per_cta();
 }  // namespace kvinc
 
 using namespace kvinc;
@@ -311,7 +312,7 @@ int append_device(kv_cache *c, int layer, const __nv_bfloat16 *q, const __nv_bfl
       std::vector<PrefillRow> sel;
       for (const PrefillRow &r : prows)
         if ((r.n * rep >= kTcMinRows) == (kind == 1)) sel.push_back(r);
-      const int rows_per_cta = kind == 1 ? 128 : 64;
+      const int rows_per_cta = kind == 1 ? prefill_tc_rows_per_cta() : 64;
       for (size_t r0 = 0; r0 < sel.size(); r0 += kMaxRowsPerLaunch) {
         const size_t r1 = std::min(sel.size(), r0 + kMaxRowsPerLaunch);
         pp.tmap_k = c->tmK[layer];

@@ -8,16 +8,24 @@
 // chunk is committed to it ("inkling: ring-buffer KV cache for sliding-window
 // layers", How it works; Lab 07 section 3; tiny_agent/generate.py `_append_chunk`).
 //
-// One CTA owns 128 query rows (the MMA's M) of one (row, kv head).  Warp roles:
-//   warps 0-3  softmax: thread i owns query row i = TMEM lane i.  They rotate the
-//              queries into shared memory, read S from TMEM, mask, run the online
-//              softmax (lazy rescaling: O in TMEM is rescaled only when a row's
-//              maximum grows by more than 2^8), write P as bf16 high and low parts
-//              into shared memory, and finally read O from TMEM and normalise.
-//   warp 4     TMA producer of 64-key K and V tiles (128-byte swizzle).
-//   warp 5     TMEM owner and MMA issuer (one thread): S = Q K^T (M=128, N=64)
-//              into one of two TMEM S buffers, O += P_hi V + P_lo V (M=128, N=D),
-//              with V read in place as an MN-major operand (keys are its K).
+// One CTA owns up to two 128-row query tiles (the MMA's M) of one (row, kv head);
+// both tiles share every K/V tile the CTA streams.  Warp roles:
+//   warps 0-7  softmax, four per query tile: thread i of a tile owns query row i =
+//              TMEM lane i of that tile's accumulators.  They rotate the queries into
+//              shared memory, read S from TMEM, mask, run the online softmax (lazy
+//              rescaling: O in TMEM is rescaled only when a row's maximum grows by
+//              more than 2^8), write P as bf16 high and low parts into shared memory,
+//              and finally read O from TMEM and normalise.  Two warps of different
+//              tiles share each SM sub-partition and hide each other's latency.
+//   warp 8     TMA producer of 64-key K and V tiles (128-byte swizzle).
+//   warp 9     TMEM owner and MMA issuer (one thread).  For each query tile it keeps
+//              two cursors: S = Q K^T (M=128, N=64) of K/V tile j into one of the
+//              tile's two TMEM S buffers once the K/V stage has landed and that buffer
+//              is free, and O += P_hi V + P_lo V (M=128, N=D) once the softmax warps
+//              have written P of tile j, with V read in place as an MN-major operand
+//              (keys are its K).  It polls both query tiles and issues whichever step
+//              is ready, so one tile's slow softmax does not stall the other's MMAs; a
+//              K/V stage is released when both tiles' PV of it has been issued.
 // Every mbarrier wait is bounded; on a timeout the CTA records the error, lets its
 // own TMA loads and MMAs finish (bounded), frees its TMEM and returns.
 #include "kvinc_internal.h"
@@ -26,28 +34,30 @@
 namespace kvinc {
 namespace {
 
-constexpr int kRows = 128;        // query rows per CTA (MMA M)
+constexpr int kRows = 128;        // query rows per tile (MMA M)
+constexpr int kTilesQ = 2;        // query tiles per CTA
 constexpr int kKeys = kTileKeys;  // keys per tile (MMA N of S, K of PV)
-constexpr int kThreads = 6 * 32;
-constexpr int kSoftmaxWarps = 4;
-constexpr int kProducerWarp = 4, kMmaWarp = 5;
-constexpr int kStages = 3;
+constexpr int kSoftmaxWarps = 4;  // per query tile
+constexpr int kProducerWarp = kTilesQ * kSoftmaxWarps, kMmaWarp = kProducerWarp + 1;
+constexpr int kThreads = (kMmaWarp + 1) * 32;
 constexpr float kRescaleLog2 = 8.f;  // lazy rescale threshold (log2 units)
 
 template <int D>
 struct TcCfg {
   static constexpr int kPanels = D / 64;
-  static constexpr int kQBytes = kPanels * kRows * 128;   // Q, K-major, 128-byte swizzle
+  static constexpr int kStages = D == 128 ? 3 : 4;
+  static constexpr int kQBytes = kPanels * kRows * 128;   // one Q tile, K-major, 128B swizzle
   static constexpr int kKVTile = kPanels * kKeys * 128;    // one K or V tile (TMA layout)
   static constexpr int kStageBytes = 2 * kKVTile;
   static constexpr int kPBytes = kRows * 128;              // P: 128 rows x 64 keys bf16
-  static constexpr int kTmemCols = 256;                    // S0 | S1 | O
+  static constexpr int kTmemCols = 512;                    // [S0 S0' S1 S1'] [O0] [O1]
   static constexpr int kOff_Q = 0;
-  static constexpr int kOff_KV = kOff_Q + kQBytes;
-  static constexpr int kOff_P = kOff_KV + kStages * kStageBytes;  // [buf][hi | lo]
-  static constexpr int kOff_Bar = kOff_P + 2 * 2 * kPBytes;
-  static constexpr int kBars = 2 * kStages + 4 * 2 + 1;
+  static constexpr int kOff_KV = kOff_Q + kTilesQ * kQBytes;
+  static constexpr int kOff_P = kOff_KV + kStages * kStageBytes;  // [tile][hi | lo]
+  static constexpr int kOff_Bar = kOff_P + kTilesQ * 2 * kPBytes;
+  static constexpr int kBars = 2 * kStages + kTilesQ * 6 + 1;
   static constexpr int kSmem = 1024 + kOff_Bar + kBars * 8 + 32;
+  static_assert(kSmem <= 232448, "shared memory per CTA");
 };
 
 __device__ __forceinline__ int find_cta_row(const PrefillParams &p, int b) {
@@ -100,41 +110,36 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-__device__ __forceinline__ void stsm_x4(uint32_t addr, uint32_t r0, uint32_t r1, uint32_t r2,
-                                        uint32_t r3) {
-  asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};" ::"r"(addr),
-               "r"(r0), "r"(r1), "r"(r2), "r"(r3)
-               : "memory");
-}
-
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
   using Cfg = TcCfg<D>;
+  constexpr int kStages = Cfg::kStages;
   constexpr int kHalf = D / 2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t *qsm = smem + Cfg::kOff_Q;
+  uint8_t *qsm = smem + Cfg::kOff_Q;     // Q tile qt at qt * kQBytes
   uint8_t *kv = smem + Cfg::kOff_KV;
-  uint8_t *pbuf = smem + Cfg::kOff_P;  // P tile b: hi at b * 2 * kPBytes, lo kPBytes later
+  uint8_t *pbuf = smem + Cfg::kOff_P;    // P of tile qt: hi at qt * 2 * kPBytes, lo after it
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::kOff_Bar);
-  uint64_t *kv_full = bars;                 // [kStages] TMA -> MMA and softmax
-  uint64_t *kv_empty = kv_full + kStages;   // [kStages] QK and PV of the stage done
-  uint64_t *s_full = kv_empty + kStages;    // [2] QK done -> softmax
-  uint64_t *s_free = s_full + 2;            // [2] softmax read S -> MMA
-  uint64_t *p_full = s_free + 2;            // [2] softmax wrote P buffer -> MMA
-  uint64_t *o_done = p_full + 2;            // [2] PV that read P buffer b done -> softmax
-  uint64_t *drain = o_done + 2;             // [1] every MMA done (teardown)
+  uint64_t *kv_full = bars;                       // [kStages] TMA -> MMA and softmax
+  uint64_t *kv_empty = kv_full + kStages;         // [kStages] every MMA of the stage done
+  uint64_t *s_full = kv_empty + kStages;          // [tile][2] QK done -> softmax
+  uint64_t *s_free = s_full + 2 * kTilesQ;        // [tile][2] softmax read S -> MMA
+  uint64_t *p_full = s_free + 2 * kTilesQ;        // [tile] softmax wrote P -> MMA
+  uint64_t *o_done = p_full + kTilesQ;            // [tile] PV done -> softmax
+  uint64_t *drain = o_done + kTilesQ;             // [1] every MMA done (teardown)
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + Cfg::kBars);
   volatile int *fail = reinterpret_cast<volatile int *>(tmem_slot + 1);
   volatile int *issued = fail + 1;
 
   const PrefillRow &row = p.rows[find_cta_row(p, blockIdx.x)];
   const int g = blockIdx.y;
-  const int rho0 = (blockIdx.x - row.cta0) * kRows;
+  const int rho0 = (blockIdx.x - row.cta0) * kRows * kTilesQ;
   const int n_rho = row.n * p.rep;
-  const int rho_last = min(n_rho, rho0 + kRows) - 1;
+  const int n_qt = min(kTilesQ, (n_rho - rho0 + kRows - 1) / kRows);  // query tiles in use
+  const int rho_last = min(n_rho, rho0 + kRows * kTilesQ) - 1;
   const int t_max = rho_last / p.rep;
   const int lens = row.lens;
   const int warp = threadIdx.x >> 5;
@@ -152,13 +157,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(&kv_full[s], 1);
       ptx::mbar_init(&kv_empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      ptx::mbar_init(&s_full[b], 1);
-      ptx::mbar_init(&s_free[b], kSoftmaxWarps);
-    }
-    for (int b = 0; b < 2; ++b) {
-      ptx::mbar_init(&p_full[b], kSoftmaxWarps);
-      ptx::mbar_init(&o_done[b], 1);
+    for (int qt = 0; qt < kTilesQ; ++qt) {
+      for (int b = 0; b < 2; ++b) {
+        ptx::mbar_init(&s_full[2 * qt + b], 1);
+        ptx::mbar_init(&s_free[2 * qt + b], kSoftmaxWarps);
+      }
+      ptx::mbar_init(&p_full[qt], kSoftmaxWarps);
+      ptx::mbar_init(&o_done[qt], 1);
     }
     ptx::mbar_init(drain, 1);
     *fail = 0;
@@ -166,15 +171,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::fence_barrier_init();
   }
   if (warp == kMmaWarp) tc::alloc(tmem_slot, Cfg::kTmemCols);
-  if (warp < kSoftmaxWarps) {
-    // Rotated query of this thread's row into the 128-byte-swizzled Q tile.
-    const int r = threadIdx.x;
-    const int rho = rho0 + r;
+  const int qt_me = warp / kSoftmaxWarps;  // query tile of a softmax warp
+  if (warp < kProducerWarp) {
+    // Rotated query of this thread's row into its tile's 128-byte-swizzled Q tile.
+    const int r = threadIdx.x % kRows;
+    const int rho = rho0 + qt_me * kRows + r;
     const bool valid = rho < n_rho;
     const int t = valid ? rho / p.rep : 0, h = valid ? rho % p.rep : 0;
     const __nv_bfloat16 *q = p.q + (int64_t)row.call_row * p.q_row_stride +
                              ((int64_t)t * p.Hq + g * p.rep + h) * D;
     const float2 *cs = p.rope + (int64_t)(lens + t) * kHalf;
+    uint8_t *qtile = qsm + qt_me * Cfg::kQBytes;
 #pragma unroll 2
     for (int c = 0; c < kHalf / 8; ++c) {
       uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
@@ -194,8 +201,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       const int c_lo = c, c_hi = kHalf / 8 + c;  // 16-byte chunk index along D
-      *reinterpret_cast<uint4 *>(qsm + (c_lo / 8) * kRows * 128 + ptx::swz128(r, c_lo % 8)) = lo;
-      *reinterpret_cast<uint4 *>(qsm + (c_hi / 8) * kRows * 128 + ptx::swz128(r, c_hi % 8)) = hi;
+      *reinterpret_cast<uint4 *>(qtile + (c_lo / 8) * kRows * 128 + ptx::swz128(r, c_lo % 8)) = lo;
+      *reinterpret_cast<uint4 *>(qtile + (c_hi / 8) * kRows * 128 + ptx::swz128(r, c_hi % 8)) = hi;
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // Q -> tensor core
   }
@@ -203,8 +210,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS[2] = {tmem, tmem + kKeys};
-  const uint32_t tO = tmem + 2 * kKeys;
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ TMA producer
@@ -240,46 +245,70 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t kIdQK = tc::idesc_bf16_f32(kRows, kKeys);
       constexpr uint32_t kIdPV = tc::idesc_bf16_f32(kRows, D, /*b_mn_major=*/true);
-      const uint32_t q_addr = ptx::smem_u32(qsm);
-      auto issue_pv = [&](int i) -> bool {
-        const int b = i & 1;
-        if (!ptx::mbar_wait(&p_full[b], (i >> 1) & 1, kWaitLimit)) return false;
+      // The two query tiles advance independently: issue whichever QK or PV is ready
+      // (non-blocking polls), so one tile's softmax never stalls the other's MMAs.
+      auto issue_qk = [&](int qt, int j) {
         tc::fence_after();
-        // B = V as stored by TMA: rows = keys (K), 64-dim panels (MN) kKeys*128 bytes apart
-        const uint32_t v_addr = ptx::smem_u32(kv + (i % kStages) * Cfg::kStageBytes + Cfg::kKVTile);
-        const uint32_t ph = ptx::smem_u32(pbuf + b * 2 * Cfg::kPBytes);
-        const uint32_t pl = ph + Cfg::kPBytes;
-#pragma unroll
-        for (int ks = 0; ks < kKeys / 16; ++ks) {
-          const uint64_t bd = tc::desc_sw128_mn(v_addr + ks * 16 * 128, kKeys * 128, 1024);
-          tc::mma(tO, tc::desc_sw128(ph + 32 * ks), bd, kIdPV, i > 0 || ks > 0);
-          tc::mma(tO, tc::desc_sw128(pl + 32 * ks), bd, kIdPV, true);
-        }
-        tc::commit(&kv_empty[i % kStages]);  // V of this stage is consumed
-        tc::commit(&o_done[b]);
-        return true;
-      };
-      bool ok = true;
-      for (int j = 0; j < n_tiles && ok && !*fail; ++j) {
-        const int s = j % kStages, sb = j & 1;
-        if (!ptx::mbar_wait(&kv_full[s], (j / kStages) & 1, kWaitLimit) ||
-            (j >= 2 && !ptx::mbar_wait(&s_free[sb], ((j - 2) >> 1) & 1, kWaitLimit))) {
-          ok = false;
-          break;
-        }
-        tc::fence_after();
-        const uint32_t k_addr = ptx::smem_u32(kv + s * Cfg::kStageBytes);
+        const uint32_t k_addr = ptx::smem_u32(kv + (j % kStages) * Cfg::kStageBytes);
+        const uint32_t q_addr = ptx::smem_u32(qsm + qt * Cfg::kQBytes);
+        const uint32_t tS = tmem + (2 * qt + (j & 1)) * kKeys;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off_q = (kk / 4) * (kRows * 128) + 32 * (kk % 4);
           const uint32_t off_k = (kk / 4) * (kKeys * 128) + 32 * (kk % 4);
-          tc::mma(tS[sb], tc::desc_sw128(q_addr + off_q), tc::desc_sw128(k_addr + off_k), kIdQK,
+          tc::mma(tS, tc::desc_sw128(q_addr + off_q), tc::desc_sw128(k_addr + off_k), kIdQK,
                   kk > 0);
         }
-        tc::commit(&s_full[sb]);
-        if (j >= 1 && !issue_pv(j - 1)) ok = false;
+        tc::commit(&s_full[2 * qt + (j & 1)]);
+      };
+      int qk_next[kTilesQ] = {0, 0}, pv_next[kTilesQ] = {0, 0};
+      int pv_min = 0;  // K/V tiles below this have had every query tile's PV issued
+      bool ok = true;
+      uint32_t idle = 0;
+      while (ok && pv_min < n_tiles) {
+        if (*fail) {
+          ok = false;
+          break;
+        }
+        bool progress = false;
+        for (int qt = 0; qt < n_qt; ++qt) {
+          const int jq = qk_next[qt];
+          if (jq < n_tiles && jq < pv_next[qt] + 2 &&
+              ptx::mbar_try_wait(&kv_full[jq % kStages], (jq / kStages) & 1) &&
+              (jq < 2 || ptx::mbar_try_wait(&s_free[2 * qt + (jq & 1)], ((jq - 2) >> 1) & 1))) {
+            issue_qk(qt, jq);
+            qk_next[qt] = jq + 1;
+            progress = true;
+          }
+          const int jp = pv_next[qt];
+          if (jp < qk_next[qt] && ptx::mbar_try_wait(&p_full[qt], jp & 1)) {
+            tc::fence_after();
+            // B = V as stored by TMA: rows = keys (K), 64-dim panels (MN) kKeys*128 apart
+            const uint32_t v_addr =
+                ptx::smem_u32(kv + (jp % kStages) * Cfg::kStageBytes + Cfg::kKVTile);
+            const uint32_t ph = ptx::smem_u32(pbuf + qt * 2 * Cfg::kPBytes);
+            const uint32_t pl = ph + Cfg::kPBytes;
+            const uint32_t tO = tmem + 4 * kKeys + qt * D;
+#pragma unroll
+            for (int ks = 0; ks < kKeys / 16; ++ks) {
+              const uint64_t bd = tc::desc_sw128_mn(v_addr + ks * 16 * 128, kKeys * 128, 1024);
+              tc::mma(tO, tc::desc_sw128(ph + 32 * ks), bd, kIdPV, jp > 0 || ks > 0);
+              tc::mma(tO, tc::desc_sw128(pl + 32 * ks), bd, kIdPV, true);
+            }
+            tc::commit(&o_done[qt]);
+            pv_next[qt] = jp + 1;
+            progress = true;
+          }
+        }
+        int m = pv_next[0];
+        for (int qt = 1; qt < n_qt; ++qt) m = min(m, pv_next[qt]);
+        for (; pv_min < m; ++pv_min) tc::commit(&kv_empty[pv_min % kStages]);  // stage consumed
+        if (progress) {
+          idle = 0;
+        } else if (++idle > kWaitLimit) {
+          ok = false;
+        }
       }
-      if (ok && !*fail && n_tiles > 0 && !issue_pv(n_tiles - 1)) ok = false;
       if (!ok) {
         atomicExch(p.err, 1);
         *fail = 1;
@@ -288,37 +317,42 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::commit(drain);
       ptx::mbar_wait(drain, 0, kWaitLimit);
     }
-  } else {
+  } else if (qt_me < n_qt) {
     // ------------------------------------------------------------ softmax warps
-    const int r = threadIdx.x;  // query row of this thread = TMEM lane
-    const int rho = rho0 + r;
+    const int qt = qt_me;
+    const int r = threadIdx.x % kRows;  // query row of this thread = TMEM lane
+    const int rho = rho0 + qt * kRows + r;
     const bool qvalid = rho < n_rho;
     const int qpos = lens + (qvalid ? rho / p.rep : 0);
-    const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
+    const uint32_t lane_off = (uint32_t)(32 * (warp % 4)) << 16;
+    const uint32_t tO = tmem + 4 * kKeys + qt * D + lane_off;
+    uint8_t *p_hi = pbuf + qt * 2 * Cfg::kPBytes;
+    uint8_t *p_lo = p_hi + Cfg::kPBytes;
     float m_used = -INFINITY, l_run = 0.f;
     int rg[4];  // visible key-index ranges [rg0, rg1] and [rg2, rg3] of the current segment
     bool ok = true;
     for (int j = 0; j < n_tiles && ok; ++j) {
       const int sb = j & 1;
       // warp-uniform decisions: tcgen05.ld / st are warp-collective
-      const bool good = !*fail && ptx::mbar_wait(&s_full[sb], (j >> 1) & 1, kWaitLimit);
+      const bool good = !*fail && ptx::mbar_wait(&s_full[2 * qt + sb], (j >> 1) & 1, kWaitLimit);
       if (!__all_sync(0xffffffffu, good)) {
         ok = false;
         break;
       }
       tc::fence_after();
       float sv[kKeys];
+      const uint32_t tS = tmem + (2 * qt + sb) * kKeys + lane_off;
 #pragma unroll
       for (int c = 0; c < kKeys / 16; ++c) {
         float t16[16];
-        tc::ld16(tS[sb] + lane_off + 16 * c, t16);
+        tc::ld16(tS + 16 * c, t16);
 #pragma unroll
         for (int i = 0; i < 16; ++i) sv[16 * c + i] = t16[i];
       }
       tc::wait_ld();
       tc::fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&s_free[sb]);
+      if (lane == 0) ptx::mbar_arrive(&s_free[2 * qt + sb]);
 
       // mask and scale (log2 units): the visible keys of a segment are at most two
       // index ranges per row (computed when the segment starts)
@@ -344,13 +378,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           mt = fmaxf(mt, sv[i]);
         }
       }
-      // The P buffer of this tile was last read by PV(j-2).
-      const int pb = j & 1;
-      const bool buf_free = j < 2 || ptx::mbar_wait(&o_done[pb], ((j - 2) >> 1) & 1, kWaitLimit);
-      if (!__all_sync(0xffffffffu, buf_free)) {
+      // PV(j-1) of this tile must be complete: O is stable and the P buffer is free.
+      const bool pv_done = j < 1 || ptx::mbar_wait(&o_done[qt], (j - 1) & 1, kWaitLimit);
+      if (!__all_sync(0xffffffffu, pv_done)) {
         ok = false;
         break;
       }
+      tc::fence_after();
       float alpha = 1.f;
       bool rescale = false;
       if (m_used == -INFINITY) {
@@ -361,40 +395,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         rescale = true;
       }
       if (__any_sync(0xffffffffu, rescale)) {
-        // O may be rescaled only once PV(j-1), the last MMA to write it, is complete.
-        const bool pv_done =
-            j < 1 || ptx::mbar_wait(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, kWaitLimit);
-        if (!__all_sync(0xffffffffu, pv_done)) {
-          ok = false;
-          break;
-        }
-        tc::fence_after();
 #pragma unroll
         for (int c = 0; c < D / 16; ++c) {
           float o16[16];
-          tc::ld16(tO + lane_off + 16 * c, o16);
+          tc::ld16(tO + 16 * c, o16);
           tc::wait_ld();
 #pragma unroll
           for (int i = 0; i < 16; ++i) o16[i] *= alpha;
-          tc::st16(tO + lane_off + 16 * c, o16);
+          tc::st16(tO + 16 * c, o16);
         }
         tc::wait_st();
       }
       l_run *= alpha;
-      const float base = m_used == -INFINITY ? 0.f : m_used;
-      if (seg_len - kb < kKeys) {
+      if (qt == 0 && seg_len - kb < kKeys) {
         // Keys past the segment may hold anything: zero their V rows so that 0 * V
-        // stays 0 in the PV product (the MMA reads V only after P is published).
+        // stays 0 in the PV product (the MMA reads V only after tile 0's P is
+        // published, and tile 1's PV is issued after tile 0's).
         uint8_t *vtile = kv + (j % kStages) * Cfg::kStageBytes + Cfg::kKVTile;
         const int first = seg_len - kb > 0 ? seg_len - kb : 0;
-        for (int u = r; u < (kKeys - first) * (D / 8); u += kSoftmaxWarps * 32) {
+        for (int u = r; u < (kKeys - first) * (D / 8); u += kRows) {
           const int vr = first + u / (D / 8), ch = u % (D / 8);
           *reinterpret_cast<uint4 *>(vtile + (ch / 8) * (kKeys * 128) + ptx::swz128(vr, ch % 8)) =
               make_uint4(0, 0, 0, 0);
         }
       }
-      uint8_t *p_hi = pbuf + pb * 2 * Cfg::kPBytes;
-      uint8_t *p_lo = p_hi + Cfg::kPBytes;
+      const float base = m_used == -INFINITY ? 0.f : m_used;
       // P = 2^(s - m) as bf16 high + low parts, row r of the swizzled P tiles
 #pragma unroll
       for (int c = 0; c < kKeys / 8; ++c) {
@@ -413,11 +438,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // P -> tensor core
       tc::fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&p_full[pb]);
+      if (lane == 0) ptx::mbar_arrive(&p_full[qt]);
     }
-    const bool last_done = ok && n_tiles > 0 &&
-                           ptx::mbar_wait(&o_done[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1,
-                                          kWaitLimit);
+    const bool last_done =
+        ok && n_tiles > 0 && ptx::mbar_wait(&o_done[qt], (n_tiles - 1) & 1, kWaitLimit);
     if (!ok) {
       atomicExch(p.err, 1);
       *fail = 1;
@@ -430,7 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < D / 16; ++c) {
         float o16[16];
-        tc::ld16(tO + lane_off + 16 * c, o16);
+        tc::ld16(tO + 16 * c, o16);
         tc::wait_ld();
         uint4 w0, w1;
         w0.x = ptx::pack_bf16(o16[0] * inv, o16[1] * inv);
@@ -470,6 +494,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 }  // namespace
+
+// Query rows one CTA of the tcgen05 prefill covers.
+int prefill_tc_rows_per_cta() { return kRows * kTilesQ; }
 
 cudaError_t launch_prefill_tc(const PrefillParams &p, int D, cudaStream_t s) {
   if (p.n_ctas <= 0) return cudaSuccess;
