@@ -14,16 +14,16 @@
 //              TMEM lane i of that tile's accumulators.  They rotate the queries into
 //              shared memory, read S from TMEM, mask, run the online softmax (lazy
 //              rescaling: O in TMEM is rescaled only when a row's maximum grows by
-//              more than 2^8), write P as bf16 high and low parts into shared memory,
-//              and finally read O from TMEM and normalise.  Two warps of different
+//              more than 2^8), write P as bf16 high and low parts back into the TMEM
+//              columns that held S, and finally read O from TMEM and normalise.  Two warps of different
 //              tiles share each SM sub-partition and hide each other's latency.
 //   warp 8     TMA producer of 64-key K and V tiles (128-byte swizzle).
 //   warp 9     TMEM owner and MMA issuer (one thread).  For each query tile it keeps
 //              two cursors: S = Q K^T (M=128, N=64) of K/V tile j into one of the
-//              tile's two TMEM S buffers once the K/V stage has landed and that buffer
-//              is free, and O += P_hi V + P_lo V (M=128, N=D) once the softmax warps
-//              have written P of tile j, with V read in place as an MN-major operand
-//              (keys are its K).  It polls both query tiles and issues whichever step
+//              tile's two TMEM S buffers once the K/V stage has landed and the PV that
+//              last read that buffer is done, and O += P_hi V + P_lo V (M=128, N=D)
+//              once the softmax warps have written P of tile j, with P read from TMEM
+//              and V read in place as an MN-major operand (keys are its K).  It polls both query tiles and issues whichever step
 //              is ready, so one tile's slow softmax does not stall the other's MMAs; a
 //              K/V stage is released when both tiles' PV of it has been issued.
 // Every mbarrier wait is bounded; on a timeout the CTA records the error, lets its
@@ -45,16 +45,16 @@ constexpr float kRescaleLog2 = 8.f;  // lazy rescale threshold (log2 units)
 template <int D>
 struct TcCfg {
   static constexpr int kPanels = D / 64;
-  static constexpr int kStages = D == 128 ? 3 : 4;
+  static constexpr int kStages = D == 128 ? 5 : 8;
   static constexpr int kQBytes = kPanels * kRows * 128;   // one Q tile, K-major, 128B swizzle
   static constexpr int kKVTile = kPanels * kKeys * 128;    // one K or V tile (TMA layout)
   static constexpr int kStageBytes = 2 * kKVTile;
-  static constexpr int kPBytes = kRows * 128;              // P: 128 rows x 64 keys bf16
+  // TMEM: per query tile two 64-column S buffers (S fp32; then P as 32 columns of bf16
+  // pairs for the high part and 32 for the low part) and one D-column O accumulator.
   static constexpr int kTmemCols = 512;                    // [S0 S0' S1 S1'] [O0] [O1]
   static constexpr int kOff_Q = 0;
   static constexpr int kOff_KV = kOff_Q + kTilesQ * kQBytes;
-  static constexpr int kOff_P = kOff_KV + kStages * kStageBytes;  // [tile][hi | lo]
-  static constexpr int kOff_Bar = kOff_P + kTilesQ * 2 * kPBytes;
+  static constexpr int kOff_Bar = kOff_KV + kStages * kStageBytes;
   static constexpr int kBars = 2 * kStages + kTilesQ * 6 + 1;
   static constexpr int kSmem = 1024 + kOff_Bar + kBars * 8 + 32;
   static_assert(kSmem <= 232448, "shared memory per CTA");
@@ -121,15 +121,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t *qsm = smem + Cfg::kOff_Q;     // Q tile qt at qt * kQBytes
   uint8_t *kv = smem + Cfg::kOff_KV;
-  uint8_t *pbuf = smem + Cfg::kOff_P;    // P of tile qt: hi at qt * 2 * kPBytes, lo after it
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::kOff_Bar);
   uint64_t *kv_full = bars;                       // [kStages] TMA -> MMA and softmax
   uint64_t *kv_empty = kv_full + kStages;         // [kStages] every MMA of the stage done
-  uint64_t *s_full = kv_empty + kStages;          // [tile][2] QK done -> softmax
-  uint64_t *s_free = s_full + 2 * kTilesQ;        // [tile][2] softmax read S -> MMA
-  uint64_t *p_full = s_free + 2 * kTilesQ;        // [tile] softmax wrote P -> MMA
-  uint64_t *o_done = p_full + kTilesQ;            // [tile] PV done -> softmax
-  uint64_t *drain = o_done + kTilesQ;             // [1] every MMA done (teardown)
+  // Per query tile and S buffer b (tile j uses b = j & 1); each barrier completes one
+  // phase per use of its buffer, and a buffer is reused only after its previous PV is
+  // done, so no waiter can fall two phases behind.
+  uint64_t *s_full = kv_empty + kStages;          // [tile][b] QK done -> softmax
+  uint64_t *p_full = s_full + 2 * kTilesQ;        // [tile][b] softmax wrote P -> MMA
+  uint64_t *pv_done = p_full + 2 * kTilesQ;       // [tile][b] PV done -> MMA, softmax
+  uint64_t *drain = pv_done + 2 * kTilesQ;        // [1] every MMA done (teardown)
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + Cfg::kBars);
   volatile int *fail = reinterpret_cast<volatile int *>(tmem_slot + 1);
   volatile int *issued = fail + 1;
@@ -160,10 +161,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int qt = 0; qt < kTilesQ; ++qt) {
       for (int b = 0; b < 2; ++b) {
         ptx::mbar_init(&s_full[2 * qt + b], 1);
-        ptx::mbar_init(&s_free[2 * qt + b], kSoftmaxWarps);
+        ptx::mbar_init(&p_full[2 * qt + b], kSoftmaxWarps);
+        ptx::mbar_init(&pv_done[2 * qt + b], 1);
       }
-      ptx::mbar_init(&p_full[qt], kSoftmaxWarps);
-      ptx::mbar_init(&o_done[qt], 1);
     }
     ptx::mbar_init(drain, 1);
     *fail = 0;
@@ -245,9 +245,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t kIdQK = tc::idesc_bf16_f32(kRows, kKeys);
       constexpr uint32_t kIdPV = tc::idesc_bf16_f32(kRows, D, /*b_mn_major=*/true);
-      // The two query tiles advance independently: issue whichever QK or PV is ready
-      // (non-blocking polls), so one tile's softmax never stalls the other's MMAs.
-      auto issue_qk = [&](int qt, int j) {
+      // Fixed issue order.  Prologue QK(0, q0), QK(0, q1), QK(1, q0); then per K/V tile r:
+      //   PV(r, q0), QK(r + 1, q1), PV(r, q1), QK(r + 2, q0).
+      // QK(j, q) reuses the S buffer of PV(j - 2, q), which was issued three groups
+      // earlier, so the tensor pipe is not left waiting on its own work; each PV waits
+      // for its softmax, which runs while the three groups before it execute.  PV(r, q1)
+      // follows PV(r, q0), i.e. query tile 0's P of tile r, which is published after its
+      // softmax warps zeroed the V rows past a segment's end.
+      auto issue_qk = [&](int qt, int j) -> bool {
+        if (qt >= n_qt || j >= n_tiles) return true;
+        if (!ptx::mbar_wait(&kv_full[j % kStages], (j / kStages) & 1, kWaitLimit)) return false;
+        if (j >= 2 && !ptx::mbar_wait(&pv_done[2 * qt + (j & 1)], ((j - 2) >> 1) & 1, kWaitLimit))
+          return false;
         tc::fence_after();
         const uint32_t k_addr = ptx::smem_u32(kv + (j % kStages) * Cfg::kStageBytes);
         const uint32_t q_addr = ptx::smem_u32(qsm + qt * Cfg::kQBytes);
@@ -260,54 +269,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                   kk > 0);
         }
         tc::commit(&s_full[2 * qt + (j & 1)]);
+        return true;
       };
-      int qk_next[kTilesQ] = {0, 0}, pv_next[kTilesQ] = {0, 0};
-      int pv_min = 0;  // K/V tiles below this have had every query tile's PV issued
-      bool ok = true;
-      uint32_t idle = 0;
-      while (ok && pv_min < n_tiles) {
+      auto issue_pv = [&](int qt, int j) -> bool {
+        if (qt >= n_qt) return true;
+        if (!ptx::mbar_wait(&p_full[2 * qt + (j & 1)], (j >> 1) & 1, kWaitLimit)) return false;
+        tc::fence_after();
+        // B = V as stored by TMA: rows = keys (K), 64-dim panels (MN) kKeys*128 apart;
+        // A = P in the S buffer: high part in columns 0-31, low part in 32-63, one
+        // 16-key step = 8 columns.
+        const uint32_t v_addr =
+            ptx::smem_u32(kv + (j % kStages) * Cfg::kStageBytes + Cfg::kKVTile);
+        const uint32_t tP = tmem + (2 * qt + (j & 1)) * kKeys;
+        const uint32_t tO = tmem + 4 * kKeys + qt * D;
+#pragma unroll
+        for (int ks = 0; ks < kKeys / 16; ++ks) {
+          const uint64_t bd = tc::desc_sw128_mn(v_addr + ks * 16 * 128, kKeys * 128, 1024);
+          tc::mma_ts(tO, tP + 8 * ks, bd, kIdPV, j > 0 || ks > 0);
+          tc::mma_ts(tO, tP + kKeys / 2 + 8 * ks, bd, kIdPV, true);
+        }
+        tc::commit(&pv_done[2 * qt + (j & 1)]);
+        return true;
+      };
+      bool ok = issue_qk(0, 0) && issue_qk(1, 0) && issue_qk(0, 1);
+      for (int r = 0; ok && r < n_tiles; ++r) {
         if (*fail) {
           ok = false;
           break;
         }
-        bool progress = false;
-        for (int qt = 0; qt < n_qt; ++qt) {
-          const int jq = qk_next[qt];
-          if (jq < n_tiles && jq < pv_next[qt] + 2 &&
-              ptx::mbar_try_wait(&kv_full[jq % kStages], (jq / kStages) & 1) &&
-              (jq < 2 || ptx::mbar_try_wait(&s_free[2 * qt + (jq & 1)], ((jq - 2) >> 1) & 1))) {
-            issue_qk(qt, jq);
-            qk_next[qt] = jq + 1;
-            progress = true;
-          }
-          const int jp = pv_next[qt];
-          if (jp < qk_next[qt] && ptx::mbar_try_wait(&p_full[qt], jp & 1)) {
-            tc::fence_after();
-            // B = V as stored by TMA: rows = keys (K), 64-dim panels (MN) kKeys*128 apart
-            const uint32_t v_addr =
-                ptx::smem_u32(kv + (jp % kStages) * Cfg::kStageBytes + Cfg::kKVTile);
-            const uint32_t ph = ptx::smem_u32(pbuf + qt * 2 * Cfg::kPBytes);
-            const uint32_t pl = ph + Cfg::kPBytes;
-            const uint32_t tO = tmem + 4 * kKeys + qt * D;
-#pragma unroll
-            for (int ks = 0; ks < kKeys / 16; ++ks) {
-              const uint64_t bd = tc::desc_sw128_mn(v_addr + ks * 16 * 128, kKeys * 128, 1024);
-              tc::mma(tO, tc::desc_sw128(ph + 32 * ks), bd, kIdPV, jp > 0 || ks > 0);
-              tc::mma(tO, tc::desc_sw128(pl + 32 * ks), bd, kIdPV, true);
-            }
-            tc::commit(&o_done[qt]);
-            pv_next[qt] = jp + 1;
-            progress = true;
-          }
-        }
-        int m = pv_next[0];
-        for (int qt = 1; qt < n_qt; ++qt) m = min(m, pv_next[qt]);
-        for (; pv_min < m; ++pv_min) tc::commit(&kv_empty[pv_min % kStages]);  // stage consumed
-        if (progress) {
-          idle = 0;
-        } else if (++idle > kWaitLimit) {
-          ok = false;
-        }
+        ok = issue_pv(0, r) && issue_qk(1, r + 1) && issue_pv(1, r);
+        if (ok) tc::commit(&kv_empty[r % kStages]);  // every PV of the stage issued
+        ok = ok && issue_qk(0, r + 2);
       }
       if (!ok) {
         atomicExch(p.err, 1);
@@ -326,8 +318,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int qpos = lens + (qvalid ? rho / p.rep : 0);
     const uint32_t lane_off = (uint32_t)(32 * (warp % 4)) << 16;
     const uint32_t tO = tmem + 4 * kKeys + qt * D + lane_off;
-    uint8_t *p_hi = pbuf + qt * 2 * Cfg::kPBytes;
-    uint8_t *p_lo = p_hi + Cfg::kPBytes;
     float m_used = -INFINITY, l_run = 0.f;
     int rg[4];  // visible key-index ranges [rg0, rg1] and [rg2, rg3] of the current segment
     bool ok = true;
@@ -350,9 +340,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 16; ++i) sv[16 * c + i] = t16[i];
       }
       tc::wait_ld();
-      tc::fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&s_free[2 * qt + sb]);
 
       // mask and scale (log2 units): the visible keys of a segment are at most two
       // index ranges per row (computed when the segment starts)
@@ -378,13 +365,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           mt = fmaxf(mt, sv[i]);
         }
       }
-      // PV(j-1) of this tile must be complete: O is stable and the P buffer is free.
-      const bool pv_done = j < 1 || ptx::mbar_wait(&o_done[qt], (j - 1) & 1, kWaitLimit);
-      if (!__all_sync(0xffffffffu, pv_done)) {
-        ok = false;
-        break;
-      }
-      tc::fence_after();
       float alpha = 1.f;
       bool rescale = false;
       if (m_used == -INFINITY) {
@@ -395,6 +375,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         rescale = true;
       }
       if (__any_sync(0xffffffffu, rescale)) {
+        // O must be stable: PV(j-1) of this tile is done (PV(j) waits for this P).
+        const bool prev = j < 1 || ptx::mbar_wait(&pv_done[2 * qt + ((j - 1) & 1)],
+                                                  ((j - 1) >> 1) & 1, kWaitLimit);
+        if (!__all_sync(0xffffffffu, prev)) {
+          ok = false;
+          break;
+        }
+        tc::fence_after();
 #pragma unroll
         for (int c = 0; c < D / 16; ++c) {
           float o16[16];
@@ -409,8 +397,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       l_run *= alpha;
       if (qt == 0 && seg_len - kb < kKeys) {
         // Keys past the segment may hold anything: zero their V rows so that 0 * V
-        // stays 0 in the PV product (the MMA reads V only after tile 0's P is
-        // published, and tile 1's PV is issued after tile 0's).
+        // stays 0 in the PV product (every PV of this tile is issued after query tile
+        // 0 publishes its P).  The stage cannot be refilled before that either.
+        if (!__all_sync(0xffffffffu, ptx::mbar_wait(&kv_full[j % kStages], (j / kStages) & 1,
+                                                    kWaitLimit))) {
+          ok = false;
+          break;
+        }
         uint8_t *vtile = kv + (j % kStages) * Cfg::kStageBytes + Cfg::kKVTile;
         const int first = seg_len - kb > 0 ? seg_len - kb : 0;
         for (int u = r; u < (kKeys - first) * (D / 8); u += kRows) {
@@ -420,28 +413,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       const float base = m_used == -INFINITY ? 0.f : m_used;
-      // P = 2^(s - m) as bf16 high + low parts, row r of the swizzled P tiles
+      // P = 2^(s - m) as bf16 high + low parts over S in TMEM: keys 2i, 2i+1 of the high
+      // part in column i, of the low part in column 32 + i.
 #pragma unroll
-      for (int c = 0; c < kKeys / 8; ++c) {
-        uint32_t hv[4], lv[4];
+      for (int c = 0; c < kKeys / 32; ++c) {
+        uint32_t hv[16], lv[16];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float e0 = fast_exp2(sv[8 * c + 2 * i] - base);
-          const float e1 = fast_exp2(sv[8 * c + 2 * i + 1] - base);
+        for (int i = 0; i < 16; ++i) {
+          const float e0 = fast_exp2(sv[32 * c + 2 * i] - base);
+          const float e1 = fast_exp2(sv[32 * c + 2 * i + 1] - base);
           l_run += e0 + e1;
           ptx::split_bf16(e0, e1, hv[i], lv[i]);
         }
-        const uint32_t off = ptx::swz128(r, c);
-        *reinterpret_cast<uint4 *>(p_hi + off) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-        *reinterpret_cast<uint4 *>(p_lo + off) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
+        tc::st16(tS + 16 * c, hv);
+        tc::st16(tS + kKeys / 2 + 16 * c, lv);
       }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // P -> tensor core
+      tc::wait_st();
+      if (qt == 0 && seg_len - kb < kKeys)
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // zeroed V -> MMA
       tc::fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&p_full[qt]);
+      if (lane == 0) ptx::mbar_arrive(&p_full[2 * qt + sb]);
     }
+    // The last PV's completion implies every earlier MMA of the issuing thread is done.
     const bool last_done =
-        ok && n_tiles > 0 && ptx::mbar_wait(&o_done[qt], (n_tiles - 1) & 1, kWaitLimit);
+        ok && n_tiles > 0 &&
+        ptx::mbar_wait(&pv_done[2 * qt + ((n_tiles - 1) & 1)], ((n_tiles - 1) >> 1) & 1,
+                       kWaitLimit);
     if (!ok) {
       atomicExch(p.err, 1);
       *fail = 1;
