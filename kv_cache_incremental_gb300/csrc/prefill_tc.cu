@@ -9,23 +9,22 @@
 // layers", How it works; Lab 07 section 3; tiny_agent/generate.py `_append_chunk`).
 //
 // One CTA owns up to two 128-row query tiles (the MMA's M) of one (row, kv head);
-// both tiles share every K/V tile the CTA streams.  Warp roles:
+// both tiles share every K/V block the CTA streams.  A block is 128 keys: two 64-key
+// tiles, each a TMA box, a unit of the masking logic and one half of the softmax pass.
+// Warp roles:
 //   warps 0-7  softmax, four per query tile: thread i of a tile owns query row i =
 //              TMEM lane i of that tile's accumulators.  They rotate the queries into
 //              shared memory, read S from TMEM, mask, run the online softmax (lazy
 //              rescaling: O in TMEM is rescaled only when a row's maximum grows by
 //              more than 2^8), write P as bf16 high and low parts back into the TMEM
-//              columns that held S, and finally read O from TMEM and normalise.  Two warps of different
-//              tiles share each SM sub-partition and hide each other's latency.
-//   warp 8     TMA producer of 64-key K and V tiles (128-byte swizzle).
-//   warp 9     TMEM owner and MMA issuer (one thread).  For each query tile it keeps
-//              two cursors: S = Q K^T (M=128, N=64) of K/V tile j into one of the
-//              tile's two TMEM S buffers once the K/V stage has landed and the PV that
-//              last read that buffer is done, and O += P_hi V + P_lo V (M=128, N=D)
-//              once the softmax warps have written P of tile j, with P read from TMEM
-//              and V read in place as an MN-major operand (keys are its K).  It polls both query tiles and issues whichever step
-//              is ready, so one tile's slow softmax does not stall the other's MMAs; a
-//              K/V stage is released when both tiles' PV of it has been issued.
+//              columns that held S, and finally read O from TMEM and normalise.
+//   warp 8     TMA producer of the K and V blocks (128-byte swizzle).
+//   warp 9     TMEM owner and MMA issuer (one thread).  Per block and query tile:
+//              S = Q K^T (M=128, N=128) into the tile's S buffer, then, once the softmax
+//              wrote P, O += P_hi V + P_lo V (M=128, N=D) with P read from TMEM and V read
+//              in place as an MN-major operand (keys are its K).  Order per block b:
+//              PV(b, q0), QK(b+1, q0), PV(b, q1), QK(b+1, q1); QK(b+1, q) waits for PV(b, q)
+//              to finish reading P from the S buffer it overwrites.
 // Every mbarrier wait is bounded; on a timeout the CTA records the error, lets its
 // own TMA loads and MMAs finish (bounded), frees its TMEM and returns.
 #include "kvinc_internal.h"
@@ -36,7 +35,8 @@ namespace {
 
 constexpr int kRows = 128;        // query rows per tile (MMA M)
 constexpr int kTilesQ = 2;        // query tiles per CTA
-constexpr int kKeys = kTileKeys;  // keys per tile (MMA N of S, K of PV)
+constexpr int kKeys = kTileKeys;  // keys per tile (one TMA box, one softmax half)
+constexpr int kBlockKeys = 2 * kKeys;  // keys per K/V block (MMA N of S, K of PV)
 constexpr int kSoftmaxWarps = 4;  // per query tile
 constexpr int kProducerWarp = kTilesQ * kSoftmaxWarps, kMmaWarp = kProducerWarp + 1;
 constexpr int kThreads = (kMmaWarp + 1) * 32;
@@ -45,19 +45,23 @@ constexpr float kRescaleLog2 = 8.f;  // lazy rescale threshold (log2 units)
 template <int D>
 struct TcCfg {
   static constexpr int kPanels = D / 64;
-  static constexpr int kStages = D == 128 ? 5 : 8;
-  static constexpr int kQBytes = kPanels * kRows * 128;   // one Q tile, K-major, 128B swizzle
-  static constexpr int kKVTile = kPanels * kKeys * 128;    // one K or V tile (TMA layout)
-  static constexpr int kStageBytes = 2 * kKVTile;
-  // TMEM: per query tile two 64-column S buffers (S fp32; then P as 32 columns of bf16
-  // pairs for the high part and 32 for the low part) and one D-column O accumulator.
-  static constexpr int kTmemCols = 512;                    // [S0 S0' S1 S1'] [O0] [O1]
+  static constexpr int kStages = D == 128 ? 2 : 4;
+  static constexpr int kQBytes = kPanels * kRows * 128;        // one Q tile, K-major, 128B swizzle
+  static constexpr int kPanelBytes = kBlockKeys * 128;         // 64 dims of one K or V block
+  static constexpr int kHalfBytes = kKeys * 128;               // one 64-key TMA box of a panel
+  static constexpr int kKVBlock = kPanels * kPanelBytes;       // one K or V block
+  static constexpr int kStageBytes = 2 * kKVBlock;             // [K panels][V panels]
+  // TMEM: per query tile one 128-column S buffer (S fp32 of the block's two 64-key tiles;
+  // then per tile P as 32 columns of bf16 pairs for the high part and 32 for the low
+  // part, in the columns that held that tile's S) and one D-column O accumulator.
+  static constexpr int kTmemCols = 512;                        // [S0 S1] [O0] [O1]
   static constexpr int kOff_Q = 0;
   static constexpr int kOff_KV = kOff_Q + kTilesQ * kQBytes;
   static constexpr int kOff_Bar = kOff_KV + kStages * kStageBytes;
-  static constexpr int kBars = 2 * kStages + kTilesQ * 6 + 1;
+  static constexpr int kBars = 2 * kStages + kTilesQ * 5 + 1;
   static constexpr int kSmem = 1024 + kOff_Bar + kBars * 8 + 32;
   static_assert(kSmem <= 232448, "shared memory per CTA");
+  static_assert(kTilesQ * kBlockKeys + kTilesQ * D <= kTmemCols, "TMEM columns");
 };
 
 __device__ __forceinline__ int find_cta_row(const PrefillParams &p, int b) {
@@ -124,13 +128,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::kOff_Bar);
   uint64_t *kv_full = bars;                       // [kStages] TMA -> MMA and softmax
   uint64_t *kv_empty = kv_full + kStages;         // [kStages] every MMA of the stage done
-  // Per query tile and S buffer b (tile j uses b = j & 1); each barrier completes one
-  // phase per use of its buffer, and a buffer is reused only after its previous PV is
-  // done, so no waiter can fall two phases behind.
-  uint64_t *s_full = kv_empty + kStages;          // [tile][b] QK done -> softmax
-  uint64_t *p_full = s_full + 2 * kTilesQ;        // [tile][b] softmax wrote P -> MMA
-  uint64_t *pv_done = p_full + 2 * kTilesQ;       // [tile][b] PV done -> MMA, softmax
-  uint64_t *drain = pv_done + 2 * kTilesQ;        // [1] every MMA done (teardown)
+  // Per query tile, one phase per K/V block.  The S buffer of a block is overwritten by
+  // the next block's QK only after this block's PV is done, so no waiter can fall two
+  // phases behind.
+  uint64_t *s_full = kv_empty + kStages;          // [tile] QK done -> softmax
+  uint64_t *p_full = s_full + kTilesQ;            // [tile][half] softmax wrote P -> MMA
+  uint64_t *pv0_done = p_full + 2 * kTilesQ;      // [tile] PV of half 0 done -> softmax
+  uint64_t *pv_done = pv0_done + kTilesQ;         // [tile] PV done -> MMA, softmax
+  uint64_t *drain = pv_done + kTilesQ;            // [1] every MMA done (teardown)
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + Cfg::kBars);
   volatile int *fail = reinterpret_cast<volatile int *>(tmem_slot + 1);
   volatile int *issued = fail + 1;
@@ -149,7 +154,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int len_a = p.sliding ? min(lens, p.ring_R) : lens + t_max + 1;
   const int len_b = p.sliding ? t_max + 1 : 0;
   const int tiles_a = (len_a + kKeys - 1) / kKeys;
-  const int n_tiles = tiles_a + (len_b + kKeys - 1) / kKeys;
+  const int n_tiles = tiles_a + (len_b + kKeys - 1) / kKeys;  // 64-key tiles
+  const int n_blocks = (n_tiles + 1) / 2;                      // 128-key blocks
   const int64_t base_a = ((int64_t)row.cache_row * p.Hk + g) * p.seg_rows;
   const int64_t base_b = ((int64_t)row.cache_row * p.Hk + g) * kChunk;
 
@@ -159,11 +165,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(&kv_empty[s], 1);
     }
     for (int qt = 0; qt < kTilesQ; ++qt) {
-      for (int b = 0; b < 2; ++b) {
-        ptx::mbar_init(&s_full[2 * qt + b], 1);
-        ptx::mbar_init(&p_full[2 * qt + b], kSoftmaxWarps);
-        ptx::mbar_init(&pv_done[2 * qt + b], 1);
-      }
+      ptx::mbar_init(&s_full[qt], 1);
+      ptx::mbar_init(&p_full[2 * qt], kSoftmaxWarps);
+      ptx::mbar_init(&p_full[2 * qt + 1], kSoftmaxWarps);
+      ptx::mbar_init(&pv0_done[qt], 1);
+      ptx::mbar_init(&pv_done[qt], 1);
     }
     ptx::mbar_init(drain, 1);
     *fail = 0;
@@ -216,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       ptx::prefetch_tmap(&p.tmap_k);
       ptx::prefetch_tmap(&p.tmap_v);
-      for (int it = 0; it < n_tiles && !*fail; ++it) {
+      for (int it = 0; it < n_blocks && !*fail; ++it) {
         const int s = it % kStages;
         if (it >= kStages &&
             !ptx::mbar_wait(&kv_empty[s], ((it / kStages) - 1) & 1, kWaitLimit)) {
@@ -225,17 +231,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         uint8_t *kt = kv + s * Cfg::kStageBytes;
-        uint8_t *vtile = kt + Cfg::kKVTile;
-        const bool in_a = it < tiles_a;
-        const CUtensorMap *mk = in_a ? &p.tmap_k : &p.tmap_sk;
-        const CUtensorMap *mv = in_a ? &p.tmap_v : &p.tmap_sv;
-        const int y = static_cast<int>(in_a ? base_a + (int64_t)it * kKeys
-                                            : base_b + (int64_t)(it - tiles_a) * kKeys);
-        ptx::mbar_arrive_expect_tx(&kv_full[s], Cfg::kStageBytes);
+        uint8_t *vt = kt + Cfg::kKVBlock;
+        const int halves = min(2, n_tiles - 2 * it);  // a last block may hold one tile
+        ptx::mbar_arrive_expect_tx(&kv_full[s], halves * 2 * Cfg::kPanels * Cfg::kHalfBytes);
+        for (int h = 0; h < halves; ++h) {
+          const int j = 2 * it + h;
+          const bool in_a = j < tiles_a;
+          const CUtensorMap *mk = in_a ? &p.tmap_k : &p.tmap_sk;
+          const CUtensorMap *mv = in_a ? &p.tmap_v : &p.tmap_sv;
+          const int y = static_cast<int>(in_a ? base_a + (int64_t)j * kKeys
+                                              : base_b + (int64_t)(j - tiles_a) * kKeys);
 #pragma unroll
-        for (int pn = 0; pn < Cfg::kPanels; ++pn) {
-          ptx::tma_load_2d(kt + pn * kKeys * 128, mk, pn * 64, y, &kv_full[s]);
-          ptx::tma_load_2d(vtile + pn * kKeys * 128, mv, pn * 64, y, &kv_full[s]);
+          for (int pn = 0; pn < Cfg::kPanels; ++pn) {
+            const int off = pn * Cfg::kPanelBytes + h * Cfg::kHalfBytes;
+            ptx::tma_load_2d(kt + off, mk, pn * 64, y, &kv_full[s]);
+            ptx::tma_load_2d(vt + off, mv, pn * 64, y, &kv_full[s]);
+          }
         }
         *issued = it + 1;
       }
@@ -243,63 +254,68 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t kIdQK = tc::idesc_bf16_f32(kRows, kKeys);
+      constexpr uint32_t kIdQK = tc::idesc_bf16_f32(kRows, kBlockKeys);
       constexpr uint32_t kIdPV = tc::idesc_bf16_f32(kRows, D, /*b_mn_major=*/true);
-      // Fixed issue order.  Prologue QK(0, q0), QK(0, q1), QK(1, q0); then per K/V tile r:
-      //   PV(r, q0), QK(r + 1, q1), PV(r, q1), QK(r + 2, q0).
-      // QK(j, q) reuses the S buffer of PV(j - 2, q), which was issued three groups
-      // earlier, so the tensor pipe is not left waiting on its own work; each PV waits
-      // for its softmax, which runs while the three groups before it execute.  PV(r, q1)
-      // follows PV(r, q0), i.e. query tile 0's P of tile r, which is published after its
-      // softmax warps zeroed the V rows past a segment's end.
-      auto issue_qk = [&](int qt, int j) -> bool {
-        if (qt >= n_qt || j >= n_tiles) return true;
-        if (!ptx::mbar_wait(&kv_full[j % kStages], (j / kStages) & 1, kWaitLimit)) return false;
-        if (j >= 2 && !ptx::mbar_wait(&pv_done[2 * qt + (j & 1)], ((j - 2) >> 1) & 1, kWaitLimit))
+      // QK(b, q): S of block b into the S buffer of query tile q.  It waits for the K/V
+      // stage (query tile 1 follows tile 0's QK of the same block, which already did) and
+      // for PV(b - 1, q) to have read P out of that buffer.  A block with one tile still
+      // multiplies all 128 rows of its K stage; the softmax masks the absent half.
+      auto issue_qk = [&](int qt, int b) -> bool {
+        if (qt >= n_qt || b >= n_blocks) return true;
+        if (qt == 0 && !ptx::mbar_wait(&kv_full[b % kStages], (b / kStages) & 1, kWaitLimit))
           return false;
+        if (b >= 1 && !ptx::mbar_wait(&pv_done[qt], (b - 1) & 1, kWaitLimit)) return false;
         tc::fence_after();
-        const uint32_t k_addr = ptx::smem_u32(kv + (j % kStages) * Cfg::kStageBytes);
+        const uint32_t k_addr = ptx::smem_u32(kv + (b % kStages) * Cfg::kStageBytes);
         const uint32_t q_addr = ptx::smem_u32(qsm + qt * Cfg::kQBytes);
-        const uint32_t tS = tmem + (2 * qt + (j & 1)) * kKeys;
+        const uint32_t tS = tmem + qt * kBlockKeys;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off_q = (kk / 4) * (kRows * 128) + 32 * (kk % 4);
-          const uint32_t off_k = (kk / 4) * (kKeys * 128) + 32 * (kk % 4);
+          const uint32_t off_k = (kk / 4) * Cfg::kPanelBytes + 32 * (kk % 4);
           tc::mma(tS, tc::desc_sw128(q_addr + off_q), tc::desc_sw128(k_addr + off_k), kIdQK,
                   kk > 0);
         }
-        tc::commit(&s_full[2 * qt + (j & 1)]);
+        tc::commit(&s_full[qt]);
         return true;
       };
-      auto issue_pv = [&](int qt, int j) -> bool {
+      // PV(b, q): O += P V over the block's tiles.  B = V as stored by TMA: rows = keys
+      // (K), 64-dim panels (MN) kPanelBytes apart; A = P of tile h in S-buffer columns
+      // 64h + [0, 32) (high part) and 64h + [32, 64) (low part), 16 keys = 8 columns.
+      // The softmax publishes P per tile, so PV of tile 0 runs while it computes tile 1.
+      auto issue_pv = [&](int qt, int b) -> bool {
         if (qt >= n_qt) return true;
-        if (!ptx::mbar_wait(&p_full[2 * qt + (j & 1)], (j >> 1) & 1, kWaitLimit)) return false;
-        tc::fence_after();
-        // B = V as stored by TMA: rows = keys (K), 64-dim panels (MN) kKeys*128 apart;
-        // A = P in the S buffer: high part in columns 0-31, low part in 32-63, one
-        // 16-key step = 8 columns.
         const uint32_t v_addr =
-            ptx::smem_u32(kv + (j % kStages) * Cfg::kStageBytes + Cfg::kKVTile);
-        const uint32_t tP = tmem + (2 * qt + (j & 1)) * kKeys;
-        const uint32_t tO = tmem + 4 * kKeys + qt * D;
+            ptx::smem_u32(kv + (b % kStages) * Cfg::kStageBytes + Cfg::kKVBlock);
+        const uint32_t tP = tmem + qt * kBlockKeys;
+        const uint32_t tO = tmem + kTilesQ * kBlockKeys + qt * D;
+        const int halves = min(2, n_tiles - 2 * b);
+        for (int h = 0; h < halves; ++h) {
+          if (!ptx::mbar_wait(&p_full[2 * qt + h], b & 1, kWaitLimit)) return false;
+          tc::fence_after();
 #pragma unroll
-        for (int ks = 0; ks < kKeys / 16; ++ks) {
-          const uint64_t bd = tc::desc_sw128_mn(v_addr + ks * 16 * 128, kKeys * 128, 1024);
-          tc::mma_ts(tO, tP + 8 * ks, bd, kIdPV, j > 0 || ks > 0);
-          tc::mma_ts(tO, tP + kKeys / 2 + 8 * ks, bd, kIdPV, true);
+          for (int ks = 0; ks < kKeys / 16; ++ks) {
+            const uint64_t bd = tc::desc_sw128_mn(v_addr + h * Cfg::kHalfBytes + ks * 16 * 128,
+                                                  Cfg::kPanelBytes, 1024);
+            tc::mma_ts(tO, tP + kKeys * h + 8 * ks, bd, kIdPV, b > 0 || h > 0 || ks > 0);
+            tc::mma_ts(tO, tP + kKeys * h + kKeys / 2 + 8 * ks, bd, kIdPV, true);
+          }
+          if (h == 0) tc::commit(&pv0_done[qt]);
         }
-        tc::commit(&pv_done[2 * qt + (j & 1)]);
+        tc::commit(&pv_done[qt]);
         return true;
       };
-      bool ok = issue_qk(0, 0) && issue_qk(1, 0) && issue_qk(0, 1);
-      for (int r = 0; ok && r < n_tiles; ++r) {
+      // PV(b, q1) follows PV(b, q0), i.e. query tile 0's P of block b, which is published
+      // after its softmax warps zeroed the V rows past a segment's end.
+      bool ok = issue_qk(0, 0) && issue_qk(1, 0);
+      for (int b = 0; ok && b < n_blocks; ++b) {
         if (*fail) {
           ok = false;
           break;
         }
-        ok = issue_pv(0, r) && issue_qk(1, r + 1) && issue_pv(1, r);
-        if (ok) tc::commit(&kv_empty[r % kStages]);  // every PV of the stage issued
-        ok = ok && issue_qk(0, r + 2);
+        ok = issue_pv(0, b) && issue_qk(0, b + 1) && issue_pv(1, b);
+        if (ok) tc::commit(&kv_empty[b % kStages]);  // every PV of the stage issued
+        ok = ok && issue_qk(1, b + 1);
       }
       if (!ok) {
         atomicExch(p.err, 1);
@@ -317,54 +333,92 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool qvalid = rho < n_rho;
     const int qpos = lens + (qvalid ? rho / p.rep : 0);
     const uint32_t lane_off = (uint32_t)(32 * (warp % 4)) << 16;
-    const uint32_t tO = tmem + 4 * kKeys + qt * D + lane_off;
-    float m_used = -INFINITY, l_run = 0.f;
-    int rg[4];  // visible key-index ranges [rg0, rg1] and [rg2, rg3] of the current segment
-    bool ok = true;
-    for (int j = 0; j < n_tiles && ok; ++j) {
-      const int sb = j & 1;
-      // warp-uniform decisions: tcgen05.ld / st are warp-collective
-      const bool good = !*fail && ptx::mbar_wait(&s_full[2 * qt + sb], (j >> 1) & 1, kWaitLimit);
-      if (!__all_sync(0xffffffffu, good)) {
-        ok = false;
-        break;
-      }
-      tc::fence_after();
-      float sv[kKeys];
-      const uint32_t tS = tmem + (2 * qt + sb) * kKeys + lane_off;
+    const uint32_t tO = tmem + kTilesQ * kBlockKeys + qt * D + lane_off;
+    const uint32_t tS = tmem + qt * kBlockKeys + lane_off;
+    float m_used = -INFINITY;
+    // visible key-index ranges of this row in the two segments
+    int rga[4], rgb[4];
+    row_ranges(true, qvalid, qpos, lens, p, rga);
+    row_ranges(false, qvalid, qpos, lens, p, rgb);
+    // Mask and scale (log2 units) of 64-key tile j: returns its key base within the
+    // segment and the two ranges, or all_vis when the whole tile is visible.
+    struct TileMask {
+      int kb, r0, r1, r2, r3;
+      bool all_vis;
+    };
+    auto tile_mask = [&](int j) {
+      TileMask m;
+      const bool in_a = j < tiles_a;
+      m.kb = (in_a ? j : j - tiles_a) * kKeys;
+      m.r0 = in_a ? rga[0] : rgb[0];
+      m.r1 = in_a ? rga[1] : rgb[1];
+      m.r2 = in_a ? rga[2] : rgb[2];
+      m.r3 = in_a ? rga[3] : rgb[3];
+      m.all_vis = (m.kb >= m.r0 && m.kb + kKeys - 1 <= m.r1) ||
+                  (m.kb >= m.r2 && m.kb + kKeys - 1 <= m.r3);
+      return m;
+    };
+    // (bitwise tests: no per-element branches)
+    const float scale = p.scale_log2;
+    auto masked = [&](const TileMask &m, int i, float x) {
+      const int kidx = m.kb + i;
+      const bool vis = ((kidx >= m.r0) & (kidx <= m.r1)) | ((kidx >= m.r2) & (kidx <= m.r3));
+      return vis ? x * scale : -INFINITY;
+    };
+    // S of tile h of the block (64 columns) into v, masked and scaled; returns its max.
+    auto load_tile = [&](int j, int h, float (&v)[kKeys]) {
+      const TileMask m = tile_mask(j);
 #pragma unroll
       for (int c = 0; c < kKeys / 16; ++c) {
         float t16[16];
-        tc::ld16(tS + 16 * c, t16);
+        tc::ld16(tS + kKeys * h + 16 * c, t16);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) sv[16 * c + i] = t16[i];
+        for (int i = 0; i < 16; ++i) v[16 * c + i] = t16[i];
       }
       tc::wait_ld();
-
-      // mask and scale (log2 units): the visible keys of a segment are at most two
-      // index ranges per row (computed when the segment starts)
-      const bool in_a = j < tiles_a;
-      const int kb = (in_a ? j : j - tiles_a) * kKeys;
-      const int seg_len = in_a ? len_a : len_b;
-      if (j == 0 || j == tiles_a) row_ranges(in_a, qvalid, qpos, lens, p, rg);
       float mt = -INFINITY;
-      const bool all_vis = (kb >= rg[0] && kb + kKeys - 1 <= rg[1]) ||
-                           (kb >= rg[2] && kb + kKeys - 1 <= rg[3]);
-      if (all_vis) {
+      if (m.all_vis) {
 #pragma unroll
         for (int i = 0; i < kKeys; ++i) {
-          sv[i] *= p.scale_log2;
-          mt = fmaxf(mt, sv[i]);
+          v[i] *= scale;
+          mt = fmaxf(mt, v[i]);
         }
       } else {
 #pragma unroll
         for (int i = 0; i < kKeys; ++i) {
-          const int kidx = kb + i;
-          const bool vis = (kidx >= rg[0] && kidx <= rg[1]) || (kidx >= rg[2] && kidx <= rg[3]);
-          sv[i] = vis ? sv[i] * p.scale_log2 : -INFINITY;
-          mt = fmaxf(mt, sv[i]);
+          v[i] = masked(m, i, v[i]);
+          mt = fmaxf(mt, v[i]);
         }
       }
+      return mt;
+    };
+    // P = 2^(s - m) of tile h as bf16 high + low parts over its S columns: keys 2i, 2i+1
+    // of the high part in column 64h + i, of the low part in column 64h + 32 + i.  The
+    // row sum is kept in two packed lanes.
+    uint64_t l2 = ptx::f2_pack(0.f, 0.f);
+    auto store_p = [&](int h, const float (&v)[kKeys]) {
+      const float base = m_used == -INFINITY ? 0.f : m_used;
+      const uint64_t nb = ptx::f2_pack(base, base);
+#pragma unroll
+      for (int c = 0; c < kKeys / 32; ++c) {
+        uint32_t hv[16], lv[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          float x0, x1;
+          ptx::f2_unpack(ptx::f2_sub(ptx::f2_pack(v[32 * c + 2 * i], v[32 * c + 2 * i + 1]), nb),
+                         x0, x1);
+          const uint64_t e = ptx::f2_pack(fast_exp2(x0), fast_exp2(x1));
+          l2 = ptx::f2_add(l2, e);
+          ptx::split_bf16x2(e, hv[i], lv[i]);
+        }
+        tc::st16(tS + kKeys * h + 16 * c, hv);
+        tc::st16(tS + kKeys * h + kKeys / 2 + 16 * c, lv);
+      }
+    };
+    // Lazy rescale to the tile maximum mt (log2 units): O and l are multiplied by
+    // 2^(m_used - mt) only when mt exceeds m_used by more than 2^8.  `stable` waits until
+    // every PV issued so far for this query tile has finished writing O.
+    auto rescale_to = [&](float mt, auto stable) -> bool {
       float alpha = 1.f;
       bool rescale = false;
       if (m_used == -INFINITY) {
@@ -375,13 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         rescale = true;
       }
       if (__any_sync(0xffffffffu, rescale)) {
-        // O must be stable: PV(j-1) of this tile is done (PV(j) waits for this P).
-        const bool prev = j < 1 || ptx::mbar_wait(&pv_done[2 * qt + ((j - 1) & 1)],
-                                                  ((j - 1) >> 1) & 1, kWaitLimit);
-        if (!__all_sync(0xffffffffu, prev)) {
-          ok = false;
-          break;
-        }
+        if (!__all_sync(0xffffffffu, stable())) return false;
         tc::fence_after();
 #pragma unroll
         for (int c = 0; c < D / 16; ++c) {
@@ -393,53 +441,87 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::st16(tO + 16 * c, o16);
         }
         tc::wait_st();
+        l2 = ptx::f2_mul(l2, ptx::f2_pack(alpha, alpha));
       }
-      l_run *= alpha;
-      if (qt == 0 && seg_len - kb < kKeys) {
-        // Keys past the segment may hold anything: zero their V rows so that 0 * V
-        // stays 0 in the PV product (every PV of this tile is issued after query tile
-        // 0 publishes its P).  The stage cannot be refilled before that either.
-        if (!__all_sync(0xffffffffu, ptx::mbar_wait(&kv_full[j % kStages], (j / kStages) & 1,
-                                                    kWaitLimit))) {
+      return true;
+    };
+    // Keys past a segment's end may hold anything: query tile 0 zeroes their V rows in
+    // tile h of block b so that 0 * V stays 0 in the PV product (every PV of the block's
+    // tile h is issued after query tile 0 publishes that tile's P; the stage cannot be
+    // refilled before that either).  Returns -1 on a timeout, 1 if rows were zeroed.
+    auto zero_v = [&](int b, int h) -> int {
+      const int j = 2 * b + h;
+      const bool in_a = j < tiles_a;
+      const int kb = (in_a ? j : j - tiles_a) * kKeys;
+      const int seg_len = in_a ? len_a : len_b;
+      if (seg_len - kb >= kKeys) return 0;
+      if (!__all_sync(0xffffffffu,
+                      ptx::mbar_wait(&kv_full[b % kStages], (b / kStages) & 1, kWaitLimit)))
+        return -1;
+      uint8_t *vtile =
+          kv + (b % kStages) * Cfg::kStageBytes + Cfg::kKVBlock + h * Cfg::kHalfBytes;
+      const int first = seg_len - kb > 0 ? seg_len - kb : 0;
+      for (int u = r; u < (kKeys - first) * (D / 8); u += kRows) {
+        const int vr = first + u / (D / 8), ch = u % (D / 8);
+        *reinterpret_cast<uint4 *>(vtile + (ch / 8) * Cfg::kPanelBytes + ptx::swz128(vr, ch % 8)) =
+            make_uint4(0, 0, 0, 0);
+      }
+      return 1;
+    };
+    auto publish = [&](int h, bool zeroed) {
+      tc::wait_st();
+      if (zeroed) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // V -> MMA
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&p_full[2 * qt + h]);
+    };
+    bool ok = true;
+    for (int b = 0; b < n_blocks && ok; ++b) {
+      // warp-uniform decisions: tcgen05.ld / st are warp-collective
+      const bool good = !*fail && ptx::mbar_wait(&s_full[qt], b & 1, kWaitLimit);
+      if (!__all_sync(0xffffffffu, good)) {
+        ok = false;
+        break;
+      }
+      tc::fence_after();
+      const int j0 = 2 * b;
+      float sv[kKeys];
+      // S of this block implies PV(b-1) finished (the QK waited for it): O is final.
+      if (!rescale_to(load_tile(j0, 0, sv), [&] {
+            return b < 1 || ptx::mbar_wait(&pv_done[qt], (b - 1) & 1, kWaitLimit);
+          })) {
+        ok = false;
+        break;
+      }
+      int z = qt == 0 ? zero_v(b, 0) : 0;
+      if (z < 0) {
+        ok = false;
+        break;
+      }
+      store_p(0, sv);
+      publish(0, z > 0);
+      if (j0 + 1 < n_tiles) {
+        // a new maximum in tile 1 rescales O after PV of tile 0 (already issued) is done
+        if (!rescale_to(load_tile(j0 + 1, 1, sv),
+                        [&] { return ptx::mbar_wait(&pv0_done[qt], b & 1, kWaitLimit); })) {
           ok = false;
           break;
         }
-        uint8_t *vtile = kv + (j % kStages) * Cfg::kStageBytes + Cfg::kKVTile;
-        const int first = seg_len - kb > 0 ? seg_len - kb : 0;
-        for (int u = r; u < (kKeys - first) * (D / 8); u += kRows) {
-          const int vr = first + u / (D / 8), ch = u % (D / 8);
-          *reinterpret_cast<uint4 *>(vtile + (ch / 8) * (kKeys * 128) + ptx::swz128(vr, ch % 8)) =
-              make_uint4(0, 0, 0, 0);
+        z = qt == 0 ? zero_v(b, 1) : 0;
+        if (z < 0) {
+          ok = false;
+          break;
         }
+        store_p(1, sv);
+        publish(1, z > 0);
       }
-      const float base = m_used == -INFINITY ? 0.f : m_used;
-      // P = 2^(s - m) as bf16 high + low parts over S in TMEM: keys 2i, 2i+1 of the high
-      // part in column i, of the low part in column 32 + i.
-#pragma unroll
-      for (int c = 0; c < kKeys / 32; ++c) {
-        uint32_t hv[16], lv[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float e0 = fast_exp2(sv[32 * c + 2 * i] - base);
-          const float e1 = fast_exp2(sv[32 * c + 2 * i + 1] - base);
-          l_run += e0 + e1;
-          ptx::split_bf16(e0, e1, hv[i], lv[i]);
-        }
-        tc::st16(tS + 16 * c, hv);
-        tc::st16(tS + kKeys / 2 + 16 * c, lv);
-      }
-      tc::wait_st();
-      if (qt == 0 && seg_len - kb < kKeys)
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // zeroed V -> MMA
-      tc::fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&p_full[2 * qt + sb]);
     }
+    float l0, l1;
+    ptx::f2_unpack(l2, l0, l1);
+    const float l_run = l0 + l1;
     // The last PV's completion implies every earlier MMA of the issuing thread is done.
     const bool last_done =
-        ok && n_tiles > 0 &&
-        ptx::mbar_wait(&pv_done[2 * qt + ((n_tiles - 1) & 1)], ((n_tiles - 1) >> 1) & 1,
-                       kWaitLimit);
+        ok && n_blocks > 0 && ptx::mbar_wait(&pv_done[qt], (n_blocks - 1) & 1, kWaitLimit);
     if (!ok) {
       atomicExch(p.err, 1);
       *fail = 1;

@@ -133,6 +133,45 @@ __device__ __forceinline__ void split_bf16(float x0, float x1, uint32_t &hi, uin
   lo = *reinterpret_cast<uint32_t *>(&l);
 }
 
+// Two fp32 values in one 64-bit register pair (x in the low half) and the packed
+// two-lane fp32 arithmetic of this architecture (each lane rounds like the scalar op).
+__device__ __forceinline__ uint64_t f2_pack(float x, float y) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(x), "f"(y));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float &x, float &y) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(x), "=f"(y) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
+// split_bf16 on a packed pair: hi = bf16 RNE of (x0, x1), lo = bf16 RNE of the residuals.
+__device__ __forceinline__ void split_bf16x2(uint64_t x, uint32_t &hi, uint32_t &lo) {
+  float x0, x1;
+  f2_unpack(x, x0, x1);
+  __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+  hi = *reinterpret_cast<uint32_t *>(&h);
+  const uint64_t hf = f2_pack(__uint_as_float(hi << 16), __uint_as_float(hi & 0xFFFF0000u));
+  float r0, r1;
+  f2_unpack(f2_sub(x, hf), r0, r1);
+  __nv_bfloat162 l = __floats2bfloat162_rn(r0, r1);
+  lo = *reinterpret_cast<uint32_t *>(&l);
+}
+
 // Byte offset of 16-byte chunk `chunk` (0..7) of row `row` inside a tile stored with the
 // TMA 128-byte swizzle (rows of 128 bytes; panel base 1024-byte aligned).
 __device__ __forceinline__ uint32_t swz128(int row, int chunk) {
