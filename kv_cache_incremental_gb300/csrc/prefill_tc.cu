@@ -19,12 +19,12 @@
 //              more than 2^8), write P as bf16 high and low parts back into the TMEM
 //              columns that held S, and finally read O from TMEM and normalise.
 //   warp 8     TMA producer of the K and V blocks (128-byte swizzle).
-//   warp 9     TMEM owner and MMA issuer (one thread).  Per block and query tile:
-//              S = Q K^T (M=128, N=128) into the tile's S buffer, then, once the softmax
-//              wrote P, O += P_hi V + P_lo V (M=128, N=D) with P read from TMEM and V read
-//              in place as an MN-major operand (keys are its K).  Order per block b:
-//              PV(b, q0), QK(b+1, q0), PV(b, q1), QK(b+1, q1); QK(b+1, q) waits for PV(b, q)
-//              to finish reading P from the S buffer it overwrites.
+//   warps 9-10 MMA issuers, one thread per query tile (warp 9 also owns TMEM).  Per
+//              block: S = Q K^T (M=128, N=128) into the tile's S buffer, then, once the
+//              softmax wrote P of each 64-key tile, O += P_hi V + P_lo V (M=128, N=D)
+//              with P read from TMEM and V read in place as an MN-major operand (keys are
+//              its K).  QK(b+1) waits for PV(b) to finish reading P from the S buffer it
+//              overwrites; the two query tiles' chains run independently.
 // Every mbarrier wait is bounded; on a timeout the CTA records the error, lets its
 // own TMA loads and MMAs finish (bounded), frees its TMEM and returns.
 #include "kvinc_internal.h"
@@ -39,7 +39,7 @@ constexpr int kKeys = kTileKeys;  // keys per tile (one TMA box, one softmax hal
 constexpr int kBlockKeys = 2 * kKeys;  // keys per K/V block (MMA N of S, K of PV)
 constexpr int kSoftmaxWarps = 4;  // per query tile
 constexpr int kProducerWarp = kTilesQ * kSoftmaxWarps, kMmaWarp = kProducerWarp + 1;
-constexpr int kThreads = (kMmaWarp + 1) * 32;
+constexpr int kThreads = (kMmaWarp + kTilesQ) * 32;  // one MMA-issuing warp per query tile
 constexpr float kRescaleLog2 = 8.f;  // lazy rescale threshold (log2 units)
 
 template <int D>
@@ -58,7 +58,7 @@ struct TcCfg {
   static constexpr int kOff_Q = 0;
   static constexpr int kOff_KV = kOff_Q + kTilesQ * kQBytes;
   static constexpr int kOff_Bar = kOff_KV + kStages * kStageBytes;
-  static constexpr int kBars = 2 * kStages + kTilesQ * 5 + 1;
+  static constexpr int kBars = 3 * kStages + kTilesQ * 5 + 1;
   static constexpr int kSmem = 1024 + kOff_Bar + kBars * 8 + 32;
   static_assert(kSmem <= 232448, "shared memory per CTA");
   static_assert(kTilesQ * kBlockKeys + kTilesQ * D <= kTmemCols, "TMEM columns");
@@ -135,7 +135,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *p_full = s_full + kTilesQ;            // [tile][half] softmax wrote P -> MMA
   uint64_t *pv0_done = p_full + 2 * kTilesQ;      // [tile] PV of half 0 done -> softmax
   uint64_t *pv_done = pv0_done + kTilesQ;         // [tile] PV done -> MMA, softmax
-  uint64_t *drain = pv_done + kTilesQ;            // [1] every MMA done (teardown)
+  uint64_t *v_ready = pv_done + kTilesQ;          // [stage] tile 0 zeroed V -> MMA of tile 1
+  uint64_t *drain = v_ready + kStages;            // [1] every MMA done (teardown)
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + Cfg::kBars);
   volatile int *fail = reinterpret_cast<volatile int *>(tmem_slot + 1);
   volatile int *issued = fail + 1;
@@ -162,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(&kv_full[s], 1);
-      ptx::mbar_init(&kv_empty[s], 1);
+      ptx::mbar_init(&kv_empty[s], n_qt);  // one commit per query tile's MMA warp
     }
     for (int qt = 0; qt < kTilesQ; ++qt) {
       ptx::mbar_init(&s_full[qt], 1);
@@ -171,7 +172,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(&pv0_done[qt], 1);
       ptx::mbar_init(&pv_done[qt], 1);
     }
-    ptx::mbar_init(drain, 1);
+    for (int s = 0; s < kStages; ++s) ptx::mbar_init(&v_ready[s], kSoftmaxWarps);
+    ptx::mbar_init(drain, n_qt);
     *fail = 0;
     *issued = 0;
     ptx::fence_barrier_init();
@@ -251,24 +253,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         *issued = it + 1;
       }
     }
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+  } else if (warp >= kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuers
+    // One warp per query tile, so each tile's chain QK -> softmax -> PV -> QK runs at its
+    // own pace and the tensor pipe interleaves the two.  A K/V stage is released when
+    // both have committed their PV of it.
+    const int qt = warp - kMmaWarp;
+    if (lane == 0 && qt < n_qt) {
       constexpr uint32_t kIdQK = tc::idesc_bf16_f32(kRows, kBlockKeys);
       constexpr uint32_t kIdPV = tc::idesc_bf16_f32(kRows, D, /*b_mn_major=*/true);
-      // QK(b, q): S of block b into the S buffer of query tile q.  It waits for the K/V
-      // stage (query tile 1 follows tile 0's QK of the same block, which already did) and
-      // for PV(b - 1, q) to have read P out of that buffer.  A block with one tile still
-      // multiplies all 128 rows of its K stage; the softmax masks the absent half.
-      auto issue_qk = [&](int qt, int b) -> bool {
-        if (qt >= n_qt || b >= n_blocks) return true;
-        if (qt == 0 && !ptx::mbar_wait(&kv_full[b % kStages], (b / kStages) & 1, kWaitLimit))
-          return false;
+      const uint32_t q_addr = ptx::smem_u32(qsm + qt * Cfg::kQBytes);
+      const uint32_t tS = tmem + qt * kBlockKeys;
+      const uint32_t tO = tmem + kTilesQ * kBlockKeys + qt * D;
+      // QK(b): S of block b into this tile's S buffer, once the K/V stage has landed and
+      // PV(b - 1) has read P out of that buffer.  A block with one tile still multiplies
+      // all 128 rows of its K stage; the softmax masks the absent half.
+      auto issue_qk = [&](int b) -> bool {
+        if (!ptx::mbar_wait(&kv_full[b % kStages], (b / kStages) & 1, kWaitLimit)) return false;
         if (b >= 1 && !ptx::mbar_wait(&pv_done[qt], (b - 1) & 1, kWaitLimit)) return false;
         tc::fence_after();
         const uint32_t k_addr = ptx::smem_u32(kv + (b % kStages) * Cfg::kStageBytes);
-        const uint32_t q_addr = ptx::smem_u32(qsm + qt * Cfg::kQBytes);
-        const uint32_t tS = tmem + qt * kBlockKeys;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off_q = (kk / 4) * (kRows * 128) + 32 * (kk % 4);
@@ -279,16 +283,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::commit(&s_full[qt]);
         return true;
       };
-      // PV(b, q): O += P V over the block's tiles.  B = V as stored by TMA: rows = keys
-      // (K), 64-dim panels (MN) kPanelBytes apart; A = P of tile h in S-buffer columns
+      // A tile of the block is partial when a segment ends inside it.
+      auto partial = [&](int j) {
+        return j < n_tiles && ((j == tiles_a - 1 && len_a % kKeys != 0) ||
+                               (j == n_tiles - 1 && j >= tiles_a && len_b % kKeys != 0));
+      };
+      // PV(b): O += P V over the block's tiles.  B = V as stored by TMA: rows = keys (K),
+      // 64-dim panels (MN) kPanelBytes apart; A = P of tile h in S-buffer columns
       // 64h + [0, 32) (high part) and 64h + [32, 64) (low part), 16 keys = 8 columns.
       // The softmax publishes P per tile, so PV of tile 0 runs while it computes tile 1.
-      auto issue_pv = [&](int qt, int b) -> bool {
-        if (qt >= n_qt) return true;
+      // Query tile 1 reads V of a partial block only after tile 0's softmax zeroed the
+      // rows past the segment's end (v_ready, one barrier per stage: tile 0 cannot get
+      // kStages blocks ahead of this PV, whose stage it would need, so it cannot lap it).
+      auto issue_pv = [&](int b) -> bool {
+        if (qt == 1 && (partial(2 * b) || partial(2 * b + 1)) &&
+            !ptx::mbar_wait(&v_ready[b % kStages], (b / kStages) & 1, kWaitLimit))
+          return false;
         const uint32_t v_addr =
             ptx::smem_u32(kv + (b % kStages) * Cfg::kStageBytes + Cfg::kKVBlock);
-        const uint32_t tP = tmem + qt * kBlockKeys;
-        const uint32_t tO = tmem + kTilesQ * kBlockKeys + qt * D;
         const int halves = min(2, n_tiles - 2 * b);
         for (int h = 0; h < halves; ++h) {
           if (!ptx::mbar_wait(&p_full[2 * qt + h], b & 1, kWaitLimit)) return false;
@@ -297,31 +309,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int ks = 0; ks < kKeys / 16; ++ks) {
             const uint64_t bd = tc::desc_sw128_mn(v_addr + h * Cfg::kHalfBytes + ks * 16 * 128,
                                                   Cfg::kPanelBytes, 1024);
-            tc::mma_ts(tO, tP + kKeys * h + 8 * ks, bd, kIdPV, b > 0 || h > 0 || ks > 0);
-            tc::mma_ts(tO, tP + kKeys * h + kKeys / 2 + 8 * ks, bd, kIdPV, true);
+            tc::mma_ts(tO, (tS + kKeys * h) + 8 * ks, bd, kIdPV, b > 0 || h > 0 || ks > 0);
+            tc::mma_ts(tO, (tS + kKeys * h) + kKeys / 2 + 8 * ks, bd, kIdPV, true);
           }
           if (h == 0) tc::commit(&pv0_done[qt]);
         }
         tc::commit(&pv_done[qt]);
+        tc::commit(&kv_empty[b % kStages]);  // this tile's MMAs of the stage issued
         return true;
       };
-      // PV(b, q1) follows PV(b, q0), i.e. query tile 0's P of block b, which is published
-      // after its softmax warps zeroed the V rows past a segment's end.
-      bool ok = issue_qk(0, 0) && issue_qk(1, 0);
+      bool ok = issue_qk(0);
       for (int b = 0; ok && b < n_blocks; ++b) {
         if (*fail) {
           ok = false;
           break;
         }
-        ok = issue_pv(0, b) && issue_qk(0, b + 1) && issue_pv(1, b);
-        if (ok) tc::commit(&kv_empty[b % kStages]);  // every PV of the stage issued
-        ok = ok && issue_qk(1, b + 1);
+        ok = issue_pv(b) && (b + 1 >= n_blocks || issue_qk(b + 1));
       }
       if (!ok) {
         atomicExch(p.err, 1);
         *fail = 1;
       }
-      // Every MMA issued has completed before TMEM can be released.
+      // Every MMA issued by either warp has completed before TMEM can be released.
       tc::commit(drain);
       ptx::mbar_wait(drain, 0, kWaitLimit);
     }
@@ -446,9 +455,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       return true;
     };
     // Keys past a segment's end may hold anything: query tile 0 zeroes their V rows in
-    // tile h of block b so that 0 * V stays 0 in the PV product (every PV of the block's
-    // tile h is issued after query tile 0 publishes that tile's P; the stage cannot be
-    // refilled before that either).  Returns -1 on a timeout, 1 if rows were zeroed.
+    // tile h of block b so that 0 * V stays 0 in the PV product (its own PV waits for
+    // its P, query tile 1's PV of the block for v_ready; the stage cannot be refilled
+    // before both PVs are issued).  Returns -1 on a timeout, 1 if rows were zeroed.
     auto zero_v = [&](int b, int h) -> int {
       const int j = 2 * b + h;
       const bool in_a = j < tiles_a;
@@ -468,9 +477,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       return 1;
     };
-    auto publish = [&](int h, bool zeroed) {
+    auto publish = [&](int h) {
       tc::wait_st();
-      if (zeroed) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // V -> MMA
       tc::fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&p_full[2 * qt + h]);
@@ -485,6 +493,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc::fence_after();
       const int j0 = 2 * b;
+      if (qt == 0) {
+        const int z0 = zero_v(b, 0), z1 = j0 + 1 < n_tiles ? zero_v(b, 1) : 0;
+        if (z0 < 0 || z1 < 0) {
+          ok = false;
+          break;
+        }
+        if (z0 > 0 || z1 > 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&v_ready[b % kStages]);
+      }
       float sv[kKeys];
       // S of this block implies PV(b-1) finished (the QK waited for it): O is final.
       if (!rescale_to(load_tile(j0, 0, sv), [&] {
@@ -493,13 +511,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = false;
         break;
       }
-      int z = qt == 0 ? zero_v(b, 0) : 0;
-      if (z < 0) {
-        ok = false;
-        break;
-      }
       store_p(0, sv);
-      publish(0, z > 0);
+      publish(0);
       if (j0 + 1 < n_tiles) {
         // a new maximum in tile 1 rescales O after PV of tile 0 (already issued) is done
         if (!rescale_to(load_tile(j0 + 1, 1, sv),
@@ -507,13 +520,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        z = qt == 0 ? zero_v(b, 1) : 0;
-        if (z < 0) {
-          ok = false;
-          break;
-        }
         store_p(1, sv);
-        publish(1, z > 0);
+        publish(1);
       }
     }
     float l0, l1;
