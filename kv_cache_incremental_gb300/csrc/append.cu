@@ -54,47 +54,63 @@ __global__ void __launch_bounds__(256) append_kernel(const __grid_constant__ App
   const int half = p.D / 2;
   const int chunks = half / 8;  // 8-pair chunks per head
   const int units = kTokBlock * p.Hk * chunks;
-  for (int u = threadIdx.x; u < units; u += blockDim.x) {
-    const int tl = u / (p.Hk * chunks);
-    const int g = (u / chunks) % p.Hk;
-    const int c = u % chunks;
-    const int t = t0 + tl;
-    if (t >= c_avail) continue;  // beyond the caller's tensor: nothing to route
-    const bool real = t < row.n;
-    const int pos = row.lens + t;
-    const int64_t src = (int64_t)row.call_row * p.kv_row_stride + ((int64_t)t * p.Hk + g) * p.D;
-    const uint4 k1 = *reinterpret_cast<const uint4 *>(p.k + src + 8 * c);
-    const uint4 k2 = *reinterpret_cast<const uint4 *>(p.k + src + half + 8 * c);
-    const uint4 v1 = *reinterpret_cast<const uint4 *>(p.v + src + 8 * c);
-    const uint4 v2 = *reinterpret_cast<const uint4 *>(p.v + src + half + 8 * c);
-    uint4 o1 = k1, o2 = k2;  // padding keys are routed unrotated
-    if (real) rope8(k1, k2, p.rope + (int64_t)pos * half + 8 * c, o1, o2);
-
-    __nv_bfloat16 *dk, *dv;
-    int64_t dst;
-    if (row.mode == kDestScratch) {
-      dst = (((int64_t)row.cache_row * p.Hk + g) * kChunk + t) * p.D;
-      dk = p.scr_k;
-      dv = p.scr_v;
-    } else {
-      int slot;
-      if (row.mode == kDestGlobal) slot = real ? pos : p.max_len;
-      else slot = real ? pos % p.ring_R : p.ring_R;
-      dst = (((int64_t)row.cache_row * p.Hk + g) * p.seg_rows + slot) * p.D;
-      dk = p.cache_k;
-      dv = p.cache_v;
+  // Two units per thread and pass, both units' loads issued before either is used.
+  constexpr int kPer = 2;
+  for (int u0 = threadIdx.x; u0 < units; u0 += kPer * blockDim.x) {
+    uint4 in[kPer][4];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int u = u0 + i * blockDim.x;
+      const int t = t0 + u / (p.Hk * chunks);
+      if (u >= units || t >= c_avail) continue;
+      const int g = (u / chunks) % p.Hk, c = u % chunks;
+      const int64_t src =
+          (int64_t)row.call_row * p.kv_row_stride + ((int64_t)t * p.Hk + g) * p.D + 8 * c;
+      in[i][0] = *reinterpret_cast<const uint4 *>(p.k + src);
+      in[i][1] = *reinterpret_cast<const uint4 *>(p.k + src + half);
+      in[i][2] = *reinterpret_cast<const uint4 *>(p.v + src);
+      in[i][3] = *reinterpret_cast<const uint4 *>(p.v + src + half);
     }
-    *reinterpret_cast<uint4 *>(dk + dst + 8 * c) = o1;
-    *reinterpret_cast<uint4 *>(dk + dst + half + 8 * c) = o2;
-    *reinterpret_cast<uint4 *>(dv + dst + 8 * c) = v1;
-    *reinterpret_cast<uint4 *>(dv + dst + half + 8 * c) = v2;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int u = u0 + i * blockDim.x;
+      const int tl = u / (p.Hk * chunks);
+      const int g = (u / chunks) % p.Hk;
+      const int c = u % chunks;
+      const int t = t0 + tl;
+      if (u >= units || t >= c_avail) continue;  // beyond the caller's tensor: nothing to route
+      const bool real = t < row.n;
+      const int pos = row.lens + t;
+      const uint4 k1 = in[i][0], k2 = in[i][1], v1 = in[i][2], v2 = in[i][3];
+      uint4 o1 = k1, o2 = k2;  // padding keys are routed unrotated
+      if (real) rope8(k1, k2, p.rope + (int64_t)pos * half + 8 * c, o1, o2);
+
+      __nv_bfloat16 *dk, *dv;
+      int64_t dst;
+      if (row.mode == kDestScratch) {
+        dst = (((int64_t)row.cache_row * p.Hk + g) * kChunk + t) * p.D;
+        dk = p.scr_k;
+        dv = p.scr_v;
+      } else {
+        int slot;
+        if (row.mode == kDestGlobal) slot = real ? pos : p.max_len;
+        else slot = real ? pos % p.ring_R : p.ring_R;
+        dst = (((int64_t)row.cache_row * p.Hk + g) * p.seg_rows + slot) * p.D;
+        dk = p.cache_k;
+        dv = p.cache_v;
+      }
+      *reinterpret_cast<uint4 *>(dk + dst + 8 * c) = o1;
+      *reinterpret_cast<uint4 *>(dk + dst + half + 8 * c) = o2;
+      *reinterpret_cast<uint4 *>(dv + dst + 8 * c) = v1;
+      *reinterpret_cast<uint4 *>(dv + dst + half + 8 * c) = v2;
+    }
   }
 }
 
 // Copy the kept tokens of a sliding chunk from the chunk scratch into the ring:
 // token t is kept iff t >= n - W (the last min(n, W) real tokens; tiny_agent
 // keep rule, inkling skip rule s0 = max(0, S - win)).
-__global__ void __launch_bounds__(128) commit_kernel(const __grid_constant__ CommitParams p) {
+__global__ void __launch_bounds__(256) commit_kernel(const __grid_constant__ CommitParams p) {
   const int r = blockIdx.x, g = blockIdx.y;
   const int n = p.n[r];
   const int first = n - p.window > 0 ? n - p.window : 0;
@@ -102,14 +118,28 @@ __global__ void __launch_bounds__(128) commit_kernel(const __grid_constant__ Com
   const int units = (n - first) * vec;
   const int64_t srow = ((int64_t)p.cache_row[r] * p.Hk + g) * kChunk;
   const int64_t rrow = ((int64_t)p.cache_row[r] * p.Hk + g) * p.seg_rows;
-  for (int u = threadIdx.x; u < units; u += blockDim.x) {
-    const int t = first + u / vec;
-    const int c = u % vec;
-    const int slot = (p.lens[r] + t) % p.ring_R;
-    const int64_t s = (srow + t) * p.D + 8 * c;
-    const int64_t d = (rrow + slot) * p.D + 8 * c;
-    *reinterpret_cast<uint4 *>(p.ring_k + d) = *reinterpret_cast<const uint4 *>(p.scr_k + s);
-    *reinterpret_cast<uint4 *>(p.ring_v + d) = *reinterpret_cast<const uint4 *>(p.scr_v + s);
+  // Four units per thread and pass, every load issued before the first store.
+  constexpr int kPer = 4;
+  for (int u0 = threadIdx.x; u0 < units; u0 += kPer * blockDim.x) {
+    uint4 kk[kPer], vv[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int u = u0 + i * blockDim.x;
+      if (u >= units) continue;
+      const int64_t s = (srow + first + u / vec) * p.D + 8 * (u % vec);
+      kk[i] = *reinterpret_cast<const uint4 *>(p.scr_k + s);
+      vv[i] = *reinterpret_cast<const uint4 *>(p.scr_v + s);
+    }
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int u = u0 + i * blockDim.x;
+      if (u >= units) continue;
+      const int t = first + u / vec;
+      const int slot = (p.lens[r] + t) % p.ring_R;
+      const int64_t d = (rrow + slot) * p.D + 8 * (u % vec);
+      *reinterpret_cast<uint4 *>(p.ring_k + d) = kk[i];
+      *reinterpret_cast<uint4 *>(p.ring_v + d) = vv[i];
+    }
   }
 }
 
@@ -138,7 +168,7 @@ cudaError_t launch_append(const AppendParams &p, cudaStream_t s) {
 
 cudaError_t launch_commit(const CommitParams &p, cudaStream_t s) {
   if (p.n_rows <= 0) return cudaSuccess;
-  commit_kernel<<<dim3(p.n_rows, p.Hk), 128, 0, s>>>(p);
+  commit_kernel<<<dim3(p.n_rows, p.Hk), 256, 0, s>>>(p);
   return cudaGetLastError();
 }
 
