@@ -162,10 +162,11 @@ __device__ __forceinline__ void attend16(WarpAcc<D, NT> &acc, const uint32_t (&q
   }
 }
 
-// Half-split RoPE of 8 pairs: lo = x1 c - x2 s, hi = x1 s + x2 c in float without
-// contraction, each rounded once to bf16.
-__device__ __forceinline__ void rope8(const uint4 &x1v, const uint4 &x2v, const float2 *cs,
-                                      uint4 &lo, uint4 &hi) {
+// RoPE of 8 half-split pairs (x1[j], x2[j]) at one position, (cos, sin) pairs in
+// registers two per float4: f32 products and sums without contraction, then RNE to bf16
+// (tiny_agent/generate.py `_rope_pos`).
+__device__ __forceinline__ void rope8r(const uint4 &x1v, const uint4 &x2v, const float4 (&cs)[4],
+                                       uint4 &lo, uint4 &hi) {
   const __nv_bfloat16 *x1 = reinterpret_cast<const __nv_bfloat16 *>(&x1v);
   const __nv_bfloat16 *x2 = reinterpret_cast<const __nv_bfloat16 *>(&x2v);
   __nv_bfloat16 *o1 = reinterpret_cast<__nv_bfloat16 *>(&lo);
@@ -173,9 +174,9 @@ __device__ __forceinline__ void rope8(const uint4 &x1v, const uint4 &x2v, const 
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     const float a = __bfloat162float(x1[j]), b = __bfloat162float(x2[j]);
-    const float2 c = cs[j];
-    o1[j] = __float2bfloat16_rn(__fsub_rn(__fmul_rn(a, c.x), __fmul_rn(b, c.y)));
-    o2[j] = __float2bfloat16_rn(__fadd_rn(__fmul_rn(a, c.y), __fmul_rn(b, c.x)));
+    const float cc = (j & 1) ? cs[j / 2].z : cs[j / 2].x, sn = (j & 1) ? cs[j / 2].w : cs[j / 2].y;
+    o1[j] = __float2bfloat16_rn(__fsub_rn(__fmul_rn(a, cc), __fmul_rn(b, sn)));
+    o2[j] = __float2bfloat16_rn(__fadd_rn(__fmul_rn(a, sn), __fmul_rn(b, cc)));
   }
 }
 
@@ -260,35 +261,63 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
   // -------------------------------------------------------------- consumers
   {
     // Rotate the decode query for the group's heads into shared memory
-    // (tiny_agent/generate.py `_rope_pos`; float ops without contraction), 8 pairs
-    // per thread with 16-byte loads.
+    // (tiny_agent/generate.py `_rope_pos`; float ops without contraction), and, in the
+    // split that holds the new key, rotate it and keep it and the value plainly for the
+    // store to the cache and as row 0 of the mini-tiles.  Work units: 8-pair chunks of
+    // the query heads, then of the new key, then 16-byte chunks of the value; every
+    // thread issues all loads of its units (and their cos/sin) before using any, so
+    // the prologue costs one memory round trip.
     const __nv_bfloat16 *q = p.q + (int64_t)row.call_row * p.q_row_stride +
                              (int64_t)g * p.rep * D;
+    const __nv_bfloat16 *k = p.k_new + (int64_t)row.call_row * p.kv_row_stride + (int64_t)g * D;
+    const __nv_bfloat16 *v = p.v_new + (int64_t)row.call_row * p.kv_row_stride + (int64_t)g * D;
     const float2 *cs = p.rope + (int64_t)row.pos * kHalf;
-    constexpr int kVec = kHalf / 8;  // 8-pair groups per head
-    for (int u = threadIdx.x; u < NT * 8 * kVec; u += kConsumerWarps * 32) {
-      const int h = u / kVec, c = u % kVec;
-      uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
-      if (h < p.rep)
-        rope8(*reinterpret_cast<const uint4 *>(q + h * D + 8 * c),
-              *reinterpret_cast<const uint4 *>(q + h * D + kHalf + 8 * c), cs + 8 * c, lo, hi);
-      *reinterpret_cast<uint4 *>(qs + h * D + 8 * c) = lo;
-      *reinterpret_cast<uint4 *>(qs + h * D + kHalf + 8 * c) = hi;
+    constexpr int kVec = kHalf / 8;                 // 8-pair chunks per head
+    constexpr int kQUnits = NT * 8 * kVec;
+    constexpr int kUnits = kQUnits + kVec + D / 8;  // with the new key and value
+    constexpr int kPasses = (kUnits + kConsumerWarps * 32 - 1) / (kConsumerWarps * 32);
+    const int n_units = owner ? kUnits : kQUnits;
+    uint4 x1[kPasses], x2[kPasses];
+    float4 cv[kPasses][4];
+#pragma unroll
+    for (int i = 0; i < kPasses; ++i) {
+      const int u = threadIdx.x + i * kConsumerWarps * 32;
+      x1[i] = x2[i] = make_uint4(0, 0, 0, 0);
+      if (u < kQUnits) {
+        const int h = u / kVec, c = u % kVec;
+        if (h < p.rep) {
+          x1[i] = *reinterpret_cast<const uint4 *>(q + h * D + 8 * c);
+          x2[i] = *reinterpret_cast<const uint4 *>(q + h * D + kHalf + 8 * c);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) cv[i][j] = reinterpret_cast<const float4 *>(cs + 8 * c)[j];
+        }
+      } else if (u < kQUnits + kVec && u < n_units) {
+        const int c = u - kQUnits;
+        x1[i] = *reinterpret_cast<const uint4 *>(k + 8 * c);
+        x2[i] = *reinterpret_cast<const uint4 *>(k + kHalf + 8 * c);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) cv[i][j] = reinterpret_cast<const float4 *>(cs + 8 * c)[j];
+      } else if (u < n_units) {
+        x1[i] = *reinterpret_cast<const uint4 *>(v + 8 * (u - kQUnits - kVec));
+      }
     }
-    if (owner) {
-      // The new key (rotated) and value, kept plainly for the store to the cache,
-      // and as row 0 of the mini-tiles (rows 1..15 zero).
-      const __nv_bfloat16 *k = p.k_new + (int64_t)row.call_row * p.kv_row_stride + (int64_t)g * D;
-      const __nv_bfloat16 *v = p.v_new + (int64_t)row.call_row * p.kv_row_stride + (int64_t)g * D;
-      for (int c = threadIdx.x; c < kVec; c += kConsumerWarps * 32) {
+#pragma unroll
+    for (int i = 0; i < kPasses; ++i) {
+      const int u = threadIdx.x + i * kConsumerWarps * 32;
+      if (u < kQUnits) {
+        const int h = u / kVec, c = u % kVec;
+        uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
+        if (h < p.rep) rope8r(x1[i], x2[i], cv[i], lo, hi);
+        *reinterpret_cast<uint4 *>(qs + h * D + 8 * c) = lo;
+        *reinterpret_cast<uint4 *>(qs + h * D + kHalf + 8 * c) = hi;
+      } else if (u < kQUnits + kVec && u < n_units) {
+        const int c = u - kQUnits;
         uint4 lo, hi;
-        rope8(*reinterpret_cast<const uint4 *>(k + 8 * c),
-              *reinterpret_cast<const uint4 *>(k + kHalf + 8 * c), cs + 8 * c, lo, hi);
+        rope8r(x1[i], x2[i], cv[i], lo, hi);
         *reinterpret_cast<uint4 *>(knew + 8 * c) = lo;
         *reinterpret_cast<uint4 *>(knew + kHalf + 8 * c) = hi;
-        *reinterpret_cast<uint4 *>(vnew + 8 * c) = *reinterpret_cast<const uint4 *>(v + 8 * c);
-        *reinterpret_cast<uint4 *>(vnew + kHalf + 8 * c) =
-            *reinterpret_cast<const uint4 *>(v + kHalf + 8 * c);
+      } else if (u < n_units) {
+        *reinterpret_cast<uint4 *>(vnew + 8 * (u - kQUnits - kVec)) = x1[i];
       }
     }
     consumer_sync();
@@ -429,25 +458,50 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
 
   const bool single = row.n_splits == 1;
   const int64_t part = (int64_t)row.part0 + split;
-  for (int u = threadIdx.x; u < p.rep * D; u += kConsumerWarps * 32) {
-    const int h = u / D, d = u % D;
+  // Per head: the warps' merge weights 2^(m_w - m) (divided by l for a finished output)
+  // and this split's (m, l); then 8 consecutive dims per thread, vectorised.
+  float *wsm = ow + kConsumerWarps * kH * D;  // [warp][kH]
+  if (threadIdx.x < p.rep) {
+    const int h = threadIdx.x;
     float m = -INFINITY;
 #pragma unroll
     for (int w = 0; w < kConsumerWarps; ++w) m = fmaxf(m, mw[w * kH + h]);
-    float l = 0.f, a = 0.f;
+    float f[kConsumerWarps], l = 0.f;
 #pragma unroll
     for (int w = 0; w < kConsumerWarps; ++w) {
-      const float f = exp2f(mw[w * kH + h] - m);  // warps without keys: exp2(-inf) = 0
-      l += f * lw[w * kH + h];
-      a += f * ow[((int64_t)w * kH + h) * D + d];
+      f[w] = exp2f(mw[w * kH + h] - m);  // warps without keys: exp2(-inf) = 0
+      l += f[w] * lw[w * kH + h];
+    }
+    const float sc = single ? 1.f / l : 1.f;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) wsm[w * kH + h] = f[w] * sc;
+    if (!single) p.part_ml[part * p.Hq + g * p.rep + h] = make_float2(m, l);
+  }
+  consumer_sync();
+  for (int u = threadIdx.x; u < p.rep * (D / 8); u += kConsumerWarps * 32) {
+    const int h = u / (D / 8), d = 8 * (u % (D / 8));
+    float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) {
+      const float f = wsm[w * kH + h];
+      const float4 o0 = *reinterpret_cast<const float4 *>(ow + ((int64_t)w * kH + h) * D + d);
+      const float4 o1 = *reinterpret_cast<const float4 *>(ow + ((int64_t)w * kH + h) * D + d + 4);
+      a[0] += f * o0.x; a[1] += f * o0.y; a[2] += f * o0.z; a[3] += f * o0.w;
+      a[4] += f * o1.x; a[5] += f * o1.y; a[6] += f * o1.z; a[7] += f * o1.w;
     }
     const int hq = g * p.rep + h;
     if (single) {
-      p.out[(int64_t)row.call_row * p.out_row_stride + (int64_t)hq * D + d] =
-          __float2bfloat16_rn(a / l);
+      uint4 w8;
+      w8.x = ptx::pack_bf16(a[0], a[1]);
+      w8.y = ptx::pack_bf16(a[2], a[3]);
+      w8.z = ptx::pack_bf16(a[4], a[5]);
+      w8.w = ptx::pack_bf16(a[6], a[7]);
+      *reinterpret_cast<uint4 *>(p.out + (int64_t)row.call_row * p.out_row_stride +
+                                 (int64_t)hq * D + d) = w8;
     } else {
-      p.part_o[(part * p.Hq + hq) * D + d] = a;
-      if (d == 0) p.part_ml[part * p.Hq + hq] = make_float2(m, l);
+      float *dst = p.part_o + (part * p.Hq + hq) * D + d;
+      *reinterpret_cast<float4 *>(dst) = make_float4(a[0], a[1], a[2], a[3]);
+      *reinterpret_cast<float4 *>(dst + 4) = make_float4(a[4], a[5], a[6], a[7]);
     }
   }
   if (single) return;
