@@ -418,9 +418,9 @@ def run_ours(args):
     # independently filled caches of that length (keeps the length distribution).
     per_round = min(K, cfg["per_round"])
     rounds = (K + per_round - 1) // per_round
-    # warm-up + timed, the same steps again with per-launch events (kernel durations), and
-    # again end to end
-    reserve = 3 * (Wm + per_round)
+    # warm-up + timed, the same steps again with per-launch events (kernel durations), as
+    # decode-step graph replays, and end to end
+    reserve = 4 * (Wm + per_round)
     stream = torch.cuda.current_stream()
     dev = torch.device("cuda", local_rank)
 
@@ -522,13 +522,44 @@ def run_ours(args):
     launches = sum(p["launches"] for p in prof.values())
     del inputs
 
+    # ---- the same steps as decode-step graph replays (kv_step_graph: one graph launch per
+    # step re-planned from the host lengths), each step pointed at its own inputs
+    graph_bytes, inputs, graphs = 0.0, [], []
+    outs_l = [torch.empty((B, 1, Hq, D), dtype=torch.bfloat16, device=dev)
+              for _ in range(n_layers)]
+    for r in range(rounds):
+        lens_g = lens0[r] + (Wm if r == 0 else 0) + 2 * steps_in_round[r]
+        qs, ks, vs = make_inputs(cfg, lens_g, steps_in_round[r], caches[r][1] + 2, dev, stream)
+        inputs.append((qs, ks, vs))
+        g = caches[r][0].step_graph([qs[0, l] for l in range(n_layers)],
+                                    [ks[0, l] for l in range(n_layers)],
+                                    [vs[0, l] for l in range(n_layers)], outs_l)
+        bufs = [g.buffers([qs[s, l] for l in range(n_layers)], [ks[s, l] for l in range(n_layers)],
+                          [vs[s, l] for l in range(n_layers)], outs_l)
+                for s in range(steps_in_round[r])]
+        graphs.append((g, bufs))
+        graph_bytes += sum(kv_bytes_per_step(cfg, lens_g + s) for s in range(steps_in_round[r]))
+    torch.cuda.synchronize()
+    barrier()
+    e0.record(stream)
+    for g, bufs in graphs:
+        for b in bufs:
+            g.launch(stream, buffers=b)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    ms_graph = e0.elapsed_time(e1)
+    for g, _ in graphs:
+        g.close()
+    del inputs, graphs
+
     # ---- end to end through the host-buffer entry point (pinned host memory)
     e_bytes, ms_e2e = 0.0, 0.0
     hout = torch.empty((B, 1, Hq, D), dtype=torch.bfloat16).pin_memory()
     host_inputs = []
     for r in range(rounds):
         first = Wm if r == 0 else 0
-        lens_e = lens0[r] + first + 2 * steps_in_round[r]  # after the timed and event passes
+        lens_e = lens0[r] + first + 3 * steps_in_round[r]  # after the timed, event, graph passes
         n = steps_in_round[r] + (Wm if r == 0 else 0)
         g = make_inputs(cfg, lens_e, n, caches[r][1], dev, stream)
         host_inputs.append(tuple(x.cpu().pin_memory() for x in g))
@@ -559,8 +590,8 @@ def run_ours(args):
 
     # ---- max over ranks
     if world > 1:
-        (ms, ms_e2e), (alg_bytes, e_bytes) = reduce_over_ranks([ms, ms_e2e],
-                                                               [alg_bytes, e_bytes], dev)
+        (ms, ms_e2e, ms_graph), (alg_bytes, e_bytes, graph_bytes) = reduce_over_ranks(
+            [ms, ms_e2e, ms_graph], [alg_bytes, e_bytes, graph_bytes], dev)
     if rank != 0:
         return
     value = alg_bytes / (ms / 1e3) / 1e9
@@ -600,6 +631,10 @@ def run_ours(args):
                 "tokens_per_s": world * B * K / (ms_e2e / 1e3),
                 "h2d_bytes_per_step": n_layers * B * (Hq + 2 * Hk) * D * 2,
                 "d2h_bytes_per_step": n_layers * B * Hq * D * 2},
+        "graph": {"value": graph_bytes / (ms_graph / 1e3) / 1e9, "unit": "GB/s",
+                  "ms_per_step": ms_graph / K,
+                  "api": "kv_step_graph_launch: one CUDA-graph replay per step (all layers "
+                         "and the advance), inputs already on the device"},
         "gpu_launches": launches,
         "kernels": {k: {"launches": p["launches"], "ms": p["ms"]} for k, p in prof.items()},
         "clocks": clk,

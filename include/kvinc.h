@@ -191,7 +191,9 @@ int kv_device_error(kv_cache *c, int32_t *code_out);
  * event-timed milliseconds (it SYNCHRONISES the device) and the algorithmic
  * bytes the host counted for those launches; kv_profile_enable(c, 0) or a read
  * with reset=1 clears the record.  Kinds: KV_KERNEL_APPEND, KV_KERNEL_DECODE,
- * KV_KERNEL_COMBINE, KV_KERNEL_PREFILL, KV_KERNEL_COMMIT, KV_KERNEL_STATE.
+ * KV_KERNEL_COMBINE, KV_KERNEL_PREFILL, KV_KERNEL_COMMIT, KV_KERNEL_STATE, and
+ * KV_KERNEL_STEP: one replay of a decode-step graph (kv_step_graph_launch), all
+ * its layers' decode kernels and the state update, with their algorithmic bytes.
  */
 enum kv_kernel_kind {
     KV_KERNEL_APPEND = 0,
@@ -200,11 +202,58 @@ enum kv_kernel_kind {
     KV_KERNEL_PREFILL = 3,
     KV_KERNEL_COMMIT = 4,
     KV_KERNEL_STATE = 5,
-    KV_KERNEL_NKINDS = 6
+    KV_KERNEL_STEP = 6,
+    KV_KERNEL_NKINDS = 7
 };
 int kv_profile_enable(kv_cache *c, int enable);
 int kv_profile_read(kv_cache *c, int kind, int reset, int64_t *launches, double *total_ms,
                     double *alg_bytes, double *alg_flops);
+
+/*
+ * Static-shape decode step as a CUDA graph.  One decode step of a fixed set of rows
+ * -- for every layer, kv_append with one new token per row, then kv_advance -- is
+ * built once into a graph (one decode kernel node per layer, then the ring-state
+ * node when the cache has sliding layers) and replayed per step.  The pages keep
+ * the step's shapes fixed so that a captured graph can be replayed, and advance
+ * the host's lengths after each replay ("tinyllm/kv_cache.py" (tiny-llm):
+ * end_step / advance_host; "Lab 07 -- KV cache and sampling", Going further:
+ * static shapes for CUDA graphs).  Here positions live in each kernel's
+ * parameters, so every launch re-plans the step from the host lengths, updates the
+ * nodes' parameters and grid sizes in the instantiated graph, replays it on the
+ * stream, and then advances the host lengths: the result is bit-identical to the
+ * kv_append / kv_advance sequence, with one graph launch instead of one launch per
+ * layer.
+ *
+ *  q, k, v, out  host arrays of n_layers device pointers: layer l's bf16 query
+ *                [Bs][1][Hq][D], key and value [Bs][1][Hk][D] and output
+ *                [Bs][1][Hq][D] buffers, 16-byte aligned, read and written by the
+ *                launches that follow (the caller writes each step's inputs, in
+ *                stream order, before the launch, or points the graph at new
+ *                buffers with kv_step_graph_set_buffers)
+ *  rows          host int32 [Bs] distinct cache rows, or NULL for 0..Bs-1;
+ *                1 <= Bs <= min(B, 512)
+ *  Hq            must equal the cache's Hq
+ *
+ * kv_step_graph_create plans for the current lengths and enqueues nothing;
+ * KV_ERR_ARG for bad arguments, KV_ERR_CUDA if graph construction fails.
+ * kv_step_graph_launch returns KV_ERR_FULL (and changes no state) if a row is at
+ * max_len, KV_ERR_CUDA if a CUDA call fails; it never synchronises.  Rows of the
+ * cache that are not in `rows` are untouched.  A reset of one of the rows between
+ * launches is allowed (the next launch plans from the new length).
+ * kv_step_graph_set_buffers replaces the four pointer arrays for the following
+ * launches (same rules as at create; KV_ERR_ARG leaves the old ones in place); it
+ * enqueues nothing, since every launch rewrites the nodes' parameters anyway.
+ * kv_step_graph_destroy frees the graph (not the caller's buffers); destroy graphs
+ * before their cache.
+ */
+typedef struct kv_step_graph kv_step_graph;
+int kv_step_graph_create(kv_cache *c, kv_step_graph **out, const void *const *q,
+                         const void *const *k, const void *const *v, void *const *outp, int Hq,
+                         const int32_t *rows, int Bs);
+int kv_step_graph_set_buffers(kv_step_graph *g, const void *const *q, const void *const *k,
+                              const void *const *v, void *const *outp);
+int kv_step_graph_launch(kv_step_graph *g, void *stream);
+void kv_step_graph_destroy(kv_step_graph *g);
 
 /*
  * Decode attention that allocates nothing.  The pages have no counterpart: this

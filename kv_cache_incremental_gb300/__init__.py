@@ -13,11 +13,12 @@ in-tree when absent) and raises if that fails -- there is no CPU fallback.
 from __future__ import annotations
 
 import ctypes
+import weakref
 from typing import Optional, Sequence
 
 from ._lib import (KERNELS, KV_GLOBAL, KV_SLIDING, KVCacheFull, KVError, check, load)
 
-__all__ = ["KVCache", "KVError", "KVCacheFull", "KV_GLOBAL", "KV_SLIDING", "load"]
+__all__ = ["KVCache", "StepGraph", "KVError", "KVCacheFull", "KV_GLOBAL", "KV_SLIDING", "load"]
 
 _clib = load()
 
@@ -61,9 +62,12 @@ class KVCache:
         r = ctypes.c_int()
         _clib.kv_get_config(h, None, None, None, None, None, None, ctypes.byref(r), None)
         self.R = r.value
+        self._graphs = weakref.WeakSet()  # step graphs over this cache, closed before it
 
     # ------------------------------------------------------------------ lifecycle
     def close(self) -> None:
+        for g in list(getattr(self, "_graphs", ())):
+            g.close()
         if getattr(self, "_h", None):
             _clib.kv_cache_destroy(self._h)
             self._h = None
@@ -107,6 +111,12 @@ class KVCache:
                              n, _i32_array(rows), Bs, out.data_ptr(),
                              _stream_ptr(stream, q.device)), "kv_append")
         return out
+
+    def step_graph(self, q, k, v, out, rows=None) -> "StepGraph":
+        """A static-shape decode step (every layer, one token per row, then advance) as a
+        CUDA graph over fixed per-layer buffers q[l], k[l], v[l], out[l] of shape
+        (Bs, 1, heads, D); see StepGraph."""
+        return StepGraph(self, q, k, v, out, rows)
 
     def append_host(self, layer: int, q, k, v, n_new, rows=None, out=None, stream=None):
         """append() for CPU tensors (pinned for asynchronous copies); synchronise the stream
@@ -185,3 +195,81 @@ class KVCache:
         check(_clib.kv_profile_read(self._h, KERNELS[kernel], 1 if reset else 0, ctypes.byref(n),
                                    ctypes.byref(ms), ctypes.byref(by), ctypes.byref(fl)))
         return {"launches": n.value, "ms": ms.value, "bytes": by.value, "flops": fl.value}
+
+
+class StepGraph:
+    """One decode step of a fixed row set, replayed as a CUDA graph (kv_step_graph_*).
+
+    ``launch()`` is equivalent to ``cache.append(l, q[l], k[l], v[l], [1] * Bs, rows,
+    out=out[l])`` for every layer followed by ``cache.advance([1] * Bs, rows)``: write the
+    step's inputs into the buffers given at construction, then launch.  The buffers must
+    stay alive as long as the graph.
+    """
+
+    def __init__(self, cache: KVCache, q, k, v, out, rows=None):
+        Bs = self._check(cache, q, k, v, out, q[0].shape[0] if len(q) else 0)
+        if rows is not None and len(rows) != Bs:
+            raise ValueError("rows must have one entry per row of q")
+        h = ctypes.c_void_p()
+        check(_clib.kv_step_graph_create(cache._h, ctypes.byref(h), *self._ptrs(q, k, v, out),
+                                        cache.Hq, _i32_array(rows), Bs), "kv_step_graph_create")
+        self._h, self.cache, self.Bs = h, cache, Bs
+        self._keep = (list(q), list(k), list(v), list(out))  # the graph reads these buffers
+        cache._graphs.add(self)
+
+    @staticmethod
+    def _check(cache, q, k, v, out, Bs):
+        n = len(cache.layer_kinds)
+        if not (len(q) == len(k) == len(v) == len(out) == n):
+            raise ValueError(f"one q, k, v and out tensor per layer ({n})")
+        for l in range(n):
+            cache._check_tensor(q[l], f"q[{l}]", cache.Hq, 1, Bs)
+            cache._check_tensor(k[l], f"k[{l}]", cache.Hk, 1, Bs)
+            cache._check_tensor(v[l], f"v[{l}]", cache.Hk, 1, Bs)
+            cache._check_tensor(out[l], f"out[{l}]", cache.Hq, 1, Bs)
+        return Bs
+
+    @staticmethod
+    def _ptrs(*groups):
+        return [(ctypes.c_void_p * len(ts))(*[t.data_ptr() for t in ts]) for ts in groups]
+
+    def buffers(self, q, k, v, out) -> "StepBuffers":
+        """A validated set of per-layer buffers (same shapes as at construction) that
+        launch(buffers=...) switches to without further checks."""
+        self._check(self.cache, q, k, v, out, self.Bs)
+        return StepBuffers(self._ptrs(q, k, v, out), (list(q), list(k), list(v), list(out)))
+
+    def set_buffers(self, q, k, v, out) -> None:
+        """Point the following launches at other per-layer buffers of the same shapes."""
+        self._use(self.buffers(q, k, v, out))
+
+    def _use(self, b: "StepBuffers") -> None:
+        check(_clib.kv_step_graph_set_buffers(self._h, *b.ptrs), "kv_step_graph_set_buffers")
+        self._keep = b.tensors
+
+    def launch(self, stream=None, buffers: Optional["StepBuffers"] = None) -> None:
+        """One decode step of every layer, then advance; with `buffers`, this step (and the
+        following ones) read and write that buffer set."""
+        import torch
+        if buffers is not None:
+            self._use(buffers)
+        check(_clib.kv_step_graph_launch(self._h, _stream_ptr(stream, torch.device(
+            "cuda", self.cache.device))), "kv_step_graph_launch")
+
+    def close(self) -> None:
+        if getattr(self, "_h", None):
+            _clib.kv_step_graph_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class StepBuffers:
+    """Per-layer q, k, v, out buffers checked once for a StepGraph (see StepGraph.buffers)."""
+
+    def __init__(self, ptrs, tensors):
+        self.ptrs, self.tensors = ptrs, tensors

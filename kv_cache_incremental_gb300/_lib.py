@@ -17,7 +17,8 @@ P_i32 = ctypes.POINTER(ctypes.c_int32)
 KV_GLOBAL, KV_SLIDING = 0, 1
 (KV_OK, KV_ERR_ARG, KV_ERR_FULL, KV_ERR_DTYPE, KV_ERR_CUDA, KV_ERR_OOM, KV_ERR_DEVICE,
  KV_ERR_SCRATCH) = range(8)
-KERNELS = {"append": 0, "decode": 1, "combine": 2, "prefill": 3, "commit": 4, "state": 5}
+KERNELS = {"append": 0, "decode": 1, "combine": 2, "prefill": 3, "commit": 4, "state": 5,
+           "step": 6}
 
 # name -> (restype, argtypes); mirrors include/kvinc.h
 SIGNATURES = {
@@ -43,6 +44,14 @@ SIGNATURES = {
     "kv_decode_noalloc": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_void_p,
                                   c_void_p, c_int, P_i32, P_i32, P_i32, c_int, c_void_p,
                                   c_void_p]),
+    "kv_step_graph_create": (c_int, [c_void_p, ctypes.POINTER(c_void_p), ctypes.POINTER(c_void_p),
+                                     ctypes.POINTER(c_void_p), ctypes.POINTER(c_void_p),
+                                     ctypes.POINTER(c_void_p), c_int, P_i32, c_int]),
+    "kv_step_graph_set_buffers": (c_int, [c_void_p, ctypes.POINTER(c_void_p),
+                                          ctypes.POINTER(c_void_p), ctypes.POINTER(c_void_p),
+                                          ctypes.POINTER(c_void_p)]),
+    "kv_step_graph_launch": (c_int, [c_void_p, c_void_p]),
+    "kv_step_graph_destroy": (None, [c_void_p]),
     "kv_strerror": (ctypes.c_char_p, [c_int]),
 }
 

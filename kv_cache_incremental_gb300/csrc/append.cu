@@ -172,6 +172,18 @@ cudaError_t launch_commit(const CommitParams &p, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+cudaError_t state_node(const StateParams *p, void **args, cudaKernelNodeParams *kp) {
+  if (p->n_rows <= 0) return cudaErrorInvalidValue;
+  args[0] = const_cast<StateParams *>(p);
+  kp->func = reinterpret_cast<void *>(state_kernel);
+  kp->gridDim = dim3(p->n_rows);
+  kp->blockDim = dim3(128);
+  kp->sharedMemBytes = 0;
+  kp->kernelParams = args;
+  kp->extra = nullptr;
+  return cudaSuccess;
+}
+
 cudaError_t launch_state(const StateParams &p, cudaStream_t s) {
   if (p.n_rows <= 0) return cudaSuccess;
   state_kernel<<<p.n_rows, 128, 0, s>>>(p);

@@ -581,6 +581,34 @@ cudaError_t launch_decode(const DecodeParams &p, int D, int n_tiles_heads, cudaS
   return cudaErrorInvalidValue;
 }
 
+// The same launch as a graph kernel node: function, grid, block, shared memory and the one
+// argument (the node copies *p when it is added or its parameters are set).
+cudaError_t decode_node(const DecodeParams *p, int D, int n_tiles_heads, void **args,
+                        cudaKernelNodeParams *kp) {
+  if (p->n_items <= 0) return cudaErrorInvalidValue;
+  args[0] = const_cast<DecodeParams *>(p);
+  kp->gridDim = dim3(p->n_items, p->Hk);
+  kp->blockDim = dim3(kThreads);
+  kp->kernelParams = args;
+  kp->extra = nullptr;
+  if (D == 128 && n_tiles_heads == 1) {
+    kp->func = reinterpret_cast<void *>(decode_kernel<128, 1>);
+    kp->sharedMemBytes = decode_smem_bytes<128, 1>();
+  } else if (D == 128) {
+    kp->func = reinterpret_cast<void *>(decode_kernel<128, 2>);
+    kp->sharedMemBytes = decode_smem_bytes<128, 2>();
+  } else if (D == 64 && n_tiles_heads == 1) {
+    kp->func = reinterpret_cast<void *>(decode_kernel<64, 1>);
+    kp->sharedMemBytes = decode_smem_bytes<64, 1>();
+  } else if (D == 64) {
+    kp->func = reinterpret_cast<void *>(decode_kernel<64, 2>);
+    kp->sharedMemBytes = decode_smem_bytes<64, 2>();
+  } else {
+    return cudaErrorInvalidValue;
+  }
+  return cudaSuccess;
+}
+
 cudaError_t configure_decode() {
   cudaError_t e;
   if ((e = configure_decode_t<128, 1>()) != cudaSuccess) return e;

@@ -204,6 +204,41 @@ void plan_decode(const kv_cache *c, bool sliding, const std::vector<DecodeIn> &i
   p.n_items = item;
 }
 
+// Parameters of one decode launch (fused RoPE + append + split-K attention + merge) for a
+// batch of single-token rows; kv_bytes and flops are the algorithmic counts.
+void fill_decode(const kv_cache *c, int layer, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
+                 const __nv_bfloat16 *v, __nv_bfloat16 *out, int64_t q_row, int64_t kv_row,
+                 const std::vector<DecodeIn> &batch, DecodeParams &dp, double &bytes,
+                 double &flops) {
+  const bool sliding = c->kind[layer] == KV_SLIDING;
+  dp.tmap_k = c->tmK[layer];
+  dp.tmap_v = c->tmV[layer];
+  dp.q = q;
+  dp.q_row_stride = q_row;
+  dp.out = out;
+  dp.out_row_stride = q_row;
+  dp.rope = c->rope;
+  dp.part_o = c->part_o;
+  dp.part_ml = c->part_ml;
+  dp.counters = c->counters;
+  dp.err = c->err;
+  dp.k_new = k;
+  dp.v_new = v;
+  dp.kv_row_stride = kv_row;
+  dp.cache_k = (__nv_bfloat16 *)c->K[layer];
+  dp.cache_v = (__nv_bfloat16 *)c->V[layer];
+  dp.fuse_append = 1;
+  dp.Hq = c->Hq;
+  dp.Hk = c->Hk;
+  dp.rep = c->Hq / c->Hk;
+  dp.seg_rows = c->seg_rows[layer];
+  dp.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c->D));
+  double kvb = 0;
+  plan_decode(c, sliding, batch, dp, kvb, flops);
+  // q, k, v in; new K and V and the output out
+  bytes = kvb + (double)batch.size() * (c->Hq + 2 * c->Hk) * c->D * 2.0 * 2.0;
+}
+
 int append_device(kv_cache *c, int layer, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
                   const __nv_bfloat16 *v, int C, const int32_t *n_new,
                   const std::vector<int32_t> &cache_rows, int Bs, __nv_bfloat16 *out,
@@ -273,34 +308,10 @@ int append_device(kv_cache *c, int layer, const __nv_bfloat16 *q, const __nv_bfl
     for (size_t r0 = 0; r0 < drows.size(); r0 += kMaxRowsPerLaunch) {
       const size_t r1 = std::min(drows.size(), r0 + kMaxRowsPerLaunch);
       std::vector<DecodeIn> batch(drows.begin() + r0, drows.begin() + r1);
-      dp.tmap_k = c->tmK[layer];
-      dp.tmap_v = c->tmV[layer];
-      dp.q = q;
-      dp.q_row_stride = q_row;
-      dp.out = out;
-      dp.out_row_stride = q_row;
-      dp.rope = c->rope;
-      dp.part_o = c->part_o;
-      dp.part_ml = c->part_ml;
-      dp.counters = c->counters;
-      dp.err = c->err;
-      dp.k_new = k;
-      dp.v_new = v;
-      dp.kv_row_stride = kv_row;
-      dp.cache_k = (__nv_bfloat16 *)c->K[layer];
-      dp.cache_v = (__nv_bfloat16 *)c->V[layer];
-      dp.fuse_append = 1;
-      dp.Hq = Hq;
-      dp.Hk = Hk;
-      dp.rep = rep;
-      dp.seg_rows = c->seg_rows[layer];
-      dp.scale_log2 = scale_log2;
-      double kvb = 0, fl = 0;
-      plan_decode(c, sliding, batch, dp, kvb, fl);
-      // q, k, v in; new K and V and the output out
-      const double io = (double)batch.size() * (Hq + 2 * Hk) * D * 2.0 * 2.0;
+      double bytes = 0, fl = 0;
+      fill_decode(c, layer, q, k, v, out, q_row, kv_row, batch, dp, bytes, fl);
       const int nt = rep <= 8 ? 1 : 2;
-      cudaError_t e = timed(c, KV_KERNEL_DECODE, kvb + io, fl, s,
+      cudaError_t e = timed(c, KV_KERNEL_DECODE, bytes, fl, s,
                             [&] { return launch_decode(dp, D, nt, s); });
       if (e != cudaSuccess) return KV_ERR_CUDA;
     }
@@ -384,25 +395,31 @@ int append_device(kv_cache *c, int layer, const __nv_bfloat16 *q, const __nv_bfl
   return KV_OK;
 }
 
+// lpos update of one advance for rows [r0, r1) of `rows` (rows with n_new = 0 skipped).
+void fill_state(const kv_cache *c, const std::vector<int32_t> &rows, const int32_t *n_new,
+                bool reset, size_t r0, size_t r1, StateParams &sp) {
+  sp.lpos = c->lpos;
+  sp.ring_R = c->R;
+  sp.window = c->W;
+  sp.reset = reset ? 1 : 0;
+  int n = 0;
+  for (size_t j = r0; j < r1; ++j) {
+    if (!reset && n_new[j] == 0) continue;
+    sp.cache_row[n] = rows[j];
+    sp.lens[n] = c->lens[rows[j]];
+    sp.n[n] = reset ? 0 : n_new[j];
+    ++n;
+  }
+  sp.n_rows = n;
+}
+
 int state_update(kv_cache *c, const std::vector<int32_t> &rows, const int32_t *n_new, bool reset,
                  cudaStream_t s) {
   if (!c->lpos) return KV_OK;  // lens lives on the host; lpos exists with sliding layers only
   static thread_local StateParams sp;
   for (size_t r0 = 0; r0 < rows.size(); r0 += kMaxRowsPerLaunch) {
     const size_t r1 = std::min(rows.size(), r0 + kMaxRowsPerLaunch);
-    sp.lpos = c->lpos;
-    sp.ring_R = c->R;
-    sp.window = c->W;
-    sp.reset = reset ? 1 : 0;
-    int n = 0;
-    for (size_t j = r0; j < r1; ++j) {
-      if (!reset && n_new[j] == 0) continue;
-      sp.cache_row[n] = rows[j];
-      sp.lens[n] = c->lens[rows[j]];
-      sp.n[n] = reset ? 0 : n_new[j];
-      ++n;
-    }
-    sp.n_rows = n;
+    fill_state(c, rows, n_new, reset, r0, r1, sp);
     cudaError_t e = timed(c, KV_KERNEL_STATE, 0, 0, s, [&] { return launch_state(sp, s); });
     if (e != cudaSuccess) return KV_ERR_CUDA;
   }
@@ -745,6 +762,175 @@ int kv_profile_read(kv_cache *c, int kind, int reset, int64_t *launches, double 
     c->recs.swap(keep);
   }
   return KV_OK;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------- decode-step graph
+// One decode step of a fixed row set as a CUDA graph: a chain of one decode kernel node
+// per layer and, with sliding layers, the ring-state node.  Every launch re-plans the step
+// from the host lengths and rewrites the nodes' parameters (and grid sizes) in the
+// instantiated graph, so the kernels see exactly what kv_append / kv_advance would pass.
+struct kv_step_graph {
+  kv_cache *c = nullptr;
+  int Bs = 0;
+  std::vector<int32_t> rows;  // cache rows
+  std::vector<const __nv_bfloat16 *> q, k, v;
+  std::vector<__nv_bfloat16 *> out;
+  std::vector<DecodeParams> dps;  // per layer (each ~20 KB: kept on the heap)
+  StateParams sp;
+  std::vector<cudaGraphNode_t> dec;
+  cudaGraphNode_t state = nullptr;
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+  double bytes = 0, flops = 0;
+};
+
+namespace {
+
+// Parameters of every node for the current lengths (a full row is planned at max_len - 1;
+// launches refuse full rows before they get here).
+void plan_step(kv_step_graph *g) {
+  kv_cache *c = g->c;
+  std::vector<DecodeIn> batch(g->Bs);
+  for (int i = 0; i < g->Bs; ++i)
+    batch[i] = {g->rows[i], i, std::min(c->lens[g->rows[i]], c->max_len - 1)};
+  const int64_t q_row = (int64_t)c->Hq * c->D, kv_row = (int64_t)c->Hk * c->D;
+  g->bytes = 0;
+  g->flops = 0;
+  for (int l = 0; l < c->n_layers; ++l) {
+    double by = 0, fl = 0;
+    fill_decode(c, l, g->q[l], g->k[l], g->v[l], g->out[l], q_row, kv_row, batch, g->dps[l], by,
+                fl);
+    g->bytes += by;
+    g->flops += fl;
+  }
+  if (c->lpos) {
+    const std::vector<int32_t> ones(g->Bs, 1);
+    fill_state(c, g->rows, ones.data(), false, 0, g->rows.size(), g->sp);
+  }
+}
+
+void free_step_graph(kv_step_graph *g) {
+  if (g->exec) cudaGraphExecDestroy(g->exec);
+  if (g->graph) cudaGraphDestroy(g->graph);
+  delete g;
+}
+
+}  // namespace
+
+extern "C" {
+
+int kv_step_graph_create(kv_cache *c, kv_step_graph **out, const void *const *q,
+                         const void *const *k, const void *const *v, void *const *outp, int Hq,
+                         const int32_t *rows, int Bs) {
+  if (!c || !out || !q || !k || !v || !outp || Hq != c->Hq) return KV_ERR_ARG;
+  if (Bs < 1 || Bs > c->B || Bs > kMaxRowsPerLaunch) return KV_ERR_ARG;
+  std::vector<int32_t> cache_rows;
+  std::vector<char> seen(c->B, 0);
+  for (int i = 0; i < Bs; ++i) {
+    const int r = rows ? rows[i] : i;
+    if (r < 0 || r >= c->B || seen[r]) return KV_ERR_ARG;
+    seen[r] = 1;
+    cache_rows.push_back(r);
+  }
+  for (int l = 0; l < c->n_layers; ++l)
+    if (!q[l] || !k[l] || !v[l] || !outp[l] || !aligned16(q[l]) || !aligned16(k[l]) ||
+        !aligned16(v[l]) || !aligned16(outp[l]))
+      return KV_ERR_ARG;
+  DeviceGuard guard(c->device);
+  kv_step_graph *g = new kv_step_graph;
+  g->c = c;
+  g->Bs = Bs;
+  g->rows = cache_rows;
+  for (int l = 0; l < c->n_layers; ++l) {
+    g->q.push_back((const __nv_bfloat16 *)q[l]);
+    g->k.push_back((const __nv_bfloat16 *)k[l]);
+    g->v.push_back((const __nv_bfloat16 *)v[l]);
+    g->out.push_back((__nv_bfloat16 *)outp[l]);
+  }
+  g->dps.resize(c->n_layers);
+  plan_step(g);
+  const int nt = c->Hq / c->Hk <= 8 ? 1 : 2;
+  bool ok = cudaGraphCreate(&g->graph, 0) == cudaSuccess;
+  cudaGraphNode_t prev = nullptr;
+  for (int l = 0; ok && l < c->n_layers; ++l) {
+    void *args[1];
+    cudaKernelNodeParams kp{};
+    cudaGraphNode_t node = nullptr;
+    ok = decode_node(&g->dps[l], c->D, nt, args, &kp) == cudaSuccess &&
+         cudaGraphAddKernelNode(&node, g->graph, prev ? &prev : nullptr, prev ? 1 : 0, &kp) ==
+             cudaSuccess;
+    g->dec.push_back(node);
+    prev = node;
+  }
+  if (ok && c->lpos) {
+    void *args[1];
+    cudaKernelNodeParams kp{};
+    ok = state_node(&g->sp, args, &kp) == cudaSuccess &&
+         cudaGraphAddKernelNode(&g->state, g->graph, &prev, 1, &kp) == cudaSuccess;
+  }
+  ok = ok && cudaGraphInstantiate(&g->exec, g->graph, 0) == cudaSuccess;
+  if (!ok) {
+    free_step_graph(g);
+    cudaGetLastError();
+    return KV_ERR_CUDA;
+  }
+  *out = g;
+  return KV_OK;
+}
+
+int kv_step_graph_set_buffers(kv_step_graph *g, const void *const *q, const void *const *k,
+                              const void *const *v, void *const *outp) {
+  if (!g || !q || !k || !v || !outp) return KV_ERR_ARG;
+  const int L = g->c->n_layers;
+  for (int l = 0; l < L; ++l)
+    if (!q[l] || !k[l] || !v[l] || !outp[l] || !aligned16(q[l]) || !aligned16(k[l]) ||
+        !aligned16(v[l]) || !aligned16(outp[l]))
+      return KV_ERR_ARG;
+  for (int l = 0; l < L; ++l) {
+    g->q[l] = (const __nv_bfloat16 *)q[l];
+    g->k[l] = (const __nv_bfloat16 *)k[l];
+    g->v[l] = (const __nv_bfloat16 *)v[l];
+    g->out[l] = (__nv_bfloat16 *)outp[l];
+  }
+  return KV_OK;
+}
+
+int kv_step_graph_launch(kv_step_graph *g, void *stream) {
+  if (!g) return KV_ERR_ARG;
+  kv_cache *c = g->c;
+  for (int r : g->rows)
+    if ((int64_t)c->lens[r] + 1 > c->max_len) return KV_ERR_FULL;
+  DeviceGuard guard(c->device);
+  cudaStream_t s = (cudaStream_t)stream;
+  plan_step(g);
+  const int nt = c->Hq / c->Hk <= 8 ? 1 : 2;
+  for (int l = 0; l < c->n_layers; ++l) {
+    void *args[1];
+    cudaKernelNodeParams kp{};
+    if (decode_node(&g->dps[l], c->D, nt, args, &kp) != cudaSuccess ||
+        cudaGraphExecKernelNodeSetParams(g->exec, g->dec[l], &kp) != cudaSuccess)
+      return KV_ERR_CUDA;
+  }
+  if (g->state) {
+    void *args[1];
+    cudaKernelNodeParams kp{};
+    if (state_node(&g->sp, args, &kp) != cudaSuccess ||
+        cudaGraphExecKernelNodeSetParams(g->exec, g->state, &kp) != cudaSuccess)
+      return KV_ERR_CUDA;
+  }
+  const cudaError_t e = timed(c, KV_KERNEL_STEP, g->bytes, g->flops, s,
+                              [&] { return cudaGraphLaunch(g->exec, s); });
+  if (e != cudaSuccess) return KV_ERR_CUDA;
+  for (int r : g->rows) c->lens[r] += 1;
+  return KV_OK;
+}
+
+void kv_step_graph_destroy(kv_step_graph *g) {
+  if (!g) return;
+  DeviceGuard guard(g->c->device);
+  free_step_graph(g);
 }
 
 const char *kv_strerror(int code) {

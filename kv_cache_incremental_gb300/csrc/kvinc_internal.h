@@ -151,6 +151,11 @@ struct StateParams {
 // ---------------------------------------------------------------- launchers
 cudaError_t launch_append(const AppendParams &p, cudaStream_t s);
 cudaError_t launch_decode(const DecodeParams &p, int D, int n_tiles_heads, cudaStream_t s);
+// Graph kernel-node descriptions of the decode and state launches (args: one-slot storage
+// that must outlive the call that consumes *kp).
+cudaError_t decode_node(const DecodeParams *p, int D, int n_tiles_heads, void **args,
+                        cudaKernelNodeParams *kp);
+cudaError_t state_node(const StateParams *p, void **args, cudaKernelNodeParams *kp);
 cudaError_t launch_prefill(const PrefillParams &p, int D, cudaStream_t s);
 cudaError_t launch_commit(const CommitParams &p, cudaStream_t s);
 cudaError_t launch_state(const StateParams &p, cudaStream_t s);
