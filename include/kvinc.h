@@ -256,6 +256,45 @@ int kv_step_graph_launch(kv_step_graph *g, void *stream);
 void kv_step_graph_destroy(kv_step_graph *g);
 
 /*
+ * Prefix reuse and row export / import.  A row's state is its length and, per layer,
+ * the K/V of the positions the layer keeps: all of [0, lens) on a global layer, the
+ * last R of them on a sliding layer (ring slot p % R).  Copies move positions, so a
+ * ring is copied position by position and a global prefix linearly ("inkling:
+ * ring-buffer KV cache for sliding-window layers", review of the change: prefix reuse
+ * by grow-with-copy must copy the ring whole, keeping t % win valid, and global rows
+ * linearly; "Lab 07 -- KV cache and sampling", Going further: prefix sharing).
+ *
+ * kv_copy_rows: for i < n, destination row dst_rows[i] of `dst` becomes the first
+ *   keep[i] tokens of source row src_rows[i] of `src` (keep == NULL: the source's
+ *   whole length): its K/V, ring state (lpos) and length.  Uses: forking a sequence
+ *   into another row, reusing a shared prompt prefix, truncating a row (src == dst,
+ *   same row), and moving rows into a cache with another max_len or B (grow-with-
+ *   copy).  dst and src may be the same cache.  Both caches must have the same Hk, D,
+ *   W, layer layout, rope_theta and device.  Rows: host int32 [n]; destination rows
+ *   distinct; in one cache no destination row may be another pair's source row.
+ *   keep[i] <= the source length and <= dst's max_len, and every position the
+ *   destination keeps must still be in the source: on caches with sliding layers,
+ *   max(0, keep - R_dst) >= max(0, src_len - R_src) (a ring that has wrapped holds
+ *   only its last R positions, so such a row can be copied whole but not truncated).
+ *   Violations return KV_ERR_ARG before anything is enqueued.  Asynchronous on
+ *   `stream`; the source rows must not be written until the copy has run.
+ *
+ * kv_export_bytes: size of a row's state at length keep (-1 for a bad keep).
+ * kv_export_row: writes the first `keep` tokens of `row` (keep <= its length, same
+ *   presence rule) to the device buffer `dst` of exactly kv_export_bytes(c, keep)
+ *   bytes, 16-byte aligned: per layer in order, K [Hk][n_l][D] then V [Hk][n_l][D]
+ *   bf16, n_l = the layer's kept positions in ascending order.
+ * kv_import_row: row `row` becomes that state (its length keep <= max_len); K/V of
+ *   positions the row does not keep are left as they are.  The buffer is read on
+ *   `stream`.  KV_ERR_ARG for bad arguments or a byte count that does not match.
+ */
+int kv_copy_rows(kv_cache *dst, const int32_t *dst_rows, const kv_cache *src,
+                 const int32_t *src_rows, const int32_t *keep, int n, void *stream);
+int64_t kv_export_bytes(const kv_cache *c, int keep);
+int kv_export_row(const kv_cache *c, int row, int keep, void *dst, int64_t bytes, void *stream);
+int kv_import_row(kv_cache *c, int row, int keep, const void *src, int64_t bytes, void *stream);
+
+/*
  * Decode attention that allocates nothing.  The pages have no counterpart: this
  * entry point exists for callers that cannot call cudaMalloc -- for example a
  * process whose device memory is owned by another allocator (a framework's

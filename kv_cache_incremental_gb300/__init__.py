@@ -112,6 +112,38 @@ class KVCache:
                              _stream_ptr(stream, q.device)), "kv_append")
         return out
 
+    def copy_rows(self, src: "KVCache", src_rows, dst_rows, keep=None, stream=None) -> None:
+        """Rows dst_rows of this cache become the first keep[i] tokens (default: all) of
+        rows src_rows of `src` (this cache or another of the same layout)."""
+        import torch
+        n = len(src_rows)
+        if len(dst_rows) != n or (keep is not None and len(keep) != n):
+            raise ValueError("src_rows, dst_rows and keep need one entry per copy")
+        check(_clib.kv_copy_rows(self._h, _i32_array(dst_rows), src._h, _i32_array(src_rows),
+                                _i32_array(keep), n,
+                                _stream_ptr(stream, torch.device("cuda", self.device))),
+              "kv_copy_rows")
+
+    def export_row(self, row: int, keep: Optional[int] = None, stream=None):
+        """The first `keep` tokens (default: all) of a row as a flat uint8 device tensor."""
+        import torch
+        keep = self.lens[row] if keep is None else keep
+        nbytes = _clib.kv_export_bytes(self._h, keep)
+        if nbytes < 0:
+            raise ValueError(f"keep={keep} out of range")
+        buf = torch.empty(max(16, nbytes), dtype=torch.uint8, device=f"cuda:{self.device}")
+        check(_clib.kv_export_row(self._h, row, keep, buf.data_ptr(), nbytes,
+                                 _stream_ptr(stream, buf.device)), "kv_export_row")
+        return buf[:nbytes]
+
+    def import_row(self, row: int, buf, keep: int, stream=None) -> None:
+        """Make `row` the state exported as `buf` (a tensor from export_row) at length keep."""
+        if not buf.is_cuda or buf.device.index != self.device:
+            raise ValueError(f"buf must live on cuda:{self.device}")
+        check(_clib.kv_import_row(self._h, row, keep, buf.data_ptr(), buf.numel() *
+                                 buf.element_size(), _stream_ptr(stream, buf.device)),
+              "kv_import_row")
+
     def step_graph(self, q, k, v, out, rows=None) -> "StepGraph":
         """A static-shape decode step (every layer, one token per row, then advance) as a
         CUDA graph over fixed per-layer buffers q[l], k[l], v[l], out[l] of shape

@@ -11,7 +11,8 @@ OUT_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(OUT_DIR, "libkvinc.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
-SOURCES = ["host.cu", "append.cu", "decode.cu", "prefill.cu", "prefill_tc.cu", "noalloc.cu"]
+SOURCES = ["host.cu", "append.cu", "decode.cu", "prefill.cu", "prefill_tc.cu", "noalloc.cu",
+           "rowcopy.cu"]
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",
               "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall", f"-I{INCLUDE}"]
 

@@ -52,6 +52,10 @@ SIGNATURES = {
                                           ctypes.POINTER(c_void_p)]),
     "kv_step_graph_launch": (c_int, [c_void_p, c_void_p]),
     "kv_step_graph_destroy": (None, [c_void_p]),
+    "kv_copy_rows": (c_int, [c_void_p, P_i32, c_void_p, P_i32, P_i32, c_int, c_void_p]),
+    "kv_export_bytes": (c_int64, [c_void_p, c_int]),
+    "kv_export_row": (c_int, [c_void_p, c_int, c_int, c_void_p, c_int64, c_void_p]),
+    "kv_import_row": (c_int, [c_void_p, c_int, c_int, c_void_p, c_int64, c_void_p]),
     "kv_strerror": (ctypes.c_char_p, [c_int]),
 }
 

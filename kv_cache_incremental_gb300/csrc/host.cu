@@ -933,6 +933,205 @@ void kv_step_graph_destroy(kv_step_graph *g) {
   free_step_graph(g);
 }
 
+}  // extern "C"
+
+// ---------------------------------------------------------------- row copies
+namespace {
+
+// Positions of a row kept by a layer once its length is `keep`: all of [0, keep) on a global
+// layer, the last R of them on a sliding layer.
+int first_kept(const kv_cache *c, int layer, int keep) {
+  return c->kind[layer] == KV_SLIDING ? std::max(0, keep - c->R) : 0;
+}
+
+// Storage block of (row, layer): K, V and the element stride between heads.
+void row_block(const kv_cache *c, int layer, int row, __nv_bfloat16 *&k, __nv_bfloat16 *&v,
+               int64_t &head_stride) {
+  const int64_t off = (int64_t)row * c->Hk * c->seg_rows[layer] * c->D;
+  k = (__nv_bfloat16 *)c->K[layer] + off;
+  v = (__nv_bfloat16 *)c->V[layer] + off;
+  head_stride = (int64_t)c->seg_rows[layer] * c->D;
+}
+
+// Can the source row, at length `lens`, supply every position a destination of length `keep`
+// keeps?  Ring positions older than lens - R are gone from a sliding layer.
+bool positions_present(const kv_cache *src, int lens, int keep, int dst_R) {
+  if (keep > lens) return false;
+  bool sliding = false;
+  for (int k : src->kind) sliding |= k == KV_SLIDING;
+  if (!sliding) return true;
+  const int need_lo = std::max(0, keep - dst_R);
+  const int have_lo = std::max(0, lens - src->R);
+  return need_lo >= have_lo;
+}
+
+int flush_copies(CopyParams &cp, cudaStream_t s) {
+  const cudaError_t e = launch_copy(cp, s);
+  cp.n_items = 0;
+  return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+}
+
+int add_copy(CopyParams &cp, const CopyItem &it, cudaStream_t s) {
+  if (it.p1 <= it.p0) return KV_OK;
+  cp.items[cp.n_items++] = it;
+  return cp.n_items == kMaxCopyItems ? flush_copies(cp, s) : KV_OK;
+}
+
+// lpos of rows that now hold [0, keep): reset, then record the kept positions.
+int set_ring_state(kv_cache *c, const std::vector<int32_t> &rows, const std::vector<int32_t> &keep,
+                   cudaStream_t s) {
+  if (!c->lpos || rows.empty()) return KV_OK;
+  const std::vector<int32_t> saved = [&] {
+    std::vector<int32_t> v;
+    for (int r : rows) v.push_back(c->lens[r]);
+    return v;
+  }();
+  int rc = state_update(c, rows, nullptr, true, s);
+  for (int r : rows) c->lens[r] = 0;
+  if (rc == KV_OK) rc = state_update(c, rows, keep.data(), false, s);
+  for (size_t i = 0; i < rows.size(); ++i) c->lens[rows[i]] = saved[i];
+  return rc;
+}
+
+bool same_layout(const kv_cache *a, const kv_cache *b) {
+  return a->Hk == b->Hk && a->D == b->D && a->W == b->W && a->n_layers == b->n_layers &&
+         a->kind == b->kind && a->theta == b->theta && a->device == b->device;
+}
+
+}  // namespace
+
+extern "C" {
+
+int kv_copy_rows(kv_cache *dst, const int32_t *dst_rows, const kv_cache *src,
+                 const int32_t *src_rows, const int32_t *keep, int n, void *stream) {
+  if (!dst || !src || n < 0 || (n > 0 && (!dst_rows || !src_rows))) return KV_ERR_ARG;
+  if (!same_layout(dst, src)) return KV_ERR_ARG;
+  std::vector<int32_t> kp(n);
+  std::vector<char> dseen(dst->B, 0);
+  for (int i = 0; i < n; ++i) {
+    const int d = dst_rows[i], r = src_rows[i];
+    if (d < 0 || d >= dst->B || r < 0 || r >= src->B || dseen[d]) return KV_ERR_ARG;
+    dseen[d] = 1;
+    kp[i] = keep ? keep[i] : src->lens[r];
+    if (kp[i] < 0 || kp[i] > dst->max_len || !positions_present(src, src->lens[r], kp[i], dst->R))
+      return KV_ERR_ARG;
+  }
+  if (dst == src)  // a row written by one pair must not be read by another
+    for (int i = 0; i < n; ++i)
+      for (int j = 0; j < n; ++j)
+        if (i != j && dst_rows[i] == src_rows[j]) return KV_ERR_ARG;
+  if (n == 0) return KV_OK;
+  DeviceGuard guard(dst->device);
+  cudaStream_t s = (cudaStream_t)stream;
+  static thread_local CopyParams cp;
+  cp.Hk = dst->Hk;
+  cp.D = dst->D;
+  cp.n_items = 0;
+  for (int i = 0; i < n; ++i) {
+    if (dst == src && dst_rows[i] == src_rows[i]) continue;  // the row keeps its own slots
+    for (int l = 0; l < dst->n_layers; ++l) {
+      CopyItem it;
+      __nv_bfloat16 *sk, *sv;
+      row_block(src, l, src_rows[i], sk, sv, it.src_head_stride);
+      it.src_k = sk;
+      it.src_v = sv;
+      row_block(dst, l, dst_rows[i], it.dst_k, it.dst_v, it.dst_head_stride);
+      const bool ring = dst->kind[l] == KV_SLIDING;
+      it.p0 = first_kept(dst, l, kp[i]);
+      it.p1 = kp[i];
+      it.src_ring = ring ? src->R : 0;
+      it.dst_ring = ring ? dst->R : 0;
+      it.src_base = it.dst_base = 0;
+      if (add_copy(cp, it, s) != KV_OK) return KV_ERR_CUDA;
+    }
+  }
+  if (cp.n_items && flush_copies(cp, s) != KV_OK) return KV_ERR_CUDA;
+  std::vector<int32_t> rows(dst_rows, dst_rows + n);
+  if (set_ring_state(dst, rows, kp, s) != KV_OK) return KV_ERR_CUDA;
+  for (int i = 0; i < n; ++i) dst->lens[dst_rows[i]] = kp[i];
+  return KV_OK;
+}
+
+int64_t kv_export_bytes(const kv_cache *c, int keep) {
+  if (!c || keep < 0 || keep > c->max_len) return -1;
+  int64_t b = 0;
+  for (int l = 0; l < c->n_layers; ++l)
+    b += 2LL * c->Hk * (keep - first_kept(c, l, keep)) * c->D * 2;
+  return b;
+}
+
+// Flat layout, per layer in order: K [Hk][positions][D] then V [Hk][positions][D], positions
+// ascending over the ones the layer keeps at length `keep`.
+static int export_import(kv_cache *c, int row, int keep, void *buf, int64_t bytes,
+                         cudaStream_t s, bool to_buf) {
+  __nv_bfloat16 *b = (__nv_bfloat16 *)buf;
+  static thread_local CopyParams cp;
+  cp.Hk = c->Hk;
+  cp.D = c->D;
+  cp.n_items = 0;
+  int64_t off = 0;
+  for (int l = 0; l < c->n_layers; ++l) {
+    const int p0 = first_kept(c, l, keep), np = keep - p0;
+    const int64_t blk = (int64_t)c->Hk * np * c->D;
+    __nv_bfloat16 *rk, *rv;
+    int64_t hs;
+    row_block(c, l, row, rk, rv, hs);
+    const int ring = c->kind[l] == KV_SLIDING ? c->R : 0;
+    CopyItem it;
+    it.p0 = p0;
+    it.p1 = keep;
+    if (to_buf) {
+      it.src_k = rk;
+      it.src_v = rv;
+      it.src_head_stride = hs;
+      it.src_ring = ring;
+      it.src_base = 0;
+      it.dst_k = b + off;
+      it.dst_v = b + off + blk;
+      it.dst_head_stride = (int64_t)np * c->D;
+      it.dst_ring = 0;
+      it.dst_base = p0;
+    } else {
+      it.src_k = b + off;
+      it.src_v = b + off + blk;
+      it.src_head_stride = (int64_t)np * c->D;
+      it.src_ring = 0;
+      it.src_base = p0;
+      it.dst_k = rk;
+      it.dst_v = rv;
+      it.dst_head_stride = hs;
+      it.dst_ring = ring;
+      it.dst_base = 0;
+    }
+    off += 2 * blk;
+    if (add_copy(cp, it, s) != KV_OK) return KV_ERR_CUDA;
+  }
+  if (off * 2 != bytes) return KV_ERR_ARG;  // unreachable: checked by the callers
+  if (cp.n_items && flush_copies(cp, s) != KV_OK) return KV_ERR_CUDA;
+  return KV_OK;
+}
+
+int kv_export_row(const kv_cache *c, int row, int keep, void *dst, int64_t bytes, void *stream) {
+  if (!c || row < 0 || row >= c->B || !dst || (reinterpret_cast<uintptr_t>(dst) & 15u)) return KV_ERR_ARG;
+  if (keep < 0 || !positions_present(c, c->lens[row], keep, c->R)) return KV_ERR_ARG;
+  if (bytes != kv_export_bytes(c, keep)) return KV_ERR_ARG;
+  DeviceGuard guard(c->device);
+  return export_import(const_cast<kv_cache *>(c), row, keep, dst, bytes, (cudaStream_t)stream,
+                       true);
+}
+
+int kv_import_row(kv_cache *c, int row, int keep, const void *src, int64_t bytes, void *stream) {
+  if (!c || row < 0 || row >= c->B || !src || (reinterpret_cast<uintptr_t>(src) & 15u)) return KV_ERR_ARG;
+  if (keep < 0 || keep > c->max_len || bytes != kv_export_bytes(c, keep)) return KV_ERR_ARG;
+  DeviceGuard guard(c->device);
+  cudaStream_t s = (cudaStream_t)stream;
+  const int rc = export_import(c, row, keep, const_cast<void *>(src), bytes, s, false);
+  if (rc != KV_OK) return rc;
+  if (set_ring_state(c, {row}, {keep}, s) != KV_OK) return KV_ERR_CUDA;
+  c->lens[row] = keep;
+  return KV_OK;
+}
+
 const char *kv_strerror(int code) {
   switch (code) {
     case KV_OK: return "KV_OK";

@@ -148,7 +148,26 @@ struct StateParams {
   int32_t n[kMaxRowsPerLaunch];
 };
 
+// ---------------------------------------------------------------- position copies
+// One (row, layer) block of K/V positions [p0, p1) copied from one storage to another.
+// A storage is [Hk][slots][D] per (row, layer) at `k`/`v` with `head_stride` elements
+// between heads; position p sits at slot p % ring (ring > 0) or p - base (ring == 0).
+struct CopyItem {
+  const __nv_bfloat16 *src_k, *src_v;
+  __nv_bfloat16 *dst_k, *dst_v;
+  int64_t src_head_stride, dst_head_stride;
+  int32_t p0, p1;
+  int32_t src_ring, src_base, dst_ring, dst_base;
+};
+constexpr int kMaxCopyItems = 256;
+struct CopyParams {
+  int Hk, D;
+  int n_items;
+  CopyItem items[kMaxCopyItems];
+};
+
 // ---------------------------------------------------------------- launchers
+cudaError_t launch_copy(const CopyParams &p, cudaStream_t s);
 cudaError_t launch_append(const AppendParams &p, cudaStream_t s);
 cudaError_t launch_decode(const DecodeParams &p, int D, int n_tiles_heads, cudaStream_t s);
 // Graph kernel-node descriptions of the decode and state launches (args: one-slot storage
