@@ -64,7 +64,8 @@ enum kv_status {
     KV_ERR_CUDA = 4,   /* a CUDA runtime call failed */
     KV_ERR_OOM = 5,    /* device memory allocation failed at create */
     KV_ERR_DEVICE = 6, /* a kernel reported a timed-out wait (see kv_device_error) */
-    KV_ERR_SCRATCH = 7 /* request too large for kv_decode_noalloc's fixed scratch */
+    KV_ERR_SCRATCH = 7, /* request too large for kv_decode_noalloc's fixed scratch */
+    KV_ERR_POOL = 8     /* a paged cache has no free block for the new positions */
 };
 
 /*
@@ -91,6 +92,32 @@ enum kv_status {
  */
 int kv_cache_create(kv_cache **out, int B, int max_len, int Hq, int Hk, int D, int W,
                     int n_layers, const int32_t *layer_kind, double rope_theta, int device);
+
+/*
+ * Paged cache: as kv_cache_create, but every global layer keeps its K/V in a pool of
+ * n_blocks blocks of 16 positions ([Hk][16][D] bf16 each) and each row a table of the
+ * blocks that hold its positions 16i..16i+15, shared by all global layers (a row has
+ * the same length on all of them) ("Lab 07 -- KV cache and sampling", Going further:
+ * fixed 16-token blocks plus a per-sequence block table; "tinyllm/kv_cache.py": a
+ * dense cache reserves max_len slots per row whatever its length).  Blocks are taken
+ * from the pool when a call appends positions past a row's last block (kv_append,
+ * kv_append_host, kv_step_graph_launch, kv_copy_rows, kv_import_row) and returned on
+ * kv_reset or when a copy shortens a row.  A call whose rows need more blocks than
+ * are free returns KV_ERR_POOL before anything is enqueued.  Sliding layers keep their
+ * dense rings.  Results are those of the dense cache, bit for bit.  1 <= n_blocks,
+ * n_blocks * Hk * 16 < 2^31; with n_blocks >= B * ceil(max_len / 16) no call runs
+ * out of blocks.  The pool is reused on the caller's stream order: one stream per
+ * cache.
+ */
+int kv_cache_create_paged(kv_cache **out, int B, int max_len, int Hq, int Hk, int D, int W,
+                          int n_layers, const int32_t *layer_kind, double rope_theta, int device,
+                          int n_blocks);
+/* Pool blocks of a row, in position order (host mirror): writes min(count, capacity)
+ * entries and the count to *n_out (0 for a dense cache).  Free blocks of the pool, or
+ * -1 for NULL. */
+int kv_get_block_table(const kv_cache *c, int row, int32_t *blocks_out, int capacity,
+                       int *n_out);
+int kv_free_blocks(const kv_cache *c);
 
 /* Free all device and host memory of the cache (NULL is a no-op).  Waits for
  * the device to finish work that uses the cache. */
@@ -164,7 +191,8 @@ int kv_append_host(kv_cache *c, int layer, const void *q, const void *k, const v
 int kv_advance(kv_cache *c, const int32_t *n_new, const int32_t *rows, int Bs, void *stream);
 
 /* Bytes of K and V storage of all layers, scratch slots included ([G] nbytes,
- * [P] memory_bytes).  -1 for a NULL cache. */
+ * [P] memory_bytes); a paged cache counts its global layers' whole pools.  -1 for
+ * a NULL cache. */
 int64_t kv_nbytes(const kv_cache *c);
 
 /* Copy the host mirror of lens into lens_out (host int32 [B]).  No device sync. */
@@ -172,7 +200,9 @@ int kv_get_lens(const kv_cache *c, int32_t *lens_out);
 
 /* Device pointers of a layer's K and V storage and of lpos ([B][R] int32, or
  * NULL without sliding layers), for inspection and tests.  Layouts as in
- * kv_cache_create.  The pointers stay owned by the cache. */
+ * kv_cache_create; a paged cache's global layers point at their block pools
+ * ([n_blocks][Hk][16][D], see kv_get_block_table).  The pointers stay owned by the
+ * cache. */
 int kv_debug_ptrs(const kv_cache *c, int layer, void **K, void **V, int32_t **lpos);
 
 /* Shape query: fills any non-NULL output with the cache's parameters. */

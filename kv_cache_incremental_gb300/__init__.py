@@ -16,9 +16,11 @@ import ctypes
 import weakref
 from typing import Optional, Sequence
 
-from ._lib import (KERNELS, KV_GLOBAL, KV_SLIDING, KVCacheFull, KVError, check, load)
+from ._lib import (KERNELS, KV_GLOBAL, KV_SLIDING, KVCacheFull, KVError, KVPoolExhausted, check,
+                   load)
 
-__all__ = ["KVCache", "StepGraph", "KVError", "KVCacheFull", "KV_GLOBAL", "KV_SLIDING", "load"]
+__all__ = ["KVCache", "StepGraph", "KVError", "KVCacheFull", "KVPoolExhausted", "KV_GLOBAL",
+           "KV_SLIDING", "load"]
 
 _clib = load()
 
@@ -50,11 +52,20 @@ class KVCache:
 
     def __init__(self, B: int, max_len: int, Hq: int, Hk: int, D: int, W: int = 0,
                  layer_kinds: Sequence[int] = (KV_GLOBAL,), rope_theta: float = 1e4,
-                 device: int = 0):
+                 device: int = 0, paged_blocks: Optional[int] = None):
+        """paged_blocks: global layers in a pool of that many 16-position blocks
+        (kv_cache_create_paged) instead of max_len slots per row."""
         kinds = _i32_array(layer_kinds)
         h = ctypes.c_void_p()
-        check(_clib.kv_cache_create(ctypes.byref(h), B, max_len, Hq, Hk, D, W, len(layer_kinds),
-                                   kinds, float(rope_theta), device), "kv_cache_create")
+        if paged_blocks is None:
+            check(_clib.kv_cache_create(ctypes.byref(h), B, max_len, Hq, Hk, D, W,
+                                       len(layer_kinds), kinds, float(rope_theta), device),
+                  "kv_cache_create")
+        else:
+            check(_clib.kv_cache_create_paged(ctypes.byref(h), B, max_len, Hq, Hk, D, W,
+                                             len(layer_kinds), kinds, float(rope_theta), device,
+                                             int(paged_blocks)), "kv_cache_create_paged")
+        self.paged_blocks = paged_blocks
         self._h = h
         self.B, self.max_len, self.Hq, self.Hk, self.D, self.W = B, max_len, Hq, Hk, D, W
         self.layer_kinds = list(layer_kinds)
@@ -190,18 +201,48 @@ class KVCache:
         return int(_clib.kv_nbytes(self._h))
 
     def storage(self, layer: int):
-        """Zero-copy torch views (K, V) of a layer's storage, [B, Hk, rows, D] bf16;
-        rows = max_len + 1 (global) or R + 1 (sliding).  Valid while the cache lives."""
+        """Torch views (K, V) of a layer's storage, [B, Hk, rows, D] bf16; rows = max_len + 1
+        (global) or R + 1 (sliding).  Zero-copy and valid while the cache lives, except for a
+        paged cache's global layers: there each row's blocks are gathered from the pool into
+        a new tensor (slots past the row's blocks are zero)."""
         import torch
         kp, vp, lp = ctypes.c_void_p(), ctypes.c_void_p(), ctypes.c_void_p()
         check(_clib.kv_debug_ptrs(self._h, layer, ctypes.byref(kp), ctypes.byref(vp),
                                  ctypes.byref(lp)))
+        dev = f"cuda:{self.device}"
+        if self.paged_blocks is not None and self.layer_kinds[layer] == KV_GLOBAL:
+            pool = (self.paged_blocks, self.Hk, 16, self.D)
+            Kp = torch.as_tensor(_DevArray(kp.value, pool, "<i2"), device=dev).view(torch.bfloat16)
+            Vp = torch.as_tensor(_DevArray(vp.value, pool, "<i2"), device=dev).view(torch.bfloat16)
+            shape = (self.B, self.Hk, self.max_len + 1, self.D)
+            K = torch.zeros(shape, dtype=torch.bfloat16, device=dev)
+            V = torch.zeros(shape, dtype=torch.bfloat16, device=dev)
+            for b in range(self.B):
+                blocks = self.block_table(b)
+                if blocks:
+                    idx = torch.tensor(blocks, device=dev)
+                    n = 16 * len(blocks)
+                    m = min(n, self.max_len + 1)
+                    K[b, :, :m] = Kp[idx].permute(1, 0, 2, 3).reshape(self.Hk, n, self.D)[:, :m]
+                    V[b, :, :m] = Vp[idx].permute(1, 0, 2, 3).reshape(self.Hk, n, self.D)[:, :m]
+            return K, V
         rows = self.R + 1 if self.layer_kinds[layer] == KV_SLIDING else self.max_len + 1
         shape = (self.B, self.Hk, rows, self.D)
-        dev = f"cuda:{self.device}"
         K = torch.as_tensor(_DevArray(kp.value, shape, "<i2"), device=dev).view(torch.bfloat16)
         V = torch.as_tensor(_DevArray(vp.value, shape, "<i2"), device=dev).view(torch.bfloat16)
         return K, V
+
+    def block_table(self, row: int):
+        """Pool blocks of a row in position order (paged caches; [] otherwise)."""
+        n = ctypes.c_int()
+        check(_clib.kv_get_block_table(self._h, row, None, 0, ctypes.byref(n)))
+        buf = (ctypes.c_int32 * max(1, n.value))()
+        check(_clib.kv_get_block_table(self._h, row, buf, n.value, ctypes.byref(n)))
+        return list(buf[:n.value])
+
+    @property
+    def free_blocks(self) -> int:
+        return _clib.kv_free_blocks(self._h)
 
     def lpos(self):
         """Zero-copy view of lpos [B, R] int32 (position held by each ring slot, -1 empty)."""

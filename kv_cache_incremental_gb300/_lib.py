@@ -16,7 +16,7 @@ P_i32 = ctypes.POINTER(ctypes.c_int32)
 
 KV_GLOBAL, KV_SLIDING = 0, 1
 (KV_OK, KV_ERR_ARG, KV_ERR_FULL, KV_ERR_DTYPE, KV_ERR_CUDA, KV_ERR_OOM, KV_ERR_DEVICE,
- KV_ERR_SCRATCH) = range(8)
+ KV_ERR_SCRATCH, KV_ERR_POOL) = range(9)
 KERNELS = {"append": 0, "decode": 1, "combine": 2, "prefill": 3, "commit": 4, "state": 5,
            "step": 6}
 
@@ -24,6 +24,10 @@ KERNELS = {"append": 0, "decode": 1, "combine": 2, "prefill": 3, "commit": 4, "s
 SIGNATURES = {
     "kv_cache_create": (c_int, [ctypes.POINTER(c_void_p), c_int, c_int, c_int, c_int, c_int, c_int,
                                 c_int, P_i32, c_double, c_int]),
+    "kv_cache_create_paged": (c_int, [ctypes.POINTER(c_void_p), c_int, c_int, c_int, c_int, c_int,
+                                      c_int, c_int, P_i32, c_double, c_int, c_int]),
+    "kv_get_block_table": (c_int, [c_void_p, c_int, P_i32, c_int, ctypes.POINTER(c_int)]),
+    "kv_free_blocks": (c_int, [c_void_p]),
     "kv_cache_destroy": (None, [c_void_p]),
     "kv_reset": (c_int, [c_void_p, P_i32, c_int, c_void_p]),
     "kv_append": (c_int, [c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_int, c_int, P_i32, P_i32,
@@ -92,6 +96,8 @@ def check(code: int, what: str = "") -> None:
     if code != KV_OK:
         if code == KV_ERR_FULL:
             raise KVCacheFull(code, what)
+        if code == KV_ERR_POOL:
+            raise KVPoolExhausted(code, what)
         if code == KV_ERR_DTYPE:
             raise TypeError(load().kv_strerror(code).decode())
         raise KVError(code, what)
@@ -99,3 +105,7 @@ def check(code: int, what: str = "") -> None:
 
 class KVCacheFull(KVError, ValueError):
     """lens + n_new > max_len for some row (raised before any write)."""
+
+
+class KVPoolExhausted(KVError):
+    """A paged cache has too few free blocks for the call (raised before any write)."""

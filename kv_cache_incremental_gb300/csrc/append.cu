@@ -87,7 +87,12 @@ __global__ void __launch_bounds__(256) append_kernel(const __grid_constant__ App
 
       __nv_bfloat16 *dk, *dv;
       int64_t dst;
-      if (row.mode == kDestScratch) {
+      if (row.mode == kDestGlobal && p.pt.max_blocks) {  // paged: pads are not stored
+        if (!real) continue;
+        dst = kv_row(p.pt, row.cache_row, p.Hk, g, 0, pos) * p.D;
+        dk = p.cache_k;
+        dv = p.cache_v;
+      } else if (row.mode == kDestScratch) {
         dst = (((int64_t)row.cache_row * p.Hk + g) * kChunk + t) * p.D;
         dk = p.scr_k;
         dv = p.scr_v;
@@ -169,6 +174,19 @@ cudaError_t launch_append(const AppendParams &p, cudaStream_t s) {
 cudaError_t launch_commit(const CommitParams &p, cudaStream_t s) {
   if (p.n_rows <= 0) return cudaSuccess;
   commit_kernel<<<dim3(p.n_rows, p.Hk), 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+// Block-table entries of newly allocated blocks (the values travel in the parameters, so a
+// later change of the host's tables cannot race with this launch).
+__global__ void __launch_bounds__(256) table_kernel(const __grid_constant__ TableParams p) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < p.n; i += gridDim.x * blockDim.x)
+    p.table[(int64_t)p.row[i] * p.max_blocks + p.idx[i]] = p.blk[i];
+}
+
+cudaError_t launch_table(const TableParams &p, cudaStream_t s) {
+  if (p.n <= 0) return cudaSuccess;
+  table_kernel<<<(p.n + 255) / 256, 256, 0, s>>>(p);
   return cudaGetLastError();
 }
 

@@ -246,11 +246,25 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
         uint8_t *kt = tiles + s * Cfg::kStageBytes;
         uint8_t *vt = kt + Cfg::kTileBytes;
         ptx::mbar_arrive_expect_tx(&full[s], Cfg::kStageBytes);
-        const int y = static_cast<int>(row0 + (int64_t)it * kTileKeys);
+        if (p.pt.max_blocks == 0) {
+          const int y = static_cast<int>(row0 + (int64_t)it * kTileKeys);
 #pragma unroll
-        for (int pn = 0; pn < Cfg::kPanels; ++pn) {
-          ptx::tma_load_2d(kt + pn * kTileKeys * 128, &p.tmap_k, pn * 64, y, &full[s]);
-          ptx::tma_load_2d(vt + pn * kTileKeys * 128, &p.tmap_v, pn * 64, y, &full[s]);
+          for (int pn = 0; pn < Cfg::kPanels; ++pn) {
+            ptx::tma_load_2d(kt + pn * kTileKeys * 128, &p.tmap_k, pn * 64, y, &full[s]);
+            ptx::tma_load_2d(vt + pn * kTileKeys * 128, &p.tmap_v, pn * 64, y, &full[s]);
+          }
+        } else {  // paged: four 16-key blocks per tile, each a 16-row box
+          const int4 y4 = kv_rows4(p.pt, row.cache_row, p.Hk, g, k0 + it * kTileKeys);
+          const int ys[4] = {y4.x, y4.y, y4.z, y4.w};
+#pragma unroll
+          for (int j = 0; j < kTileKeys / kBlockTokens; ++j) {
+#pragma unroll
+            for (int pn = 0; pn < Cfg::kPanels; ++pn) {
+              const int off = pn * kTileKeys * 128 + j * kBlockTokens * 128;
+              ptx::tma_load_2d(kt + off, &p.tmap_k, pn * 64, ys[j], &full[s]);
+              ptx::tma_load_2d(vt + off, &p.tmap_v, pn * 64, ys[j], &full[s]);
+            }
+          }
         }
         *issued = it + 1;
       }
@@ -414,7 +428,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
   }
   if (owner) {
     // Every load of this CTA has landed: store the new key and value in the cache.
-    const int64_t dst = (((int64_t)row.cache_row * p.Hk + g) * p.seg_rows + row.slot) * D;
+    const int64_t dst = kv_row(p.pt, row.cache_row, p.Hk, g, p.seg_rows, row.slot) * D;
     for (int ch = threadIdx.x; ch < D / 8; ch += kConsumerWarps * 32) {
       *reinterpret_cast<uint4 *>(p.cache_k + dst + 8 * ch) =
           *reinterpret_cast<const uint4 *>(knew + 8 * ch);

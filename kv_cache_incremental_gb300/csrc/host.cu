@@ -47,12 +47,12 @@ EncodeTiledFn get_encode_fn() {
 }
 
 // 2-D bf16 view [rows][D] with 64-column x kTileKeys-row boxes, 128-byte swizzle.
-bool make_tmap(CUtensorMap *m, void *base, int64_t rows, int D) {
+bool make_tmap(CUtensorMap *m, void *base, int64_t rows, int D, int box_rows = kTileKeys) {
   EncodeTiledFn fn = get_encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-  cuuint32_t box[2] = {64, (cuuint32_t)kTileKeys};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -106,11 +106,72 @@ struct kv_cache {
   bool prof = false;
   std::vector<ProfRec> recs;
   std::vector<cudaEvent_t> free_events;
+  // paged global layers: per layer a pool of n_blocks blocks of [Hk][16][D]; one block
+  // table for all of them (their rows always have equal lengths)
+  int n_blocks = 0;                           // 0: dense cache
+  int max_blocks = 0;                         // table entries per row, a multiple of 4
+  int32_t *table = nullptr;                   // device [B][max_blocks]
+  std::vector<std::vector<int32_t>> rblocks;  // host: pool blocks of each row, in order
+  std::vector<int32_t> free_blocks;           // host: free pool blocks
 };
 
 namespace {
 
 int set_err(cudaError_t e) { return e == cudaSuccess ? KV_OK : KV_ERR_CUDA; }
+
+bool paged_layer(const kv_cache *c, int layer) {
+  return c->n_blocks > 0 && c->kind[layer] == KV_GLOBAL;
+}
+
+PageTable page_table(const kv_cache *c, int layer) {
+  PageTable pt;
+  pt.table = paged_layer(c, layer) ? c->table : nullptr;
+  pt.max_blocks = paged_layer(c, layer) ? c->max_blocks : 0;
+  return pt;
+}
+
+int blocks_for(int len) { return (len + kBlockTokens - 1) / kBlockTokens; }
+
+// Give each (row, length) of `want` the pool blocks its first `length` positions need, and
+// write the new table entries on `s`.  All or nothing: KV_ERR_POOL before any change if the
+// pool cannot supply every row.
+int ensure_blocks(kv_cache *c, const std::vector<std::pair<int, int>> &want, cudaStream_t s) {
+  if (c->n_blocks == 0) return KV_OK;
+  int64_t need = 0;
+  for (auto &w : want) need += std::max(0, blocks_for(w.second) - (int)c->rblocks[w.first].size());
+  if (need > (int64_t)c->free_blocks.size()) return KV_ERR_POOL;
+  if (need == 0) return KV_OK;
+  static thread_local TableParams tp;
+  tp.table = c->table;
+  tp.max_blocks = c->max_blocks;
+  tp.n = 0;
+  for (auto &w : want) {
+    auto &rb = c->rblocks[w.first];
+    while ((int)rb.size() < blocks_for(w.second)) {
+      const int blk = c->free_blocks.back();
+      c->free_blocks.pop_back();
+      tp.row[tp.n] = w.first;
+      tp.idx[tp.n] = (int)rb.size();
+      tp.blk[tp.n] = blk;
+      rb.push_back(blk);
+      if (++tp.n == kMaxTableEntries) {
+        if (launch_table(tp, s) != cudaSuccess) return KV_ERR_CUDA;
+        tp.n = 0;
+      }
+    }
+  }
+  return launch_table(tp, s) == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+}
+
+// Return the blocks of `row` past its first `len` positions to the pool.
+void release_blocks(kv_cache *c, int row, int len) {
+  if (c->n_blocks == 0) return;
+  auto &rb = c->rblocks[row];
+  while ((int)rb.size() > blocks_for(len)) {
+    c->free_blocks.push_back(rb.back());
+    rb.pop_back();
+  }
+}
 
 cudaEvent_t take_event(kv_cache *c) {
   if (!c->free_events.empty()) {
@@ -233,6 +294,7 @@ void fill_decode(const kv_cache *c, int layer, const __nv_bfloat16 *q, const __n
   dp.rep = c->Hq / c->Hk;
   dp.seg_rows = c->seg_rows[layer];
   dp.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c->D));
+  dp.pt = page_table(c, layer);
   double kvb = 0;
   plan_decode(c, sliding, batch, dp, kvb, flops);
   // q, k, v in; new K and V and the output out
@@ -248,6 +310,13 @@ int append_device(kv_cache *c, int layer, const __nv_bfloat16 *q, const __nv_bfl
   int max_n = 0;
   for (int i = 0; i < Bs; ++i) max_n = std::max(max_n, (int)n_new[i]);
   if (max_n == 0) return KV_OK;
+  if (c->n_blocks > 0) {  // pool blocks for the new positions, before anything is enqueued
+    std::vector<std::pair<int, int>> want;
+    for (int i = 0; i < Bs; ++i)
+      if (n_new[i] > 0) want.push_back({cache_rows[i], c->lens[cache_rows[i]] + n_new[i]});
+    const int rc = ensure_blocks(c, want, s);
+    if (rc != KV_OK) return rc;
+  }
 
   const int64_t q_row = (int64_t)C * Hq * D, kv_row = (int64_t)C * Hk * D;
   static thread_local AppendParams ap;
@@ -289,6 +358,7 @@ int append_device(kv_cache *c, int layer, const __nv_bfloat16 *q, const __nv_bfl
       ap.ring_R = c->R;
       ap.max_len = c->max_len;
       ap.c_avail = C - off;
+      ap.pt = page_table(c, layer);
       int blk = 0;
       double bytes = 0;
       for (size_t j = r0; j < r1; ++j) {
@@ -344,6 +414,7 @@ int append_device(kv_cache *c, int layer, const __nv_bfloat16 *q, const __nv_bfl
         pp.ring_R = c->R;
         pp.window = c->W;
         pp.scale_log2 = scale_log2;
+        pp.pt = page_table(c, layer);
         int cta = 0;
         double bytes = 0, fl = 0;
         for (size_t j = r0; j < r1; ++j) {
@@ -438,6 +509,7 @@ void free_all(kv_cache *c) {
   cudaFree(c->part_o);
   cudaFree(c->part_ml);
   cudaFree(c->stage);
+  cudaFree(c->table);
   for (auto &r : c->recs) {
     cudaEventDestroy(r.a);
     cudaEventDestroy(r.b);
@@ -449,10 +521,14 @@ void free_all(kv_cache *c) {
 
 extern "C" {
 
-int kv_cache_create(kv_cache **out, int B, int max_len, int Hq, int Hk, int D, int W,
-                    int n_layers, const int32_t *layer_kind, double rope_theta, int device) {
+}  // extern "C"
+
+static int create_impl(kv_cache **out, int B, int max_len, int Hq, int Hk, int D, int W,
+                       int n_layers, const int32_t *layer_kind, double rope_theta, int device,
+                       int n_blocks) {
   if (!out) return KV_ERR_ARG;
   *out = nullptr;
+  if (n_blocks < 0 || (int64_t)n_blocks * Hk * kBlockTokens >= (1LL << 31)) return KV_ERR_ARG;
   if (B < 1 || max_len < 1 || max_len > (1 << 20) || Hk < 1 || Hq < 1 || Hq % Hk != 0 ||
       Hq / Hk > kMaxRep || (D != 64 && D != 128) || n_layers < 1 || !layer_kind ||
       !(rope_theta > 0.0) || device < 0)
@@ -464,7 +540,8 @@ int kv_cache_create(kv_cache **out, int B, int max_len, int Hq, int Hk, int D, i
   }
   if (any_sliding && W < 1) return KV_ERR_ARG;
   const int R = any_sliding ? (W < max_len ? W : max_len) : 0;
-  if ((int64_t)B * Hk * (max_len + 1) >= (1LL << 31)) return KV_ERR_ARG;  // TMA coordinates
+  if (n_blocks == 0 && (int64_t)B * Hk * (max_len + 1) >= (1LL << 31))
+    return KV_ERR_ARG;  // TMA coordinates
 
   int n_dev = 0;
   if (cudaGetDeviceCount(&n_dev) != cudaSuccess || device >= n_dev) return KV_ERR_CUDA;
@@ -500,9 +577,19 @@ int kv_cache_create(kv_cache **out, int B, int max_len, int Hq, int Hk, int D, i
     return cudaMemset(*p, 0, bytes) == cudaSuccess;  // stale slots stay finite
   };
 
+  c->n_blocks = n_blocks;
+  if (n_blocks > 0) {
+    c->max_blocks = (blocks_for(max_len) + 3) / 4 * 4;
+    if (!alloc((void **)&c->table, (size_t)B * c->max_blocks * 4)) return fail(KV_ERR_OOM);
+    c->rblocks.assign(B, {});
+    for (int b = n_blocks - 1; b >= 0; --b) c->free_blocks.push_back(b);
+  }
   for (int l = 0; l < n_layers; ++l) {
-    const int rows = c->kind[l] == KV_SLIDING ? R + 1 : max_len + 1;
-    const size_t bytes = (size_t)B * Hk * rows * D * 2;
+    // dense: [B][Hk][rows][D]; paged global layer: pool [n_blocks][Hk][16][D]
+    const bool pg = n_blocks > 0 && c->kind[l] == KV_GLOBAL;
+    const int rows = pg ? kBlockTokens : c->kind[l] == KV_SLIDING ? R + 1 : max_len + 1;
+    const int64_t units = pg ? n_blocks : B;
+    const size_t bytes = (size_t)units * Hk * rows * D * 2;
     void *k = nullptr, *v = nullptr;
     if (!alloc(&k, bytes)) return fail(KV_ERR_OOM);
     c->K.push_back(k);
@@ -510,7 +597,8 @@ int kv_cache_create(kv_cache **out, int B, int max_len, int Hq, int Hk, int D, i
     c->V.push_back(v);
     c->seg_rows.push_back(rows);
     CUtensorMap mk, mv;
-    if (!make_tmap(&mk, k, (int64_t)B * Hk * rows, D) || !make_tmap(&mv, v, (int64_t)B * Hk * rows, D))
+    const int box = pg ? kBlockTokens : kTileKeys;
+    if (!make_tmap(&mk, k, units * Hk * rows, D, box) || !make_tmap(&mv, v, units * Hk * rows, D, box))
       return fail(KV_ERR_CUDA);
     c->tmK.push_back(mk);
     c->tmV.push_back(mv);
@@ -558,6 +646,35 @@ int kv_cache_create(kv_cache **out, int B, int max_len, int Hq, int Hk, int D, i
   return KV_OK;
 }
 
+extern "C" {
+
+int kv_cache_create(kv_cache **out, int B, int max_len, int Hq, int Hk, int D, int W,
+                    int n_layers, const int32_t *layer_kind, double rope_theta, int device) {
+  return create_impl(out, B, max_len, Hq, Hk, D, W, n_layers, layer_kind, rope_theta, device, 0);
+}
+
+int kv_cache_create_paged(kv_cache **out, int B, int max_len, int Hq, int Hk, int D, int W,
+                          int n_layers, const int32_t *layer_kind, double rope_theta, int device,
+                          int n_blocks) {
+  if (n_blocks < 1) return KV_ERR_ARG;
+  return create_impl(out, B, max_len, Hq, Hk, D, W, n_layers, layer_kind, rope_theta, device,
+                     n_blocks);
+}
+
+int kv_get_block_table(const kv_cache *c, int row, int32_t *blocks_out, int capacity,
+                       int *n_out) {
+  if (!c || row < 0 || row >= c->B || capacity < 0 || (capacity > 0 && !blocks_out))
+    return KV_ERR_ARG;
+  const int n = c->n_blocks > 0 ? (int)c->rblocks[row].size() : 0;
+  if (n_out) *n_out = n;
+  for (int i = 0; i < n && i < capacity; ++i) blocks_out[i] = c->rblocks[row][i];
+  return KV_OK;
+}
+
+int kv_free_blocks(const kv_cache *c) {
+  return c ? (int)c->free_blocks.size() : -1;
+}
+
 void kv_cache_destroy(kv_cache *c) {
   if (!c) return;
   DeviceGuard guard(c->device);
@@ -578,7 +695,10 @@ int kv_reset(kv_cache *c, const int32_t *rows, int n_rows, void *stream) {
   DeviceGuard guard(c->device);
   const int rc = state_update(c, rv, nullptr, true, (cudaStream_t)stream);
   if (rc != KV_OK) return rc;
-  for (int r : rv) c->lens[r] = 0;
+  for (int r : rv) {
+    c->lens[r] = 0;
+    release_blocks(c, r, 0);  // later launches on this stream may reuse them
+  }
   return KV_OK;
 }
 
@@ -674,7 +794,8 @@ int64_t kv_nbytes(const kv_cache *c) {
   if (!c) return -1;
   int64_t total = 0;
   for (int l = 0; l < c->n_layers; ++l)
-    total += 2LL * c->B * c->Hk * c->seg_rows[l] * c->D * 2;
+    total += paged_layer(c, l) ? 2LL * c->n_blocks * c->Hk * kBlockTokens * c->D * 2
+                               : 2LL * c->B * c->Hk * c->seg_rows[l] * c->D * 2;
   return total;
 }
 
@@ -904,6 +1025,12 @@ int kv_step_graph_launch(kv_step_graph *g, void *stream) {
     if ((int64_t)c->lens[r] + 1 > c->max_len) return KV_ERR_FULL;
   DeviceGuard guard(c->device);
   cudaStream_t s = (cudaStream_t)stream;
+  if (c->n_blocks > 0) {  // the new position's block, written to the table before the replay
+    std::vector<std::pair<int, int>> want;
+    for (int r : g->rows) want.push_back({r, c->lens[r] + 1});
+    const int rc = ensure_blocks(c, want, s);
+    if (rc != KV_OK) return rc;
+  }
   plan_step(g);
   const int nt = c->Hq / c->Hk <= 8 ? 1 : 2;
   for (int l = 0; l < c->n_layers; ++l) {
@@ -945,12 +1072,21 @@ int first_kept(const kv_cache *c, int layer, int keep) {
 }
 
 // Storage block of (row, layer): K, V and the element stride between heads.
+// A paged global layer returns its pool and the row's block-table row instead.
 void row_block(const kv_cache *c, int layer, int row, __nv_bfloat16 *&k, __nv_bfloat16 *&v,
-               int64_t &head_stride) {
+               int64_t &head_stride, const int32_t *&table) {
+  if (paged_layer(c, layer)) {
+    k = (__nv_bfloat16 *)c->K[layer];
+    v = (__nv_bfloat16 *)c->V[layer];
+    head_stride = 0;
+    table = c->table + (int64_t)row * c->max_blocks;
+    return;
+  }
   const int64_t off = (int64_t)row * c->Hk * c->seg_rows[layer] * c->D;
   k = (__nv_bfloat16 *)c->K[layer] + off;
   v = (__nv_bfloat16 *)c->V[layer] + off;
   head_stride = (int64_t)c->seg_rows[layer] * c->D;
+  table = nullptr;
 }
 
 // Can the source row, at length `lens`, supply every position a destination of length `keep`
@@ -1023,6 +1159,12 @@ int kv_copy_rows(kv_cache *dst, const int32_t *dst_rows, const kv_cache *src,
   if (n == 0) return KV_OK;
   DeviceGuard guard(dst->device);
   cudaStream_t s = (cudaStream_t)stream;
+  {  // destination blocks for [0, keep) (all or nothing, before any copy is enqueued)
+    std::vector<std::pair<int, int>> want;
+    for (int i = 0; i < n; ++i) want.push_back({dst_rows[i], kp[i]});
+    const int rc = ensure_blocks(dst, want, s);
+    if (rc != KV_OK) return rc;
+  }
   static thread_local CopyParams cp;
   cp.Hk = dst->Hk;
   cp.D = dst->D;
@@ -1032,10 +1174,10 @@ int kv_copy_rows(kv_cache *dst, const int32_t *dst_rows, const kv_cache *src,
     for (int l = 0; l < dst->n_layers; ++l) {
       CopyItem it;
       __nv_bfloat16 *sk, *sv;
-      row_block(src, l, src_rows[i], sk, sv, it.src_head_stride);
+      row_block(src, l, src_rows[i], sk, sv, it.src_head_stride, it.src_table);
       it.src_k = sk;
       it.src_v = sv;
-      row_block(dst, l, dst_rows[i], it.dst_k, it.dst_v, it.dst_head_stride);
+      row_block(dst, l, dst_rows[i], it.dst_k, it.dst_v, it.dst_head_stride, it.dst_table);
       const bool ring = dst->kind[l] == KV_SLIDING;
       it.p0 = first_kept(dst, l, kp[i]);
       it.p1 = kp[i];
@@ -1048,7 +1190,10 @@ int kv_copy_rows(kv_cache *dst, const int32_t *dst_rows, const kv_cache *src,
   if (cp.n_items && flush_copies(cp, s) != KV_OK) return KV_ERR_CUDA;
   std::vector<int32_t> rows(dst_rows, dst_rows + n);
   if (set_ring_state(dst, rows, kp, s) != KV_OK) return KV_ERR_CUDA;
-  for (int i = 0; i < n; ++i) dst->lens[dst_rows[i]] = kp[i];
+  for (int i = 0; i < n; ++i) {
+    dst->lens[dst_rows[i]] = kp[i];
+    release_blocks(dst, dst_rows[i], kp[i]);  // a shortened row gives its tail back
+  }
   return KV_OK;
 }
 
@@ -1075,7 +1220,8 @@ static int export_import(kv_cache *c, int row, int keep, void *buf, int64_t byte
     const int64_t blk = (int64_t)c->Hk * np * c->D;
     __nv_bfloat16 *rk, *rv;
     int64_t hs;
-    row_block(c, l, row, rk, rv, hs);
+    const int32_t *tab;
+    row_block(c, l, row, rk, rv, hs, tab);
     const int ring = c->kind[l] == KV_SLIDING ? c->R : 0;
     CopyItem it;
     it.p0 = p0;
@@ -1084,22 +1230,26 @@ static int export_import(kv_cache *c, int row, int keep, void *buf, int64_t byte
       it.src_k = rk;
       it.src_v = rv;
       it.src_head_stride = hs;
+      it.src_table = tab;
       it.src_ring = ring;
       it.src_base = 0;
       it.dst_k = b + off;
       it.dst_v = b + off + blk;
       it.dst_head_stride = (int64_t)np * c->D;
+      it.dst_table = nullptr;
       it.dst_ring = 0;
       it.dst_base = p0;
     } else {
       it.src_k = b + off;
       it.src_v = b + off + blk;
       it.src_head_stride = (int64_t)np * c->D;
+      it.src_table = nullptr;
       it.src_ring = 0;
       it.src_base = p0;
       it.dst_k = rk;
       it.dst_v = rv;
       it.dst_head_stride = hs;
+      it.dst_table = tab;
       it.dst_ring = ring;
       it.dst_base = 0;
     }
@@ -1125,10 +1275,13 @@ int kv_import_row(kv_cache *c, int row, int keep, const void *src, int64_t bytes
   if (keep < 0 || keep > c->max_len || bytes != kv_export_bytes(c, keep)) return KV_ERR_ARG;
   DeviceGuard guard(c->device);
   cudaStream_t s = (cudaStream_t)stream;
-  const int rc = export_import(c, row, keep, const_cast<void *>(src), bytes, s, false);
+  int rc = ensure_blocks(c, {{row, keep}}, s);
+  if (rc != KV_OK) return rc;
+  rc = export_import(c, row, keep, const_cast<void *>(src), bytes, s, false);
   if (rc != KV_OK) return rc;
   if (set_ring_state(c, {row}, {keep}, s) != KV_OK) return KV_ERR_CUDA;
   c->lens[row] = keep;
+  release_blocks(c, row, keep);
   return KV_OK;
 }
 
@@ -1142,6 +1295,7 @@ const char *kv_strerror(int code) {
     case KV_ERR_OOM: return "KV_ERR_OOM: device allocation failed";
     case KV_ERR_DEVICE: return "KV_ERR_DEVICE: a kernel reported a timed-out wait";
     case KV_ERR_SCRATCH: return "KV_ERR_SCRATCH: request exceeds the fixed no-allocation scratch";
+    case KV_ERR_POOL: return "KV_ERR_POOL: no free block in the paged cache's pool";
     default: return "unknown kv status";
   }
 }

@@ -25,6 +25,36 @@ constexpr int kMaxRep = 16;
 // reaching it sets the device error word and abandons the work item.
 constexpr uint32_t kWaitLimit = 1u << 24;
 
+// Paged global layers: a row's key slots are grouped in blocks of kBlockTokens, each block
+// a [Hk][kBlockTokens][D] piece of the layer's block pool, found through the row's block
+// table (shared by all global layers of the cache: their rows have the same lengths).
+constexpr int kBlockTokens = 16;
+struct PageTable {
+  const int32_t *table;  // [B][max_blocks] pool block of each block of a row
+  int max_blocks;        // 0: the layer's storage is dense [B][Hk][seg_rows][D]
+};
+
+// Row of key slot `slot` of (row, kv head g) in the 2-D [rows][D] view of a layer's storage:
+// dense (row * Hk + g) * seg_rows + slot; paged (table[row][slot / 16] * Hk + g) * 16 + slot % 16.
+// A slot past the table (only masked keys) reads the row's last table entry.
+__device__ __forceinline__ int64_t kv_row(const PageTable &pt, int row, int Hk, int g,
+                                          int seg_rows, int slot) {
+  if (pt.max_blocks == 0) return ((int64_t)row * Hk + g) * seg_rows + slot;
+  const int idx = min(slot / kBlockTokens, pt.max_blocks - 1);
+  const int64_t blk = pt.table[(int64_t)row * pt.max_blocks + idx];
+  return (blk * Hk + g) * kBlockTokens + slot % kBlockTokens;
+}
+
+// Storage rows of the four 16-key blocks of the 64-key tile at `slot0` (a multiple of 64) of
+// (row, kv head g) in a paged layer, with one 16-byte table load (the table's rows are padded
+// to a multiple of 4 entries and every entry holds a valid pool block).
+__device__ __forceinline__ int4 kv_rows4(const PageTable &pt, int row, int Hk, int g, int slot0) {
+  const int4 b = *reinterpret_cast<const int4 *>(pt.table + (int64_t)row * pt.max_blocks +
+                                                 slot0 / kBlockTokens);
+  return make_int4((b.x * Hk + g) * kBlockTokens, (b.y * Hk + g) * kBlockTokens,
+                   (b.z * Hk + g) * kBlockTokens, (b.w * Hk + g) * kBlockTokens);
+}
+
 enum DestMode : int32_t {
   kDestGlobal = 0,   // cache slot lens + t (pads: scratch slot max_len)
   kDestRing = 1,     // ring slot (lens + t) % R (pads: scratch slot R)
@@ -57,6 +87,7 @@ struct AppendParams {
   int c_avail;             // tokens per call row present in the tensors from the sub-chunk on
   int n_rows;
   int n_blocks;            // token blocks in the grid
+  PageTable pt;            // paged global layer: pads are not written
   AppendRow rows[kMaxRowsPerLaunch];
 };
 
@@ -96,6 +127,7 @@ struct DecodeParams {  // 64-byte aligned through its CUtensorMap members
   int Hq, Hk, rep, seg_rows;
   int n_rows, n_items;
   float scale_log2;         // log2(e) / sqrt(D)
+  PageTable pt;             // paged global layer: tmap_k/v boxes are 16 rows
   DecodeRow rows[kMaxRowsPerLaunch];
 };
 
@@ -124,6 +156,7 @@ struct PrefillParams {  // 64-byte aligned through its CUtensorMap members
   int ring_R, window;
   int n_rows, n_ctas;
   float scale_log2;
+  PageTable pt;             // paged global layer: tmap_k/v boxes are 16 rows
   PrefillRow rows[kMaxRowsPerLaunch];
 };
 
@@ -152,10 +185,13 @@ struct StateParams {
 // One (row, layer) block of K/V positions [p0, p1) copied from one storage to another.
 // A storage is [Hk][slots][D] per (row, layer) at `k`/`v` with `head_stride` elements
 // between heads; position p sits at slot p % ring (ring > 0) or p - base (ring == 0).
+// A paged side (table != nullptr: the row's block-table row) has `k`/`v` at its pool's
+// start and position p at pool row (table[p / 16] * Hk + h) * 16 + p % 16.
 struct CopyItem {
   const __nv_bfloat16 *src_k, *src_v;
   __nv_bfloat16 *dst_k, *dst_v;
   int64_t src_head_stride, dst_head_stride;
+  const int32_t *src_table, *dst_table;
   int32_t p0, p1;
   int32_t src_ring, src_base, dst_ring, dst_base;
 };
@@ -166,8 +202,18 @@ struct CopyParams {
   CopyItem items[kMaxCopyItems];
 };
 
+// ---------------------------------------------------------------- block tables
+constexpr int kMaxTableEntries = 2048;
+struct TableParams {
+  int32_t *table;  // [B][max_blocks]
+  int max_blocks;
+  int n;
+  int32_t row[kMaxTableEntries], idx[kMaxTableEntries], blk[kMaxTableEntries];
+};
+
 // ---------------------------------------------------------------- launchers
 cudaError_t launch_copy(const CopyParams &p, cudaStream_t s);
+cudaError_t launch_table(const TableParams &p, cudaStream_t s);
 cudaError_t launch_append(const AppendParams &p, cudaStream_t s);
 cudaError_t launch_decode(const DecodeParams &p, int D, int n_tiles_heads, cudaStream_t s);
 // Graph kernel-node descriptions of the decode and state launches (args: one-slot storage

@@ -11,8 +11,12 @@
 namespace kvinc {
 namespace {
 
-__device__ __forceinline__ int64_t slot_of(int p, int ring, int base) {
-  return ring > 0 ? p % ring : p - base;
+// Element offset of position p, head h of one side of a copy.
+__device__ __forceinline__ int64_t elem_of(int p, int h, int Hk, int D, const int32_t *table,
+                                           int64_t head_stride, int ring, int base) {
+  if (table)
+    return (((int64_t)table[p / kBlockTokens] * Hk + h) * kBlockTokens + p % kBlockTokens) * D;
+  return h * head_stride + (int64_t)(ring > 0 ? p % ring : p - base) * D;
 }
 
 // grid (items, Hk): one CTA per (item, kv head); 16-byte chunks of K and V, every load of
@@ -22,10 +26,8 @@ __global__ void __launch_bounds__(256) copy_kernel(const __grid_constant__ CopyP
   const int h = blockIdx.y;
   const int vec = p.D / 8;
   const int units = (it.p1 - it.p0) * vec;
-  const __nv_bfloat16 *sk = it.src_k + h * it.src_head_stride;
-  const __nv_bfloat16 *sv = it.src_v + h * it.src_head_stride;
-  __nv_bfloat16 *dk = it.dst_k + h * it.dst_head_stride;
-  __nv_bfloat16 *dv = it.dst_v + h * it.dst_head_stride;
+  const __nv_bfloat16 *sk = it.src_k, *sv = it.src_v;
+  __nv_bfloat16 *dk = it.dst_k, *dv = it.dst_v;
   constexpr int kPer = 4;
   for (int u0 = threadIdx.x; u0 < units; u0 += kPer * blockDim.x) {
     uint4 kk[kPer], vv[kPer];
@@ -34,7 +36,9 @@ __global__ void __launch_bounds__(256) copy_kernel(const __grid_constant__ CopyP
       const int u = u0 + i * blockDim.x;
       if (u >= units) continue;
       const int pos = it.p0 + u / vec, c = u % vec;
-      const int64_t s = slot_of(pos, it.src_ring, it.src_base) * p.D + 8 * c;
+      const int64_t s =
+          elem_of(pos, h, p.Hk, p.D, it.src_table, it.src_head_stride, it.src_ring, it.src_base) +
+          8 * c;
       kk[i] = *reinterpret_cast<const uint4 *>(sk + s);
       vv[i] = *reinterpret_cast<const uint4 *>(sv + s);
     }
@@ -43,7 +47,9 @@ __global__ void __launch_bounds__(256) copy_kernel(const __grid_constant__ CopyP
       const int u = u0 + i * blockDim.x;
       if (u >= units) continue;
       const int pos = it.p0 + u / vec, c = u % vec;
-      const int64_t d = slot_of(pos, it.dst_ring, it.dst_base) * p.D + 8 * c;
+      const int64_t d =
+          elem_of(pos, h, p.Hk, p.D, it.dst_table, it.dst_head_stride, it.dst_ring, it.dst_base) +
+          8 * c;
       *reinterpret_cast<uint4 *>(dk + d) = kk[i];
       *reinterpret_cast<uint4 *>(dv + d) = vv[i];
     }

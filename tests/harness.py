@@ -44,10 +44,11 @@ class Scenario:
     """One cache plus the bookkeeping needed to regenerate every row's history."""
 
     def __init__(self, B, max_len, Hq, Hk, D, W=0, kinds=(0,), theta=1e4, seed=0, device=0,
-                 pad_value=None):
+                 pad_value=None, paged_blocks=None):
         import kv_cache_incremental_gb300 as kvi
         self.kvi = kvi
-        self.cache = kvi.KVCache(B, max_len, Hq, Hk, D, W, list(kinds), theta, device)
+        self.cache = kvi.KVCache(B, max_len, Hq, Hk, D, W, list(kinds), theta, device,
+                                 paged_blocks=paged_blocks)
         self.B, self.max_len, self.Hq, self.Hk, self.D, self.W = B, max_len, Hq, Hk, D, W
         self.kinds = list(kinds)
         self.theta, self.seed = theta, seed
