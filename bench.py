@@ -56,6 +56,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--fill-only", action="store_true",
                     help="time only the chunked-prefill cache fill of one cache (TFLOP/s)")
+    ap.add_argument("--paged", action="store_true",
+                    help="global layers in a paged cache (16-position blocks, a pool as large "
+                         "as the dense cache)")
     ap.add_argument("--fill-to", type=int, default=0,
                     help="fill every row to this length instead of the workload's length "
                          "draw (small cases for profiling)")
@@ -346,7 +349,9 @@ def run_fill_only(args):
     torch.cuda.set_device(0)
     stream = torch.cuda.current_stream()
     B, Hq, Hk, D = cfg["B"], cfg["Hq"], cfg["Hk"], cfg["D"]
-    c = kvi.KVCache(B, cfg["max_len"], Hq, Hk, D, cfg["W"], cfg["kinds"], 1e4, 0)
+    pool = B * ((cfg["max_len"] + 15) // 16) if args.paged else None
+    c = kvi.KVCache(B, cfg["max_len"], Hq, Hk, D, cfg["W"], cfg["kinds"], 1e4, 0,
+                    paged_blocks=pool)
     if args.fill_to:
         target = np.full(B, args.fill_to, dtype=np.int64)
     else:
@@ -368,7 +373,8 @@ def run_fill_only(args):
         "metric": "chunked-prefill TFLOP/s (cache fill, 64-token chunks)", "value": tflops,
         "unit": "TFLOP/s", "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": args.workload, "B": B, "Hq": Hq, "Hk": Hk, "D": D,
-                   "layers": len(cfg["kinds"]), "fill_to": int(target.max())},
+                   "layers": len(cfg["kinds"]), "fill_to": int(target.max()),
+                   "paged": bool(args.paged)},
         "frac_of_bf16_sustained": tflops / peak_tflops() if tflops else None,
         "kernels": {"prefill": pre, "append": app, "commit": com}, "wall_s": wall,
         "flops_counted": "4*Hq*D per visible (query, key) pair, causal only"}), flush=True)
@@ -429,7 +435,9 @@ def run_ours(args):
     pre = {"launches": 0, "ms": 0.0, "bytes": 0.0, "flops": 0.0}
     for r in range(rounds):
         seed_r = args.seed + 7919 * rank + 104729 * r
-        c = kvi.KVCache(B, cfg["max_len"], Hq, Hk, D, cfg["W"], cfg["kinds"], 1e4, local_rank)
+        pool = B * ((cfg["max_len"] + 15) // 16) if args.paged else None
+        c = kvi.KVCache(B, cfg["max_len"], Hq, Hk, D, cfg["W"], cfg["kinds"], 1e4, local_rank,
+                        paged_blocks=pool)
         l0 = initial_lens(cfg, reserve, seed_r)
         if args.fill_to:  # small-case profiling: every row at the same, shorter length
             l0 = np.full(B, min(args.fill_to, cfg["max_len"] - reserve - 1), dtype=np.int64)
@@ -622,6 +630,7 @@ def run_ours(args):
                    "window": cfg["W"] or None,
                    "lens": f"U[{cfg['lo']}, {cfg['max_len'] - reserve - 1}] per cache",
                    "caches": rounds, "steps_per_cache": per_round,
+                   "paged": bool(args.paged),
                    "l2": "inputs larger than L2 (K/V read per step >> 129 MB)",
                    "parallelism": f"replicas x{world}"},
         "tokens_per_s": tok_s,

@@ -95,7 +95,8 @@ int kv_cache_create(kv_cache **out, int B, int max_len, int Hq, int Hk, int D, i
 
 /*
  * Paged cache: as kv_cache_create, but every global layer keeps its K/V in a pool of
- * n_blocks blocks of 16 positions ([Hk][16][D] bf16 each) and each row a table of the
+ * n_blocks blocks of 16 positions (bf16 [Hk][n_blocks][16][D]: head-major, so that a
+ * row's consecutive blocks are contiguous per head) and each row a table of the
  * blocks that hold its positions 16i..16i+15, shared by all global layers (a row has
  * the same length on all of them) ("Lab 07 -- KV cache and sampling", Going further:
  * fixed 16-token blocks plus a per-sequence block table; "tinyllm/kv_cache.py": a
@@ -201,7 +202,7 @@ int kv_get_lens(const kv_cache *c, int32_t *lens_out);
 /* Device pointers of a layer's K and V storage and of lpos ([B][R] int32, or
  * NULL without sliding layers), for inspection and tests.  Layouts as in
  * kv_cache_create; a paged cache's global layers point at their block pools
- * ([n_blocks][Hk][16][D], see kv_get_block_table).  The pointers stay owned by the
+ * ([Hk][n_blocks][16][D], see kv_get_block_table).  The pointers stay owned by the
  * cache. */
 int kv_debug_ptrs(const kv_cache *c, int layer, void **K, void **V, int32_t **lpos);
 

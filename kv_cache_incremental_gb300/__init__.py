@@ -211,9 +211,10 @@ class KVCache:
                                  ctypes.byref(lp)))
         dev = f"cuda:{self.device}"
         if self.paged_blocks is not None and self.layer_kinds[layer] == KV_GLOBAL:
-            pool = (self.paged_blocks, self.Hk, 16, self.D)
+            pool = (self.Hk, self.paged_blocks, 16, self.D)   # head-major pool
             Kp = torch.as_tensor(_DevArray(kp.value, pool, "<i2"), device=dev).view(torch.bfloat16)
             Vp = torch.as_tensor(_DevArray(vp.value, pool, "<i2"), device=dev).view(torch.bfloat16)
+            Kp, Vp = Kp.transpose(0, 1), Vp.transpose(0, 1)  # [block][Hk][16][D]
             shape = (self.B, self.Hk, self.max_len + 1, self.D)
             K = torch.zeros(shape, dtype=torch.bfloat16, device=dev)
             V = torch.zeros(shape, dtype=torch.bfloat16, device=dev)

@@ -253,16 +253,24 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
             ptx::tma_load_2d(kt + pn * kTileKeys * 128, &p.tmap_k, pn * 64, y, &full[s]);
             ptx::tma_load_2d(vt + pn * kTileKeys * 128, &p.tmap_v, pn * 64, y, &full[s]);
           }
-        } else {  // paged: four 16-key blocks per tile, each a 16-row box
-          const int4 y4 = kv_rows4(p.pt, row.cache_row, p.Hk, g, k0 + it * kTileKeys);
-          const int ys[4] = {y4.x, y4.y, y4.z, y4.w};
-#pragma unroll
-          for (int j = 0; j < kTileKeys / kBlockTokens; ++j) {
+        } else {  // paged: the tile's four 16-key blocks, one box when consecutive
+          const int4 y4 = kv_rows4(p.pt, row.cache_row, g, k0 + it * kTileKeys);
+          if (rows4_contiguous(y4)) {
 #pragma unroll
             for (int pn = 0; pn < Cfg::kPanels; ++pn) {
-              const int off = pn * kTileKeys * 128 + j * kBlockTokens * 128;
-              ptx::tma_load_2d(kt + off, &p.tmap_k, pn * 64, ys[j], &full[s]);
-              ptx::tma_load_2d(vt + off, &p.tmap_v, pn * 64, ys[j], &full[s]);
+              ptx::tma_load_2d(kt + pn * kTileKeys * 128, &p.tmap_k, pn * 64, y4.x, &full[s]);
+              ptx::tma_load_2d(vt + pn * kTileKeys * 128, &p.tmap_v, pn * 64, y4.x, &full[s]);
+            }
+          } else {
+            const int ys[4] = {y4.x, y4.y, y4.z, y4.w};
+#pragma unroll
+            for (int j = 0; j < kTileKeys / kBlockTokens; ++j) {
+#pragma unroll
+              for (int pn = 0; pn < Cfg::kPanels; ++pn) {
+                const int off = pn * kTileKeys * 128 + j * kBlockTokens * 128;
+                ptx::tma_load_2d(kt + off, &p.tmap_k16, pn * 64, ys[j], &full[s]);
+                ptx::tma_load_2d(vt + off, &p.tmap_v16, pn * 64, ys[j], &full[s]);
+              }
             }
           }
         }

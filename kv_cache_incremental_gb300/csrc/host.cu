@@ -93,6 +93,7 @@ struct kv_cache {
   std::vector<void *> K, V;
   std::vector<int> seg_rows;
   std::vector<CUtensorMap> tmK, tmV;
+  std::vector<CUtensorMap> tmK16, tmV16;  // paged layers: 16-row boxes over the pool
   CUtensorMap tmSK, tmSV;
   void *scrK = nullptr, *scrV = nullptr;
   float2 *rope = nullptr;
@@ -127,6 +128,7 @@ PageTable page_table(const kv_cache *c, int layer) {
   PageTable pt;
   pt.table = paged_layer(c, layer) ? c->table : nullptr;
   pt.max_blocks = paged_layer(c, layer) ? c->max_blocks : 0;
+  pt.n_pool = c->n_blocks;
   return pt;
 }
 
@@ -295,6 +297,8 @@ void fill_decode(const kv_cache *c, int layer, const __nv_bfloat16 *q, const __n
   dp.seg_rows = c->seg_rows[layer];
   dp.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c->D));
   dp.pt = page_table(c, layer);
+  dp.tmap_k16 = c->tmK16[layer];
+  dp.tmap_v16 = c->tmV16[layer];
   double kvb = 0;
   plan_decode(c, sliding, batch, dp, kvb, flops);
   // q, k, v in; new K and V and the output out
@@ -415,6 +419,8 @@ int append_device(kv_cache *c, int layer, const __nv_bfloat16 *q, const __nv_bfl
         pp.window = c->W;
         pp.scale_log2 = scale_log2;
         pp.pt = page_table(c, layer);
+        pp.tmap_k16 = c->tmK16[layer];
+        pp.tmap_v16 = c->tmV16[layer];
         int cta = 0;
         double bytes = 0, fl = 0;
         for (size_t j = r0; j < r1; ++j) {
@@ -585,7 +591,7 @@ static int create_impl(kv_cache **out, int B, int max_len, int Hq, int Hk, int D
     for (int b = n_blocks - 1; b >= 0; --b) c->free_blocks.push_back(b);
   }
   for (int l = 0; l < n_layers; ++l) {
-    // dense: [B][Hk][rows][D]; paged global layer: pool [n_blocks][Hk][16][D]
+    // dense: [B][Hk][rows][D]; paged global layer: pool [Hk][n_blocks][16][D]
     const bool pg = n_blocks > 0 && c->kind[l] == KV_GLOBAL;
     const int rows = pg ? kBlockTokens : c->kind[l] == KV_SLIDING ? R + 1 : max_len + 1;
     const int64_t units = pg ? n_blocks : B;
@@ -596,12 +602,21 @@ static int create_impl(kv_cache **out, int B, int max_len, int Hq, int Hk, int D
     if (!alloc(&v, bytes)) return fail(KV_ERR_OOM);
     c->V.push_back(v);
     c->seg_rows.push_back(rows);
-    CUtensorMap mk, mv;
-    const int box = pg ? kBlockTokens : kTileKeys;
-    if (!make_tmap(&mk, k, units * Hk * rows, D, box) || !make_tmap(&mv, v, units * Hk * rows, D, box))
+    CUtensorMap mk, mv, mk16, mv16;
+    if (!make_tmap(&mk, k, units * Hk * rows, D) || !make_tmap(&mv, v, units * Hk * rows, D))
       return fail(KV_ERR_CUDA);
+    if (pg) {
+      if (!make_tmap(&mk16, k, units * Hk * rows, D, kBlockTokens) ||
+          !make_tmap(&mv16, v, units * Hk * rows, D, kBlockTokens))
+        return fail(KV_ERR_CUDA);
+    } else {
+      mk16 = mk;
+      mv16 = mv;
+    }
     c->tmK.push_back(mk);
     c->tmV.push_back(mv);
+    c->tmK16.push_back(mk16);
+    c->tmV16.push_back(mv16);
   }
   const size_t scr = (size_t)B * Hk * kChunk * D * 2;
   if (!alloc(&c->scrK, scr) || !alloc(&c->scrV, scr)) return fail(KV_ERR_OOM);
@@ -1074,7 +1089,8 @@ int first_kept(const kv_cache *c, int layer, int keep) {
 // Storage block of (row, layer): K, V and the element stride between heads.
 // A paged global layer returns its pool and the row's block-table row instead.
 void row_block(const kv_cache *c, int layer, int row, __nv_bfloat16 *&k, __nv_bfloat16 *&v,
-               int64_t &head_stride, const int32_t *&table) {
+               int64_t &head_stride, const int32_t *&table, int32_t &pool) {
+  pool = c->n_blocks;
   if (paged_layer(c, layer)) {
     k = (__nv_bfloat16 *)c->K[layer];
     v = (__nv_bfloat16 *)c->V[layer];
@@ -1174,10 +1190,11 @@ int kv_copy_rows(kv_cache *dst, const int32_t *dst_rows, const kv_cache *src,
     for (int l = 0; l < dst->n_layers; ++l) {
       CopyItem it;
       __nv_bfloat16 *sk, *sv;
-      row_block(src, l, src_rows[i], sk, sv, it.src_head_stride, it.src_table);
+      row_block(src, l, src_rows[i], sk, sv, it.src_head_stride, it.src_table, it.src_pool);
       it.src_k = sk;
       it.src_v = sv;
-      row_block(dst, l, dst_rows[i], it.dst_k, it.dst_v, it.dst_head_stride, it.dst_table);
+      row_block(dst, l, dst_rows[i], it.dst_k, it.dst_v, it.dst_head_stride, it.dst_table,
+                it.dst_pool);
       const bool ring = dst->kind[l] == KV_SLIDING;
       it.p0 = first_kept(dst, l, kp[i]);
       it.p1 = kp[i];
@@ -1221,7 +1238,8 @@ static int export_import(kv_cache *c, int row, int keep, void *buf, int64_t byte
     __nv_bfloat16 *rk, *rv;
     int64_t hs;
     const int32_t *tab;
-    row_block(c, l, row, rk, rv, hs, tab);
+    int32_t pool;
+    row_block(c, l, row, rk, rv, hs, tab, pool);
     const int ring = c->kind[l] == KV_SLIDING ? c->R : 0;
     CopyItem it;
     it.p0 = p0;
@@ -1231,12 +1249,14 @@ static int export_import(kv_cache *c, int row, int keep, void *buf, int64_t byte
       it.src_v = rv;
       it.src_head_stride = hs;
       it.src_table = tab;
+      it.src_pool = pool;
       it.src_ring = ring;
       it.src_base = 0;
       it.dst_k = b + off;
       it.dst_v = b + off + blk;
       it.dst_head_stride = (int64_t)np * c->D;
       it.dst_table = nullptr;
+      it.dst_pool = 0;
       it.dst_ring = 0;
       it.dst_base = p0;
     } else {
@@ -1244,12 +1264,14 @@ static int export_import(kv_cache *c, int row, int keep, void *buf, int64_t byte
       it.src_v = b + off + blk;
       it.src_head_stride = (int64_t)np * c->D;
       it.src_table = nullptr;
+      it.src_pool = 0;
       it.src_ring = 0;
       it.src_base = p0;
       it.dst_k = rk;
       it.dst_v = rv;
       it.dst_head_stride = hs;
       it.dst_table = tab;
+      it.dst_pool = pool;
       it.dst_ring = ring;
       it.dst_base = 0;
     }

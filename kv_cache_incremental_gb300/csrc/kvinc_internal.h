@@ -25,34 +25,42 @@ constexpr int kMaxRep = 16;
 // reaching it sets the device error word and abandons the work item.
 constexpr uint32_t kWaitLimit = 1u << 24;
 
-// Paged global layers: a row's key slots are grouped in blocks of kBlockTokens, each block
-// a [Hk][kBlockTokens][D] piece of the layer's block pool, found through the row's block
-// table (shared by all global layers of the cache: their rows have the same lengths).
+// Paged global layers: a row's key slots are grouped in blocks of kBlockTokens, found
+// through the row's block table (shared by all global layers of the cache: their rows have
+// the same lengths).  A layer's pool is head-major, [Hk][n_pool][kBlockTokens][D], so that
+// consecutive pool blocks of one head are contiguous.
 constexpr int kBlockTokens = 16;
 struct PageTable {
   const int32_t *table;  // [B][max_blocks] pool block of each block of a row
   int max_blocks;        // 0: the layer's storage is dense [B][Hk][seg_rows][D]
+  int n_pool;            // blocks in the pool
 };
 
 // Row of key slot `slot` of (row, kv head g) in the 2-D [rows][D] view of a layer's storage:
-// dense (row * Hk + g) * seg_rows + slot; paged (table[row][slot / 16] * Hk + g) * 16 + slot % 16.
-// A slot past the table (only masked keys) reads the row's last table entry.
+// dense (row * Hk + g) * seg_rows + slot; paged (g * n_pool + table[row][slot / 16]) * 16 +
+// slot % 16.  A slot past the table (only masked keys) reads the row's last table entry.
 __device__ __forceinline__ int64_t kv_row(const PageTable &pt, int row, int Hk, int g,
                                           int seg_rows, int slot) {
   if (pt.max_blocks == 0) return ((int64_t)row * Hk + g) * seg_rows + slot;
   const int idx = min(slot / kBlockTokens, pt.max_blocks - 1);
   const int64_t blk = pt.table[(int64_t)row * pt.max_blocks + idx];
-  return (blk * Hk + g) * kBlockTokens + slot % kBlockTokens;
+  return ((int64_t)g * pt.n_pool + blk) * kBlockTokens + slot % kBlockTokens;
 }
 
 // Storage rows of the four 16-key blocks of the 64-key tile at `slot0` (a multiple of 64) of
 // (row, kv head g) in a paged layer, with one 16-byte table load (the table's rows are padded
 // to a multiple of 4 entries and every entry holds a valid pool block).
-__device__ __forceinline__ int4 kv_rows4(const PageTable &pt, int row, int Hk, int g, int slot0) {
+__device__ __forceinline__ int4 kv_rows4(const PageTable &pt, int row, int g, int slot0) {
   const int4 b = *reinterpret_cast<const int4 *>(pt.table + (int64_t)row * pt.max_blocks +
                                                  slot0 / kBlockTokens);
-  return make_int4((b.x * Hk + g) * kBlockTokens, (b.y * Hk + g) * kBlockTokens,
-                   (b.z * Hk + g) * kBlockTokens, (b.w * Hk + g) * kBlockTokens);
+  const int h0 = g * pt.n_pool;
+  return make_int4((h0 + b.x) * kBlockTokens, (h0 + b.y) * kBlockTokens,
+                   (h0 + b.z) * kBlockTokens, (h0 + b.w) * kBlockTokens);
+}
+// The tile's four blocks are consecutive in the pool: one 64-row box covers them.
+__device__ __forceinline__ bool rows4_contiguous(const int4 &y) {
+  return y.y == y.x + kBlockTokens && y.z == y.x + 2 * kBlockTokens &&
+         y.w == y.x + 3 * kBlockTokens;
 }
 
 enum DestMode : int32_t {
@@ -106,8 +114,10 @@ struct DecodeRow {
 };
 
 struct DecodeParams {  // 64-byte aligned through its CUtensorMap members
-  CUtensorMap tmap_k;       // layer K storage as 2-D [B*Hk*seg_rows][D], box 64 x kTileKeys
+  CUtensorMap tmap_k;       // layer K storage as 2-D [rows][D], box 64 x kTileKeys
   CUtensorMap tmap_v;
+  CUtensorMap tmap_k16;     // paged layer: the pool with box 64 x kBlockTokens
+  CUtensorMap tmap_v16;
   const __nv_bfloat16 *q;   // [Bs][C][Hq][D] (token 0 of each row is the decode token)
   int64_t q_row_stride;
   __nv_bfloat16 *out;       // [Bs][C][Hq][D]
@@ -127,7 +137,7 @@ struct DecodeParams {  // 64-byte aligned through its CUtensorMap members
   int Hq, Hk, rep, seg_rows;
   int n_rows, n_items;
   float scale_log2;         // log2(e) / sqrt(D)
-  PageTable pt;             // paged global layer: tmap_k/v boxes are 16 rows
+  PageTable pt;             // paged global layer (tmap_k16 / tmap_v16 valid)
   DecodeRow rows[kMaxRowsPerLaunch];
 };
 
@@ -141,8 +151,10 @@ struct PrefillRow {
 };
 
 struct PrefillParams {  // 64-byte aligned through its CUtensorMap members
-  CUtensorMap tmap_k;       // layer storage (global cache or ring)
+  CUtensorMap tmap_k;       // layer storage (global cache or ring), box 64 x kTileKeys
   CUtensorMap tmap_v;
+  CUtensorMap tmap_k16;     // paged layer: the pool with box 64 x kBlockTokens
+  CUtensorMap tmap_v16;
   CUtensorMap tmap_sk;      // chunk scratch [B*Hk*64][D] (sliding only)
   CUtensorMap tmap_sv;
   const __nv_bfloat16 *q;   // [Bs][C][Hq][D], offset to the sub-chunk
@@ -156,7 +168,7 @@ struct PrefillParams {  // 64-byte aligned through its CUtensorMap members
   int ring_R, window;
   int n_rows, n_ctas;
   float scale_log2;
-  PageTable pt;             // paged global layer: tmap_k/v boxes are 16 rows
+  PageTable pt;             // paged global layer (tmap_k16 / tmap_v16 valid)
   PrefillRow rows[kMaxRowsPerLaunch];
 };
 
@@ -186,12 +198,13 @@ struct StateParams {
 // A storage is [Hk][slots][D] per (row, layer) at `k`/`v` with `head_stride` elements
 // between heads; position p sits at slot p % ring (ring > 0) or p - base (ring == 0).
 // A paged side (table != nullptr: the row's block-table row) has `k`/`v` at its pool's
-// start and position p at pool row (table[p / 16] * Hk + h) * 16 + p % 16.
+// start and position p of head h at pool row (h * n_pool + table[p / 16]) * 16 + p % 16.
 struct CopyItem {
   const __nv_bfloat16 *src_k, *src_v;
   __nv_bfloat16 *dst_k, *dst_v;
   int64_t src_head_stride, dst_head_stride;
   const int32_t *src_table, *dst_table;
+  int32_t src_pool, dst_pool;  // pool blocks of a paged side
   int32_t p0, p1;
   int32_t src_ring, src_base, dst_ring, dst_base;
 };

@@ -178,6 +178,9 @@ extern "C" int kv_decode_noalloc(const void *K, const void *V, int n_cache_rows,
   dp.cache_k = nullptr;
   dp.cache_v = nullptr;
   dp.fuse_append = 0;
+  dp.pt = PageTable{nullptr, 0, 0};  // the caller's storage is dense
+  dp.tmap_k16 = dp.tmap_k;
+  dp.tmap_v16 = dp.tmap_v;
   dp.Hq = Hq;
   dp.Hk = Hk;
   dp.rep = Hq / Hk;

@@ -153,23 +153,24 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(const __grid_constant
         const int y = static_cast<int>(in_a ? base_a + (int64_t)it * kTileKeys
                                             : base_b + (int64_t)(it - tiles_a) * kTileKeys);
         ptx::mbar_arrive_expect_tx(&full[s], Cfg::kStageBytes);
-        if (in_a && p.pt.max_blocks) {  // paged cache: four 16-key blocks, 16-row boxes
-          const int4 y4 = kv_rows4(p.pt, row.cache_row, p.Hk, g, it * kTileKeys);
+        int4 y4 = make_int4(y, y + kBlockTokens, y + 2 * kBlockTokens, y + 3 * kBlockTokens);
+        if (in_a && p.pt.max_blocks) y4 = kv_rows4(p.pt, row.cache_row, g, it * kTileKeys);
+        if (rows4_contiguous(y4)) {  // dense, or a paged tile of consecutive blocks
+#pragma unroll
+          for (int pn = 0; pn < Cfg::kPanels; ++pn) {
+            ptx::tma_load_2d(kt + pn * kTileKeys * 128, mk, pn * 64, y4.x, &full[s]);
+            ptx::tma_load_2d(vt + pn * kTileKeys * 128, mv, pn * 64, y4.x, &full[s]);
+          }
+        } else {  // paged: four 16-key blocks, 16-row boxes
           const int ys[4] = {y4.x, y4.y, y4.z, y4.w};
 #pragma unroll
           for (int j = 0; j < kTileKeys / kBlockTokens; ++j)
 #pragma unroll
             for (int pn = 0; pn < Cfg::kPanels; ++pn) {
               const int off = pn * kTileKeys * 128 + j * kBlockTokens * 128;
-              ptx::tma_load_2d(kt + off, mk, pn * 64, ys[j], &full[s]);
-              ptx::tma_load_2d(vt + off, mv, pn * 64, ys[j], &full[s]);
+              ptx::tma_load_2d(kt + off, &p.tmap_k16, pn * 64, ys[j], &full[s]);
+              ptx::tma_load_2d(vt + off, &p.tmap_v16, pn * 64, ys[j], &full[s]);
             }
-        } else {
-#pragma unroll
-          for (int pn = 0; pn < Cfg::kPanels; ++pn) {
-            ptx::tma_load_2d(kt + pn * kTileKeys * 128, mk, pn * 64, y, &full[s]);
-            ptx::tma_load_2d(vt + pn * kTileKeys * 128, mv, pn * 64, y, &full[s]);
-          }
         }
         *issued = it + 1;
       }

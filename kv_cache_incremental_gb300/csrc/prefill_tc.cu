@@ -243,8 +243,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           const CUtensorMap *mv = in_a ? &p.tmap_v : &p.tmap_sv;
           const int y = static_cast<int>(in_a ? base_a + (int64_t)j * kKeys
                                               : base_b + (int64_t)(j - tiles_a) * kKeys);
-          if (in_a && p.pt.max_blocks) {  // paged cache: four 16-key blocks, 16-row boxes
-            const int4 y4 = kv_rows4(p.pt, row.cache_row, p.Hk, g, j * kKeys);
+          int4 y4 = make_int4(y, y + kBlockTokens, y + 2 * kBlockTokens, y + 3 * kBlockTokens);
+          if (in_a && p.pt.max_blocks) y4 = kv_rows4(p.pt, row.cache_row, g, j * kKeys);
+          if (rows4_contiguous(y4)) {  // dense, or a paged tile of consecutive blocks
+#pragma unroll
+            for (int pn = 0; pn < Cfg::kPanels; ++pn) {
+              const int off = pn * Cfg::kPanelBytes + h * Cfg::kHalfBytes;
+              ptx::tma_load_2d(kt + off, mk, pn * 64, y4.x, &kv_full[s]);
+              ptx::tma_load_2d(vt + off, mv, pn * 64, y4.x, &kv_full[s]);
+            }
+          } else {  // paged: four 16-key blocks, 16-row boxes
             const int ys[4] = {y4.x, y4.y, y4.z, y4.w};
 #pragma unroll
             for (int q4 = 0; q4 < kKeys / kBlockTokens; ++q4)
@@ -252,16 +260,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int pn = 0; pn < Cfg::kPanels; ++pn) {
                 const int off =
                     pn * Cfg::kPanelBytes + h * Cfg::kHalfBytes + q4 * kBlockTokens * 128;
-                ptx::tma_load_2d(kt + off, mk, pn * 64, ys[q4], &kv_full[s]);
-                ptx::tma_load_2d(vt + off, mv, pn * 64, ys[q4], &kv_full[s]);
+                ptx::tma_load_2d(kt + off, &p.tmap_k16, pn * 64, ys[q4], &kv_full[s]);
+                ptx::tma_load_2d(vt + off, &p.tmap_v16, pn * 64, ys[q4], &kv_full[s]);
               }
-          } else {
-#pragma unroll
-            for (int pn = 0; pn < Cfg::kPanels; ++pn) {
-              const int off = pn * Cfg::kPanelBytes + h * Cfg::kHalfBytes;
-              ptx::tma_load_2d(kt + off, mk, pn * 64, y, &kv_full[s]);
-              ptx::tma_load_2d(vt + off, mv, pn * 64, y, &kv_full[s]);
-            }
           }
         }
         *issued = it + 1;

@@ -12,10 +12,10 @@ namespace kvinc {
 namespace {
 
 // Element offset of position p, head h of one side of a copy.
-__device__ __forceinline__ int64_t elem_of(int p, int h, int Hk, int D, const int32_t *table,
+__device__ __forceinline__ int64_t elem_of(int p, int h, int D, const int32_t *table, int pool,
                                            int64_t head_stride, int ring, int base) {
   if (table)
-    return (((int64_t)table[p / kBlockTokens] * Hk + h) * kBlockTokens + p % kBlockTokens) * D;
+    return (((int64_t)h * pool + table[p / kBlockTokens]) * kBlockTokens + p % kBlockTokens) * D;
   return h * head_stride + (int64_t)(ring > 0 ? p % ring : p - base) * D;
 }
 
@@ -37,7 +37,8 @@ __global__ void __launch_bounds__(256) copy_kernel(const __grid_constant__ CopyP
       if (u >= units) continue;
       const int pos = it.p0 + u / vec, c = u % vec;
       const int64_t s =
-          elem_of(pos, h, p.Hk, p.D, it.src_table, it.src_head_stride, it.src_ring, it.src_base) +
+          elem_of(pos, h, p.D, it.src_table, it.src_pool, it.src_head_stride, it.src_ring,
+                  it.src_base) +
           8 * c;
       kk[i] = *reinterpret_cast<const uint4 *>(sk + s);
       vv[i] = *reinterpret_cast<const uint4 *>(sv + s);
@@ -48,7 +49,8 @@ __global__ void __launch_bounds__(256) copy_kernel(const __grid_constant__ CopyP
       if (u >= units) continue;
       const int pos = it.p0 + u / vec, c = u % vec;
       const int64_t d =
-          elem_of(pos, h, p.Hk, p.D, it.dst_table, it.dst_head_stride, it.dst_ring, it.dst_base) +
+          elem_of(pos, h, p.D, it.dst_table, it.dst_pool, it.dst_head_stride, it.dst_ring,
+                  it.dst_base) +
           8 * c;
       *reinterpret_cast<uint4 *>(dk + d) = kk[i];
       *reinterpret_cast<uint4 *>(dv + d) = vv[i];
