@@ -71,6 +71,10 @@ def _load():
                                       ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                       ctypes.c_int, ctypes.c_double, _F64P]
         lib.oracle_attend.restype = ctypes.c_int
+        lib.oracle_attend_hybrid.argtypes = [_U16P, _I32P, ctypes.c_int, _U16P, _U16P, _U16P,
+                                             _U16P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                             ctypes.c_int, ctypes.c_int, ctypes.c_double, _F64P]
+        lib.oracle_attend_hybrid.restype = ctypes.c_int
         lib.oracle_kv_nbytes.argtypes = [ctypes.c_int] * 10
         lib.oracle_kv_nbytes.restype = ctypes.c_int64
         lib.oracle_num_threads.argtypes = []
@@ -155,6 +159,28 @@ def attend(q, qpos, k, v, k_base: int, Hq: int, Hk: int, W: int = 0,
                            float(theta), out)
     if rc != 0:
         raise ValueError("oracle_attend: invalid arguments or history does not cover the window")
+    return out
+
+
+def attend_hybrid(q, qpos, kg, vg, kl, vl, Hq: int, Hk: int, W: int,
+                  theta: float = 1e4) -> np.ndarray:
+    """Hybrid attention (tiny_agent/generate.py `_append_chunk`): one softmax over the group's
+    global keys at every position <= p and the layer's local keys in its window.
+
+    q: uint16 [n_q, Hq, D] (pre-RoPE), qpos: [n_q]; kg, vg, kl, vl: uint16 [n_k, Hk, D] for
+    positions 0 .. n_k-1.  Returns float64 [n_q, Hq, D]."""
+    lib = _load()
+    arrs = [np.ascontiguousarray(x, dtype=np.uint16) for x in (q, kg, vg, kl, vl)]
+    q, kg, vg, kl, vl = arrs
+    qpos = np.ascontiguousarray(qpos, dtype=np.int32)
+    n_q, hq, D = q.shape
+    n_k = kg.shape[0]
+    assert hq == Hq and all(x.shape == (n_k, Hk, D) for x in (kg, vg, kl, vl))
+    out = np.zeros((n_q, Hq, D), dtype=np.float64)
+    rc = lib.oracle_attend_hybrid(q, qpos, n_q, kg, vg, kl, vl, n_k, Hq, Hk, D, int(W),
+                                  float(theta), out)
+    if rc != 0:
+        raise ValueError("oracle_attend_hybrid: invalid arguments or uncovered position")
     return out
 
 

@@ -237,6 +237,106 @@ int oracle_attend(const uint16_t *q, const int32_t *qpos, int n_q,
     return rc;
 }
 
+/*
+ * Hybrid attention (tiny_agent/generate.py, module docstring and `_append_chunk`): a layer
+ * of a group scores its query against two key sets in ONE softmax -- the group's global
+ * keys (written by the group's full layer) at every position j <= p, and the layer's own
+ * local keys at the positions of its window (j <= p and p - j < W) -- and sums both sets'
+ * values with those weights.  `s = cat([q Kg^T, q Kl^T])`, one softmax, `y = p_g Vg + p_l Vl`.
+ *
+ *   q            [n_q][Hq][D] bf16 bits, pre-RoPE
+ *   qpos         [n_q]
+ *   kg, vg       [n_k][Hk][D] bf16 bits: pre-RoPE global keys / values of positions 0..n_k-1
+ *   kl, vl       [n_k][Hk][D] bf16 bits: pre-RoPE local keys / values of the same positions
+ *   out          [n_q][Hq][D] double
+ *
+ * Returns 0, or -1 when the arguments are invalid or a query's position is not covered.
+ */
+int oracle_attend_hybrid(const uint16_t *q, const int32_t *qpos, int n_q,
+                         const uint16_t *kg, const uint16_t *vg, const uint16_t *kl,
+                         const uint16_t *vl, int n_k, int Hq, int Hk, int D, int W,
+                         double theta, double *out)
+{
+    if (n_q < 0 || n_k < 0 || Hq <= 0 || Hk <= 0 || D <= 0 || (D % 2) != 0 ||
+        (Hq % Hk) != 0 || W < 1)
+        return -1;
+    int rep = Hq / Hk;
+    for (int i = 0; i < n_q; ++i)
+        if (qpos[i] < 0 || qpos[i] >= n_k) return -1;
+
+    size_t nkv = (size_t)n_k * Hk * D;
+    uint16_t *kgr = (uint16_t *)malloc(nkv * sizeof(uint16_t) + 1);
+    uint16_t *klr = (uint16_t *)malloc(nkv * sizeof(uint16_t) + 1);
+    if (!kgr || !klr) {
+        free(kgr);
+        free(klr);
+        return -1;
+    }
+#pragma omp parallel for schedule(static)
+    for (int j = 0; j < n_k; ++j)
+        for (int g = 0; g < Hk; ++g) {
+            size_t o = ((size_t)j * Hk + g) * D;
+            oracle_rope_bf16(&kg[o], j, D, theta, &kgr[o]);
+            oracle_rope_bf16(&kl[o], j, D, theta, &klr[o]);
+        }
+
+    int rc = 0;
+#pragma omp parallel for collapse(2) schedule(dynamic)
+    for (int i = 0; i < n_q; ++i) {
+        for (int h = 0; h < Hq; ++h) {
+            int p = qpos[i];
+            int g = h / rep;
+            uint16_t *qr = (uint16_t *)malloc((size_t)D * sizeof(uint16_t));
+            double *s = (double *)malloc((size_t)2 * (p + 1) * sizeof(double)); /* [global | local] */
+            double *acc = &out[((size_t)i * Hq + h) * D];
+            if (!qr || !s) {
+                free(qr);
+                free(s);
+#pragma omp atomic write
+                rc = -1;
+                continue;
+            }
+            oracle_rope_bf16(&q[((size_t)i * Hq + h) * D], p, D, theta, qr);
+            double m = -INFINITY;
+            for (int set = 0; set < 2; ++set) {
+                const uint16_t *kr = set == 0 ? kgr : klr;
+                for (int j = 0; j <= p; ++j) {
+                    double *sj = &s[(size_t)set * (p + 1) + j];
+                    if (set == 1 && !oracle_visible(p, j, W)) {
+                        *sj = -INFINITY;
+                        continue;
+                    }
+                    const uint16_t *kj = &kr[((size_t)j * Hk + g) * D];
+                    double dot = 0.0;
+                    for (int d = 0; d < D; ++d)
+                        dot += (double)oracle_bf16_to_f32(qr[d]) * (double)oracle_bf16_to_f32(kj[d]);
+                    *sj = dot / sqrt((double)D);
+                    if (*sj > m) m = *sj;
+                }
+            }
+            double denom = 0.0;
+            for (int d = 0; d < D; ++d) acc[d] = 0.0;
+            for (int set = 0; set < 2; ++set) {
+                const uint16_t *vv = set == 0 ? vg : vl;
+                for (int j = 0; j <= p; ++j) {
+                    double sj = s[(size_t)set * (p + 1) + j];
+                    if (sj == -INFINITY) continue;
+                    double w = exp(sj - m);
+                    denom += w;
+                    const uint16_t *vj = &vv[((size_t)j * Hk + g) * D];
+                    for (int d = 0; d < D; ++d) acc[d] += w * (double)oracle_bf16_to_f32(vj[d]);
+                }
+            }
+            for (int d = 0; d < D; ++d) acc[d] /= denom;
+            free(qr);
+            free(s);
+        }
+    }
+    free(kgr);
+    free(klr);
+    return rc;
+}
+
 /* ---------------------------------------------------------------- memory */
 
 /* K+V bytes of a cache whose global layers keep max_len rows per (row, kv

@@ -402,3 +402,77 @@ def test_oracle_chunking_and_incremental_are_the_same_call():
                                    Hq, Hk))
         s += c
     assert np.array_equal(np.concatenate(parts), full)
+
+
+# ------------------------------------------------------------------ hybrid layer
+
+def _rand_bf16(rng, shape):
+    return _bf16(rng.standard_normal(shape).astype(np.float32))
+
+
+def test_hybrid_same_keys_and_full_window_equal_plain_attention():
+    """With the local keys and values equal to the global ones and a window covering
+    every position, each key appears twice with the same score: the two softmax halves
+    share the same normalisation, so the result is plain attention over the global set."""
+    rng = np.random.default_rng(21)
+    D, Hq, Hk, n = 16, 4, 2, 11
+    q = _rand_bf16(rng, (n, Hq, D))
+    k = _rand_bf16(rng, (n, Hk, D))
+    v = _rand_bf16(rng, (n, Hk, D))
+    pos = np.arange(n)
+    got = oracle.attend_hybrid(q, pos, k, v, k, v, Hq, Hk, W=n)
+    ref = oracle.attend(q, pos, k, v, 0, Hq, Hk)
+    assert np.allclose(got, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_hybrid_reduces_to_each_branch_when_the_other_is_negligible():
+    """Keys that score far below the others (about -60 logits) drop out of the softmax:
+    hybrid = global-only attention when the local keys are pushed away, and = local
+    window attention when the global keys are.  theta is huge and the queries' first pair
+    is zero, so RoPE leaves the relevant dot products unrotated (only pair 0 has
+    frequency 1)."""
+    rng = np.random.default_rng(22)
+    D, Hq, Hk, n, W = 16, 2, 1, 9, 3
+    theta = 1e30
+    q = _bf16(np.full((n, Hq, D), 1.0, np.float32))
+    q[:, :, 0] = 0
+    q[:, :, D // 2] = 0                       # pair 0 (elements 0 and D/2) carries nothing
+    far = _bf16(np.full((n, Hk, D), -16.0, np.float32))   # score -16 * (D-2) / 4 = -56
+    k = _rand_bf16(rng, (n, Hk, D))
+    k[:] = _bf16(np.float32(0.0))
+    vg = _rand_bf16(rng, (n, Hk, D))
+    vl = _rand_bf16(rng, (n, Hk, D))
+    pos = np.arange(n)
+    g_only = oracle.attend_hybrid(q, pos, k, vg, far, vl, Hq, Hk, W=W, theta=theta)
+    assert np.allclose(g_only, oracle.attend(q, pos, k, vg, 0, Hq, Hk, theta=theta),
+                       rtol=0, atol=1e-20)
+    l_only = oracle.attend_hybrid(q, pos, far, vg, k, vl, Hq, Hk, W=W, theta=theta)
+    assert np.allclose(l_only, oracle.attend(q, pos, k, vl, 0, Hq, Hk, W=W, theta=theta),
+                       rtol=0, atol=1e-20)
+
+
+def test_hybrid_log_sum_exp_merge_of_the_two_sets():
+    """One softmax over two disjoint key sets is the two per-set softmaxes merged by their
+    partition functions: out = (Zg Og + Zl Ol) / (Zg + Zl), with Z = sum of exp(scores)
+    computed here from the rotated keys (scipy), and Og, Ol from the plain oracle."""
+    rng = np.random.default_rng(23)
+    D, Hq, Hk, n, W = 32, 4, 2, 14, 5
+    q = _rand_bf16(rng, (n, Hq, D))
+    kg, vg, kl, vl = (_rand_bf16(rng, (n, Hk, D)) for _ in range(4))
+    pos = np.arange(n)
+    got = oracle.attend_hybrid(q, pos, kg, vg, kl, vl, Hq, Hk, W=W)
+    Og = oracle.attend(q, pos, kg, vg, 0, Hq, Hk)
+    Ol = oracle.attend(q, pos, kl, vl, 0, Hq, Hk, W=W)
+    Qr = _f(oracle.rope_bf16(q, pos[:, None]))
+    Kgr = _f(oracle.rope_bf16(kg, pos[:, None]))
+    Klr = _f(oracle.rope_bf16(kl, pos[:, None]))
+    for h in range(Hq):
+        g = h // (Hq // Hk)
+        for p in range(n):
+            sg = Kgr[: p + 1, g] @ Qr[p, h] / math.sqrt(D)
+            lo = max(0, p - W + 1)
+            sl = Klr[lo: p + 1, g] @ Qr[p, h] / math.sqrt(D)
+            m = max(sg.max(), sl.max())
+            Zg, Zl = np.exp(sg - m).sum(), np.exp(sl - m).sum()
+            ref = (Zg * Og[p, h] + Zl * Ol[p, h]) / (Zg + Zl)
+            assert np.allclose(got[p, h], ref, rtol=1e-11, atol=1e-12)
