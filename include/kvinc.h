@@ -52,8 +52,16 @@ typedef struct kv_cache kv_cache; /* opaque; the library owns all cache memory *
 
 /* Layer kinds of the layer layout. */
 enum kv_layer_kind {
-    KV_GLOBAL = 0,  /* full-length cache, every past key visible ([G] global K/V) */
-    KV_SLIDING = 1  /* ring of W slots, keys p-W+1..p visible ([I], [G] local K/V) */
+    KV_GLOBAL = 0,        /* full-length cache, every past key visible ([G] global K/V) */
+    KV_SLIDING = 1,       /* ring of W slots, keys p-W+1..p visible ([I], [G] local K/V) */
+    /* [G]'s hybrid layers (tiny_agent/generate.py, module docstring and `_append_chunk`):
+     * a group of layers shares one global K/V, written by the group's first layer, and
+     * every layer of the group also keeps its own local ring of W slots; a layer attends
+     * to the group's global keys at every position <= p and to its own local keys at
+     * p-W+1..p, in ONE softmax.  Use kv_append_hybrid on these layers. */
+    KV_HYBRID_FULL = 2,   /* opens a group: owns the group's global K/V, and its ring */
+    KV_HYBRID_LOCAL = 3   /* reads the global K/V of the nearest preceding KV_HYBRID_FULL
+                             layer; owns its ring */
 };
 
 enum kv_status {
@@ -167,6 +175,23 @@ int kv_append(kv_cache *c, int layer, const void *q, const void *k, const void *
               void *stream);
 
 /*
+ * kv_append for a hybrid layer.  k_local, v_local: device bf16 [Bs][C][Hk][D], the
+ * layer's own pre-RoPE local keys and values (stored in its ring by the keep rule, as on
+ * a sliding layer).  k_global, v_global: the group's pre-RoPE global keys and values
+ * (same shape), required on a KV_HYBRID_FULL layer (stored in the group's cache, as on a
+ * global layer) and NULL on a KV_HYBRID_LOCAL layer, whose group's full layer must
+ * already have been appended in this step (stream order).  out: for every real token t
+ * at p = lens[row] + t, softmax over the group's global keys j <= p and the layer's local
+ * keys p-W < j <= p together, of (rope(q, p) . K_j) / sqrt(D), times the matching V_j.
+ * Same rules and errors as kv_append; KV_ERR_ARG on a layer that is not hybrid (and
+ * kv_append returns KV_ERR_ARG on a hybrid layer).
+ */
+int kv_append_hybrid(kv_cache *c, int layer, const void *q, const void *k_local,
+                     const void *v_local, const void *k_global, const void *v_global, int Hq,
+                     int C, const int32_t *n_new, const int32_t *rows, int Bs, void *out,
+                     void *stream);
+
+/*
  * Same as kv_append, but q, k, v and out are HOST buffers.  Page-locked buffers
  * (cudaHostAlloc / cudaHostRegister, e.g. torch pin_memory) are read and written
  * by the kernels directly through their device addresses: on GB300 host memory
@@ -200,11 +225,13 @@ int64_t kv_nbytes(const kv_cache *c);
 int kv_get_lens(const kv_cache *c, int32_t *lens_out);
 
 /* Device pointers of a layer's K and V storage and of lpos ([B][R] int32, or
- * NULL without sliding layers), for inspection and tests.  Layouts as in
+ * NULL without sliding or hybrid layers), for inspection and tests.  For a hybrid
+ * layer: its group's global storage; kv_debug_ring_ptrs gives its ring ([B][Hk][R+1][D]).  Layouts as in
  * kv_cache_create; a paged cache's global layers point at their block pools
  * ([Hk][n_blocks][16][D], see kv_get_block_table).  The pointers stay owned by the
  * cache. */
 int kv_debug_ptrs(const kv_cache *c, int layer, void **K, void **V, int32_t **lpos);
+int kv_debug_ring_ptrs(const kv_cache *c, int layer, void **K, void **V);
 
 /* Shape query: fills any non-NULL output with the cache's parameters. */
 int kv_get_config(const kv_cache *c, int *B, int *max_len, int *Hq, int *Hk, int *D, int *W,

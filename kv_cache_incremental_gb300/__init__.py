@@ -16,11 +16,11 @@ import ctypes
 import weakref
 from typing import Optional, Sequence
 
-from ._lib import (KERNELS, KV_GLOBAL, KV_SLIDING, KVCacheFull, KVError, KVPoolExhausted, check,
-                   load)
+from ._lib import (KERNELS, KV_GLOBAL, KV_HYBRID_FULL, KV_HYBRID_LOCAL, KV_SLIDING, KVCacheFull,
+                   KVError, KVPoolExhausted, check, load)
 
 __all__ = ["KVCache", "StepGraph", "KVError", "KVCacheFull", "KVPoolExhausted", "KV_GLOBAL",
-           "KV_SLIDING", "load"]
+           "KV_SLIDING", "KV_HYBRID_FULL", "KV_HYBRID_LOCAL", "load"]
 
 _clib = load()
 
@@ -123,6 +123,42 @@ class KVCache:
                              _stream_ptr(stream, q.device)), "kv_append")
         return out
 
+    def append_hybrid(self, layer: int, q, k_local, v_local, n_new, k_global=None,
+                      v_global=None, rows=None, out=None, stream=None):
+        """append() for a hybrid layer: k_local, v_local go to the layer's ring; k_global,
+        v_global (a KV_HYBRID_FULL layer only) to its group's cache.  One softmax over the
+        group's global keys <= p and the layer's local keys in the window."""
+        import torch
+        self._check_tensor(q, "q", self.Hq)
+        Bs, C = q.shape[0], q.shape[1]
+        for x, name in ((k_local, "k_local"), (v_local, "v_local"), (k_global, "k_global"),
+                        (v_global, "v_global")):
+            if x is not None:
+                self._check_tensor(x, name, self.Hk, C, Bs)
+        if out is None:
+            out = torch.empty_like(q)
+        else:
+            self._check_tensor(out, "out", self.Hq, C, Bs)
+        if len(n_new) != Bs or (rows is not None and len(rows) != Bs):
+            raise ValueError("n_new and rows must have one entry per row of q")
+        ptr = lambda x: None if x is None else x.data_ptr()
+        check(_clib.kv_append_hybrid(self._h, layer, q.data_ptr(), k_local.data_ptr(),
+                                    v_local.data_ptr(), ptr(k_global), ptr(v_global), self.Hq,
+                                    C, _i32_array(n_new), _i32_array(rows), Bs, out.data_ptr(),
+                                    _stream_ptr(stream, q.device)), "kv_append_hybrid")
+        return out
+
+    def ring_storage(self, layer: int):
+        """Zero-copy torch views (K, V) of a hybrid layer's ring, [B, Hk, R + 1, D] bf16."""
+        import torch
+        kp, vp = ctypes.c_void_p(), ctypes.c_void_p()
+        check(_clib.kv_debug_ring_ptrs(self._h, layer, ctypes.byref(kp), ctypes.byref(vp)))
+        dev = f"cuda:{self.device}"
+        shape = (self.B, self.Hk, self.R + 1, self.D)
+        K = torch.as_tensor(_DevArray(kp.value, shape, "<i2"), device=dev).view(torch.bfloat16)
+        V = torch.as_tensor(_DevArray(vp.value, shape, "<i2"), device=dev).view(torch.bfloat16)
+        return K, V
+
     def copy_rows(self, src: "KVCache", src_rows, dst_rows, keep=None, stream=None) -> None:
         """Rows dst_rows of this cache become the first keep[i] tokens (default: all) of
         rows src_rows of `src` (this cache or another of the same layout)."""
@@ -202,15 +238,16 @@ class KVCache:
 
     def storage(self, layer: int):
         """Torch views (K, V) of a layer's storage, [B, Hk, rows, D] bf16; rows = max_len + 1
-        (global) or R + 1 (sliding).  Zero-copy and valid while the cache lives, except for a
-        paged cache's global layers: there each row's blocks are gathered from the pool into
-        a new tensor (slots past the row's blocks are zero)."""
+        (global, and a hybrid layer's group cache) or R + 1 (sliding).  Zero-copy and valid
+        while the cache lives, except for a paged cache's global layers: there each row's
+        blocks are gathered from the pool into a new tensor (slots past the row's blocks are
+        zero)."""
         import torch
         kp, vp, lp = ctypes.c_void_p(), ctypes.c_void_p(), ctypes.c_void_p()
         check(_clib.kv_debug_ptrs(self._h, layer, ctypes.byref(kp), ctypes.byref(vp),
                                  ctypes.byref(lp)))
         dev = f"cuda:{self.device}"
-        if self.paged_blocks is not None and self.layer_kinds[layer] == KV_GLOBAL:
+        if self.paged_blocks is not None and self.layer_kinds[layer] != KV_SLIDING:
             pool = (self.Hk, self.paged_blocks, 16, self.D)   # head-major pool
             Kp = torch.as_tensor(_DevArray(kp.value, pool, "<i2"), device=dev).view(torch.bfloat16)
             Vp = torch.as_tensor(_DevArray(vp.value, pool, "<i2"), device=dev).view(torch.bfloat16)

@@ -14,7 +14,7 @@ c_int, c_int32, c_int64, c_double, c_void_p = (ctypes.c_int, ctypes.c_int32, cty
                                                ctypes.c_double, ctypes.c_void_p)
 P_i32 = ctypes.POINTER(ctypes.c_int32)
 
-KV_GLOBAL, KV_SLIDING = 0, 1
+KV_GLOBAL, KV_SLIDING, KV_HYBRID_FULL, KV_HYBRID_LOCAL = 0, 1, 2, 3
 (KV_OK, KV_ERR_ARG, KV_ERR_FULL, KV_ERR_DTYPE, KV_ERR_CUDA, KV_ERR_OOM, KV_ERR_DEVICE,
  KV_ERR_SCRATCH, KV_ERR_POOL) = range(9)
 KERNELS = {"append": 0, "decode": 1, "combine": 2, "prefill": 3, "commit": 4, "state": 5,
@@ -32,6 +32,8 @@ SIGNATURES = {
     "kv_reset": (c_int, [c_void_p, P_i32, c_int, c_void_p]),
     "kv_append": (c_int, [c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_int, c_int, P_i32, P_i32,
                           c_int, c_void_p, c_void_p]),
+    "kv_append_hybrid": (c_int, [c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                 c_int, c_int, P_i32, P_i32, c_int, c_void_p, c_void_p]),
     "kv_append_host": (c_int, [c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_int, c_int, P_i32,
                                P_i32, c_int, c_void_p, c_void_p]),
     "kv_advance": (c_int, [c_void_p, P_i32, P_i32, c_int, c_void_p]),
@@ -39,6 +41,8 @@ SIGNATURES = {
     "kv_get_lens": (c_int, [c_void_p, P_i32]),
     "kv_debug_ptrs": (c_int, [c_void_p, c_int, ctypes.POINTER(c_void_p), ctypes.POINTER(c_void_p),
                               ctypes.POINTER(c_void_p)]),
+    "kv_debug_ring_ptrs": (c_int, [c_void_p, c_int, ctypes.POINTER(c_void_p),
+                                   ctypes.POINTER(c_void_p)]),
     "kv_get_config": (c_int, [c_void_p] + [ctypes.POINTER(c_int)] * 8),
     "kv_device_error": (c_int, [c_void_p, P_i32]),
     "kv_profile_enable": (c_int, [c_void_p, c_int]),

@@ -210,11 +210,23 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
   const int item = blockIdx.x;
   const int g = blockIdx.y;
   const DecodeRow &row = p.rows[find_item_row(p, item)];
-  const int split = item - row.item0;
-  const int k0 = split * row.split_len;
-  const int k1 = min(row.nk, k0 + row.split_len);
+  // The item's key segment: 0 = the layer storage (a global cache, a sliding ring, or a
+  // hybrid layer's group cache), 1 = a hybrid layer's own ring.
+  const int split = item - row.item0;          // over all the row's splits (merge slot)
+  const bool seg1 = split >= row.n_splits;
+  const int n_total = row.n_splits + row.n_splits2;
+  const int ssplit = seg1 ? split - row.n_splits : split;
+  const int split_len = seg1 ? row.split_len2 : row.split_len;
+  const int k0 = ssplit * split_len;
+  const int k1 = min(seg1 ? row.nk2 : row.nk, k0 + split_len);
   const int n_tiles = (k1 - k0 + kTileKeys - 1) / kTileKeys;
-  const bool owner = p.fuse_append && row.slot >= k0 && row.slot < k1;  // holds the new key
+  const int new_slot = seg1 ? row.slot2 : row.slot;
+  const bool owner = (seg1 ? p.fuse_append2 : p.fuse_append) && new_slot >= k0 && new_slot < k1;
+  const CUtensorMap *map_k = seg1 ? &p.tmap_k2 : &p.tmap_k;
+  const CUtensorMap *map_v = seg1 ? &p.tmap_v2 : &p.tmap_v;
+  const int seg_rows = seg1 ? p.seg_rows2 : p.seg_rows;
+  PageTable pt = p.pt;
+  if (seg1) pt.max_blocks = 0;                 // rings are dense
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
@@ -228,13 +240,13 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
     ptx::fence_barrier_init();
   }
   __syncthreads();  // barriers ready: the producer streams while consumers set up
-  const int64_t row0 = ((int64_t)row.cache_row * p.Hk + g) * p.seg_rows + k0;
+  const int64_t row0 = ((int64_t)row.cache_row * p.Hk + g) * seg_rows + k0;
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      ptx::prefetch_tmap(&p.tmap_k);
-      ptx::prefetch_tmap(&p.tmap_v);
+      ptx::prefetch_tmap(map_k);
+      ptx::prefetch_tmap(map_v);
       for (int it = 0; it < n_tiles; ++it) {
         const int s = it % kStages;
         if (it >= kStages) {
@@ -246,15 +258,15 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
         uint8_t *kt = tiles + s * Cfg::kStageBytes;
         uint8_t *vt = kt + Cfg::kTileBytes;
         ptx::mbar_arrive_expect_tx(&full[s], Cfg::kStageBytes);
-        if (p.pt.max_blocks == 0) {
+        if (pt.max_blocks == 0) {
           const int y = static_cast<int>(row0 + (int64_t)it * kTileKeys);
 #pragma unroll
           for (int pn = 0; pn < Cfg::kPanels; ++pn) {
-            ptx::tma_load_2d(kt + pn * kTileKeys * 128, &p.tmap_k, pn * 64, y, &full[s]);
-            ptx::tma_load_2d(vt + pn * kTileKeys * 128, &p.tmap_v, pn * 64, y, &full[s]);
+            ptx::tma_load_2d(kt + pn * kTileKeys * 128, map_k, pn * 64, y, &full[s]);
+            ptx::tma_load_2d(vt + pn * kTileKeys * 128, map_v, pn * 64, y, &full[s]);
           }
         } else {  // paged: the tile's four 16-key blocks, one box when consecutive
-          const int4 y4 = kv_rows4(p.pt, row.cache_row, g, k0 + it * kTileKeys);
+          const int4 y4 = kv_rows4(pt, row.cache_row, g, k0 + it * kTileKeys);
           if (rows4_contiguous(y4)) {
 #pragma unroll
             for (int pn = 0; pn < Cfg::kPanels; ++pn) {
@@ -291,8 +303,10 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
     // the prologue costs one memory round trip.
     const __nv_bfloat16 *q = p.q + (int64_t)row.call_row * p.q_row_stride +
                              (int64_t)g * p.rep * D;
-    const __nv_bfloat16 *k = p.k_new + (int64_t)row.call_row * p.kv_row_stride + (int64_t)g * D;
-    const __nv_bfloat16 *v = p.v_new + (int64_t)row.call_row * p.kv_row_stride + (int64_t)g * D;
+    const __nv_bfloat16 *k = (seg1 ? p.k_new2 : p.k_new) + (int64_t)row.call_row * p.kv_row_stride +
+                             (int64_t)g * D;
+    const __nv_bfloat16 *v = (seg1 ? p.v_new2 : p.v_new) + (int64_t)row.call_row * p.kv_row_stride +
+                             (int64_t)g * D;
     const float2 *cs = p.rope + (int64_t)row.pos * kHalf;
     constexpr int kVec = kHalf / 8;                 // 8-pair chunks per head
     constexpr int kQUnits = NT * 8 * kVec;
@@ -396,7 +410,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
     uint8_t *vt = kt + Cfg::kTileBytes;
     const int key_base = k0 + it * kTileKeys + 16 * warp;  // first key of this warp
     const int n_valid = k1 - key_base;                      // may be <= 0 or >= 16
-    const int skip = owner ? row.slot - key_base : -1;      // stale slot of the new key
+    const int skip = owner ? new_slot - key_base : -1;      // stale slot of the new key
     const bool skip_here = skip >= 0 && skip < 16;
 
     if (n_valid < 16 || skip_here) {
@@ -436,11 +450,12 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
   }
   if (owner) {
     // Every load of this CTA has landed: store the new key and value in the cache.
-    const int64_t dst = kv_row(p.pt, row.cache_row, p.Hk, g, p.seg_rows, row.slot) * D;
+    const int64_t dst = kv_row(pt, row.cache_row, p.Hk, g, seg_rows, new_slot) * D;
+    __nv_bfloat16 *ck = seg1 ? p.cache_k2 : p.cache_k, *cv = seg1 ? p.cache_v2 : p.cache_v;
     for (int ch = threadIdx.x; ch < D / 8; ch += kConsumerWarps * 32) {
-      *reinterpret_cast<uint4 *>(p.cache_k + dst + 8 * ch) =
+      *reinterpret_cast<uint4 *>(ck + dst + 8 * ch) =
           *reinterpret_cast<const uint4 *>(knew + 8 * ch);
-      *reinterpret_cast<uint4 *>(p.cache_v + dst + 8 * ch) =
+      *reinterpret_cast<uint4 *>(cv + dst + 8 * ch) =
           *reinterpret_cast<const uint4 *>(vnew + 8 * ch);
     }
   }
@@ -478,7 +493,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
     }
   consumer_sync();
 
-  const bool single = row.n_splits == 1;
+  const bool single = n_total == 1;
   const int64_t part = (int64_t)row.part0 + split;
   // Per head: the warps' merge weights 2^(m_w - m) (divided by l for a finished output)
   // and this split's (m, l); then 8 consecutive dims per thread, vectorised.
@@ -535,14 +550,14 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
   __threadfence();
   consumer_sync();
   int32_t *ticket = p.counters + (int64_t)row.ctr * p.Hk + g;
-  if (threadIdx.x == 0) *last = atomicAdd(ticket, 1) == row.n_splits - 1;
+  if (threadIdx.x == 0) *last = atomicAdd(ticket, 1) == n_total - 1;
   consumer_sync();
   if (!*last) return;
   __threadfence();
   // Stage every split's (m, l) of the group's heads, turn them into merge weights
   // 2^(m_s - max m) / sum_s 2^(m_s - max m) l_s, then sum the weighted partials with
   // all loads of an element in flight at once.
-  const int ns = row.n_splits;
+  const int ns = n_total;
   const int64_t base = row.part0;
   float2 *wml = reinterpret_cast<float2 *>(tiles);            // [split][rep] (m, l) -> weight
   for (int u = threadIdx.x; u < ns * p.rep; u += kConsumerWarps * 32) {

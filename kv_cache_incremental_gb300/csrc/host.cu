@@ -94,6 +94,12 @@ struct kv_cache {
   std::vector<int> seg_rows;
   std::vector<CUtensorMap> tmK, tmV;
   std::vector<CUtensorMap> tmK16, tmV16;  // paged layers: 16-row boxes over the pool
+  // hybrid layers: K/V above is the group's global storage (owned by the group's full
+  // layer, aliased by its local layers); every hybrid layer also owns a ring
+  std::vector<int> group;                 // full layer of a hybrid layer's group, else -1
+  std::vector<char> owns;                 // K[l] / V[l] allocated for this layer
+  std::vector<void *> RK, RV;             // hybrid rings [B][Hk][R+1][D], else nullptr
+  std::vector<CUtensorMap> tmRK, tmRV;
   CUtensorMap tmSK, tmSV;
   void *scrK = nullptr, *scrV = nullptr;
   float2 *rope = nullptr;
@@ -114,14 +120,29 @@ struct kv_cache {
   int32_t *table = nullptr;                   // device [B][max_blocks]
   std::vector<std::vector<int32_t>> rblocks;  // host: pool blocks of each row, in order
   std::vector<int32_t> free_blocks;           // host: free pool blocks
+  // hybrid full layers: per row, lens + the tokens of its last append in this step (a
+  // local layer of the group may only append the same tokens after it)
+  std::vector<std::vector<int32_t>> hy_end;
 };
 
 namespace {
 
 int set_err(cudaError_t e) { return e == cudaSuccess ? KV_OK : KV_ERR_CUDA; }
 
+bool is_hybrid(int kind) { return kind == KV_HYBRID_FULL || kind == KV_HYBRID_LOCAL; }
+
+bool has_hybrid(const kv_cache *c) {
+  for (int k : c->kind)
+    if (is_hybrid(k)) return true;
+  return false;
+}
+
+// A layer whose storage (K[l], V[l]) is a full-length cache: global layers and the group
+// caches of hybrid layers.
+bool cache_layer(const kv_cache *c, int layer) { return c->kind[layer] != KV_SLIDING; }
+
 bool paged_layer(const kv_cache *c, int layer) {
-  return c->n_blocks > 0 && c->kind[layer] == KV_GLOBAL;
+  return c->n_blocks > 0 && cache_layer(c, layer);
 }
 
 PageTable page_table(const kv_cache *c, int layer) {
@@ -224,29 +245,40 @@ struct DecodeIn {
   int cache_row, call_row, pos;
 };
 
-// Split-K schedule for one batch of decode rows (<= kMaxRowsPerLaunch).
-void plan_decode(const kv_cache *c, bool sliding, const std::vector<DecodeIn> &in,
+// Split-K schedule for one batch of decode rows (<= kMaxRowsPerLaunch).  Segment 0 holds
+// storage slots [0, nk) of the layer storage (the ring of a sliding layer, else a cache);
+// a hybrid layer adds segment 1, its own ring, with its own splits.
+void plan_decode(const kv_cache *c, int layer, const std::vector<DecodeIn> &in,
                  DecodeParams &p, double &kv_bytes, double &flops) {
+  const bool sliding = c->kind[layer] == KV_SLIDING, hybrid = is_hybrid(c->kind[layer]);
+  const auto tiles_of = [](int keys) { return (keys + kTileKeys - 1) / kTileKeys; };
   int64_t total_tiles = 0;
-  std::vector<int> nk(in.size());
+  std::vector<int> nk(in.size()), nk2(in.size(), 0);
   for (size_t i = 0; i < in.size(); ++i) {
     nk[i] = sliding ? std::min(in[i].pos + 1, c->R) : in[i].pos + 1;
-    total_tiles += (nk[i] + kTileKeys - 1) / kTileKeys;
+    if (hybrid) nk2[i] = std::min(in[i].pos + 1, c->R);
+    total_tiles += tiles_of(nk[i]) + tiles_of(nk2[i]);
   }
   // Aim for about four waves of two CTAs per SM; splits of at least eight tiles (512 keys):
   // a shorter row is one CTA with no split merge, which is what small (ring) layers want.
   const int64_t target = (int64_t)c->num_sms * 2 * 4;
   int64_t per = (total_tiles * c->Hk + target - 1) / target;
   if (per < 8) per = 8;
+  // splits of one segment: at most `cap`, each a whole number of tiles
+  const auto splits = [&](int keys, int cap, int &st) {
+    const int tiles = tiles_of(keys);
+    int ns = (int)std::min<int64_t>(cap, (tiles + per - 1) / per);
+    if (ns < 1) ns = 1;
+    st = (tiles + ns - 1) / ns;
+    return (tiles + st - 1) / st;
+  };
   int item = 0, part = 0;
   kv_bytes = 0;
   flops = 0;
   for (size_t i = 0; i < in.size(); ++i) {
-    const int tiles = (nk[i] + kTileKeys - 1) / kTileKeys;
-    int ns = (int)std::min<int64_t>(kMaxSplits, (tiles + per - 1) / per);
-    if (ns < 1) ns = 1;
-    const int st = (tiles + ns - 1) / ns;
-    ns = (tiles + st - 1) / st;
+    int st = 0, st2 = 0;
+    const int ns2 = hybrid ? splits(nk2[i], kMaxSplits / 4, st2) : 0;
+    const int ns = splits(nk[i], kMaxSplits - ns2, st);
     DecodeRow &r = p.rows[i];
     r.cache_row = in[i].cache_row;
     r.call_row = in[i].call_row;
@@ -255,13 +287,18 @@ void plan_decode(const kv_cache *c, bool sliding, const std::vector<DecodeIn> &i
     r.item0 = item;
     r.split_len = st * kTileKeys;
     r.n_splits = ns;
-    r.part0 = ns > 1 ? part : 0;
     r.slot = sliding ? in[i].pos % c->R : in[i].pos;
+    r.nk2 = nk2[i];
+    r.split_len2 = st2 * kTileKeys;
+    r.n_splits2 = ns2;
+    r.slot2 = hybrid ? in[i].pos % c->R : -1;
     r.ctr = in[i].cache_row;
-    if (ns > 1) part += ns;
-    item += ns;
-    kv_bytes += 2.0 * nk[i] * c->Hk * c->D * 2.0;
-    flops += 4.0 * nk[i] * c->Hq * c->D;
+    const int total = ns + ns2;
+    r.part0 = total > 1 ? part : 0;
+    if (total > 1) part += total;
+    item += total;
+    kv_bytes += 2.0 * (nk[i] + nk2[i]) * c->Hk * c->D * 2.0;
+    flops += 4.0 * (nk[i] + nk2[i]) * c->Hq * c->D;
   }
   p.n_rows = (int)in.size();
   p.n_items = item;
@@ -269,11 +306,15 @@ void plan_decode(const kv_cache *c, bool sliding, const std::vector<DecodeIn> &i
 
 // Parameters of one decode launch (fused RoPE + append + split-K attention + merge) for a
 // batch of single-token rows; kv_bytes and flops are the algorithmic counts.
+// A hybrid layer's segment 0 is its group's cache: its new global key (k, v) is appended
+// by the kernel on a full layer only (on a local layer that key is already in the cache);
+// segment 1 is its ring, which takes the new local key (k_local, v_local).
 void fill_decode(const kv_cache *c, int layer, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
                  const __nv_bfloat16 *v, __nv_bfloat16 *out, int64_t q_row, int64_t kv_row,
                  const std::vector<DecodeIn> &batch, DecodeParams &dp, double &bytes,
-                 double &flops) {
-  const bool sliding = c->kind[layer] == KV_SLIDING;
+                 double &flops, const __nv_bfloat16 *k_local = nullptr,
+                 const __nv_bfloat16 *v_local = nullptr) {
+  const bool hybrid = is_hybrid(c->kind[layer]);
   dp.tmap_k = c->tmK[layer];
   dp.tmap_v = c->tmV[layer];
   dp.q = q;
@@ -290,7 +331,7 @@ void fill_decode(const kv_cache *c, int layer, const __nv_bfloat16 *q, const __n
   dp.kv_row_stride = kv_row;
   dp.cache_k = (__nv_bfloat16 *)c->K[layer];
   dp.cache_v = (__nv_bfloat16 *)c->V[layer];
-  dp.fuse_append = 1;
+  dp.fuse_append = c->kind[layer] != KV_HYBRID_LOCAL;
   dp.Hq = c->Hq;
   dp.Hk = c->Hk;
   dp.rep = c->Hq / c->Hk;
@@ -299,17 +340,31 @@ void fill_decode(const kv_cache *c, int layer, const __nv_bfloat16 *q, const __n
   dp.pt = page_table(c, layer);
   dp.tmap_k16 = c->tmK16[layer];
   dp.tmap_v16 = c->tmV16[layer];
+  dp.fuse_append2 = hybrid ? 1 : 0;
+  dp.tmap_k2 = hybrid ? c->tmRK[layer] : c->tmK[layer];
+  dp.tmap_v2 = hybrid ? c->tmRV[layer] : c->tmV[layer];
+  dp.k_new2 = k_local;
+  dp.v_new2 = v_local;
+  dp.cache_k2 = (__nv_bfloat16 *)c->RK[layer];
+  dp.cache_v2 = (__nv_bfloat16 *)c->RV[layer];
+  dp.seg_rows2 = c->R + 1;
   double kvb = 0;
-  plan_decode(c, sliding, batch, dp, kvb, flops);
-  // q, k, v in; new K and V and the output out
-  bytes = kvb + (double)batch.size() * (c->Hq + 2 * c->Hk) * c->D * 2.0 * 2.0;
+  plan_decode(c, layer, batch, dp, kvb, flops);
+  // q, k, v in (and a hybrid layer's local k, v); new K and V and the output out
+  bytes = kvb + (double)batch.size() * (c->Hq + (hybrid ? 4 : 2) * c->Hk) * c->D * 2.0 * 2.0;
 }
 
+// One layer's chunk for rows `cache_rows`.  k, v: the keys and values of the layer
+// storage (a hybrid layer: its group's global keys, nullptr on a local layer); kl, vl: a
+// hybrid layer's own local keys and values (its ring), else nullptr.
 int append_device(kv_cache *c, int layer, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
                   const __nv_bfloat16 *v, int C, const int32_t *n_new,
                   const std::vector<int32_t> &cache_rows, int Bs, __nv_bfloat16 *out,
-                  cudaStream_t s) {
-  const bool sliding = c->kind[layer] == KV_SLIDING;
+                  cudaStream_t s, const __nv_bfloat16 *kl = nullptr,
+                  const __nv_bfloat16 *vl = nullptr) {
+  const bool sliding = c->kind[layer] == KV_SLIDING, hybrid = is_hybrid(c->kind[layer]);
+  const bool writes_global = c->kind[layer] != KV_HYBRID_LOCAL;  // appends k, v anywhere
+  const bool ringed = sliding || hybrid;                          // keeps a ring
   const int Hq = c->Hq, Hk = c->Hk, D = c->D, rep = Hq / Hk;
   int max_n = 0;
   for (int i = 0; i < Bs; ++i) max_n = std::max(max_n, (int)n_new[i]);
@@ -330,7 +385,7 @@ int append_device(kv_cache *c, int layer, const __nv_bfloat16 *q, const __nv_bfl
   const float scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
 
   for (int off = 0; off < max_n; off += kChunk) {
-    std::vector<AppendRow> arows;
+    std::vector<AppendRow> arows, lrows;  // to the layer storage / a hybrid ring's scratch
     std::vector<DecodeIn> drows;
     std::vector<PrefillRow> prows;
     for (int i = 0; i < Bs; ++i) {
@@ -340,16 +395,22 @@ int append_device(kv_cache *c, int layer, const __nv_bfloat16 *q, const __nv_bfl
         drows.push_back({b, i, c->lens[b]});  // appended inside the decode kernel
       } else if (n >= 2 && n - off >= 1) {
         const int ns = std::min(kChunk, n - off);
-        arows.push_back({b, i, c->lens[b] + off, ns, sliding ? kDestScratch : kDestGlobal, 0});
+        if (writes_global)
+          arows.push_back({b, i, c->lens[b] + off, ns, sliding ? kDestScratch : kDestGlobal, 0});
+        if (hybrid) lrows.push_back({b, i, c->lens[b] + off, ns, kDestScratch, 0});
         prows.push_back({b, i, c->lens[b] + off, ns, 0});
       }
     }
 
-    // ---- RoPE + append (decode rows and chunk rows of this sub-chunk)
-    for (size_t r0 = 0; r0 < arows.size(); r0 += kMaxRowsPerLaunch) {
-      const size_t r1 = std::min(arows.size(), r0 + kMaxRowsPerLaunch);
-      ap.k = k + (int64_t)off * Hk * D;
-      ap.v = v + (int64_t)off * Hk * D;
+    // ---- RoPE + append of the chunk rows of this sub-chunk (a hybrid layer: the global
+    // keys to the group's cache, then its local keys to the chunk scratch)
+    for (int pass = 0; pass < 2; ++pass) {
+    const std::vector<AppendRow> &rows_p = pass == 0 ? arows : lrows;
+    const __nv_bfloat16 *kp = pass == 0 ? k : kl, *vp = pass == 0 ? v : vl;
+    for (size_t r0 = 0; r0 < rows_p.size(); r0 += kMaxRowsPerLaunch) {
+      const size_t r1 = std::min(rows_p.size(), r0 + kMaxRowsPerLaunch);
+      ap.k = kp + (int64_t)off * Hk * D;
+      ap.v = vp + (int64_t)off * Hk * D;
       ap.kv_row_stride = kv_row;
       ap.cache_k = (__nv_bfloat16 *)c->K[layer];
       ap.cache_v = (__nv_bfloat16 *)c->V[layer];
@@ -366,7 +427,7 @@ int append_device(kv_cache *c, int layer, const __nv_bfloat16 *q, const __nv_bfl
       int blk = 0;
       double bytes = 0;
       for (size_t j = r0; j < r1; ++j) {
-        AppendRow r = arows[j];
+        AppendRow r = rows_p[j];
         r.blk0 = blk;
         blk += (r.n + 7) / 8;
         ap.rows[j - r0] = r;
@@ -377,13 +438,14 @@ int append_device(kv_cache *c, int layer, const __nv_bfloat16 *q, const __nv_bfl
       cudaError_t e = timed(c, KV_KERNEL_APPEND, bytes, 0, s, [&] { return launch_append(ap, s); });
       if (e != cudaSuccess) return KV_ERR_CUDA;
     }
+    }
 
     // ---- split-K decode for single-token rows (append and split merge fused in)
     for (size_t r0 = 0; r0 < drows.size(); r0 += kMaxRowsPerLaunch) {
       const size_t r1 = std::min(drows.size(), r0 + kMaxRowsPerLaunch);
       std::vector<DecodeIn> batch(drows.begin() + r0, drows.begin() + r1);
       double bytes = 0, fl = 0;
-      fill_decode(c, layer, q, k, v, out, q_row, kv_row, batch, dp, bytes, fl);
+      fill_decode(c, layer, q, k, v, out, q_row, kv_row, batch, dp, bytes, fl, kl, vl);
       const int nt = rep <= 8 ? 1 : 2;
       cudaError_t e = timed(c, KV_KERNEL_DECODE, bytes, fl, s,
                             [&] { return launch_decode(dp, D, nt, s); });
@@ -392,11 +454,12 @@ int append_device(kv_cache *c, int layer, const __nv_bfloat16 *q, const __nv_bfl
 
     // ---- chunked prefill (+ ring commit on sliding layers).  Rows whose GQA group x
     // chunk gives at least 64 query rows go to the tcgen05 kernel (128-row tiles);
-    // smaller ones to the mma.sync kernel (16-row warp tiles).
+    // smaller ones to the mma.sync kernel (16-row warp tiles).  Hybrid layers (three key
+    // segments) all go to the tcgen05 kernel.
     for (int kind = 0; kind < 2; ++kind) {
       std::vector<PrefillRow> sel;
       for (const PrefillRow &r : prows)
-        if ((r.n * rep >= kTcMinRows) == (kind == 1)) sel.push_back(r);
+        if ((hybrid || r.n * rep >= kTcMinRows) == (kind == 1)) sel.push_back(r);
       const int rows_per_cta = kind == 1 ? prefill_tc_rows_per_cta() : 64;
       for (size_t r0 = 0; r0 < sel.size(); r0 += kMaxRowsPerLaunch) {
         const size_t r1 = std::min(sel.size(), r0 + kMaxRowsPerLaunch);
@@ -421,6 +484,10 @@ int append_device(kv_cache *c, int layer, const __nv_bfloat16 *q, const __nv_bfl
         pp.pt = page_table(c, layer);
         pp.tmap_k16 = c->tmK16[layer];
         pp.tmap_v16 = c->tmV16[layer];
+        pp.hybrid = hybrid ? 1 : 0;
+        pp.tmap_k2 = hybrid ? c->tmRK[layer] : c->tmK[layer];
+        pp.tmap_v2 = hybrid ? c->tmRV[layer] : c->tmV[layer];
+        pp.seg_rows2 = c->R + 1;
         int cta = 0;
         double bytes = 0, fl = 0;
         for (size_t j = r0; j < r1; ++j) {
@@ -428,11 +495,13 @@ int append_device(kv_cache *c, int layer, const __nv_bfloat16 *q, const __nv_bfl
           r.cta0 = cta;
           cta += (r.n * rep + rows_per_cta - 1) / rows_per_cta;
           pp.rows[j - r0] = r;
-          const int keys = sliding ? std::min(r.lens, c->R) + r.n : r.lens + r.n;
+          const int lkeys = std::min(r.lens, c->R) + r.n;
+          const int keys = sliding ? lkeys : hybrid ? r.lens + r.n + lkeys : r.lens + r.n;
           bytes += 2.0 * keys * Hk * D * 2.0 + 2.0 * r.n * Hq * D * 2.0;
           for (int t = 0; t < r.n; ++t) {
             const int pz = r.lens + t;
-            const int vis = sliding ? std::min(pz + 1, c->W) : pz + 1;
+            const int lvis = std::min(pz + 1, c->W);
+            const int vis = sliding ? lvis : hybrid ? pz + 1 + lvis : pz + 1;
             fl += 4.0 * vis * Hq * D;
           }
         }
@@ -444,18 +513,18 @@ int append_device(kv_cache *c, int layer, const __nv_bfloat16 *q, const __nv_bfl
         if (e != cudaSuccess) return KV_ERR_CUDA;
       }
     }
-    if (sliding) {
+    if (ringed) {
       for (size_t r0 = 0; r0 < prows.size(); r0 += kMaxRowsPerLaunch) {
         const size_t r1 = std::min(prows.size(), r0 + kMaxRowsPerLaunch);
         mp.scr_k = (const __nv_bfloat16 *)c->scrK;
         mp.scr_v = (const __nv_bfloat16 *)c->scrV;
-        mp.ring_k = (__nv_bfloat16 *)c->K[layer];
-        mp.ring_v = (__nv_bfloat16 *)c->V[layer];
+        mp.ring_k = (__nv_bfloat16 *)(hybrid ? c->RK[layer] : c->K[layer]);
+        mp.ring_v = (__nv_bfloat16 *)(hybrid ? c->RV[layer] : c->V[layer]);
         mp.Hk = Hk;
         mp.D = D;
         mp.ring_R = c->R;
         mp.window = c->W;
-        mp.seg_rows = c->seg_rows[layer];
+        mp.seg_rows = hybrid ? c->R + 1 : c->seg_rows[layer];
         double cb = 0;
         for (size_t j = r0; j < r1; ++j) {
           mp.cache_row[j - r0] = prows[j].cache_row;
@@ -504,8 +573,13 @@ int state_update(kv_cache *c, const std::vector<int32_t> &rows, const int32_t *n
 }
 
 void free_all(kv_cache *c) {
-  for (void *p : c->K) cudaFree(p);
-  for (void *p : c->V) cudaFree(p);
+  for (size_t l = 0; l < c->K.size(); ++l)
+    if (l < c->owns.size() && c->owns[l]) {
+      cudaFree(c->K[l]);
+      cudaFree(c->V[l]);
+    }
+  for (void *p : c->RK) cudaFree(p);
+  for (void *p : c->RV) cudaFree(p);
   cudaFree(c->scrK);
   cudaFree(c->scrV);
   cudaFree(c->rope);
@@ -539,10 +613,15 @@ static int create_impl(kv_cache **out, int B, int max_len, int Hq, int Hk, int D
       Hq / Hk > kMaxRep || (D != 64 && D != 128) || n_layers < 1 || !layer_kind ||
       !(rope_theta > 0.0) || device < 0)
     return KV_ERR_ARG;
-  bool any_sliding = false;
+  bool any_sliding = false;  // any ring (sliding or hybrid layers)
+  int last_full = -1;
   for (int l = 0; l < n_layers; ++l) {
-    if (layer_kind[l] != KV_GLOBAL && layer_kind[l] != KV_SLIDING) return KV_ERR_ARG;
-    any_sliding |= layer_kind[l] == KV_SLIDING;
+    const int k = layer_kind[l];
+    if (k != KV_GLOBAL && k != KV_SLIDING && k != KV_HYBRID_FULL && k != KV_HYBRID_LOCAL)
+      return KV_ERR_ARG;
+    if (k == KV_HYBRID_FULL) last_full = l;
+    if (k == KV_HYBRID_LOCAL && last_full < 0) return KV_ERR_ARG;  // no group to read
+    any_sliding |= k != KV_GLOBAL;
   }
   if (any_sliding && W < 1) return KV_ERR_ARG;
   const int R = any_sliding ? (W < max_len ? W : max_len) : 0;
@@ -590,10 +669,50 @@ static int create_impl(kv_cache **out, int B, int max_len, int Hq, int Hk, int D
     c->rblocks.assign(B, {});
     for (int b = n_blocks - 1; b >= 0; --b) c->free_blocks.push_back(b);
   }
+  int group_full = -1;
+  c->hy_end.assign(n_layers, {});
   for (int l = 0; l < n_layers; ++l) {
-    // dense: [B][Hk][rows][D]; paged global layer: pool [Hk][n_blocks][16][D]
-    const bool pg = n_blocks > 0 && c->kind[l] == KV_GLOBAL;
+    if (c->kind[l] == KV_HYBRID_FULL) {
+      group_full = l;
+      c->hy_end[l].assign(B, 0);
+    }
+    c->group.push_back(is_hybrid(c->kind[l]) ? group_full : -1);
+    // the ring of a hybrid layer
+    if (is_hybrid(c->kind[l])) {
+      const size_t rbytes = (size_t)B * Hk * (R + 1) * D * 2;
+      void *rk = nullptr, *rv = nullptr;
+      if (!alloc(&rk, rbytes)) return fail(KV_ERR_OOM);
+      c->RK.push_back(rk);
+      if (!alloc(&rv, rbytes)) return fail(KV_ERR_OOM);
+      c->RV.push_back(rv);
+      CUtensorMap rmk, rmv;
+      if (!make_tmap(&rmk, rk, (int64_t)B * Hk * (R + 1), D) ||
+          !make_tmap(&rmv, rv, (int64_t)B * Hk * (R + 1), D))
+        return fail(KV_ERR_CUDA);
+      c->tmRK.push_back(rmk);
+      c->tmRV.push_back(rmv);
+    } else {
+      c->RK.push_back(nullptr);
+      c->RV.push_back(nullptr);
+      c->tmRK.push_back(CUtensorMap{});
+      c->tmRV.push_back(CUtensorMap{});
+    }
+    if (c->kind[l] == KV_HYBRID_LOCAL) {  // the group's cache, owned by its full layer
+      const int f = c->group[l];
+      c->K.push_back(c->K[f]);
+      c->V.push_back(c->V[f]);
+      c->owns.push_back(0);
+      c->seg_rows.push_back(c->seg_rows[f]);
+      c->tmK.push_back(c->tmK[f]);
+      c->tmV.push_back(c->tmV[f]);
+      c->tmK16.push_back(c->tmK16[f]);
+      c->tmV16.push_back(c->tmV16[f]);
+      continue;
+    }
+    // dense: [B][Hk][rows][D]; paged cache layer: pool [Hk][n_blocks][16][D]
+    const bool pg = n_blocks > 0 && c->kind[l] != KV_SLIDING;
     const int rows = pg ? kBlockTokens : c->kind[l] == KV_SLIDING ? R + 1 : max_len + 1;
+    c->owns.push_back(1);
     const int64_t units = pg ? n_blocks : B;
     const size_t bytes = (size_t)units * Hk * rows * D * 2;
     void *k = nullptr, *v = nullptr;
@@ -713,6 +832,8 @@ int kv_reset(kv_cache *c, const int32_t *rows, int n_rows, void *stream) {
   for (int r : rv) {
     c->lens[r] = 0;
     release_blocks(c, r, 0);  // later launches on this stream may reuse them
+    for (auto &he : c->hy_end)
+      if (!he.empty()) he[r] = 0;
   }
   return KV_OK;
 }
@@ -720,6 +841,7 @@ int kv_reset(kv_cache *c, const int32_t *rows, int n_rows, void *stream) {
 int kv_append(kv_cache *c, int layer, const void *q, const void *k, const void *v, int Hq, int C,
               const int32_t *n_new, const int32_t *rows, int Bs, void *out, void *stream) {
   if (!c || layer < 0 || layer >= c->n_layers || Hq != c->Hq || C < 1) return KV_ERR_ARG;
+  if (is_hybrid(c->kind[layer])) return KV_ERR_ARG;  // kv_append_hybrid
   std::vector<int32_t> cache_rows;
   const int rc = check_rows(c, n_new, rows, Bs, C, cache_rows);
   if (rc != KV_OK) return rc;
@@ -750,6 +872,7 @@ int kv_append_host(kv_cache *c, int layer, const void *q, const void *k, const v
                    int C, const int32_t *n_new, const int32_t *rows, int Bs, void *out,
                    void *stream) {
   if (!c || layer < 0 || layer >= c->n_layers || Hq != c->Hq || C < 1) return KV_ERR_ARG;
+  if (is_hybrid(c->kind[layer])) return KV_ERR_ARG;
   std::vector<int32_t> cache_rows;
   const int rc = check_rows(c, n_new, rows, Bs, C, cache_rows);
   if (rc != KV_OK) return rc;
@@ -793,6 +916,44 @@ int kv_append_host(kv_cache *c, int layer, const void *q, const void *k, const v
   return set_err(cudaMemcpyAsync(out, dout, qb, cudaMemcpyDeviceToHost, s));
 }
 
+int kv_append_hybrid(kv_cache *c, int layer, const void *q, const void *k_local,
+                     const void *v_local, const void *k_global, const void *v_global, int Hq,
+                     int C, const int32_t *n_new, const int32_t *rows, int Bs, void *out,
+                     void *stream) {
+  if (!c || layer < 0 || layer >= c->n_layers || Hq != c->Hq || C < 1) return KV_ERR_ARG;
+  if (!is_hybrid(c->kind[layer])) return KV_ERR_ARG;
+  const bool full = c->kind[layer] == KV_HYBRID_FULL;
+  std::vector<int32_t> cache_rows;
+  const int rc = check_rows(c, n_new, rows, Bs, C, cache_rows);
+  if (rc != KV_OK) return rc;
+  bool any = false;
+  for (int i = 0; i < Bs; ++i) any |= n_new[i] > 0;
+  if (!any) return KV_OK;
+  if (!q || !k_local || !v_local || !out || !aligned16(q) || !aligned16(k_local) ||
+      !aligned16(v_local) || !aligned16(out))
+    return KV_ERR_ARG;
+  if (full ? (!k_global || !v_global || !aligned16(k_global) || !aligned16(v_global))
+           : (k_global || v_global))
+    return KV_ERR_ARG;
+  // a local layer reads the group's global keys of these tokens: its full layer must
+  // have appended exactly them
+  const std::vector<int32_t> &he = c->hy_end[c->group[layer]];
+  if (!full)
+    for (int i = 0; i < Bs; ++i)
+      if (n_new[i] > 0 && he[cache_rows[i]] != c->lens[cache_rows[i]] + n_new[i])
+        return KV_ERR_ARG;
+  DeviceGuard guard(c->device);
+  const int r = append_device(c, layer, (const __nv_bfloat16 *)q,
+                              (const __nv_bfloat16 *)k_global, (const __nv_bfloat16 *)v_global,
+                              C, n_new, cache_rows, Bs, (__nv_bfloat16 *)out,
+                              (cudaStream_t)stream, (const __nv_bfloat16 *)k_local,
+                              (const __nv_bfloat16 *)v_local);
+  if (r == KV_OK && full)
+    for (int i = 0; i < Bs; ++i)
+      if (n_new[i] > 0) c->hy_end[layer][cache_rows[i]] = c->lens[cache_rows[i]] + n_new[i];
+  return r;
+}
+
 int kv_advance(kv_cache *c, const int32_t *n_new, const int32_t *rows, int Bs, void *stream) {
   if (!c) return KV_ERR_ARG;
   std::vector<int32_t> cache_rows;
@@ -808,9 +969,12 @@ int kv_advance(kv_cache *c, const int32_t *n_new, const int32_t *rows, int Bs, v
 int64_t kv_nbytes(const kv_cache *c) {
   if (!c) return -1;
   int64_t total = 0;
-  for (int l = 0; l < c->n_layers; ++l)
-    total += paged_layer(c, l) ? 2LL * c->n_blocks * c->Hk * kBlockTokens * c->D * 2
-                               : 2LL * c->B * c->Hk * c->seg_rows[l] * c->D * 2;
+  for (int l = 0; l < c->n_layers; ++l) {
+    if (c->owns[l])
+      total += paged_layer(c, l) ? 2LL * c->n_blocks * c->Hk * kBlockTokens * c->D * 2
+                                 : 2LL * c->B * c->Hk * c->seg_rows[l] * c->D * 2;
+    if (c->RK[l]) total += 2LL * c->B * c->Hk * (c->R + 1) * c->D * 2;  // a hybrid ring
+  }
   return total;
 }
 
@@ -825,6 +989,13 @@ int kv_debug_ptrs(const kv_cache *c, int layer, void **K, void **V, int32_t **lp
   if (K) *K = c->K[layer];
   if (V) *V = c->V[layer];
   if (lpos) *lpos = c->lpos;
+  return KV_OK;
+}
+
+int kv_debug_ring_ptrs(const kv_cache *c, int layer, void **K, void **V) {
+  if (!c || layer < 0 || layer >= c->n_layers || !is_hybrid(c->kind[layer])) return KV_ERR_ARG;
+  if (K) *K = c->RK[layer];
+  if (V) *V = c->RV[layer];
   return KV_OK;
 }
 
@@ -961,7 +1132,7 @@ int kv_step_graph_create(kv_cache *c, kv_step_graph **out, const void *const *q,
                          const void *const *k, const void *const *v, void *const *outp, int Hq,
                          const int32_t *rows, int Bs) {
   if (!c || !out || !q || !k || !v || !outp || Hq != c->Hq) return KV_ERR_ARG;
-  if (Bs < 1 || Bs > c->B || Bs > kMaxRowsPerLaunch) return KV_ERR_ARG;
+  if (Bs < 1 || Bs > c->B || Bs > kMaxRowsPerLaunch || has_hybrid(c)) return KV_ERR_ARG;
   std::vector<int32_t> cache_rows;
   std::vector<char> seen(c->B, 0);
   for (int i = 0; i < Bs; ++i) {
@@ -1157,7 +1328,7 @@ extern "C" {
 int kv_copy_rows(kv_cache *dst, const int32_t *dst_rows, const kv_cache *src,
                  const int32_t *src_rows, const int32_t *keep, int n, void *stream) {
   if (!dst || !src || n < 0 || (n > 0 && (!dst_rows || !src_rows))) return KV_ERR_ARG;
-  if (!same_layout(dst, src)) return KV_ERR_ARG;
+  if (!same_layout(dst, src) || has_hybrid(src)) return KV_ERR_ARG;
   std::vector<int32_t> kp(n);
   std::vector<char> dseen(dst->B, 0);
   for (int i = 0; i < n; ++i) {
@@ -1215,7 +1386,7 @@ int kv_copy_rows(kv_cache *dst, const int32_t *dst_rows, const kv_cache *src,
 }
 
 int64_t kv_export_bytes(const kv_cache *c, int keep) {
-  if (!c || keep < 0 || keep > c->max_len) return -1;
+  if (!c || keep < 0 || keep > c->max_len || has_hybrid(c)) return -1;
   int64_t b = 0;
   for (int l = 0; l < c->n_layers; ++l)
     b += 2LL * c->Hk * (keep - first_kept(c, l, keep)) * c->D * 2;

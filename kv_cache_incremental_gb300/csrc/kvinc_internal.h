@@ -100,17 +100,21 @@ struct AppendParams {
 };
 
 // ---------------------------------------------------------------- decode
+// Keys of a decode row: segment 0 (storage slots [0, nk) of the layer storage) and, for a
+// hybrid layer, segment 1 (its ring, slots [0, nk2)); each segment has its own splits, and
+// the items of segment 1 follow those of segment 0.  All splits merge into one output.
 struct DecodeRow {
   int32_t cache_row;
   int32_t call_row;
   int32_t pos;        // absolute position of the new token
-  int32_t nk;         // keys to scan: storage slots [0, nk)
+  int32_t nk;         // segment 0: storage slots [0, nk)
   int32_t item0;      // first work item of this row
-  int32_t split_len;  // keys per split (multiple of kTileKeys)
-  int32_t n_splits;
+  int32_t split_len;  // segment 0 keys per split (multiple of kTileKeys)
+  int32_t n_splits;   // segment 0 splits
   int32_t part0;      // first partial slot of this row (items of multi-split rows)
-  int32_t slot;       // storage slot of the new token's key (fused append)
+  int32_t slot;       // segment 0 storage slot of the new token's key (fused append)
   int32_t ctr;        // row index of this row's merge tickets
+  int32_t nk2, split_len2, n_splits2, slot2;  // segment 1 (hybrid ring); n_splits2 = 0 else
 };
 
 struct DecodeParams {  // 64-byte aligned through its CUtensorMap members
@@ -138,6 +142,13 @@ struct DecodeParams {  // 64-byte aligned through its CUtensorMap members
   int n_rows, n_items;
   float scale_log2;         // log2(e) / sqrt(D)
   PageTable pt;             // paged global layer (tmap_k16 / tmap_v16 valid)
+  // segment 1 of a hybrid layer: the layer's own ring and its new local key
+  CUtensorMap tmap_k2;
+  CUtensorMap tmap_v2;
+  const __nv_bfloat16 *k_new2, *v_new2;
+  __nv_bfloat16 *cache_k2, *cache_v2;  // ring storage [B][Hk][seg_rows2][D]
+  int seg_rows2;
+  int fuse_append2;
   DecodeRow rows[kMaxRowsPerLaunch];
 };
 
@@ -169,6 +180,12 @@ struct PrefillParams {  // 64-byte aligned through its CUtensorMap members
   int n_rows, n_ctas;
   float scale_log2;
   PageTable pt;             // paged global layer (tmap_k16 / tmap_v16 valid)
+  // hybrid layer: keys = the group's cache (tmap_k/v) + the layer's ring (tmap_k2/v2,
+  // seg_rows2 rows per (row, kv head)) + the chunk scratch
+  int hybrid;
+  CUtensorMap tmap_k2;
+  CUtensorMap tmap_v2;
+  int seg_rows2;
   PrefillRow rows[kMaxRowsPerLaunch];
 };
 
@@ -239,5 +256,15 @@ cudaError_t launch_commit(const CommitParams &p, cudaStream_t s);
 cudaError_t launch_state(const StateParams &p, cudaStream_t s);
 // Opt kernels into their dynamic shared memory sizes (once per process and device).
 cudaError_t configure_kernels();
+
+// Kernel parameters are passed by value: at most 32764 bytes per launch.
+constexpr size_t kMaxParamBytes = 32764;
+static_assert(sizeof(DecodeParams) <= kMaxParamBytes, "decode parameters too large");
+static_assert(sizeof(PrefillParams) <= kMaxParamBytes, "prefill parameters too large");
+static_assert(sizeof(AppendParams) <= kMaxParamBytes, "append parameters too large");
+static_assert(sizeof(CommitParams) <= kMaxParamBytes, "commit parameters too large");
+static_assert(sizeof(CopyParams) <= kMaxParamBytes, "copy parameters too large");
+static_assert(sizeof(TableParams) <= kMaxParamBytes, "table parameters too large");
+static_assert(sizeof(StateParams) <= kMaxParamBytes, "state parameters too large");
 
 }  // namespace kvinc

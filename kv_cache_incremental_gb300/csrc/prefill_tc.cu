@@ -75,21 +75,23 @@ __device__ __forceinline__ int find_cta_row(const PrefillParams &p, int b) {
 }
 
 // Visible key indices of one query row within a key segment, as two inclusive ranges
-// (an empty range has lo > hi).  Global layer: cache slots 0..p.  Sliding layer, ring
-// segment: slot s holds position s + base (s <= rem) or s + base - R (s > rem), or just s
-// while lens <= R; it is visible iff that position is >= p - W + 1.  Sliding layer, chunk
-// scratch: token j sits at lens + j and is visible iff p - W + 1 <= lens + j <= p.
-__device__ __forceinline__ void row_ranges(bool ring_or_cache, bool qvalid, int qpos, int lens,
+// (an empty range has lo > hi).  mode 0, a global cache (which holds this chunk too): slots
+// 0..p.  mode 1, a ring: slot s holds position s + base (s <= rem) or s + base - R
+// (s > rem), or just s while lens <= R; it is visible iff that position is >= p - W + 1.
+// mode 2, the chunk scratch: token j sits at lens + j and is visible iff
+// p - W + 1 <= lens + j <= p.
+enum SegMode { kSegGlobal = 0, kSegRing = 1, kSegScratch = 2 };
+__device__ __forceinline__ void row_ranges(int mode, bool qvalid, int qpos, int lens,
                                            const PrefillParams &p, int (&rg)[4]) {
   rg[0] = 1; rg[1] = 0; rg[2] = 1; rg[3] = 0;
   if (!qvalid) return;
-  if (!p.sliding) {  // the global cache holds this chunk too: slots 0..qpos
+  if (mode == kSegGlobal) {
     rg[0] = 0;
     rg[1] = qpos;
     return;
   }
   const int thr = qpos - p.window + 1;  // first visible position
-  if (!ring_or_cache) {                 // chunk scratch
+  if (mode == kSegScratch) {
     rg[0] = max(0, thr - lens);
     rg[1] = qpos - lens;
     return;
@@ -152,13 +154,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  const int len_a = p.sliding ? min(lens, p.ring_R) : lens + t_max + 1;
-  const int len_b = p.sliding ? t_max + 1 : 0;
-  const int tiles_a = (len_a + kKeys - 1) / kKeys;
-  const int n_tiles = tiles_a + (len_b + kKeys - 1) / kKeys;  // 64-key tiles
+  // Key segments: 0 the layer storage (a global cache: slots [0, lens + t_max]; a sliding
+  // layer: its ring), 1 a hybrid layer's own ring (after its group's cache), 2 the chunk
+  // scratch (sliding and hybrid layers).  Tiles of segment s start at tile seg_t0[s].
+  // (scalars, not arrays: a runtime index would put them in local memory)
+  const int sl0 = p.sliding && !p.hybrid ? min(lens, p.ring_R) : lens + t_max + 1;
+  const int sl1 = p.hybrid ? min(lens, p.ring_R) : 0;
+  const int sl2 = p.sliding || p.hybrid ? t_max + 1 : 0;
+  const int st1 = (sl0 + kKeys - 1) / kKeys, st2 = st1 + (sl1 + kKeys - 1) / kKeys;
+  const int n_tiles = st2 + (sl2 + kKeys - 1) / kKeys;  // 64-key tiles
+  const int seg0_mode = p.sliding && !p.hybrid ? kSegRing : kSegGlobal;
+  auto seg_of = [&](int j) { return j < st1 ? 0 : j < st2 ? 1 : 2; };
+  auto seg_len = [&](int sg) { return sg == 0 ? sl0 : sg == 1 ? sl1 : sl2; };
+  auto seg_t0 = [&](int sg) { return sg == 0 ? 0 : sg == 1 ? st1 : st2; };
   const int n_blocks = (n_tiles + 1) / 2;                      // 128-key blocks
-  const int64_t base_a = ((int64_t)row.cache_row * p.Hk + g) * p.seg_rows;
-  const int64_t base_b = ((int64_t)row.cache_row * p.Hk + g) * kChunk;
+  const int64_t rh = (int64_t)row.cache_row * p.Hk + g;
+  auto seg_base = [&](int sg) {
+    return rh * (sg == 0 ? p.seg_rows : sg == 1 ? p.seg_rows2 : kChunk);
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -238,11 +251,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_arrive_expect_tx(&kv_full[s], halves * 2 * Cfg::kPanels * Cfg::kHalfBytes);
         for (int h = 0; h < halves; ++h) {
           const int j = 2 * it + h;
-          const bool in_a = j < tiles_a;
-          const CUtensorMap *mk = in_a ? &p.tmap_k : &p.tmap_sk;
-          const CUtensorMap *mv = in_a ? &p.tmap_v : &p.tmap_sv;
-          const int y = static_cast<int>(in_a ? base_a + (int64_t)j * kKeys
-                                              : base_b + (int64_t)(j - tiles_a) * kKeys);
+          const int sg = seg_of(j);
+          const CUtensorMap *mk = sg == 0 ? &p.tmap_k : sg == 1 ? &p.tmap_k2 : &p.tmap_sk;
+          const CUtensorMap *mv = sg == 0 ? &p.tmap_v : sg == 1 ? &p.tmap_v2 : &p.tmap_sv;
+          const bool in_a = sg == 0;
+          const int y = static_cast<int>(seg_base(sg) + (int64_t)(j - seg_t0(sg)) * kKeys);
           int4 y4 = make_int4(y, y + kBlockTokens, y + 2 * kBlockTokens, y + 3 * kBlockTokens);
           if (in_a && p.pt.max_blocks) y4 = kv_rows4(p.pt, row.cache_row, g, j * kKeys);
           if (rows4_contiguous(y4)) {  // dense, or a paged tile of consecutive blocks
@@ -300,8 +313,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       // A tile of the block is partial when a segment ends inside it.
       auto partial = [&](int j) {
-        return j < n_tiles && ((j == tiles_a - 1 && len_a % kKeys != 0) ||
-                               (j == n_tiles - 1 && j >= tiles_a && len_b % kKeys != 0));
+        if (j >= n_tiles) return false;
+        const int sg = seg_of(j);
+        const int next = sg == 0 ? st1 : sg == 1 ? st2 : n_tiles;
+        return j == next - 1 && seg_len(sg) % kKeys != 0;
       };
       // PV(b): O += P V over the block's tiles.  B = V as stored by TMA: rows = keys (K),
       // 64-dim panels (MN) kPanelBytes apart; A = P of tile h in S-buffer columns
@@ -361,9 +376,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tmem + qt * kBlockKeys + lane_off;
     float m_used = -INFINITY;
     // visible key-index ranges of this row in the two segments
-    int rga[4], rgb[4];
-    row_ranges(true, qvalid, qpos, lens, p, rga);
-    row_ranges(false, qvalid, qpos, lens, p, rgb);
+    int rg3[3][4];
+    row_ranges(seg0_mode, qvalid, qpos, lens, p, rg3[0]);
+    row_ranges(kSegRing, qvalid, qpos, lens, p, rg3[1]);
+    row_ranges(kSegScratch, qvalid, qpos, lens, p, rg3[2]);
     // Mask and scale (log2 units) of 64-key tile j: returns its key base within the
     // segment and the two ranges, or all_vis when the whole tile is visible.
     struct TileMask {
@@ -372,12 +388,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     auto tile_mask = [&](int j) {
       TileMask m;
-      const bool in_a = j < tiles_a;
-      m.kb = (in_a ? j : j - tiles_a) * kKeys;
-      m.r0 = in_a ? rga[0] : rgb[0];
-      m.r1 = in_a ? rga[1] : rgb[1];
-      m.r2 = in_a ? rga[2] : rgb[2];
-      m.r3 = in_a ? rga[3] : rgb[3];
+      const int sg = seg_of(j);
+      m.kb = (j - seg_t0(sg)) * kKeys;
+      m.r0 = sg == 0 ? rg3[0][0] : sg == 1 ? rg3[1][0] : rg3[2][0];
+      m.r1 = sg == 0 ? rg3[0][1] : sg == 1 ? rg3[1][1] : rg3[2][1];
+      m.r2 = sg == 0 ? rg3[0][2] : sg == 1 ? rg3[1][2] : rg3[2][2];
+      m.r3 = sg == 0 ? rg3[0][3] : sg == 1 ? rg3[1][3] : rg3[2][3];
       m.all_vis = (m.kb >= m.r0 && m.kb + kKeys - 1 <= m.r1) ||
                   (m.kb >= m.r2 && m.kb + kKeys - 1 <= m.r3);
       return m;
@@ -475,16 +491,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     // before both PVs are issued).  Returns -1 on a timeout, 1 if rows were zeroed.
     auto zero_v = [&](int b, int h) -> int {
       const int j = 2 * b + h;
-      const bool in_a = j < tiles_a;
-      const int kb = (in_a ? j : j - tiles_a) * kKeys;
-      const int seg_len = in_a ? len_a : len_b;
-      if (seg_len - kb >= kKeys) return 0;
+      const int sg = seg_of(j);
+      const int kb = (j - seg_t0(sg)) * kKeys;
+      const int seg_len_j = seg_len(sg);
+      if (seg_len_j - kb >= kKeys) return 0;
       if (!__all_sync(0xffffffffu,
                       ptx::mbar_wait(&kv_full[b % kStages], (b / kStages) & 1, kWaitLimit)))
         return -1;
       uint8_t *vtile =
           kv + (b % kStages) * Cfg::kStageBytes + Cfg::kKVBlock + h * Cfg::kHalfBytes;
-      const int first = seg_len - kb > 0 ? seg_len - kb : 0;
+      const int first = seg_len_j - kb > 0 ? seg_len_j - kb : 0;
       for (int u = r; u < (kKeys - first) * (D / 8); u += kRows) {
         const int vr = first + u / (D / 8), ch = u % (D / 8);
         *reinterpret_cast<uint4 *>(vtile + (ch / 8) * Cfg::kPanelBytes + ptx::swz128(vr, ch % 8)) =

@@ -17,7 +17,8 @@ the same generator written in CUDA).  Both implement one definition:
   support +-6, computed with integer arithmetic only so that the CPU and
   the GPU produce identical bits.
 
-``tensor`` ids: 0 = q, 1 = k, 2 = v (any other small integer is allowed).
+``tensor`` ids: 0 = q, 1 = k, 2 = v, 3 = a layer group's global k, 4 = its global v (any
+other small integer is allowed).
 ``seq`` counts the sequences a row has held (it changes after a reset).
 """
 from __future__ import annotations
@@ -34,7 +35,7 @@ _M1 = np.uint64(0xBF58476D1CE4E5B9)
 _M2 = np.uint64(0x94D049BB133111EB)
 _MEAN12 = 393210  # 12 * 32767.5
 
-Q, K, V = 0, 1, 2
+Q, K, V, KG, VG = 0, 1, 2, 3, 4
 
 
 def _mix(z: np.ndarray) -> np.ndarray:

@@ -4,6 +4,10 @@ Inputs come from the counter-based generator (synth): the value of q/k/v at
 (layer, row, seq, position, head, d) is fixed by the seed, so the oracle can
 regenerate any row's whole history when it checks an output.  `seq` counts the
 sequences a row has held (it advances on every reset).
+
+Hybrid layers (kinds 2 = group's full layer, 3 = a local layer of the group): a layer's
+own q/k/v streams feed its query and ring; the group's global keys and values are the
+streams KG/VG of the group's full layer.
 """
 from __future__ import annotations
 
@@ -57,6 +61,10 @@ class Scenario:
         self.seq = [0] * B
         self.pad_value = pad_value  # None: generator values at pad positions; else a constant
         self.max_ratio = 0.0
+        self.group, f = [], -1      # full layer of each hybrid layer's group, else -1
+        for kind in self.kinds:
+            f = len(self.group) if kind == 2 else f
+            self.group.append(f if kind in (2, 3) else -1)
 
     # ------------------------------------------------------------------ inputs
     def gen(self, tensor, layer, row, positions, H):
@@ -78,6 +86,39 @@ class Scenario:
                 q[i, n:], k[i, n:], v[i, n:] = pad, pad, pad
         return q, k, v
 
+    def global_inputs(self, layer, rows, n_new, C):
+        """The group's global k, v of a hybrid layer's chunk (streams KG/VG of its full layer)."""
+        f = self.group[layer]
+        Bs = len(rows)
+        kg = np.zeros((Bs, C, self.Hk, self.D), np.uint16)
+        vg = np.zeros((Bs, C, self.Hk, self.D), np.uint16)
+        for i, (b, n) in enumerate(zip(rows, n_new)):
+            pos = np.arange(self.lens[b], self.lens[b] + C)
+            kg[i] = self.gen(synth.KG, f, b, pos, self.Hk)
+            vg[i] = self.gen(synth.VG, f, b, pos, self.Hk)
+            if self.pad_value is not None and n < C:
+                kg[i, n:] = vg[i, n:] = np.uint16(self.pad_value)
+        return kg, vg
+
+    def append_layer(self, layer, rows, rows_arg, n_new, C):
+        """One layer's append through the binding; returns (q bits, out tensor)."""
+        import torch
+        q, k, v = self.chunk_inputs(layer, rows, n_new, C)
+        qt, kt, vt = (bf16_bits_to_torch(x, self.dev) for x in (q, k, v))
+        sentinel = torch.full_like(qt, 12345.0)
+        kind = self.kinds[layer]
+        if kind in (2, 3):
+            kg = vg = None
+            if kind == 2:
+                kg, vg = (bf16_bits_to_torch(x, self.dev)
+                          for x in self.global_inputs(layer, rows, n_new, C))
+            out = self.cache.append_hybrid(layer, qt, kt, vt, list(n_new), k_global=kg,
+                                           v_global=vg, rows=rows_arg, out=sentinel.clone())
+        else:
+            out = self.cache.append(layer, qt, kt, vt, list(n_new), rows_arg,
+                                    out=sentinel.clone())
+        return q, out
+
     # ------------------------------------------------------------------ one step
     def step(self, n_new, rows=None, C=None, resets=(), check=True, check_state=False):
         import torch
@@ -90,11 +131,7 @@ class Scenario:
         C = C or max(1, max(n_new))
         outs = []
         for layer in range(len(self.kinds)):
-            q, k, v = self.chunk_inputs(layer, rows_eff, n_new, C)
-            qt, kt, vt = (bf16_bits_to_torch(x, self.dev) for x in (q, k, v))
-            sentinel = torch.full_like(qt, 12345.0)
-            out = self.cache.append(layer, qt, kt, vt, list(n_new), rows, out=sentinel.clone())
-            outs.append((q, out))
+            outs.append(self.append_layer(layer, rows_eff, rows, n_new, C))
         torch.cuda.synchronize()
         if check:
             for layer, (q, out) in enumerate(outs):
@@ -108,6 +145,8 @@ class Scenario:
 
     # ------------------------------------------------------------------ checks
     def check_outputs(self, layer, rows, n_new, q, out_bits):
+        if self.kinds[layer] in (2, 3):
+            return self.check_outputs_hybrid(layer, rows, n_new, q, out_bits)
         sliding = self.kinds[layer] == 1
         W = self.W if sliding else 0
         sentinel = np.uint16(0x4641)  # bf16(12345.0) rounds to 0x4641 (12352)
@@ -128,28 +167,55 @@ class Scenario:
             r = check_close(out_bits[i, :n], ref, f"layer {layer} row {b} lens {L} n {n}")
             self.max_ratio = max(self.max_ratio, r)
 
+    def check_outputs_hybrid(self, layer, rows, n_new, q, out_bits):
+        sentinel = np.uint16(0x4641)
+        f = self.group[layer]
+        for i, (b, n) in enumerate(zip(rows, n_new)):
+            assert np.all(out_bits[i, n:] == sentinel), f"layer {layer} row {b}: pad written"
+            if n == 0:
+                continue
+            L = self.lens[b]
+            hist = np.arange(L + n)
+            kg = self.gen(synth.KG, f, b, hist, self.Hk)
+            vg = self.gen(synth.VG, f, b, hist, self.Hk)
+            kl = self.gen(synth.K, layer, b, hist, self.Hk)
+            vl = self.gen(synth.V, layer, b, hist, self.Hk)
+            ref = oracle.attend_hybrid(q[i, :n], np.arange(L, L + n), kg, vg, kl, vl, self.Hq,
+                                       self.Hk, self.W, theta=self.theta)
+            r = check_close(out_bits[i, :n], ref, f"hybrid layer {layer} row {b} lens {L} n {n}")
+            self.max_ratio = max(self.max_ratio, r)
+
     def check_state(self):
         """Cache contents, ring slots, lpos and lens against the oracle, bit for bit."""
         import torch
         assert self.cache.lens == self.lens
         R = self.cache.R
+        # (storage, layer of the streams, k stream, v stream, ring?) of every layer; a
+        # hybrid layer has its group's cache and its own ring
+        views = []
         for layer, kind in enumerate(self.kinds):
-            K, V = self.cache.storage(layer)
+            if kind in (2, 3):
+                views.append((self.cache.storage(layer), self.group[layer], synth.KG, synth.VG,
+                              False))
+                views.append((self.cache.ring_storage(layer), layer, synth.K, synth.V, True))
+            else:
+                views.append((self.cache.storage(layer), layer, synth.K, synth.V, kind == 1))
+        for (K, V), layer, tk, tv, ringed in views:
             Kb, Vb = torch_to_bits(K), torch_to_bits(V)
             for b in range(self.B):
                 L = self.lens[b]
                 if L == 0:
                     continue
-                if kind == 0:
+                if not ringed:
                     pos = np.arange(L)
                     slots = pos
                 else:
                     ring = oracle.ring_positions(L, R)
                     slots = np.nonzero(ring >= 0)[0]
                     pos = ring[slots]
-                kr = oracle.rope_bf16(self.gen(synth.K, layer, b, pos, self.Hk), pos[:, None],
+                kr = oracle.rope_bf16(self.gen(tk, layer, b, pos, self.Hk), pos[:, None],
                                       self.theta)
-                vv = self.gen(synth.V, layer, b, pos, self.Hk)
+                vv = self.gen(tv, layer, b, pos, self.Hk)
                 got_k = Kb[b][:, slots].transpose(1, 0, 2)
                 got_v = Vb[b][:, slots].transpose(1, 0, 2)
                 assert np.array_equal(got_k, kr), f"layer {layer} row {b}: K differs"
