@@ -9,7 +9,7 @@ combine) plus kv_advance for all rows.  The K/V read per step (~1.2 GB) is far a
 the 129 MB L2, so no flush is needed between steps.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload decode_bw|long_ctx]
+                    [--workload decode_bw|long_ctx|hybrid]
 
 Under torchrun (N > 1) every rank runs an independent replica on its own GPU (the
 path has no exchange step); value = all ranks' units / max-over-ranks time.
@@ -42,7 +42,13 @@ WORKLOADS = {
     "long_ctx": dict(B=16, Hq=64, Hk=8, D=128, max_len=32768, W=512,
                      kinds=[1, 1, 1, 1, 1, 0, 1, 1, 1, 1, 1, 0], lo=16384, steps=200,
                      per_round=20),
+    # the long-context shapes as hybrid layers: 3 groups of 4 layers, each group sharing
+    # one global K/V (written by its first layer), every layer with its own W=512 ring
+    "hybrid": dict(B=16, Hq=64, Hk=8, D=128, max_len=32768, W=512,
+                   kinds=[2, 3, 3, 3] * 3, lo=16384, steps=100, per_round=20),
 }
+
+HYBRID = (2, 3)  # KV_HYBRID_FULL, KV_HYBRID_LOCAL
 
 
 def parse():
@@ -100,10 +106,22 @@ def kv_bytes_per_step(cfg, lens):
     B, Hq, Hk, D = cfg["B"], cfg["Hq"], cfg["Hk"], cfg["D"]
     total = 0.0
     for kind in cfg["kinds"]:
-        keys = np.minimum(lens + 1, cfg["W"]) if kind == 1 else lens + 1
+        local = np.minimum(lens + 1, cfg["W"])
+        keys = local if kind == 1 else lens + 1 + local if kind in HYBRID else lens + 1
         total += float(np.sum(2.0 * Hk * keys * D * 2))
-        total += B * (Hq + 2 * Hk) * D * 2 + 2 * B * Hk * D * 2 + B * Hq * D * 2
+        # new key/value streams: one (global or sliding), a hybrid full layer's two, a
+        # hybrid local layer's one (its ring's)
+        kv_new = 2 if kind == 2 else 1
+        total += B * (Hq + 2 * kv_new * Hk) * D * 2 + 2 * kv_new * B * Hk * D * 2 + B * Hq * D * 2
     return total
+
+
+def append_layer(cache, kind, layer, q, k, v, kg, vg, n, out, stream):
+    """One layer's append through the binding (hybrid layers with their global keys)."""
+    if kind in HYBRID:
+        return cache.append_hybrid(layer, q, k, v, n, k_global=kg if kind == 2 else None,
+                                   v_global=vg if kind == 2 else None, out=out, stream=stream)
+    return cache.append(layer, q, k, v, n, out=out, stream=stream)
 
 
 class ClockSampler:
@@ -269,11 +287,20 @@ def oracle_sample(cfg, lens, seed, budget_s=20.0, max_rows=None):
         kh = synth.normal_bf16(seed, synth.K, 0, b, 0, range(lo, p + 1), Hk, D)
         vh = synth.normal_bf16(seed, synth.V, 0, b, 0, range(lo, p + 1), Hk, D)
         q = synth.normal_bf16(seed, synth.Q, 0, b, 0, [p], Hq, D)
-        t0 = time.perf_counter()
-        oracle.attend(q, [p], kh, vh, lo, Hq, Hk, W=W if kind == 1 else 0)
-        spent += time.perf_counter() - t0
+        if kind in HYBRID:  # the group's global keys and the layer's local keys
+            kg = synth.normal_bf16(seed, synth.KG, 0, b, 0, range(p + 1), Hk, D)
+            vg = synth.normal_bf16(seed, synth.VG, 0, b, 0, range(p + 1), Hk, D)
+            t0 = time.perf_counter()
+            oracle.attend_hybrid(q, [p], kg, vg, kh, vh, Hq, Hk, W)
+            spent += time.perf_counter() - t0
+            keys = p + 1 + min(p + 1, W)
+        else:
+            t0 = time.perf_counter()
+            oracle.attend(q, [p], kh, vh, lo, Hq, Hk, W=W if kind == 1 else 0)
+            spent += time.perf_counter() - t0
+            keys = p + 1 - lo
         rows += 1
-        byts += 2.0 * Hk * (p + 1 - lo) * D * 2 + (Hq + 2 * Hk) * D * 2 + Hq * D * 2
+        byts += 2.0 * Hk * keys * D * 2 + (Hq + 2 * Hk) * D * 2 + Hq * D * 2
     return byts / spent / 1e9, rows / spent, rows, oracle.num_threads(), spent
 
 
@@ -320,7 +347,8 @@ def fill_cache(cache, cfg, lens_target, seed, stream):
 
 def make_inputs(cfg, lens, n_steps, seed, dev, stream):
     """Decode inputs of n_steps steps for every layer, generated on the device at positions
-    lens + s: tensors [n_steps, n_layers, B, 1, H, D]."""
+    lens + s: tensors [n_steps, n_layers, B, 1, H, D] (q, k, v, and the global k, v of a
+    hybrid full layer; those two are None without hybrid layers)."""
     import torch
     import synth
     B, Hq, Hk, D = cfg["B"], cfg["Hq"], cfg["Hk"], cfg["D"]
@@ -328,16 +356,27 @@ def make_inputs(cfg, lens, n_steps, seed, dev, stream):
     qs = torch.empty((n_steps, L, B, 1, Hq, D), dtype=torch.bfloat16, device=dev)
     ks = torch.empty((n_steps, L, B, 1, Hk, D), dtype=torch.bfloat16, device=dev)
     vs = torch.empty_like(ks)
+    hyb = any(k in HYBRID for k in cfg["kinds"])
+    kgs = torch.empty_like(ks) if hyb else None
+    vgs = torch.empty_like(ks) if hyb else None
     rows = torch.arange(B, dtype=torch.int32, device=dev)
     seqs = torch.zeros(B, dtype=torch.int32, device=dev)
     for s in range(n_steps):
         pos0 = torch.from_numpy((lens + s).astype(np.int32)).to(dev)
         for layer in range(L):
-            for t, x, H in ((synth.Q, qs, Hq), (synth.K, ks, Hk), (synth.V, vs, Hk)):
+            streams = [(synth.Q, qs, Hq), (synth.K, ks, Hk), (synth.V, vs, Hk)]
+            if cfg["kinds"][layer] == 2:
+                streams += [(synth.KG, kgs, Hk), (synth.VG, vgs, Hk)]
+            for t, x, H in streams:
                 synth.fill_device(x[s, layer].data_ptr(), seed, t, layer, rows.data_ptr(),
                                   seqs.data_ptr(), pos0.data_ptr(), B, 1, H, D,
                                   stream.cuda_stream)
-    return qs, ks, vs
+    return qs, ks, vs, kgs, vgs
+
+
+def step_inputs(inputs, s, layer):
+    """(q, k, v, kg, vg) of one step and layer from make_inputs' tensors."""
+    return tuple(None if x is None else x[s, layer] for x in inputs)
 
 
 def run_fill_only(args):
@@ -389,7 +428,7 @@ def fill_cache_from(cache, cfg, lens_from, lens_target, seed, stream):
     dev = torch.device("cuda", torch.cuda.current_device())
     q = torch.empty((B, C, Hq, D), dtype=torch.bfloat16, device=dev)
     k = torch.empty((B, C, Hk, D), dtype=torch.bfloat16, device=dev)
-    v = torch.empty_like(k)
+    v, kg, vg = torch.empty_like(k), torch.empty_like(k), torch.empty_like(k)
     out = torch.empty_like(q)
     rows = torch.arange(B, dtype=torch.int32, device=dev)
     seqs = torch.zeros(B, dtype=torch.int32, device=dev)
@@ -397,11 +436,14 @@ def fill_cache_from(cache, cfg, lens_from, lens_target, seed, stream):
     while (lens < lens_target).any():
         n = np.minimum(C, lens_target - lens).astype(np.int32)
         pos0 = torch.from_numpy(lens.astype(np.int32)).to(dev)
-        for layer in range(len(cfg["kinds"])):
-            for t, (x, H) in zip((synth.Q, synth.K, synth.V), ((q, Hq), (k, Hk), (v, Hk))):
+        for layer, kind in enumerate(cfg["kinds"]):
+            streams = [(synth.Q, q, Hq), (synth.K, k, Hk), (synth.V, v, Hk)]
+            if kind == 2:
+                streams += [(synth.KG, kg, Hk), (synth.VG, vg, Hk)]
+            for t, x, H in streams:
                 synth.fill_device(x.data_ptr(), seed, t, layer, rows.data_ptr(), seqs.data_ptr(),
                                   pos0.data_ptr(), B, C, H, D, stream.cuda_stream)
-            cache.append(layer, q, k, v, n.tolist(), out=out, stream=stream)
+            append_layer(cache, kind, layer, q, k, v, kg, vg, n.tolist(), out, stream)
         cache.advance(n.tolist(), stream=stream)
         lens += n
 
@@ -466,10 +508,12 @@ def run_ours(args):
         n = steps_in_round[r] + start
         inputs.append(make_inputs(cfg, lens0[r], n, caches[r][1], dev, stream))
     torch.cuda.synchronize()
+    kinds = cfg["kinds"]
+    hybrid = any(k in HYBRID for k in kinds)
     for s in range(Wm):
         for layer in range(n_layers):
-            caches[0][0].append(layer, inputs[0][0][s, layer], inputs[0][1][s, layer],
-                                inputs[0][2][s, layer], ones, out=out, stream=stream)
+            append_layer(caches[0][0], kinds[layer], layer, *step_inputs(inputs[0], s, layer),
+                         ones, out, stream)
         caches[0][0].advance(ones, stream=stream)
     torch.cuda.synchronize()
     alg_bytes = 0.0
@@ -480,12 +524,11 @@ def run_ours(args):
     def run_rounds(first_of):
         for r in range(rounds):
             c = caches[r][0]
-            qs, ks, vs = inputs[r]
             first = first_of(r)
             for s in range(first, first + steps_in_round[r]):
                 for layer in range(n_layers):
-                    c.append(layer, qs[s, layer], ks[s, layer], vs[s, layer], ones, out=out,
-                             stream=stream)
+                    append_layer(c, kinds[layer], layer, *step_inputs(inputs[r], s, layer),
+                                 ones, out, stream)
                 c.advance(ones, stream=stream)
 
     # Timed region: the workload alone.  The library's per-launch events (kernel
@@ -519,10 +562,10 @@ def run_ours(args):
         c.profile(True)
     run_rounds(lambda r: 0)
     torch.cuda.synchronize()
-    kinds = ("append", "decode", "combine", "state")
-    prof = {k: {"launches": 0, "ms": 0.0, "bytes": 0.0, "flops": 0.0} for k in kinds}
+    kkinds = ("append", "decode", "combine", "state")
+    prof = {k: {"launches": 0, "ms": 0.0, "bytes": 0.0, "flops": 0.0} for k in kkinds}
     for c, _ in caches:
-        for k in kinds:
+        for k in kkinds:
             rec = c.profile_read(k, reset=True)
             for f in rec:
                 prof[k][f] += rec[f]
@@ -535,9 +578,10 @@ def run_ours(args):
     graph_bytes, inputs, graphs = 0.0, [], []
     outs_l = [torch.empty((B, 1, Hq, D), dtype=torch.bfloat16, device=dev)
               for _ in range(n_layers)]
-    for r in range(rounds):
+    for r in range(rounds if not hybrid else 0):  # the step graph covers global/sliding layers
         lens_g = lens0[r] + (Wm if r == 0 else 0) + 2 * steps_in_round[r]
-        qs, ks, vs = make_inputs(cfg, lens_g, steps_in_round[r], caches[r][1] + 2, dev, stream)
+        qs, ks, vs, _, _ = make_inputs(cfg, lens_g, steps_in_round[r], caches[r][1] + 2, dev,
+                                       stream)
         inputs.append((qs, ks, vs))
         g = caches[r][0].step_graph([qs[0, l] for l in range(n_layers)],
                                     [ks[0, l] for l in range(n_layers)],
@@ -556,7 +600,7 @@ def run_ours(args):
     e1.record(stream)
     torch.cuda.synchronize()
     barrier()
-    ms_graph = e0.elapsed_time(e1)
+    ms_graph = e0.elapsed_time(e1) if graphs else None
     for g, _ in graphs:
         g.close()
     del inputs, graphs
@@ -570,16 +614,30 @@ def run_ours(args):
         lens_e = lens0[r] + first + 3 * steps_in_round[r]  # after the timed, event, graph passes
         n = steps_in_round[r] + (Wm if r == 0 else 0)
         g = make_inputs(cfg, lens_e, n, caches[r][1], dev, stream)
-        host_inputs.append(tuple(x.cpu().pin_memory() for x in g))
+        host_inputs.append(tuple(None if x is None else x.cpu().pin_memory() for x in g))
         del g
         e_bytes += sum(kv_bytes_per_step(cfg, lens_e + (Wm if r == 0 else 0) + s)
                        for s in range(steps_in_round[r]))
     torch.cuda.synchronize()
 
+    # hybrid layers: the step's inputs copied from pinned host memory on the stream, the
+    # device call, the output copied back (kv_append_host covers global/sliding layers)
+    dq = torch.empty((B, 1, Hq, D), dtype=torch.bfloat16, device=dev)
+    dkv = [torch.empty((B, 1, Hk, D), dtype=torch.bfloat16, device=dev) for _ in range(4)]
+
     def step_host(c, hin, s):
         for layer in range(n_layers):
-            c.append_host(layer, hin[0][s, layer], hin[1][s, layer], hin[2][s, layer], ones,
-                          out=hout, stream=stream)
+            if kinds[layer] in HYBRID:
+                dq.copy_(hin[0][s, layer], non_blocking=True)
+                xs = [None, None, None, None]
+                for i in range(4 if kinds[layer] == 2 else 2):
+                    dkv[i].copy_(hin[1 + i][s, layer], non_blocking=True)
+                    xs[i] = dkv[i]
+                append_layer(c, kinds[layer], layer, dq, *xs, ones, out, stream)
+                hout.copy_(out, non_blocking=True)
+            else:
+                c.append_host(layer, hin[0][s, layer], hin[1][s, layer], hin[2][s, layer], ones,
+                              out=hout, stream=stream)
         c.advance(ones, stream=stream)
 
     for s in range(Wm):
@@ -599,7 +657,7 @@ def run_ours(args):
     # ---- max over ranks
     if world > 1:
         (ms, ms_e2e, ms_graph), (alg_bytes, e_bytes, graph_bytes) = reduce_over_ranks(
-            [ms, ms_e2e, ms_graph], [alg_bytes, e_bytes, graph_bytes], dev)
+            [ms, ms_e2e, ms_graph or 0.0], [alg_bytes, e_bytes, graph_bytes], dev)
     if rank != 0:
         return
     value = alg_bytes / (ms / 1e3) / 1e9
@@ -638,12 +696,13 @@ def run_ours(args):
         "roofline": roofline,
         "e2e": {"value": e_bytes / (ms_e2e / 1e3) / 1e9, "unit": "GB/s",
                 "tokens_per_s": world * B * K / (ms_e2e / 1e3),
-                "h2d_bytes_per_step": n_layers * B * (Hq + 2 * Hk) * D * 2,
+                "h2d_bytes_per_step": sum(B * (Hq + (4 if k == 2 else 2) * Hk) * D * 2
+                                          for k in kinds),
                 "d2h_bytes_per_step": n_layers * B * Hq * D * 2},
         "graph": {"value": graph_bytes / (ms_graph / 1e3) / 1e9, "unit": "GB/s",
                   "ms_per_step": ms_graph / K,
                   "api": "kv_step_graph_launch: one CUDA-graph replay per step (all layers "
-                         "and the advance), inputs already on the device"},
+                         "and the advance), inputs already on the device"} if ms_graph else None,
         "gpu_launches": launches,
         "kernels": {k: {"launches": p["launches"], "ms": p["ms"]} for k, p in prof.items()},
         "clocks": clk,

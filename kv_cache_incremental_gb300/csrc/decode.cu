@@ -216,14 +216,12 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
   const bool seg1 = split >= row.n_splits;
   const int n_total = row.n_splits + row.n_splits2;
   const int ssplit = seg1 ? split - row.n_splits : split;
-  const int split_len = seg1 ? row.split_len2 : row.split_len;
+  const int split_len = (seg1 ? row.split_tiles2 : row.split_tiles) * kTileKeys;
   const int k0 = ssplit * split_len;
-  const int k1 = min(seg1 ? row.nk2 : row.nk, k0 + split_len);
+  const int k1 = min(seg1 ? min(row.pos + 1, p.ring_R) : row.nk, k0 + split_len);
   const int n_tiles = (k1 - k0 + kTileKeys - 1) / kTileKeys;
-  const int new_slot = seg1 ? row.slot2 : row.slot;
+  const int new_slot = seg1 || p.seg0_ring ? row.pos % p.ring_R : row.pos;
   const bool owner = (seg1 ? p.fuse_append2 : p.fuse_append) && new_slot >= k0 && new_slot < k1;
-  const CUtensorMap *map_k = seg1 ? &p.tmap_k2 : &p.tmap_k;
-  const CUtensorMap *map_v = seg1 ? &p.tmap_v2 : &p.tmap_v;
   const int seg_rows = seg1 ? p.seg_rows2 : p.seg_rows;
   PageTable pt = p.pt;
   if (seg1) pt.max_blocks = 0;                 // rings are dense
@@ -244,7 +242,9 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    // One copy of the loop per segment, so that each names its tensor maps by their
+    // fixed parameter addresses.
+    auto produce = [&](const CUtensorMap *map_k, const CUtensorMap *map_v) {
       ptx::prefetch_tmap(map_k);
       ptx::prefetch_tmap(map_v);
       for (int it = 0; it < n_tiles; ++it) {
@@ -288,6 +288,12 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
         }
         *issued = it + 1;
       }
+    };
+    if (lane == 0) {
+      if (seg1)
+        produce(&p.tmap_k2, &p.tmap_v2);
+      else
+        produce(&p.tmap_k, &p.tmap_v);
     }
     return;
   }

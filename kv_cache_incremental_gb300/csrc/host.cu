@@ -281,20 +281,17 @@ void plan_decode(const kv_cache *c, int layer, const std::vector<DecodeIn> &in,
     const int ns = splits(nk[i], kMaxSplits - ns2, st);
     DecodeRow &r = p.rows[i];
     r.cache_row = in[i].cache_row;
-    r.call_row = in[i].call_row;
+    r.call_row = (uint16_t)in[i].call_row;
     r.pos = in[i].pos;
     r.nk = nk[i];
-    r.item0 = item;
-    r.split_len = st * kTileKeys;
-    r.n_splits = ns;
-    r.slot = sliding ? in[i].pos % c->R : in[i].pos;
-    r.nk2 = nk2[i];
-    r.split_len2 = st2 * kTileKeys;
-    r.n_splits2 = ns2;
-    r.slot2 = hybrid ? in[i].pos % c->R : -1;
+    r.item0 = (uint16_t)item;
+    r.split_tiles = st;
+    r.n_splits = (uint8_t)ns;
+    r.split_tiles2 = st2;
+    r.n_splits2 = (uint8_t)ns2;
     r.ctr = in[i].cache_row;
     const int total = ns + ns2;
-    r.part0 = total > 1 ? part : 0;
+    r.part0 = (uint16_t)(total > 1 ? part : 0);
     if (total > 1) part += total;
     item += total;
     kv_bytes += 2.0 * (nk[i] + nk2[i]) * c->Hk * c->D * 2.0;
@@ -302,6 +299,8 @@ void plan_decode(const kv_cache *c, int layer, const std::vector<DecodeIn> &in,
   }
   p.n_rows = (int)in.size();
   p.n_items = item;
+  p.seg0_ring = sliding ? 1 : 0;
+  p.ring_R = c->R > 0 ? c->R : 1;
 }
 
 // Parameters of one decode launch (fused RoPE + append + split-K attention + merge) for a

@@ -103,19 +103,24 @@ struct AppendParams {
 // Keys of a decode row: segment 0 (storage slots [0, nk) of the layer storage) and, for a
 // hybrid layer, segment 1 (its ring, slots [0, nk2)); each segment has its own splits, and
 // the items of segment 1 follow those of segment 0.  All splits merge into one output.
+// One decode row, 32 bytes: the parameter block (all rows of a launch) is fetched on every
+// launch, so the fields that follow from others (the new key's slots, a ring's length) are
+// derived in the kernel and the small ones are 16 or 8 bits wide.
 struct DecodeRow {
   int32_t cache_row;
-  int32_t call_row;
-  int32_t pos;        // absolute position of the new token
-  int32_t nk;         // segment 0: storage slots [0, nk)
-  int32_t item0;      // first work item of this row
-  int32_t split_len;  // segment 0 keys per split (multiple of kTileKeys)
-  int32_t n_splits;   // segment 0 splits
-  int32_t part0;      // first partial slot of this row (items of multi-split rows)
-  int32_t slot;       // segment 0 storage slot of the new token's key (fused append)
-  int32_t ctr;        // row index of this row's merge tickets
-  int32_t nk2, split_len2, n_splits2, slot2;  // segment 1 (hybrid ring); n_splits2 = 0 else
+  int32_t pos;          // absolute position of the new token
+  int32_t nk;           // segment 0: storage slots [0, nk)
+  int32_t ctr;          // row index of this row's merge tickets
+  int32_t split_tiles;  // segment 0 tiles (kTileKeys keys) per split
+  int32_t split_tiles2; // segment 1 (hybrid ring; keys min(pos + 1, ring_R)) tiles per split
+  uint16_t call_row;    // < kMaxRowsPerLaunch
+  uint16_t item0;       // first work item of this row (< kMaxRowsPerLaunch * kMaxSplits)
+  uint16_t part0;       // first partial slot of this row (items of multi-split rows)
+  uint8_t n_splits;     // segment 0 splits
+  uint8_t n_splits2;    // segment 1 splits; 0 unless the layer is hybrid
 };
+static_assert(sizeof(DecodeRow) == 32, "decode row layout");
+static_assert(kMaxRowsPerLaunch * kMaxSplits <= 65535, "item and partial indices in 16 bits");
 
 struct DecodeParams {  // 64-byte aligned through its CUtensorMap members
   CUtensorMap tmap_k;       // layer K storage as 2-D [rows][D], box 64 x kTileKeys
@@ -137,7 +142,9 @@ struct DecodeParams {  // 64-byte aligned through its CUtensorMap members
   int64_t kv_row_stride;
   __nv_bfloat16 *cache_k;      // layer storage [B][Hk][seg_rows][D]
   __nv_bfloat16 *cache_v;
-  int fuse_append;
+  int fuse_append;          // the new key goes to segment 0 at slot pos (global) or
+  int seg0_ring;            // pos % ring_R (seg0_ring = 1: a sliding layer's ring)
+  int ring_R;
   int Hq, Hk, rep, seg_rows;
   int n_rows, n_items;
   float scale_log2;         // log2(e) / sqrt(D)

@@ -139,14 +139,15 @@ extern "C" int kv_decode_noalloc(const void *K, const void *V, int n_cache_rows,
     ns = (tiles + st - 1) / st;
     DecodeRow &r = dp.rows[i];
     r.cache_row = cache_rows[i];
-    r.call_row = i;
+    r.call_row = (uint16_t)i;
     r.pos = pos[i];
     r.nk = n_keys[i];
-    r.item0 = item;
-    r.split_len = st * kTileKeys;
-    r.n_splits = ns;
-    r.part0 = ns > 1 ? part : 0;
-    r.slot = -1;  // the caller has stored the new key already
+    r.item0 = (uint16_t)item;
+    r.split_tiles = st;
+    r.n_splits = (uint8_t)ns;
+    r.split_tiles2 = 0;
+    r.n_splits2 = 0;  // one key segment
+    r.part0 = (uint16_t)(ns > 1 ? part : 0);
     r.ctr = i;
     if (ns > 1) part += ns;
     item += ns;
@@ -177,7 +178,10 @@ extern "C" int kv_decode_noalloc(const void *K, const void *V, int n_cache_rows,
   dp.kv_row_stride = 0;
   dp.cache_k = nullptr;
   dp.cache_v = nullptr;
-  dp.fuse_append = 0;
+  dp.fuse_append = 0;  // the caller has stored the new key already
+  dp.fuse_append2 = 0;
+  dp.seg0_ring = 0;
+  dp.ring_R = 1;
   dp.pt = PageTable{nullptr, 0, 0};  // the caller's storage is dense
   dp.tmap_k16 = dp.tmap_k;
   dp.tmap_v16 = dp.tmap_v;
