@@ -68,7 +68,13 @@ def parse():
     ap.add_argument("--fill-to", type=int, default=0,
                     help="fill every row to this length instead of the workload's length "
                          "draw (small cases for profiling)")
-    return ap.parse_args()
+    ap.add_argument("--max-len", type=int, default=0,
+                    help="allocate the cache for this many positions instead of the "
+                         "workload's (small cases for profiling; with --fill-to)")
+    args = ap.parse_args()
+    if args.max_len:
+        WORKLOADS[args.workload] = dict(WORKLOADS[args.workload], max_len=args.max_len)
+    return args
 
 
 def dist_env():
@@ -480,9 +486,10 @@ def run_ours(args):
         pool = B * ((cfg["max_len"] + 15) // 16) if args.paged else None
         c = kvi.KVCache(B, cfg["max_len"], Hq, Hk, D, cfg["W"], cfg["kinds"], 1e4, local_rank,
                         paged_blocks=pool)
-        l0 = initial_lens(cfg, reserve, seed_r)
         if args.fill_to:  # small-case profiling: every row at the same, shorter length
             l0 = np.full(B, min(args.fill_to, cfg["max_len"] - reserve - 1), dtype=np.int64)
+        else:
+            l0 = initial_lens(cfg, reserve, seed_r)
         c.profile(r == 0)  # the chunked-prefill kernel, timed on the first fill
         fill_cache(c, cfg, l0, seed_r, stream)
         if r == 0:
@@ -611,7 +618,8 @@ def run_ours(args):
     host_inputs = []
     for r in range(rounds):
         first = Wm if r == 0 else 0
-        lens_e = lens0[r] + first + 3 * steps_in_round[r]  # after the timed, event, graph passes
+        # after the timed, event and (without hybrid layers) graph passes
+        lens_e = lens0[r] + first + (2 if hybrid else 3) * steps_in_round[r]
         n = steps_in_round[r] + (Wm if r == 0 else 0)
         g = make_inputs(cfg, lens_e, n, caches[r][1], dev, stream)
         host_inputs.append(tuple(None if x is None else x.cpu().pin_memory() for x in g))
