@@ -9,7 +9,7 @@ combine) plus kv_advance for all rows.  The K/V read per step (~1.2 GB) is far a
 the 129 MB L2, so no flush is needed between steps.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload decode_bw|long_ctx|hybrid]
+                    [--workload decode_bw|long_ctx|hybrid|cont_batch]
 
 Under torchrun (N > 1) every rank runs an independent replica on its own GPU (the
 path has no exchange step); value = all ranks' units / max-over-ranks time.
@@ -46,6 +46,11 @@ WORKLOADS = {
     # one global K/V (written by its first layer), every layer with its own W=512 ring
     "hybrid": dict(B=16, Hq=64, Hk=8, D=128, max_len=32768, W=512,
                    kinds=[2, 3, 3, 3] * 3, lo=16384, steps=100, per_round=20),
+    # continuous batching: 4 layers (1 and 3 global, 0 and 2 sliding W=1024), lens U[0, 12000];
+    # each step resets 5% of the rows, then appends a right-padded 64-token batch with n_new
+    # 1 (40%), 0 (30%) or U[2, 64] (30%)
+    "cont_batch": dict(B=128, Hq=16, Hk=4, D=64, max_len=16384, W=1024, kinds=[1, 0, 1, 0],
+                       lo=0, hi=12000, steps=50, per_round=50, mix=True),
 }
 
 HYBRID = (2, 3)  # KV_HYBRID_FULL, KV_HYBRID_LOCAL
@@ -733,12 +738,263 @@ def run_ours(args):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------- continuous batching
+
+def cont_plan(cfg, n_steps, seed):
+    """Initial lengths and n_steps steps of the continuous-batch mix: per step the rows
+    reset first (5% of B) and every row's n_new; lengths stay within max_len."""
+    rng = np.random.default_rng(seed)
+    B = cfg["B"]
+    lens0 = rng.integers(cfg["lo"], cfg["hi"] + 1, size=B).astype(np.int64)
+    lens, steps = lens0.copy(), []
+    for _ in range(n_steps):
+        resets = rng.choice(B, size=max(1, B // 20), replace=False)
+        lens[resets] = 0
+        u = rng.random(B)
+        n = np.where(u < 0.4, 1, np.where(u < 0.7, 0, rng.integers(2, 65, size=B)))
+        n = np.minimum(n, cfg["max_len"] - lens)
+        steps.append((resets.tolist(), n.astype(np.int64), lens.copy()))
+        lens += n
+    return lens0, steps
+
+
+def cont_inputs(cfg, steps, seed, dev, stream):
+    """q, k, v of every step and layer, [n_steps, n_layers, B, 64, H, D], generated on the
+    device at each row's positions."""
+    import torch
+    import synth
+    B, Hq, Hk, D, C = cfg["B"], cfg["Hq"], cfg["Hk"], cfg["D"], 64
+    L = len(cfg["kinds"])
+    qs = torch.empty((len(steps), L, B, C, Hq, D), dtype=torch.bfloat16, device=dev)
+    ks = torch.empty((len(steps), L, B, C, Hk, D), dtype=torch.bfloat16, device=dev)
+    vs = torch.empty_like(ks)
+    rows = torch.arange(B, dtype=torch.int32, device=dev)
+    seqs = torch.zeros(B, dtype=torch.int32, device=dev)
+    for i, (_, _, lens) in enumerate(steps):
+        pos0 = torch.from_numpy(lens.astype(np.int32)).to(dev)
+        for layer in range(L):
+            for t, x, H in ((synth.Q, qs, Hq), (synth.K, ks, Hk), (synth.V, vs, Hk)):
+                synth.fill_device(x[i, layer].data_ptr(), seed, t, layer, rows.data_ptr(),
+                                  seqs.data_ptr(), pos0.data_ptr(), B, C, H, D,
+                                  stream.cuda_stream)
+    return qs, ks, vs
+
+
+def cont_oracle_sample(cfg, steps, seed, budget_s):
+    """The oracle on whole rows (all layers, all of a row's new tokens) of the mix's first
+    steps until about budget_s of oracle time; returns (tokens/s, tokens, threads, seconds)."""
+    import oracle
+    import synth
+    Hq, Hk, D, W = cfg["Hq"], cfg["Hk"], cfg["D"], cfg["W"]
+    spent, tokens = 0.0, 0
+    for _, n, lens in steps:
+        for b in (int(x) for x in np.nonzero(n > 0)[0]):
+            if spent >= budget_s:
+                break
+            L, m = int(lens[b]), int(n[b])
+            for layer, kind in enumerate(cfg["kinds"]):
+                lo = max(0, L - W + 1) if kind == 1 else 0
+                pos = range(lo, L + m)
+                kh = synth.normal_bf16(seed, synth.K, layer, b, 0, pos, Hk, D)
+                vh = synth.normal_bf16(seed, synth.V, layer, b, 0, pos, Hk, D)
+                q = synth.normal_bf16(seed, synth.Q, layer, b, 0, range(L, L + m), Hq, D)
+                t0 = time.perf_counter()
+                oracle.attend(q, range(L, L + m), kh, vh, lo, Hq, Hk, W=W if kind == 1 else 0)
+                spent += time.perf_counter() - t0
+            tokens += m
+        if spent >= budget_s:
+            break
+    return tokens / spent, tokens, oracle.num_threads(), spent
+
+
+def run_cont_batch(args):
+    """Config 5: tokens/s of the continuous-batch mix (decode rows, chunk rows, idle rows and
+    resets in every step).  Three passes run the same step plan, each on a freshly filled
+    cache: the timed region (no per-launch events), a pass with the library's per-launch
+    events (kernel split, GB/s and TFLOP/s), and end to end through the host-buffer entry
+    point."""
+    import torch
+    import kv_cache_incremental_gb300 as kvi
+    rank, local_rank, world = dist_env()
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    cfg = WORKLOADS[args.workload]
+    B, Hq, Hk, D, C = cfg["B"], cfg["Hq"], cfg["Hk"], cfg["D"], 64
+    kinds = cfg["kinds"]
+    K = args.steps if args.steps else cfg["steps"]
+    Wm = max(3, args.warmup)
+    seed = args.seed + 7919 * rank
+    stream = torch.cuda.current_stream()
+    dev = torch.device("cuda", local_rank)
+    lens0, steps = cont_plan(cfg, Wm + K, seed)
+    tokens = int(sum(int(n.sum()) for _, n, _ in steps[Wm:]))
+    qs, ks, vs = cont_inputs(cfg, steps, seed, dev, stream)
+    out = torch.empty((B, C, Hq, D), dtype=torch.bfloat16, device=dev)
+
+    def fresh():
+        c = kvi.KVCache(B, cfg["max_len"], Hq, Hk, D, cfg["W"], kinds, 1e4, local_rank)
+        fill_cache(c, cfg, lens0, seed, stream)
+        return c
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def run(c, i0, i1, host=None):
+        for i in range(i0, i1):
+            resets, n, _ = steps[i]
+            c.reset(resets, stream=stream)
+            nl = n.tolist()
+            for layer in range(len(kinds)):
+                if host is None:
+                    c.append(layer, qs[i, layer], ks[i, layer], vs[i, layer], nl, out=out,
+                             stream=stream)
+                else:
+                    c.append_host(layer, host[0][i, layer], host[1][i, layer], host[2][i, layer],
+                                  nl, out=host[3], stream=stream)
+            c.advance(nl, stream=stream)
+
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # ---- timed region
+    c = fresh()
+    run(c, 0, Wm)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    barrier()
+    torch.cuda.synchronize()
+    clocks.mark_start()
+    torch.cuda.profiler.start()
+    e0.record(stream)
+    run(c, Wm, Wm + K)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    torch.cuda.profiler.stop()
+    clocks.mark_stop()
+    barrier()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1)
+    c.close()
+    # ---- the same steps with per-launch events
+    c = fresh()
+    run(c, 0, Wm)
+    torch.cuda.synchronize()
+    c.profile(True)
+    run(c, Wm, Wm + K)
+    torch.cuda.synchronize()
+    prof = {k: c.profile_read(k, reset=True) for k in ("append", "decode", "prefill", "combine",
+                                                     "commit", "state")}
+    c.profile(False)
+    c.close()
+    # ---- end to end: host buffers (pinned), copies inside the timed region
+    host = tuple(x.cpu().pin_memory() for x in (qs, ks, vs))
+    host = host + (torch.empty((B, C, Hq, D), dtype=torch.bfloat16).pin_memory(),)
+    c = fresh()
+    run(c, 0, Wm, host)
+    torch.cuda.synchronize()
+    barrier()
+    e0.record(stream)
+    run(c, Wm, Wm + K, host)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    ms_e2e = e0.elapsed_time(e1)
+    c.close()
+    if world > 1:
+        (ms, ms_e2e), (tokens_all,) = reduce_over_ranks([ms, ms_e2e], [float(tokens)], dev)
+    else:
+        tokens_all = float(tokens)
+    if rank != 0:
+        return
+    tot_bytes = sum(p["bytes"] for p in prof.values())
+    tot_flops = sum(p["flops"] for p in prof.values())
+    dec, pre = prof["decode"], prof["prefill"]
+    if pre["ms"] >= dec["ms"]:
+        tf = pre["flops"] / (pre["ms"] / 1e3) / 1e12 if pre["ms"] else None
+        roofline = {"bound": "tensor", "achieved": tf, "peak": peak_tflops(), "unit": "TFLOP/s",
+                    "frac": tf / peak_tflops() if tf else None, "traffic": None,
+                    "kernel": "prefill (chunk rows: tcgen05 prefill_tc_kernel and mma.sync "
+                              "prefill_kernel)",
+                    "peak_source": "measured bf16_tflops_sustained (kernel inside a long step)"}
+    else:
+        peak, kind = measured_peaks()
+        gb = dec["bytes"] / (dec["ms"] / 1e3) / 1e9 if dec["ms"] else None
+        roofline = {"bound": "hbm", "achieved": gb, "peak": peak, "unit": "GB/s",
+                    "frac": gb / peak if gb else None, "traffic": None,
+                    "kernel": "decode_kernel (decode rows)",
+                    "peak_source": f"{kind} hbm_gbs (copy bandwidth, burst)"}
+    roofline["timing"] = ("CUDA events around every library launch on the launch stream, over a "
+                          "second pass of the same steps on a freshly filled cache")
+    h2d = len(kinds) * B * C * (Hq + 2 * Hk) * D * 2
+    line = {
+        "metric": "continuous-batch tokens/s (B=128, 4 layers, 64-token right-padded mix)",
+        "value": tokens_all / (ms / 1e3), "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": Wm, "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "B": B, "Hq": Hq, "Hk": Hk, "D": D,
+                   "max_len": cfg["max_len"], "layers": len(kinds), "window": cfg["W"],
+                   "lens": f"U[{cfg['lo']}, {cfg['hi']}] initial", "chunk": C,
+                   "mix": "n_new 1 (40%), 0 (30%), U[2,64] (30%); 5% of rows reset per step",
+                   "l2": "inputs larger than L2 (per step ~0.6 GB of K/V, 0.2 GB of inputs)",
+                   "parallelism": f"replicas x{world}"},
+        "gbs": tot_bytes / (ms / 1e3) / 1e9, "tflops": tot_flops / (ms / 1e3) / 1e12,
+        "roofline": roofline,
+        "e2e": {"value": tokens_all / (ms_e2e / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": len(kinds) * B * C * Hq * D * 2},
+        "gpu_launches": sum(p["launches"] for p in prof.values()),
+        "kernels": {k: {"launches": p["launches"], "ms": p["ms"]} for k, p in prof.items()},
+        "clocks": clk,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        tps, nt, thr, t = cont_oracle_sample(cfg, steps[Wm:], seed, budget_s=15.0)
+        line["cpu_baseline"] = {"value": tps, "unit": "tokens/s", "cores": thr, "kind": "oracle",
+                                "sample": f"{nt} tokens (whole rows of the first timed steps, "
+                                          f"all {len(kinds)} layers), {t:.1f} s of oracle time"}
+    print(json.dumps(line), flush=True)
+
+
+def run_reference_cont(args):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return
+    cfg = WORKLOADS[args.workload]
+    if not args.steps:
+        args.steps = 10
+    _, steps = cont_plan(cfg, max(3, args.warmup) + args.steps, args.seed)
+    cont_oracle_sample(cfg, steps[:1], args.seed, budget_s=0.5)
+    total_tok, total_t, thr = 0, 0.0, 1
+    for i in range(args.steps):
+        _, tok, thr, t = cont_oracle_sample(cfg, steps[i:i + 1], args.seed, budget_s=1.0)
+        total_tok += tok
+        total_t += t
+    value = total_tok / total_t
+    print(json.dumps({
+        "impl": "reference", "metric": "continuous-batch tokens/s (B=128, 4 layers, 64-token "
+                                       "right-padded mix)", "value": value, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total_t / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, **{k: cfg[k] for k in ("B", "Hq", "Hk", "D",
+                                                                    "max_len")}},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": thr, "kind": "oracle",
+                         "sample": f"{total_tok} tokens (whole rows, all layers) over "
+                                   f"{args.steps} steps, about 1 s of oracle time each"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0}}), flush=True)
+
+
 def main():
     args = parse()
+    mix = WORKLOADS[args.workload].get("mix", False)
     if args.impl == "reference":
-        run_reference(args)
+        run_reference_cont(args) if mix else run_reference(args)
     elif args.fill_only:
         run_fill_only(args)
+    elif mix:
+        run_cont_batch(args)
     else:
         run_ours(args)
 

@@ -82,6 +82,10 @@ constexpr size_t kMaxProfRecs = 1 << 16;
 // Chunk rows with at least this many query rows (tokens x GQA group) use the tcgen05
 // prefill kernel.
 constexpr int kTcMinRows = 64;
+// Key splits of chunked prefill: at most this many per row, of at least this many
+// 128-key blocks each.
+constexpr int kMaxPrefillSplits = 16;
+constexpr int kMinSplitBlocks = 4;
 
 }  // namespace
 
@@ -106,6 +110,10 @@ struct kv_cache {
   int32_t *lpos = nullptr, *err = nullptr, *counters = nullptr;
   float *part_o = nullptr;
   float2 *part_ml = nullptr;
+  // prefill key-split partials ([vector][D] fp32 O, [vector] (m, l)), grown on demand
+  float *ppart_o = nullptr;
+  float2 *ppart_ml = nullptr;
+  int64_t ppart_cap = 0;  // vectors
   // host-buffer entry point staging
   void *stage = nullptr;
   size_t stage_bytes = 0;
@@ -353,6 +361,83 @@ void fill_decode(const kv_cache *c, int layer, const __nv_bfloat16 *q, const __n
   bytes = kvb + (double)batch.size() * (c->Hq + (hybrid ? 4 : 2) * c->Hk) * c->D * 2.0 * 2.0;
 }
 
+// Entries of one prefill launch kind for the rows `sel`, each with its key-tile range.
+// Without splitting every row is one entry over all its keys.  A launch whose longest CTA
+// (a row's whole key range) exceeds the average load per SM is rebalanced: rows longer
+// than `per` blocks (about two waves' worth of work per CTA) are cut into key splits,
+// each an entry that writes partials at part (vectors counted in *part_vecs), merged
+// afterwards by the rows appended to `merges`.
+std::vector<PrefillRow> split_prefill_rows(const kv_cache *c, int layer,
+                                           const std::vector<PrefillRow> &sel, int rows_per_cta,
+                                           int ctas_per_sm, std::vector<MergeRow> &merges,
+                                           int64_t *part_vecs) {
+  const bool sliding = c->kind[layer] == KV_SLIDING, hybrid = is_hybrid(c->kind[layer]);
+  const int rep = c->Hq / c->Hk;
+  const auto tiles = [](int keys) { return (keys + kTileKeys - 1) / kTileKeys; };
+  // the kernels' tile count for a row's last token (t_max = n - 1)
+  const auto blocks_of = [&](const PrefillRow &r) {
+    const int lr = std::min(r.lens, c->R);
+    const int t = sliding ? tiles(lr) + tiles(r.n)
+                          : hybrid ? tiles(r.lens + r.n) + tiles(lr) + tiles(r.n)
+                                   : tiles(r.lens + r.n);
+    return (t + 1) / 2;
+  };
+  int64_t work = 0;
+  int max_blocks = 0;
+  for (const PrefillRow &r : sel) {
+    const int q = (r.n * rep + rows_per_cta - 1) / rows_per_cta;
+    work += (int64_t)q * c->Hk * blocks_of(r);
+    max_blocks = std::max(max_blocks, blocks_of(r));
+  }
+  const int64_t cap = (int64_t)c->num_sms * ctas_per_sm;
+  const bool split = max_blocks > (work + cap - 1) / cap;
+  const int64_t per =
+      std::max<int64_t>(kMinSplitBlocks, (work + 2 * cap - 1) / (2 * cap));
+  std::vector<PrefillRow> out;
+  for (PrefillRow r : sel) {
+    const int blocks = blocks_of(r);
+    int ns = split ? (int)std::min<int64_t>(kMaxPrefillSplits, (blocks + per - 1) / per) : 1;
+    if (ns <= 1) {
+      r.tile0 = 0;
+      r.tile1 = INT32_MAX;
+      r.part = -1;
+      out.push_back(r);
+      continue;
+    }
+    const int bs = (blocks + ns - 1) / ns;
+    ns = (blocks + bs - 1) / bs;
+    const int n_rho = r.n * rep;
+    const int64_t base = *part_vecs;
+    *part_vecs += (int64_t)ns * c->Hk * n_rho;
+    for (int k = 0; k < ns; ++k) {
+      r.tile0 = 2 * bs * k;
+      r.tile1 = k == ns - 1 ? INT32_MAX : 2 * bs * (k + 1);
+      r.part = (int32_t)(base + (int64_t)k * c->Hk * n_rho);
+      out.push_back(r);
+    }
+    merges.push_back({r.call_row, n_rho, ns, (int32_t)base, 0});
+  }
+  return out;
+}
+
+// Room for n prefill partial vectors.  Growing waits for the work queued on s (the old
+// buffer may be in use).
+int ensure_prefill_parts(kv_cache *c, int64_t n, cudaStream_t s) {
+  if (n <= c->ppart_cap) return KV_OK;
+  if ((c->ppart_o || c->ppart_ml) && cudaStreamSynchronize(s) != cudaSuccess) return KV_ERR_CUDA;
+  cudaFree(c->ppart_o);
+  cudaFree(c->ppart_ml);
+  c->ppart_o = nullptr;
+  c->ppart_ml = nullptr;
+  c->ppart_cap = 0;
+  const int64_t cap = std::max<int64_t>(n, 1 << 16);
+  if (cudaMalloc((void **)&c->ppart_o, cap * c->D * sizeof(float)) != cudaSuccess ||
+      cudaMalloc((void **)&c->ppart_ml, cap * sizeof(float2)) != cudaSuccess)
+    return KV_ERR_OOM;
+  c->ppart_cap = cap;
+  return KV_OK;
+}
+
 // One layer's chunk for rows `cache_rows`.  k, v: the keys and values of the layer
 // storage (a hybrid layer: its group's global keys, nullptr on a local layer); kl, vl: a
 // hybrid layer's own local keys and values (its ring), else nullptr.
@@ -455,10 +540,23 @@ int append_device(kv_cache *c, int layer, const __nv_bfloat16 *q, const __nv_bfl
     // chunk gives at least 64 query rows go to the tcgen05 kernel (128-row tiles);
     // smaller ones to the mma.sync kernel (16-row warp tiles).  Hybrid layers (three key
     // segments) all go to the tcgen05 kernel.
+    std::vector<PrefillRow> ents[2];
+    std::vector<MergeRow> merges;
+    int64_t part_vecs = 0;
     for (int kind = 0; kind < 2; ++kind) {
       std::vector<PrefillRow> sel;
       for (const PrefillRow &r : prows)
         if ((hybrid || r.n * rep >= kTcMinRows) == (kind == 1)) sel.push_back(r);
+      // the tcgen05 kernel holds one CTA per SM, the mma.sync kernel two
+      ents[kind] = split_prefill_rows(c, layer, sel, kind == 1 ? prefill_tc_rows_per_cta() : 64,
+                                      kind == 1 ? 1 : 2, merges, &part_vecs);
+    }
+    if (part_vecs > 0) {
+      const int rc = ensure_prefill_parts(c, part_vecs, s);
+      if (rc != KV_OK) return rc;
+    }
+    for (int kind = 0; kind < 2; ++kind) {
+      const std::vector<PrefillRow> &sel = ents[kind];
       const int rows_per_cta = kind == 1 ? prefill_tc_rows_per_cta() : 64;
       for (size_t r0 = 0; r0 < sel.size(); r0 += kMaxRowsPerLaunch) {
         const size_t r1 = std::min(sel.size(), r0 + kMaxRowsPerLaunch);
@@ -487,6 +585,8 @@ int append_device(kv_cache *c, int layer, const __nv_bfloat16 *q, const __nv_bfl
         pp.tmap_k2 = hybrid ? c->tmRK[layer] : c->tmK[layer];
         pp.tmap_v2 = hybrid ? c->tmRV[layer] : c->tmV[layer];
         pp.seg_rows2 = c->R + 1;
+        pp.part_o = c->ppart_o;
+        pp.part_ml = c->ppart_ml;
         int cta = 0;
         double bytes = 0, fl = 0;
         for (size_t j = r0; j < r1; ++j) {
@@ -494,6 +594,7 @@ int append_device(kv_cache *c, int layer, const __nv_bfloat16 *q, const __nv_bfl
           r.cta0 = cta;
           cta += (r.n * rep + rows_per_cta - 1) / rows_per_cta;
           pp.rows[j - r0] = r;
+          if (r.tile0 != 0) continue;  // a row's work is counted with its first entry
           const int lkeys = std::min(r.lens, c->R) + r.n;
           const int keys = sliding ? lkeys : hybrid ? r.lens + r.n + lkeys : r.lens + r.n;
           bytes += 2.0 * keys * Hk * D * 2.0 + 2.0 * r.n * Hq * D * 2.0;
@@ -511,6 +612,32 @@ int append_device(kv_cache *c, int layer, const __nv_bfloat16 *q, const __nv_bfl
         });
         if (e != cudaSuccess) return KV_ERR_CUDA;
       }
+    }
+    // ---- merge of the key-split rows (log-sum-exp over their partials)
+    for (size_t r0 = 0; r0 < merges.size(); r0 += kMaxRowsPerLaunch) {
+      const size_t r1 = std::min(merges.size(), r0 + kMaxRowsPerLaunch);
+      static thread_local MergeParams mg;
+      mg.part_o = c->ppart_o;
+      mg.part_ml = c->ppart_ml;
+      mg.out = out + (int64_t)off * Hq * D;
+      mg.out_row_stride = q_row;
+      mg.Hq = Hq;
+      mg.Hk = Hk;
+      mg.rep = rep;
+      int vec = 0;
+      double mb = 0;
+      for (size_t j = r0; j < r1; ++j) {
+        MergeRow m = merges[j];
+        m.vec0 = vec;
+        vec += Hk * m.n_rho;
+        mg.rows[j - r0] = m;
+        mb += (double)Hk * m.n_rho * (m.n_splits * (D * 4.0 + 8.0) + D * 2.0);
+      }
+      mg.n_rows = (int)(r1 - r0);
+      mg.n_vec = vec;
+      cudaError_t e = timed(c, KV_KERNEL_COMBINE, mb, 0, s,
+                            [&] { return launch_prefill_merge(mg, D, s); });
+      if (e != cudaSuccess) return KV_ERR_CUDA;
     }
     if (ringed) {
       for (size_t r0 = 0; r0 < prows.size(); r0 += kMaxRowsPerLaunch) {
@@ -587,6 +714,8 @@ void free_all(kv_cache *c) {
   cudaFree(c->err);
   cudaFree(c->part_o);
   cudaFree(c->part_ml);
+  cudaFree(c->ppart_o);
+  cudaFree(c->ppart_ml);
   cudaFree(c->stage);
   cudaFree(c->table);
   for (auto &r : c->recs) {

@@ -160,12 +160,19 @@ struct DecodeParams {  // 64-byte aligned through its CUtensorMap members
 };
 
 // ---------------------------------------------------------------- prefill
+// One row of a prefill launch, or one key split of it: the CTAs of the entry read the
+// 64-key tiles [tile0, tile1) of the row's key space (tile0 even: 128-key blocks; tile1
+// beyond the last tile means "to the end").  part < 0: the entry covers all keys and
+// writes the output; else it writes unnormalised partials -- vector (kv head g, query row
+// rho) at part + g * n * rep + rho of PrefillParams::part_o / part_ml -- for the merge.
 struct PrefillRow {
   int32_t cache_row;
   int32_t call_row;
   int32_t lens;   // position of token 0 of the sub-chunk
   int32_t n;      // tokens of the sub-chunk
-  int32_t cta0;   // first CTA (query tile) of this row
+  int32_t cta0;   // first CTA (query tile) of this entry
+  int32_t tile0, tile1;
+  int32_t part;
 };
 
 struct PrefillParams {  // 64-byte aligned through its CUtensorMap members
@@ -193,7 +200,31 @@ struct PrefillParams {  // 64-byte aligned through its CUtensorMap members
   CUtensorMap tmap_k2;
   CUtensorMap tmap_v2;
   int seg_rows2;
+  // key splits: [vector][D] fp32 O (relative to m), [vector] (m in log2 units, l)
+  float *part_o;
+  float2 *part_ml;
   PrefillRow rows[kMaxRowsPerLaunch];
+};
+
+// Merge of a prefill row's key splits: out = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s
+// (M = max_s m_s) for every (kv head, query row) vector; split s of the row starts at
+// part + s * Hk * n_rho.
+struct MergeRow {
+  int32_t call_row;
+  int32_t n_rho;     // query rows per kv head (tokens x GQA group)
+  int32_t n_splits;
+  int32_t part;
+  int32_t vec0;      // first vector of this row in the launch
+};
+
+struct MergeParams {
+  const float *part_o;
+  const float2 *part_ml;
+  __nv_bfloat16 *out;       // offset to the sub-chunk
+  int64_t out_row_stride;
+  int Hq, Hk, rep;
+  int n_rows, n_vec;
+  MergeRow rows[kMaxRowsPerLaunch];
 };
 
 // ---------------------------------------------------------------- ring commit / state
@@ -259,6 +290,7 @@ cudaError_t decode_node(const DecodeParams *p, int D, int n_tiles_heads, void **
                         cudaKernelNodeParams *kp);
 cudaError_t state_node(const StateParams *p, void **args, cudaKernelNodeParams *kp);
 cudaError_t launch_prefill(const PrefillParams &p, int D, cudaStream_t s);
+cudaError_t launch_prefill_merge(const MergeParams &p, int D, cudaStream_t s);
 cudaError_t launch_commit(const CommitParams &p, cudaStream_t s);
 cudaError_t launch_state(const StateParams &p, cudaStream_t s);
 // Opt kernels into their dynamic shared memory sizes (once per process and device).
@@ -273,5 +305,6 @@ static_assert(sizeof(CommitParams) <= kMaxParamBytes, "commit parameters too lar
 static_assert(sizeof(CopyParams) <= kMaxParamBytes, "copy parameters too large");
 static_assert(sizeof(TableParams) <= kMaxParamBytes, "table parameters too large");
 static_assert(sizeof(StateParams) <= kMaxParamBytes, "state parameters too large");
+static_assert(sizeof(MergeParams) <= kMaxParamBytes, "merge parameters too large");
 
 }  // namespace kvinc

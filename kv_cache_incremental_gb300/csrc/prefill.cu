@@ -90,6 +90,9 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(const __grid_constant
   const int len_b = p.sliding ? t_max + 1 : 0;
   const int tiles_a = (len_a + kTileKeys - 1) / kTileKeys;
   const int n_tiles = tiles_a + (len_b + kTileKeys - 1) / kTileKeys;
+  // This entry's tiles [j_begin, j_end): a key split, or all of them.
+  const int j_begin = row.tile0, j_end = min(row.tile1, n_tiles);
+  const int n_local = max(0, j_end - j_begin);
   const int64_t base_a = ((int64_t)row.cache_row * p.Hk + g) * p.seg_rows;
   const int64_t base_b = ((int64_t)row.cache_row * p.Hk + g) * kChunk;
 
@@ -138,7 +141,7 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(const __grid_constant
     if (lane == 0) {
       ptx::prefetch_tmap(&p.tmap_k);
       ptx::prefetch_tmap(&p.tmap_v);
-      for (int it = 0; it < n_tiles; ++it) {
+      for (int it = 0; it < n_local; ++it) {
         const int s = it % kStages;
         if (it >= kStages &&
             !ptx::mbar_wait(&empty[s], ((it / kStages) - 1) & 1, kWaitLimit)) {
@@ -147,14 +150,15 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(const __grid_constant
         }
         uint8_t *kt = tiles + s * Cfg::kStageBytes;
         uint8_t *vt = kt + Cfg::kTileBytes;
-        const bool in_a = it < tiles_a;
+        const int jt = j_begin + it;  // tile of the row's key space
+        const bool in_a = jt < tiles_a;
         const CUtensorMap *mk = in_a ? &p.tmap_k : &p.tmap_sk;
         const CUtensorMap *mv = in_a ? &p.tmap_v : &p.tmap_sv;
-        const int y = static_cast<int>(in_a ? base_a + (int64_t)it * kTileKeys
-                                            : base_b + (int64_t)(it - tiles_a) * kTileKeys);
+        const int y = static_cast<int>(in_a ? base_a + (int64_t)jt * kTileKeys
+                                            : base_b + (int64_t)(jt - tiles_a) * kTileKeys);
         ptx::mbar_arrive_expect_tx(&full[s], Cfg::kStageBytes);
         int4 y4 = make_int4(y, y + kBlockTokens, y + 2 * kBlockTokens, y + 3 * kBlockTokens);
-        if (in_a && p.pt.max_blocks) y4 = kv_rows4(p.pt, row.cache_row, g, it * kTileKeys);
+        if (in_a && p.pt.max_blocks) y4 = kv_rows4(p.pt, row.cache_row, g, jt * kTileKeys);
         if (rows4_contiguous(y4)) {  // dense, or a paged tile of consecutive blocks
 #pragma unroll
           for (int pn = 0; pn < Cfg::kPanels; ++pn) {
@@ -206,7 +210,7 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(const __grid_constant
   for (int nd = 0; nd < D / 8; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
   float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
 
-  for (int it = 0; it < n_tiles; ++it) {
+  for (int it = 0; it < n_local; ++it) {
     const int s = it % kStages;
     // After a give-up the loop keeps running without waiting or computing, so that
     // every consumer warp passes the same named barriers in the same order.
@@ -217,8 +221,9 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(const __grid_constant
     }
     uint8_t *kt = tiles + s * Cfg::kStageBytes;
     uint8_t *vt = kt + Cfg::kTileBytes;
-    const bool in_a = it < tiles_a;
-    const int kb = (in_a ? it : it - tiles_a) * kTileKeys;  // first key index of the tile
+    const int jt = j_begin + it;
+    const bool in_a = jt < tiles_a;
+    const int kb = (in_a ? jt : jt - tiles_a) * kTileKeys;  // first key index of the tile
     const int seg_len = in_a ? len_a : len_b;
     const int n_valid = seg_len - kb;
 
@@ -349,6 +354,22 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(const __grid_constant
     l_run[rj] += __shfl_xor_sync(0xffffffffu, l_run[rj], 1);
     l_run[rj] += __shfl_xor_sync(0xffffffffu, l_run[rj], 2);
   }
+  if (row.part >= 0) {
+    // A key split: unnormalised O of the lane's dims, the row's maximum (log2 units), sum.
+#pragma unroll
+    for (int rj = 0; rj < 2; ++rj) {
+      const int rho = rho0 + 16 * warp + gq + 8 * rj;
+      if (rho >= n_rho) continue;
+      const int64_t vec = (int64_t)row.part + (int64_t)g * n_rho + rho;
+      float *po = p.part_o + vec * D;
+#pragma unroll
+      for (int nd = 0; nd < D / 8; ++nd)
+        *reinterpret_cast<float2 *>(po + 8 * nd + 2 * qq) =
+            make_float2(o[nd][2 * rj], o[nd][2 * rj + 1]);
+      if (qq == 0) p.part_ml[vec] = make_float2(m_run[rj], l_run[rj]);
+    }
+    return;
+  }
 #pragma unroll
   for (int rj = 0; rj < 2; ++rj) {
     const int rho = rho0 + 16 * warp + gq + 8 * rj;
@@ -365,6 +386,68 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(const __grid_constant
   }
 }
 
+__device__ __forceinline__ int find_merge_row(const MergeParams &p, int v) {
+  int lo = 0, hi = p.n_rows - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.rows[mid].vec0 <= v) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+constexpr int kMergeWarps = 8;
+
+// One warp per (row, kv head, query row) vector: the log-sum-exp merge of the row's key
+// splits (a split in which the query row sees no key has m = -inf and weighs nothing).
+template <int D>
+__global__ void __launch_bounds__(kMergeWarps * 32)
+    prefill_merge_kernel(const __grid_constant__ MergeParams p) {
+  constexpr int kPer = D / 32;  // dims per lane
+  const int v = blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (v >= p.n_vec) return;
+  const MergeRow &row = p.rows[find_merge_row(p, v)];
+  const int local = v - row.vec0;  // g * n_rho + rho
+  const int g = local / row.n_rho, rho = local % row.n_rho;
+  const int64_t stride = (int64_t)p.Hk * row.n_rho;
+  float m_max = -INFINITY;
+  for (int sp = 0; sp < row.n_splits; ++sp)
+    m_max = fmaxf(m_max, p.part_ml[row.part + sp * stride + local].x);
+  float acc[kPer] = {};
+  float l = 0.f;
+  for (int sp = 0; sp < row.n_splits; ++sp) {
+    const int64_t vec = row.part + sp * stride + local;
+    const float2 ml = p.part_ml[vec];
+    const float w = ml.x == -INFINITY ? 0.f : exp2f(ml.x - m_max);
+    l += w * ml.y;
+    const float *po = p.part_o + vec * D + kPer * lane;
+    if (kPer == 4) {
+      const float4 x = *reinterpret_cast<const float4 *>(po);
+      acc[0] += w * x.x;
+      acc[1] += w * x.y;
+      acc[2 % kPer] += w * x.z;
+      acc[3 % kPer] += w * x.w;
+    } else {
+      const float2 x = *reinterpret_cast<const float2 *>(po);
+      acc[0] += w * x.x;
+      acc[1] += w * x.y;
+    }
+  }
+  const float inv = l > 0.f ? 1.f / l : 0.f;
+  const int t = rho / p.rep, h = rho % p.rep;
+  __nv_bfloat16 *dst = p.out + (int64_t)row.call_row * p.out_row_stride +
+                       ((int64_t)t * p.Hq + g * p.rep + h) * D + kPer * lane;
+  if (kPer == 4) {
+    uint2 w;
+    w.x = ptx::pack_bf16(acc[0] * inv, acc[1] * inv);
+    w.y = ptx::pack_bf16(acc[2 % kPer] * inv, acc[3 % kPer] * inv);
+    *reinterpret_cast<uint2 *>(dst) = w;
+  } else {
+    *reinterpret_cast<uint32_t *>(dst) = ptx::pack_bf16(acc[0] * inv, acc[1] * inv);
+  }
+}
+
 template <int D>
 cudaError_t launch_prefill_t(const PrefillParams &p, cudaStream_t s) {
   prefill_kernel<D><<<dim3(p.n_ctas, p.Hk), kThreads, prefill_smem_bytes<D>(), s>>>(p);
@@ -378,6 +461,15 @@ cudaError_t launch_prefill(const PrefillParams &p, int D, cudaStream_t s) {
   if (D == 128) return launch_prefill_t<128>(p, s);
   if (D == 64) return launch_prefill_t<64>(p, s);
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_prefill_merge(const MergeParams &p, int D, cudaStream_t s) {
+  if (p.n_vec <= 0) return cudaSuccess;
+  const int blocks = (p.n_vec + kMergeWarps - 1) / kMergeWarps;
+  if (D == 128) prefill_merge_kernel<128><<<blocks, kMergeWarps * 32, 0, s>>>(p);
+  else if (D == 64) prefill_merge_kernel<64><<<blocks, kMergeWarps * 32, 0, s>>>(p);
+  else return cudaErrorInvalidValue;
+  return cudaGetLastError();
 }
 
 cudaError_t configure_prefill() {

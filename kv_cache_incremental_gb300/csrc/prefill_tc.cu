@@ -167,7 +167,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto seg_of = [&](int j) { return j < st1 ? 0 : j < st2 ? 1 : 2; };
   auto seg_len = [&](int sg) { return sg == 0 ? sl0 : sg == 1 ? sl1 : sl2; };
   auto seg_t0 = [&](int sg) { return sg == 0 ? 0 : sg == 1 ? st1 : st2; };
-  const int n_blocks = (n_tiles + 1) / 2;                      // 128-key blocks
+  // This entry's tiles [j_begin, j_end) (a key split, or all of them): blocks
+  // b_begin .. b_begin + n_blocks - 1 of 128 keys; loop indices below count from b_begin.
+  const int j_begin = row.tile0, j_end = min(row.tile1, n_tiles);
+  const int b_begin = j_begin / 2;
+  const int n_blocks = j_end > j_begin ? (j_end - j_begin + 1) / 2 : 0;
   const int64_t rh = (int64_t)row.cache_row * p.Hk + g;
   auto seg_base = [&](int sg) {
     return rh * (sg == 0 ? p.seg_rows : sg == 1 ? p.seg_rows2 : kChunk);
@@ -247,10 +251,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         uint8_t *kt = kv + s * Cfg::kStageBytes;
         uint8_t *vt = kt + Cfg::kKVBlock;
-        const int halves = min(2, n_tiles - 2 * it);  // a last block may hold one tile
+        const int halves = min(2, j_end - 2 * (b_begin + it));  // a last block may hold one tile
         ptx::mbar_arrive_expect_tx(&kv_full[s], halves * 2 * Cfg::kPanels * Cfg::kHalfBytes);
         for (int h = 0; h < halves; ++h) {
-          const int j = 2 * it + h;
+          const int j = 2 * (b_begin + it) + h;
           const int sg = seg_of(j);
           const CUtensorMap *mk = sg == 0 ? &p.tmap_k : sg == 1 ? &p.tmap_k2 : &p.tmap_sk;
           const CUtensorMap *mv = sg == 0 ? &p.tmap_v : sg == 1 ? &p.tmap_v2 : &p.tmap_sv;
@@ -313,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       // A tile of the block is partial when a segment ends inside it.
       auto partial = [&](int j) {
-        if (j >= n_tiles) return false;
+        if (j >= j_end) return false;
         const int sg = seg_of(j);
         const int next = sg == 0 ? st1 : sg == 1 ? st2 : n_tiles;
         return j == next - 1 && seg_len(sg) % kKeys != 0;
@@ -326,12 +330,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       // rows past the segment's end (v_ready, one barrier per stage: tile 0 cannot get
       // kStages blocks ahead of this PV, whose stage it would need, so it cannot lap it).
       auto issue_pv = [&](int b) -> bool {
-        if (qt == 1 && (partial(2 * b) || partial(2 * b + 1)) &&
+        const int jb = 2 * (b_begin + b);
+        if (qt == 1 && (partial(jb) || partial(jb + 1)) &&
             !ptx::mbar_wait(&v_ready[b % kStages], (b / kStages) & 1, kWaitLimit))
           return false;
         const uint32_t v_addr =
             ptx::smem_u32(kv + (b % kStages) * Cfg::kStageBytes + Cfg::kKVBlock);
-        const int halves = min(2, n_tiles - 2 * b);
+        const int halves = min(2, j_end - jb);
         for (int h = 0; h < halves; ++h) {
           if (!ptx::mbar_wait(&p_full[2 * qt + h], b & 1, kWaitLimit)) return false;
           tc::fence_after();
@@ -348,21 +353,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::commit(&kv_empty[b % kStages]);  // this tile's MMAs of the stage issued
         return true;
       };
-      bool ok = issue_qk(0);
-      for (int b = 0; ok && b < n_blocks; ++b) {
-        if (*fail) {
-          ok = false;
-          break;
+      if (n_blocks > 0) {  // (a key split past this CTA's last tile has no work)
+        bool ok = issue_qk(0);
+        for (int b = 0; ok && b < n_blocks; ++b) {
+          if (*fail) {
+            ok = false;
+            break;
+          }
+          ok = issue_pv(b) && (b + 1 >= n_blocks || issue_qk(b + 1));
         }
-        ok = issue_pv(b) && (b + 1 >= n_blocks || issue_qk(b + 1));
+        if (!ok) {
+          atomicExch(p.err, 1);
+          *fail = 1;
+        }
+        // Every MMA issued by either warp has completed before TMEM can be released.
+        tc::commit(drain);
+        ptx::mbar_wait(drain, 0, kWaitLimit);
       }
-      if (!ok) {
-        atomicExch(p.err, 1);
-        *fail = 1;
-      }
-      // Every MMA issued by either warp has completed before TMEM can be released.
-      tc::commit(drain);
-      ptx::mbar_wait(drain, 0, kWaitLimit);
     }
   } else if (qt_me < n_qt) {
     // ------------------------------------------------------------ softmax warps
@@ -490,7 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // its P, query tile 1's PV of the block for v_ready; the stage cannot be refilled
     // before both PVs are issued).  Returns -1 on a timeout, 1 if rows were zeroed.
     auto zero_v = [&](int b, int h) -> int {
-      const int j = 2 * b + h;
+      const int j = 2 * (b_begin + b) + h;
       const int sg = seg_of(j);
       const int kb = (j - seg_t0(sg)) * kKeys;
       const int seg_len_j = seg_len(sg);
@@ -523,9 +530,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc::fence_after();
-      const int j0 = 2 * b;
+      const int j0 = 2 * (b_begin + b);
       if (qt == 0) {
-        const int z0 = zero_v(b, 0), z1 = j0 + 1 < n_tiles ? zero_v(b, 1) : 0;
+        const int z0 = zero_v(b, 0), z1 = j0 + 1 < j_end ? zero_v(b, 1) : 0;
         if (z0 < 0 || z1 < 0) {
           ok = false;
           break;
@@ -544,7 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       store_p(0, sv);
       publish(0);
-      if (j0 + 1 < n_tiles) {
+      if (j0 + 1 < j_end) {
         // a new maximum in tile 1 rescales O after PV of tile 0 (already issued) is done
         if (!rescale_to(load_tile(j0 + 1, 1, sv),
                         [&] { return ptx::mbar_wait(&pv0_done[qt], b & 1, kWaitLimit); })) {
@@ -564,6 +571,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok) {
       atomicExch(p.err, 1);
       *fail = 1;
+    } else if (row.part >= 0 && (n_blocks == 0 || __all_sync(0xffffffffu, last_done))) {
+      // A key split: this row's unnormalised O, its maximum (log2 units) and sum.
+      if (n_blocks > 0) tc::fence_after();
+      const int64_t vec = (int64_t)row.part + (int64_t)g * n_rho + rho;
+      float4 *po = reinterpret_cast<float4 *>(p.part_o + vec * D);
+#pragma unroll
+      for (int c = 0; c < D / 16; ++c) {
+        float o16[16];
+        if (n_blocks > 0) {
+          tc::ld16(tO + 16 * c, o16);
+          tc::wait_ld();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) o16[i] = 0.f;
+        }
+        if (qvalid) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            po[4 * c + i] = make_float4(o16[4 * i], o16[4 * i + 1], o16[4 * i + 2], o16[4 * i + 3]);
+        }
+      }
+      if (qvalid) p.part_ml[vec] = make_float2(m_used, l_run);
     } else if (__all_sync(0xffffffffu, last_done)) {
       tc::fence_after();
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
@@ -589,7 +618,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           *reinterpret_cast<uint4 *>(dst + 16 * c + 8) = w1;
         }
       }
-    } else if (n_tiles > 0) {
+    } else if (n_blocks > 0) {
       atomicExch(p.err, 1);
       *fail = 1;
     }
