@@ -24,7 +24,10 @@
 //              softmax wrote P of each 64-key tile, O += P_hi V + P_lo V (M=128, N=D)
 //              with P read from TMEM and V read in place as an MN-major operand (keys are
 //              its K).  QK(b+1) waits for PV(b) to finish reading P from the S buffer it
-//              overwrites; the two query tiles' chains run independently.
+//              overwrites; the two query tiles' chains run independently.  A CTA with a
+//              single query tile in use double-buffers S in the other tile's columns
+//              instead: QK(b+1) then waits only for PV(b-1), so it runs during the
+//              softmax of block b.
 // Every mbarrier wait is bounded; on a timeout the CTA records the error, lets its
 // own TMA loads and MMAs finish (bounded), frees its TMEM and returns.
 #include "kvinc_internal.h"
@@ -133,6 +136,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Per query tile, one phase per K/V block.  The S buffer of a block is overwritten by
   // the next block's QK only after this block's PV is done, so no waiter can fall two
   // phases behind.
+  // With one query tile, S buffer i (i = block parity) uses s_full[i] and p_full[2i + h].
   uint64_t *s_full = kv_empty + kStages;          // [tile] QK done -> softmax
   uint64_t *p_full = s_full + kTilesQ;            // [tile][half] softmax wrote P -> MMA
   uint64_t *pv0_done = p_full + 2 * kTilesQ;      // [tile] PV of half 0 done -> softmax
@@ -149,6 +153,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_rho = row.n * p.rep;
   const int n_qt = min(kTilesQ, (n_rho - rho0 + kRows - 1) / kRows);  // query tiles in use
   const int rho_last = min(n_rho, rho0 + kRows * kTilesQ) - 1;
+  const bool dbl = n_qt == 1;  // one query tile: S double-buffered (see the MMA issuers)
   const int t_max = rho_last / p.rep;
   const int lens = row.lens;
   const int warp = threadIdx.x >> 5;
@@ -295,15 +300,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kIdQK = tc::idesc_bf16_f32(kRows, kBlockKeys);
       constexpr uint32_t kIdPV = tc::idesc_bf16_f32(kRows, D, /*b_mn_major=*/true);
       const uint32_t q_addr = ptx::smem_u32(qsm + qt * Cfg::kQBytes);
-      const uint32_t tS = tmem + qt * kBlockKeys;
       const uint32_t tO = tmem + kTilesQ * kBlockKeys + qt * D;
-      // QK(b): S of block b into this tile's S buffer, once the K/V stage has landed and
-      // PV(b - 1) has read P out of that buffer.  A block with one tile still multiplies
-      // all 128 rows of its K stage; the softmax masks the absent half.
+      // S buffer of block b, its barriers' index and phase: this tile's own, or with one
+      // query tile, buffer b & 1 (phase b >> 1).
+      auto sbuf = [&](int b) { return dbl ? (b & 1) : qt; };
+      auto sphase = [&](int b) -> uint32_t { return dbl ? (b >> 1) & 1 : b & 1; };
+      // QK(b): S of block b into its S buffer, once the K/V stage has landed and the PV
+      // that last read P out of that buffer (PV(b - 1), or PV(b - 2) when double-buffered)
+      // has finished.  A block with one tile still multiplies all 128 rows of its K stage;
+      // the softmax masks the absent half.
       auto issue_qk = [&](int b) -> bool {
         if (!ptx::mbar_wait(&kv_full[b % kStages], (b / kStages) & 1, kWaitLimit)) return false;
-        if (b >= 1 && !ptx::mbar_wait(&pv_done[qt], (b - 1) & 1, kWaitLimit)) return false;
+        const int prev = dbl ? b - 2 : b - 1;
+        if (prev >= 0 && !ptx::mbar_wait(&pv_done[qt], prev & 1, kWaitLimit)) return false;
         tc::fence_after();
+        const uint32_t tS = tmem + sbuf(b) * kBlockKeys;
         const uint32_t k_addr = ptx::smem_u32(kv + (b % kStages) * Cfg::kStageBytes);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -312,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::mma(tS, tc::desc_sw128(q_addr + off_q), tc::desc_sw128(k_addr + off_k), kIdQK,
                   kk > 0);
         }
-        tc::commit(&s_full[qt]);
+        tc::commit(&s_full[sbuf(b)]);
         return true;
       };
       // A tile of the block is partial when a segment ends inside it.
@@ -337,8 +348,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t v_addr =
             ptx::smem_u32(kv + (b % kStages) * Cfg::kStageBytes + Cfg::kKVBlock);
         const int halves = min(2, j_end - jb);
+        const uint32_t tS = tmem + sbuf(b) * kBlockKeys;
         for (int h = 0; h < halves; ++h) {
-          if (!ptx::mbar_wait(&p_full[2 * qt + h], b & 1, kWaitLimit)) return false;
+          if (!ptx::mbar_wait(&p_full[2 * sbuf(b) + h], sphase(b), kWaitLimit)) return false;
           tc::fence_after();
 #pragma unroll
           for (int ks = 0; ks < kKeys / 16; ++ks) {
@@ -354,13 +366,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
       if (n_blocks > 0) {  // (a key split past this CTA's last tile has no work)
+        // PV(b - 1) is issued before QK(b + 1) waits for it (double-buffered), and QK(b + 1)
+        // is issued before PV(b) waits for the softmax of block b, so it overlaps that.
         bool ok = issue_qk(0);
         for (int b = 0; ok && b < n_blocks; ++b) {
           if (*fail) {
             ok = false;
             break;
           }
-          ok = issue_pv(b) && (b + 1 >= n_blocks || issue_qk(b + 1));
+          if (dbl)
+            ok = (b + 1 >= n_blocks || issue_qk(b + 1)) && issue_pv(b);
+          else
+            ok = issue_pv(b) && (b + 1 >= n_blocks || issue_qk(b + 1));
         }
         if (!ok) {
           atomicExch(p.err, 1);
@@ -380,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int qpos = lens + (qvalid ? rho / p.rep : 0);
     const uint32_t lane_off = (uint32_t)(32 * (warp % 4)) << 16;
     const uint32_t tO = tmem + kTilesQ * kBlockKeys + qt * D + lane_off;
-    const uint32_t tS = tmem + qt * kBlockKeys + lane_off;
+    uint32_t tS = tmem + qt * kBlockKeys + lane_off;  // S buffer of the current block
     float m_used = -INFINITY;
     // visible key-index ranges of this row in the two segments
     int rg3[3][4];
@@ -515,16 +532,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       return 1;
     };
+    int buf = qt;  // S buffer (and barrier index) of the current block
     auto publish = [&](int h) {
       tc::wait_st();
       tc::fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&p_full[2 * qt + h]);
+      if (lane == 0) ptx::mbar_arrive(&p_full[2 * buf + h]);
     };
     bool ok = true;
     for (int b = 0; b < n_blocks && ok; ++b) {
+      buf = dbl ? (b & 1) : qt;
+      tS = tmem + buf * kBlockKeys + lane_off;
+      const uint32_t sph = dbl ? (b >> 1) & 1 : b & 1;
       // warp-uniform decisions: tcgen05.ld / st are warp-collective
-      const bool good = !*fail && ptx::mbar_wait(&s_full[qt], b & 1, kWaitLimit);
+      const bool good = !*fail && ptx::mbar_wait(&s_full[buf], sph, kWaitLimit);
       if (!__all_sync(0xffffffffu, good)) {
         ok = false;
         break;
@@ -552,9 +573,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       store_p(0, sv);
       publish(0);
       if (j0 + 1 < j_end) {
-        // a new maximum in tile 1 rescales O after PV of tile 0 (already issued) is done
-        if (!rescale_to(load_tile(j0 + 1, 1, sv),
-                        [&] { return ptx::mbar_wait(&pv0_done[qt], b & 1, kWaitLimit); })) {
+        // a new maximum in tile 1 rescales O after PV of tile 0 (already issued) is done.
+        // With S double-buffered, PV(b - 1) was issued after QK(b) and may still run: its
+        // phase is waited for first (a parity wait must not be two phases ahead).
+        if (!rescale_to(load_tile(j0 + 1, 1, sv), [&] {
+              return (b < 1 || ptx::mbar_wait(&pv_done[qt], (b - 1) & 1, kWaitLimit)) &&
+                     ptx::mbar_wait(&pv0_done[qt], b & 1, kWaitLimit);
+            })) {
           ok = false;
           break;
         }
@@ -566,8 +591,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::f2_unpack(l2, l0, l1);
     const float l_run = l0 + l1;
     // The last PV's completion implies every earlier MMA of the issuing thread is done.
+    // Double-buffered, PV(n_blocks - 2) may still run here, so pv_done may be two phases
+    // behind, or already done with both: wait on the one-phase drain barrier instead.
     const bool last_done =
-        ok && n_blocks > 0 && ptx::mbar_wait(&pv_done[qt], (n_blocks - 1) & 1, kWaitLimit);
+        ok && n_blocks > 0 &&
+        (dbl ? ptx::mbar_wait(drain, 0, kWaitLimit)
+             : ptx::mbar_wait(&pv_done[qt], (n_blocks - 1) & 1, kWaitLimit));
     if (!ok) {
       atomicExch(p.err, 1);
       *fail = 1;
