@@ -21,7 +21,7 @@ cudaError_t configure_decode();
 cudaError_t configure_prefill();
 cudaError_t configure_prefill_tc();
 cudaError_t launch_prefill_tc(const PrefillParams &p, int D, cudaStream_t s);
-int prefill_tc_rows_per_cta();
+int prefill_tc_tiles(int D);
 }  // namespace kvinc
 
 using namespace kvinc;
@@ -548,7 +548,7 @@ int append_device(kv_cache *c, int layer, const __nv_bfloat16 *q, const __nv_bfl
       for (const PrefillRow &r : prows)
         if ((hybrid || r.n * rep >= kTcMinRows) == (kind == 1)) sel.push_back(r);
       // the tcgen05 kernel holds one CTA per SM, the mma.sync kernel two
-      ents[kind] = split_prefill_rows(c, layer, sel, kind == 1 ? prefill_tc_rows_per_cta() : 64,
+      ents[kind] = split_prefill_rows(c, layer, sel, kind == 1 ? 128 * prefill_tc_tiles(D) : 64,
                                       kind == 1 ? 1 : 2, merges, &part_vecs);
     }
     if (part_vecs > 0) {
@@ -557,7 +557,7 @@ int append_device(kv_cache *c, int layer, const __nv_bfloat16 *q, const __nv_bfl
     }
     for (int kind = 0; kind < 2; ++kind) {
       const std::vector<PrefillRow> &sel = ents[kind];
-      const int rows_per_cta = kind == 1 ? prefill_tc_rows_per_cta() : 64;
+      const int rows_per_cta = kind == 1 ? 128 * prefill_tc_tiles(D) : 64;
       for (size_t r0 = 0; r0 < sel.size(); r0 += kMaxRowsPerLaunch) {
         const size_t r1 = std::min(sel.size(), r0 + kMaxRowsPerLaunch);
         pp.tmap_k = c->tmK[layer];
@@ -587,6 +587,7 @@ int append_device(kv_cache *c, int layer, const __nv_bfloat16 *q, const __nv_bfl
         pp.seg_rows2 = c->R + 1;
         pp.part_o = c->ppart_o;
         pp.part_ml = c->ppart_ml;
+        pp.tc_tiles = prefill_tc_tiles(D);
         int cta = 0;
         double bytes = 0, fl = 0;
         for (size_t j = r0; j < r1; ++j) {

@@ -119,6 +119,27 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// Maximum of 64 values: eight running three-input maxima, then a short tree (36
+// instructions, eight temporaries).
+__device__ __forceinline__ float max64(const float (&v)[64]) {
+  float a[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) a[k] = fmax3(v[k], v[8 + k], v[16 + k]);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) a[k] = fmax3(a[k], v[24 + k], v[32 + k]);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) a[k] = fmax3(a[k], v[40 + k], v[48 + k]);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) a[k] = fmaxf(a[k], v[56 + k]);
+  return fmax3(fmax3(a[0], a[1], a[2]), fmax3(a[3], a[4], a[5]), fmaxf(a[6], a[7]));
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
@@ -149,10 +170,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const PrefillRow &row = p.rows[find_cta_row(p, blockIdx.x)];
   const int g = blockIdx.y;
-  const int rho0 = (blockIdx.x - row.cta0) * kRows * kTilesQ;
+  const int tiles_cta = p.tc_tiles;  // query tiles per CTA of this launch (1 or 2)
+  const int rho0 = (blockIdx.x - row.cta0) * kRows * tiles_cta;
   const int n_rho = row.n * p.rep;
-  const int n_qt = min(kTilesQ, (n_rho - rho0 + kRows - 1) / kRows);  // query tiles in use
-  const int rho_last = min(n_rho, rho0 + kRows * kTilesQ) - 1;
+  const int n_qt = min(tiles_cta, (n_rho - rho0 + kRows - 1) / kRows);  // query tiles in use
+  const int rho_last = min(n_rho, rho0 + kRows * tiles_cta) - 1;
   const bool dbl = n_qt == 1;  // one query tile: S double-buffered (see the MMA issuers)
   const int t_max = rho_last / p.rep;
   const int lens = row.lens;
@@ -440,21 +462,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 16; ++i) v[16 * c + i] = t16[i];
       }
       tc::wait_ld();
-      float mt = -INFINITY;
       if (m.all_vis) {
 #pragma unroll
-        for (int i = 0; i < kKeys; ++i) {
-          v[i] *= scale;
-          mt = fmaxf(mt, v[i]);
-        }
+        for (int i = 0; i < kKeys; ++i) v[i] *= scale;
       } else {
 #pragma unroll
-        for (int i = 0; i < kKeys; ++i) {
-          v[i] = masked(m, i, v[i]);
-          mt = fmaxf(mt, v[i]);
-        }
+        for (int i = 0; i < kKeys; ++i) v[i] = masked(m, i, v[i]);
       }
-      return mt;
+      return max64(v);
     };
     // P = 2^(s - m) of tile h as bf16 high + low parts over its S columns: keys 2i, 2i+1
     // of the high part in column 64h + i, of the low part in column 64h + 32 + i.  The
@@ -672,8 +687,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-// Query rows one CTA of the tcgen05 prefill covers.
-int prefill_tc_rows_per_cta() { return kRows * kTilesQ; }
+// Query tiles (of 128 rows) per CTA of the tcgen05 prefill.  Two tiles share every K/V
+// block the CTA streams; a CTA whose row has only one tile of queries double-buffers S
+// instead.  (One tile per CTA throughout measured 10-40% slower: each K/V block is then
+// streamed once per tile.)
+int prefill_tc_tiles(int) { return kTilesQ; }
 
 cudaError_t launch_prefill_tc(const PrefillParams &p, int D, cudaStream_t s) {
   if (p.n_ctas <= 0) return cudaSuccess;
