@@ -590,16 +590,18 @@ def run_ours(args):
     graph_bytes, inputs, graphs = 0.0, [], []
     outs_l = [torch.empty((B, 1, Hq, D), dtype=torch.bfloat16, device=dev)
               for _ in range(n_layers)]
-    for r in range(rounds if not hybrid else 0):  # the step graph covers global/sliding layers
+    for r in range(rounds):
         lens_g = lens0[r] + (Wm if r == 0 else 0) + 2 * steps_in_round[r]
-        qs, ks, vs, _, _ = make_inputs(cfg, lens_g, steps_in_round[r], caches[r][1] + 2, dev,
-                                       stream)
-        inputs.append((qs, ks, vs))
-        g = caches[r][0].step_graph([qs[0, l] for l in range(n_layers)],
-                                    [ks[0, l] for l in range(n_layers)],
-                                    [vs[0, l] for l in range(n_layers)], outs_l)
-        bufs = [g.buffers([qs[s, l] for l in range(n_layers)], [ks[s, l] for l in range(n_layers)],
-                          [vs[s, l] for l in range(n_layers)], outs_l)
+        qs, ks, vs, kgs, vgs = make_inputs(cfg, lens_g, steps_in_round[r], caches[r][1] + 2,
+                                           dev, stream)
+        inputs.append((qs, ks, vs, kgs, vgs))
+        per_layer = lambda x, s: [x[s, l] for l in range(n_layers)]
+        glob = lambda x, s: ([x[s, l] if kinds[l] == 2 else None for l in range(n_layers)]
+                             if hybrid else None)
+        g = caches[r][0].step_graph(per_layer(qs, 0), per_layer(ks, 0), per_layer(vs, 0), outs_l,
+                                    k_global=glob(kgs, 0), v_global=glob(vgs, 0))
+        bufs = [g.buffers(per_layer(qs, s), per_layer(ks, s), per_layer(vs, s), outs_l,
+                          k_global=glob(kgs, s), v_global=glob(vgs, s))
                 for s in range(steps_in_round[r])]
         graphs.append((g, bufs))
         graph_bytes += sum(kv_bytes_per_step(cfg, lens_g + s) for s in range(steps_in_round[r]))
@@ -633,21 +635,14 @@ def run_ours(args):
                        for s in range(steps_in_round[r]))
     torch.cuda.synchronize()
 
-    # hybrid layers: the step's inputs copied from pinned host memory on the stream, the
-    # device call, the output copied back (kv_append_host covers global/sliding layers)
-    dq = torch.empty((B, 1, Hq, D), dtype=torch.bfloat16, device=dev)
-    dkv = [torch.empty((B, 1, Hk, D), dtype=torch.bfloat16, device=dev) for _ in range(4)]
-
     def step_host(c, hin, s):
         for layer in range(n_layers):
             if kinds[layer] in HYBRID:
-                dq.copy_(hin[0][s, layer], non_blocking=True)
-                xs = [None, None, None, None]
-                for i in range(4 if kinds[layer] == 2 else 2):
-                    dkv[i].copy_(hin[1 + i][s, layer], non_blocking=True)
-                    xs[i] = dkv[i]
-                append_layer(c, kinds[layer], layer, dq, *xs, ones, out, stream)
-                hout.copy_(out, non_blocking=True)
+                full = kinds[layer] == 2
+                c.append_hybrid_host(layer, hin[0][s, layer], hin[1][s, layer], hin[2][s, layer],
+                                     ones, k_global=hin[3][s, layer] if full else None,
+                                     v_global=hin[4][s, layer] if full else None, out=hout,
+                                     stream=stream)
             else:
                 c.append_host(layer, hin[0][s, layer], hin[1][s, layer], hin[2][s, layer], ones,
                               out=hout, stream=stream)

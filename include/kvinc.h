@@ -190,6 +190,12 @@ int kv_append_hybrid(kv_cache *c, int layer, const void *q, const void *k_local,
                      const void *v_local, const void *k_global, const void *v_global, int Hq,
                      int C, const int32_t *n_new, const int32_t *rows, int Bs, void *out,
                      void *stream);
+/* kv_append_hybrid with HOST buffers, as kv_append_host (page-locked ones used in place,
+ * pageable ones staged; `out` is written when the stream reaches this call). */
+int kv_append_hybrid_host(kv_cache *c, int layer, const void *q, const void *k_local,
+                          const void *v_local, const void *k_global, const void *v_global, int Hq,
+                          int C, const int32_t *n_new, const int32_t *rows, int Bs, void *out,
+                          void *stream);
 
 /*
  * Same as kv_append, but q, k, v and out are HOST buffers.  Page-locked buffers
@@ -310,13 +316,30 @@ int kv_step_graph_create(kv_cache *c, kv_step_graph **out, const void *const *q,
                          const int32_t *rows, int Bs);
 int kv_step_graph_set_buffers(kv_step_graph *g, const void *const *q, const void *const *k,
                               const void *const *v, void *const *outp);
+/* The step graph of a cache with hybrid layers (kv_step_graph_create returns KV_ERR_ARG
+ * for one): k[l], v[l] of a hybrid layer are its local keys and values, k_global[l],
+ * v_global[l] the group's global ones -- device bf16 [Bs][1][Hk][D], 16-byte aligned,
+ * given exactly for the KV_HYBRID_FULL layers and NULL for every other layer (the arrays
+ * themselves may be NULL on a cache without full hybrid layers).  A launch is then
+ * kv_append_hybrid / kv_append on every layer in order, then kv_advance.  Works on any
+ * cache. */
+int kv_step_graph_create_hybrid(kv_cache *c, kv_step_graph **out, const void *const *q,
+                                const void *const *k, const void *const *v,
+                                const void *const *k_global, const void *const *v_global,
+                                void *const *outp, int Hq, const int32_t *rows, int Bs);
+int kv_step_graph_set_buffers_hybrid(kv_step_graph *g, const void *const *q,
+                                     const void *const *k, const void *const *v,
+                                     const void *const *k_global, const void *const *v_global,
+                                     void *const *outp);
 int kv_step_graph_launch(kv_step_graph *g, void *stream);
 void kv_step_graph_destroy(kv_step_graph *g);
 
 /*
- * Prefix reuse and row export / import.  A row's state is its length and, per layer,
- * the K/V of the positions the layer keeps: all of [0, lens) on a global layer, the
- * last R of them on a sliding layer (ring slot p % R).  Copies move positions, so a
+ * Prefix reuse and row export / import.  A row's state is its length and, per storage
+ * unit, the K/V of the positions it keeps: all of [0, lens) in a full-length cache (a
+ * global layer's, a hybrid group's), the last R of them in a ring (a sliding layer's, a
+ * hybrid layer's own; slot p % R).  Units in order: per layer, the storage it owns (a
+ * hybrid local layer owns none), then its hybrid ring.  Copies move positions, so a
  * ring is copied position by position and a global prefix linearly ("inkling:
  * ring-buffer KV cache for sliding-window layers", review of the change: prefix reuse
  * by grow-with-copy must copy the ring whole, keeping t % win valid, and global rows
@@ -331,7 +354,7 @@ void kv_step_graph_destroy(kv_step_graph *g);
  *   W, layer layout, rope_theta and device.  Rows: host int32 [n]; destination rows
  *   distinct; in one cache no destination row may be another pair's source row.
  *   keep[i] <= the source length and <= dst's max_len, and every position the
- *   destination keeps must still be in the source: on caches with sliding layers,
+ *   destination keeps must still be in the source: on caches with rings,
  *   max(0, keep - R_dst) >= max(0, src_len - R_src) (a ring that has wrapped holds
  *   only its last R positions, so such a row can be copied whole but not truncated).
  *   Violations return KV_ERR_ARG before anything is enqueued.  Asynchronous on
@@ -340,8 +363,8 @@ void kv_step_graph_destroy(kv_step_graph *g);
  * kv_export_bytes: size of a row's state at length keep (-1 for a bad keep).
  * kv_export_row: writes the first `keep` tokens of `row` (keep <= its length, same
  *   presence rule) to the device buffer `dst` of exactly kv_export_bytes(c, keep)
- *   bytes, 16-byte aligned: per layer in order, K [Hk][n_l][D] then V [Hk][n_l][D]
- *   bf16, n_l = the layer's kept positions in ascending order.
+ *   bytes, 16-byte aligned: per storage unit in order, K [Hk][n_u][D] then V [Hk][n_u][D]
+ *   bf16, n_u = the unit's kept positions in ascending order.
  * kv_import_row: row `row` becomes that state (its length keep <= max_len); K/V of
  *   positions the row does not keep are left as they are.  The buffer is read on
  *   `stream`.  KV_ERR_ARG for bad arguments or a byte count that does not match.

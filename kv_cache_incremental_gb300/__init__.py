@@ -191,11 +191,12 @@ class KVCache:
                                  buf.element_size(), _stream_ptr(stream, buf.device)),
               "kv_import_row")
 
-    def step_graph(self, q, k, v, out, rows=None) -> "StepGraph":
+    def step_graph(self, q, k, v, out, rows=None, k_global=None, v_global=None) -> "StepGraph":
         """A static-shape decode step (every layer, one token per row, then advance) as a
         CUDA graph over fixed per-layer buffers q[l], k[l], v[l], out[l] of shape
-        (Bs, 1, heads, D); see StepGraph."""
-        return StepGraph(self, q, k, v, out, rows)
+        (Bs, 1, heads, D); hybrid full layers also take k_global[l], v_global[l]; see
+        StepGraph."""
+        return StepGraph(self, q, k, v, out, rows, k_global, v_global)
 
     def append_host(self, layer: int, q, k, v, n_new, rows=None, out=None, stream=None):
         """append() for CPU tensors (pinned for asynchronous copies); synchronise the stream
@@ -213,6 +214,30 @@ class KVCache:
                                   self.Hq, C, _i32_array(n_new), _i32_array(rows), Bs,
                                   out.data_ptr(), _stream_ptr(stream, self.device)),
               "kv_append_host")
+        return out
+
+    def append_hybrid_host(self, layer: int, q, k_local, v_local, n_new, k_global=None,
+                           v_global=None, rows=None, out=None, stream=None):
+        """append_hybrid() for CPU tensors (pinned for asynchronous copies); synchronise the
+        stream before reading `out`."""
+        import torch
+        for x, name in ((q, "q"), (k_local, "k_local"), (v_local, "v_local"),
+                        (k_global, "k_global"), (v_global, "v_global")):
+            if x is None:
+                continue
+            if x.dtype != torch.bfloat16:
+                raise TypeError(f"{name}: cache dtype bfloat16 != incoming dtype {x.dtype}")
+            if x.is_cuda or not x.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous CPU tensor")
+        Bs, C = q.shape[0], q.shape[1]
+        if out is None:
+            out = torch.empty_like(q)
+        ptr = lambda x: None if x is None else x.data_ptr()
+        check(_clib.kv_append_hybrid_host(self._h, layer, q.data_ptr(), k_local.data_ptr(),
+                                         v_local.data_ptr(), ptr(k_global), ptr(v_global),
+                                         self.Hq, C, _i32_array(n_new), _i32_array(rows), Bs,
+                                         out.data_ptr(), _stream_ptr(stream, self.device)),
+              "kv_append_hybrid_host")
         return out
 
     def advance(self, n_new, rows=None, stream=None) -> None:
@@ -313,23 +338,40 @@ class StepGraph:
 
     ``launch()`` is equivalent to ``cache.append(l, q[l], k[l], v[l], [1] * Bs, rows,
     out=out[l])`` for every layer followed by ``cache.advance([1] * Bs, rows)``: write the
-    step's inputs into the buffers given at construction, then launch.  The buffers must
-    stay alive as long as the graph.
+    step's inputs into the buffers given at construction, then launch.  On a cache with
+    hybrid layers, k[l], v[l] of a hybrid layer are its local keys and values and
+    k_global[l], v_global[l] the group's global ones (given for KV_HYBRID_FULL layers,
+    None elsewhere), as in append_hybrid.  The buffers must stay alive as long as the graph.
     """
 
-    def __init__(self, cache: KVCache, q, k, v, out, rows=None):
-        Bs = self._check(cache, q, k, v, out, q[0].shape[0] if len(q) else 0)
+    def __init__(self, cache: KVCache, q, k, v, out, rows=None, k_global=None, v_global=None):
+        Bs = q[0].shape[0] if len(q) else 0
+        self.hybrid = any(kind in (KV_HYBRID_FULL, KV_HYBRID_LOCAL) for kind in cache.layer_kinds)
+        self._check(cache, q, k, v, out, Bs, k_global, v_global)
         if rows is not None and len(rows) != Bs:
             raise ValueError("rows must have one entry per row of q")
         h = ctypes.c_void_p()
-        check(_clib.kv_step_graph_create(cache._h, ctypes.byref(h), *self._ptrs(q, k, v, out),
-                                        cache.Hq, _i32_array(rows), Bs), "kv_step_graph_create")
+        if self.hybrid:
+            qp, kp, vp, op = self._ptrs(q, k, v, out)
+            gk, gv = self._ptrs(self._opt(k_global, len(q)), self._opt(v_global, len(q)))
+            check(_clib.kv_step_graph_create_hybrid(cache._h, ctypes.byref(h), qp, kp, vp, gk, gv,
+                                                   op, cache.Hq, _i32_array(rows), Bs),
+                  "kv_step_graph_create_hybrid")
+        else:
+            check(_clib.kv_step_graph_create(cache._h, ctypes.byref(h),
+                                            *self._ptrs(q, k, v, out), cache.Hq,
+                                            _i32_array(rows), Bs), "kv_step_graph_create")
         self._h, self.cache, self.Bs = h, cache, Bs
-        self._keep = (list(q), list(k), list(v), list(out))  # the graph reads these buffers
+        # the graph reads these buffers
+        self._keep = (list(q), list(k), list(v), list(out), k_global, v_global)
         cache._graphs.add(self)
 
     @staticmethod
-    def _check(cache, q, k, v, out, Bs):
+    def _opt(ts, n):
+        return [None] * n if ts is None else list(ts)
+
+    @staticmethod
+    def _check(cache, q, k, v, out, Bs, k_global=None, v_global=None):
         n = len(cache.layer_kinds)
         if not (len(q) == len(k) == len(v) == len(out) == n):
             raise ValueError(f"one q, k, v and out tensor per layer ({n})")
@@ -338,24 +380,42 @@ class StepGraph:
             cache._check_tensor(k[l], f"k[{l}]", cache.Hk, 1, Bs)
             cache._check_tensor(v[l], f"v[{l}]", cache.Hk, 1, Bs)
             cache._check_tensor(out[l], f"out[{l}]", cache.Hq, 1, Bs)
+        for name, ts in (("k_global", k_global), ("v_global", v_global)):
+            ts = StepGraph._opt(ts, n)
+            if len(ts) != n:
+                raise ValueError(f"{name}: one entry per layer ({n})")
+            for l, t in enumerate(ts):
+                if (t is not None) != (cache.layer_kinds[l] == KV_HYBRID_FULL):
+                    raise ValueError(f"{name}[{l}]: a tensor exactly on KV_HYBRID_FULL layers")
+                if t is not None:
+                    cache._check_tensor(t, f"{name}[{l}]", cache.Hk, 1, Bs)
         return Bs
 
     @staticmethod
     def _ptrs(*groups):
-        return [(ctypes.c_void_p * len(ts))(*[t.data_ptr() for t in ts]) for ts in groups]
+        return [(ctypes.c_void_p * len(ts))(*[None if t is None else t.data_ptr() for t in ts])
+                for ts in groups]
 
-    def buffers(self, q, k, v, out) -> "StepBuffers":
+    def buffers(self, q, k, v, out, k_global=None, v_global=None) -> "StepBuffers":
         """A validated set of per-layer buffers (same shapes as at construction) that
         launch(buffers=...) switches to without further checks."""
-        self._check(self.cache, q, k, v, out, self.Bs)
-        return StepBuffers(self._ptrs(q, k, v, out), (list(q), list(k), list(v), list(out)))
+        self._check(self.cache, q, k, v, out, self.Bs, k_global, v_global)
+        n = len(q)
+        ptrs = self._ptrs(q, k, v, self._opt(k_global, n), self._opt(v_global, n), out)
+        return StepBuffers(ptrs, (list(q), list(k), list(v), list(out), k_global, v_global))
 
-    def set_buffers(self, q, k, v, out) -> None:
+    def set_buffers(self, q, k, v, out, k_global=None, v_global=None) -> None:
         """Point the following launches at other per-layer buffers of the same shapes."""
-        self._use(self.buffers(q, k, v, out))
+        self._use(self.buffers(q, k, v, out, k_global, v_global))
 
     def _use(self, b: "StepBuffers") -> None:
-        check(_clib.kv_step_graph_set_buffers(self._h, *b.ptrs), "kv_step_graph_set_buffers")
+        qp, kp, vp, gk, gv, op = b.ptrs
+        if self.hybrid:
+            check(_clib.kv_step_graph_set_buffers_hybrid(self._h, qp, kp, vp, gk, gv, op),
+                  "kv_step_graph_set_buffers_hybrid")
+        else:
+            check(_clib.kv_step_graph_set_buffers(self._h, qp, kp, vp, op),
+                  "kv_step_graph_set_buffers")
         self._keep = b.tensors
 
     def launch(self, stream=None, buffers: Optional["StepBuffers"] = None) -> None:

@@ -34,6 +34,9 @@ SIGNATURES = {
                           c_int, c_void_p, c_void_p]),
     "kv_append_hybrid": (c_int, [c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                  c_int, c_int, P_i32, P_i32, c_int, c_void_p, c_void_p]),
+    "kv_append_hybrid_host": (c_int, [c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_void_p,
+                                      c_void_p, c_int, c_int, P_i32, P_i32, c_int, c_void_p,
+                                      c_void_p]),
     "kv_append_host": (c_int, [c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_int, c_int, P_i32,
                                P_i32, c_int, c_void_p, c_void_p]),
     "kv_advance": (c_int, [c_void_p, P_i32, P_i32, c_int, c_void_p]),
@@ -58,6 +61,9 @@ SIGNATURES = {
     "kv_step_graph_set_buffers": (c_int, [c_void_p, ctypes.POINTER(c_void_p),
                                           ctypes.POINTER(c_void_p), ctypes.POINTER(c_void_p),
                                           ctypes.POINTER(c_void_p)]),
+    "kv_step_graph_create_hybrid": (c_int, [c_void_p, ctypes.POINTER(c_void_p)]
+                                    + [ctypes.POINTER(c_void_p)] * 6 + [c_int, P_i32, c_int]),
+    "kv_step_graph_set_buffers_hybrid": (c_int, [c_void_p] + [ctypes.POINTER(c_void_p)] * 6),
     "kv_step_graph_launch": (c_int, [c_void_p, c_void_p]),
     "kv_step_graph_destroy": (None, [c_void_p]),
     "kv_copy_rows": (c_int, [c_void_p, P_i32, c_void_p, P_i32, P_i32, c_int, c_void_p]),

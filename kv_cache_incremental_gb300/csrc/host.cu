@@ -997,6 +997,60 @@ static const void *mapped_host(const void *p) {
   return nullptr;
 }
 
+// Host-buffer form of one layer's append: k, v are the layer's keys and values (a hybrid
+// layer: the group's global ones, NULL on a local layer), kl, vl a hybrid layer's local ones.
+// Page-locked buffers are used in place (the kernels read the inputs and write the outputs in
+// host memory; the bytes cross NVLink-C2C inside the kernels); pageable ones are staged
+// through device buffers owned by the cache.
+static int append_host_impl(kv_cache *c, int layer, const void *q, const void *k, const void *v,
+                            const void *kl, const void *vl, int C, const int32_t *n_new,
+                            const std::vector<int32_t> &cache_rows, int Bs, void *out,
+                            cudaStream_t s) {
+  const void *src[5] = {q, k, v, kl, vl};
+  const void *mapped[5] = {};
+  bool all_mapped = true;
+  for (int i = 0; i < 5; ++i) {
+    if (!src[i]) continue;
+    mapped[i] = mapped_host(src[i]);
+    all_mapped = all_mapped && mapped[i] && aligned16(mapped[i]);
+  }
+  void *mo = const_cast<void *>(mapped_host(out));
+  if (all_mapped && mo && aligned16(mo))
+    return append_device(c, layer, (const __nv_bfloat16 *)mapped[0],
+                         (const __nv_bfloat16 *)mapped[1], (const __nv_bfloat16 *)mapped[2], C,
+                         n_new, cache_rows, Bs, (__nv_bfloat16 *)mo, s,
+                         (const __nv_bfloat16 *)mapped[3], (const __nv_bfloat16 *)mapped[4]);
+  const size_t qb = (size_t)Bs * C * c->Hq * c->D * 2, kb = (size_t)Bs * C * c->Hk * c->D * 2;
+  const size_t sizes[5] = {qb, kb, kb, kb, kb};
+  auto al = [](size_t x) { return (x + 15) & ~size_t(15); };
+  size_t need = al(qb) + 64;  // the output
+  for (int i = 0; i < 5; ++i)
+    if (src[i]) need += al(sizes[i]);
+  if (need > c->stage_bytes) {
+    // The old buffer may still be in use by queued work on this stream.
+    if (c->stage && cudaStreamSynchronize(s) != cudaSuccess) return KV_ERR_CUDA;
+    cudaFree(c->stage);
+    c->stage = nullptr;
+    c->stage_bytes = 0;
+    if (cudaMalloc(&c->stage, need) != cudaSuccess) return KV_ERR_OOM;
+    c->stage_bytes = need;
+  }
+  char *cur = (char *)c->stage;
+  const __nv_bfloat16 *dev[5] = {};
+  for (int i = 0; i < 5; ++i) {
+    if (!src[i]) continue;
+    if (cudaMemcpyAsync(cur, src[i], sizes[i], cudaMemcpyHostToDevice, s) != cudaSuccess)
+      return KV_ERR_CUDA;
+    dev[i] = (const __nv_bfloat16 *)cur;
+    cur += al(sizes[i]);
+  }
+  __nv_bfloat16 *dout = (__nv_bfloat16 *)cur;
+  const int r = append_device(c, layer, dev[0], dev[1], dev[2], C, n_new, cache_rows, Bs, dout,
+                              s, dev[3], dev[4]);
+  if (r != KV_OK) return r;
+  return set_err(cudaMemcpyAsync(out, dout, qb, cudaMemcpyDeviceToHost, s));
+}
+
 int kv_append_host(kv_cache *c, int layer, const void *q, const void *k, const void *v, int Hq,
                    int C, const int32_t *n_new, const int32_t *rows, int Bs, void *out,
                    void *stream) {
@@ -1010,60 +1064,26 @@ int kv_append_host(kv_cache *c, int layer, const void *q, const void *k, const v
   if (!any) return KV_OK;
   if (!q || !k || !v || !out) return KV_ERR_ARG;
   DeviceGuard guard(c->device);
-  cudaStream_t s = (cudaStream_t)stream;
-  // Page-locked buffers: the kernels read the inputs and write the outputs in host
-  // memory directly; the bytes cross NVLink-C2C inside the kernels.
-  const void *mq = mapped_host(q), *mk = mapped_host(k), *mv = mapped_host(v);
-  void *mo = const_cast<void *>(mapped_host(out));
-  if (mq && mk && mv && mo && aligned16(mq) && aligned16(mk) && aligned16(mv) && aligned16(mo))
-    return append_device(c, layer, (const __nv_bfloat16 *)mq, (const __nv_bfloat16 *)mk,
-                         (const __nv_bfloat16 *)mv, C, n_new, cache_rows, Bs,
-                         (__nv_bfloat16 *)mo, s);
-  // Pageable buffers: stage through device buffers owned by the cache.
-  const size_t qb = (size_t)Bs * C * c->Hq * c->D * 2, kb = (size_t)Bs * C * c->Hk * c->D * 2;
-  const size_t need = 2 * qb + 2 * kb + 64;
-  if (need > c->stage_bytes) {
-    // The old buffer may still be in use by queued work on this stream.
-    if (c->stage && cudaStreamSynchronize(s) != cudaSuccess) return KV_ERR_CUDA;
-    cudaFree(c->stage);
-    c->stage = nullptr;
-    c->stage_bytes = 0;
-    if (cudaMalloc(&c->stage, need) != cudaSuccess) return KV_ERR_OOM;
-    c->stage_bytes = need;
-  }
-  auto al = [](size_t x) { return (x + 15) & ~size_t(15); };
-  char *base = (char *)c->stage;
-  char *dq = base, *dk = dq + al(qb), *dv = dk + al(kb), *dout = dv + al(kb);
-  if (cudaMemcpyAsync(dq, q, qb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-      cudaMemcpyAsync(dk, k, kb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-      cudaMemcpyAsync(dv, v, kb, cudaMemcpyHostToDevice, s) != cudaSuccess)
-    return KV_ERR_CUDA;
-  const int r = append_device(c, layer, (const __nv_bfloat16 *)dq, (const __nv_bfloat16 *)dk,
-                              (const __nv_bfloat16 *)dv, C, n_new, cache_rows, Bs,
-                              (__nv_bfloat16 *)dout, s);
-  if (r != KV_OK) return r;
-  return set_err(cudaMemcpyAsync(out, dout, qb, cudaMemcpyDeviceToHost, s));
+  return append_host_impl(c, layer, q, k, v, nullptr, nullptr, C, n_new, cache_rows, Bs, out,
+                          (cudaStream_t)stream);
 }
 
-int kv_append_hybrid(kv_cache *c, int layer, const void *q, const void *k_local,
-                     const void *v_local, const void *k_global, const void *v_global, int Hq,
-                     int C, const int32_t *n_new, const int32_t *rows, int Bs, void *out,
-                     void *stream) {
+// Checks shared by the hybrid entry points; fills cache_rows.  KV_OK with any = false: no
+// row has new tokens.
+static int check_hybrid(kv_cache *c, int layer, const void *q, const void *k_local,
+                        const void *v_local, const void *k_global, const void *v_global, int Hq,
+                        int C, const int32_t *n_new, const int32_t *rows, int Bs, const void *out,
+                        std::vector<int32_t> &cache_rows, bool &any) {
   if (!c || layer < 0 || layer >= c->n_layers || Hq != c->Hq || C < 1) return KV_ERR_ARG;
   if (!is_hybrid(c->kind[layer])) return KV_ERR_ARG;
   const bool full = c->kind[layer] == KV_HYBRID_FULL;
-  std::vector<int32_t> cache_rows;
   const int rc = check_rows(c, n_new, rows, Bs, C, cache_rows);
   if (rc != KV_OK) return rc;
-  bool any = false;
+  any = false;
   for (int i = 0; i < Bs; ++i) any |= n_new[i] > 0;
   if (!any) return KV_OK;
-  if (!q || !k_local || !v_local || !out || !aligned16(q) || !aligned16(k_local) ||
-      !aligned16(v_local) || !aligned16(out))
-    return KV_ERR_ARG;
-  if (full ? (!k_global || !v_global || !aligned16(k_global) || !aligned16(v_global))
-           : (k_global || v_global))
-    return KV_ERR_ARG;
+  if (!q || !k_local || !v_local || !out) return KV_ERR_ARG;
+  if (full ? (!k_global || !v_global) : (k_global || v_global)) return KV_ERR_ARG;
   // a local layer reads the group's global keys of these tokens: its full layer must
   // have appended exactly them
   const std::vector<int32_t> &he = c->hy_end[c->group[layer]];
@@ -1071,16 +1091,51 @@ int kv_append_hybrid(kv_cache *c, int layer, const void *q, const void *k_local,
     for (int i = 0; i < Bs; ++i)
       if (n_new[i] > 0 && he[cache_rows[i]] != c->lens[cache_rows[i]] + n_new[i])
         return KV_ERR_ARG;
+  return KV_OK;
+}
+
+static void note_hybrid_append(kv_cache *c, int layer, const int32_t *n_new,
+                               const std::vector<int32_t> &cache_rows, int Bs) {
+  if (c->kind[layer] != KV_HYBRID_FULL) return;
+  for (int i = 0; i < Bs; ++i)
+    if (n_new[i] > 0) c->hy_end[layer][cache_rows[i]] = c->lens[cache_rows[i]] + n_new[i];
+}
+
+int kv_append_hybrid(kv_cache *c, int layer, const void *q, const void *k_local,
+                     const void *v_local, const void *k_global, const void *v_global, int Hq,
+                     int C, const int32_t *n_new, const int32_t *rows, int Bs, void *out,
+                     void *stream) {
+  std::vector<int32_t> cache_rows;
+  bool any = false;
+  int rc = check_hybrid(c, layer, q, k_local, v_local, k_global, v_global, Hq, C, n_new, rows,
+                        Bs, out, cache_rows, any);
+  if (rc != KV_OK || !any) return rc;
+  for (const void *x : {q, k_local, v_local, (const void *)out})
+    if (!aligned16(x)) return KV_ERR_ARG;
+  if (k_global && (!aligned16(k_global) || !aligned16(v_global))) return KV_ERR_ARG;
   DeviceGuard guard(c->device);
-  const int r = append_device(c, layer, (const __nv_bfloat16 *)q,
-                              (const __nv_bfloat16 *)k_global, (const __nv_bfloat16 *)v_global,
-                              C, n_new, cache_rows, Bs, (__nv_bfloat16 *)out,
-                              (cudaStream_t)stream, (const __nv_bfloat16 *)k_local,
-                              (const __nv_bfloat16 *)v_local);
-  if (r == KV_OK && full)
-    for (int i = 0; i < Bs; ++i)
-      if (n_new[i] > 0) c->hy_end[layer][cache_rows[i]] = c->lens[cache_rows[i]] + n_new[i];
-  return r;
+  rc = append_device(c, layer, (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)k_global,
+                     (const __nv_bfloat16 *)v_global, C, n_new, cache_rows, Bs,
+                     (__nv_bfloat16 *)out, (cudaStream_t)stream,
+                     (const __nv_bfloat16 *)k_local, (const __nv_bfloat16 *)v_local);
+  if (rc == KV_OK) note_hybrid_append(c, layer, n_new, cache_rows, Bs);
+  return rc;
+}
+
+int kv_append_hybrid_host(kv_cache *c, int layer, const void *q, const void *k_local,
+                          const void *v_local, const void *k_global, const void *v_global, int Hq,
+                          int C, const int32_t *n_new, const int32_t *rows, int Bs, void *out,
+                          void *stream) {
+  std::vector<int32_t> cache_rows;
+  bool any = false;
+  int rc = check_hybrid(c, layer, q, k_local, v_local, k_global, v_global, Hq, C, n_new, rows,
+                        Bs, out, cache_rows, any);
+  if (rc != KV_OK || !any) return rc;
+  DeviceGuard guard(c->device);
+  rc = append_host_impl(c, layer, q, k_global, v_global, k_local, v_local, C, n_new, cache_rows,
+                        Bs, out, (cudaStream_t)stream);
+  if (rc == KV_OK) note_hybrid_append(c, layer, n_new, cache_rows, Bs);
+  return rc;
 }
 
 int kv_advance(kv_cache *c, const int32_t *n_new, const int32_t *rows, int Bs, void *stream) {
@@ -1212,6 +1267,7 @@ struct kv_step_graph {
   int Bs = 0;
   std::vector<int32_t> rows;  // cache rows
   std::vector<const __nv_bfloat16 *> q, k, v;
+  std::vector<const __nv_bfloat16 *> kg, vg;  // hybrid full layers: the group's new global keys
   std::vector<__nv_bfloat16 *> out;
   std::vector<DecodeParams> dps;  // per layer (each ~20 KB: kept on the heap)
   StateParams sp;
@@ -1236,8 +1292,12 @@ void plan_step(kv_step_graph *g) {
   g->flops = 0;
   for (int l = 0; l < c->n_layers; ++l) {
     double by = 0, fl = 0;
-    fill_decode(c, l, g->q[l], g->k[l], g->v[l], g->out[l], q_row, kv_row, batch, g->dps[l], by,
-                fl);
+    if (is_hybrid(c->kind[l]))  // k, v: the layer's local keys; kg, vg: the group's
+      fill_decode(c, l, g->q[l], g->kg[l], g->vg[l], g->out[l], q_row, kv_row, batch,
+                  g->dps[l], by, fl, g->k[l], g->v[l]);
+    else
+      fill_decode(c, l, g->q[l], g->k[l], g->v[l], g->out[l], q_row, kv_row, batch, g->dps[l],
+                  by, fl);
     g->bytes += by;
     g->flops += fl;
   }
@@ -1247,21 +1307,50 @@ void plan_step(kv_step_graph *g) {
   }
 }
 
-void free_step_graph(kv_step_graph *g) {
-  if (g->exec) cudaGraphExecDestroy(g->exec);
-  if (g->graph) cudaGraphDestroy(g->graph);
-  delete g;
+// Per-layer buffer arrays valid for the cache's layers: every q, k, v, out set and 16-byte
+// aligned; kg, vg (may be NULL on a cache without hybrid full layers) set exactly on
+// KV_HYBRID_FULL layers.
+bool step_buffers_ok(const kv_cache *c, const void *const *q, const void *const *k,
+                     const void *const *v, const void *const *kg, const void *const *vg,
+                     void *const *outp) {
+  if (!q || !k || !v || !outp) return false;
+  for (int l = 0; l < c->n_layers; ++l) {
+    if (!q[l] || !k[l] || !v[l] || !outp[l] || !aligned16(q[l]) || !aligned16(k[l]) ||
+        !aligned16(v[l]) || !aligned16(outp[l]))
+      return false;
+    const bool full = c->kind[l] == KV_HYBRID_FULL;
+    const void *a = kg ? kg[l] : nullptr, *b = vg ? vg[l] : nullptr;
+    if (full ? (!a || !b || !aligned16(a) || !aligned16(b)) : (a || b)) return false;
+  }
+  return true;
 }
 
-}  // namespace
+void set_step_buffers(kv_step_graph *g, const void *const *q, const void *const *k,
+                      const void *const *v, const void *const *kg, const void *const *vg,
+                      void *const *outp) {
+  const int L = g->c->n_layers;
+  g->q.assign(L, nullptr);
+  g->k.assign(L, nullptr);
+  g->v.assign(L, nullptr);
+  g->kg.assign(L, nullptr);
+  g->vg.assign(L, nullptr);
+  g->out.assign(L, nullptr);
+  for (int l = 0; l < L; ++l) {
+    g->q[l] = (const __nv_bfloat16 *)q[l];
+    g->k[l] = (const __nv_bfloat16 *)k[l];
+    g->v[l] = (const __nv_bfloat16 *)v[l];
+    g->kg[l] = (const __nv_bfloat16 *)(kg ? kg[l] : nullptr);
+    g->vg[l] = (const __nv_bfloat16 *)(vg ? vg[l] : nullptr);
+    g->out[l] = (__nv_bfloat16 *)outp[l];
+  }
+}
 
-extern "C" {
-
-int kv_step_graph_create(kv_cache *c, kv_step_graph **out, const void *const *q,
-                         const void *const *k, const void *const *v, void *const *outp, int Hq,
-                         const int32_t *rows, int Bs) {
-  if (!c || !out || !q || !k || !v || !outp || Hq != c->Hq) return KV_ERR_ARG;
-  if (Bs < 1 || Bs > c->B || Bs > kMaxRowsPerLaunch || has_hybrid(c)) return KV_ERR_ARG;
+int step_graph_create(kv_cache *c, kv_step_graph **out, const void *const *q,
+                      const void *const *k, const void *const *v, const void *const *kg,
+                      const void *const *vg, void *const *outp, int Hq, const int32_t *rows,
+                      int Bs) {
+  if (!c || !out || Hq != c->Hq) return KV_ERR_ARG;
+  if (Bs < 1 || Bs > c->B || Bs > kMaxRowsPerLaunch) return KV_ERR_ARG;
   std::vector<int32_t> cache_rows;
   std::vector<char> seen(c->B, 0);
   for (int i = 0; i < Bs; ++i) {
@@ -1270,21 +1359,13 @@ int kv_step_graph_create(kv_cache *c, kv_step_graph **out, const void *const *q,
     seen[r] = 1;
     cache_rows.push_back(r);
   }
-  for (int l = 0; l < c->n_layers; ++l)
-    if (!q[l] || !k[l] || !v[l] || !outp[l] || !aligned16(q[l]) || !aligned16(k[l]) ||
-        !aligned16(v[l]) || !aligned16(outp[l]))
-      return KV_ERR_ARG;
+  if (!step_buffers_ok(c, q, k, v, kg, vg, outp)) return KV_ERR_ARG;
   DeviceGuard guard(c->device);
   kv_step_graph *g = new kv_step_graph;
   g->c = c;
   g->Bs = Bs;
   g->rows = cache_rows;
-  for (int l = 0; l < c->n_layers; ++l) {
-    g->q.push_back((const __nv_bfloat16 *)q[l]);
-    g->k.push_back((const __nv_bfloat16 *)k[l]);
-    g->v.push_back((const __nv_bfloat16 *)v[l]);
-    g->out.push_back((__nv_bfloat16 *)outp[l]);
-  }
+  set_step_buffers(g, q, k, v, kg, vg, outp);
   g->dps.resize(c->n_layers);
   plan_step(g);
   const int nt = c->Hq / c->Hk <= 8 ? 1 : 2;
@@ -1308,7 +1389,9 @@ int kv_step_graph_create(kv_cache *c, kv_step_graph **out, const void *const *q,
   }
   ok = ok && cudaGraphInstantiate(&g->exec, g->graph, 0) == cudaSuccess;
   if (!ok) {
-    free_step_graph(g);
+    if (g->exec) cudaGraphExecDestroy(g->exec);
+    if (g->graph) cudaGraphDestroy(g->graph);
+    delete g;
     cudaGetLastError();
     return KV_ERR_CUDA;
   }
@@ -1316,20 +1399,44 @@ int kv_step_graph_create(kv_cache *c, kv_step_graph **out, const void *const *q,
   return KV_OK;
 }
 
+void free_step_graph(kv_step_graph *g) {
+  if (g->exec) cudaGraphExecDestroy(g->exec);
+  if (g->graph) cudaGraphDestroy(g->graph);
+  delete g;
+}
+
+}  // namespace
+
+extern "C" {
+
+int kv_step_graph_create(kv_cache *c, kv_step_graph **out, const void *const *q,
+                         const void *const *k, const void *const *v, void *const *outp, int Hq,
+                         const int32_t *rows, int Bs) {
+  if (!c || has_hybrid(c)) return KV_ERR_ARG;  // kv_step_graph_create_hybrid
+  return step_graph_create(c, out, q, k, v, nullptr, nullptr, outp, Hq, rows, Bs);
+}
+
+int kv_step_graph_create_hybrid(kv_cache *c, kv_step_graph **out, const void *const *q,
+                                const void *const *k, const void *const *v,
+                                const void *const *k_global, const void *const *v_global,
+                                void *const *outp, int Hq, const int32_t *rows, int Bs) {
+  return step_graph_create(c, out, q, k, v, k_global, v_global, outp, Hq, rows, Bs);
+}
+
 int kv_step_graph_set_buffers(kv_step_graph *g, const void *const *q, const void *const *k,
                               const void *const *v, void *const *outp) {
-  if (!g || !q || !k || !v || !outp) return KV_ERR_ARG;
-  const int L = g->c->n_layers;
-  for (int l = 0; l < L; ++l)
-    if (!q[l] || !k[l] || !v[l] || !outp[l] || !aligned16(q[l]) || !aligned16(k[l]) ||
-        !aligned16(v[l]) || !aligned16(outp[l]))
-      return KV_ERR_ARG;
-  for (int l = 0; l < L; ++l) {
-    g->q[l] = (const __nv_bfloat16 *)q[l];
-    g->k[l] = (const __nv_bfloat16 *)k[l];
-    g->v[l] = (const __nv_bfloat16 *)v[l];
-    g->out[l] = (__nv_bfloat16 *)outp[l];
-  }
+  if (!g || has_hybrid(g->c) || !step_buffers_ok(g->c, q, k, v, nullptr, nullptr, outp))
+    return KV_ERR_ARG;
+  set_step_buffers(g, q, k, v, nullptr, nullptr, outp);
+  return KV_OK;
+}
+
+int kv_step_graph_set_buffers_hybrid(kv_step_graph *g, const void *const *q,
+                                     const void *const *k, const void *const *v,
+                                     const void *const *k_global, const void *const *v_global,
+                                     void *const *outp) {
+  if (!g || !step_buffers_ok(g->c, q, k, v, k_global, v_global, outp)) return KV_ERR_ARG;
+  set_step_buffers(g, q, k, v, k_global, v_global, outp);
   return KV_OK;
 }
 
@@ -1365,7 +1472,11 @@ int kv_step_graph_launch(kv_step_graph *g, void *stream) {
   const cudaError_t e = timed(c, KV_KERNEL_STEP, g->bytes, g->flops, s,
                               [&] { return cudaGraphLaunch(g->exec, s); });
   if (e != cudaSuccess) return KV_ERR_CUDA;
-  for (int r : g->rows) c->lens[r] += 1;
+  for (int r : g->rows) {
+    c->lens[r] += 1;
+    for (auto &he : c->hy_end)
+      if (!he.empty()) he[r] = c->lens[r];  // the step's layers ran in order
+  }
   return KV_OK;
 }
 
@@ -1380,17 +1491,42 @@ void kv_step_graph_destroy(kv_step_graph *g) {
 // ---------------------------------------------------------------- row copies
 namespace {
 
-// Positions of a row kept by a layer once its length is `keep`: all of [0, keep) on a global
-// layer, the last R of them on a sliding layer.
-int first_kept(const kv_cache *c, int layer, int keep) {
-  return c->kind[layer] == KV_SLIDING ? std::max(0, keep - c->R) : 0;
+// A storage unit of a row's state: a layer's own storage (a global cache, a sliding ring,
+// a hybrid group's cache held by its full layer; a hybrid local layer has none of its own),
+// or a hybrid layer's ring.  Units in order: per layer, its storage, then its ring.
+struct Unit {
+  int layer;
+  bool hring;  // the layer's hybrid ring (else its storage K[layer] / V[layer])
+  bool ring;   // positions p live at slot p % R
+};
+
+std::vector<Unit> units(const kv_cache *c) {
+  std::vector<Unit> u;
+  for (int l = 0; l < c->n_layers; ++l) {
+    if (c->owns[l]) u.push_back({l, false, c->kind[l] == KV_SLIDING});
+    if (is_hybrid(c->kind[l])) u.push_back({l, true, true});
+  }
+  return u;
 }
 
-// Storage block of (row, layer): K, V and the element stride between heads.
+int first_kept(const kv_cache *c, const Unit &u, int keep) {
+  return u.ring ? std::max(0, keep - c->R) : 0;
+}
+
+// Storage block of (row, unit): K, V and the element stride between heads.
 // A paged global layer returns its pool and the row's block-table row instead.
-void row_block(const kv_cache *c, int layer, int row, __nv_bfloat16 *&k, __nv_bfloat16 *&v,
-               int64_t &head_stride, const int32_t *&table, int32_t &pool) {
+void row_block(const kv_cache *c, const Unit &u, int row, __nv_bfloat16 *&k,
+               __nv_bfloat16 *&v, int64_t &head_stride, const int32_t *&table, int32_t &pool) {
+  const int layer = u.layer;
   pool = c->n_blocks;
+  table = nullptr;
+  if (u.hring) {
+    const int64_t off = (int64_t)row * c->Hk * (c->R + 1) * c->D;
+    k = (__nv_bfloat16 *)c->RK[layer] + off;
+    v = (__nv_bfloat16 *)c->RV[layer] + off;
+    head_stride = (int64_t)(c->R + 1) * c->D;
+    return;
+  }
   if (paged_layer(c, layer)) {
     k = (__nv_bfloat16 *)c->K[layer];
     v = (__nv_bfloat16 *)c->V[layer];
@@ -1409,9 +1545,9 @@ void row_block(const kv_cache *c, int layer, int row, __nv_bfloat16 *&k, __nv_bf
 // keeps?  Ring positions older than lens - R are gone from a sliding layer.
 bool positions_present(const kv_cache *src, int lens, int keep, int dst_R) {
   if (keep > lens) return false;
-  bool sliding = false;
-  for (int k : src->kind) sliding |= k == KV_SLIDING;
-  if (!sliding) return true;
+  bool ringed = false;  // any ring: sliding or hybrid layers
+  for (int k : src->kind) ringed |= k != KV_GLOBAL;
+  if (!ringed) return true;
   const int need_lo = std::max(0, keep - dst_R);
   const int have_lo = std::max(0, lens - src->R);
   return need_lo >= have_lo;
@@ -1457,7 +1593,7 @@ extern "C" {
 int kv_copy_rows(kv_cache *dst, const int32_t *dst_rows, const kv_cache *src,
                  const int32_t *src_rows, const int32_t *keep, int n, void *stream) {
   if (!dst || !src || n < 0 || (n > 0 && (!dst_rows || !src_rows))) return KV_ERR_ARG;
-  if (!same_layout(dst, src) || has_hybrid(src)) return KV_ERR_ARG;
+  if (!same_layout(dst, src)) return KV_ERR_ARG;
   std::vector<int32_t> kp(n);
   std::vector<char> dseen(dst->B, 0);
   for (int i = 0; i < n; ++i) {
@@ -1485,18 +1621,19 @@ int kv_copy_rows(kv_cache *dst, const int32_t *dst_rows, const kv_cache *src,
   cp.Hk = dst->Hk;
   cp.D = dst->D;
   cp.n_items = 0;
+  const std::vector<Unit> us = units(dst);  // the same for src (same layout)
   for (int i = 0; i < n; ++i) {
     if (dst == src && dst_rows[i] == src_rows[i]) continue;  // the row keeps its own slots
-    for (int l = 0; l < dst->n_layers; ++l) {
+    for (const Unit &u : us) {
       CopyItem it;
       __nv_bfloat16 *sk, *sv;
-      row_block(src, l, src_rows[i], sk, sv, it.src_head_stride, it.src_table, it.src_pool);
+      row_block(src, u, src_rows[i], sk, sv, it.src_head_stride, it.src_table, it.src_pool);
       it.src_k = sk;
       it.src_v = sv;
-      row_block(dst, l, dst_rows[i], it.dst_k, it.dst_v, it.dst_head_stride, it.dst_table,
+      row_block(dst, u, dst_rows[i], it.dst_k, it.dst_v, it.dst_head_stride, it.dst_table,
                 it.dst_pool);
-      const bool ring = dst->kind[l] == KV_SLIDING;
-      it.p0 = first_kept(dst, l, kp[i]);
+      const bool ring = u.ring;
+      it.p0 = first_kept(dst, u, kp[i]);
       it.p1 = kp[i];
       it.src_ring = ring ? src->R : 0;
       it.dst_ring = ring ? dst->R : 0;
@@ -1510,20 +1647,22 @@ int kv_copy_rows(kv_cache *dst, const int32_t *dst_rows, const kv_cache *src,
   for (int i = 0; i < n; ++i) {
     dst->lens[dst_rows[i]] = kp[i];
     release_blocks(dst, dst_rows[i], kp[i]);  // a shortened row gives its tail back
+    for (auto &he : dst->hy_end)
+      if (!he.empty()) he[dst_rows[i]] = kp[i];  // no step in progress
   }
   return KV_OK;
 }
 
 int64_t kv_export_bytes(const kv_cache *c, int keep) {
-  if (!c || keep < 0 || keep > c->max_len || has_hybrid(c)) return -1;
+  if (!c || keep < 0 || keep > c->max_len) return -1;
   int64_t b = 0;
-  for (int l = 0; l < c->n_layers; ++l)
-    b += 2LL * c->Hk * (keep - first_kept(c, l, keep)) * c->D * 2;
+  for (const Unit &u : units(c)) b += 2LL * c->Hk * (keep - first_kept(c, u, keep)) * c->D * 2;
   return b;
 }
 
-// Flat layout, per layer in order: K [Hk][positions][D] then V [Hk][positions][D], positions
-// ascending over the ones the layer keeps at length `keep`.
+// Flat layout, per storage unit in order (a layer's own storage, then a hybrid layer's
+// ring): K [Hk][positions][D] then V [Hk][positions][D], positions ascending over the ones
+// the unit keeps at length `keep`.
 static int export_import(kv_cache *c, int row, int keep, void *buf, int64_t bytes,
                          cudaStream_t s, bool to_buf) {
   __nv_bfloat16 *b = (__nv_bfloat16 *)buf;
@@ -1532,15 +1671,15 @@ static int export_import(kv_cache *c, int row, int keep, void *buf, int64_t byte
   cp.D = c->D;
   cp.n_items = 0;
   int64_t off = 0;
-  for (int l = 0; l < c->n_layers; ++l) {
-    const int p0 = first_kept(c, l, keep), np = keep - p0;
+  for (const Unit &u : units(c)) {
+    const int p0 = first_kept(c, u, keep), np = keep - p0;
     const int64_t blk = (int64_t)c->Hk * np * c->D;
     __nv_bfloat16 *rk, *rv;
     int64_t hs;
     const int32_t *tab;
     int32_t pool;
-    row_block(c, l, row, rk, rv, hs, tab, pool);
-    const int ring = c->kind[l] == KV_SLIDING ? c->R : 0;
+    row_block(c, u, row, rk, rv, hs, tab, pool);
+    const int ring = u.ring ? c->R : 0;
     CopyItem it;
     it.p0 = p0;
     it.p1 = keep;
@@ -1604,6 +1743,8 @@ int kv_import_row(kv_cache *c, int row, int keep, const void *src, int64_t bytes
   if (set_ring_state(c, {row}, {keep}, s) != KV_OK) return KV_ERR_CUDA;
   c->lens[row] = keep;
   release_blocks(c, row, keep);
+  for (auto &he : c->hy_end)
+    if (!he.empty()) he[row] = keep;
   return KV_OK;
 }
 

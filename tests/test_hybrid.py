@@ -113,10 +113,157 @@ def test_hybrid_refusals():
         c.append_hybrid(1, q, k, k, [1, 1])             # other tokens than the full layer's
     c.append_hybrid(1, q, k, k, [1, 0])
     torch.cuda.synchronize()
-    with pytest.raises(kvi.KVError):
+    with pytest.raises(ValueError):                     # global buffers of the full layer
         c.step_graph([q] * 3, [k] * 3, [k] * 3, [q] * 3)
-    with pytest.raises(kvi.KVError):
-        c.copy_rows(c, [0], [1])
-    with pytest.raises(ValueError):
-        c.export_row(0)
     assert c.lens == [10, 3]
+
+
+def _bufs(sc, Bs):
+    import torch
+    mk = lambda H: torch.zeros((Bs, 1, H, sc.D), dtype=torch.bfloat16, device=sc.dev)
+    q = [mk(sc.Hq) for _ in sc.kinds]
+    k = [mk(sc.Hk) for _ in sc.kinds]
+    v = [mk(sc.Hk) for _ in sc.kinds]
+    o = [mk(sc.Hq) for _ in sc.kinds]
+    kg = [mk(sc.Hk) if kind == 2 else None for kind in sc.kinds]
+    vg = [mk(sc.Hk) if kind == 2 else None for kind in sc.kinds]
+    return q, k, v, o, kg, vg
+
+
+def _state(c, kinds, row):
+    """(positions, K bits, V bits) of every storage unit of a row: a layer's own storage,
+    then its hybrid ring."""
+    L, out = c.lens[row], []
+    for layer, kind in enumerate(kinds):
+        views = []
+        if kind in (0, 2):
+            views.append((c.storage(layer), False))
+        if kind == 1:
+            views.append((c.storage(layer), True))
+        if kind in (2, 3):
+            views.append((c.ring_storage(layer), True))
+        for (K, V), ring in views:
+            Kb, Vb = torch_to_bits(K)[row], torch_to_bits(V)[row]
+            pos = np.arange(max(0, L - c.R) if ring else 0, L)
+            slots = pos % c.R if ring else pos
+            out.append((pos, Kb[:, slots], Vb[:, slots]))
+    return out
+
+
+def _same(a, ra, b, rb, kinds):
+    assert a.lens[ra] == b.lens[rb]
+    for x, y in zip(_state(a, kinds, ra), _state(b, kinds, rb)):
+        for u, w in zip(x, y):
+            assert np.array_equal(u, w)
+
+
+def test_hybrid_step_graph_equals_append():
+    """Graph replays on a layout with global, sliding and hybrid layers: outputs, group
+    caches, rings, lpos and lens bit for bit equal to kv_append(_hybrid) + kv_advance."""
+    import torch
+    from harness import bf16_bits_to_torch
+    kw = dict(B=4, max_len=200, Hq=16, Hk=4, D=64, W=12, kinds=[2, 3, 0, 1, 2, 3], seed=41)
+    a, b = Scenario(**kw), Scenario(**kw)
+    for sc in (a, b):
+        sc.step([30, 3, 17, 0], C=30, check=False)
+    rows = [3, 0, 2]
+    q, k, v, o, kg, vg = _bufs(b, len(rows))
+    g = b.cache.step_graph(q, k, v, o, rows=rows, k_global=kg, v_global=vg)
+    ones = [1] * len(rows)
+    for _ in range(5):
+        outs_a = a.step(ones, rows, C=1)                 # checked against the oracle
+        for layer, kind in enumerate(b.kinds):
+            qq, kk, vv = b.chunk_inputs(layer, rows, ones, 1)
+            for dst, src in ((q, qq), (k, kk), (v, vv)):
+                dst[layer].copy_(bf16_bits_to_torch(src, b.dev))
+            if kind == 2:
+                gk, gvv = b.global_inputs(layer, rows, ones, 1)
+                kg[layer].copy_(bf16_bits_to_torch(gk, b.dev))
+                vg[layer].copy_(bf16_bits_to_torch(gvv, b.dev))
+        g.launch()
+        torch.cuda.synchronize()
+        for r in rows:
+            b.lens[r] += 1
+        for layer in range(len(b.kinds)):
+            assert np.array_equal(torch_to_bits(outs_a[layer][1]), torch_to_bits(o[layer]))
+    for r in range(4):
+        _same(a.cache, r, b.cache, r, b.kinds)
+    assert np.array_equal(a.cache.lpos().cpu().numpy(), b.cache.lpos().cpu().numpy())
+    b.check_state()
+    # a local layer may follow its full layer again after the graph's steps
+    b.step([2, 1], rows=[0, 1], C=2, check_state=True)
+    g.close()
+
+
+def test_hybrid_copies_and_export_import():
+    """Fork rows whose rings have wrapped, truncate an unwrapped row, move a row to another
+    cache through export / import: states equal position by position, and rows sharing a
+    state decode identically."""
+    import torch
+    kinds = [2, 3, 1, 2]
+    kw = dict(B=5, max_len=160, Hq=8, Hk=2, D=64, W=10, kinds=kinds, seed=43)
+    sc = Scenario(**kw)
+    sc.step([37, 8, 0, 64, 5], C=64, check_state=True)
+    c = sc.cache
+    c.copy_rows(c, src_rows=[0, 0], dst_rows=[2, 4])      # whole rows (rings wrapped)
+    c.copy_rows(c, src_rows=[1], dst_rows=[1], keep=[6])   # truncation of an unwrapped row
+    assert c.lens == [37, 6, 37, 64, 37]
+    for d in (2, 4):
+        _same(c, 0, c, d, kinds)
+    other = Scenario(**dict(kw, B=2, max_len=200)).cache
+    buf = c.export_row(3)
+    other.import_row(1, buf, keep=64)
+    _same(c, 3, other, 1, kinds)
+    # identical inputs -> identical outputs for rows 0, 2, 4
+    gen = torch.Generator().manual_seed(0)
+    for _ in range(3):
+        outs = []
+        for layer, kind in enumerate(kinds):
+            mk = lambda H: torch.randn((1, 1, H, 64), generator=gen).to(torch.bfloat16).expand(
+                3, -1, -1, -1).contiguous().cuda()
+            q, kl, vl = mk(8), mk(2), mk(2)
+            kg, vg = (mk(2), mk(2)) if kind == 2 else (None, None)
+            if kind in (2, 3):
+                o = c.append_hybrid(layer, q, kl, vl, [1, 1, 1], k_global=kg, v_global=vg,
+                                    rows=[0, 2, 4])
+            else:
+                o = c.append(layer, q, kl, vl, [1, 1, 1], rows=[0, 2, 4])
+            outs.append(torch_to_bits(o))
+        c.advance([1, 1, 1], rows=[0, 2, 4])
+        torch.cuda.synchronize()
+        for x in outs:
+            assert np.array_equal(x[0], x[1]) and np.array_equal(x[0], x[2])
+    for d in (2, 4):
+        _same(c, 0, c, d, kinds)
+
+
+def test_hybrid_host_buffers_equal_device():
+    """kv_append_hybrid_host (pinned and pageable buffers) gives the device path's bits."""
+    import torch
+    kinds = [2, 3]
+    kw = dict(B=3, max_len=120, Hq=8, Hk=2, D=64, W=16, kinds=kinds, seed=44)
+    a, b = Scenario(**kw), Scenario(**kw)
+    for sc in (a, b):
+        sc.step([20, 5, 40], C=40, check=False)
+    gen = torch.Generator().manual_seed(1)
+    for it, (n, C) in enumerate((([1, 1, 1], 1), ([9, 0, 30], 30), ([1, 2, 1], 2))):
+        pin = it % 2 == 0
+        for layer, kind in enumerate(kinds):
+            mk = lambda H: torch.randn((3, C, H, 64), generator=gen).to(torch.bfloat16)
+            q, kl, vl = mk(8), mk(2), mk(2)
+            kg, vg = (mk(2), mk(2)) if kind == 2 else (None, None)
+            dev = lambda x: None if x is None else x.cuda()
+            od = a.cache.append_hybrid(layer, dev(q), dev(kl), dev(vl), n, k_global=dev(kg),
+                                       v_global=dev(vg))
+            hp = (lambda x: None if x is None else x.pin_memory()) if pin else (lambda x: x)
+            oh = torch.empty_like(q).pin_memory() if pin else torch.empty_like(q)
+            b.cache.append_hybrid_host(layer, hp(q), hp(kl), hp(vl), n, k_global=hp(kg),
+                                       v_global=hp(vg), out=oh)
+            torch.cuda.synchronize()
+            for i, m in enumerate(n):
+                assert np.array_equal(torch_to_bits(od)[i, :m], torch_to_bits(oh)[i, :m])
+        for sc in (a, b):
+            sc.cache.advance(n)
+    torch.cuda.synchronize()
+    for r in range(3):
+        _same(a.cache, r, b.cache, r, kinds)
