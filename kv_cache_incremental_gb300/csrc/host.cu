@@ -85,6 +85,10 @@ constexpr int kTcMinRows = 64;
 // Key splits of chunked prefill: at most this many per row, of at least this many
 // 128-key blocks each.
 constexpr int kMaxPrefillSplits = 16;
+// Decode splits hold at least this many 64-key tiles: a shorter row is one CTA with no
+// split merge, which is what small (ring) layers want (4 measured 10% slower on the
+// long-context step: more prologues and merges for the same keys).
+constexpr int kMinDecodeSplitTiles = 8;
 constexpr int kMinSplitBlocks = 4;
 
 }  // namespace
@@ -267,11 +271,11 @@ void plan_decode(const kv_cache *c, int layer, const std::vector<DecodeIn> &in,
     if (hybrid) nk2[i] = std::min(in[i].pos + 1, c->R);
     total_tiles += tiles_of(nk[i]) + tiles_of(nk2[i]);
   }
-  // Aim for about four waves of two CTAs per SM; splits of at least eight tiles (512 keys):
-  // a shorter row is one CTA with no split merge, which is what small (ring) layers want.
+  // Aim for about four waves of two CTAs per SM; splits of at least kMinDecodeSplitTiles
+  // tiles.
   const int64_t target = (int64_t)c->num_sms * 2 * 4;
   int64_t per = (total_tiles * c->Hk + target - 1) / target;
-  if (per < 8) per = 8;
+  if (per < kMinDecodeSplitTiles) per = kMinDecodeSplitTiles;
   // splits of one segment: at most `cap`, each a whole number of tiles
   const auto splits = [&](int keys, int cap, int &st) {
     const int tiles = tiles_of(keys);
