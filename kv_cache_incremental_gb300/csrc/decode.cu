@@ -57,7 +57,11 @@ constexpr int decode_smem_bytes() {
          16 /*flags*/;
 }
 
+// Row of work item `item`: a division when every row of the launch has the same number of
+// items (each probe of the search below is a dependent parameter load, slow at kernel
+// start), else a binary search over the rows' first items.
 __device__ __forceinline__ int find_item_row(const DecodeParams &p, int item) {
+  if (p.uniform_items > 0) return item / p.uniform_items;
   int lo = 0, hi = p.n_rows - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;

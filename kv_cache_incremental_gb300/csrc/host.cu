@@ -311,6 +311,9 @@ void plan_decode(const kv_cache *c, int layer, const std::vector<DecodeIn> &in,
   }
   p.n_rows = (int)in.size();
   p.n_items = item;
+  p.uniform_items = in.empty() ? 0 : p.rows[0].n_splits + p.rows[0].n_splits2;
+  for (size_t i = 1; i < in.size() && p.uniform_items; ++i)
+    if (p.rows[i].n_splits + p.rows[i].n_splits2 != p.uniform_items) p.uniform_items = 0;
   p.seg0_ring = sliding ? 1 : 0;
   p.ring_R = c->R > 0 ? c->R : 1;
 }

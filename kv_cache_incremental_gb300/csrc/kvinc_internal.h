@@ -147,6 +147,7 @@ struct DecodeParams {  // 64-byte aligned through its CUtensorMap members
   int ring_R;
   int Hq, Hk, rep, seg_rows;
   int n_rows, n_items;
+  int uniform_items;        // > 0: every row has exactly this many items (row = item / it)
   float scale_log2;         // log2(e) / sqrt(D)
   PageTable pt;             // paged global layer (tmap_k16 / tmap_v16 valid)
   // segment 1 of a hybrid layer: the layer's own ring and its new local key
