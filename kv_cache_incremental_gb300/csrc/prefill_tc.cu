@@ -327,14 +327,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       // query tile, buffer b & 1 (phase b >> 1).
       auto sbuf = [&](int b) { return dbl ? (b & 1) : qt; };
       auto sphase = [&](int b) -> uint32_t { return dbl ? (b >> 1) & 1 : b & 1; };
-      // QK(b): S of block b into its S buffer, once the K/V stage has landed and the PV
-      // that last read P out of that buffer (PV(b - 1), or PV(b - 2) when double-buffered)
-      // has finished.  A block with one tile still multiplies all 128 rows of its K stage;
-      // the softmax masks the absent half.
+      // QK(b): S of block b into its S buffer, once the K/V stage has landed.  The PV that
+      // last read P out of that buffer (PV(b - 1), or PV(b - 2) when double-buffered) was
+      // issued before by this thread: successive tcgen05.mma of one thread execute in issue
+      // order, so the overwrite follows its reads with no wait.  A block with one tile
+      // still multiplies all 128 rows of its K stage; the softmax masks the absent half.
       auto issue_qk = [&](int b) -> bool {
         if (!ptx::mbar_wait(&kv_full[b % kStages], (b / kStages) & 1, kWaitLimit)) return false;
-        const int prev = dbl ? b - 2 : b - 1;
-        if (prev >= 0 && !ptx::mbar_wait(&pv_done[qt], prev & 1, kWaitLimit)) return false;
         tc::fence_after();
         const uint32_t tS = tmem + sbuf(b) * kBlockKeys;
         const uint32_t k_addr = ptx::smem_u32(kv + (b % kStages) * Cfg::kStageBytes);
