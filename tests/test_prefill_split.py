@@ -44,3 +44,19 @@ def test_split_paged_and_resets():
     sc.check_state()
     sc.step([20, 3, 64, 60], C=64, resets=[1], check_state=True)
     sc.step([5, 64, 1, 2], C=64, check_state=True)
+
+
+def test_more_rows_than_one_launch():
+    """700 rows in one call: every launch kind (append, decode, prefill, ring commit,
+    state) runs in batches of at most 512 rows, on sliding, global and hybrid layers."""
+    sc = Scenario(B=700, max_len=640, Hq=4, Hk=1, D=64, W=8, kinds=[1, 0, 2, 3], seed=35)
+    sc.step([5] * 700, C=5, check_state=True)
+    sc.step([1] * 700, C=1, check_state=True)
+    rows = list(range(0, 700, 3))
+    sc.step([60] * len(rows), rows=rows, C=64, check=False)
+    for _ in range(8):
+        sc.step([64] * len(rows), rows=rows, C=64, check=False)
+    sc.check_state()
+    # a mixed step over all rows: long rows (~590 keys) among short ones
+    n = [(r * 7) % 40 + 1 for r in range(700)]
+    sc.step(n, C=40, check_state=True)
