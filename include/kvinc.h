@@ -248,6 +248,13 @@ int kv_get_config(const kv_cache *c, int *B, int *max_len, int *Hq, int *Hk, int
  * non-zero, else KV_OK. */
 int kv_device_error(kv_cache *c, int32_t *code_out);
 
+/* Failure-path check: enqueues, on `stream`, a kernel whose bounded wait on a barrier
+ * that nothing completes gives up after `limit` polls (1 <= limit <= 2^20; every kernel
+ * of the library bounds its waits the same way, with a larger limit) and records the
+ * timeout in the cache's device error word, which kv_device_error then reports.  Touches
+ * nothing else.  KV_ERR_ARG for a bad limit. */
+int kv_debug_wait_timeout(kv_cache *c, uint32_t limit, void *stream);
+
 /*
  * Kernel timing for measurement.  kv_profile_enable(c, 1) makes the library
  * record a CUDA event pair around each kernel launch it makes, on the stream

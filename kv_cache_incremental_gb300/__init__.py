@@ -317,6 +317,12 @@ class KVCache:
         return torch.as_tensor(_DevArray(lp.value, (self.B, self.R), "<i4"),
                                device=f"cuda:{self.device}")
 
+    def debug_wait_timeout(self, limit: int = 4096, stream=None) -> None:
+        """Enqueue a kernel whose bounded wait runs out (kv_debug_wait_timeout); the timeout
+        then shows in device_error()."""
+        check(_clib.kv_debug_wait_timeout(self._h, int(limit), _stream_ptr(stream, self.device)),
+              "kv_debug_wait_timeout")
+
     def device_error(self) -> int:
         code = ctypes.c_int32()
         _clib.kv_device_error(self._h, ctypes.byref(code))

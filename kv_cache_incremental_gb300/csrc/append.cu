@@ -14,6 +14,7 @@
 // ("inkling: ring-buffer KV cache for sliding-window layers", How it works:
 // the batch is read from scratch and appended after scoring).
 #include "kvinc_internal.h"
+#include "ptx.cuh"
 
 namespace kvinc {
 namespace {
@@ -205,6 +206,28 @@ cudaError_t state_node(const StateParams *p, void **args, cudaKernelNodeParams *
 cudaError_t launch_state(const StateParams &p, cudaStream_t s) {
   if (p.n_rows <= 0) return cudaSuccess;
   state_kernel<<<p.n_rows, 128, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+namespace {
+
+// The kernels' failure path with nothing else around it: a bounded wait on an mbarrier
+// that no thread or copy ever completes gives up after `limit` polls and records the
+// error in the cache's error word, as every kernel of the library does on a timed-out wait.
+__global__ void __launch_bounds__(32) wait_probe_kernel(int32_t *err, uint32_t limit) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&bar, 1);
+    ptx::fence_barrier_init();
+  }
+  __syncwarp();
+  if (threadIdx.x == 0 && !ptx::mbar_wait(&bar, 0, limit)) atomicExch(err, 1);
+}
+
+}  // namespace
+
+cudaError_t launch_wait_probe(int32_t *err, uint32_t limit, cudaStream_t s) {
+  wait_probe_kernel<<<1, 32, 0, s>>>(err, limit);
   return cudaGetLastError();
 }
 

@@ -1214,6 +1214,12 @@ int kv_device_error(kv_cache *c, int32_t *code_out) {
   return v ? KV_ERR_DEVICE : KV_OK;
 }
 
+int kv_debug_wait_timeout(kv_cache *c, uint32_t limit, void *stream) {
+  if (!c || limit < 1 || limit > (1u << 20)) return KV_ERR_ARG;
+  DeviceGuard guard(c->device);
+  return set_err(launch_wait_probe(c->err, limit, (cudaStream_t)stream));
+}
+
 int kv_profile_enable(kv_cache *c, int enable) {
   if (!c) return KV_ERR_ARG;
   if (!enable) {

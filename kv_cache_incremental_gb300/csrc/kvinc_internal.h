@@ -295,6 +295,7 @@ cudaError_t launch_prefill(const PrefillParams &p, int D, cudaStream_t s);
 cudaError_t launch_prefill_merge(const MergeParams &p, int D, cudaStream_t s);
 cudaError_t launch_commit(const CommitParams &p, cudaStream_t s);
 cudaError_t launch_state(const StateParams &p, cudaStream_t s);
+cudaError_t launch_wait_probe(int32_t *err, uint32_t limit, cudaStream_t s);
 // Opt kernels into their dynamic shared memory sizes (once per process and device).
 cudaError_t configure_kernels();
 
