@@ -20,8 +20,8 @@ namespace kvinc {
 cudaError_t configure_decode();
 cudaError_t configure_prefill();
 cudaError_t configure_prefill_tc();
-cudaError_t launch_prefill_tc(const PrefillParams &p, int D, cudaStream_t s);
-int prefill_tc_tiles(int D);
+cudaError_t launch_prefill_tc(const PrefillParams &p, int D, int tiles, cudaStream_t s);
+int prefill_tc_tiles(int D, int n_rho);
 }  // namespace kvinc
 
 using namespace kvinc;
@@ -547,24 +547,31 @@ int append_device(kv_cache *c, int layer, const __nv_bfloat16 *q, const __nv_bfl
     // chunk gives at least 64 query rows go to the tcgen05 kernel (128-row tiles);
     // smaller ones to the mma.sync kernel (16-row warp tiles).  Hybrid layers (three key
     // segments) all go to the tcgen05 kernel.
-    std::vector<PrefillRow> ents[2];
+    // launch kinds: 0 mma.sync kernel (64 query rows per CTA, two CTAs per SM), 1 tcgen05
+    // kernel with two 128-row query tiles per CTA (one CTA per SM), 2 tcgen05 kernel with
+    // one tile per CTA (two CTAs per SM)
+    constexpr int kKinds = 3;
+    const int rows_per_cta[kKinds] = {64, 256, 128}, ctas_per_sm[kKinds] = {2, 1, 2};
+    auto kind_of = [&](const PrefillRow &r) {
+      if (!hybrid && r.n * rep < kTcMinRows) return 0;
+      return prefill_tc_tiles(D, r.n * rep) == 2 ? 1 : 2;
+    };
+    std::vector<PrefillRow> ents[kKinds];
     std::vector<MergeRow> merges;
     int64_t part_vecs = 0;
-    for (int kind = 0; kind < 2; ++kind) {
+    for (int kind = 0; kind < kKinds; ++kind) {
       std::vector<PrefillRow> sel;
       for (const PrefillRow &r : prows)
-        if ((hybrid || r.n * rep >= kTcMinRows) == (kind == 1)) sel.push_back(r);
-      // the tcgen05 kernel holds one CTA per SM, the mma.sync kernel two
-      ents[kind] = split_prefill_rows(c, layer, sel, kind == 1 ? 128 * prefill_tc_tiles(D) : 64,
-                                      kind == 1 ? 1 : 2, merges, &part_vecs);
+        if (kind_of(r) == kind) sel.push_back(r);
+      ents[kind] = split_prefill_rows(c, layer, sel, rows_per_cta[kind], ctas_per_sm[kind],
+                                      merges, &part_vecs);
     }
     if (part_vecs > 0) {
       const int rc = ensure_prefill_parts(c, part_vecs, s);
       if (rc != KV_OK) return rc;
     }
-    for (int kind = 0; kind < 2; ++kind) {
+    for (int kind = 0; kind < kKinds; ++kind) {
       const std::vector<PrefillRow> &sel = ents[kind];
-      const int rows_per_cta = kind == 1 ? 128 * prefill_tc_tiles(D) : 64;
       for (size_t r0 = 0; r0 < sel.size(); r0 += kMaxRowsPerLaunch) {
         const size_t r1 = std::min(sel.size(), r0 + kMaxRowsPerLaunch);
         pp.tmap_k = c->tmK[layer];
@@ -594,13 +601,12 @@ int append_device(kv_cache *c, int layer, const __nv_bfloat16 *q, const __nv_bfl
         pp.seg_rows2 = c->R + 1;
         pp.part_o = c->ppart_o;
         pp.part_ml = c->ppart_ml;
-        pp.tc_tiles = prefill_tc_tiles(D);
         int cta = 0;
         double bytes = 0, fl = 0;
         for (size_t j = r0; j < r1; ++j) {
           PrefillRow r = sel[j];
           r.cta0 = cta;
-          cta += (r.n * rep + rows_per_cta - 1) / rows_per_cta;
+          cta += (r.n * rep + rows_per_cta[kind] - 1) / rows_per_cta[kind];
           pp.rows[j - r0] = r;
           if (r.tile0 != 0) continue;  // a row's work is counted with its first entry
           const int lkeys = std::min(r.lens, c->R) + r.n;
@@ -616,7 +622,8 @@ int append_device(kv_cache *c, int layer, const __nv_bfloat16 *q, const __nv_bfl
         pp.n_rows = (int)(r1 - r0);
         pp.n_ctas = cta;
         cudaError_t e = timed(c, KV_KERNEL_PREFILL, bytes, fl, s, [&] {
-          return kind == 1 ? launch_prefill_tc(pp, D, s) : launch_prefill(pp, D, s);
+          return kind == 0 ? launch_prefill(pp, D, s)
+                           : launch_prefill_tc(pp, D, kind == 1 ? 2 : 1, s);
         });
         if (e != cudaSuccess) return KV_ERR_CUDA;
       }

@@ -201,7 +201,6 @@ struct PrefillParams {  // 64-byte aligned through its CUtensorMap members
   CUtensorMap tmap_k2;
   CUtensorMap tmap_v2;
   int seg_rows2;
-  int tc_tiles;             // tcgen05 kernel: query tiles of 128 rows per CTA (1 or 2)
   // key splits: [vector][D] fp32 O (relative to m), [vector] (m in log2 units, l)
   float *part_o;
   float2 *part_ml;

@@ -8,10 +8,11 @@
 // chunk is committed to it ("inkling: ring-buffer KV cache for sliding-window
 // layers", How it works; Lab 07 section 3; tiny_agent/generate.py `_append_chunk`).
 //
-// One CTA owns up to two 128-row query tiles (the MMA's M) of one (row, kv head);
-// both tiles share every K/V block the CTA streams.  A block is 128 keys: two 64-key
+// One CTA owns one or two 128-row query tiles (the MMA's M) of one (row, kv head): two at
+// D = 128, sharing every K/V block the CTA streams; one at D = 64, two CTAs per SM.  A block is 128 keys: two 64-key
 // tiles, each a TMA box, a unit of the masking logic and one half of the softmax pass.
 // Warp roles:
+// Warp roles (with two tiles; with one, warps 0-3, 4 and 5):
 //   warps 0-7  softmax, four per query tile: thread i of a tile owns query row i =
 //              TMEM lane i of that tile's accumulators.  They rotate the queries into
 //              shared memory, read S from TMEM, mask, run the online softmax (lazy
@@ -37,18 +38,26 @@ namespace kvinc {
 namespace {
 
 constexpr int kRows = 128;        // query rows per tile (MMA M)
-constexpr int kTilesQ = 2;        // query tiles per CTA
 constexpr int kKeys = kTileKeys;  // keys per tile (one TMA box, one softmax half)
 constexpr int kBlockKeys = 2 * kKeys;  // keys per K/V block (MMA N of S, K of PV)
 constexpr int kSoftmaxWarps = 4;  // per query tile
-constexpr int kProducerWarp = kTilesQ * kSoftmaxWarps, kMmaWarp = kProducerWarp + 1;
-constexpr int kThreads = (kMmaWarp + kTilesQ) * 32;  // one MMA-issuing warp per query tile
 constexpr float kRescaleLog2 = 8.f;  // lazy rescale threshold (log2 units)
 
-template <int D>
+// Warp roles of a CTA with TQ query tiles: softmax warps, then the producer, then one
+// MMA-issuing warp per tile.
+template <int TQ>
+struct Roles {
+  static constexpr int kProducerWarp = TQ * kSoftmaxWarps, kMmaWarp = kProducerWarp + 1;
+  static constexpr int kThreads = (kMmaWarp + TQ) * 32;
+};
+
+// TQ = 2 (D = 128): two query tiles share every K/V block (one CTA per SM).  TQ = 1
+// (D = 64): one tile in 256 TMEM columns and two K/V stages, so that two CTAs fit on an SM.
+template <int D, int TQ>
 struct TcCfg {
+  static constexpr int kTilesQ = TQ;
   static constexpr int kPanels = D / 64;
-  static constexpr int kStages = D == 128 ? 2 : 4;
+  static constexpr int kStages = D == 128 ? 2 : TQ == 2 ? 4 : 2;
   static constexpr int kQBytes = kPanels * kRows * 128;        // one Q tile, K-major, 128B swizzle
   static constexpr int kPanelBytes = kBlockKeys * 128;         // 64 dims of one K or V block
   static constexpr int kHalfBytes = kKeys * 128;               // one 64-key TMA box of a panel
@@ -57,7 +66,7 @@ struct TcCfg {
   // TMEM: per query tile one 128-column S buffer (S fp32 of the block's two 64-key tiles;
   // then per tile P as 32 columns of bf16 pairs for the high part and 32 for the low
   // part, in the columns that held that tile's S) and one D-column O accumulator.
-  static constexpr int kTmemCols = 512;                        // [S0 S1] [O0] [O1]
+  static constexpr int kTmemCols = TQ == 2 ? 512 : 256;        // [S0 S1] [O0] [O1] or [S0] [O0]
   static constexpr int kOff_Q = 0;
   static constexpr int kOff_KV = kOff_Q + kTilesQ * kQBytes;
   static constexpr int kOff_Bar = kOff_KV + kStages * kStageBytes;
@@ -140,10 +149,12 @@ __device__ __forceinline__ float max64(const float (&v)[64]) {
   return fmax3(fmax3(a[0], a[1], a[2]), fmax3(a[3], a[4], a[5]), fmaxf(a[6], a[7]));
 }
 
-template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int D, int TQ>
+__global__ void __launch_bounds__(Roles<TQ>::kThreads, TQ == 1 ? 2 : 1)
     prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
-  using Cfg = TcCfg<D>;
+  using Cfg = TcCfg<D, TQ>;
+  constexpr int kTilesQ = TQ;
+  constexpr int kProducerWarp = Roles<TQ>::kProducerWarp, kMmaWarp = Roles<TQ>::kMmaWarp;
   constexpr int kStages = Cfg::kStages;
   constexpr int kHalf = D / 2;
   extern __shared__ uint8_t smem_raw[];
@@ -170,12 +181,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const PrefillRow &row = p.rows[find_cta_row(p, blockIdx.x)];
   const int g = blockIdx.y;
-  const int tiles_cta = p.tc_tiles;  // query tiles per CTA of this launch (1 or 2)
-  const int rho0 = (blockIdx.x - row.cta0) * kRows * tiles_cta;
+  const int rho0 = (blockIdx.x - row.cta0) * kRows * kTilesQ;
   const int n_rho = row.n * p.rep;
-  const int n_qt = min(tiles_cta, (n_rho - rho0 + kRows - 1) / kRows);  // query tiles in use
-  const int rho_last = min(n_rho, rho0 + kRows * tiles_cta) - 1;
-  const bool dbl = n_qt == 1;  // one query tile: S double-buffered (see the MMA issuers)
+  const int n_qt = min(kTilesQ, (n_rho - rho0 + kRows - 1) / kRows);  // query tiles in use
+  const int rho_last = min(n_rho, rho0 + kRows * kTilesQ) - 1;
+  // one query tile in use in a two-tile CTA: S double-buffered in the other tile's columns
+  const bool dbl = kTilesQ == 2 && n_qt == 1;
   const int t_max = rho_last / p.rep;
   const int lens = row.lens;
   const int warp = threadIdx.x >> 5;
@@ -686,31 +697,36 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-// Query tiles (of 128 rows) per CTA of the tcgen05 prefill.  Two tiles share every K/V
-// block the CTA streams; a CTA whose row has only one tile of queries double-buffers S
-// instead.  (One tile per CTA throughout measured 10-40% slower: each K/V block is then
-// streamed once per tile.)
-int prefill_tc_tiles(int) { return kTilesQ; }
+// Query tiles per CTA of the tcgen05 prefill for head dimension D.  D = 128: two tiles
+// share every K/V block (a CTA whose row fills one tile double-buffers S instead).  D = 64:
+// one tile per CTA, two CTAs per SM (two independent chains per SM; each K/V block is
+// streamed once per tile).  Measured on the continuous-batch mix (D = 64): 2.49 M tokens/s
+// with one tile per CTA, 2.39 M with two; rows of one tile alone on the one-tile kernel,
+// 2.24 M.
+int prefill_tc_tiles(int D, int) { return D == 64 ? 1 : 2; }
 
-cudaError_t launch_prefill_tc(const PrefillParams &p, int D, cudaStream_t s) {
+template <int D, int TQ>
+static void launch_tc(const PrefillParams &p, cudaStream_t s) {
+  prefill_tc_kernel<D, TQ>
+      <<<dim3(p.n_ctas, p.Hk), Roles<TQ>::kThreads, TcCfg<D, TQ>::kSmem, s>>>(p);
+}
+
+cudaError_t launch_prefill_tc(const PrefillParams &p, int D, int tiles, cudaStream_t s) {
   if (p.n_ctas <= 0) return cudaSuccess;
-  if (D == 128) {
-    prefill_tc_kernel<128><<<dim3(p.n_ctas, p.Hk), kThreads, TcCfg<128>::kSmem, s>>>(p);
-  } else if (D == 64) {
-    prefill_tc_kernel<64><<<dim3(p.n_ctas, p.Hk), kThreads, TcCfg<64>::kSmem, s>>>(p);
-  } else {
-    return cudaErrorInvalidValue;
-  }
+  if (D == 128 && tiles == 2) launch_tc<128, 2>(p, s);
+  else if (D == 64 && tiles == 1) launch_tc<64, 1>(p, s);
+  else return cudaErrorInvalidValue;
   return cudaGetLastError();
 }
 
 cudaError_t configure_prefill_tc() {
-  cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<128>,
+  cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<128, 2>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       TcCfg<128>::kSmem);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(prefill_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              TcCfg<64>::kSmem);
+                                       TcCfg<128, 2>::kSmem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(prefill_tc_kernel<64, 1>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<64, 1>::kSmem);
+  return e;
 }
 
 }  // namespace kvinc
