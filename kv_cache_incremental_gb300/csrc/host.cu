@@ -80,8 +80,10 @@ struct ProfRec {
 
 constexpr size_t kMaxProfRecs = 1 << 16;
 // Chunk rows with at least this many query rows (tokens x GQA group) use the tcgen05
-// prefill kernel.
-constexpr int kTcMinRows = 64;
+// prefill kernel, the others the mma.sync kernel.  At D = 64 the one-tile tcgen05 kernel
+// (two CTAs per SM) takes every row: the continuous-batch mix ran 2.78 M tokens/s that way
+// against 2.48 M with rows under 64 query rows on the mma.sync kernel.
+int tc_min_rows(int D) { return D == 64 ? 1 : 64; }
 // Key splits of chunked prefill: at most this many per row, of at least this many
 // 128-key blocks each.
 constexpr int kMaxPrefillSplits = 16;
@@ -553,7 +555,7 @@ int append_device(kv_cache *c, int layer, const __nv_bfloat16 *q, const __nv_bfl
     constexpr int kKinds = 3;
     const int rows_per_cta[kKinds] = {64, 256, 128}, ctas_per_sm[kKinds] = {2, 1, 2};
     auto kind_of = [&](const PrefillRow &r) {
-      if (!hybrid && r.n * rep < kTcMinRows) return 0;
+      if (!hybrid && r.n * rep < tc_min_rows(D)) return 0;
       return prefill_tc_tiles(D, r.n * rep) == 2 ? 1 : 2;
     };
     std::vector<PrefillRow> ents[kKinds];
