@@ -84,14 +84,13 @@ constexpr size_t kMaxProfRecs = 1 << 16;
 // (two CTAs per SM) takes every row: the continuous-batch mix ran 2.78 M tokens/s that way
 // against 2.48 M with rows under 64 query rows on the mma.sync kernel.
 int tc_min_rows(int D) { return D == 64 ? 1 : 64; }
-// Key splits of chunked prefill: at most this many per row, of at least this many
+// Key splits of chunked prefill: at most kMaxPrefillSplits per row, of at least this many
 // 128-key blocks each.
-constexpr int kMaxPrefillSplits = 16;
+constexpr int kMinSplitBlocks = 4;
 // Decode splits hold at least this many 64-key tiles: a shorter row is one CTA with no
 // split merge, which is what small (ring) layers want (4 measured 10% slower on the
 // long-context step: more prologues and merges for the same keys).
 constexpr int kMinDecodeSplitTiles = 8;
-constexpr int kMinSplitBlocks = 4;
 
 }  // namespace
 

@@ -210,6 +210,10 @@ struct PrefillParams {  // 64-byte aligned through its CUtensorMap members
 // Merge of a prefill row's key splits: out = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s
 // (M = max_s m_s) for every (kv head, query row) vector; split s of the row starts at
 // part + s * Hk * n_rho.
+// At most this many key splits per prefill row (the merge holds all of a row's partials of
+// one vector in registers).
+constexpr int kMaxPrefillSplits = 16;
+
 struct MergeRow {
   int32_t call_row;
   int32_t n_rho;     // query rows per kv head (tokens x GQA group)

@@ -400,6 +400,8 @@ constexpr int kMergeWarps = 8;
 
 // One warp per (row, kv head, query row) vector: the log-sum-exp merge of the row's key
 // splits (a split in which the query row sees no key has m = -inf and weighs nothing).
+// Every split's (m, l) and then every split's slice of O are loaded before any is used, so
+// a vector costs two memory round trips whatever its split count.
 template <int D>
 __global__ void __launch_bounds__(kMergeWarps * 32)
     prefill_merge_kernel(const __grid_constant__ MergeParams p) {
@@ -411,28 +413,42 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
   const int local = v - row.vec0;  // g * n_rho + rho
   const int g = local / row.n_rho, rho = local % row.n_rho;
   const int64_t stride = (int64_t)p.Hk * row.n_rho;
+  const int ns = row.n_splits;
+  float2 ml[kMaxPrefillSplits];
+#pragma unroll
+  for (int sp = 0; sp < kMaxPrefillSplits; ++sp)
+    ml[sp] = sp < ns ? p.part_ml[row.part + sp * stride + local] : make_float2(-INFINITY, 0.f);
+  float o[kMaxPrefillSplits][kPer];
+#pragma unroll
+  for (int sp = 0; sp < kMaxPrefillSplits; ++sp) {
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) o[sp][i] = 0.f;
+    if (sp < ns) {
+      const float *po = p.part_o + (row.part + sp * stride + local) * D + kPer * lane;
+      if (kPer == 4) {
+        const float4 x = *reinterpret_cast<const float4 *>(po);
+        o[sp][0] = x.x;
+        o[sp][1] = x.y;
+        o[sp][2 % kPer] = x.z;
+        o[sp][3 % kPer] = x.w;
+      } else {
+        const float2 x = *reinterpret_cast<const float2 *>(po);
+        o[sp][0] = x.x;
+        o[sp][1] = x.y;
+      }
+    }
+  }
   float m_max = -INFINITY;
-  for (int sp = 0; sp < row.n_splits; ++sp)
-    m_max = fmaxf(m_max, p.part_ml[row.part + sp * stride + local].x);
+#pragma unroll
+  for (int sp = 0; sp < kMaxPrefillSplits; ++sp) m_max = fmaxf(m_max, ml[sp].x);
   float acc[kPer] = {};
   float l = 0.f;
-  for (int sp = 0; sp < row.n_splits; ++sp) {
-    const int64_t vec = row.part + sp * stride + local;
-    const float2 ml = p.part_ml[vec];
-    const float w = ml.x == -INFINITY ? 0.f : exp2f(ml.x - m_max);
-    l += w * ml.y;
-    const float *po = p.part_o + vec * D + kPer * lane;
-    if (kPer == 4) {
-      const float4 x = *reinterpret_cast<const float4 *>(po);
-      acc[0] += w * x.x;
-      acc[1] += w * x.y;
-      acc[2 % kPer] += w * x.z;
-      acc[3 % kPer] += w * x.w;
-    } else {
-      const float2 x = *reinterpret_cast<const float2 *>(po);
-      acc[0] += w * x.x;
-      acc[1] += w * x.y;
-    }
+#pragma unroll
+  for (int sp = 0; sp < kMaxPrefillSplits; ++sp) {
+    const float w = ml[sp].x == -INFINITY ? 0.f : exp2f(ml[sp].x - m_max);
+    l += w * ml[sp].y;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) acc[i] += w * o[sp][i];
   }
   const float inv = l > 0.f ? 1.f / l : 0.f;
   const int t = rho / p.rep, h = rho % p.rep;
