@@ -283,15 +283,18 @@ def reduce_over_ranks(times, units, device):
 
 def oracle_sample(cfg, lens, seed, budget_s=20.0, max_rows=None):
     """Time the CPU oracle on whole rows of one decode step of the same workload (first
-    layer kind), until about `budget_s` of oracle time has been spent.  Returns
-    (GB/s-equivalent, tokens/s, rows, threads, seconds)."""
+    layer kind), until about `budget_s` of oracle time has been spent or three times that
+    in wall time (regenerating a row's history costs more than the oracle on it).  Returns
+    (GB/s-equivalent, tokens/s, rows, threads, seconds of oracle time)."""
     import oracle
     import synth
     Hq, Hk, D, W = cfg["Hq"], cfg["Hk"], cfg["D"], cfg["W"]
     kind = cfg["kinds"][0]
     spent, rows, byts = 0.0, 0, 0.0
+    wall0 = time.perf_counter()
     for b in range(cfg["B"]):
-        if spent >= budget_s or (max_rows and rows >= max_rows):
+        if spent >= budget_s or (max_rows and rows >= max_rows) or \
+                (rows and time.perf_counter() - wall0 >= 3 * budget_s):
             break
         p = int(lens[b])
         lo = max(0, p - W + 1) if kind == 1 else 0
@@ -729,7 +732,8 @@ def run_ours(args):
                                 "tokens_per_s": tps,
                                 "sample": f"{nr} row-decodes of one step of the workload (all "
                                           f"{Hq} heads over each row's whole history), "
-                                          f"{t:.1f} s of oracle time"}
+                                          f"{t:.1f} s of oracle time (at most 45 s of wall "
+                                          f"time with the inputs' generation)"}
     print(json.dumps(line), flush=True)
 
 
@@ -777,14 +781,16 @@ def cont_inputs(cfg, steps, seed, dev, stream):
 
 def cont_oracle_sample(cfg, steps, seed, budget_s):
     """The oracle on whole rows (all layers, all of a row's new tokens) of the mix's first
-    steps until about budget_s of oracle time; returns (tokens/s, tokens, threads, seconds)."""
+    steps until about budget_s of oracle time, or three times that in wall time; returns
+    (tokens/s, tokens, threads, seconds of oracle time)."""
     import oracle
     import synth
     Hq, Hk, D, W = cfg["Hq"], cfg["Hk"], cfg["D"], cfg["W"]
     spent, tokens = 0.0, 0
+    wall0 = time.perf_counter()
     for _, n, lens in steps:
         for b in (int(x) for x in np.nonzero(n > 0)[0]):
-            if spent >= budget_s:
+            if spent >= budget_s or (tokens and time.perf_counter() - wall0 >= 3 * budget_s):
                 break
             L, m = int(lens[b]), int(n[b])
             for layer, kind in enumerate(cfg["kinds"]):
@@ -797,7 +803,7 @@ def cont_oracle_sample(cfg, steps, seed, budget_s):
                 oracle.attend(q, range(L, L + m), kh, vh, lo, Hq, Hk, W=W if kind == 1 else 0)
                 spent += time.perf_counter() - t0
             tokens += m
-        if spent >= budget_s:
+        if spent >= budget_s or (tokens and time.perf_counter() - wall0 >= 3 * budget_s):
             break
     return tokens / spent, tokens, oracle.num_threads(), spent
 
