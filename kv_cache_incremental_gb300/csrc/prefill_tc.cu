@@ -7,11 +7,15 @@
 // lens) and of the chunk scratch (sliding layers), reading the ring before this
 // chunk is committed to it ("inkling: ring-buffer KV cache for sliding-window
 // layers", How it works; Lab 07 section 3; tiny_agent/generate.py `_append_chunk`).
+// A hybrid layer's keys are three segments in one softmax: its group's global cache,
+// its own ring, the chunk's local keys.  A launch entry may cover a range of the key
+// tiles only (a key split): it then writes its unnormalised partials for the merge
+// instead of the output.
 //
-// One CTA owns one or two 128-row query tiles (the MMA's M) of one (row, kv head): two at
-// D = 128, sharing every K/V block the CTA streams; one at D = 64, two CTAs per SM.  A block is 128 keys: two 64-key
-// tiles, each a TMA box, a unit of the masking logic and one half of the softmax pass.
-// Warp roles:
+// One CTA owns one or two 128-row query tiles (the MMA's M) of one (row, kv head): two
+// at D = 128, sharing every K/V block the CTA streams; one at D = 64, two CTAs per SM.
+// A block is 128 keys: two 64-key tiles, each a TMA box, a unit of the masking logic and
+// one half of the softmax pass.
 // Warp roles (with two tiles; with one, warps 0-3, 4 and 5):
 //   warps 0-7  softmax, four per query tile: thread i of a tile owns query row i =
 //              TMEM lane i of that tile's accumulators.  They rotate the queries into
@@ -24,11 +28,12 @@
 //              block: S = Q K^T (M=128, N=128) into the tile's S buffer, then, once the
 //              softmax wrote P of each 64-key tile, O += P_hi V + P_lo V (M=128, N=D)
 //              with P read from TMEM and V read in place as an MN-major operand (keys are
-//              its K).  QK(b+1) waits for PV(b) to finish reading P from the S buffer it
-//              overwrites; the two query tiles' chains run independently.  A CTA with a
-//              single query tile in use double-buffers S in the other tile's columns
-//              instead: QK(b+1) then waits only for PV(b-1), so it runs during the
-//              softmax of block b.
+//              its K).  QK(b+1) is issued right after PV(b), which reads P from the S
+//              buffer it overwrites: successive tcgen05.mma of one thread execute in
+//              issue order.  The two query tiles' chains run independently.  A two-tile
+//              CTA with a single query tile in use double-buffers S in the other tile's
+//              columns, so QK(b+1) is issued before PV(b) and runs during the softmax of
+//              block b.
 // Every mbarrier wait is bounded; on a timeout the CTA records the error, lets its
 // own TMA loads and MMAs finish (bounded), frees its TMEM and returns.
 #include "kvinc_internal.h"
