@@ -242,7 +242,9 @@ int oracle_attend(const uint16_t *q, const int32_t *qpos, int n_q,
  * of a group scores its query against two key sets in ONE softmax -- the group's global
  * keys (written by the group's full layer) at every position j <= p, and the layer's own
  * local keys at the positions of its window (j <= p and p - j < W) -- and sums both sets'
- * values with those weights.  `s = cat([q Kg^T, q Kl^T])`, one softmax, `y = p_g Vg + p_l Vl`.
+ * values with those weights: the two score vectors form one vector over which a single
+ * max-subtracted softmax is taken, and the output is the weighted sum of the global values
+ * plus the weighted sum of the local values.
  *
  *   q            [n_q][Hq][D] bf16 bits, pre-RoPE
  *   qpos         [n_q]
