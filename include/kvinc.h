@@ -256,6 +256,49 @@ int kv_device_error(kv_cache *c, int32_t *code_out);
 int kv_debug_wait_timeout(kv_cache *c, uint32_t limit, void *stream);
 
 /*
+ * Host-only schedules, for inspection and tests: the work split that kv_append plans for
+ * one call on a layer, computed from the shapes alone -- no cache, no CUDA call, no
+ * device work, so they run without a GPU.  Shape arguments as at kv_cache_create, plus
+ * num_sms (the device's SM count, which a cache reads from its device), R (the ring
+ * slots of a sliding or hybrid layer, min(W, max_len); ignored when kind = KV_GLOBAL)
+ * and kind (the layer's kv_layer_kind).  Both write nothing and return KV_ERR_ARG for
+ * a shape kv_cache_create refuses, a NULL array that is needed, or inputs out of range.
+ *
+ * kv_plan_decode: the split-K schedule of one decode launch, n_rows <= 512 single-token
+ * rows at positions pos[] (host, each < 2^20; a row's pos is its lens).  A row's keys
+ * are one or two segments: segment 0 the layer storage -- keys 0..pos of a global
+ * layer's cache or of a hybrid layer's group cache, or the min(pos + 1, R) ring slots of
+ * a sliding layer -- and, on a hybrid layer, segment 1 its own ring (min(pos + 1, R)
+ * slots).  Each segment is cut into splits of whole 64-key tiles.  Per row (host arrays
+ * of n_rows): n_splits / split_tiles -- segment 0's splits and the tiles of each (the
+ * last split takes the rest); n_splits2 / split_tiles2 -- the same for segment 1 (0 off
+ * hybrid layers); part0 -- the first of the row's n_splits + n_splits2 partial slots,
+ * -1 for a row with one split in all (no merge).  *n_items: the launch's CTAs per kv
+ * head, the sum of every row's splits.
+ *
+ * kv_plan_prefill: the prefill launches of one sub-chunk of n_rows chunk rows, row i
+ * with n[i] (1..64) new tokens after lens[i] cached ones (host arrays; lens + n <= 2^20).
+ * Entries (host arrays of `capacity`, in launch order): entry_row -- the input row;
+ * entry_kind -- 0 the mma.sync kernel (64 query rows per CTA), 1 the tcgen05 kernel
+ * with two 128-row query tiles per CTA, 2 the tcgen05 kernel with one; tile0, tile1 --
+ * the 64-key tiles [tile0, tile1) of the row's key space the entry reads (INT32_MAX:
+ * to the end); part -- the first partial vector a key split writes, -1 for a row in one
+ * entry.  A row's key space runs over its storage segments in order (a global layer:
+ * cache keys 0..lens+n-1; a sliding layer: its ring keys, then the chunk; a hybrid
+ * layer: the group cache, its ring, then the chunk).  *n_entries: the entries; if that
+ * is above capacity the call returns KV_ERR_ARG and writes nothing else.  n_splits[i]:
+ * the entries of row i; *part_vecs: the partial vectors of the sub-chunk
+ * (Hk * n * Hq / Hk per split of a split row).
+ */
+int kv_plan_decode(int num_sms, int Hq, int Hk, int D, int R, int kind, int n_rows,
+                   const int32_t *pos, int32_t *n_splits, int32_t *split_tiles,
+                   int32_t *n_splits2, int32_t *split_tiles2, int32_t *part0, int32_t *n_items);
+int kv_plan_prefill(int num_sms, int Hq, int Hk, int D, int R, int kind, int n_rows,
+                    const int32_t *lens, const int32_t *n, int capacity, int32_t *entry_row,
+                    int32_t *entry_kind, int32_t *tile0, int32_t *tile1, int32_t *part,
+                    int32_t *n_entries, int32_t *n_splits, int64_t *part_vecs);
+
+/*
  * Kernel timing for measurement.  kv_profile_enable(c, 1) makes the library
  * record a CUDA event pair around each kernel launch it makes, on the stream
  * of the launch; kv_profile_read sums, per kernel kind, the launches, the

@@ -20,7 +20,8 @@ from ._lib import (KERNELS, KV_GLOBAL, KV_HYBRID_FULL, KV_HYBRID_LOCAL, KV_SLIDI
                    KVError, KVPoolExhausted, check, load)
 
 __all__ = ["KVCache", "StepGraph", "KVError", "KVCacheFull", "KVPoolExhausted", "KV_GLOBAL",
-           "KV_SLIDING", "KV_HYBRID_FULL", "KV_HYBRID_LOCAL", "load"]
+           "KV_SLIDING", "KV_HYBRID_FULL", "KV_HYBRID_LOCAL", "load", "plan_decode",
+           "plan_prefill"]
 
 _clib = load()
 
@@ -450,3 +451,41 @@ class StepBuffers:
 
     def __init__(self, ptrs, tensors):
         self.ptrs, self.tensors = ptrs, tensors
+
+
+def plan_decode(num_sms: int, Hq: int, Hk: int, D: int, R: int, kind: int, pos) -> dict:
+    """The split-K schedule of one decode launch (kv_plan_decode): per row the splits and
+    64-key tiles per split of its storage segment and of a hybrid layer's ring, its first
+    partial slot (-1: one split, no merge), and the launch's CTAs per kv head.  Host only."""
+    n = len(pos)
+    outs = [(ctypes.c_int32 * max(1, n))() for _ in range(5)]
+    items = ctypes.c_int32()
+    check(_clib.kv_plan_decode(num_sms, Hq, Hk, D, R, kind, n, _i32_array(pos), *outs,
+                               ctypes.byref(items)), "kv_plan_decode")
+    names = ("n_splits", "split_tiles", "n_splits2", "split_tiles2", "part0")
+    plan = {k: list(a)[:n] for k, a in zip(names, outs)}
+    plan["n_items"] = items.value
+    return plan
+
+
+def plan_prefill(num_sms: int, Hq: int, Hk: int, D: int, R: int, kind: int, lens, n) -> dict:
+    """The prefill launches of one sub-chunk (kv_plan_prefill): the entries in launch order
+    (input row, kernel kind, 64-key tile range, first partial vector or -1), the entries
+    per row and the partial vectors.  Host only."""
+    rows = len(lens)
+    if len(n) != rows:
+        raise ValueError("lens and n differ in length")
+    count, vecs = ctypes.c_int32(), ctypes.c_int64()
+    splits = (ctypes.c_int32 * max(1, rows))()
+    args = (num_sms, Hq, Hk, D, R, kind, rows, _i32_array(lens), _i32_array(n))
+    _clib.kv_plan_prefill(*args, 0, None, None, None, None, None, ctypes.byref(count), splits,
+                          ctypes.byref(vecs))
+    cap = count.value
+    ents = [(ctypes.c_int32 * max(1, cap))() for _ in range(5)]
+    check(_clib.kv_plan_prefill(*args, cap, *ents, ctypes.byref(count), splits,
+                                ctypes.byref(vecs)), "kv_plan_prefill")
+    names = ("row", "kind", "tile0", "tile1", "part")
+    plan = {k: list(a)[:cap] for k, a in zip(names, ents)}
+    plan["n_splits"] = list(splits)[:rows]
+    plan["part_vecs"] = vecs.value
+    return plan

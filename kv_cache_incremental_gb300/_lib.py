@@ -49,6 +49,9 @@ SIGNATURES = {
     "kv_get_config": (c_int, [c_void_p] + [ctypes.POINTER(c_int)] * 8),
     "kv_device_error": (c_int, [c_void_p, P_i32]),
     "kv_debug_wait_timeout": (c_int, [c_void_p, ctypes.c_uint32, c_void_p]),
+    "kv_plan_decode": (c_int, [c_int] * 7 + [P_i32] * 6 + [P_i32]),
+    "kv_plan_prefill": (c_int, [c_int] * 7 + [P_i32, P_i32, c_int] + [P_i32] * 7
+                        + [ctypes.POINTER(c_int64)]),
     "kv_profile_enable": (c_int, [c_void_p, c_int]),
     "kv_profile_read": (c_int, [c_void_p, c_int, c_int, ctypes.POINTER(c_int64),
                                 ctypes.POINTER(c_double), ctypes.POINTER(c_double),

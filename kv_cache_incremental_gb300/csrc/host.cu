@@ -11,6 +11,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <memory>
 #include <vector>
 
 #include "../../include/kvinc.h"
@@ -86,12 +87,14 @@ constexpr size_t kMaxProfRecs = 1 << 16;
 // tiles, one CTA per SM) the mma.sync kernel stays faster for those rows: 2-7-token chunks
 // against 8k cached keys, 64 rows, Hq = 64, Hk = 8: 38.1 vs 39.4 ms of prefill over 30 steps.
 int tc_min_rows(int D) { return D == 64 ? 1 : 64; }
-// Key splits of chunked prefill: at most kMaxPrefillSplits per row, of at least this many
-// 128-key blocks each.
+// Key splits of chunked prefill: at most kMaxPrefillSplits per row, and at most one per
+// kMinSplitBlocks 128-key blocks (rounded up), so a row of up to that many blocks is never
+// split.
 constexpr int kMinSplitBlocks = 4;
-// Decode splits hold at least this many 64-key tiles: a shorter row is one CTA with no
-// split merge, which is what small (ring) layers want (4 measured 10% slower on the
-// long-context step: more prologues and merges for the same keys).
+// Decode splits: at most one per kMinDecodeSplitTiles 64-key tiles of a segment (rounded
+// up), so a row of up to that many tiles is one CTA with no split merge, which is what
+// small (ring) layers want (4 measured 10% slower on the long-context step: more
+// prologues and merges for the same keys).
 constexpr int kMinDecodeSplitTiles = 8;
 
 }  // namespace
@@ -260,24 +263,34 @@ struct DecodeIn {
   int cache_row, call_row, pos;
 };
 
+// What the split planners read of a layer: the device's SM count and the layer's shape
+// (R: the ring slots of a sliding or hybrid layer).
+struct Geom {
+  int num_sms, Hq, Hk, D, R, kind;
+};
+
+Geom geom_of(const kv_cache *c, int layer) {
+  return {c->num_sms, c->Hq, c->Hk, c->D, c->R, c->kind[layer]};
+}
+
 // Split-K schedule for one batch of decode rows (<= kMaxRowsPerLaunch).  Segment 0 holds
 // storage slots [0, nk) of the layer storage (the ring of a sliding layer, else a cache);
 // a hybrid layer adds segment 1, its own ring, with its own splits.
-void plan_decode(const kv_cache *c, int layer, const std::vector<DecodeIn> &in,
-                 DecodeParams &p, double &kv_bytes, double &flops) {
-  const bool sliding = c->kind[layer] == KV_SLIDING, hybrid = is_hybrid(c->kind[layer]);
+void plan_decode(const Geom &g, const std::vector<DecodeIn> &in, DecodeParams &p,
+                 double &kv_bytes, double &flops) {
+  const bool sliding = g.kind == KV_SLIDING, hybrid = is_hybrid(g.kind);
   const auto tiles_of = [](int keys) { return (keys + kTileKeys - 1) / kTileKeys; };
   int64_t total_tiles = 0;
   std::vector<int> nk(in.size()), nk2(in.size(), 0);
   for (size_t i = 0; i < in.size(); ++i) {
-    nk[i] = sliding ? std::min(in[i].pos + 1, c->R) : in[i].pos + 1;
-    if (hybrid) nk2[i] = std::min(in[i].pos + 1, c->R);
+    nk[i] = sliding ? std::min(in[i].pos + 1, g.R) : in[i].pos + 1;
+    if (hybrid) nk2[i] = std::min(in[i].pos + 1, g.R);
     total_tiles += tiles_of(nk[i]) + tiles_of(nk2[i]);
   }
-  // Aim for about four waves of two CTAs per SM; splits of at least kMinDecodeSplitTiles
-  // tiles.
-  const int64_t target = (int64_t)c->num_sms * 2 * 4;
-  int64_t per = (total_tiles * c->Hk + target - 1) / target;
+  // Aim for about four waves of two CTAs per SM: `per` tiles per split, at least
+  // kMinDecodeSplitTiles.
+  const int64_t target = (int64_t)g.num_sms * 2 * 4;
+  int64_t per = (total_tiles * g.Hk + target - 1) / target;
   if (per < kMinDecodeSplitTiles) per = kMinDecodeSplitTiles;
   // splits of one segment: at most `cap`, each a whole number of tiles
   const auto splits = [&](int keys, int cap, int &st) {
@@ -309,8 +322,8 @@ void plan_decode(const kv_cache *c, int layer, const std::vector<DecodeIn> &in,
     r.part0 = (uint16_t)(total > 1 ? part : 0);
     if (total > 1) part += total;
     item += total;
-    kv_bytes += 2.0 * (nk[i] + nk2[i]) * c->Hk * c->D * 2.0;
-    flops += 4.0 * (nk[i] + nk2[i]) * c->Hq * c->D;
+    kv_bytes += 2.0 * (nk[i] + nk2[i]) * g.Hk * g.D * 2.0;
+    flops += 4.0 * (nk[i] + nk2[i]) * g.Hq * g.D;
   }
   p.n_rows = (int)in.size();
   p.n_items = item;
@@ -318,7 +331,7 @@ void plan_decode(const kv_cache *c, int layer, const std::vector<DecodeIn> &in,
   for (size_t i = 1; i < in.size() && p.uniform_items; ++i)
     if (p.rows[i].n_splits + p.rows[i].n_splits2 != p.uniform_items) p.uniform_items = 0;
   p.seg0_ring = sliding ? 1 : 0;
-  p.ring_R = c->R > 0 ? c->R : 1;
+  p.ring_R = g.R > 0 ? g.R : 1;
 }
 
 // Parameters of one decode launch (fused RoPE + append + split-K attention + merge) for a
@@ -366,7 +379,7 @@ void fill_decode(const kv_cache *c, int layer, const __nv_bfloat16 *q, const __n
   dp.cache_v2 = (__nv_bfloat16 *)c->RV[layer];
   dp.seg_rows2 = c->R + 1;
   double kvb = 0;
-  plan_decode(c, layer, batch, dp, kvb, flops);
+  plan_decode(geom_of(c, layer), batch, dp, kvb, flops);
   // q, k, v in (and a hybrid layer's local k, v); new K and V and the output out
   bytes = kvb + (double)batch.size() * (c->Hq + (hybrid ? 4 : 2) * c->Hk) * c->D * 2.0 * 2.0;
 }
@@ -377,16 +390,15 @@ void fill_decode(const kv_cache *c, int layer, const __nv_bfloat16 *q, const __n
 // than `per` blocks (about two waves' worth of work per CTA) are cut into key splits,
 // each an entry that writes partials at part (vectors counted in *part_vecs), merged
 // afterwards by the rows appended to `merges`.
-std::vector<PrefillRow> split_prefill_rows(const kv_cache *c, int layer,
-                                           const std::vector<PrefillRow> &sel, int rows_per_cta,
-                                           int ctas_per_sm, std::vector<MergeRow> &merges,
-                                           int64_t *part_vecs) {
-  const bool sliding = c->kind[layer] == KV_SLIDING, hybrid = is_hybrid(c->kind[layer]);
-  const int rep = c->Hq / c->Hk;
+std::vector<PrefillRow> split_prefill_rows(const Geom &g, const std::vector<PrefillRow> &sel,
+                                           int rows_per_cta, int ctas_per_sm,
+                                           std::vector<MergeRow> &merges, int64_t *part_vecs) {
+  const bool sliding = g.kind == KV_SLIDING, hybrid = is_hybrid(g.kind);
+  const int rep = g.Hq / g.Hk;
   const auto tiles = [](int keys) { return (keys + kTileKeys - 1) / kTileKeys; };
   // the kernels' tile count for a row's last token (t_max = n - 1)
   const auto blocks_of = [&](const PrefillRow &r) {
-    const int lr = std::min(r.lens, c->R);
+    const int lr = std::min(r.lens, g.R);
     const int t = sliding ? tiles(lr) + tiles(r.n)
                           : hybrid ? tiles(r.lens + r.n) + tiles(lr) + tiles(r.n)
                                    : tiles(r.lens + r.n);
@@ -396,10 +408,10 @@ std::vector<PrefillRow> split_prefill_rows(const kv_cache *c, int layer,
   int max_blocks = 0;
   for (const PrefillRow &r : sel) {
     const int q = (r.n * rep + rows_per_cta - 1) / rows_per_cta;
-    work += (int64_t)q * c->Hk * blocks_of(r);
+    work += (int64_t)q * g.Hk * blocks_of(r);
     max_blocks = std::max(max_blocks, blocks_of(r));
   }
-  const int64_t cap = (int64_t)c->num_sms * ctas_per_sm;
+  const int64_t cap = (int64_t)g.num_sms * ctas_per_sm;
   const bool split = max_blocks > (work + cap - 1) / cap;
   const int64_t per =
       std::max<int64_t>(kMinSplitBlocks, (work + 2 * cap - 1) / (2 * cap));
@@ -418,16 +430,48 @@ std::vector<PrefillRow> split_prefill_rows(const kv_cache *c, int layer,
     ns = (blocks + bs - 1) / bs;
     const int n_rho = r.n * rep;
     const int64_t base = *part_vecs;
-    *part_vecs += (int64_t)ns * c->Hk * n_rho;
+    *part_vecs += (int64_t)ns * g.Hk * n_rho;
     for (int k = 0; k < ns; ++k) {
       r.tile0 = 2 * bs * k;
       r.tile1 = k == ns - 1 ? INT32_MAX : 2 * bs * (k + 1);
-      r.part = (int32_t)(base + (int64_t)k * c->Hk * n_rho);
+      r.part = (int32_t)(base + (int64_t)k * g.Hk * n_rho);
       out.push_back(r);
     }
     merges.push_back({r.call_row, n_rho, ns, (int32_t)base, 0});
   }
   return out;
+}
+
+// Prefill launch kinds: 0 the mma.sync kernel (64 query rows per CTA, two CTAs per SM),
+// 1 the tcgen05 kernel with two 128-row query tiles per CTA (one CTA per SM), 2 the
+// tcgen05 kernel with one tile per CTA (two CTAs per SM).
+constexpr int kPrefillKinds = 3;
+constexpr int kRowsPerCta[kPrefillKinds] = {64, 256, 128};
+constexpr int kCtasPerSm[kPrefillKinds] = {2, 1, 2};
+
+// Rows whose GQA group x chunk gives at least tc_min_rows(D) query rows go to the tcgen05
+// kernel, smaller ones to the mma.sync kernel; hybrid layers (three key segments) all go
+// to the tcgen05 kernel.
+int prefill_kind(const Geom &g, int n) {
+  const int n_rho = n * (g.Hq / g.Hk);
+  if (!is_hybrid(g.kind) && n_rho < tc_min_rows(g.D)) return 0;
+  return prefill_tc_tiles(g.D, n_rho) == 2 ? 1 : 2;
+}
+
+// The prefill entries of one sub-chunk, per launch kind, with their key splits; the
+// merges of the split rows and the partial vectors they need.
+void plan_prefill(const Geom &g, const std::vector<PrefillRow> &prows,
+                  std::vector<PrefillRow> ents[kPrefillKinds], std::vector<MergeRow> &merges,
+                  int64_t *part_vecs) {
+  *part_vecs = 0;
+  merges.clear();
+  for (int kind = 0; kind < kPrefillKinds; ++kind) {
+    std::vector<PrefillRow> sel;
+    for (const PrefillRow &r : prows)
+      if (prefill_kind(g, r.n) == kind) sel.push_back(r);
+    ents[kind] = split_prefill_rows(g, sel, kRowsPerCta[kind], kCtasPerSm[kind], merges,
+                                    part_vecs);
+  }
 }
 
 // Room for n prefill partial vectors.  Growing waits for the work queued on s (the old
@@ -546,34 +590,16 @@ int append_device(kv_cache *c, int layer, const __nv_bfloat16 *q, const __nv_bfl
       if (e != cudaSuccess) return KV_ERR_CUDA;
     }
 
-    // ---- chunked prefill (+ ring commit on sliding layers).  Rows whose GQA group x
-    // chunk gives at least 64 query rows go to the tcgen05 kernel (128-row tiles);
-    // smaller ones to the mma.sync kernel (16-row warp tiles).  Hybrid layers (three key
-    // segments) all go to the tcgen05 kernel.
-    // launch kinds: 0 mma.sync kernel (64 query rows per CTA, two CTAs per SM), 1 tcgen05
-    // kernel with two 128-row query tiles per CTA (one CTA per SM), 2 tcgen05 kernel with
-    // one tile per CTA (two CTAs per SM)
-    constexpr int kKinds = 3;
-    const int rows_per_cta[kKinds] = {64, 256, 128}, ctas_per_sm[kKinds] = {2, 1, 2};
-    auto kind_of = [&](const PrefillRow &r) {
-      if (!hybrid && r.n * rep < tc_min_rows(D)) return 0;
-      return prefill_tc_tiles(D, r.n * rep) == 2 ? 1 : 2;
-    };
-    std::vector<PrefillRow> ents[kKinds];
+    // ---- chunked prefill (+ ring commit on sliding layers), in launches of each kind
+    std::vector<PrefillRow> ents[kPrefillKinds];
     std::vector<MergeRow> merges;
     int64_t part_vecs = 0;
-    for (int kind = 0; kind < kKinds; ++kind) {
-      std::vector<PrefillRow> sel;
-      for (const PrefillRow &r : prows)
-        if (kind_of(r) == kind) sel.push_back(r);
-      ents[kind] = split_prefill_rows(c, layer, sel, rows_per_cta[kind], ctas_per_sm[kind],
-                                      merges, &part_vecs);
-    }
+    plan_prefill(geom_of(c, layer), prows, ents, merges, &part_vecs);
     if (part_vecs > 0) {
       const int rc = ensure_prefill_parts(c, part_vecs, s);
       if (rc != KV_OK) return rc;
     }
-    for (int kind = 0; kind < kKinds; ++kind) {
+    for (int kind = 0; kind < kPrefillKinds; ++kind) {
       const std::vector<PrefillRow> &sel = ents[kind];
       for (size_t r0 = 0; r0 < sel.size(); r0 += kMaxRowsPerLaunch) {
         const size_t r1 = std::min(sel.size(), r0 + kMaxRowsPerLaunch);
@@ -609,7 +635,7 @@ int append_device(kv_cache *c, int layer, const __nv_bfloat16 *q, const __nv_bfl
         for (size_t j = r0; j < r1; ++j) {
           PrefillRow r = sel[j];
           r.cta0 = cta;
-          cta += (r.n * rep + rows_per_cta[kind] - 1) / rows_per_cta[kind];
+          cta += (r.n * rep + kRowsPerCta[kind] - 1) / kRowsPerCta[kind];
           pp.rows[j - r0] = r;
           if (r.tile0 != 0) continue;  // a row's work is counted with its first entry
           const int lkeys = std::min(r.lens, c->R) + r.n;
@@ -1228,6 +1254,87 @@ int kv_debug_wait_timeout(kv_cache *c, uint32_t limit, void *stream) {
   if (!c || limit < 1 || limit > (1u << 20)) return KV_ERR_ARG;
   DeviceGuard guard(c->device);
   return set_err(launch_wait_probe(c->err, limit, (cudaStream_t)stream));
+}
+
+// ---- host-only schedules (no cache, no CUDA call)
+
+constexpr int kPlanMaxLen = 1 << 20;  // the largest max_len a cache takes
+
+static bool plan_geom_ok(int num_sms, int Hq, int Hk, int D, int R, int kind) {
+  if (num_sms < 1 || num_sms > 4096 || Hk < 1 || Hq < Hk || Hq % Hk || Hq / Hk > kMaxRep)
+    return false;
+  if (D != 64 && D != 128) return false;
+  if (kind < KV_GLOBAL || kind > KV_HYBRID_LOCAL) return false;
+  return kind == KV_GLOBAL || (R >= 1 && R <= kPlanMaxLen);
+}
+
+int kv_plan_decode(int num_sms, int Hq, int Hk, int D, int R, int kind, int n_rows,
+                   const int32_t *pos, int32_t *n_splits, int32_t *split_tiles,
+                   int32_t *n_splits2, int32_t *split_tiles2, int32_t *part0, int32_t *n_items) {
+  if (!plan_geom_ok(num_sms, Hq, Hk, D, R, kind) || n_rows < 0 ||
+      n_rows > kMaxRowsPerLaunch || !n_items)
+    return KV_ERR_ARG;
+  if (n_rows > 0 && (!pos || !n_splits || !split_tiles || !n_splits2 || !split_tiles2 || !part0))
+    return KV_ERR_ARG;
+  std::vector<DecodeIn> in(n_rows);
+  for (int i = 0; i < n_rows; ++i) {
+    if (pos[i] < 0 || pos[i] >= kPlanMaxLen) return KV_ERR_ARG;
+    in[i] = {i, i, pos[i]};
+  }
+  const Geom g{num_sms, Hq, Hk, D, kind == KV_GLOBAL ? 0 : R, kind};
+  std::unique_ptr<DecodeParams> p(new DecodeParams());
+  double bytes = 0, flops = 0;
+  plan_decode(g, in, *p, bytes, flops);
+  for (int i = 0; i < n_rows; ++i) {
+    const DecodeRow &r = p->rows[i];
+    n_splits[i] = r.n_splits;
+    split_tiles[i] = r.split_tiles;
+    n_splits2[i] = r.n_splits2;
+    split_tiles2[i] = r.split_tiles2;
+    part0[i] = r.n_splits + r.n_splits2 > 1 ? r.part0 : -1;
+  }
+  *n_items = p->n_items;
+  return KV_OK;
+}
+
+int kv_plan_prefill(int num_sms, int Hq, int Hk, int D, int R, int kind, int n_rows,
+                    const int32_t *lens, const int32_t *n, int capacity, int32_t *entry_row,
+                    int32_t *entry_kind, int32_t *tile0, int32_t *tile1, int32_t *part,
+                    int32_t *n_entries, int32_t *n_splits, int64_t *part_vecs) {
+  if (!plan_geom_ok(num_sms, Hq, Hk, D, R, kind) || n_rows < 0 || capacity < 0 ||
+      !n_entries || !part_vecs)
+    return KV_ERR_ARG;
+  if (n_rows > 0 && (!lens || !n || !n_splits)) return KV_ERR_ARG;
+  if (capacity > 0 && (!entry_row || !entry_kind || !tile0 || !tile1 || !part)) return KV_ERR_ARG;
+  std::vector<PrefillRow> prows(n_rows);
+  for (int i = 0; i < n_rows; ++i) {
+    if (lens[i] < 0 || n[i] < 1 || n[i] > kChunk || lens[i] > kPlanMaxLen - n[i])
+      return KV_ERR_ARG;
+    prows[i] = {i, i, lens[i], n[i], 0, 0, 0, 0};
+  }
+  const Geom g{num_sms, Hq, Hk, D, kind == KV_GLOBAL ? 0 : R, kind};
+  std::vector<PrefillRow> ents[kPrefillKinds];
+  std::vector<MergeRow> merges;
+  int64_t vecs = 0;
+  plan_prefill(g, prows, ents, merges, &vecs);
+  int total = 0;
+  for (const auto &e : ents) total += (int)e.size();
+  *n_entries = total;
+  if (total > capacity) return KV_ERR_ARG;
+  int j = 0;
+  for (int kd = 0; kd < kPrefillKinds; ++kd)
+    for (const PrefillRow &r : ents[kd]) {
+      entry_row[j] = r.call_row;
+      entry_kind[j] = kd;
+      tile0[j] = r.tile0;
+      tile1[j] = r.tile1;
+      part[j] = r.part;
+      ++j;
+    }
+  for (int i = 0; i < n_rows; ++i) n_splits[i] = 1;
+  for (const MergeRow &m : merges) n_splits[m.call_row] = m.n_splits;
+  *part_vecs = vecs;
+  return KV_OK;
 }
 
 int kv_profile_enable(kv_cache *c, int enable) {
