@@ -433,9 +433,10 @@ int kv_import_row(kv_cache *c, int row, int keep, const void *src, int64_t bytes
  * latency-critical loop that must never allocate.  Such a caller cannot create a
  * kv_cache, so it passes its own memory: the cache storage, the queries, the
  * RoPE table and the output.  The call runs the same split-K decode kernel as
- * kv_append; its split partials and merge tickets live in one file-scope device
- * array of 18 MiB + 128 KiB + 256 bytes that every GPU which loads the library
- * holds until the process exits.
+ * kv_append, with kv_append's split schedule (kv_plan_decode with kind KV_GLOBAL
+ * and pos = n_keys - 1 gives it); its split partials and merge tickets live in
+ * one file-scope device array of 18 MiB + 128 KiB + 256 bytes that every GPU
+ * which loads the library holds until the process exits.
  *
  *  K, V        device bf16 [n_cache_rows][Hk][seg_rows][D] (one layer's storage in
  *              the kv_cache layout, e.g. from kv_debug_ptrs, or the caller's own)

@@ -273,24 +273,16 @@ Geom geom_of(const kv_cache *c, int layer) {
   return {c->num_sms, c->Hq, c->Hk, c->D, c->R, c->kind[layer]};
 }
 
-// Split-K schedule for one batch of decode rows (<= kMaxRowsPerLaunch).  Segment 0 holds
-// storage slots [0, nk) of the layer storage (the ring of a sliding layer, else a cache);
-// a hybrid layer adds segment 1, its own ring, with its own splits.
-void plan_decode(const Geom &g, const std::vector<DecodeIn> &in, DecodeParams &p,
-                 double &kv_bytes, double &flops) {
-  const bool sliding = g.kind == KV_SLIDING, hybrid = is_hybrid(g.kind);
+}  // namespace
+
+int kvinc::plan_decode_splits(int num_sms, int Hk, int n, const int *nk2, DecodeParams &p) {
   const auto tiles_of = [](int keys) { return (keys + kTileKeys - 1) / kTileKeys; };
   int64_t total_tiles = 0;
-  std::vector<int> nk(in.size()), nk2(in.size(), 0);
-  for (size_t i = 0; i < in.size(); ++i) {
-    nk[i] = sliding ? std::min(in[i].pos + 1, g.R) : in[i].pos + 1;
-    if (hybrid) nk2[i] = std::min(in[i].pos + 1, g.R);
-    total_tiles += tiles_of(nk[i]) + tiles_of(nk2[i]);
-  }
+  for (int i = 0; i < n; ++i) total_tiles += tiles_of(p.rows[i].nk) + tiles_of(nk2[i]);
   // Aim for about four waves of two CTAs per SM: `per` tiles per split, at least
   // kMinDecodeSplitTiles.
-  const int64_t target = (int64_t)g.num_sms * 2 * 4;
-  int64_t per = (total_tiles * g.Hk + target - 1) / target;
+  const int64_t target = (int64_t)num_sms * 2 * 4;
+  int64_t per = (total_tiles * Hk + target - 1) / target;
   if (per < kMinDecodeSplitTiles) per = kMinDecodeSplitTiles;
   // splits of one segment: at most `cap`, each a whole number of tiles
   const auto splits = [&](int keys, int cap, int &st) {
@@ -301,35 +293,53 @@ void plan_decode(const Geom &g, const std::vector<DecodeIn> &in, DecodeParams &p
     return (tiles + st - 1) / st;
   };
   int item = 0, part = 0;
-  kv_bytes = 0;
-  flops = 0;
-  for (size_t i = 0; i < in.size(); ++i) {
-    int st = 0, st2 = 0;
-    const int ns2 = hybrid ? splits(nk2[i], kMaxSplits / 4, st2) : 0;
-    const int ns = splits(nk[i], kMaxSplits - ns2, st);
+  for (int i = 0; i < n; ++i) {
     DecodeRow &r = p.rows[i];
-    r.cache_row = in[i].cache_row;
-    r.call_row = (uint16_t)in[i].call_row;
-    r.pos = in[i].pos;
-    r.nk = nk[i];
+    int st = 0, st2 = 0;
+    const int ns2 = nk2[i] > 0 ? splits(nk2[i], kMaxSplits / 4, st2) : 0;
+    const int ns = splits(r.nk, kMaxSplits - ns2, st);
     r.item0 = (uint16_t)item;
     r.split_tiles = st;
     r.n_splits = (uint8_t)ns;
     r.split_tiles2 = st2;
     r.n_splits2 = (uint8_t)ns2;
-    r.ctr = in[i].cache_row;
     const int total = ns + ns2;
     r.part0 = (uint16_t)(total > 1 ? part : 0);
     if (total > 1) part += total;
     item += total;
-    kv_bytes += 2.0 * (nk[i] + nk2[i]) * g.Hk * g.D * 2.0;
-    flops += 4.0 * (nk[i] + nk2[i]) * g.Hq * g.D;
   }
-  p.n_rows = (int)in.size();
+  p.n_rows = n;
   p.n_items = item;
-  p.uniform_items = in.empty() ? 0 : p.rows[0].n_splits + p.rows[0].n_splits2;
-  for (size_t i = 1; i < in.size() && p.uniform_items; ++i)
+  p.uniform_items = n == 0 ? 0 : p.rows[0].n_splits + p.rows[0].n_splits2;
+  for (int i = 1; i < n && p.uniform_items; ++i)
     if (p.rows[i].n_splits + p.rows[i].n_splits2 != p.uniform_items) p.uniform_items = 0;
+  return part;
+}
+
+namespace {
+
+// Split-K schedule for one batch of decode rows (<= kMaxRowsPerLaunch).  Segment 0 holds
+// storage slots [0, nk) of the layer storage (the ring of a sliding layer, else a cache);
+// a hybrid layer adds segment 1, its own ring, with its own splits.  Merge tickets are
+// kept per cache row.
+void plan_decode(const Geom &g, const std::vector<DecodeIn> &in, DecodeParams &p,
+                 double &kv_bytes, double &flops) {
+  const bool sliding = g.kind == KV_SLIDING, hybrid = is_hybrid(g.kind);
+  std::vector<int> nk2(in.size(), 0);
+  kv_bytes = 0;
+  flops = 0;
+  for (size_t i = 0; i < in.size(); ++i) {
+    DecodeRow &r = p.rows[i];
+    r.cache_row = in[i].cache_row;
+    r.call_row = (uint16_t)in[i].call_row;
+    r.pos = in[i].pos;
+    r.nk = sliding ? std::min(in[i].pos + 1, g.R) : in[i].pos + 1;
+    r.ctr = in[i].cache_row;
+    if (hybrid) nk2[i] = std::min(in[i].pos + 1, g.R);
+    kv_bytes += 2.0 * (r.nk + nk2[i]) * g.Hk * g.D * 2.0;
+    flops += 4.0 * (r.nk + nk2[i]) * g.Hq * g.D;
+  }
+  plan_decode_splits(g.num_sms, g.Hk, (int)in.size(), nk2.data(), p);
   p.seg0_ring = sliding ? 1 : 0;
   p.ring_R = g.R > 0 ? g.R : 1;
 }

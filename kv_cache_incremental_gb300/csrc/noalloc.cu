@@ -13,7 +13,6 @@
 // call's contents, so calls whose work overlaps on the GPU (two streams, or two
 // host threads) race on it.  The merge tickets and the error word must start at
 // zero: each call clears the ones it uses on its stream before the kernel runs.
-#include <algorithm>
 #include <cmath>
 #include <mutex>
 
@@ -36,6 +35,9 @@ constexpr size_t kErrBytes = 256;                  // device error word
 constexpr size_t kNoallocScratchBytes = kPartOBytes + kPartMLBytes + kTicketBytes + kErrBytes;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
+
+// segment-1 keys of every row: none (the caller's storage is one segment)
+const int kNoRing[kMaxRowsPerLaunch] = {};
 
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mu;
@@ -124,34 +126,17 @@ extern "C" int kv_decode_noalloc(const void *K, const void *V, int n_cache_rows,
       !encode(&dp.tmap_v, V, (int64_t)n_cache_rows * Hk * seg_rows, D))
     return KV_ERR_CUDA;
 
-  // Split schedule as in kv_append: about four waves of two CTAs per SM.
-  int64_t total_tiles = 0;
-  for (int i = 0; i < Bs; ++i) total_tiles += (n_keys[i] + kTileKeys - 1) / kTileKeys;
-  const int64_t target = (int64_t)num_sms * 2 * 4;
-  int64_t per = (total_tiles * Hk + target - 1) / target;
-  if (per < 4) per = 4;
-  int item = 0, part = 0;
+  // The split schedule of kv_append over one key segment; merge tickets per call row (the
+  // caller's rows may lie beyond the ticket array).
   for (int i = 0; i < Bs; ++i) {
-    const int tiles = (n_keys[i] + kTileKeys - 1) / kTileKeys;
-    int ns = (int)std::min<int64_t>(kMaxSplits, (tiles + per - 1) / per);
-    if (ns < 1) ns = 1;
-    const int st = (tiles + ns - 1) / ns;
-    ns = (tiles + st - 1) / st;
     DecodeRow &r = dp.rows[i];
     r.cache_row = cache_rows[i];
     r.call_row = (uint16_t)i;
     r.pos = pos[i];
     r.nk = n_keys[i];
-    r.item0 = (uint16_t)item;
-    r.split_tiles = st;
-    r.n_splits = (uint8_t)ns;
-    r.split_tiles2 = 0;
-    r.n_splits2 = 0;  // one key segment
-    r.part0 = (uint16_t)(ns > 1 ? part : 0);
     r.ctr = i;
-    if (ns > 1) part += ns;
-    item += ns;
   }
+  const int part = plan_decode_splits(num_sms, Hk, Bs, kNoRing, dp);
   // The partials of this call must fit the fixed scratch.
   if ((size_t)part * Hq * D * sizeof(float) > kPartOBytes ||
       (size_t)part * Hq * sizeof(float2) > kPartMLBytes)
@@ -180,7 +165,6 @@ extern "C" int kv_decode_noalloc(const void *K, const void *V, int n_cache_rows,
   dp.cache_v = nullptr;
   dp.fuse_append = 0;  // the caller has stored the new key already
   dp.fuse_append2 = 0;
-  dp.uniform_items = 0;  // rows found by search
   dp.seg0_ring = 0;
   dp.ring_R = 1;
   dp.pt = PageTable{nullptr, 0, 0};  // the caller's storage is dense
@@ -190,8 +174,6 @@ extern "C" int kv_decode_noalloc(const void *K, const void *V, int n_cache_rows,
   dp.Hk = Hk;
   dp.rep = Hq / Hk;
   dp.seg_rows = seg_rows;
-  dp.n_rows = Bs;
-  dp.n_items = item;
   dp.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
   if (launch_decode(dp, D, dp.rep <= 8 ? 1 : 2, s) != cudaSuccess) return KV_ERR_CUDA;
   return KV_OK;
