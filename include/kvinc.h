@@ -349,7 +349,8 @@ int kv_profile_read(kv_cache *c, int kind, int reset, int64_t *launches, double 
  *  Hq            must equal the cache's Hq
  *
  * kv_step_graph_create plans for the current lengths and enqueues nothing;
- * KV_ERR_ARG for bad arguments, KV_ERR_CUDA if graph construction fails.
+ * KV_ERR_ARG for bad arguments, KV_ERR_CUDA if graph construction fails, and on
+ * any failure *out is NULL (when out is not).
  * kv_step_graph_launch returns KV_ERR_FULL (and changes no state) if a row is at
  * max_len, KV_ERR_CUDA if a CUDA call fails; it never synchronises.  Rows of the
  * cache that are not in `rows` are untouched.  A reset of one of the rows between

@@ -487,7 +487,7 @@ void plan_prefill(const Geom &g, const std::vector<PrefillRow> &prows,
 // Room for n prefill partial vectors.  Growing waits for the work queued on s (the old
 // buffer may be in use).
 int ensure_prefill_parts(kv_cache *c, int64_t n, cudaStream_t s) {
-  if (n <= c->ppart_cap) return KV_OK;
+  if (n <= 0 || n <= c->ppart_cap) return KV_OK;
   if ((c->ppart_o || c->ppart_ml) && cudaStreamSynchronize(s) != cudaSuccess) return KV_ERR_CUDA;
   cudaFree(c->ppart_o);
   cudaFree(c->ppart_ml);
@@ -517,6 +517,28 @@ int append_device(kv_cache *c, int layer, const __nv_bfloat16 *q, const __nv_bfl
   int max_n = 0;
   for (int i = 0; i < Bs; ++i) max_n = std::max(max_n, (int)n_new[i]);
   if (max_n == 0) return KV_OK;
+  // the chunk rows of the sub-chunk at token offset `off`: rows of two or more new tokens
+  // with tokens left there
+  const auto chunk_rows = [&](int off) {
+    std::vector<PrefillRow> rows;
+    for (int i = 0; i < Bs; ++i)
+      if (n_new[i] >= 2 && n_new[i] > off)
+        rows.push_back({cache_rows[i], i, c->lens[cache_rows[i]] + off,
+                        std::min(kChunk, n_new[i] - off), 0});
+    return rows;
+  };
+  {  // room for every sub-chunk's prefill partials before anything is enqueued or taken
+    int64_t most = 0;
+    for (int off = 0; off < max_n; off += kChunk) {
+      std::vector<PrefillRow> ents[kPrefillKinds];
+      std::vector<MergeRow> merges;
+      int64_t vecs = 0;
+      plan_prefill(geom_of(c, layer), chunk_rows(off), ents, merges, &vecs);
+      most = std::max(most, vecs);
+    }
+    const int rc = ensure_prefill_parts(c, most, s);
+    if (rc != KV_OK) return rc;
+  }
   if (c->n_blocks > 0) {  // pool blocks for the new positions, before anything is enqueued
     std::vector<std::pair<int, int>> want;
     for (int i = 0; i < Bs; ++i)
@@ -534,20 +556,16 @@ int append_device(kv_cache *c, int layer, const __nv_bfloat16 *q, const __nv_bfl
 
   for (int off = 0; off < max_n; off += kChunk) {
     std::vector<AppendRow> arows, lrows;  // to the layer storage / a hybrid ring's scratch
-    std::vector<DecodeIn> drows;
-    std::vector<PrefillRow> prows;
-    for (int i = 0; i < Bs; ++i) {
-      const int n = n_new[i];
-      const int b = cache_rows[i];
-      if (n == 1 && off == 0) {
-        drows.push_back({b, i, c->lens[b]});  // appended inside the decode kernel
-      } else if (n >= 2 && n - off >= 1) {
-        const int ns = std::min(kChunk, n - off);
-        if (writes_global)
-          arows.push_back({b, i, c->lens[b] + off, ns, sliding ? kDestScratch : kDestGlobal, 0});
-        if (hybrid) lrows.push_back({b, i, c->lens[b] + off, ns, kDestScratch, 0});
-        prows.push_back({b, i, c->lens[b] + off, ns, 0});
-      }
+    std::vector<DecodeIn> drows;          // single-token rows: appended inside the decode kernel
+    const std::vector<PrefillRow> prows = chunk_rows(off);
+    if (off == 0)
+      for (int i = 0; i < Bs; ++i)
+        if (n_new[i] == 1) drows.push_back({cache_rows[i], i, c->lens[cache_rows[i]]});
+    for (const PrefillRow &r : prows) {
+      if (writes_global)
+        arows.push_back({r.cache_row, r.call_row, r.lens, r.n,
+                         sliding ? kDestScratch : kDestGlobal, 0});
+      if (hybrid) lrows.push_back({r.cache_row, r.call_row, r.lens, r.n, kDestScratch, 0});
     }
 
     // ---- RoPE + append of the chunk rows of this sub-chunk (a hybrid layer: the global
@@ -605,7 +623,7 @@ int append_device(kv_cache *c, int layer, const __nv_bfloat16 *q, const __nv_bfl
     std::vector<MergeRow> merges;
     int64_t part_vecs = 0;
     plan_prefill(geom_of(c, layer), prows, ents, merges, &part_vecs);
-    if (part_vecs > 0) {
+    if (part_vecs > 0) {  // the room made before the first sub-chunk: no allocation here
       const int rc = ensure_prefill_parts(c, part_vecs, s);
       if (rc != KV_OK) return rc;
     }
@@ -781,10 +799,6 @@ void free_all(kv_cache *c) {
 
 }  // namespace
 
-extern "C" {
-
-}  // extern "C"
-
 static int create_impl(kv_cache **out, int B, int max_len, int Hq, int Hk, int D, int W,
                        int n_layers, const int32_t *layer_kind, double rope_theta, int device,
                        int n_blocks) {
@@ -807,8 +821,10 @@ static int create_impl(kv_cache **out, int B, int max_len, int Hq, int Hk, int D
   }
   if (any_sliding && W < 1) return KV_ERR_ARG;
   const int R = any_sliding ? (W < max_len ? W : max_len) : 0;
-  if (n_blocks == 0 && (int64_t)B * Hk * (max_len + 1) >= (1LL << 31))
-    return KV_ERR_ARG;  // TMA coordinates
+  // TMA row coordinates of the dense caches, the rings and the chunk scratch
+  if (n_blocks == 0 && (int64_t)B * Hk * (max_len + 1) >= (1LL << 31)) return KV_ERR_ARG;
+  if ((int64_t)B * Hk * (R + 1) >= (1LL << 31) || (int64_t)B * Hk * kChunk >= (1LL << 31))
+    return KV_ERR_ARG;
 
   int n_dev = 0;
   if (cudaGetDeviceCount(&n_dev) != cudaSuccess || device >= n_dev) return KV_ERR_CUDA;
@@ -949,7 +965,8 @@ static int create_impl(kv_cache **out, int B, int max_len, int Hq, int Hk, int D
     if (cudaMalloc((void **)&c->lpos, (size_t)B * R * 4) != cudaSuccess) return fail(KV_ERR_OOM);
     if (cudaMemset(c->lpos, 0xFF, (size_t)B * R * 4) != cudaSuccess) return fail(KV_ERR_CUDA);
   }
-  const size_t parts = (size_t)B * kMaxSplits * Hq;
+  // decode partial slots are numbered per launch (at most kMaxRowsPerLaunch rows)
+  const size_t parts = (size_t)std::min(B, kMaxRowsPerLaunch) * kMaxSplits * Hq;
   if (!alloc((void **)&c->part_o, parts * D * 4) || !alloc((void **)&c->part_ml, parts * 8))
     return fail(KV_ERR_OOM);
   if (cudaDeviceSynchronize() != cudaSuccess) return fail(KV_ERR_CUDA);
@@ -972,7 +989,10 @@ int kv_cache_create(kv_cache **out, int B, int max_len, int Hq, int Hk, int D, i
 int kv_cache_create_paged(kv_cache **out, int B, int max_len, int Hq, int Hk, int D, int W,
                           int n_layers, const int32_t *layer_kind, double rope_theta, int device,
                           int n_blocks) {
-  if (n_blocks < 1) return KV_ERR_ARG;
+  if (n_blocks < 1) {
+    if (out) *out = nullptr;
+    return KV_ERR_ARG;
+  }
   return create_impl(out, B, max_len, Hq, Hk, D, W, n_layers, layer_kind, rope_theta, device,
                      n_blocks);
 }
@@ -1489,6 +1509,7 @@ int step_graph_create(kv_cache *c, kv_step_graph **out, const void *const *q,
                       const void *const *k, const void *const *v, const void *const *kg,
                       const void *const *vg, void *const *outp, int Hq, const int32_t *rows,
                       int Bs) {
+  if (out) *out = nullptr;
   if (!c || !out || Hq != c->Hq) return KV_ERR_ARG;
   if (Bs < 1 || Bs > c->B || Bs > kMaxRowsPerLaunch) return KV_ERR_ARG;
   std::vector<int32_t> cache_rows;
@@ -1552,7 +1573,10 @@ extern "C" {
 int kv_step_graph_create(kv_cache *c, kv_step_graph **out, const void *const *q,
                          const void *const *k, const void *const *v, void *const *outp, int Hq,
                          const int32_t *rows, int Bs) {
-  if (!c || has_hybrid(c)) return KV_ERR_ARG;  // kv_step_graph_create_hybrid
+  if (!c || has_hybrid(c)) {  // kv_step_graph_create_hybrid
+    if (out) *out = nullptr;
+    return KV_ERR_ARG;
+  }
   return step_graph_create(c, out, q, k, v, nullptr, nullptr, outp, Hq, rows, Bs);
 }
 

@@ -52,6 +52,20 @@ def test_strerror_and_null_handling_need_no_gpu():
     sliding = (ctypes.c_int32 * 1)(1)
     assert lib.kv_cache_create(ctypes.byref(out), 2, 16, 4, 2, 64, 0, 1, sliding, 1e4, 0) == 1
     assert lib.kv_cache_create(ctypes.byref(out), 2, 16, 64, 2, 64, 0, 1, kinds, 1e4, 0) == 1
+    # a paged cache needs a pool; *out is cleared on that refusal too
+    out.value = 123
+    assert lib.kv_cache_create_paged(ctypes.byref(out), 2, 16, 4, 2, 64, 0, 1, kinds, 1e4, 0,
+                                     0) == 1
+    assert out.value is None
+    # ring rows beyond TMA's 2^31 row coordinates (65536 rows x 16 heads x 2049 slots), on
+    # a paged cache whose global pool is small: refused before any CUDA call
+    assert lib.kv_cache_create_paged(ctypes.byref(out), 65536, 4096, 16, 16, 64, 2048, 1,
+                                     sliding, 1e4, 0, 1) == 1
+    # a refused step graph leaves *out NULL
+    g = ctypes.c_void_p(77)
+    assert lib.kv_step_graph_create(None, ctypes.byref(g), None, None, None, None, 4, None,
+                                    1) == 1
+    assert g.value is None
 
 
 def test_package_import_fails_loudly_without_library(tmp_path, monkeypatch):
