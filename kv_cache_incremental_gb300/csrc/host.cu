@@ -1723,10 +1723,23 @@ int flush_copies(CopyParams &cp, cudaStream_t s) {
   return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
 }
 
+// Copy items span at most this many positions: a long row is cut into pieces that run in
+// CTAs of their own (both sides address positions absolutely -- slot p, p % R, p - base or
+// a block-table entry -- so the pieces are independent).
+constexpr int kCopySpan = 2048;
+
 int add_copy(CopyParams &cp, const CopyItem &it, cudaStream_t s) {
-  if (it.p1 <= it.p0) return KV_OK;
-  cp.items[cp.n_items++] = it;
-  return cp.n_items == kMaxCopyItems ? flush_copies(cp, s) : KV_OK;
+  for (int p = it.p0; p < it.p1; p += kCopySpan) {
+    CopyItem piece = it;
+    piece.p0 = p;
+    piece.p1 = std::min(it.p1, p + kCopySpan);
+    cp.items[cp.n_items++] = piece;
+    if (cp.n_items == kMaxCopyItems) {
+      const int rc = flush_copies(cp, s);
+      if (rc != KV_OK) return rc;
+    }
+  }
+  return KV_OK;
 }
 
 // lpos of rows that now hold [0, keep): reset, then record the kept positions.

@@ -19,8 +19,9 @@ __device__ __forceinline__ int64_t elem_of(int p, int h, int D, const int32_t *t
   return h * head_stride + (int64_t)(ring > 0 ? p % ring : p - base) * D;
 }
 
-// grid (items, Hk): one CTA per (item, kv head); 16-byte chunks of K and V, every load of
-// a pass issued before the first store.
+// grid (items, Hk): one CTA per (item, kv head), the host cutting long rows into items of at
+// most 2048 positions; 16-byte chunks of K and V, every load of a pass issued before the
+// first store.
 __global__ void __launch_bounds__(256) copy_kernel(const __grid_constant__ CopyParams p) {
   const CopyItem &it = p.items[blockIdx.x];
   const int h = blockIdx.y;
