@@ -56,7 +56,7 @@ WORKLOADS = {
 HYBRID = (2, 3)  # KV_HYBRID_FULL, KV_HYBRID_LOCAL
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=0, help="0: the workload's default")
@@ -76,7 +76,7 @@ def parse():
     ap.add_argument("--max-len", type=int, default=0,
                     help="allocate the cache for this many positions instead of the "
                          "workload's (small cases for profiling; with --fill-to)")
-    args = ap.parse_args()
+    args = ap.parse_args(argv)
     if args.max_len:
         WORKLOADS[args.workload] = dict(WORKLOADS[args.workload], max_len=args.max_len)
     return args
@@ -109,6 +109,45 @@ def initial_lens(cfg, total_steps, seed):
     rng = np.random.default_rng(seed)
     hi = cfg["max_len"] - total_steps - 1
     return rng.integers(cfg["lo"], hi + 1, size=cfg["B"]).astype(np.int64)
+
+
+def decode_plan(cfg, args):
+    """Timed steps K, warm-up steps, steps per cache fill, cache fills and the length reserve
+    of a decode workload.  The configuration times per_round steps per cache fill; longer
+    runs use several independently filled caches of that length (keeps the length
+    distribution).  The reserve covers warm-up + timed steps, the same steps again with
+    per-launch events (kernel durations), as decode-step graph replays, and end to end."""
+    K = args.steps if args.steps else cfg["steps"]
+    Wm = max(3, args.warmup)
+    per_round = min(K, cfg["per_round"])
+    rounds = (K + per_round - 1) // per_round
+    return K, Wm, per_round, rounds, 4 * (Wm + per_round)
+
+
+def decode_config(args, cfg, world):
+    """`config` of a decode workload's JSON line, the same for both arms."""
+    _, _, per_round, rounds, reserve = decode_plan(cfg, args)
+    return {"workload": args.workload, "B": cfg["B"], "Hq": cfg["Hq"], "Hk": cfg["Hk"],
+            "D": cfg["D"], "max_len": cfg["max_len"], "layers": len(cfg["kinds"]),
+            "window": cfg["W"] or None,
+            "lens": f"U[{cfg['lo']}, {cfg['max_len'] - reserve - 1}] per cache",
+            "caches": rounds, "steps_per_cache": per_round, "paged": bool(args.paged),
+            "l2": "inputs larger than L2 (K/V read per step >> 129 MB)",
+            "parallelism": f"replicas x{world}"}
+
+
+CONT_CHUNK = 64  # right-padded chunk width of the continuous-batch mix
+
+
+def cont_config(args, cfg, world):
+    """`config` of the continuous-batch workload's JSON line, the same for both arms."""
+    return {"workload": args.workload, "B": cfg["B"], "Hq": cfg["Hq"], "Hk": cfg["Hk"],
+            "D": cfg["D"], "max_len": cfg["max_len"], "layers": len(cfg["kinds"]),
+            "window": cfg["W"], "lens": f"U[{cfg['lo']}, {cfg['hi']}] initial",
+            "chunk": CONT_CHUNK,
+            "mix": "n_new 1 (40%), 0 (30%), U[2,64] (30%); 5% of rows reset per step",
+            "l2": "inputs larger than L2 (per step ~0.6 GB of K/V, 0.2 GB of inputs)",
+            "parallelism": f"replicas x{world}"}
 
 
 def kv_bytes_per_step(cfg, lens):
@@ -323,9 +362,11 @@ def run_reference(args):
     if rank != 0:
         return
     cfg = WORKLOADS[args.workload]
+    config = decode_config(args, cfg, world)
+    _, _, _, _, reserve = decode_plan(cfg, args)
     if not args.steps:
         args.steps = 10
-    lens = initial_lens(cfg, 2 * (args.warmup + cfg["per_round"]), args.seed)
+    lens = initial_lens(cfg, reserve, args.seed)   # the first cache fill of the timed arm
     # each step: a bounded sample of rows of one decode step, sized to finish in seconds
     for _ in range(max(0, args.warmup)):
         oracle_sample(cfg, lens, args.seed, budget_s=0.5, max_rows=1)
@@ -340,8 +381,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": args.workload, **{k: cfg[k] for k in (
-            "B", "Hq", "Hk", "D", "max_len")}},
+        "data": "synthetic", "config": config,
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": thr, "kind": "oracle",
                          "sample": f"{rows} row-decodes (all {cfg['Hq']} heads, full history) "
                                    f"of the workload's first layer over {args.steps} steps"},
@@ -474,15 +514,7 @@ def run_ours(args):
     cfg = WORKLOADS[args.workload]
     B, Hq, Hk, D = cfg["B"], cfg["Hq"], cfg["Hk"], cfg["D"]
     n_layers = len(cfg["kinds"])
-    K = args.steps if args.steps else cfg["steps"]
-    Wm = max(3, args.warmup)
-    # The configuration times 100 steps per cache fill; longer runs use several
-    # independently filled caches of that length (keeps the length distribution).
-    per_round = min(K, cfg["per_round"])
-    rounds = (K + per_round - 1) // per_round
-    # warm-up + timed, the same steps again with per-launch events (kernel durations), as
-    # decode-step graph replays, and end to end
-    reserve = 4 * (Wm + per_round)
+    K, Wm, per_round, rounds, reserve = decode_plan(cfg, args)
     stream = torch.cuda.current_stream()
     dev = torch.device("cuda", local_rank)
 
@@ -694,14 +726,7 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": Wm, "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": args.workload, "B": B, "Hq": Hq, "Hk": Hk, "D": D,
-                   "max_len": cfg["max_len"], "layers": n_layers,
-                   "window": cfg["W"] or None,
-                   "lens": f"U[{cfg['lo']}, {cfg['max_len'] - reserve - 1}] per cache",
-                   "caches": rounds, "steps_per_cache": per_round,
-                   "paged": bool(args.paged),
-                   "l2": "inputs larger than L2 (K/V read per step >> 129 MB)",
-                   "parallelism": f"replicas x{world}"},
+        "config": decode_config(args, cfg, world),
         "tokens_per_s": tok_s,
         "frac_of_nominal_8TBs": value / NOMINAL_HBM_GBS,
         "roofline": roofline,
@@ -822,7 +847,7 @@ def run_cont_batch(args):
         import torch.distributed as dist
         dist.init_process_group("nccl")
     cfg = WORKLOADS[args.workload]
-    B, Hq, Hk, D, C = cfg["B"], cfg["Hq"], cfg["Hk"], cfg["D"], 64
+    B, Hq, Hk, D, C = cfg["B"], cfg["Hq"], cfg["Hk"], cfg["D"], CONT_CHUNK
     kinds = cfg["kinds"]
     K = args.steps if args.steps else cfg["steps"]
     Wm = max(3, args.warmup)
@@ -935,12 +960,7 @@ def run_cont_batch(args):
         "value": tokens_all / (ms / 1e3), "unit": "tokens/s", "n_gpus": world, "steps": K,
         "warmup": Wm, "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": args.workload, "B": B, "Hq": Hq, "Hk": Hk, "D": D,
-                   "max_len": cfg["max_len"], "layers": len(kinds), "window": cfg["W"],
-                   "lens": f"U[{cfg['lo']}, {cfg['hi']}] initial", "chunk": C,
-                   "mix": "n_new 1 (40%), 0 (30%), U[2,64] (30%); 5% of rows reset per step",
-                   "l2": "inputs larger than L2 (per step ~0.6 GB of K/V, 0.2 GB of inputs)",
-                   "parallelism": f"replicas x{world}"},
+        "config": cont_config(args, cfg, world),
         "gbs": tot_bytes / (ms / 1e3) / 1e9, "tflops": tot_flops / (ms / 1e3) / 1e12,
         "roofline": roofline,
         "e2e": {"value": tokens_all / (ms_e2e / 1e3), "unit": "tokens/s",
@@ -962,12 +982,14 @@ def run_reference_cont(args):
     if rank != 0:
         return
     cfg = WORKLOADS[args.workload]
+    config = cont_config(args, cfg, world)
     if not args.steps:
         args.steps = 10
-    _, steps = cont_plan(cfg, max(3, args.warmup) + args.steps, args.seed)
+    Wm = max(3, args.warmup)
+    _, steps = cont_plan(cfg, Wm + args.steps, args.seed)
     cont_oracle_sample(cfg, steps[:1], args.seed, budget_s=0.5)
     total_tok, total_t, thr = 0, 0.0, 1
-    for i in range(args.steps):
+    for i in range(Wm, Wm + args.steps):   # the steps the timed arm times
         _, tok, thr, t = cont_oracle_sample(cfg, steps[i:i + 1], args.seed, budget_s=1.0)
         total_tok += tok
         total_t += t
@@ -978,8 +1000,7 @@ def run_reference_cont(args):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * total_t / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": args.workload, **{k: cfg[k] for k in ("B", "Hq", "Hk", "D",
-                                                                    "max_len")}},
+        "config": config,
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": thr, "kind": "oracle",
                          "sample": f"{total_tok} tokens (whole rows, all layers) over "
                                    f"{args.steps} steps, about 1 s of oracle time each"},

@@ -68,10 +68,15 @@ def _reference_line(workload):
     return json.loads(lines[0])
 
 
-def test_reference_arm_line_for_the_continuous_batch_mix():
-    for workload, unit in (("cont_batch", "tokens/s"),):
+def test_reference_arm_lines_carry_the_timed_arms_config():
+    """The reference arm reports the timed arm's metric unit and its exact config (the same
+    function builds both), with the oracle as its CPU baseline."""
+    for workload, unit in (("cont_batch", "tokens/s"), ("decode_bw", "GB/s")):
         d = _reference_line(workload)
         assert d["impl"] == "reference" and d["unit"] == unit and d["value"] > 0
-        assert d["config"]["workload"] == workload
+        args = bench.parse(["--workload", workload, "--steps", "1", "--warmup", "1"])
+        cfg = bench.WORKLOADS[workload]
+        want = (bench.cont_config if cfg.get("mix") else bench.decode_config)(args, cfg, 1)
+        assert d["config"] == want
         assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
         assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
