@@ -54,7 +54,7 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch):
     small = dict(B=2, Hq=4, Hk=2, D=64, max_len=300, W=0, kinds=[0], lo=100, steps=2,
                  per_round=2)
     monkeypatch.setitem(bench.WORKLOADS, "tiny", small)
-    args = type("A", (), dict(workload="tiny", steps=2, warmup=1, seed=0))()
+    args = bench.parse(["--workload", "tiny", "--steps", "2", "--warmup", "1"])
     monkeypatch.setenv("RANK", "1")
     monkeypatch.setenv("WORLD_SIZE", "2")
     buf = io.StringIO()
@@ -68,4 +68,5 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch):
     line = json.loads(buf.getvalue())
     assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["n_gpus"] == 2
+    assert line["config"] == bench.decode_config(args, small, 2)
     assert line["e2e"]["h2d_bytes_per_step"] == 0
