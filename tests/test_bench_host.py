@@ -77,6 +77,6 @@ def test_reference_arm_lines_carry_the_timed_arms_config():
         args = bench.parse(["--workload", workload, "--steps", "1", "--warmup", "1"])
         cfg = bench.WORKLOADS[workload]
         want = (bench.cont_config if cfg.get("mix") else bench.decode_config)(args, cfg, 1)
-        assert d["config"] == want
+        assert d["config"] == want and d["metric"] == bench.METRICS[workload]
         assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
         assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
