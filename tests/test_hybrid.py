@@ -40,7 +40,7 @@ def test_hybrid_mixed_with_global_and_sliding_layers():
     assert sc.max_ratio <= 1.0
 
 
-@pytest.mark.parametrize("Hq,Hk", [(16, 4), (32, 8), (8, 8)])
+@pytest.mark.parametrize("Hq,Hk", [(16, 4), (64, 8), (32, 2), (8, 8)])
 def test_hybrid_d128_long_rows_split_decode(Hq, Hk):
     """D=128, long rows: the decode splits the group cache over several CTAs and adds the
     ring as its own split; tensor-core prefill over 128-key blocks of all three segments."""

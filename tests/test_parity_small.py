@@ -68,7 +68,7 @@ def test_config2_sliding_ring_wraps():
 
 
 @pytest.mark.parametrize("D,Hq,Hk", [(64, 4, 4), (64, 8, 4), (128, 16, 4), (128, 32, 4),
-                                     (64, 16, 1), (128, 8, 8)])
+                                     (64, 16, 1), (128, 8, 8), (128, 32, 2)])
 def test_head_layouts_decode_and_prefill(D, Hq, Hk):
     """GQA groups of 1, 2, 4, 8 and 16 query heads per kv head, both head dims."""
     sc = Scenario(B=3, max_len=300, Hq=Hq, Hk=Hk, D=D, W=40, kinds=[0, 1], seed=4)
