@@ -91,6 +91,17 @@ def test_long_decode_multi_split_and_tails():
         sc.step([1, 1, 1], C=1)
 
 
+@pytest.mark.parametrize("D,Hq,Hk", [(64, 8, 2), (128, 16, 4)])
+def test_one_token_sub_chunks(D, Hq, Hk):
+    """Rows of 65 and 129 tokens end in a sub-chunk of one token, which takes the chunk path
+    (append, prefill, ring commit), not the decode path; every layer kind, rings wrapping
+    inside the chunk (W = 8)."""
+    sc = Scenario(B=3, max_len=400, Hq=Hq, Hk=Hk, D=D, W=8, kinds=[1, 0, 2, 3], seed=12)
+    sc.step([65, 129, 1], C=129, check_state=True)
+    sc.step([1, 1, 1], C=1, check_state=True)
+    sc.step([66, 0, 65], C=66, check_state=True)
+
+
 def test_rows_subset_resets_and_idle_rows():
     sc = Scenario(B=6, max_len=200, Hq=4, Hk=2, D=64, W=16, kinds=[1, 0], seed=6)
     sc.step([10, 20, 0, 5], rows=[4, 0, 2, 5], C=20, check_state=True)
