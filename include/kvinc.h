@@ -259,7 +259,7 @@ int kv_debug_wait_timeout(kv_cache *c, uint32_t limit, void *stream);
  * Host-only schedules, for inspection and tests: the work split that kv_append plans for
  * one call on a layer, computed from the shapes alone -- no cache, no CUDA call, no
  * device work, so they run without a GPU.  Shape arguments as at kv_cache_create, plus
- * num_sms (the device's SM count, which a cache reads from its device), R (the ring
+ * num_sms (the device's SM count, 1..4096, which a cache reads from its device), R (the ring
  * slots of a sliding or hybrid layer, min(W, max_len); ignored when kind = KV_GLOBAL)
  * and kind (the layer's kv_layer_kind).  Both write nothing and return KV_ERR_ARG for
  * a shape kv_cache_create refuses, a NULL array that is needed, or inputs out of range.
