@@ -95,7 +95,12 @@ enum kv_status {
  *    sliding layer  [B][Hk][R + 1][D] bf16         (slot R = scratch)
  * plus lens [B] and lpos [B][R] (int32), a chunk scratch [B][Hk][64][D] for K
  * and V, the RoPE table [max_len][D/2] of (cos, sin) float pairs computed on
- * the host in double, and split-K partials.  All lens start at 0.
+ * the host in double, decode split-K partials (min(B, 512) x 32 x Hq vectors of
+ * D floats) and chunked-prefill key-split partials (min(1024 x SMs,
+ * B x Hq x 64 x 16) vectors of D floats).  Every later call works within this
+ * memory: none allocates device memory except kv_append_host / kv_append_hybrid_host
+ * with pageable buffers (their staging) and kv_step_graph_create (the graph's own
+ * resources, at instantiation).  All lens start at 0.
  * On success *out holds the cache; on failure *out is NULL.
  */
 int kv_cache_create(kv_cache **out, int B, int max_len, int Hq, int Hk, int D, int W,
@@ -167,8 +172,13 @@ int kv_reset(kv_cache *c, const int32_t *rows, int n_rows, void *stream);
  * rule).  lens is NOT advanced: every layer of a step sees the same
  * positions, and the caller ends the step with kv_advance ([P] update/
  * advance, [L]).  Tokens are processed in sub-chunks of 64 per row.
+ * The call allocates nothing and never synchronises: it plans on the host
+ * (lens is mirrored there) and enqueues kernels that use only the memory
+ * reserved by kv_cache_create -- the chunked-prefill key splits are planned to
+ * fit the reserved partials (longer splits when a call would need more).
  * Errors: KV_ERR_FULL if lens[row] + n_new[i] > max_len for any row,
- * KV_ERR_ARG for bad sizes, rows, counts or pointers.
+ * KV_ERR_ARG for bad sizes, rows, counts or pointers, KV_ERR_POOL (paged cache)
+ * when the pool has too few free blocks, KV_ERR_CUDA if a launch fails.
  */
 int kv_append(kv_cache *c, int layer, const void *q, const void *k, const void *v, int Hq,
               int C, const int32_t *n_new, const int32_t *rows, int Bs, void *out,
@@ -202,12 +212,16 @@ int kv_append_hybrid_host(kv_cache *c, int layer, const void *q, const void *k_l
  * (cudaHostAlloc / cudaHostRegister, e.g. torch pin_memory) are read and written
  * by the kernels directly through their device addresses: on GB300 host memory
  * is coherent over NVLink-C2C, so the inputs and outputs cross the link inside
- * the kernels with no copy-engine operation.  Pageable buffers are staged
- * through device buffers the cache owns (allocated on the first such call and
- * grown when a larger call arrives) with cudaMemcpyAsync.  Either way the work
- * is queued on `stream` and the call returns before it finishes: synchronise the
- * stream before reading `out`.  Padding positions of `out` are not written with
- * page-locked buffers and are unspecified with pageable ones.
+ * the kernels with no copy-engine operation; the work is queued on `stream` and
+ * the call returns before it finishes (synchronise the stream before reading
+ * `out`) and, like kv_append, allocates nothing and never synchronises.
+ * Pageable buffers are staged with cudaMemcpyAsync through a device buffer the
+ * cache owns, allocated on the first such call and grown when a larger call
+ * arrives: growing synchronises `stream` (the old buffer may still be in use),
+ * frees it and allocates the new one (KV_ERR_OOM if that fails; the cache is
+ * unchanged), and the copies from and to pageable memory make the call return
+ * only after `stream` has finished it.  Padding positions of `out` are not
+ * written with page-locked buffers and are unspecified with pageable ones.
  */
 int kv_append_host(kv_cache *c, int layer, const void *q, const void *k, const void *v,
                    int Hq, int C, const int32_t *n_new, const int32_t *rows, int Bs,
@@ -288,7 +302,8 @@ int kv_debug_wait_timeout(kv_cache *c, uint32_t limit, void *stream);
  * layer: the group cache, its ring, then the chunk).  *n_entries: the entries; if that
  * is above capacity the call returns KV_ERR_ARG and writes nothing else.  n_splits[i]:
  * the entries of row i; *part_vecs: the partial vectors of the sub-chunk
- * (Hk * n * Hq / Hk per split of a split row).
+ * (Hk * n * Hq / Hk per split of a split row), never above 1024 * num_sms -- the
+ * reserve a cache makes at create -- because splits are lengthened until they fit.
  */
 int kv_plan_decode(int num_sms, int Hq, int Hk, int D, int R, int kind, int n_rows,
                    const int32_t *pos, int32_t *n_splits, int32_t *split_tiles,
@@ -433,10 +448,11 @@ int kv_import_row(kv_cache *c, int row, int keep, const void *src, int64_t bytes
  * caching pool or a fixed arena that forbids allocations from outside it), or a
  * latency-critical loop that must never allocate.  Such a caller cannot create a
  * kv_cache, so it passes its own memory: the cache storage, the queries, the
- * RoPE table and the output.  The call runs the same split-K decode kernel as
- * kv_append, with kv_append's split schedule (kv_plan_decode with kind KV_GLOBAL
- * and pos = n_keys - 1 gives it); its split partials and merge tickets live in
- * one file-scope device array of 18 MiB + 128 KiB + 256 bytes that every GPU
+ * RoPE table, the output and an error word.  The call runs the same split-K
+ * decode kernel as kv_append, with kv_append's split schedule (kv_plan_decode with
+ * kind KV_GLOBAL and pos = n_keys - 1 gives it) except that splits are made longer
+ * when their partials would not fit the scratch; its split partials and merge
+ * tickets live in one file-scope device array of 18 MiB + 128 KiB that every GPU
  * which loads the library holds until the process exits.
  *
  *  K, V        device bf16 [n_cache_rows][Hk][seg_rows][D] (one layer's storage in
@@ -451,24 +467,28 @@ int kv_import_row(kv_cache *c, int row, int keep, const void *src, int64_t bytes
  *              (1 <= n_keys <= seg_rows); the new token's key must already be
  *              stored (global layer: n_keys = pos + 1; ring: min(pos + 1, R))
  *  out         device bf16 [Bs][Hq][D]
+ *  err         device int32, 4-byte aligned, owned by the caller: a kernel whose
+ *              bounded wait timed out sets it to 1 (that call's output is then
+ *              incomplete); the call never clears it, so the caller zeroes it once
+ *              and reads it whenever it synchronises
  *  D is 64 or 128, Hq % Hk == 0, Hq / Hk <= 16.
  *
- * Limits: Bs <= 512, Hk <= 64, and the call's split partials must fit the fixed
- * scratch (16 MiB of float partial outputs, 2 MiB of (max, sum) pairs); a
- * request beyond any limit returns KV_ERR_SCRATCH before any work is enqueued.
+ * Limits: Bs <= 512 and Hk <= 64; a request beyond them returns KV_ERR_SCRATCH
+ * before any work is enqueued.  Within them every call fits the scratch (16 MiB of
+ * float partial outputs, 2 MiB of (max, sum) pairs, merge tickets for 512 x 64
+ * (row, kv head) pairs).
  * Set-up: the first call on each device (made with that device current)
  * resolves the scratch array's device address with cudaGetSymbolAddress and
  * opts the kernels into their shared-memory size, so make that first call
  * before any stream capture.  All calls share the scratch and it keeps the
  * last call's contents: calls whose work overlaps on the GPU (different
  * streams or host threads) race on it and must be ordered by the caller.
- * Each call clears the merge tickets it uses and the error word on `stream`
- * before its kernel.
+ * Each call clears the merge tickets it uses on `stream` before its kernel.
  */
 int kv_decode_noalloc(const void *K, const void *V, int n_cache_rows, int seg_rows, int Hq,
                       int Hk, int D, const void *q, const void *rope, int rope_positions,
                       const int32_t *cache_rows, const int32_t *pos, const int32_t *n_keys,
-                      int Bs, void *out, void *stream);
+                      int Bs, void *out, int32_t *err, void *stream);
 
 /* Static name of a status code. */
 const char *kv_strerror(int code);

@@ -58,7 +58,7 @@ SIGNATURES = {
                                 ctypes.POINTER(c_double)]),
     "kv_decode_noalloc": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_void_p,
                                   c_void_p, c_int, P_i32, P_i32, P_i32, c_int, c_void_p,
-                                  c_void_p]),
+                                  c_void_p, c_void_p]),
     "kv_step_graph_create": (c_int, [c_void_p, ctypes.POINTER(c_void_p), ctypes.POINTER(c_void_p),
                                      ctypes.POINTER(c_void_p), ctypes.POINTER(c_void_p),
                                      ctypes.POINTER(c_void_p), c_int, P_i32, c_int]),

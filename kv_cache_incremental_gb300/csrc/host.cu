@@ -91,6 +91,12 @@ int tc_min_rows(int D) { return D == 64 ? 1 : 64; }
 // kMinSplitBlocks 128-key blocks (rounded up), so a row of up to that many blocks is never
 // split.
 constexpr int kMinSplitBlocks = 4;
+// Prefill key-split partials: a cache reserves room for this many vectors per SM at
+// create (capped by the most its rows can ever need), and the planner lengthens a call's
+// splits until its partials fit.  Load balancing alone stays below about 4 waves of split
+// CTAs (2560 vectors per SM over the three launch kinds); the mixes measured need under
+// 600 per SM (continuous-batch mix at 152 SMs: 78k vectors).
+constexpr int64_t kPrefillPartVecsPerSm = 1024;
 // Decode splits: at most one per kMinDecodeSplitTiles 64-key tiles of a segment (rounded
 // up), so a row of up to that many tiles is one CTA with no split merge, which is what
 // small (ring) layers want (4 measured 10% slower on the long-context step: more
@@ -120,7 +126,7 @@ struct kv_cache {
   int32_t *lpos = nullptr, *err = nullptr, *counters = nullptr;
   float *part_o = nullptr;
   float2 *part_ml = nullptr;
-  // prefill key-split partials ([vector][D] fp32 O, [vector] (m, l)), grown on demand
+  // prefill key-split partials ([vector][D] fp32 O, [vector] (m, l)), reserved at create
   float *ppart_o = nullptr;
   float2 *ppart_ml = nullptr;
   int64_t ppart_cap = 0;  // vectors
@@ -275,10 +281,15 @@ Geom geom_of(const kv_cache *c, int layer) {
 
 }  // namespace
 
-int kvinc::plan_decode_splits(int num_sms, int Hk, int n, const int *nk2, DecodeParams &p) {
+int kvinc::plan_decode_splits(int num_sms, int Hk, int n, const int *nk2, DecodeParams &p,
+                              int max_parts) {
   const auto tiles_of = [](int keys) { return (keys + kTileKeys - 1) / kTileKeys; };
   int64_t total_tiles = 0;
-  for (int i = 0; i < n; ++i) total_tiles += tiles_of(p.rows[i].nk) + tiles_of(nk2[i]);
+  int most_tiles = 1;
+  for (int i = 0; i < n; ++i) {
+    total_tiles += tiles_of(p.rows[i].nk) + tiles_of(nk2[i]);
+    most_tiles = std::max(most_tiles, std::max(tiles_of(p.rows[i].nk), tiles_of(nk2[i])));
+  }
   // Aim for about four waves of two CTAs per SM: `per` tiles per split, at least
   // kMinDecodeSplitTiles.
   const int64_t target = (int64_t)num_sms * 2 * 4;
@@ -292,6 +303,20 @@ int kvinc::plan_decode_splits(int num_sms, int Hk, int n, const int *nk2, Decode
     st = (tiles + ns - 1) / ns;
     return (tiles + st - 1) / st;
   };
+  // Partial slots the schedule at `per` needs (one per split of a row of two or more).
+  const auto parts_at = [&]() {
+    int64_t part = 0;
+    for (int i = 0; i < n; ++i) {
+      int st = 0, st2 = 0;
+      const int ns2 = nk2[i] > 0 ? splits(nk2[i], kMaxSplits / 4, st2) : 0;
+      const int ns = splits(p.rows[i].nk, kMaxSplits - ns2, st);
+      if (ns + ns2 > 1) part += ns + ns2;
+    }
+    return part;
+  };
+  // Fewer, longer splits until the partials fit: at per >= most_tiles every segment is
+  // one split, so only hybrid rows (two segments) still need slots, 2 per row.
+  while (per < most_tiles && parts_at() > max_parts) per *= 2;
   int item = 0, part = 0;
   for (int i = 0; i < n; ++i) {
     DecodeRow &r = p.rows[i];
@@ -339,7 +364,8 @@ void plan_decode(const Geom &g, const std::vector<DecodeIn> &in, DecodeParams &p
     kv_bytes += 2.0 * (r.nk + nk2[i]) * g.Hk * g.D * 2.0;
     flops += 4.0 * (r.nk + nk2[i]) * g.Hq * g.D;
   }
-  plan_decode_splits(g.num_sms, g.Hk, (int)in.size(), nk2.data(), p);
+  // the cache's partial buffer holds kMaxSplits slots per row of a launch: no bound
+  plan_decode_splits(g.num_sms, g.Hk, (int)in.size(), nk2.data(), p, INT32_MAX);
   p.seg0_ring = sliding ? 1 : 0;
   p.ring_R = g.R > 0 ? g.R : 1;
 }
@@ -401,7 +427,7 @@ void fill_decode(const kv_cache *c, int layer, const __nv_bfloat16 *q, const __n
 // each an entry that writes partials at part (vectors counted in *part_vecs), merged
 // afterwards by the rows appended to `merges`.
 std::vector<PrefillRow> split_prefill_rows(const Geom &g, const std::vector<PrefillRow> &sel,
-                                           int rows_per_cta, int ctas_per_sm,
+                                           int rows_per_cta, int ctas_per_sm, int64_t min_per,
                                            std::vector<MergeRow> &merges, int64_t *part_vecs) {
   const bool sliding = g.kind == KV_SLIDING, hybrid = is_hybrid(g.kind);
   const int rep = g.Hq / g.Hk;
@@ -423,8 +449,7 @@ std::vector<PrefillRow> split_prefill_rows(const Geom &g, const std::vector<Pref
   }
   const int64_t cap = (int64_t)g.num_sms * ctas_per_sm;
   const bool split = max_blocks > (work + cap - 1) / cap;
-  const int64_t per =
-      std::max<int64_t>(kMinSplitBlocks, (work + 2 * cap - 1) / (2 * cap));
+  const int64_t per = std::max<int64_t>(min_per, (work + 2 * cap - 1) / (2 * cap));
   std::vector<PrefillRow> out;
   for (PrefillRow r : sel) {
     const int blocks = blocks_of(r);
@@ -468,38 +493,34 @@ int prefill_kind(const Geom &g, int n) {
   return prefill_tc_tiles(g.D, n_rho) == 2 ? 1 : 2;
 }
 
+// Partial vectors a cache reserves for prefill key splits (the planner keeps every call
+// within it): kPrefillPartVecsPerSm per SM, or the most B rows can need (every query
+// vector of a 64-token sub-chunk in kMaxPrefillSplits splits), whichever is smaller.
+int64_t prefill_part_cap(int num_sms) { return kPrefillPartVecsPerSm * num_sms; }
+int64_t prefill_part_reserve(int num_sms, int B, int Hq) {
+  return std::min<int64_t>(prefill_part_cap(num_sms),
+                           (int64_t)B * Hq * kChunk * kMaxPrefillSplits);
+}
+
 // The prefill entries of one sub-chunk, per launch kind, with their key splits; the
-// merges of the split rows and the partial vectors they need.
+// merges of the split rows and the partial vectors they need, at most
+// prefill_part_cap(num_sms): when the load-balancing splits would need more, every split
+// is made longer (the minimum blocks per split doubles) until they fit -- at a minimum
+// of more blocks than any row has, no row is split.
 void plan_prefill(const Geom &g, const std::vector<PrefillRow> &prows,
                   std::vector<PrefillRow> ents[kPrefillKinds], std::vector<MergeRow> &merges,
                   int64_t *part_vecs) {
-  *part_vecs = 0;
-  merges.clear();
-  for (int kind = 0; kind < kPrefillKinds; ++kind) {
-    std::vector<PrefillRow> sel;
-    for (const PrefillRow &r : prows)
-      if (prefill_kind(g, r.n) == kind) sel.push_back(r);
-    ents[kind] = split_prefill_rows(g, sel, kRowsPerCta[kind], kCtasPerSm[kind], merges,
-                                    part_vecs);
+  std::vector<PrefillRow> sel[kPrefillKinds];
+  for (const PrefillRow &r : prows) sel[prefill_kind(g, r.n)].push_back(r);
+  const int64_t cap = prefill_part_cap(g.num_sms);
+  for (int64_t min_per = kMinSplitBlocks;; min_per *= 2) {
+    *part_vecs = 0;
+    merges.clear();
+    for (int kind = 0; kind < kPrefillKinds; ++kind)
+      ents[kind] = split_prefill_rows(g, sel[kind], kRowsPerCta[kind], kCtasPerSm[kind], min_per,
+                                      merges, part_vecs);
+    if (*part_vecs <= cap || merges.empty()) return;
   }
-}
-
-// Room for n prefill partial vectors.  Growing waits for the work queued on s (the old
-// buffer may be in use).
-int ensure_prefill_parts(kv_cache *c, int64_t n, cudaStream_t s) {
-  if (n <= 0 || n <= c->ppart_cap) return KV_OK;
-  if ((c->ppart_o || c->ppart_ml) && cudaStreamSynchronize(s) != cudaSuccess) return KV_ERR_CUDA;
-  cudaFree(c->ppart_o);
-  cudaFree(c->ppart_ml);
-  c->ppart_o = nullptr;
-  c->ppart_ml = nullptr;
-  c->ppart_cap = 0;
-  const int64_t cap = std::max<int64_t>(n, 1 << 16);
-  if (cudaMalloc((void **)&c->ppart_o, cap * c->D * sizeof(float)) != cudaSuccess ||
-      cudaMalloc((void **)&c->ppart_ml, cap * sizeof(float2)) != cudaSuccess)
-    return KV_ERR_OOM;
-  c->ppart_cap = cap;
-  return KV_OK;
 }
 
 // One layer's chunk for rows `cache_rows`.  k, v: the keys and values of the layer
@@ -527,18 +548,6 @@ int append_device(kv_cache *c, int layer, const __nv_bfloat16 *q, const __nv_bfl
                         std::min(kChunk, n_new[i] - off), 0});
     return rows;
   };
-  {  // room for every sub-chunk's prefill partials before anything is enqueued or taken
-    int64_t most = 0;
-    for (int off = 0; off < max_n; off += kChunk) {
-      std::vector<PrefillRow> ents[kPrefillKinds];
-      std::vector<MergeRow> merges;
-      int64_t vecs = 0;
-      plan_prefill(geom_of(c, layer), chunk_rows(off), ents, merges, &vecs);
-      most = std::max(most, vecs);
-    }
-    const int rc = ensure_prefill_parts(c, most, s);
-    if (rc != KV_OK) return rc;
-  }
   if (c->n_blocks > 0) {  // pool blocks for the new positions, before anything is enqueued
     std::vector<std::pair<int, int>> want;
     for (int i = 0; i < Bs; ++i)
@@ -621,12 +630,8 @@ int append_device(kv_cache *c, int layer, const __nv_bfloat16 *q, const __nv_bfl
     // ---- chunked prefill (+ ring commit on sliding layers), in launches of each kind
     std::vector<PrefillRow> ents[kPrefillKinds];
     std::vector<MergeRow> merges;
-    int64_t part_vecs = 0;
+    int64_t part_vecs = 0;  // within the reserve made at create (the planner's bound)
     plan_prefill(geom_of(c, layer), prows, ents, merges, &part_vecs);
-    if (part_vecs > 0) {  // the room made before the first sub-chunk: no allocation here
-      const int rc = ensure_prefill_parts(c, part_vecs, s);
-      if (rc != KV_OK) return rc;
-    }
     for (int kind = 0; kind < kPrefillKinds; ++kind) {
       const std::vector<PrefillRow> &sel = ents[kind];
       for (size_t r0 = 0; r0 < sel.size(); r0 += kMaxRowsPerLaunch) {
@@ -968,6 +973,12 @@ static int create_impl(kv_cache **out, int B, int max_len, int Hq, int Hk, int D
   // decode partial slots are numbered per launch (at most kMaxRowsPerLaunch rows)
   const size_t parts = (size_t)std::min(B, kMaxRowsPerLaunch) * kMaxSplits * Hq;
   if (!alloc((void **)&c->part_o, parts * D * 4) || !alloc((void **)&c->part_ml, parts * 8))
+    return fail(KV_ERR_OOM);
+  // prefill key-split partials: every call's plan fits (plan_prefill), so kv_append never
+  // allocates
+  c->ppart_cap = prefill_part_reserve(c->num_sms, B, Hq);
+  if (!alloc((void **)&c->ppart_o, (size_t)c->ppart_cap * D * 4) ||
+      !alloc((void **)&c->ppart_ml, (size_t)c->ppart_cap * 8))
     return fail(KV_ERR_OOM);
   if (cudaDeviceSynchronize() != cudaSuccess) return fail(KV_ERR_CUDA);
   if (const char *log = std::getenv("KVINC_LOG")) {

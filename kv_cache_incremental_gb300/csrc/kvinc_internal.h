@@ -292,7 +292,11 @@ cudaError_t launch_table(const TableParams &p, cudaStream_t s);
 // 0 and nk2[i] slots of segment 1 (0: none).  Sets each row's splits, tiles per split,
 // first item and first partial slot, and p.n_rows, p.n_items, p.uniform_items, aiming at
 // about four waves of two CTAs per SM over Hk kv heads; returns the partial slots used.
-int plan_decode_splits(int num_sms, int Hk, int n, const int *nk2, DecodeParams &p);
+// When that schedule would use more than max_parts partial slots the splits are made
+// longer (down to one per segment) until it does not; only rows with two segments (a
+// hybrid layer) then still use slots, two each.
+int plan_decode_splits(int num_sms, int Hk, int n, const int *nk2, DecodeParams &p,
+                       int max_parts);
 cudaError_t launch_append(const AppendParams &p, cudaStream_t s);
 cudaError_t launch_decode(const DecodeParams &p, int D, int n_tiles_heads, cudaStream_t s);
 // Graph kernel-node descriptions of the decode and state launches (args: one-slot storage

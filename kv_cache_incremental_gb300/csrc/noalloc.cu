@@ -3,16 +3,19 @@
 // Some callers cannot call cudaMalloc at all: processes whose device memory is
 // owned by another allocator (a framework's caching pool or a fixed arena that
 // forbids allocations from outside it), or latency-critical loops that must not
-// allocate.  Such a caller owns the K/V storage, the queries, the RoPE table and
-// the output; this entry point runs the same split-K decode kernel as kv_append,
-// with its split partials and merge tickets in the file-scope device array below
-// instead of memory from kv_cache_create.
+// allocate.  Such a caller owns the K/V storage, the queries, the RoPE table, the
+// output and an error word; this entry point runs the same split-K decode kernel
+// as kv_append, with its split partials and merge tickets in the file-scope device
+// array below instead of memory from kv_cache_create.
 //
 // The array is fixed at kNoallocScratchBytes; every GPU that loads the library
 // holds it until the process exits.  All calls share it and it keeps the last
 // call's contents, so calls whose work overlaps on the GPU (two streams, or two
-// host threads) race on it.  The merge tickets and the error word must start at
-// zero: each call clears the ones it uses on its stream before the kernel runs.
+// host threads) race on it.  The merge tickets must start at zero: each call
+// clears the ones it uses on its stream before the kernel runs.  The split
+// schedule is kv_append's, with splits made longer when the partials of a call
+// would not fit the array, so every call within the row and head limits fits.
+#include <algorithm>
 #include <cmath>
 #include <mutex>
 
@@ -31,8 +34,7 @@ constexpr int kNoallocMaxHk = 64;                  // kv heads per call
 constexpr size_t kPartOBytes = size_t(16) << 20;   // float partial outputs: 4 Mi floats
 constexpr size_t kPartMLBytes = size_t(2) << 20;   // float2 (m, l): 256 Ki entries
 constexpr size_t kTicketBytes = size_t(kMaxRowsPerLaunch) * kNoallocMaxHk * 4;  // 128 KiB
-constexpr size_t kErrBytes = 256;                  // device error word
-constexpr size_t kNoallocScratchBytes = kPartOBytes + kPartMLBytes + kTicketBytes + kErrBytes;
+constexpr size_t kNoallocScratchBytes = kPartOBytes + kPartMLBytes + kTicketBytes;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
@@ -70,17 +72,20 @@ int setup_device(int dev, unsigned char **scratch, int *num_sms) {
   return KV_OK;
 }
 
+EncodeTiledFn g_encode_fn = nullptr;
+std::once_flag g_encode_once;
+
 bool encode(CUtensorMap *m, const void *base, int64_t rows, int D) {
-  static EncodeTiledFn fn = nullptr;
-  if (!fn) {
+  std::call_once(g_encode_once, [] {
     void *p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      return false;
-    fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode_fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  const EncodeTiledFn fn = g_encode_fn;
+  if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)D * 2};
   cuuint32_t box[2] = {64, (cuuint32_t)kTileKeys};
@@ -98,14 +103,16 @@ extern "C" int kv_decode_noalloc(const void *K, const void *V, int n_cache_rows,
                                  int Hq, int Hk, int D, const void *q, const void *rope,
                                  int rope_positions, const int32_t *cache_rows,
                                  const int32_t *pos, const int32_t *n_keys, int Bs, void *out,
-                                 void *stream) {
-  if (!K || !V || !q || !rope || !out || !cache_rows || !pos || !n_keys) return KV_ERR_ARG;
+                                 int32_t *err, void *stream) {
+  if (!K || !V || !q || !rope || !out || !err || !cache_rows || !pos || !n_keys)
+    return KV_ERR_ARG;
   if (n_cache_rows < 1 || seg_rows < 1 || Hk < 1 || Hq < 1 || Hq % Hk != 0 ||
       Hq / Hk > kMaxRep || (D != 64 && D != 128) || rope_positions < 1 || Bs < 1)
     return KV_ERR_ARG;
   if (Hk > kNoallocMaxHk) return KV_ERR_SCRATCH;
   if ((int64_t)n_cache_rows * Hk * seg_rows >= (1LL << 31)) return KV_ERR_ARG;
-  if (!aligned16(K) || !aligned16(V) || !aligned16(q) || !aligned16(out) || !aligned16(rope))
+  if (!aligned16(K) || !aligned16(V) || !aligned16(q) || !aligned16(out) || !aligned16(rope) ||
+      (reinterpret_cast<uintptr_t>(err) & 3u) != 0)
     return KV_ERR_ARG;
   if (Bs > kMaxRowsPerLaunch) return KV_ERR_SCRATCH;
   for (int i = 0; i < Bs; ++i) {
@@ -136,17 +143,15 @@ extern "C" int kv_decode_noalloc(const void *K, const void *V, int n_cache_rows,
     r.nk = n_keys[i];
     r.ctr = i;
   }
-  const int part = plan_decode_splits(num_sms, Hk, Bs, kNoRing, dp);
-  // The partials of this call must fit the fixed scratch.
-  if ((size_t)part * Hq * D * sizeof(float) > kPartOBytes ||
-      (size_t)part * Hq * sizeof(float2) > kPartMLBytes)
-    return KV_ERR_SCRATCH;
+  // The partials of a call must fit the fixed scratch: the planner lengthens the splits
+  // until they do (one split per row needs no partial slot at all).
+  const int max_parts = (int)std::min(kPartOBytes / ((size_t)Hq * D * sizeof(float)),
+                                      kPartMLBytes / ((size_t)Hq * sizeof(float2)));
+  plan_decode_splits(num_sms, Hk, Bs, kNoRing, dp, max_parts);
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int32_t *tickets = reinterpret_cast<int32_t *>(scratch + kPartOBytes + kPartMLBytes);
-  int32_t *err = reinterpret_cast<int32_t *>(scratch + kPartOBytes + kPartMLBytes + kTicketBytes);
-  if (cudaMemsetAsync(tickets, 0, (size_t)Bs * Hk * sizeof(int32_t), s) != cudaSuccess ||
-      cudaMemsetAsync(err, 0, sizeof(int32_t), s) != cudaSuccess)
+  if (cudaMemsetAsync(tickets, 0, (size_t)Bs * Hk * sizeof(int32_t), s) != cudaSuccess)
     return KV_ERR_CUDA;
 
   dp.q = static_cast<const __nv_bfloat16 *>(q);
@@ -157,7 +162,7 @@ extern "C" int kv_decode_noalloc(const void *K, const void *V, int n_cache_rows,
   dp.part_o = reinterpret_cast<float *>(scratch);
   dp.part_ml = reinterpret_cast<float2 *>(scratch + kPartOBytes);
   dp.counters = tickets;
-  dp.err = err;
+  dp.err = err;  // the caller's word: set to 1 by a timed-out wait, never cleared here
   dp.k_new = nullptr;
   dp.v_new = nullptr;
   dp.kv_row_stride = 0;

@@ -8,6 +8,14 @@ sequences a row has held (it advances on every reset).
 Hybrid layers (kinds 2 = group's full layer, 3 = a local layer of the group): a layer's
 own q/k/v streams feed its query and ring; the group's global keys and values are the
 streams KG/VG of the group's full layer.
+
+A row's history is a list of spans (p0, p1, seed, row, seq): positions p0 <= p < p1 came
+from that stream.  A fresh or reset row has one open span of its own; a row that became a
+prefix of another row (kv_copy_rows, kv_import_row) takes the source's spans up to the
+kept length, then continues with a fresh stream of its own.
+
+q_scale (a power of two) multiplies every query exactly (an exponent shift in bf16), so
+scores leave the N(0,1) range by that factor: the oracle receives the same scaled bits.
 """
 from __future__ import annotations
 
@@ -17,6 +25,7 @@ import oracle
 import synth
 
 TOL_ABS, TOL_REL = 2e-3, 1e-2  # |err| <= 2e-3 + 1e-2 |ref|, elementwise
+_OPEN = 1 << 62                # end of a row's last history span
 
 
 def bf16_bits_to_torch(bits, device):
@@ -48,7 +57,7 @@ class Scenario:
     """One cache plus the bookkeeping needed to regenerate every row's history."""
 
     def __init__(self, B, max_len, Hq, Hk, D, W=0, kinds=(0,), theta=1e4, seed=0, device=0,
-                 pad_value=None, paged_blocks=None):
+                 pad_value=None, paged_blocks=None, q_scale=1):
         import kv_cache_incremental_gb300 as kvi
         self.kvi = kvi
         self.cache = kvi.KVCache(B, max_len, Hq, Hk, D, W, list(kinds), theta, device,
@@ -60,6 +69,10 @@ class Scenario:
         self.lens = [0] * B
         self.seq = [0] * B
         self.pad_value = pad_value  # None: generator values at pad positions; else a constant
+        self.q_scale = q_scale
+        assert q_scale > 0 and np.log2(q_scale) == np.round(np.log2(q_scale)), \
+            "q_scale must be a power of two"
+        self.spans = [[(0, _OPEN, seed, b, 0)] for b in range(B)]
         self.max_ratio = 0.0
         self.group, f = [], -1      # full layer of each hybrid layer's group, else -1
         for kind in self.kinds:
@@ -68,8 +81,60 @@ class Scenario:
 
     # ------------------------------------------------------------------ inputs
     def gen(self, tensor, layer, row, positions, H):
-        return synth.normal_bf16(self.seed, tensor, layer, row, self.seq[row], positions, H,
-                                 self.D)
+        positions = np.asarray(positions, dtype=np.int64).reshape(-1)
+        spans = self.spans[row]
+        if len(spans) == 1:
+            _, _, seed, srow, sseq = spans[0]
+            x = synth.normal_bf16(seed, tensor, layer, srow, sseq, positions, H, self.D)
+        else:
+            x = np.empty((positions.size, H, self.D), np.uint16)
+            for p0, p1, seed, srow, sseq in spans:
+                m = (positions >= p0) & (positions < p1)
+                if m.any():
+                    x[m] = synth.normal_bf16(seed, tensor, layer, srow, sseq, positions[m], H,
+                                             self.D)
+        if tensor == synth.Q and self.q_scale != 1:
+            x = oracle.f32_to_bf16(oracle.bf16_to_f32(x) * np.float32(self.q_scale))
+        return x
+
+    def _fresh_stream(self, b):
+        """Row b starts a new sequence: a stream no earlier sequence of the row used."""
+        self.seq[b] += 1
+        return (self.seed, b, self.seq[b])
+
+    def mark_reset(self, rows):
+        """Bookkeeping of a kv_reset of `rows`: empty, each with a fresh stream."""
+        for b in rows:
+            self.lens[b] = 0
+            seed, r, q = self._fresh_stream(b)
+            self.spans[b] = [(0, _OPEN, seed, r, q)]
+
+    def prefix_spans(self, b, keep):
+        """Spans of row b's first `keep` positions."""
+        return [(p0, min(p1, keep), seed, r, q) for p0, p1, seed, r, q in self.spans[b]
+                if p0 < keep]
+
+    def adopt(self, b, spans, keep):
+        """Row b now holds `keep` positions from `spans` (a copy or an import): its history is
+        those spans, then a fresh stream of its own from position keep on."""
+        seed, r, q = self._fresh_stream(b)
+        self.spans[b] = list(spans) + [(keep, _OPEN, seed, r, q)]
+        self.lens[b] = keep
+
+    def copy_rows(self, src, src_rows, dst_rows, keep=None):
+        """kv_copy_rows from Scenario `src` (may be self) into this one, with the histories."""
+        self.cache.copy_rows(src.cache, src_rows=list(src_rows), dst_rows=list(dst_rows),
+                             keep=None if keep is None else list(keep))
+        kept = [src.lens[s] if keep is None else k
+                for s, k in zip(src_rows, keep or [None] * len(src_rows))]
+        spans = [src.prefix_spans(s, k) for s, k in zip(src_rows, kept)]
+        for d, sp, k in zip(dst_rows, spans, kept):
+            self.adopt(d, sp, k)
+
+    def import_row(self, row, buf, keep, src, src_row):
+        """kv_import_row of a buffer exported from row src_row of Scenario `src`."""
+        self.cache.import_row(row, buf, keep=keep)
+        self.adopt(row, src.prefix_spans(src_row, keep), keep)
 
     def chunk_inputs(self, layer, rows, n_new, C):
         Bs = len(rows)
@@ -125,9 +190,7 @@ class Scenario:
         rows_eff = list(range(len(n_new))) if rows is None else list(rows)
         if resets:
             self.cache.reset(list(resets))
-            for b in resets:
-                self.lens[b] = 0
-                self.seq[b] += 1
+            self.mark_reset(resets)
         C = C or max(1, max(n_new))
         outs = []
         for layer in range(len(self.kinds)):

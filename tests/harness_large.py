@@ -3,6 +3,10 @@
 The counter-based generator fixes every q/k/v value by (seed, tensor, layer, row, seq,
 position, head, d), so the oracle regenerates exactly the history of the rows and
 layers it samples; nothing of the GPU path is stored or reused as an expected value.
+Long histories are regenerated with the generator's device form (synth.fill_torch: the
+same integer arithmetic, bit-identical to the numpy form by
+tests/test_synth.py::test_device_generator_matches_numpy), which is input generation,
+not the library under test.
 """
 from __future__ import annotations
 
@@ -68,6 +72,16 @@ class LargeScenario:
             self.step(n, C)
 
     # ------------------------------------------------------------------ checks
+    def hist(self, tensor, layer, b, s, lo, hi, H):
+        """Generator values of positions [lo, hi) of row b, sequence s: uint16 [n][H][D]."""
+        if hi - lo <= 2048:
+            return synth.normal_bf16(self.seed, tensor, layer, b, s, np.arange(lo, hi), H,
+                                     self.D)
+        import torch
+        x = torch.empty((1, hi - lo, H, self.D), dtype=torch.bfloat16, device=self.dev)
+        synth.fill_torch(x, self.seed, tensor, layer, [b], [s], [lo])
+        return torch_to_bits(x)[0]
+
     def check_outputs(self, out, layer, rows, n_new, lens_before):
         """Every output element of the sampled rows of one layer against the oracle."""
         bits = torch_to_bits(out)
@@ -78,12 +92,11 @@ class LargeScenario:
                 continue
             L = int(lens_before[b])
             lo = max(0, L - (W - 1)) if W else 0
-            hist = np.arange(lo, L + n)
             s = int(self.seq[b])
             q = synth.normal_bf16(self.seed, synth.Q, layer, b, s, np.arange(L, L + n), self.Hq,
                                   self.D)
-            kh = synth.normal_bf16(self.seed, synth.K, layer, b, s, hist, self.Hk, self.D)
-            vh = synth.normal_bf16(self.seed, synth.V, layer, b, s, hist, self.Hk, self.D)
+            kh = self.hist(synth.K, layer, b, s, lo, L + n, self.Hk)
+            vh = self.hist(synth.V, layer, b, s, lo, L + n, self.Hk)
             ref = oracle.attend(q, np.arange(L, L + n), kh, vh, lo, self.Hq, self.Hk, W=W,
                                 theta=self.theta)
             r = check_close(bits[b, :n], ref, f"layer {layer} row {b} lens {L} n {n}")

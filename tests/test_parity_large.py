@@ -30,19 +30,50 @@ def test_config3_decode_bandwidth_full_size():
 
 def test_config4_long_context_mixed_layout():
     """12 layers (5 and 11 global, the rest sliding W=512), B=16, Hq=64, Hk=8, D=128,
-    max_len=32768, lens uniform in [16384, 32768 - steps], single-token decode steps."""
+    max_len=32768, lens uniform in [16384, 32768 - steps], single-token decode steps.
+
+    The cache fill (64-token chunks) is sampled whole-chunk: all 64 query positions of a
+    row on a sliding and a global layer, for each kind of launch the planner makes on the
+    way -- rows of equal length in two-tile tcgen05 CTAs (the call at 16384), a row cut
+    into key splits merged afterwards (late calls, when few rows are still filling), and
+    a row's last partial chunk of 5 tokens (5 x 8 query rows: the mma.sync kernel)."""
+    import torch
+    import kv_cache_incremental_gb300 as kvi
     rng = np.random.default_rng(4)
     kinds = [1, 1, 1, 1, 1, 0, 1, 1, 1, 1, 1, 0]
     sc = LargeScenario(B=16, max_len=32768, Hq=64, Hk=8, D=128, W=512, kinds=kinds, seed=44)
     targets = rng.integers(16384, 32768 - 8, size=16)
-    # sample the chunked-prefill outputs of one fill call midway
+    targets[2] = 16384 + 64 * 40 + 5          # its last fill chunk has 5 tokens
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
     sc.fill_to(np.minimum(targets, 16384))
     kept, lens_before = sc.step(np.minimum(64, targets - sc.lens).tolist(), C=64,
                                 keep_layers=(0, 5))
     n_fill = (sc.lens - lens_before).tolist()
     sc.check_outputs(kept[5], 5, [3], n_fill, lens_before)
     sc.check_outputs(kept[0], 0, [3, 7], n_fill, lens_before)
-    sc.fill_to(targets)
+    seen_split = seen_small = False
+    while (sc.lens < targets).any():
+        n = np.minimum(64, targets - sc.lens)
+        act = np.nonzero(n > 0)[0]
+        plan = kvi.plan_prefill(sms, 64, 8, 128, 0, 0, sc.lens[act].tolist(), n[act].tolist())
+        split_rows = [int(act[i]) for i, k in enumerate(plan["n_splits"]) if k > 1]
+        want_split = bool(split_rows) and not seen_split
+        want_small = n[2] == 5 and not seen_small
+        if not (want_split or want_small):
+            sc.step(n.tolist(), C=64)
+            continue
+        kept, lens_before = sc.step(n.tolist(), C=64, keep_layers=(5, 6, 10, 11))
+        if want_split:
+            seen_split = True
+            b = split_rows[0]
+            sc.check_outputs(kept[5], 5, [b], n.tolist(), lens_before)
+            sc.check_outputs(kept[6], 6, [b], n.tolist(), lens_before)
+        if want_small:
+            seen_small = True
+            assert plan["kind"][plan["row"].index(int(np.nonzero(act == 2)[0][0]))] == 0
+            sc.check_outputs(kept[11], 11, [2], n.tolist(), lens_before)
+            sc.check_outputs(kept[10], 10, [2], n.tolist(), lens_before)
+    assert seen_split and seen_small
     for step in range(2):
         kept, lens_before = sc.step([1] * 16, C=1, keep_layers=(0, 5, 6, 11))
         sc.check_outputs(kept[5], 5, [1, 9], [1] * 16, lens_before)
@@ -62,7 +93,7 @@ def test_config5_continuous_batch_mix():
     B = 128
     sc = LargeScenario(B=B, max_len=16384, Hq=16, Hk=4, D=64, W=1024, kinds=kinds, seed=55)
     sc.fill_to(rng.integers(0, 12001, size=B))
-    for step in range(6):
+    for step in range(20):
         resets = rng.choice(B, size=max(1, B // 20), replace=False)
         u = rng.random(B)
         n = np.where(u < 0.4, 1, np.where(u < 0.7, 0, rng.integers(2, 65, size=B)))
@@ -75,6 +106,8 @@ def test_config5_continuous_batch_mix():
             if len(idx):
                 pick.append(int(rng.choice(idx)))
         pick += rng.choice(B, size=2, replace=False).tolist()
-        for layer in (0, 1) if step % 2 == 0 else (2, 3):
-            sc.check_outputs(kept[layer], layer, sorted(set(pick)), n, lens_before)
+        if step % 3 == 0 or step == 19:
+            for layer in (0, 1) if step % 2 == 0 else (2, 3):
+                sc.check_outputs(kept[layer], layer, sorted(set(pick)), n, lens_before)
     sc.check_state(sorted(set(pick)), [0, 1, 2, 3])
+    sc.check_state(rng.choice(B, size=12, replace=False).tolist(), [0, 1, 2, 3])

@@ -19,6 +19,7 @@ MAX_RING_SPLITS = 8    # decode: splits of a hybrid layer's ring
 MIN_DECODE_TILES = 8   # decode: at most one split per this many tiles
 MAX_PREFILL_SPLITS = 16
 MIN_PREFILL_BLOCKS = 4  # prefill: at most one split per this many 128-key blocks
+PART_VECS_PER_SM = 1024  # prefill: key-split partial vectors a cache reserves per SM
 INF = 2**31 - 1
 
 
@@ -149,6 +150,46 @@ def expected_kind(kind, Hq, Hk, D, n):
     return 1 if (kind in (FULL, LOCAL) or n * Hq // Hk >= 64) else 0
 
 
+PER_CTA, PER_SM = {0: 64, 1: 256, 2: 128}, {0: 2, 1: 1, 2: 2}
+
+
+def planned_splits(num_sms, Hq, Hk, D, R, kind, lens, n, min_per):
+    """Splits per row of the documented rule at a minimum of min_per blocks per split:
+    within each launch kind, rows are split only when the longest row outweighs the
+    average load per SM, into at most 16 pieces of about max(min_per, half that load)."""
+    rep = Hq // Hk
+    blocks = [-(-key_tiles(kind, R, lens[i], n[i]) // 2) for i in range(len(lens))]
+    ns_all = [1] * len(lens)
+    for kd in range(3):
+        sel = [i for i in range(len(lens)) if expected_kind(kind, Hq, Hk, D, n[i]) == kd]
+        if not sel:
+            continue
+        work = sum(-(-n[i] * rep // PER_CTA[kd]) * Hk * blocks[i] for i in sel)
+        cap = num_sms * PER_SM[kd]
+        if max(blocks[i] for i in sel) <= -(-work // cap):
+            continue
+        per = max(min_per, -(-work // (2 * cap)))
+        for i in sel:
+            ns = min(MAX_PREFILL_SPLITS, -(-blocks[i] // per))
+            if ns > 1:
+                bs = -(-blocks[i] // ns)
+                ns = -(-blocks[i] // bs)
+            ns_all[i] = max(1, ns)
+    return ns_all
+
+
+def reserve_min_per(num_sms, Hq, Hk, D, R, kind, lens, n):
+    """The smallest minimum split length (4, 8, 16, ...) whose splits fit the partial
+    vectors a cache reserves (PART_VECS_PER_SM per SM), as the planner chooses it."""
+    min_per = MIN_PREFILL_BLOCKS
+    while True:
+        ns = planned_splits(num_sms, Hq, Hk, D, R, kind, lens, n, min_per)
+        vecs = sum(k * n[i] * Hq for i, k in enumerate(ns) if k > 1)
+        if vecs <= PART_VECS_PER_SM * num_sms or max(ns, default=1) == 1:
+            return min_per, ns
+        min_per *= 2
+
+
 def check_prefill(num_sms, Hq, Hk, D, R, kind, lens, n):
     p = kvi.plan_prefill(num_sms, Hq, Hk, D, R, kind, lens, n)
     rep = Hq // Hk
@@ -159,8 +200,12 @@ def check_prefill(num_sms, Hq, Hk, D, R, kind, lens, n):
     # launch order: kind by kind, input order within a kind
     order = [(p["kind"][j], p["row"][j]) for j in range(len(p["row"]))]
     assert order == sorted(order)
+    # the partials fit the reserve of a cache on this many SMs
+    assert p["part_vecs"] <= PART_VECS_PER_SM * num_sms
+    min_per, want_ns = reserve_min_per(num_sms, Hq, Hk, D, R, kind, lens, n)
+    assert p["n_splits"] == want_ns
     # the split decision and the share bound of a launch kind
-    per_cta, per_sm = {0: 64, 1: 256, 2: 128}, {0: 2, 1: 1, 2: 2}
+    per_cta, per_sm = PER_CTA, PER_SM
     blocks = [-(-key_tiles(kind, R, lens[i], n[i]) // 2) for i in range(rows)]
     spans = []
     for kd in range(3):
@@ -170,7 +215,7 @@ def check_prefill(num_sms, Hq, Hk, D, R, kind, lens, n):
         work = sum(-(-n[i] * rep // per_cta[kd]) * Hk * blocks[i] for i in sel)
         cap = num_sms * per_sm[kd]
         split_any = max(blocks[i] for i in sel) > -(-work // cap)
-        share = max(MIN_PREFILL_BLOCKS, -(-work // (2 * cap)))
+        share = max(min_per, -(-work // (2 * cap)))
         for i in sel:
             ns = p["n_splits"][i]
             if not split_any:
@@ -261,3 +306,41 @@ def test_prefill_rejects_bad_rows():
         kvi.plan_prefill(152, 8, 2, 64, 0, 7, [5], [3])
     p = kvi.plan_prefill(152, 8, 2, 64, 0, GLOBAL, [], [])
     assert p["row"] == [] and p["part_vecs"] == 0
+
+
+def test_prefill_partials_fit_the_create_reserve():
+    """kv_append allocates nothing: every sub-chunk's key-split partials fit the vectors a
+    cache reserves at create, min(1024 x SMs, B x Hq x 64 x 16).  Shapes that would need
+    more (few SMs, long rows among short ones, wide GQA groups) get longer splits, down
+    to none."""
+    # Both launch kinds of D = 128 splitting at once: 64-token rows (two 128-row tiles per
+    # CTA) and 15-token rows (mma.sync) behind one row at the largest length.  The
+    # load-balancing rule alone asks for 1.32 x the reserve of 152 SMs.
+    lens = [(1 << 20) - 64] + [361816] * 147 + [527055] * 149
+    n = [64] * 148 + [15] * 149
+    natural = planned_splits(152, 8, 2, 128, 0, GLOBAL, lens, n, MIN_PREFILL_BLOCKS)
+    vecs = sum(k * n[i] * 8 for i, k in enumerate(natural) if k > 1)
+    assert vecs > 1.3 * PART_VECS_PER_SM * 152
+    p = check_prefill(152, 8, 2, 128, 0, GLOBAL, lens, n)
+    assert 0 < p["part_vecs"] <= PART_VECS_PER_SM * 152 and max(p["n_splits"]) > 1
+    # random long/short row mixes on any SM count
+    rng = np.random.default_rng(5)
+    worst = 0
+    for _ in range(400):
+        num_sms = int(rng.choice([1, 2, 8, 16, 152, 4096]))
+        Hk = int(rng.choice([1, 2, 4, 8, 16]))
+        rep = int(rng.choice([1, 2, 4, 8, 16]))
+        D = int(rng.choice([64, 128]))
+        kind = int(rng.integers(0, 4))
+        R = int(rng.integers(1, 1 << 20))
+        rows = int(rng.integers(1, 513))
+        n_long = int(rng.integers(1, rows + 1))
+        lens = ([int(x) for x in rng.integers((1 << 20) - 2 ** 18, (1 << 20) - 64, n_long)]
+                + [int(x) for x in rng.integers(0, 1 << int(rng.integers(1, 16)),
+                                                rows - n_long)])
+        n = [64 if rng.random() < 0.7 else int(rng.integers(1, 65)) for _ in range(rows)]
+        p = check_prefill(num_sms, Hk * rep, Hk, D, R, kind, lens, n)
+        reserve = min(PART_VECS_PER_SM * num_sms, rows * Hk * rep * 64 * MAX_PREFILL_SPLITS)
+        assert p["part_vecs"] <= reserve
+        worst = max(worst, p["part_vecs"] / (PART_VECS_PER_SM * num_sms))
+    assert worst > 0.5       # the search reached the bound's neighbourhood

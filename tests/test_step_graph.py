@@ -91,8 +91,7 @@ def test_graph_row_subset_and_reset_between_launches():
         if it == 2:
             for sc in (a, b):
                 sc.cache.reset([1])
-                sc.lens[1] = 0
-                sc.seq[1] += 1
+                sc.mark_reset([1])
         outs_a = a.step([1] * 3, rows, C=1)
         qs, outs_b = _graph_step(b, g, bufs, rows)
         for layer in range(2):

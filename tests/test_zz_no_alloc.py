@@ -1,11 +1,12 @@
 """kv_decode_noalloc: the decode entry point for callers that cannot call cudaMalloc.
 
 Such callers (a process whose device memory belongs to another allocator, or a loop
-that must never allocate) pass their own cache storage, queries, RoPE table and
-output; the split partials live in the library's fixed device scratch.  These tests
-call it through the C ABI and compare it with kv_append, the entry point that uses
-memory from kv_cache_create, on two decode calls in a row.  This file is collected
-last so that a run stopping at the first failure has already run every other test.
+that must never allocate) pass their own cache storage, queries, RoPE table, output and
+error word; the split partials live in the library's fixed device scratch.  These tests
+call it through the C ABI on two decode calls in a row and check its output against the
+oracle (cache-free attention over each row's history) and against kv_append, the entry
+point that uses memory from kv_cache_create.  This file is collected last so that a run
+stopping at the first failure has already run every other test.
 """
 import ctypes
 
@@ -13,6 +14,7 @@ import numpy as np
 import pytest
 
 import oracle
+import synth
 from harness import Scenario, bf16_bits_to_torch, check_close, torch_to_bits
 
 pytestmark = pytest.mark.gpu
@@ -29,19 +31,42 @@ def _rope_table(max_len, D, theta):
     return torch.from_numpy(tab).to("cuda")
 
 
-def test_noalloc_decode_matches_kv_append_on_two_calls():
+def _call(lib, K, V, n_cache_rows, seg_rows, Hq, Hk, D, q, rope, rope_positions, rows, pos,
+          n_keys, out, err, stream=None):
+    return lib.kv_decode_noalloc(K.data_ptr(), V.data_ptr(), n_cache_rows, seg_rows, Hq, Hk, D,
+                                 q.data_ptr(), rope.data_ptr(), rope_positions, _i32(rows),
+                                 _i32(pos), _i32(n_keys), len(rows), out.data_ptr(),
+                                 None if err is None else err.data_ptr(),
+                                 ctypes.c_void_p(stream))
+
+
+CASES = [
+    # D, Hq, Hk, layer kind (0 global cache, 1 sliding ring), W
+    pytest.param(128, 16, 4, 0, 0, id="d128-rep4-global"),
+    pytest.param(64, 16, 4, 0, 0, id="d64-rep4-global"),
+    pytest.param(128, 32, 2, 0, 0, id="d128-rep16-global"),
+    pytest.param(64, 32, 2, 1, 200, id="d64-rep16-ring"),
+    pytest.param(128, 16, 4, 1, 96, id="d128-rep4-ring"),
+]
+
+
+@pytest.mark.parametrize("D,Hq,Hk,kind,W", CASES)
+def test_noalloc_decode_matches_oracle_and_kv_append_on_two_calls(D, Hq, Hk, kind, W):
     import torch
     from kv_cache_incremental_gb300 import _lib
     lib = _lib.load()
-    B, max_len, Hq, Hk, D = 6, 3000, 16, 4, 128
-    sc = Scenario(B=B, max_len=max_len, Hq=Hq, Hk=Hk, D=D, seed=21)
+    B, max_len = 6, 3000
+    sc = Scenario(B=B, max_len=max_len, Hq=Hq, Hk=Hk, D=D, W=W, kinds=[kind], seed=21 + D + Hq)
     targets = [2900, 700, 65, 1, 1500, 2111]  # many splits, one split, one key
     while any(t > l for t, l in zip(targets, sc.lens)):
         n = [min(64, t - l) for t, l in zip(targets, sc.lens)]
         sc.step(n, C=64, check=False)
     rope = _rope_table(max_len, D, 1e4)
     K, V = sc.cache.storage(0)
+    R = sc.cache.R
+    seg_rows = K.shape[2]                      # max_len + 1, or R + 1 for a ring
     stream = torch.cuda.current_stream().cuda_stream
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
     rows = list(range(B))
     for call in range(2):
         q, k, v = sc.chunk_inputs(0, rows, [1] * B, 1)
@@ -49,19 +74,79 @@ def test_noalloc_decode_matches_kv_append_on_two_calls():
         ref = sc.cache.append(0, qt, kt, vt, [1] * B)  # appends the new keys, then attends
         out = torch.full((B, Hq, D), 7.0, dtype=torch.bfloat16, device="cuda")
         pos = list(sc.lens)
-        rc = lib.kv_decode_noalloc(K.data_ptr(), V.data_ptr(), B, max_len + 1, Hq, Hk, D,
-                                   qt.data_ptr(), rope.data_ptr(), max_len, _i32(rows),
-                                   _i32(pos), _i32([p + 1 for p in pos]), B, out.data_ptr(),
-                                   ctypes.c_void_p(stream))
+        n_keys = [min(p + 1, R) if kind == 1 else p + 1 for p in pos]
+        rc = _call(lib, K, V, B, seg_rows, Hq, Hk, D, qt, rope, max_len, rows, pos, n_keys,
+                   out, err, stream)
         assert rc == 0, lib.kv_strerror(rc)
         torch.cuda.synchronize()
+        got = torch_to_bits(out)
+        # the oracle: cache-free attention over each row's history
+        sc.check_outputs(0, rows, [1] * B, q, got[:, None])
+        # the entry point that uses kv_cache_create's memory
         ref_f = oracle.bf16_to_f32(torch_to_bits(ref)[:, 0]).astype(np.float64)
-        check_close(torch_to_bits(out), ref_f, f"call {call}")
+        check_close(got, ref_f, f"call {call} vs kv_append")
         sc.cache.advance([1] * B)
         sc.lens = [l + 1 for l in sc.lens]
+    assert int(err.item()) == 0
 
 
-def test_noalloc_rejects_requests_beyond_its_scratch():
+def test_noalloc_many_partials_fit_by_longer_splits():
+    """130 query rows of 8192 keys at Hq=128, Hk=8, D=128: kv_append's schedule would take
+    two splits per row, 260 partial slots of 64 KiB -- more than the 256 the fixed scratch
+    holds -- so the planner lengthens the splits instead of refusing the call."""
+    import torch
+    from harness_large import LargeScenario
+    from kv_cache_incremental_gb300 import _lib, plan_decode
+    lib = _lib.load()
+    Hq, Hk, D, max_len = 128, 8, 128, 8200
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    Bs = 130
+    full = plan_decode(sms, Hq, Hk, D, 0, 0, [8191] * Bs)
+    if sms == 152:  # the schedule of kv_append overflows the scratch on this part
+        assert sum(n for n in full["n_splits"] if n > 1) * Hq * D * 4 > (16 << 20)
+    sc = LargeScenario(B=2, max_len=max_len, Hq=Hq, Hk=Hk, D=D, seed=77)
+    sc.fill_to([8191, 6000])
+    kept, lens_before = sc.step([1, 1], C=1, keep_layers=(0,))   # appends the keys at pos
+    sc.check_outputs(kept[0], 0, [0, 1], [1, 1], lens_before)
+    q2 = torch.empty((2, 1, Hq, D), dtype=torch.bfloat16, device="cuda")
+    rows_d = torch.arange(2, dtype=torch.int32, device="cuda")
+    seqs = torch.zeros(2, dtype=torch.int32, device="cuda")
+    pos0 = torch.from_numpy(lens_before.astype(np.int32)).to("cuda")
+    synth.fill_device(q2.data_ptr(), 77, synth.Q, 0, rows_d.data_ptr(), seqs.data_ptr(),
+                      pos0.data_ptr(), 2, 1, Hq, D, torch.cuda.current_stream().cuda_stream)
+    cache_rows = [i % 2 for i in range(Bs)]
+    q = q2[cache_rows, 0].contiguous()               # [Bs][Hq][D]
+    K, V = sc.cache.storage(0)
+    rope = _rope_table(max_len, D, 1e4)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ref = oracle.bf16_to_f32(torch_to_bits(kept[0])[:, 0]).astype(np.float64)
+    for _ in range(2):
+        out = torch.zeros((Bs, Hq, D), dtype=torch.bfloat16, device="cuda")
+        pos = [int(lens_before[r]) for r in cache_rows]
+        rc = _call(lib, K, V, 2, max_len + 1, Hq, Hk, D, q, rope, max_len, cache_rows, pos,
+                   [p + 1 for p in pos], out, err, torch.cuda.current_stream().cuda_stream)
+        assert rc == 0, lib.kv_strerror(rc)
+        torch.cuda.synchronize()
+        got = torch_to_bits(out)
+        for i in (0, 1, Bs - 2, Bs - 1):
+            check_close(got[i], ref[cache_rows[i]], f"row {i} vs kv_append")
+        # rows that share a cache row and a query have the same splits and the same output
+        for r in (0, 1):
+            assert np.array_equal(got[r::2], np.broadcast_to(got[r], got[r::2].shape))
+    # every row against the oracle (rows 0 and 1 were checked above through kv_append's
+    # outputs; here the noalloc outputs themselves)
+    L0 = lens_before.copy()
+    for r in (0, 1):
+        hist = np.arange(L0[r] + 1)
+        kh = synth.normal_bf16(77, synth.K, 0, r, 0, hist, Hk, D)
+        vh = synth.normal_bf16(77, synth.V, 0, r, 0, hist, Hk, D)
+        qh = synth.normal_bf16(77, synth.Q, 0, r, 0, [L0[r]], Hq, D)
+        want = oracle.attend(qh, [L0[r]], kh, vh, 0, Hq, Hk)
+        check_close(got[r], want[0], f"cache row {r} vs the oracle")
+    assert int(err.item()) == 0
+
+
+def test_noalloc_refusals_and_error_word():
     import torch
     from kv_cache_incremental_gb300 import _lib
     lib = _lib.load()
@@ -70,10 +155,27 @@ def test_noalloc_rejects_requests_beyond_its_scratch():
     q = torch.zeros((n_rows, Hq, D), dtype=torch.bfloat16, device="cuda")
     rope = _rope_table(4, D, 1e4)
     out = torch.zeros_like(q)
-    Bs = 513  # one more row than the fixed scratch plans for
-    rc = lib.kv_decode_noalloc(K.data_ptr(), K.data_ptr(), n_rows, 4, Hq, Hk, D, q.data_ptr(),
-                               rope.data_ptr(), 4, _i32(range(Bs)), _i32([0] * Bs),
-                               _i32([1] * Bs), Bs, out.data_ptr(), None)
+    err = torch.full((2,), 5, dtype=torch.int32, device="cuda")
+    # one more row than the fixed scratch plans for
+    rc = _call(lib, K, K, n_rows, 4, Hq, Hk, D, q, rope, 4, range(513), [0] * 513, [1] * 513,
+               out, err)
+    assert rc == _lib.KV_ERR_SCRATCH and b"scratch" in lib.kv_strerror(rc)
+    # more kv heads than the merge tickets cover
+    K65 = torch.zeros((1, 65, 4, D), dtype=torch.bfloat16, device="cuda")
+    q65 = torch.zeros((1, 65, D), dtype=torch.bfloat16, device="cuda")
+    rc = _call(lib, K65, K65, 1, 4, 65, 65, D, q65, rope, 4, [0], [0], [1], out, err)
     assert rc == _lib.KV_ERR_SCRATCH
-    assert b"scratch" in lib.kv_strerror(rc)
+    # no error word, or a misaligned one
+    rc = _call(lib, K, K, n_rows, 4, Hq, Hk, D, q, rope, 4, [0], [0], [1], out, None)
+    assert rc == _lib.KV_ERR_ARG
+    rc = lib.kv_decode_noalloc(K.data_ptr(), K.data_ptr(), n_rows, 4, Hq, Hk, D, q.data_ptr(),
+                               rope.data_ptr(), 4, _i32([0]), _i32([0]), _i32([1]), 1,
+                               out.data_ptr(), err.data_ptr() + 2, None)
+    assert rc == _lib.KV_ERR_ARG
+    torch.cuda.synchronize()
     assert torch.count_nonzero(out).item() == 0
+    # a call that runs leaves the caller's error word as it was (never cleared by the call)
+    rc = _call(lib, K, K, n_rows, 4, Hq, Hk, D, q, rope, 4, [0, 1], [0, 3], [1, 4], out, err)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert err.tolist() == [5, 5]
