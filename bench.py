@@ -74,6 +74,9 @@ def parse(argv=None):
     ap.add_argument("--workload", default="decode_bw", choices=sorted(WORKLOADS))
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sub-workloads", action="store_true",
+                    help="the default workload's line without the long-context and "
+                         "continuous-batch records")
     ap.add_argument("--fill-only", action="store_true",
                     help="time only the chunked-prefill cache fill of one cache (TFLOP/s)")
     ap.add_argument("--paged", action="store_true",
@@ -193,7 +196,7 @@ class ClockSampler:
     REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
                0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, index, period_s=0.005):
+    def __init__(self, index, period_s=0.001):
         import threading
         self.index, self.period = index, period_s
         self.samples = []  # (t, sm_mhz, max_mhz, reasons_mask)
@@ -512,15 +515,33 @@ def fill_cache_from(cache, cfg, lens_from, lens_target, seed, stream):
         lens += n
 
 
-def run_ours(args):
+def init_dist(local_rank, world):
+    """One NCCL process group per job (the headline and its sub-workloads share it)."""
+    import torch
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group("nccl")
+
+
+def step_times(events):
+    """Per-step device times (ms) from events recorded after each step (events[0]: start)."""
+    ms = [a.elapsed_time(b) for a, b in zip(events, events[1:])]
+    if not ms:
+        return None
+    return {"first": ms[0], "median": float(np.median(ms)), "min": min(ms), "max": max(ms),
+            "last": ms[-1], "n": len(ms)}
+
+
+def run_ours(args, sub=False):
+    """A decode workload; returns rank 0's JSON record (None on other ranks).  sub: a
+    sub-record of the headline line (no CPU baseline)."""
     import torch
     import kv_cache_incremental_gb300 as kvi
 
     rank, local_rank, world = dist_env()
-    torch.cuda.set_device(local_rank)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
+    init_dist(local_rank, world)
     cfg = WORKLOADS[args.workload]
     B, Hq, Hk, D = cfg["B"], cfg["Hq"], cfg["Hk"], cfg["D"]
     n_layers = len(cfg["kinds"])
@@ -567,18 +588,12 @@ def run_ours(args):
     torch.cuda.synchronize()
     kinds = cfg["kinds"]
     hybrid = any(k in HYBRID for k in kinds)
-    for s in range(Wm):
-        for layer in range(n_layers):
-            append_layer(caches[0][0], kinds[layer], layer, *step_inputs(inputs[0], s, layer),
-                         ones, out, stream)
-        caches[0][0].advance(ones, stream=stream)
-    torch.cuda.synchronize()
     alg_bytes = 0.0
     for r in range(rounds):
         base = lens0[r] + (Wm if r == 0 else 0)
         alg_bytes += sum(kv_bytes_per_step(cfg, base + s) for s in range(steps_in_round[r]))
 
-    def run_rounds(first_of):
+    def run_rounds(first_of, after_step=None, after_layer=None):
         for r in range(rounds):
             c = caches[r][0]
             first = first_of(r)
@@ -586,26 +601,41 @@ def run_ours(args):
                 for layer in range(n_layers):
                     append_layer(c, kinds[layer], layer, *step_inputs(inputs[r], s, layer),
                                  ones, out, stream)
+                    if after_layer:
+                        after_layer(c, kinds[layer])
                 c.advance(ones, stream=stream)
+                if after_step:
+                    after_step()
 
     # Timed region: the workload alone.  The library's per-launch events (kernel
-    # durations) cost ~10% of a 12-layer step, so they run in a second pass below.
+    # durations) cost ~10% of a 12-layer step, so they run in a second pass below; an
+    # event after each step (a stream marker, no host wait) gives the per-step times.
+    # The warm-up steps run right before it, after the clock sampler has started, so the
+    # GPU is busy up to the first timed step.
     clocks = ClockSampler(local_rank)
     clocks.start()
+    for s in range(Wm):
+        for layer in range(n_layers):
+            append_layer(caches[0][0], kinds[layer], layer, *step_inputs(inputs[0], s, layer),
+                         ones, out, stream)
+        caches[0][0].advance(ones, stream=stream)
+    torch.cuda.synchronize()
     barrier()
     torch.cuda.synchronize()
     clocks.mark_start()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
+    e0, e1 = evs[0], evs[-1]
+    it = iter(evs[1:])
     torch.cuda.profiler.start()  # profilers started with --profile-from-start off see this range
     e0.record(stream)
-    run_rounds(lambda r: Wm if r == 0 else 0)
-    e1.record(stream)
+    run_rounds(lambda r: Wm if r == 0 else 0, after_step=lambda: next(it).record(stream))
     torch.cuda.synchronize()
     torch.cuda.profiler.stop()
     clocks.mark_stop()
     barrier()
     clk = clocks.stop()
     ms = e0.elapsed_time(e1)
+    per_step = step_times(evs)
 
     # Kernel durations: the same number of steps per cache, continuing from where the timed
     # region left each cache, with CUDA events around every library launch (on the launch
@@ -617,10 +647,22 @@ def run_ours(args):
     torch.cuda.synchronize()
     for c, _ in caches:
         c.profile(True)
-    run_rounds(lambda r: 0)
-    torch.cuda.synchronize()
     kkinds = ("append", "decode", "combine", "state")
     prof = {k: {"launches": 0, "ms": 0.0, "bytes": 0.0, "flops": 0.0} for k in kkinds}
+    # the decode launches by layer kind (global, sliding, hybrid), read after every layer
+    by_kind = {}
+
+    def after_layer(c, kind):
+        rec = c.profile_read("decode", reset=True)
+        name = "global" if kind == 0 else "sliding" if kind == 1 else "hybrid"
+        acc = by_kind.setdefault(name, {"launches": 0, "ms": 0.0, "bytes": 0.0})
+        for f in acc:
+            acc[f] += rec[f]
+        for f in rec:
+            prof["decode"][f] += rec[f]
+
+    run_rounds(lambda r: 0, after_layer=after_layer)
+    torch.cuda.synchronize()
     for c, _ in caches:
         for k in kkinds:
             rec = c.profile_read(k, reset=True)
@@ -628,6 +670,12 @@ def run_ours(args):
                 prof[k][f] += rec[f]
         c.profile(False)
     launches = sum(p["launches"] for p in prof.values())
+    peak, peak_kind = measured_peaks()
+    split = {name: {"launches": a["launches"], "avg_launch_ms": a["ms"] / max(1, a["launches"]),
+                    "alg_bytes_per_launch": a["bytes"] / max(1, a["launches"]),
+                    "achieved": a["bytes"] / (a["ms"] / 1e3) / 1e9 if a["ms"] else None,
+                    "frac": a["bytes"] / (a["ms"] / 1e3) / 1e9 / peak if a["ms"] else None}
+             for name, a in by_kind.items()}
     del inputs
 
     # ---- the same steps as decode-step graph replays (kv_step_graph: one graph launch per
@@ -711,11 +759,12 @@ def run_ours(args):
     if world > 1:
         (ms, ms_e2e, ms_graph), (alg_bytes, e_bytes, graph_bytes) = reduce_over_ranks(
             [ms, ms_e2e, ms_graph or 0.0], [alg_bytes, e_bytes, graph_bytes], dev)
+    for c, _ in caches:
+        c.close()
     if rank != 0:
-        return
+        return None
     value = alg_bytes / (ms / 1e3) / 1e9
     tok_s = world * B * K / (ms / 1e3)
-    peak, peak_kind = measured_peaks()
     dec = prof["decode"]
     achieved = dec["bytes"] / (dec["ms"] / 1e3) / 1e9 if dec["ms"] > 0 else None
     traffic = traffic_record("decode.cu", args.workload)
@@ -728,6 +777,7 @@ def run_ours(args):
         "alg_bytes_per_launch": dec["bytes"] / max(1, dec["launches"]),
         "avg_launch_ms": dec["ms"] / max(1, dec["launches"]),
         "frac_of_nominal_8TBs": (achieved / NOMINAL_HBM_GBS) if achieved else None,
+        "by_layer_kind": split,
         "timing": "CUDA events around every library launch on the launch stream, over a "
                   "second pass of the same number of steps per cache (the timed region "
                   "runs without them)",
@@ -740,6 +790,9 @@ def run_ours(args):
         "config": decode_config(args, cfg, world),
         "tokens_per_s": tok_s,
         "frac_of_nominal_8TBs": value / NOMINAL_HBM_GBS,
+        "frac_of_measured_hbm": value / peak,
+        "step_ms": per_step,
+        "steady_value": (alg_bytes / K) / (per_step["median"] / 1e3) / 1e9 if per_step else None,
         "roofline": roofline,
         "e2e": {"value": e_bytes / (ms_e2e / 1e3) / 1e9, "unit": "GB/s",
                 "tokens_per_s": world * B * K / (ms_e2e / 1e3),
@@ -761,7 +814,7 @@ def run_ours(args):
                                                / peak_tflops()) if pre["ms"] else None,
                     "flops_counted": "4*Hq*D per visible (query, key) pair, causal only"},
     }
-    if world == 1 and not args.no_cpu_baseline:
+    if world == 1 and not args.no_cpu_baseline and not sub:
         gbs, tps, nr, thr, t = oracle_sample(cfg, lens0[0] + Wm + per_round, caches[0][1],
                                              budget_s=15.0)
         line["cpu_baseline"] = {"value": gbs, "unit": "GB/s", "cores": thr, "kind": "oracle",
@@ -770,7 +823,7 @@ def run_ours(args):
                                           f"{Hq} heads over each row's whole history), "
                                           f"{t:.1f} s of oracle time (at most 45 s of wall "
                                           f"time with the inputs' generation)"}
-    print(json.dumps(line), flush=True)
+    return line
 
 
 # ---------------------------------------------------------------- continuous batching
@@ -844,7 +897,7 @@ def cont_oracle_sample(cfg, steps, seed, budget_s):
     return tokens / spent, tokens, oracle.num_threads(), spent
 
 
-def run_cont_batch(args):
+def run_cont_batch(args, sub=False):
     """Config 5: tokens/s of the continuous-batch mix (decode rows, chunk rows, idle rows and
     resets in every step).  Three passes run the same step plan, each on a freshly filled
     cache: the timed region (no per-launch events), a pass with the library's per-launch
@@ -853,10 +906,7 @@ def run_cont_batch(args):
     import torch
     import kv_cache_incremental_gb300 as kvi
     rank, local_rank, world = dist_env()
-    torch.cuda.set_device(local_rank)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
+    init_dist(local_rank, world)
     cfg = WORKLOADS[args.workload]
     B, Hq, Hk, D, C = cfg["B"], cfg["Hq"], cfg["Hk"], cfg["D"], CONT_CHUNK
     kinds = cfg["kinds"]
@@ -880,7 +930,7 @@ def run_cont_batch(args):
             import torch.distributed as dist
             dist.barrier()
 
-    def run(c, i0, i1, host=None):
+    def run(c, i0, i1, host=None, after_step=None):
         for i in range(i0, i1):
             resets, n, _ = steps[i]
             c.reset(resets, stream=stream)
@@ -893,27 +943,31 @@ def run_cont_batch(args):
                     c.append_host(layer, host[0][i, layer], host[1][i, layer], host[2][i, layer],
                                   nl, out=host[3], stream=stream)
             c.advance(nl, stream=stream)
+            if after_step:
+                after_step()
 
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    # ---- timed region
+    # ---- timed region (warm-up right before it, events after every step)
     c = fresh()
-    run(c, 0, Wm)
-    torch.cuda.synchronize()
     clocks = ClockSampler(local_rank)
     clocks.start()
+    run(c, 0, Wm)
+    torch.cuda.synchronize()
     barrier()
     torch.cuda.synchronize()
     clocks.mark_start()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
+    it = iter(evs[1:])
     torch.cuda.profiler.start()
-    e0.record(stream)
-    run(c, Wm, Wm + K)
-    e1.record(stream)
+    evs[0].record(stream)
+    run(c, Wm, Wm + K, after_step=lambda: next(it).record(stream))
     torch.cuda.synchronize()
     torch.cuda.profiler.stop()
     clocks.mark_stop()
     barrier()
     clk = clocks.stop()
-    ms = e0.elapsed_time(e1)
+    ms = evs[0].elapsed_time(evs[-1])
+    per_step = step_times(evs)
     c.close()
     # ---- the same steps with per-launch events
     c = fresh()
@@ -945,7 +999,7 @@ def run_cont_batch(args):
     else:
         tokens_all = float(tokens)
     if rank != 0:
-        return
+        return None
     tot_bytes = sum(p["bytes"] for p in prof.values())
     tot_flops = sum(p["flops"] for p in prof.values())
     dec, pre = prof["decode"], prof["prefill"]
@@ -977,15 +1031,19 @@ def run_cont_batch(args):
         "e2e": {"value": tokens_all / (ms_e2e / 1e3), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": len(kinds) * B * C * Hq * D * 2},
         "gpu_launches": sum(p["launches"] for p in prof.values()),
-        "kernels": {k: {"launches": p["launches"], "ms": p["ms"]} for k, p in prof.items()},
+        "kernels": {k: {"launches": p["launches"], "ms": p["ms"],
+                        "gbs": p["bytes"] / (p["ms"] / 1e3) / 1e9 if p["ms"] else None,
+                        "tflops": p["flops"] / (p["ms"] / 1e3) / 1e12 if p["ms"] else None}
+                    for k, p in prof.items()},
+        "step_ms": per_step,
         "clocks": clk,
     }
-    if world == 1 and not args.no_cpu_baseline:
+    if world == 1 and not args.no_cpu_baseline and not sub:
         tps, nt, thr, t = cont_oracle_sample(cfg, steps[Wm:], seed, budget_s=15.0)
         line["cpu_baseline"] = {"value": tps, "unit": "tokens/s", "cores": thr, "kind": "oracle",
                                 "sample": f"{nt} tokens (whole rows of the first timed steps, "
                                           f"all {len(kinds)} layers), {t:.1f} s of oracle time"}
-    print(json.dumps(line), flush=True)
+    return line
 
 
 def run_reference_cont(args):
@@ -1019,17 +1077,44 @@ def run_reference_cont(args):
                 "d2h_bytes_per_step": 0}}), flush=True)
 
 
+# Workloads whose records the default (headline) line carries beside its own: the
+# long-context mixed layout (config 4, the >= 70% of HBM peak target) and the
+# continuous-batch mix (config 5).
+SUB_WORKLOADS = ("long_ctx", "cont_batch")
+SUB_KEYS = ("metric", "value", "unit", "steps", "warmup", "ms_per_step", "step_ms",
+            "steady_value", "tokens_per_s", "frac_of_measured_hbm", "frac_of_nominal_8TBs",
+            "gbs", "tflops", "roofline", "graph", "e2e", "gpu_launches", "kernels", "clocks",
+            "config", "prefill")
+
+
+def run_workload(args, sub=False):
+    mix = WORKLOADS[args.workload].get("mix", False)
+    return run_cont_batch(args, sub) if mix else run_ours(args, sub)
+
+
 def main():
     args = parse()
     mix = WORKLOADS[args.workload].get("mix", False)
     if args.impl == "reference":
         run_reference_cont(args) if mix else run_reference(args)
-    elif args.fill_only:
+        return
+    if args.fill_only:
         run_fill_only(args)
-    elif mix:
-        run_cont_batch(args)
-    else:
-        run_ours(args)
+        return
+    line = run_workload(args)
+    if args.workload == "decode_bw" and not args.no_sub_workloads and not args.max_len \
+            and not args.fill_to:
+        subs = {}
+        for w in SUB_WORKLOADS:
+            a2 = argparse.Namespace(**vars(args))
+            a2.workload = w
+            rec = run_workload(a2, sub=True)
+            if rec is not None:
+                subs[w] = {k: rec[k] for k in SUB_KEYS if k in rec}
+        if line is not None:
+            line["workloads"] = subs
+    if line is not None:
+        print(json.dumps(line), flush=True)
 
 
 if __name__ == "__main__":

@@ -22,6 +22,13 @@
 // all splits (log-sum-exp) and writes the bf16 output, then re-arms the ticket.
 // A row with a single split writes its output directly.
 //
+// Programmatic dependent launch: the kernel may be launched so that it starts while
+// the previous kernel on the stream finishes.  The consumers wait for the previous grid
+// (griddepcontrol.wait) before any other read or write, then let the next launch start;
+// the producer waits too unless the host allowed early K/V loads (early_kv: the launch
+// before it wrote none of this layer's storage -- with every PDL launch letting its
+// successor start only after its own wait, all older grids have completed by then).
+//
 // What is computed follows tiny_agent/generate.py `_append_chunk` (grouped
 // queries straight against the cache, scale 1/sqrt(D), float softmax) and the
 // inkling ring-buffer pull request (the sliding scan covers the last W
@@ -294,6 +301,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
       }
     };
     if (lane == 0) {
+      if (!p.early_kv) ptx::grid_dep_wait();
       if (seg1)
         produce(&p.tmap_k2, &p.tmap_v2);
       else
@@ -301,6 +309,11 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
     }
     return;
   }
+
+  // Inputs, partials, tickets and the cache are read or written only after the previous
+  // grid on the stream has completed; the next launch may then start.
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
 
   // -------------------------------------------------------------- consumers
   {
@@ -606,10 +619,23 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
 }
 
 template <int D, int NT>
-cudaError_t launch_decode_t(const DecodeParams &p, cudaStream_t s) {
+cudaError_t launch_decode_t(const DecodeParams &p, cudaStream_t s, bool pdl) {
   constexpr int smem = decode_smem_bytes<D, NT>();
-  decode_kernel<D, NT><<<dim3(p.n_items, p.Hk), kThreads, smem, s>>>(p);
-  return cudaGetLastError();
+  if (!pdl) {
+    decode_kernel<D, NT><<<dim3(p.n_items, p.Hk), kThreads, smem, s>>>(p);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.n_items, p.Hk);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_kernel<D, NT>, p);
 }
 
 template <int D, int NT>
@@ -621,10 +647,15 @@ cudaError_t configure_decode_t() {
 
 }  // namespace
 
-cudaError_t launch_decode(const DecodeParams &p, int D, int n_tiles_heads, cudaStream_t s) {
+cudaError_t launch_decode(const DecodeParams &p, int D, int n_tiles_heads, cudaStream_t s,
+                          bool pdl) {
   if (p.n_items <= 0) return cudaSuccess;
-  if (D == 128) return n_tiles_heads == 1 ? launch_decode_t<128, 1>(p, s) : launch_decode_t<128, 2>(p, s);
-  if (D == 64) return n_tiles_heads == 1 ? launch_decode_t<64, 1>(p, s) : launch_decode_t<64, 2>(p, s);
+  if (D == 128)
+    return n_tiles_heads == 1 ? launch_decode_t<128, 1>(p, s, pdl)
+                              : launch_decode_t<128, 2>(p, s, pdl);
+  if (D == 64)
+    return n_tiles_heads == 1 ? launch_decode_t<64, 1>(p, s, pdl)
+                              : launch_decode_t<64, 2>(p, s, pdl);
   return cudaErrorInvalidValue;
 }
 

@@ -147,6 +147,13 @@ struct kv_cache {
   // hybrid full layers: per row, lens + the tokens of its last append in this step (a
   // local layer of the group may only append the same tokens after it)
   std::vector<std::vector<int32_t>> hy_end;
+  // the cache's last kernel launch (stream, kernel kind or -1 for one that may write any
+  // storage, layer) and the layer of the call in progress: a decode launch may stream
+  // K/V before its grid dependency wait only when the launch before it on the stream
+  // wrote none of that layer's storage
+  bool pdl = true;  // decode launches use programmatic dependent launch (KVINC_PDL=0: off)
+  cudaStream_t last_stream = nullptr;
+  int last_kind = -1, last_layer = -1, cur_layer = -1;
 };
 
 namespace {
@@ -202,11 +209,15 @@ int ensure_blocks(kv_cache *c, const std::vector<std::pair<int, int>> &want, cud
       tp.blk[tp.n] = blk;
       rb.push_back(blk);
       if (++tp.n == kMaxTableEntries) {
+        c->last_stream = s;
+        c->last_kind = -1;
         if (launch_table(tp, s) != cudaSuccess) return KV_ERR_CUDA;
         tp.n = 0;
       }
     }
   }
+  c->last_stream = s;  // table entries: not to be read before a grid dependency wait
+  c->last_kind = -1;
   return launch_table(tp, s) == cudaSuccess ? KV_OK : KV_ERR_CUDA;
 }
 
@@ -231,9 +242,18 @@ cudaEvent_t take_event(kv_cache *c) {
   return e;
 }
 
+// Record a launch of kernel kind `kind` (-1: one that may write any storage of the cache)
+// for the layer of the call in progress.
+void note_launch(kv_cache *c, cudaStream_t s, int kind) {
+  c->last_stream = s;
+  c->last_kind = kind;
+  c->last_layer = c->cur_layer;
+}
+
 // Launch `fn` with an optional event pair around it.
 template <class F>
 cudaError_t timed(kv_cache *c, int kind, double bytes, double flops, cudaStream_t s, F fn) {
+  note_launch(c, s, kind);
   if (!c->prof || c->recs.size() >= kMaxProfRecs) return fn();
   ProfRec r{take_event(c), take_event(c), kind, bytes, flops};
   if (!r.a || !r.b) return fn();
@@ -277,6 +297,24 @@ struct Geom {
 
 Geom geom_of(const kv_cache *c, int layer) {
   return {c->num_sms, c->Hq, c->Hk, c->D, c->R, c->kind[layer]};
+}
+
+// The storage a layer's decode reads: its own, or for a hybrid layer its group's (the
+// group cache, written by the full layer, and the rings of the group's layers).
+int storage_id(const kv_cache *c, int layer) {
+  return c->group[layer] >= 0 ? c->group[layer] : layer;
+}
+
+// Whether a decode launch of `layer` on `s` may stream K/V before its grid dependency
+// wait: the cache's previous launch on s wrote nothing it reads -- a decode of another
+// storage (new keys, partials, tickets, outputs) or a ring-state update (lpos only).
+// Launches of the caller between them write no cache storage; older grids have completed
+// by the time a programmatic launch starts.
+bool early_kv_ok(const kv_cache *c, int layer, cudaStream_t s) {
+  if (!c->pdl || c->last_stream != s) return false;
+  if (c->last_kind == KV_KERNEL_STATE) return true;
+  return c->last_kind == KV_KERNEL_DECODE && c->last_layer >= 0 &&
+         storage_id(c, c->last_layer) != storage_id(c, layer);
 }
 
 }  // namespace
@@ -407,6 +445,7 @@ void fill_decode(const kv_cache *c, int layer, const __nv_bfloat16 *q, const __n
   dp.tmap_k16 = c->tmK16[layer];
   dp.tmap_v16 = c->tmV16[layer];
   dp.fuse_append2 = hybrid ? 1 : 0;
+  dp.early_kv = 0;
   dp.tmap_k2 = hybrid ? c->tmRK[layer] : c->tmK[layer];
   dp.tmap_v2 = hybrid ? c->tmRV[layer] : c->tmV[layer];
   dp.k_new2 = k_local;
@@ -533,6 +572,7 @@ int append_device(kv_cache *c, int layer, const __nv_bfloat16 *q, const __nv_bfl
                   const __nv_bfloat16 *vl = nullptr) {
   const bool sliding = c->kind[layer] == KV_SLIDING, hybrid = is_hybrid(c->kind[layer]);
   const bool writes_global = c->kind[layer] != KV_HYBRID_LOCAL;  // appends k, v anywhere
+  c->cur_layer = layer;
   const bool ringed = sliding || hybrid;                          // keeps a ring
   const int Hq = c->Hq, Hk = c->Hk, D = c->D, rep = Hq / Hk;
   int max_n = 0;
@@ -622,8 +662,9 @@ int append_device(kv_cache *c, int layer, const __nv_bfloat16 *q, const __nv_bfl
       double bytes = 0, fl = 0;
       fill_decode(c, layer, q, k, v, out, q_row, kv_row, batch, dp, bytes, fl, kl, vl);
       const int nt = rep <= 8 ? 1 : 2;
+      dp.early_kv = early_kv_ok(c, layer, s) ? 1 : 0;
       cudaError_t e = timed(c, KV_KERNEL_DECODE, bytes, fl, s,
-                            [&] { return launch_decode(dp, D, nt, s); });
+                            [&] { return launch_decode(dp, D, nt, s, c->pdl); });
       if (e != cudaSuccess) return KV_ERR_CUDA;
     }
 
@@ -981,6 +1022,7 @@ static int create_impl(kv_cache **out, int B, int max_len, int Hq, int Hk, int D
       !alloc((void **)&c->ppart_ml, (size_t)c->ppart_cap * 8))
     return fail(KV_ERR_OOM);
   if (cudaDeviceSynchronize() != cudaSuccess) return fail(KV_ERR_CUDA);
+  if (const char *pdl = std::getenv("KVINC_PDL")) c->pdl = pdl[0] != '0';
   if (const char *log = std::getenv("KVINC_LOG")) {
     if (log[0] == '1')
       std::fprintf(stderr, "[kv] %.1f MiB K/V (%d layers, B=%d, Hk=%d, D=%d, max_len=%d, R=%d)\n",
@@ -1830,6 +1872,9 @@ int kv_copy_rows(kv_cache *dst, const int32_t *dst_rows, const kv_cache *src,
     }
   }
   if (cp.n_items && flush_copies(cp, s) != KV_OK) return KV_ERR_CUDA;
+  dst->last_stream = s;  // the copies wrote the destination's storage
+  dst->last_kind = -1;
+  dst->cur_layer = -1;
   std::vector<int32_t> rows(dst_rows, dst_rows + n);
   if (set_ring_state(dst, rows, kp, s) != KV_OK) return KV_ERR_CUDA;
   for (int i = 0; i < n; ++i) {
@@ -1907,6 +1952,11 @@ static int export_import(kv_cache *c, int row, int keep, void *buf, int64_t byte
   }
   if (off * 2 != bytes) return KV_ERR_ARG;  // unreachable: checked by the callers
   if (cp.n_items && flush_copies(cp, s) != KV_OK) return KV_ERR_CUDA;
+  if (!to_buf) {  // an import wrote the cache's storage
+    c->last_stream = s;
+    c->last_kind = -1;
+    c->cur_layer = -1;
+  }
   return KV_OK;
 }
 

@@ -157,6 +157,11 @@ struct DecodeParams {  // 64-byte aligned through its CUtensorMap members
   __nv_bfloat16 *cache_k2, *cache_v2;  // ring storage [B][Hk][seg_rows2][D]
   int seg_rows2;
   int fuse_append2;
+  // Programmatic dependent launch: 1 lets the producer stream K/V tiles before the grid
+  // dependency wait (the host sets it only when the launch before it on the stream wrote
+  // none of the storage this launch reads); every other read and every write of the
+  // kernel follows the wait.
+  int early_kv;
   DecodeRow rows[kMaxRowsPerLaunch];
 };
 
@@ -298,7 +303,10 @@ cudaError_t launch_table(const TableParams &p, cudaStream_t s);
 int plan_decode_splits(int num_sms, int Hk, int n, const int *nk2, DecodeParams &p,
                        int max_parts);
 cudaError_t launch_append(const AppendParams &p, cudaStream_t s);
-cudaError_t launch_decode(const DecodeParams &p, int D, int n_tiles_heads, cudaStream_t s);
+// pdl: launch with programmatic stream serialisation, so that the kernel may start while
+// the previous kernel on the stream finishes (see DecodeParams::early_kv).
+cudaError_t launch_decode(const DecodeParams &p, int D, int n_tiles_heads, cudaStream_t s,
+                          bool pdl = false);
 // Graph kernel-node descriptions of the decode and state launches (args: one-slot storage
 // that must outlive the call that consumes *kp).
 cudaError_t decode_node(const DecodeParams *p, int D, int n_tiles_heads, void **args,

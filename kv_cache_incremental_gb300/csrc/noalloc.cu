@@ -170,6 +170,7 @@ extern "C" int kv_decode_noalloc(const void *K, const void *V, int n_cache_rows,
   dp.cache_v = nullptr;
   dp.fuse_append = 0;  // the caller has stored the new key already
   dp.fuse_append2 = 0;
+  dp.early_kv = 0;  // a plain launch: nothing runs before the previous kernel completes
   dp.seg0_ring = 0;
   dp.ring_R = 1;
   dp.pt = PageTable{nullptr, 0, 0};  // the caller's storage is dense

@@ -71,6 +71,17 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32
 }
 
 // ---------------------------------------------------------------- TMA
+// Programmatic dependent launch.  grid_dep_wait: wait until the grids this one depends on
+// have completed and their memory is visible (returns at once without a dependency).
+// grid_dep_launch: this CTA allows the dependent grid to start once every CTA of this grid
+// has done so or exited.
+__device__ __forceinline__ void grid_dep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
 }

@@ -108,11 +108,11 @@ def test_mma_sync_prefill_and_key_splits_with_large_scores():
     sc.step([1, 1, 1, 1], check_state=True)
 
 
-@pytest.mark.parametrize("q_scale", [4, 16, 64])
+@pytest.mark.parametrize("q_scale", [4, 64])
 def test_decode_splits_and_merge_with_large_scores(q_scale):
-    """Decode rows split over many CTAs (D = 128, rows to 8k keys), merged by the last."""
-    sc = Scenario(B=4, max_len=8300, Hq=32, Hk=8, D=128, seed=83, q_scale=q_scale)
-    targets = [8200, 3000, 65, 1]
+    """Decode rows split over many CTAs (D = 128, rows to 4k keys), merged by the last."""
+    sc = Scenario(B=4, max_len=4300, Hq=32, Hk=8, D=128, seed=83, q_scale=q_scale)
+    targets = [4200, 1500, 65, 1]
     while any(t > l for t, l in zip(targets, sc.lens)):
         sc.step([min(64, t - l) for t, l in zip(targets, sc.lens)], C=64, check=False)
     for _ in range(3):

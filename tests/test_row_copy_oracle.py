@@ -51,7 +51,7 @@ def test_grow_with_copy_of_wrapped_rings_into_a_larger_cache():
     small = Scenario(B=3, max_len=48, Hq=8, Hk=2, D=64, W=8, kinds=kinds, seed=63)
     small.step([40, 9, 3], C=40, check_state=True)
     big = Scenario(B=6, max_len=300, Hq=8, Hk=2, D=64, W=8, kinds=kinds, seed=64)
-    big.step([0, 5, 0, 0, 0, 0], C=5)                        # row 0 is overwritten below
+    big.step([5, 0, 0, 0, 0, 0], C=5)                        # row 0 is overwritten below
     big.copy_rows(small, src_rows=[0, 1, 2], dst_rows=[5, 0, 3])
     assert big.cache.lens == [9, 0, 0, 3, 0, 40]
     big.check_state()
@@ -130,9 +130,9 @@ def test_paged_truncation_and_prefix_like_the_oracle():
     prefixes share no blocks, and the rows then grow into fresh blocks."""
     p = Scenario(B=3, max_len=256, Hq=8, Hk=2, D=128, kinds=[0, 0], seed=73, paged_blocks=40)
     p.step([100, 37, 0], C=100, check=False)
-    free = p.cache.free_blocks()
+    free = p.cache.free_blocks
     p.copy_rows(p, src_rows=[0], dst_rows=[0], keep=[33])    # 7 blocks -> 3
-    assert p.cache.free_blocks() == free + 4
+    assert p.cache.free_blocks == free + 4
     p.copy_rows(p, src_rows=[1], dst_rows=[2], keep=[17])
     p.check_state()
     for _ in range(3):
