@@ -628,7 +628,9 @@ def run_ours(args, sub=False):
     it = iter(evs[1:])
     torch.cuda.profiler.start()  # profilers started with --profile-from-start off see this range
     e0.record(stream)
+    h0 = time.perf_counter()
     run_rounds(lambda r: Wm if r == 0 else 0, after_step=lambda: next(it).record(stream))
+    host_ms = (time.perf_counter() - h0) * 1e3   # enqueue time of the K steps
     torch.cuda.synchronize()
     torch.cuda.profiler.stop()
     clocks.mark_stop()
@@ -793,6 +795,7 @@ def run_ours(args, sub=False):
         "frac_of_measured_hbm": value / peak,
         "step_ms": per_step,
         "steady_value": (alg_bytes / K) / (per_step["median"] / 1e3) / 1e9 if per_step else None,
+        "host_ms_per_step": host_ms / K,
         "roofline": roofline,
         "e2e": {"value": e_bytes / (ms_e2e / 1e3) / 1e9, "unit": "GB/s",
                 "tokens_per_s": world * B * K / (ms_e2e / 1e3),
@@ -960,7 +963,9 @@ def run_cont_batch(args, sub=False):
     it = iter(evs[1:])
     torch.cuda.profiler.start()
     evs[0].record(stream)
+    h0 = time.perf_counter()
     run(c, Wm, Wm + K, after_step=lambda: next(it).record(stream))
+    host_ms = (time.perf_counter() - h0) * 1e3   # enqueue time of the K steps
     torch.cuda.synchronize()
     torch.cuda.profiler.stop()
     clocks.mark_stop()
@@ -1036,6 +1041,7 @@ def run_cont_batch(args, sub=False):
                         "tflops": p["flops"] / (p["ms"] / 1e3) / 1e12 if p["ms"] else None}
                     for k, p in prof.items()},
         "step_ms": per_step,
+        "host_ms_per_step": host_ms / K,
         "clocks": clk,
     }
     if world == 1 and not args.no_cpu_baseline and not sub:
@@ -1082,6 +1088,7 @@ def run_reference_cont(args):
 # continuous-batch mix (config 5).
 SUB_WORKLOADS = ("long_ctx", "cont_batch")
 SUB_KEYS = ("metric", "value", "unit", "steps", "warmup", "ms_per_step", "step_ms",
+            "host_ms_per_step",
             "steady_value", "tokens_per_s", "frac_of_measured_hbm", "frac_of_nominal_8TBs",
             "gbs", "tflops", "roofline", "graph", "e2e", "gpu_launches", "kernels", "clocks",
             "config", "prefill")

@@ -48,6 +48,8 @@ __device__ __forceinline__ void rope8(const uint4 &x1v, const uint4 &x2v, const 
 }
 
 __global__ void __launch_bounds__(256) append_kernel(const __grid_constant__ AppendParams p) {
+  ptx::grid_dep_wait();  // the previous grid on the stream has completed
+  ptx::grid_dep_launch();
   const int c_avail = p.c_avail < kChunk ? p.c_avail : kChunk;
   const int r = find_row_blk(p, blockIdx.x);
   const AppendRow &row = p.rows[r];
@@ -117,6 +119,8 @@ __global__ void __launch_bounds__(256) append_kernel(const __grid_constant__ App
 // token t is kept iff t >= n - W (the last min(n, W) real tokens; tiny_agent
 // keep rule, inkling skip rule s0 = max(0, S - win)).
 __global__ void __launch_bounds__(256) commit_kernel(const __grid_constant__ CommitParams p) {
+  ptx::grid_dep_wait();  // the previous grid on the stream has completed
+  ptx::grid_dep_launch();
   const int r = blockIdx.x, g = blockIdx.y;
   const int n = p.n[r];
   const int first = n - p.window > 0 ? n - p.window : 0;
@@ -152,6 +156,8 @@ __global__ void __launch_bounds__(256) commit_kernel(const __grid_constant__ Com
 // lpos (tiny_agent/generate.py keeps the position held by every ring slot): -1 on
 // reset; on advance, the kept tokens' positions at their slots.
 __global__ void __launch_bounds__(128) state_kernel(const __grid_constant__ StateParams p) {
+  ptx::grid_dep_wait();  // the previous grid on the stream has completed
+  ptx::grid_dep_launch();
   const int r = blockIdx.x;
   const int b = p.cache_row[r];
   if (p.reset) {
@@ -166,16 +172,14 @@ __global__ void __launch_bounds__(128) state_kernel(const __grid_constant__ Stat
 
 }  // namespace
 
-cudaError_t launch_append(const AppendParams &p, cudaStream_t s) {
+cudaError_t launch_append(const AppendParams &p, cudaStream_t s, bool pdl) {
   if (p.n_blocks <= 0) return cudaSuccess;
-  append_kernel<<<p.n_blocks, 256, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_k(append_kernel, dim3(p.n_blocks), dim3(256), 0, s, p, pdl);
 }
 
-cudaError_t launch_commit(const CommitParams &p, cudaStream_t s) {
+cudaError_t launch_commit(const CommitParams &p, cudaStream_t s, bool pdl) {
   if (p.n_rows <= 0) return cudaSuccess;
-  commit_kernel<<<dim3(p.n_rows, p.Hk), 256, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_k(commit_kernel, dim3(p.n_rows, p.Hk), dim3(256), 0, s, p, pdl);
 }
 
 // Block-table entries of newly allocated blocks (the values travel in the parameters, so a
@@ -203,10 +207,9 @@ cudaError_t state_node(const StateParams *p, void **args, cudaKernelNodeParams *
   return cudaSuccess;
 }
 
-cudaError_t launch_state(const StateParams &p, cudaStream_t s) {
+cudaError_t launch_state(const StateParams &p, cudaStream_t s, bool pdl) {
   if (p.n_rows <= 0) return cudaSuccess;
-  state_kernel<<<p.n_rows, 128, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_k(state_kernel, dim3(p.n_rows), dim3(128), 0, s, p, pdl);
 }
 
 namespace {

@@ -47,18 +47,21 @@ constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kMiniRows = 16;  // rows of the new-key mini-tile
 
-template <int D>
+// Stages of the K/V ring: 96 KB at either head dimension (two CTAs per SM), or with
+// DEEP 192 KB (one CTA per SM) for launches of at most one wave, whose CTAs each need
+// twice the bytes in flight to keep HBM busy.
+template <int D, bool DEEP>
 struct DecodeCfg {
   static constexpr int kPanels = D / 64;                        // 128-byte swizzle panels
   static constexpr int kTileBytes = kPanels * kTileKeys * 128;  // one K or V tile
-  static constexpr int kStages = D == 128 ? 3 : 6;
+  static constexpr int kStages = (D == 128 ? 3 : 6) * (DEEP ? 2 : 1);
   static constexpr int kStageBytes = 2 * kTileBytes;
   static constexpr int kMiniBytes = kPanels * kMiniRows * 128;  // one K or V mini-tile
 };
 
-template <int D, int NT>
+template <int D, int NT, bool DEEP>
 constexpr int decode_smem_bytes() {
-  using C = DecodeCfg<D>;
+  using C = DecodeCfg<D, DEEP>;
   return 1024 /*alignment slack*/ + C::kStages * C::kStageBytes + 2 * C::kMiniBytes +
          NT * 8 * D * 2 /*Q*/ + 2 * D * 2 /*new K, V*/ + 2 * C::kStages * 8 /*barriers*/ +
          16 /*flags*/;
@@ -197,9 +200,12 @@ __device__ __forceinline__ void zero_v_chunk(uint8_t *vt, int pstride, int r, in
       make_uint4(0, 0, 0, 0);
 }
 
-template <int D, int NT>
-__global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant__ DecodeParams p) {
-  using Cfg = DecodeCfg<D>;
+// Occupancy is set by shared memory (two CTAs per SM, one with DEEP); the bound tells the
+// register allocator so (left alone it chose 64 registers and spilled at D = 64).
+template <int D, int NT, bool DEEP>
+__global__ void __launch_bounds__(kThreads, DEEP ? 1 : 2)
+    decode_kernel(const __grid_constant__ DecodeParams p) {
+  using Cfg = DecodeCfg<D, DEEP>;
   constexpr int kStages = Cfg::kStages;
   constexpr int kHalf = D / 2;
   static_assert(kHalf % 8 == 0, "head dim must be a multiple of 16");
@@ -618,31 +624,38 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
   if (threadIdx.x == 0) *ticket = 0;  // re-armed for the next launch on the stream
 }
 
-template <int D, int NT>
+template <int D, int NT, bool DEEP>
 cudaError_t launch_decode_t(const DecodeParams &p, cudaStream_t s, bool pdl) {
-  constexpr int smem = decode_smem_bytes<D, NT>();
-  if (!pdl) {
-    decode_kernel<D, NT><<<dim3(p.n_items, p.Hk), kThreads, smem, s>>>(p);
-    return cudaGetLastError();
-  }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.n_items, p.Hk);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_kernel<D, NT>, p);
+  return launch_k(decode_kernel<D, NT, DEEP>, dim3(p.n_items, p.Hk), dim3(kThreads),
+                  decode_smem_bytes<D, NT, DEEP>(), s, p, pdl);
 }
 
-template <int D, int NT>
+template <int D, int NT, bool DEEP>
 cudaError_t configure_decode_t() {
-  constexpr int smem = decode_smem_bytes<D, NT>();
-  return cudaFuncSetAttribute(decode_kernel<D, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              smem);
+  constexpr int smem = decode_smem_bytes<D, NT, DEEP>();
+  return cudaFuncSetAttribute(decode_kernel<D, NT, DEEP>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+}
+
+// Function and shared memory of the variant for (D, tiles of heads, deep pipeline).
+template <int D, int NT>
+bool pick_t(bool deep, void **fn, int *smem) {
+  if (deep) {
+    *fn = reinterpret_cast<void *>(decode_kernel<D, NT, true>);
+    *smem = decode_smem_bytes<D, NT, true>();
+  } else {
+    *fn = reinterpret_cast<void *>(decode_kernel<D, NT, false>);
+    *smem = decode_smem_bytes<D, NT, false>();
+  }
+  return true;
+}
+
+bool pick(int D, int n_tiles_heads, bool deep, void **fn, int *smem) {
+  if (D == 128) return n_tiles_heads == 1 ? pick_t<128, 1>(deep, fn, smem)
+                                          : pick_t<128, 2>(deep, fn, smem);
+  if (D == 64) return n_tiles_heads == 1 ? pick_t<64, 1>(deep, fn, smem)
+                                         : pick_t<64, 2>(deep, fn, smem);
+  return false;
 }
 
 }  // namespace
@@ -650,12 +663,17 @@ cudaError_t configure_decode_t() {
 cudaError_t launch_decode(const DecodeParams &p, int D, int n_tiles_heads, cudaStream_t s,
                           bool pdl) {
   if (p.n_items <= 0) return cudaSuccess;
-  if (D == 128)
-    return n_tiles_heads == 1 ? launch_decode_t<128, 1>(p, s, pdl)
-                              : launch_decode_t<128, 2>(p, s, pdl);
-  if (D == 64)
-    return n_tiles_heads == 1 ? launch_decode_t<64, 1>(p, s, pdl)
-                              : launch_decode_t<64, 2>(p, s, pdl);
+  const bool deep = p.deep_pipeline != 0;
+  if (D == 128) {
+    if (n_tiles_heads == 1)
+      return deep ? launch_decode_t<128, 1, true>(p, s, pdl) : launch_decode_t<128, 1, false>(p, s, pdl);
+    return deep ? launch_decode_t<128, 2, true>(p, s, pdl) : launch_decode_t<128, 2, false>(p, s, pdl);
+  }
+  if (D == 64) {
+    if (n_tiles_heads == 1)
+      return deep ? launch_decode_t<64, 1, true>(p, s, pdl) : launch_decode_t<64, 1, false>(p, s, pdl);
+    return deep ? launch_decode_t<64, 2, true>(p, s, pdl) : launch_decode_t<64, 2, false>(p, s, pdl);
+  }
   return cudaErrorInvalidValue;
 }
 
@@ -669,30 +687,23 @@ cudaError_t decode_node(const DecodeParams *p, int D, int n_tiles_heads, void **
   kp->blockDim = dim3(kThreads);
   kp->kernelParams = args;
   kp->extra = nullptr;
-  if (D == 128 && n_tiles_heads == 1) {
-    kp->func = reinterpret_cast<void *>(decode_kernel<128, 1>);
-    kp->sharedMemBytes = decode_smem_bytes<128, 1>();
-  } else if (D == 128) {
-    kp->func = reinterpret_cast<void *>(decode_kernel<128, 2>);
-    kp->sharedMemBytes = decode_smem_bytes<128, 2>();
-  } else if (D == 64 && n_tiles_heads == 1) {
-    kp->func = reinterpret_cast<void *>(decode_kernel<64, 1>);
-    kp->sharedMemBytes = decode_smem_bytes<64, 1>();
-  } else if (D == 64) {
-    kp->func = reinterpret_cast<void *>(decode_kernel<64, 2>);
-    kp->sharedMemBytes = decode_smem_bytes<64, 2>();
-  } else {
+  int smem = 0;
+  if (!pick(D, n_tiles_heads, p->deep_pipeline != 0, &kp->func, &smem))
     return cudaErrorInvalidValue;
-  }
+  kp->sharedMemBytes = smem;
   return cudaSuccess;
 }
 
 cudaError_t configure_decode() {
   cudaError_t e;
-  if ((e = configure_decode_t<128, 1>()) != cudaSuccess) return e;
-  if ((e = configure_decode_t<128, 2>()) != cudaSuccess) return e;
-  if ((e = configure_decode_t<64, 1>()) != cudaSuccess) return e;
-  return configure_decode_t<64, 2>();
+  if ((e = configure_decode_t<128, 1, false>()) != cudaSuccess) return e;
+  if ((e = configure_decode_t<128, 2, false>()) != cudaSuccess) return e;
+  if ((e = configure_decode_t<64, 1, false>()) != cudaSuccess) return e;
+  if ((e = configure_decode_t<64, 2, false>()) != cudaSuccess) return e;
+  if ((e = configure_decode_t<128, 1, true>()) != cudaSuccess) return e;
+  if ((e = configure_decode_t<128, 2, true>()) != cudaSuccess) return e;
+  if ((e = configure_decode_t<64, 1, true>()) != cudaSuccess) return e;
+  return configure_decode_t<64, 2, true>();
 }
 
 }  // namespace kvinc

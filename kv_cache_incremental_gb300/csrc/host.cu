@@ -21,7 +21,8 @@ namespace kvinc {
 cudaError_t configure_decode();
 cudaError_t configure_prefill();
 cudaError_t configure_prefill_tc();
-cudaError_t launch_prefill_tc(const PrefillParams &p, int D, int tiles, cudaStream_t s);
+cudaError_t launch_prefill_tc(const PrefillParams &p, int D, int tiles, cudaStream_t s,
+                              bool pdl);
 int prefill_tc_tiles(int D, int n_rho);
 }  // namespace kvinc
 
@@ -373,6 +374,13 @@ int kvinc::plan_decode_splits(int num_sms, int Hk, int n, const int *nk2, Decode
   }
   p.n_rows = n;
   p.n_items = item;
+  // one wave or less: the deep-pipeline variant (one CTA per SM, twice the stages);
+  // KVINC_DEEP=0 in the environment keeps every launch on the shallow one (measurement)
+  static const bool deep_ok = [] {
+    const char *e = std::getenv("KVINC_DEEP");
+    return !(e && e[0] == '0');
+  }();
+  p.deep_pipeline = deep_ok && (int64_t)item * Hk <= num_sms ? 1 : 0;
   p.uniform_items = n == 0 ? 0 : p.rows[0].n_splits + p.rows[0].n_splits2;
   for (int i = 1; i < n && p.uniform_items; ++i)
     if (p.rows[i].n_splits + p.rows[i].n_splits2 != p.uniform_items) p.uniform_items = 0;
@@ -650,7 +658,7 @@ int append_device(kv_cache *c, int layer, const __nv_bfloat16 *q, const __nv_bfl
       }
       ap.n_rows = (int)(r1 - r0);
       ap.n_blocks = blk;
-      cudaError_t e = timed(c, KV_KERNEL_APPEND, bytes, 0, s, [&] { return launch_append(ap, s); });
+      cudaError_t e = timed(c, KV_KERNEL_APPEND, bytes, 0, s, [&] { return launch_append(ap, s, c->pdl); });
       if (e != cudaSuccess) return KV_ERR_CUDA;
     }
     }
@@ -663,6 +671,9 @@ int append_device(kv_cache *c, int layer, const __nv_bfloat16 *q, const __nv_bfl
       fill_decode(c, layer, q, k, v, out, q_row, kv_row, batch, dp, bytes, fl, kl, vl);
       const int nt = rep <= 8 ? 1 : 2;
       dp.early_kv = early_kv_ok(c, layer, s) ? 1 : 0;
+      // the deep variant pays off with the programmatic overlap of successive launches
+      // (long-context step 6058 -> 6201 GB/s), not without it
+      if (!c->pdl) dp.deep_pipeline = 0;
       cudaError_t e = timed(c, KV_KERNEL_DECODE, bytes, fl, s,
                             [&] { return launch_decode(dp, D, nt, s, c->pdl); });
       if (e != cudaSuccess) return KV_ERR_CUDA;
@@ -725,8 +736,8 @@ int append_device(kv_cache *c, int layer, const __nv_bfloat16 *q, const __nv_bfl
         pp.n_rows = (int)(r1 - r0);
         pp.n_ctas = cta;
         cudaError_t e = timed(c, KV_KERNEL_PREFILL, bytes, fl, s, [&] {
-          return kind == 0 ? launch_prefill(pp, D, s)
-                           : launch_prefill_tc(pp, D, kind == 1 ? 2 : 1, s);
+          return kind == 0 ? launch_prefill(pp, D, s, c->pdl)
+                           : launch_prefill_tc(pp, D, kind == 1 ? 2 : 1, s, c->pdl);
         });
         if (e != cudaSuccess) return KV_ERR_CUDA;
       }
@@ -754,7 +765,7 @@ int append_device(kv_cache *c, int layer, const __nv_bfloat16 *q, const __nv_bfl
       mg.n_rows = (int)(r1 - r0);
       mg.n_vec = vec;
       cudaError_t e = timed(c, KV_KERNEL_COMBINE, mb, 0, s,
-                            [&] { return launch_prefill_merge(mg, D, s); });
+                            [&] { return launch_prefill_merge(mg, D, s, c->pdl); });
       if (e != cudaSuccess) return KV_ERR_CUDA;
     }
     if (ringed) {
@@ -777,7 +788,7 @@ int append_device(kv_cache *c, int layer, const __nv_bfloat16 *q, const __nv_bfl
           cb += 4.0 * std::min(prows[j].n, c->W) * Hk * D * 2.0;
         }
         mp.n_rows = (int)(r1 - r0);
-        cudaError_t e = timed(c, KV_KERNEL_COMMIT, cb, 0, s, [&] { return launch_commit(mp, s); });
+        cudaError_t e = timed(c, KV_KERNEL_COMMIT, cb, 0, s, [&] { return launch_commit(mp, s, c->pdl); });
         if (e != cudaSuccess) return KV_ERR_CUDA;
       }
     }
@@ -810,7 +821,7 @@ int state_update(kv_cache *c, const std::vector<int32_t> &rows, const int32_t *n
   for (size_t r0 = 0; r0 < rows.size(); r0 += kMaxRowsPerLaunch) {
     const size_t r1 = std::min(rows.size(), r0 + kMaxRowsPerLaunch);
     fill_state(c, rows, n_new, reset, r0, r1, sp);
-    cudaError_t e = timed(c, KV_KERNEL_STATE, 0, 0, s, [&] { return launch_state(sp, s); });
+    cudaError_t e = timed(c, KV_KERNEL_STATE, 0, 0, s, [&] { return launch_state(sp, s, c->pdl); });
     if (e != cudaSuccess) return KV_ERR_CUDA;
   }
   return KV_OK;
@@ -1511,6 +1522,10 @@ void plan_step(kv_step_graph *g) {
     else
       fill_decode(c, l, g->q[l], g->k[l], g->v[l], g->out[l], q_row, kv_row, batch, g->dps[l],
                   by, fl);
+    // graph nodes start only when the node before them has completed (no programmatic
+    // overlap), where the one-CTA-per-SM deep variant measured slower (5970 vs 6054 GB/s
+    // on the long-context step)
+    g->dps[l].deep_pipeline = 0;
     g->bytes += by;
     g->flops += fl;
   }

@@ -162,6 +162,9 @@ struct DecodeParams {  // 64-byte aligned through its CUtensorMap members
   // none of the storage this launch reads); every other read and every write of the
   // kernel follows the wait.
   int early_kv;
+  // Host only: the launch fits one wave (n_items x Hk <= the SM count), so it runs the
+  // variant with twice the K/V stages and one CTA per SM.
+  int deep_pipeline;
   DecodeRow rows[kMaxRowsPerLaunch];
 };
 
@@ -290,6 +293,31 @@ struct TableParams {
 };
 
 // ---------------------------------------------------------------- launchers
+// Launch kernel(p) on s.  With pdl, as a programmatic dependent launch: the grid may start
+// while the previous kernel on the stream finishes, and waits for it (griddepcontrol.wait)
+// before it touches global memory; every kernel of the library does so at its start and
+// only then lets its own successor start, so that when a grid starts, every grid before
+// its predecessor has completed.
+template <typename P>
+cudaError_t launch_k(void (*kernel)(P), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                     const P &p, bool pdl) {
+  if (!pdl) {
+    kernel<<<grid, block, smem, s>>>(p);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
 cudaError_t launch_copy(const CopyParams &p, cudaStream_t s);
 cudaError_t launch_table(const TableParams &p, cudaStream_t s);
 // Split-K schedule of one decode launch over p.rows[0, n) (n <= kMaxRowsPerLaunch), whose
@@ -302,7 +330,7 @@ cudaError_t launch_table(const TableParams &p, cudaStream_t s);
 // hybrid layer) then still use slots, two each.
 int plan_decode_splits(int num_sms, int Hk, int n, const int *nk2, DecodeParams &p,
                        int max_parts);
-cudaError_t launch_append(const AppendParams &p, cudaStream_t s);
+cudaError_t launch_append(const AppendParams &p, cudaStream_t s, bool pdl = false);
 // pdl: launch with programmatic stream serialisation, so that the kernel may start while
 // the previous kernel on the stream finishes (see DecodeParams::early_kv).
 cudaError_t launch_decode(const DecodeParams &p, int D, int n_tiles_heads, cudaStream_t s,
@@ -312,10 +340,10 @@ cudaError_t launch_decode(const DecodeParams &p, int D, int n_tiles_heads, cudaS
 cudaError_t decode_node(const DecodeParams *p, int D, int n_tiles_heads, void **args,
                         cudaKernelNodeParams *kp);
 cudaError_t state_node(const StateParams *p, void **args, cudaKernelNodeParams *kp);
-cudaError_t launch_prefill(const PrefillParams &p, int D, cudaStream_t s);
-cudaError_t launch_prefill_merge(const MergeParams &p, int D, cudaStream_t s);
-cudaError_t launch_commit(const CommitParams &p, cudaStream_t s);
-cudaError_t launch_state(const StateParams &p, cudaStream_t s);
+cudaError_t launch_prefill(const PrefillParams &p, int D, cudaStream_t s, bool pdl = false);
+cudaError_t launch_prefill_merge(const MergeParams &p, int D, cudaStream_t s, bool pdl = false);
+cudaError_t launch_commit(const CommitParams &p, cudaStream_t s, bool pdl = false);
+cudaError_t launch_state(const StateParams &p, cudaStream_t s, bool pdl = false);
 cudaError_t launch_wait_probe(int32_t *err, uint32_t limit, cudaStream_t s);
 // Opt kernels into their dynamic shared memory sizes (once per process and device).
 cudaError_t configure_kernels();

@@ -58,6 +58,8 @@ __device__ __forceinline__ int find_cta_row(const PrefillParams &p, int b) {
 
 template <int D>
 __global__ void __launch_bounds__(kThreads) prefill_kernel(const __grid_constant__ PrefillParams p) {
+  ptx::grid_dep_wait();  // the previous grid on the stream has completed
+  ptx::grid_dep_launch();
   using Cfg = PrefillCfg<D>;
   constexpr int kStages = Cfg::kStages;
   constexpr int kHalf = D / 2;
@@ -405,6 +407,8 @@ constexpr int kMergeWarps = 8;
 template <int D>
 __global__ void __launch_bounds__(kMergeWarps * 32)
     prefill_merge_kernel(const __grid_constant__ MergeParams p) {
+  ptx::grid_dep_wait();  // the previous grid on the stream has completed
+  ptx::grid_dep_launch();
   constexpr int kPer = D / 32;  // dims per lane
   const int v = blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -465,27 +469,26 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
 }
 
 template <int D>
-cudaError_t launch_prefill_t(const PrefillParams &p, cudaStream_t s) {
-  prefill_kernel<D><<<dim3(p.n_ctas, p.Hk), kThreads, prefill_smem_bytes<D>(), s>>>(p);
-  return cudaGetLastError();
+cudaError_t launch_prefill_t(const PrefillParams &p, cudaStream_t s, bool pdl) {
+  return launch_k(prefill_kernel<D>, dim3(p.n_ctas, p.Hk), dim3(kThreads),
+                  prefill_smem_bytes<D>(), s, p, pdl);
 }
 
 }  // namespace
 
-cudaError_t launch_prefill(const PrefillParams &p, int D, cudaStream_t s) {
+cudaError_t launch_prefill(const PrefillParams &p, int D, cudaStream_t s, bool pdl) {
   if (p.n_ctas <= 0) return cudaSuccess;
-  if (D == 128) return launch_prefill_t<128>(p, s);
-  if (D == 64) return launch_prefill_t<64>(p, s);
+  if (D == 128) return launch_prefill_t<128>(p, s, pdl);
+  if (D == 64) return launch_prefill_t<64>(p, s, pdl);
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_prefill_merge(const MergeParams &p, int D, cudaStream_t s) {
+cudaError_t launch_prefill_merge(const MergeParams &p, int D, cudaStream_t s, bool pdl) {
   if (p.n_vec <= 0) return cudaSuccess;
-  const int blocks = (p.n_vec + kMergeWarps - 1) / kMergeWarps;
-  if (D == 128) prefill_merge_kernel<128><<<blocks, kMergeWarps * 32, 0, s>>>(p);
-  else if (D == 64) prefill_merge_kernel<64><<<blocks, kMergeWarps * 32, 0, s>>>(p);
-  else return cudaErrorInvalidValue;
-  return cudaGetLastError();
+  const dim3 blocks((p.n_vec + kMergeWarps - 1) / kMergeWarps), threads(kMergeWarps * 32);
+  if (D == 128) return launch_k(prefill_merge_kernel<128>, blocks, threads, 0, s, p, pdl);
+  if (D == 64) return launch_k(prefill_merge_kernel<64>, blocks, threads, 0, s, p, pdl);
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t configure_prefill() {

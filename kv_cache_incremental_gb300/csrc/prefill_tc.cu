@@ -184,6 +184,8 @@ __global__ void __launch_bounds__(Roles<TQ>::kThreads, TQ == 1 ? 2 : 1)
   volatile int *fail = reinterpret_cast<volatile int *>(tmem_slot + 1);
   volatile int *issued = fail + 1;
 
+  ptx::grid_dep_wait();  // the previous grid on the stream has completed
+  ptx::grid_dep_launch();
   const PrefillRow &row = p.rows[find_cta_row(p, blockIdx.x)];
   const int g = blockIdx.y;
   const int rho0 = (blockIdx.x - row.cta0) * kRows * kTilesQ;
@@ -711,17 +713,17 @@ __global__ void __launch_bounds__(Roles<TQ>::kThreads, TQ == 1 ? 2 : 1)
 int prefill_tc_tiles(int D, int) { return D == 64 ? 1 : 2; }
 
 template <int D, int TQ>
-static void launch_tc(const PrefillParams &p, cudaStream_t s) {
-  prefill_tc_kernel<D, TQ>
-      <<<dim3(p.n_ctas, p.Hk), Roles<TQ>::kThreads, TcCfg<D, TQ>::kSmem, s>>>(p);
+static cudaError_t launch_tc(const PrefillParams &p, cudaStream_t s, bool pdl) {
+  return launch_k(prefill_tc_kernel<D, TQ>, dim3(p.n_ctas, p.Hk), dim3(Roles<TQ>::kThreads),
+                  TcCfg<D, TQ>::kSmem, s, p, pdl);
 }
 
-cudaError_t launch_prefill_tc(const PrefillParams &p, int D, int tiles, cudaStream_t s) {
+cudaError_t launch_prefill_tc(const PrefillParams &p, int D, int tiles, cudaStream_t s,
+                              bool pdl) {
   if (p.n_ctas <= 0) return cudaSuccess;
-  if (D == 128 && tiles == 2) launch_tc<128, 2>(p, s);
-  else if (D == 64 && tiles == 1) launch_tc<64, 1>(p, s);
-  else return cudaErrorInvalidValue;
-  return cudaGetLastError();
+  if (D == 128 && tiles == 2) return launch_tc<128, 2>(p, s, pdl);
+  if (D == 64 && tiles == 1) return launch_tc<64, 1>(p, s, pdl);
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t configure_prefill_tc() {
