@@ -16,6 +16,8 @@ import ctypes
 import weakref
 from typing import Optional, Sequence
 
+import numpy as np
+
 from ._lib import (KERNELS, KV_GLOBAL, KV_HYBRID_FULL, KV_HYBRID_LOCAL, KV_SLIDING, KVCacheFull,
                    KVError, KVPoolExhausted, check, load)
 
@@ -26,11 +28,39 @@ __all__ = ["KVCache", "StepGraph", "KVError", "KVCacheFull", "KVPoolExhausted", 
 _clib = load()
 
 
-def _i32_array(values) -> Optional[ctypes.Array]:
+_P_I32 = ctypes.POINTER(ctypes.c_int32)
+
+
+def _i32_array(values):
+    """Host int32 array for the C ABI: a pointer into a numpy buffer it keeps alive (values
+    that do not fit int32 raise OverflowError)."""
     if values is None:
         return None
-    vals = [int(x) for x in values]
-    return (ctypes.c_int32 * max(1, len(vals)))(*vals)
+    a = np.ascontiguousarray(values, dtype=np.int32).reshape(-1)
+    if a.size == 0:
+        a = np.zeros(1, dtype=np.int32)
+    return a.ctypes.data_as(_P_I32)
+
+
+class _I32Memo:
+    """The last list marshalled for one argument and its int32 array: decode loops pass the
+    same per-row counts every step (e.g. [1] * B), which then cost a list comparison instead
+    of a conversion."""
+
+    __slots__ = ("key", "ptr")
+
+    def __init__(self):
+        self.key, self.ptr = None, None
+
+    def get(self, values):
+        if values is None:
+            return None
+        if type(values) is list and values == self.key:
+            return self.ptr
+        ptr = _i32_array(values)
+        if type(values) is list:
+            self.key, self.ptr = list(values), ptr
+        return ptr
 
 
 def _stream_ptr(stream, device):
@@ -75,6 +105,7 @@ class KVCache:
         _clib.kv_get_config(h, None, None, None, None, None, None, ctypes.byref(r), None)
         self.R = r.value
         self._graphs = weakref.WeakSet()  # step graphs over this cache, closed before it
+        self._memo_n, self._memo_rows = _I32Memo(), _I32Memo()
 
     # ------------------------------------------------------------------ lifecycle
     def close(self) -> None:
@@ -116,12 +147,11 @@ class KVCache:
             out = torch.empty_like(q)
         else:
             self._check_tensor(out, "out", self.Hq, C, Bs)
-        n = _i32_array(n_new)
         if len(n_new) != Bs or (rows is not None and len(rows) != Bs):
             raise ValueError("n_new and rows must have one entry per row of q")
         check(_clib.kv_append(self._h, layer, q.data_ptr(), k.data_ptr(), v.data_ptr(), self.Hq, C,
-                             n, _i32_array(rows), Bs, out.data_ptr(),
-                             _stream_ptr(stream, q.device)), "kv_append")
+                             self._memo_n.get(n_new), self._memo_rows.get(rows), Bs,
+                             out.data_ptr(), _stream_ptr(stream, q.device)), "kv_append")
         return out
 
     def append_hybrid(self, layer: int, q, k_local, v_local, n_new, k_global=None,
@@ -244,7 +274,7 @@ class KVCache:
     def advance(self, n_new, rows=None, stream=None) -> None:
         """End the step: lens[row] += n_new (call once, after every layer was appended)."""
         Bs = len(n_new)
-        check(_clib.kv_advance(self._h, _i32_array(n_new), _i32_array(rows), Bs,
+        check(_clib.kv_advance(self._h, self._memo_n.get(n_new), self._memo_rows.get(rows), Bs,
                               _stream_ptr(stream, self.device)), "kv_advance")
 
     def reset(self, rows, stream=None) -> None:
