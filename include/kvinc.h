@@ -35,6 +35,13 @@
  *  - Device work runs asynchronously on the caller's CUDA stream (`stream`,
  *    a cudaStream_t passed as void*, NULL = legacy default stream).  No entry
  *    point synchronises the device unless its comment says so.
+ *  - The library's kernels are programmatic dependent launches: one may be
+ *    scheduled while the kernel before it on the stream finishes, and waits for
+ *    that kernel to complete before it reads or writes memory.  Stream order is
+ *    kept for every caller kernel launched the ordinary way; a caller kernel
+ *    that is itself launched programmatically after a library call must wait
+ *    for its predecessor (griddepcontrol.wait) before reading the call's output,
+ *    as with any programmatic launch.
  *  - Not thread-safe: one cache is driven from one host thread and one
  *    stream at a time.
  *  - Tensors are bfloat16, row-major, contiguous, 16-byte aligned.

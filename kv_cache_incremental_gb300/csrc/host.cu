@@ -1522,10 +1522,13 @@ void plan_step(kv_step_graph *g) {
     else
       fill_decode(c, l, g->q[l], g->k[l], g->v[l], g->out[l], q_row, kv_row, batch, g->dps[l],
                   by, fl);
-    // graph nodes start only when the node before them has completed (no programmatic
-    // overlap), where the one-CTA-per-SM deep variant measured slower (5970 vs 6054 GB/s
-    // on the long-context step)
+    // Graph nodes keep the shallow variant: a node's kernel is fixed at instantiation (the
+    // deep variant would change it between replays).  Their edges are programmatic (as
+    // stream launches are), so a node may stream K/V early when the node before it decodes
+    // another storage.
     g->dps[l].deep_pipeline = 0;
+    g->dps[l].early_kv =
+        c->pdl && l > 0 && storage_id(c, l - 1) != storage_id(c, l) ? 1 : 0;
     g->bytes += by;
     g->flops += fl;
   }
@@ -1573,6 +1576,17 @@ void set_step_buffers(kv_step_graph *g, const void *const *q, const void *const 
   }
 }
 
+// Edge from -> to: programmatic (the downstream kernel may start once every CTA of the
+// upstream one has let it, and waits for its completion with griddepcontrol.wait) or full.
+bool add_edge(cudaGraph_t graph, cudaGraphNode_t from, cudaGraphNode_t to, bool programmatic) {
+  cudaGraphEdgeData e{};
+  if (programmatic) {
+    e.from_port = cudaGraphKernelNodePortProgrammatic;
+    e.type = cudaGraphDependencyTypeProgrammatic;
+  }
+  return cudaGraphAddDependencies(graph, &from, &to, &e, 1) == cudaSuccess;
+}
+
 int step_graph_create(kv_cache *c, kv_step_graph **out, const void *const *q,
                       const void *const *k, const void *const *v, const void *const *kg,
                       const void *const *vg, void *const *outp, int Hq, const int32_t *rows,
@@ -1605,8 +1619,8 @@ int step_graph_create(kv_cache *c, kv_step_graph **out, const void *const *q,
     cudaKernelNodeParams kp{};
     cudaGraphNode_t node = nullptr;
     ok = decode_node(&g->dps[l], c->D, nt, args, &kp) == cudaSuccess &&
-         cudaGraphAddKernelNode(&node, g->graph, prev ? &prev : nullptr, prev ? 1 : 0, &kp) ==
-             cudaSuccess;
+         cudaGraphAddKernelNode(&node, g->graph, nullptr, 0, &kp) == cudaSuccess &&
+         (!prev || add_edge(g->graph, prev, node, c->pdl));
     g->dec.push_back(node);
     prev = node;
   }
@@ -1614,7 +1628,8 @@ int step_graph_create(kv_cache *c, kv_step_graph **out, const void *const *q,
     void *args[1];
     cudaKernelNodeParams kp{};
     ok = state_node(&g->sp, args, &kp) == cudaSuccess &&
-         cudaGraphAddKernelNode(&g->state, g->graph, &prev, 1, &kp) == cudaSuccess;
+         cudaGraphAddKernelNode(&g->state, g->graph, nullptr, 0, &kp) == cudaSuccess &&
+         add_edge(g->graph, prev, g->state, c->pdl);
   }
   ok = ok && cudaGraphInstantiate(&g->exec, g->graph, 0) == cudaSuccess;
   if (!ok) {
