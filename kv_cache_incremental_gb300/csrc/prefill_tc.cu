@@ -584,39 +584,41 @@ __global__ void __launch_bounds__(Roles<TQ>::kThreads, TQ == 1 ? 2 : 1)
       }
       tc::fence_after();
       const int j0 = 2 * (b_begin + b);
+      const int halves = j0 + 1 < j_end ? 2 : 1;  // a last block may hold one tile
+      // The block's two 64-key tiles run through one copy of the code (a loop that is not
+      // unrolled): short CTAs, as in continuous batching, otherwise spend much of their time
+      // fetching instructions.
       if (qt == 0) {
-        const int z0 = zero_v(b, 0), z1 = j0 + 1 < j_end ? zero_v(b, 1) : 0;
-        if (z0 < 0 || z1 < 0) {
+        int z = 0;
+#pragma unroll 1
+        for (int h = 0; h < halves && z >= 0; ++h) {
+          const int zh = zero_v(b, h);
+          z = zh < 0 ? -1 : max(z, zh);
+        }
+        if (z < 0) {
           ok = false;
           break;
         }
-        if (z0 > 0 || z1 > 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        if (z > 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&v_ready[b % kStages]);
       }
       float sv[kKeys];
-      // S of this block implies PV(b-1) finished (the QK waited for it): O is final.
-      if (!rescale_to(load_tile(j0, 0, sv), [&] {
-            return b < 1 || ptx::mbar_wait(&pv_done[qt], (b - 1) & 1, kWaitLimit);
-          })) {
-        ok = false;
-        break;
-      }
-      store_p(0, sv);
-      publish(0);
-      if (j0 + 1 < j_end) {
-        // a new maximum in tile 1 rescales O after PV of tile 0 (already issued) is done.
-        // With S double-buffered, PV(b - 1) was issued after QK(b) and may still run: its
-        // phase is waited for first (a parity wait must not be two phases ahead).
-        if (!rescale_to(load_tile(j0 + 1, 1, sv), [&] {
+#pragma unroll 1
+      for (int h = 0; h < halves; ++h) {
+        // Tile 0: S of this block implies PV(b-1) finished (the QK waited for it), so O is
+        // final.  Tile 1: a new maximum rescales O after PV of tile 0 (already issued) is
+        // done; with S double-buffered, PV(b - 1) was issued after QK(b) and may still run,
+        // so its phase is waited for first (a parity wait must not be two phases ahead).
+        if (!rescale_to(load_tile(j0 + h, h, sv), [&] {
               return (b < 1 || ptx::mbar_wait(&pv_done[qt], (b - 1) & 1, kWaitLimit)) &&
-                     ptx::mbar_wait(&pv0_done[qt], b & 1, kWaitLimit);
+                     (h == 0 || ptx::mbar_wait(&pv0_done[qt], b & 1, kWaitLimit));
             })) {
           ok = false;
           break;
         }
-        store_p(1, sv);
-        publish(1);
+        store_p(h, sv);
+        publish(h);
       }
     }
     float l0, l1;
