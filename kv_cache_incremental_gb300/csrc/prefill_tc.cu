@@ -527,7 +527,7 @@ __global__ void __launch_bounds__(Roles<TQ>::kThreads, TQ == 1 ? 2 : 1)
       if (__any_sync(0xffffffffu, rescale)) {
         if (!__all_sync(0xffffffffu, stable())) return false;
         tc::fence_after();
-#pragma unroll
+#pragma unroll 1  // one 16-column chunk of code (instruction fetch)
         for (int c = 0; c < D / 16; ++c) {
           float o16[16];
           tc::ld16(tO + 16 * c, o16);
@@ -639,7 +639,7 @@ __global__ void __launch_bounds__(Roles<TQ>::kThreads, TQ == 1 ? 2 : 1)
       if (n_blocks > 0) tc::fence_after();
       const int64_t vec = (int64_t)row.part + (int64_t)g * n_rho + rho;
       float4 *po = reinterpret_cast<float4 *>(p.part_o + vec * D);
-#pragma unroll
+#pragma unroll 1  // one 16-column chunk of code (instruction fetch)
       for (int c = 0; c < D / 16; ++c) {
         float o16[16];
         if (n_blocks > 0) {
@@ -662,7 +662,7 @@ __global__ void __launch_bounds__(Roles<TQ>::kThreads, TQ == 1 ? 2 : 1)
       const int t = qvalid ? rho / p.rep : 0, h = qvalid ? rho % p.rep : 0;
       __nv_bfloat16 *dst = p.out + (int64_t)row.call_row * p.out_row_stride +
                            ((int64_t)t * p.Hq + g * p.rep + h) * D;
-#pragma unroll
+#pragma unroll 1  // one 16-column chunk of code (instruction fetch)
       for (int c = 0; c < D / 16; ++c) {
         float o16[16];
         tc::ld16(tO + 16 * c, o16);
