@@ -47,14 +47,16 @@ constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kMiniRows = 16;  // rows of the new-key mini-tile
 
-// Stages of the K/V ring: 96 KB at either head dimension (two CTAs per SM), or with
-// DEEP 192 KB (one CTA per SM) for launches of at most one wave, whose CTAs each need
+// Stages of the K/V ring: 96 KB at D = 128 (two CTAs per SM) and 64 KB at D = 64 (three CTAs
+// per SM: more warps to hide the shorter tiles' latency; the continuous-batch mix's decode
+// launches 5.45 -> 5.04 ms over 50 steps against six stages at two CTAs per SM), or with
+// DEEP twice that (one CTA per SM) for launches of at most one wave, whose CTAs each need
 // twice the bytes in flight to keep HBM busy.
 template <int D, bool DEEP>
 struct DecodeCfg {
   static constexpr int kPanels = D / 64;                        // 128-byte swizzle panels
   static constexpr int kTileBytes = kPanels * kTileKeys * 128;  // one K or V tile
-  static constexpr int kStages = (D == 128 ? 3 : 6) * (DEEP ? 2 : 1);
+  static constexpr int kStages = (D == 128 ? 3 : 4) * (DEEP ? 2 : 1);
   static constexpr int kStageBytes = 2 * kTileBytes;
   static constexpr int kMiniBytes = kPanels * kMiniRows * 128;  // one K or V mini-tile
 };
@@ -200,10 +202,11 @@ __device__ __forceinline__ void zero_v_chunk(uint8_t *vt, int pstride, int r, in
       make_uint4(0, 0, 0, 0);
 }
 
-// Occupancy is set by shared memory (two CTAs per SM, one with DEEP); the bound tells the
-// register allocator so (left alone it chose 64 registers and spilled at D = 64).
+// Occupancy is set by shared memory (two CTAs per SM at D = 128, three at D = 64, one with
+// DEEP); the bound tells the register allocator so (left alone it chose 64 registers and
+// spilled at D = 64).
 template <int D, int NT, bool DEEP>
-__global__ void __launch_bounds__(kThreads, DEEP ? 1 : 2)
+__global__ void __launch_bounds__(kThreads, DEEP ? 1 : D == 64 ? 3 : 2)
     decode_kernel(const __grid_constant__ DecodeParams p) {
   using Cfg = DecodeCfg<D, DEEP>;
   constexpr int kStages = Cfg::kStages;
