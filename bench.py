@@ -196,7 +196,7 @@ class ClockSampler:
     REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
                0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, index, period_s=0.001):
+    def __init__(self, index, period_s=0.0005):
         import threading
         self.index, self.period = index, period_s
         self.samples = []  # (t, sm_mhz, max_mhz, reasons_mask)
@@ -222,11 +222,13 @@ class ClockSampler:
         import ctypes
         lib, h, reasons_fn = self.nvml
         sm, mx, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        # the maximum clock does not change: read once, then poll only the current clock and
+        # the reasons (two queries per sample, so short regions get more samples)
+        have_max = lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0
         while not self.stop_flag.is_set():
             t = time.perf_counter()
-            ok = lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(sm)) == 0  # NVML_CLOCK_SM
-            ok &= lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0
-            ok &= reasons_fn(h, ctypes.byref(rs)) == 0
+            ok = have_max and lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(sm)) == 0  # SM clock
+            ok = ok and reasons_fn(h, ctypes.byref(rs)) == 0
             if ok:
                 self.samples.append((t, sm.value, mx.value, rs.value))
             self.stop_flag.wait(self.period)
