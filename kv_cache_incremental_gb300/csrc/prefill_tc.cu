@@ -468,7 +468,10 @@ __global__ void __launch_bounds__(Roles<TQ>::kThreads, TQ == 1 ? 2 : 1)
       const bool vis = ((kidx >= m.r0) & (kidx <= m.r1)) | ((kidx >= m.r2) & (kidx <= m.r3));
       return vis ? x * scale : -INFINITY;
     };
-    // S of tile h of the block (64 columns) into v, masked and scaled; returns its max.
+    // S of tile h of the block (64 columns) into v; returns its maximum in log2 units.  A
+    // tile entirely visible stays unscaled (raw = true: the scale goes into the exponent's
+    // FMA); any other is masked and scaled here.
+    bool raw = false;
     auto load_tile = [&](int j, int h, float (&v)[kKeys]) {
       const TileMask m = tile_mask(j);
 #pragma unroll
@@ -479,13 +482,10 @@ __global__ void __launch_bounds__(Roles<TQ>::kThreads, TQ == 1 ? 2 : 1)
         for (int i = 0; i < 16; ++i) v[16 * c + i] = t16[i];
       }
       tc::wait_ld();
-      if (m.all_vis) {
+      raw = m.all_vis;
+      if (raw) return max64(v) * scale;  // scaling by a positive number commutes with max
 #pragma unroll
-        for (int i = 0; i < kKeys; ++i) v[i] *= scale;
-      } else {
-#pragma unroll
-        for (int i = 0; i < kKeys; ++i) v[i] = masked(m, i, v[i]);
-      }
+      for (int i = 0; i < kKeys; ++i) v[i] = masked(m, i, v[i]);
       return max64(v);
     };
     // P = 2^(s - m) of tile h as bf16 high + low parts over its S columns: keys 2i, 2i+1
@@ -494,15 +494,19 @@ __global__ void __launch_bounds__(Roles<TQ>::kThreads, TQ == 1 ? 2 : 1)
     uint64_t l2 = ptx::f2_pack(0.f, 0.f);
     auto store_p = [&](int h, const float (&v)[kKeys]) {
       const float base = m_used == -INFINITY ? 0.f : m_used;
-      const uint64_t nb = ptx::f2_pack(base, base);
+      const uint64_t nb = ptx::f2_pack(-base, -base);
+      // x = s * scale - m for a raw tile, s - m for a scaled one (one packed FMA per pair)
+      const float sc = raw ? scale : 1.f;
+      const uint64_t sc2 = ptx::f2_pack(sc, sc);
 #pragma unroll
       for (int c = 0; c < kKeys / 32; ++c) {
         uint32_t hv[16], lv[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           float x0, x1;
-          ptx::f2_unpack(ptx::f2_sub(ptx::f2_pack(v[32 * c + 2 * i], v[32 * c + 2 * i + 1]), nb),
-                         x0, x1);
+          ptx::f2_unpack(
+              ptx::f2_fma(ptx::f2_pack(v[32 * c + 2 * i], v[32 * c + 2 * i + 1]), sc2, nb), x0,
+              x1);
           const uint64_t e = ptx::f2_pack(fast_exp2(x0), fast_exp2(x1));
           l2 = ptx::f2_add(l2, e);
           ptx::split_bf16x2(e, hv[i], lv[i]);
