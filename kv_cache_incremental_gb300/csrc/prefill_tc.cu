@@ -72,10 +72,16 @@ struct TcCfg {
   // then per tile P as 32 columns of bf16 pairs for the high part and 32 for the low
   // part, in the columns that held that tile's S) and one D-column O accumulator.
   static constexpr int kTmemCols = TQ == 2 ? 512 : 256;        // [S0 S1] [O0] [O1] or [S0] [O0]
+  // With one query tile the columns left after [S0][O0] (64 at D = 64) hold P of the
+  // block's second 64-key tile, so that QK of the next block, which overwrites S0, waits
+  // only for the PV of the first tile's P and for the softmax to have read the second
+  // tile's S.
+  static constexpr bool kSpareP1 = TQ == 1 && kBlockKeys + D + kKeys <= kTmemCols;
+  static constexpr int kColP1 = kBlockKeys + D;
   static constexpr int kOff_Q = 0;
   static constexpr int kOff_KV = kOff_Q + kTilesQ * kQBytes;
   static constexpr int kOff_Bar = kOff_KV + kStages * kStageBytes;
-  static constexpr int kBars = 3 * kStages + kTilesQ * 5 + 1;
+  static constexpr int kBars = 3 * kStages + kTilesQ * 6 + 1;
   static constexpr int kSmem = 1024 + kOff_Bar + kBars * 8 + 32;
   static_assert(kSmem <= 232448, "shared memory per CTA");
   static_assert(kTilesQ * kBlockKeys + kTilesQ * D <= kTmemCols, "TMEM columns");
@@ -170,9 +176,10 @@ __global__ void __launch_bounds__(Roles<TQ>::kThreads, TQ == 1 ? 2 : 1)
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::kOff_Bar);
   uint64_t *kv_full = bars;                       // [kStages] TMA -> MMA and softmax
   uint64_t *kv_empty = kv_full + kStages;         // [kStages] every MMA of the stage done
-  // Per query tile, one phase per K/V block.  The S buffer of a block is overwritten by
-  // the next block's QK only after this block's PV is done, so no waiter can fall two
-  // phases behind.
+  // Per query tile, one phase per K/V block.  Every barrier's phases are waited for in
+  // block order, and no phase can complete before its predecessor has been waited for,
+  // so no parity wait is ever two phases ahead or behind (the argument is given at each
+  // wait whose predecessor is not waited for by the same thread).
   // With one query tile, S buffer i (i = block parity) uses s_full[i] and p_full[2i + h].
   uint64_t *s_full = kv_empty + kStages;          // [tile] QK done -> softmax
   uint64_t *p_full = s_full + kTilesQ;            // [tile][half] softmax wrote P -> MMA
@@ -180,6 +187,7 @@ __global__ void __launch_bounds__(Roles<TQ>::kThreads, TQ == 1 ? 2 : 1)
   uint64_t *pv_done = pv0_done + kTilesQ;         // [tile] PV done -> MMA, softmax
   uint64_t *v_ready = pv_done + kTilesQ;          // [stage] tile 0 zeroed V -> MMA of tile 1
   uint64_t *drain = v_ready + kStages;            // [1] every MMA done (teardown)
+  uint64_t *s1_read = drain + 1;                  // [tile] softmax read S of tile 1 -> MMA
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + Cfg::kBars);
   volatile int *fail = reinterpret_cast<volatile int *>(tmem_slot + 1);
   volatile int *issued = fail + 1;
@@ -233,6 +241,7 @@ __global__ void __launch_bounds__(Roles<TQ>::kThreads, TQ == 1 ? 2 : 1)
       ptx::mbar_init(&p_full[2 * qt + 1], kSoftmaxWarps);
       ptx::mbar_init(&pv0_done[qt], 1);
       ptx::mbar_init(&pv_done[qt], 1);
+      ptx::mbar_init(&s1_read[qt], kSoftmaxWarps);
     }
     for (int s = 0; s < kStages; ++s) ptx::mbar_init(&v_ready[s], kSoftmaxWarps);
     ptx::mbar_init(drain, n_qt);
@@ -345,10 +354,10 @@ __global__ void __launch_bounds__(Roles<TQ>::kThreads, TQ == 1 ? 2 : 1)
       // query tile, buffer b & 1 (phase b >> 1).
       auto sbuf = [&](int b) { return dbl ? (b & 1) : qt; };
       auto sphase = [&](int b) -> uint32_t { return dbl ? (b >> 1) & 1 : b & 1; };
-      // QK(b): S of block b into its S buffer, once the K/V stage has landed.  The PV that
-      // last read P out of that buffer (PV(b - 1), or PV(b - 2) when double-buffered) was
-      // issued before by this thread: successive tcgen05.mma of one thread execute in issue
-      // order, so the overwrite follows its reads with no wait.  A block with one tile
+      // QK(b): S of block b into its S buffer, once the K/V stage has landed.  The caller
+      // has waited for the PV that last read P out of that buffer: tcgen05.mma operations
+      // are ordered only among those with the same accumulator and shape, so a QK issued
+      // behind a PV could overwrite P before the PV has read it.  A block with one tile
       // still multiplies all 128 rows of its K stage; the softmax masks the absent half.
       auto issue_qk = [&](int b) -> bool {
         if (!ptx::mbar_wait(&kv_full[b % kStages], (b / kStages) & 1, kWaitLimit)) return false;
@@ -374,8 +383,12 @@ __global__ void __launch_bounds__(Roles<TQ>::kThreads, TQ == 1 ? 2 : 1)
       };
       // PV(b): O += P V over the block's tiles.  B = V as stored by TMA: rows = keys (K),
       // 64-dim panels (MN) kPanelBytes apart; A = P of tile h in S-buffer columns
-      // 64h + [0, 32) (high part) and 64h + [32, 64) (low part), 16 keys = 8 columns.
+      // 64h + [0, 32) (high part) and 64h + [32, 64) (low part), 16 keys = 8 columns (tile
+      // 1 in the spare columns kColP1 + [0, 64) when there are any).
       // The softmax publishes P per tile, so PV of tile 0 runs while it computes tile 1.
+      // With the spare columns, QK(b + 1) is issued between the block's two PVs, once the
+      // softmax has read tile 1's S and PV of tile 0 has finished, so that it runs while
+      // the softmax computes tile 1.
       // Query tile 1 reads V of a partial block only after tile 0's softmax zeroed the
       // rows past the segment's end (v_ready, one barrier per stage: tile 0 cannot get
       // kStages blocks ahead of this PV, whose stage it would need, so it cannot lap it).
@@ -391,22 +404,33 @@ __global__ void __launch_bounds__(Roles<TQ>::kThreads, TQ == 1 ? 2 : 1)
         for (int h = 0; h < halves; ++h) {
           if (!ptx::mbar_wait(&p_full[2 * sbuf(b) + h], sphase(b), kWaitLimit)) return false;
           tc::fence_after();
+          const uint32_t tP = Cfg::kSpareP1 && h == 1 ? tmem + Cfg::kColP1 : tS + kKeys * h;
 #pragma unroll
           for (int ks = 0; ks < kKeys / 16; ++ks) {
             const uint64_t bd = tc::desc_sw128_mn(v_addr + h * Cfg::kHalfBytes + ks * 16 * 128,
                                                   Cfg::kPanelBytes, 1024);
-            tc::mma_ts(tO, (tS + kKeys * h) + 8 * ks, bd, kIdPV, b > 0 || h > 0 || ks > 0);
-            tc::mma_ts(tO, (tS + kKeys * h) + kKeys / 2 + 8 * ks, bd, kIdPV, true);
+            tc::mma_ts(tO, tP + 8 * ks, bd, kIdPV, b > 0 || h > 0 || ks > 0);
+            tc::mma_ts(tO, tP + kKeys / 2 + 8 * ks, bd, kIdPV, true);
           }
-          if (h == 0) tc::commit(&pv0_done[qt]);
+          if (h == 0) {
+            tc::commit(&pv0_done[qt]);
+            // (s1_read and pv0_done: this thread waited for phase b - 1 of each in block
+            // b - 1, which had two tiles since block b follows it)
+            if (Cfg::kSpareP1 && halves == 2 && b + 1 < n_blocks &&
+                !(ptx::mbar_wait(&s1_read[qt], b & 1, kWaitLimit) &&
+                  ptx::mbar_wait(&pv0_done[qt], b & 1, kWaitLimit) && issue_qk(b + 1)))
+              return false;
+          }
         }
         tc::commit(&pv_done[qt]);
         tc::commit(&kv_empty[b % kStages]);  // this tile's MMAs of the stage issued
         return true;
       };
       if (n_blocks > 0) {  // (a key split past this CTA's last tile has no work)
-        // PV(b - 1) is issued before QK(b + 1) waits for it (double-buffered), and QK(b + 1)
-        // is issued before PV(b) waits for the softmax of block b, so it overlaps that.
+        // Double-buffered, QK(b + 1) goes into the buffer PV(b - 1) read, once that has
+        // finished, and is issued before PV(b) waits for the softmax of block b, so it
+        // overlaps that.  Otherwise QK(b + 1) waits for PV(b), or, with the spare columns,
+        // is issued inside PV(b).
         bool ok = issue_qk(0);
         for (int b = 0; ok && b < n_blocks; ++b) {
           if (*fail) {
@@ -414,9 +438,16 @@ __global__ void __launch_bounds__(Roles<TQ>::kThreads, TQ == 1 ? 2 : 1)
             break;
           }
           if (dbl)
-            ok = (b + 1 >= n_blocks || issue_qk(b + 1)) && issue_pv(b);
+            ok = (b + 1 >= n_blocks ||
+                  ((b < 1 || ptx::mbar_wait(&pv_done[qt], (b - 1) & 1, kWaitLimit)) &&
+                   issue_qk(b + 1))) &&
+                 issue_pv(b);
+          else if (Cfg::kSpareP1)
+            ok = issue_pv(b);
           else
-            ok = issue_pv(b) && (b + 1 >= n_blocks || issue_qk(b + 1));
+            ok = issue_pv(b) &&
+                 (b + 1 >= n_blocks ||
+                  (ptx::mbar_wait(&pv_done[qt], b & 1, kWaitLimit) && issue_qk(b + 1)));
         }
         if (!ok) {
           atomicExch(p.err, 1);
@@ -488,9 +519,10 @@ __global__ void __launch_bounds__(Roles<TQ>::kThreads, TQ == 1 ? 2 : 1)
       for (int i = 0; i < kKeys; ++i) v[i] = masked(m, i, v[i]);
       return max64(v);
     };
-    // P = 2^(s - m) of tile h as bf16 high + low parts over its S columns: keys 2i, 2i+1
-    // of the high part in column 64h + i, of the low part in column 64h + 32 + i.  The
-    // row sum is kept in two packed lanes.
+    // P = 2^(s - m) of tile h as bf16 high + low parts over its S columns (tile 1: the
+    // spare columns, when there are any): keys 2i, 2i+1 of the high part in column
+    // 64h + i, of the low part in column 64h + 32 + i.  The row sum is kept in two packed
+    // lanes.
     uint64_t l2 = ptx::f2_pack(0.f, 0.f);
     auto store_p = [&](int h, const float (&v)[kKeys]) {
       const float base = m_used == -INFINITY ? 0.f : m_used;
@@ -498,6 +530,7 @@ __global__ void __launch_bounds__(Roles<TQ>::kThreads, TQ == 1 ? 2 : 1)
       // x = s * scale - m for a raw tile, s - m for a scaled one (one packed FMA per pair)
       const float sc = raw ? scale : 1.f;
       const uint64_t sc2 = ptx::f2_pack(sc, sc);
+      const uint32_t tP = Cfg::kSpareP1 && h == 1 ? tmem + Cfg::kColP1 + lane_off : tS + kKeys * h;
 #pragma unroll
       for (int c = 0; c < kKeys / 32; ++c) {
         uint32_t hv[16], lv[16];
@@ -511,8 +544,8 @@ __global__ void __launch_bounds__(Roles<TQ>::kThreads, TQ == 1 ? 2 : 1)
           l2 = ptx::f2_add(l2, e);
           ptx::split_bf16x2(e, hv[i], lv[i]);
         }
-        tc::st16(tS + kKeys * h + 16 * c, hv);
-        tc::st16(tS + kKeys * h + kKeys / 2 + 16 * c, lv);
+        tc::st16(tP + 16 * c, hv);
+        tc::st16(tP + kKeys / 2 + 16 * c, lv);
       }
     };
     // Lazy rescale to the tile maximum mt (log2 units): O and l are multiplied by
@@ -610,16 +643,33 @@ __global__ void __launch_bounds__(Roles<TQ>::kThreads, TQ == 1 ? 2 : 1)
       float sv[kKeys];
 #pragma unroll 1
       for (int h = 0; h < halves; ++h) {
-        // Tile 0: S of this block implies PV(b-1) finished (the QK waited for it), so O is
-        // final.  Tile 1: a new maximum rescales O after PV of tile 0 (already issued) is
-        // done; with S double-buffered, PV(b - 1) was issued after QK(b) and may still run,
-        // so its phase is waited for first (a parity wait must not be two phases ahead).
-        if (!rescale_to(load_tile(j0 + h, h, sv), [&] {
+        // A new maximum rescales O once every PV issued so far has finished: PV(b - 1),
+        // which may still run when S is double-buffered or the spare columns are used, and
+        // for tile 1 PV of tile 0.  Its phases are waited for in order, so a parity wait is
+        // never two phases ahead.
+        const float mt = load_tile(j0 + h, h, sv);
+        if (Cfg::kSpareP1 && h == 1) {  // S of this block may now be overwritten
+          tc::fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&s1_read[qt]);
+        }
+        if (!rescale_to(mt, [&] {
               return (b < 1 || ptx::mbar_wait(&pv_done[qt], (b - 1) & 1, kWaitLimit)) &&
                      (h == 0 || ptx::mbar_wait(&pv0_done[qt], b & 1, kWaitLimit));
             })) {
           ok = false;
           break;
+        }
+        // The spare columns still hold P of block b - 1 until its PV has finished (QK of
+        // this block was issued before that PV).  Phase b - 2 was waited for here in block
+        // b - 1, so this wait is not two phases ahead.
+        if (Cfg::kSpareP1 && h == 1 && b > 0) {
+          if (!__all_sync(0xffffffffu,
+                          ptx::mbar_wait(&pv_done[qt], (b - 1) & 1, kWaitLimit))) {
+            ok = false;
+            break;
+          }
+          tc::fence_after();
         }
         store_p(h, sv);
         publish(h);
@@ -629,12 +679,13 @@ __global__ void __launch_bounds__(Roles<TQ>::kThreads, TQ == 1 ? 2 : 1)
     ptx::f2_unpack(l2, l0, l1);
     const float l_run = l0 + l1;
     // The last PV's completion implies every earlier MMA of the issuing thread is done.
-    // Double-buffered, PV(n_blocks - 2) may still run here, so pv_done may be two phases
-    // behind, or already done with both: wait on the one-phase drain barrier instead.
+    // Double-buffered or with the spare columns, PV(n_blocks - 2) may still run here, so
+    // pv_done may be two phases behind, or already done with both: wait on the one-phase
+    // drain barrier instead.
     const bool last_done =
         ok && n_blocks > 0 &&
-        (dbl ? ptx::mbar_wait(drain, 0, kWaitLimit)
-             : ptx::mbar_wait(&pv_done[qt], (n_blocks - 1) & 1, kWaitLimit));
+        (dbl || Cfg::kSpareP1 ? ptx::mbar_wait(drain, 0, kWaitLimit)
+                              : ptx::mbar_wait(&pv_done[qt], (n_blocks - 1) & 1, kWaitLimit));
     if (!ok) {
       atomicExch(p.err, 1);
       *fail = 1;
