@@ -118,17 +118,24 @@ int kv_cache_create(kv_cache **out, int B, int max_len, int Hq, int Hk, int D, i
  * n_blocks blocks of 16 positions (bf16 [Hk][n_blocks][16][D]: head-major, so that a
  * row's consecutive blocks are contiguous per head) and each row a table of the
  * blocks that hold its positions 16i..16i+15, shared by all global layers (a row has
- * the same length on all of them) ("Lab 07 -- KV cache and sampling", Going further:
+ * the same length on all of them) ("Lab 07 -- KV cache and sampling", Stretch:
  * fixed 16-token blocks plus a per-sequence block table; "tinyllm/kv_cache.py": a
  * dense cache reserves max_len slots per row whatever its length).  Blocks are taken
  * from the pool when a call appends positions past a row's last block (kv_append,
- * kv_append_host, kv_step_graph_launch, kv_copy_rows, kv_import_row) and returned on
- * kv_reset or when a copy shortens a row.  A call whose rows need more blocks than
- * are free returns KV_ERR_POOL before anything is enqueued.  Sliding layers keep their
- * dense rings.  Results are those of the dense cache, bit for bit.  1 <= n_blocks,
- * n_blocks * Hk * 16 < 2^31; with n_blocks >= B * ceil(max_len / 16) no call runs
- * out of blocks.  The pool is reused on the caller's stream order: one stream per
- * cache.
+ * kv_append_host, kv_step_graph_launch, kv_copy_rows, kv_import_row) and let go of on
+ * kv_reset or when a copy shortens or replaces a row.  Blocks are reference-counted
+ * (same page, Stretch: prefix sharing): kv_copy_rows inside one paged cache gives the
+ * destination row the source row's full blocks of the kept prefix instead of copies,
+ * and a block returns to the pool when the last row holding it lets go.  A block held
+ * by several rows lies below each holder's length, so no append writes it; a row cut in
+ * place inside such a block first takes a copy of it, and kv_import_row and copies from
+ * another cache give the row blocks of its own.  kv_get_block_table shows the sharing
+ * (equal block ids) and kv_free_blocks the memory it saves.  A call whose rows need
+ * more blocks than are free returns KV_ERR_POOL before anything is enqueued.  Sliding
+ * layers keep their dense rings.  Results are those of the dense cache, bit for bit.
+ * 1 <= n_blocks, n_blocks * Hk * 16 < 2^31; with n_blocks >= B * ceil(max_len / 16)
+ * no call runs out of blocks.  The pool is reused on the caller's stream order: one
+ * stream per cache.
  */
 int kv_cache_create_paged(kv_cache **out, int B, int max_len, int Hq, int Hk, int D, int W,
                           int n_layers, const int32_t *layer_kind, double rope_theta, int device,
@@ -420,7 +427,9 @@ void kv_step_graph_destroy(kv_step_graph *g);
  *
  * kv_copy_rows: for i < n, destination row dst_rows[i] of `dst` becomes the first
  *   keep[i] tokens of source row src_rows[i] of `src` (keep == NULL: the source's
- *   whole length): its K/V, ring state (lpos) and length.  Uses: forking a sequence
+ *   whole length): its K/V, ring state (lpos) and length.  Inside one paged cache the
+ *   global layers' full blocks of the prefix are shared with the source row, not
+ *   copied (see kv_cache_create_paged); only a partly filled last block is copied.  Uses: forking a sequence
  *   into another row, reusing a shared prompt prefix, truncating a row (src == dst,
  *   same row), and moving rows into a cache with another max_len or B (grow-with-
  *   copy).  dst and src may be the same cache.  Both caches must have the same Hk, D,

@@ -12,6 +12,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <memory>
+#include <unordered_map>
 #include <vector>
 
 #include "../../include/kvinc.h"
@@ -145,6 +146,10 @@ struct kv_cache {
   int32_t *table = nullptr;                   // device [B][max_blocks]
   std::vector<std::vector<int32_t>> rblocks;  // host: pool blocks of each row, in order
   std::vector<int32_t> free_blocks;           // host: free pool blocks
+  // host: per pool block, the rows whose tables hold it (0: free).  A block held by
+  // several rows (a shared prompt prefix) lies below every holder's length, so no append
+  // writes it.
+  std::vector<int32_t> refs;
   // hybrid full layers: per row, lens + the tokens of its last append in this step (a
   // local layer of the group may only append the same tokens after it)
   std::vector<std::vector<int32_t>> hy_end;
@@ -187,6 +192,19 @@ PageTable page_table(const kv_cache *c, int layer) {
 
 int blocks_for(int len) { return (len + kBlockTokens - 1) / kBlockTokens; }
 
+// A free pool block, now held by one row (the caller has checked that one is free).
+int take_block(kv_cache *c) {
+  const int blk = c->free_blocks.back();
+  c->free_blocks.pop_back();
+  c->refs[blk] = 1;
+  return blk;
+}
+
+// One row lets go of `blk`; the last one returns it to the pool.
+void drop_block(kv_cache *c, int blk) {
+  if (--c->refs[blk] == 0) c->free_blocks.push_back(blk);
+}
+
 // Give each (row, length) of `want` the pool blocks its first `length` positions need, and
 // write the new table entries on `s`.  All or nothing: KV_ERR_POOL before any change if the
 // pool cannot supply every row.
@@ -203,8 +221,7 @@ int ensure_blocks(kv_cache *c, const std::vector<std::pair<int, int>> &want, cud
   for (auto &w : want) {
     auto &rb = c->rblocks[w.first];
     while ((int)rb.size() < blocks_for(w.second)) {
-      const int blk = c->free_blocks.back();
-      c->free_blocks.pop_back();
+      const int blk = take_block(c);
       tp.row[tp.n] = w.first;
       tp.idx[tp.n] = (int)rb.size();
       tp.blk[tp.n] = blk;
@@ -222,12 +239,13 @@ int ensure_blocks(kv_cache *c, const std::vector<std::pair<int, int>> &want, cud
   return launch_table(tp, s) == cudaSuccess ? KV_OK : KV_ERR_CUDA;
 }
 
-// Return the blocks of `row` past its first `len` positions to the pool.
+// Let go of the blocks of `row` past its first `len` positions (the pool gets back those
+// no other row holds).
 void release_blocks(kv_cache *c, int row, int len) {
   if (c->n_blocks == 0) return;
   auto &rb = c->rblocks[row];
   while ((int)rb.size() > blocks_for(len)) {
-    c->free_blocks.push_back(rb.back());
+    drop_block(c, rb.back());
     rb.pop_back();
   }
 }
@@ -922,6 +940,7 @@ static int create_impl(kv_cache **out, int B, int max_len, int Hq, int Hk, int D
     c->max_blocks = (blocks_for(max_len) + 3) / 4 * 4;
     if (!alloc((void **)&c->table, (size_t)B * c->max_blocks * 4)) return fail(KV_ERR_OOM);
     c->rblocks.assign(B, {});
+    c->refs.assign(n_blocks, 0);
     for (int b = n_blocks - 1; b >= 0; --b) c->free_blocks.push_back(b);
   }
   int group_full = -1;
@@ -1846,6 +1865,38 @@ bool same_layout(const kv_cache *a, const kv_cache *b) {
          a->kind == b->kind && a->theta == b->theta && a->device == b->device;
 }
 
+// Table entry (row, idx) = blk, written on `s` in batches of kMaxTableEntries.
+int put_entry(kv_cache *c, TableParams &tp, int row, int idx, int blk, cudaStream_t s) {
+  tp.row[tp.n] = row;
+  tp.idx[tp.n] = idx;
+  tp.blk[tp.n] = blk;
+  if (++tp.n < kMaxTableEntries) return KV_OK;
+  c->last_stream = s;
+  c->last_kind = -1;
+  tp.n = 0;
+  return launch_table(tp, s) == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+}
+
+// Copy item for positions [p0, p1) of one pool block to another (paged unit u): both
+// sides addressed as a dense [Hk][16][D] block inside the head-major pool.
+CopyItem block_item(const kv_cache *c, const Unit &u, int from, int to, int p0, int p1) {
+  CopyItem it;
+  const int64_t blk_elems = (int64_t)kBlockTokens * c->D;
+  const int64_t hs = (int64_t)c->n_blocks * blk_elems;
+  it.src_k = (const __nv_bfloat16 *)c->K[u.layer] + from * blk_elems;
+  it.src_v = (const __nv_bfloat16 *)c->V[u.layer] + from * blk_elems;
+  it.dst_k = (__nv_bfloat16 *)c->K[u.layer] + to * blk_elems;
+  it.dst_v = (__nv_bfloat16 *)c->V[u.layer] + to * blk_elems;
+  it.src_head_stride = it.dst_head_stride = hs;
+  it.src_table = it.dst_table = nullptr;
+  it.src_pool = it.dst_pool = 0;
+  it.p0 = p0;
+  it.p1 = p1;
+  it.src_ring = it.dst_ring = 0;
+  it.src_base = it.dst_base = (p0 / kBlockTokens) * kBlockTokens;
+  return it;
+}
+
 }  // namespace
 
 extern "C" {
@@ -1871,20 +1922,91 @@ int kv_copy_rows(kv_cache *dst, const int32_t *dst_rows, const kv_cache *src,
   if (n == 0) return KV_OK;
   DeviceGuard guard(dst->device);
   cudaStream_t s = (cudaStream_t)stream;
-  {  // destination blocks for [0, keep) (all or nothing, before any copy is enqueued)
-    std::vector<std::pair<int, int>> want;
-    for (int i = 0; i < n; ++i) want.push_back({dst_rows[i], kp[i]});
-    const int rc = ensure_blocks(dst, want, s);
-    if (rc != KV_OK) return rc;
+  const bool paged = dst->n_blocks > 0;
+  const bool share = paged && dst == src;  // forks inside one paged cache share blocks
+  auto in_place = [&](int i) { return dst == src && dst_rows[i] == src_rows[i]; };
+  if (paged) {
+    // Blocks this call takes against those it frees, all or nothing before anything is
+    // enqueued.  Each destination row lets go of its blocks (past keep, when it is cut in
+    // place).  A fork inside the cache then holds the source's full blocks of the prefix
+    // and takes one block for a partly filled last one; a row cut in place inside a block
+    // that other rows hold takes a copy of it; a copy from another cache takes fresh
+    // blocks.  (A block a source row holds is never freed here: no source row is another
+    // pair's destination.)
+    std::unordered_map<int32_t, int32_t> drops;
+    int64_t take = 0;
+    for (int i = 0; i < n; ++i) {
+      const auto &rb = dst->rblocks[dst_rows[i]];
+      const int k = kp[i];
+      for (size_t x = in_place(i) ? blocks_for(k) : 0; x < rb.size(); ++x) ++drops[rb[x]];
+      if (in_place(i))
+        take += k % kBlockTokens != 0 && dst->refs[rb[k / kBlockTokens]] > 1;
+      else
+        take += share ? (k % kBlockTokens != 0) : blocks_for(k);
+    }
+    int64_t freed = 0;
+    for (const auto &e : drops) freed += dst->refs[e.first] == e.second;
+    if (take > (int64_t)dst->free_blocks.size() + freed) return KV_ERR_POOL;
   }
   static thread_local CopyParams cp;
   cp.Hk = dst->Hk;
   cp.D = dst->D;
   cp.n_items = 0;
   const std::vector<Unit> us = units(dst);  // the same for src (same layout)
+  auto paged_unit = [&](const Unit &u) { return paged && !u.hring && paged_layer(dst, u.layer); };
+  std::vector<CopyItem> block_copies;  // partly filled blocks a row now holds alone
+  if (paged) {
+    static thread_local TableParams tp;
+    tp.table = dst->table;
+    tp.max_blocks = dst->max_blocks;
+    tp.n = 0;
+    int rc = KV_OK;
+    for (int i = 0; i < n; ++i) release_blocks(dst, dst_rows[i], in_place(i) ? kp[i] : 0);
+    for (int i = 0; i < n && rc == KV_OK; ++i) {
+      const int d = dst_rows[i], k = kp[i], last = k / kBlockTokens;
+      auto &rb = dst->rblocks[d];
+      if (in_place(i)) {
+        if (k % kBlockTokens == 0 || dst->refs[rb[last]] == 1) continue;
+        const int old = rb[last], nb = take_block(dst);
+        drop_block(dst, old);  // still held by another row
+        rb[last] = nb;
+        for (const Unit &u : us)
+          if (paged_unit(u)) block_copies.push_back(block_item(dst, u, old, nb, last * kBlockTokens, k));
+        rc = put_entry(dst, tp, d, last, nb, s);
+      } else if (share) {
+        const auto &sb = dst->rblocks[src_rows[i]];
+        for (int x = 0; x < last && rc == KV_OK; ++x) {
+          ++dst->refs[sb[x]];
+          rb.push_back(sb[x]);
+          rc = put_entry(dst, tp, d, x, sb[x], s);
+        }
+        if (k % kBlockTokens == 0 || rc != KV_OK) continue;
+        const int nb = take_block(dst);
+        rb.push_back(nb);
+        for (const Unit &u : us)
+          if (paged_unit(u)) block_copies.push_back(block_item(dst, u, sb[last], nb, last * kBlockTokens, k));
+        rc = put_entry(dst, tp, d, last, nb, s);
+      }
+    }
+    if (rc == KV_OK && tp.n > 0) {
+      dst->last_stream = s;
+      dst->last_kind = -1;
+      rc = launch_table(tp, s) == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+    }
+    if (rc != KV_OK) return rc;
+  }
+  if (!share) {  // fresh destination blocks for [0, keep) (checked above: cannot run out)
+    std::vector<std::pair<int, int>> want;
+    for (int i = 0; i < n; ++i) want.push_back({dst_rows[i], kp[i]});
+    const int rc = ensure_blocks(dst, want, s);
+    if (rc != KV_OK) return rc;
+  }
+  for (const CopyItem &it : block_copies)
+    if (add_copy(cp, it, s) != KV_OK) return KV_ERR_CUDA;
   for (int i = 0; i < n; ++i) {
-    if (dst == src && dst_rows[i] == src_rows[i]) continue;  // the row keeps its own slots
+    if (in_place(i)) continue;  // the row keeps its own slots
     for (const Unit &u : us) {
+      if (share && paged_unit(u)) continue;  // held, or copied block by block above
       CopyItem it;
       __nv_bfloat16 *sk, *sv;
       row_block(src, u, src_rows[i], sk, sv, it.src_head_stride, it.src_table, it.src_pool);
@@ -2004,6 +2126,12 @@ int kv_import_row(kv_cache *c, int row, int keep, const void *src, int64_t bytes
   if (keep < 0 || keep > c->max_len || bytes != kv_export_bytes(c, keep)) return KV_ERR_ARG;
   DeviceGuard guard(c->device);
   cudaStream_t s = (cudaStream_t)stream;
+  if (c->n_blocks > 0) {  // the row lets go of its blocks and writes fresh ones of its own
+    int64_t avail = (int64_t)c->free_blocks.size();
+    for (int b : c->rblocks[row]) avail += c->refs[b] == 1;
+    if (blocks_for(keep) > avail) return KV_ERR_POOL;
+    release_blocks(c, row, 0);
+  }
   int rc = ensure_blocks(c, {{row, keep}}, s);
   if (rc != KV_OK) return rc;
   rc = export_import(c, row, keep, const_cast<void *>(src), bytes, s, false);

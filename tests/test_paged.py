@@ -2,8 +2,8 @@
 
 The same scenarios as the dense parity tests run on paged caches against the oracle
 (outputs within tolerance, cache contents, ring state and lens bit for bit), a paged
-and a dense cache fed the same inputs agree bit for bit, and pool exhaustion is
-refused without any change.
+and a dense cache fed the same inputs agree bit for bit, pool exhaustion is refused
+without any change, and forks inside a paged cache share the prefix's blocks.
 """
 import numpy as np
 import pytest
@@ -145,3 +145,88 @@ def test_paged_step_graph_and_copies():
     assert p.cache.lens[3] == 110 and len(p.cache.block_table(3)) == 7
     gd.close()
     gp.close()
+
+
+def _pool_accounting(sc):
+    """Every pool block is free or held by some row, never both; a block that several rows
+    hold lies below each holder's length (no append can write it)."""
+    tables = [sc.cache.block_table(r) for r in range(sc.B)]
+    held = {}
+    for r, t in enumerate(tables):
+        assert len(t) == (sc.lens[r] + 15) // 16
+        for i, blk in enumerate(t):
+            held.setdefault(blk, []).append((r, i))
+    assert len(held) + sc.cache.free_blocks == sc.cache.paged_blocks
+    for blk, holders in held.items():
+        if len(holders) > 1:
+            assert all(16 * (i + 1) <= sc.lens[r] for r, i in holders), (blk, holders)
+    return tables
+
+
+def test_shared_prefix_blocks_like_the_oracle():
+    """Prefix sharing with reference-counted blocks ("Lab 07 -- KV cache and sampling",
+    Stretch: prompts with the same 32-token system prompt share its blocks).  Forks inside
+    one paged cache hold the source's full blocks of the prefix -- equal block ids, the pool
+    giving only a partly filled last block -- and every row then decodes and prefills its
+    own continuation like the oracle.  A row cut in place inside a block other rows hold
+    takes a copy of it first; resets and imports let go of shared blocks, which return to
+    the pool with their last holder."""
+    sc = Scenario(B=6, max_len=256, Hq=8, Hk=2, D=64, W=128, kinds=[0, 1, 0], seed=81,
+                  paged_blocks=64)   # (rings that do not wrap: any prefix can be copied)
+    sc.step([40, 0, 0, 0, 0, 0], C=40, check=False)        # row 0: a 40-token prompt
+    t0 = sc.cache.block_table(0)
+    free = sc.cache.free_blocks
+    # rows 1 and 2: its 32-token system prompt (two full blocks); row 3: all 40 tokens
+    sc.copy_rows(sc, src_rows=[0, 0, 0], dst_rows=[1, 2, 3], keep=[32, 32, 40])
+    tables = _pool_accounting(sc)
+    assert tables[1] == tables[2] == t0[:2]
+    assert tables[3][:2] == t0[:2] and tables[3][2] != t0[2]
+    assert sc.cache.free_blocks == free - 1               # 8 blocks of prompts, 4 in the pool
+    sc.check_state()
+    for _ in range(2):
+        sc.step([1, 1, 1, 1, 0, 0], check_state=True)
+    sc.step([5, 17, 3, 30, 0, 0], C=30, check_state=True)  # into blocks of their own
+    tables = _pool_accounting(sc)
+    assert all(tables[r][:2] == t0[:2] for r in (1, 2, 3))
+    # row 0 cut to 20 tokens in place: its second block, held by rows 1-3 too, is copied
+    sc.copy_rows(sc, src_rows=[0], dst_rows=[0], keep=[20])
+    tables = _pool_accounting(sc)
+    assert tables[0][0] == t0[0] and tables[0][1] != t0[1]
+    assert all(tables[r][1] == t0[1] for r in (1, 2, 3))
+    sc.check_state()
+    sc.step([12, 1, 1, 1, 0, 0], C=12, check_state=True)
+    # a fork of a fork, then resets and an import over shared rows
+    sc.copy_rows(sc, src_rows=[3], dst_rows=[4], keep=[33])
+    tables = _pool_accounting(sc)
+    assert tables[4][:2] == t0[:2]
+    free = sc.cache.free_blocks
+    own = len(tables[1]) - 2 + len(tables[2]) - 2
+    sc.step([0, 0, 0, 0, 0, 0], resets=[1, 2], check=False)
+    assert sc.cache.free_blocks == free + own            # t0[:2] still held by rows 3, 4
+    sc.import_row(3, sc.cache.export_row(4), keep=33, src=sc, src_row=4)
+    tables = _pool_accounting(sc)
+    assert not set(tables[3]) & set(tables[4])           # an import writes blocks of its own
+    sc.check_state()
+    sc.step([3, 2, 1, 1, 1, 4], C=4, check_state=True)
+    sc.step([0, 0, 0, 0, 0, 0], resets=[0, 1, 2, 3, 4, 5], check=False)
+    _pool_accounting(sc)
+    assert sc.cache.free_blocks == 64
+
+
+def test_shared_prefix_memory_saved():
+    """The pool memory prefix sharing saves: eight requests with a common 32-token system
+    prompt hold its two blocks once instead of eight times, and a fork of a 100-token row
+    takes one block (its partly filled last one) instead of seven."""
+    sc = Scenario(B=9, max_len=256, Hq=8, Hk=2, D=64, kinds=[0, 0], seed=82, paged_blocks=64)
+    sc.step([32] + [0] * 8, C=32, check=False)             # the system prompt, in row 0
+    free = sc.cache.free_blocks
+    sc.copy_rows(sc, src_rows=[0] * 8, dst_rows=list(range(1, 9)))
+    assert sc.cache.free_blocks == free                   # 8 x 2 blocks held, none taken
+    sc.step([0] + [20] * 8, C=20, check_state=True)        # each request's own continuation
+    used = 64 - sc.cache.free_blocks
+    copied = sum((sc.lens[r] + 15) // 16 for r in range(9))
+    assert (used, copied) == (2 + 8 * 2, 2 + 8 * 4)       # 18 blocks held instead of 34
+    block_bytes = 2 * 2 * sc.Hk * 16 * sc.D * 2            # 2 layers x (K, V) x [Hk][16][D] bf16
+    assert (copied - used) * block_bytes == 16 * 16384
+    sc.copy_rows(sc, src_rows=[1], dst_rows=[0], keep=[52])  # 52 = 3 full blocks + 4
+    assert 64 - sc.cache.free_blocks == used + 1           # row 0's old blocks: still held

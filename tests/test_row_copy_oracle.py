@@ -127,7 +127,7 @@ def test_paged_copies_and_import_like_the_oracle():
 
 def test_paged_truncation_and_prefix_like_the_oracle():
     """Global layers only (no ring, so any prefix is present): truncation gives blocks back,
-    prefixes share no blocks, and the rows then grow into fresh blocks."""
+    a prefix shares the source's full blocks, and the rows then grow into fresh blocks."""
     p = Scenario(B=3, max_len=256, Hq=8, Hk=2, D=128, kinds=[0, 0], seed=73, paged_blocks=40)
     p.step([100, 37, 0], C=100, check=False)
     free = p.cache.free_blocks
