@@ -359,7 +359,7 @@ int kv_profile_read(kv_cache *c, int kind, int reset, int64_t *launches, double 
  * node when the cache has sliding layers) and replayed per step.  The pages keep
  * the step's shapes fixed so that a captured graph can be replayed, and advance
  * the host's lengths after each replay ("tinyllm/kv_cache.py" (tiny-llm):
- * end_step / advance_host; "Lab 07 -- KV cache and sampling", Going further:
+ * end_step / advance_host; "Lab 07 -- KV cache and sampling", Stretch:
  * static shapes for CUDA graphs).  Here positions live in each kernel's
  * parameters, so every launch re-plans the step from the host lengths, updates the
  * nodes' parameters and grid sizes in the instantiated graph, replays it on the
@@ -423,7 +423,7 @@ void kv_step_graph_destroy(kv_step_graph *g);
  * ring is copied position by position and a global prefix linearly ("inkling:
  * ring-buffer KV cache for sliding-window layers", review of the change: prefix reuse
  * by grow-with-copy must copy the ring whole, keeping t % win valid, and global rows
- * linearly; "Lab 07 -- KV cache and sampling", Going further: prefix sharing).
+ * linearly; "Lab 07 -- KV cache and sampling", Stretch: prefix sharing).
  *
  * kv_copy_rows: for i < n, destination row dst_rows[i] of `dst` becomes the first
  *   keep[i] tokens of source row src_rows[i] of `src` (keep == NULL: the source's
