@@ -1953,7 +1953,9 @@ int kv_copy_rows(kv_cache *dst, const int32_t *dst_rows, const kv_cache *src,
   cp.D = dst->D;
   cp.n_items = 0;
   const std::vector<Unit> us = units(dst);  // the same for src (same layout)
-  auto paged_unit = [&](const Unit &u) { return paged && !u.hring && paged_layer(dst, u.layer); };
+  auto paged_unit = [&](const Unit &u) {
+    return paged && !u.hring && paged_layer(dst, u.layer);
+  };
   std::vector<CopyItem> block_copies;  // partly filled blocks a row now holds alone
   if (paged) {
     static thread_local TableParams tp;
@@ -1971,7 +1973,8 @@ int kv_copy_rows(kv_cache *dst, const int32_t *dst_rows, const kv_cache *src,
         drop_block(dst, old);  // still held by another row
         rb[last] = nb;
         for (const Unit &u : us)
-          if (paged_unit(u)) block_copies.push_back(block_item(dst, u, old, nb, last * kBlockTokens, k));
+          if (paged_unit(u))
+            block_copies.push_back(block_item(dst, u, old, nb, last * kBlockTokens, k));
         rc = put_entry(dst, tp, d, last, nb, s);
       } else if (share) {
         const auto &sb = dst->rblocks[src_rows[i]];
@@ -1984,7 +1987,8 @@ int kv_copy_rows(kv_cache *dst, const int32_t *dst_rows, const kv_cache *src,
         const int nb = take_block(dst);
         rb.push_back(nb);
         for (const Unit &u : us)
-          if (paged_unit(u)) block_copies.push_back(block_item(dst, u, sb[last], nb, last * kBlockTokens, k));
+          if (paged_unit(u))
+            block_copies.push_back(block_item(dst, u, sb[last], nb, last * kBlockTokens, k));
         rc = put_entry(dst, tp, d, last, nb, s);
       }
     }

@@ -81,7 +81,7 @@ struct TcCfg {
   static constexpr int kOff_Q = 0;
   static constexpr int kOff_KV = kOff_Q + kTilesQ * kQBytes;
   static constexpr int kOff_Bar = kOff_KV + kStages * kStageBytes;
-  static constexpr int kBars = 3 * kStages + kTilesQ * 6 + 1;
+  static constexpr int kBars = 3 * kStages + kTilesQ * 7 + 1;
   static constexpr int kSmem = 1024 + kOff_Bar + kBars * 8 + 32;
   static_assert(kSmem <= 232448, "shared memory per CTA");
   static_assert(kTilesQ * kBlockKeys + kTilesQ * D <= kTmemCols, "TMEM columns");
@@ -188,6 +188,7 @@ __global__ void __launch_bounds__(Roles<TQ>::kThreads, TQ == 1 ? 2 : 1)
   uint64_t *v_ready = pv_done + kTilesQ;          // [stage] tile 0 zeroed V -> MMA of tile 1
   uint64_t *drain = v_ready + kStages;            // [1] every MMA done (teardown)
   uint64_t *s1_read = drain + 1;                  // [tile] softmax read S of tile 1 -> MMA
+  uint64_t *q_ready = s1_read + kTilesQ;          // [tile] rotated Q tile stored -> MMA
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + Cfg::kBars);
   volatile int *fail = reinterpret_cast<volatile int *>(tmem_slot + 1);
   volatile int *issued = fail + 1;
@@ -242,6 +243,7 @@ __global__ void __launch_bounds__(Roles<TQ>::kThreads, TQ == 1 ? 2 : 1)
       ptx::mbar_init(&pv0_done[qt], 1);
       ptx::mbar_init(&pv_done[qt], 1);
       ptx::mbar_init(&s1_read[qt], kSoftmaxWarps);
+      ptx::mbar_init(&q_ready[qt], kSoftmaxWarps);
     }
     for (int s = 0; s < kStages; ++s) ptx::mbar_init(&v_ready[s], kSoftmaxWarps);
     ptx::mbar_init(drain, n_qt);
@@ -250,45 +252,11 @@ __global__ void __launch_bounds__(Roles<TQ>::kThreads, TQ == 1 ? 2 : 1)
     ptx::fence_barrier_init();
   }
   if (warp == kMmaWarp) tc::alloc(tmem_slot, Cfg::kTmemCols);
-  const int qt_me = warp / kSoftmaxWarps;  // query tile of a softmax warp
-  if (warp < kProducerWarp) {
-    // Rotated query of this thread's row into its tile's 128-byte-swizzled Q tile.
-    const int r = threadIdx.x % kRows;
-    const int rho = rho0 + qt_me * kRows + r;
-    const bool valid = rho < n_rho;
-    const int t = valid ? rho / p.rep : 0, h = valid ? rho % p.rep : 0;
-    const __nv_bfloat16 *q = p.q + (int64_t)row.call_row * p.q_row_stride +
-                             ((int64_t)t * p.Hq + g * p.rep + h) * D;
-    const float2 *cs = p.rope + (int64_t)(lens + t) * kHalf;
-    uint8_t *qtile = qsm + qt_me * Cfg::kQBytes;
-#pragma unroll 2
-    for (int c = 0; c < kHalf / 8; ++c) {
-      uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
-      if (valid) {
-        const uint4 x1v = *reinterpret_cast<const uint4 *>(q + 8 * c);
-        const uint4 x2v = *reinterpret_cast<const uint4 *>(q + kHalf + 8 * c);
-        const __nv_bfloat16 *x1 = reinterpret_cast<const __nv_bfloat16 *>(&x1v);
-        const __nv_bfloat16 *x2 = reinterpret_cast<const __nv_bfloat16 *>(&x2v);
-        __nv_bfloat16 *o1 = reinterpret_cast<__nv_bfloat16 *>(&lo);
-        __nv_bfloat16 *o2 = reinterpret_cast<__nv_bfloat16 *>(&hi);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float a = __bfloat162float(x1[j]), b = __bfloat162float(x2[j]);
-          const float2 e = cs[8 * c + j];
-          o1[j] = __float2bfloat16_rn(__fsub_rn(__fmul_rn(a, e.x), __fmul_rn(b, e.y)));
-          o2[j] = __float2bfloat16_rn(__fadd_rn(__fmul_rn(a, e.y), __fmul_rn(b, e.x)));
-        }
-      }
-      const int c_lo = c, c_hi = kHalf / 8 + c;  // 16-byte chunk index along D
-      *reinterpret_cast<uint4 *>(qtile + (c_lo / 8) * kRows * 128 + ptx::swz128(r, c_lo % 8)) = lo;
-      *reinterpret_cast<uint4 *>(qtile + (c_hi / 8) * kRows * 128 + ptx::swz128(r, c_hi % 8)) = hi;
-    }
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // Q -> tensor core
-  }
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
   const uint32_t tmem = *tmem_slot;
+  const int qt_me = warp / kSoftmaxWarps;  // query tile of a softmax warp
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ TMA producer
@@ -431,7 +399,7 @@ __global__ void __launch_bounds__(Roles<TQ>::kThreads, TQ == 1 ? 2 : 1)
         // finished, and is issued before PV(b) waits for the softmax of block b, so it
         // overlaps that.  Otherwise QK(b + 1) waits for PV(b), or, with the spare columns,
         // is issued inside PV(b).
-        bool ok = issue_qk(0);
+        bool ok = ptx::mbar_wait(&q_ready[qt], 0, kWaitLimit) && issue_qk(0);
         for (int b = 0; ok && b < n_blocks; ++b) {
           if (*fail) {
             ok = false;
@@ -460,6 +428,44 @@ __global__ void __launch_bounds__(Roles<TQ>::kThreads, TQ == 1 ? 2 : 1)
     }
   } else if (qt_me < n_qt) {
     // ------------------------------------------------------------ softmax warps
+    {  // Rotated query of this thread's row into its tile's 128-byte-swizzled Q tile,
+       // while the producer already streams K/V (the query may sit in host memory).
+      const int r = threadIdx.x % kRows;
+      const int rho = rho0 + qt_me * kRows + r;
+      const bool valid = rho < n_rho;
+      const int t = valid ? rho / p.rep : 0, h = valid ? rho % p.rep : 0;
+      const __nv_bfloat16 *q = p.q + (int64_t)row.call_row * p.q_row_stride +
+                               ((int64_t)t * p.Hq + g * p.rep + h) * D;
+      const float2 *cs = p.rope + (int64_t)(lens + t) * kHalf;
+      uint8_t *qtile = qsm + qt_me * Cfg::kQBytes;
+#pragma unroll 2
+      for (int c = 0; c < kHalf / 8; ++c) {
+        uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
+        if (valid) {
+          const uint4 x1v = *reinterpret_cast<const uint4 *>(q + 8 * c);
+          const uint4 x2v = *reinterpret_cast<const uint4 *>(q + kHalf + 8 * c);
+          const __nv_bfloat16 *x1 = reinterpret_cast<const __nv_bfloat16 *>(&x1v);
+          const __nv_bfloat16 *x2 = reinterpret_cast<const __nv_bfloat16 *>(&x2v);
+          __nv_bfloat16 *o1 = reinterpret_cast<__nv_bfloat16 *>(&lo);
+          __nv_bfloat16 *o2 = reinterpret_cast<__nv_bfloat16 *>(&hi);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float a = __bfloat162float(x1[j]), b = __bfloat162float(x2[j]);
+            const float2 e = cs[8 * c + j];
+            o1[j] = __float2bfloat16_rn(__fsub_rn(__fmul_rn(a, e.x), __fmul_rn(b, e.y)));
+            o2[j] = __float2bfloat16_rn(__fadd_rn(__fmul_rn(a, e.y), __fmul_rn(b, e.x)));
+          }
+        }
+        const int c_lo = c, c_hi = kHalf / 8 + c;  // 16-byte chunk index along D
+        *reinterpret_cast<uint4 *>(qtile + (c_lo / 8) * kRows * 128 +
+                                   ptx::swz128(r, c_lo % 8)) = lo;
+        *reinterpret_cast<uint4 *>(qtile + (c_hi / 8) * kRows * 128 +
+                                   ptx::swz128(r, c_hi % 8)) = hi;
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // Q -> tensor core
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&q_ready[qt_me]);
+    }
     const int qt = qt_me;
     const int r = threadIdx.x % kRows;  // query row of this thread = TMEM lane
     const int rho = rho0 + qt * kRows + r;
