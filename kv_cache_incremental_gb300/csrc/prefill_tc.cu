@@ -608,6 +608,13 @@ __global__ void __launch_bounds__(Roles<TQ>::kThreads, TQ == 1 ? 2 : 1)
       return 1;
     };
     int buf = qt;  // S buffer (and barrier index) of the current block
+    // A warp whose 32 rows are all past the CTA's last query row (a part-filled tile) computes
+    // nothing: PV reads its lanes' P (stale or zero), which only reach O rows that are never
+    // stored, and its sub-partition's issue slots and exponent unit go to the other warps on
+    // it.  It still waits for S before each arrival, so it never arrives for a later phase.
+    // Only in the one-tile kernel, whose short chunk rows leave tiles part-filled: the
+    // two-tile kernel's fills have none, and the branch costs them 1-2%.
+    const bool warp_idle = kTilesQ == 1 && rho0 + qt * kRows + 32 * (warp % 4) >= n_rho;
     auto publish = [&](int h) {
       tc::wait_st();
       tc::fence_before();
@@ -646,6 +653,24 @@ __global__ void __launch_bounds__(Roles<TQ>::kThreads, TQ == 1 ? 2 : 1)
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&v_ready[b % kStages]);
       }
+      if (warp_idle) {  // its rows' P reaches no output: only the barriers' arrivals
+#pragma unroll 1
+        for (int h = 0; h < halves && ok; ++h) {
+          if (Cfg::kSpareP1 && h == 1) {
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&s1_read[qt]);
+            // With the spare columns S of this block can land before the other warps have
+            // published tile 1's P of block b - 1; arriving now could complete that phase.
+            // PV(b - 1) having finished shows it is complete (the wait the other warps make
+            // before writing P into the spare columns).
+            ok = b < 1 || __all_sync(0xffffffffu,
+                                     ptx::mbar_wait(&pv_done[qt], (b - 1) & 1, kWaitLimit));
+            if (!ok) break;
+          }
+          publish(h);
+        }
+        continue;
+      }
       float sv[kKeys];
 #pragma unroll 1
       for (int h = 0; h < halves; ++h) {
@@ -681,70 +706,78 @@ __global__ void __launch_bounds__(Roles<TQ>::kThreads, TQ == 1 ? 2 : 1)
         publish(h);
       }
     }
-    float l0, l1;
-    ptx::f2_unpack(l2, l0, l1);
-    const float l_run = l0 + l1;
-    // The last PV's completion implies every earlier MMA of the issuing thread is done.
-    // Double-buffered or with the spare columns, PV(n_blocks - 2) may still run here, so
-    // pv_done may be two phases behind, or already done with both: wait on the one-phase
-    // drain barrier instead.
-    const bool last_done =
-        ok && n_blocks > 0 &&
-        (dbl || Cfg::kSpareP1 ? ptx::mbar_wait(drain, 0, kWaitLimit)
-                              : ptx::mbar_wait(&pv_done[qt], (n_blocks - 1) & 1, kWaitLimit));
-    if (!ok) {
-      atomicExch(p.err, 1);
-      *fail = 1;
-    } else if (row.part >= 0 && (n_blocks == 0 || __all_sync(0xffffffffu, last_done))) {
-      // A key split: this row's unnormalised O, its maximum (log2 units) and sum.
-      if (n_blocks > 0) tc::fence_after();
-      const int64_t vec = (int64_t)row.part + (int64_t)g * n_rho + rho;
-      float4 *po = reinterpret_cast<float4 *>(p.part_o + vec * D);
+    if (warp_idle) {
+      if (!ok) {
+        atomicExch(p.err, 1);
+        *fail = 1;
+      }
+    } else {
+      float l0, l1;
+      ptx::f2_unpack(l2, l0, l1);
+      const float l_run = l0 + l1;
+      // The last PV's completion implies every earlier MMA of the issuing thread is done.
+      // Double-buffered or with the spare columns, PV(n_blocks - 2) may still run here, so
+      // pv_done may be two phases behind, or already done with both: wait on the one-phase
+      // drain barrier instead.
+      const bool last_done =
+          ok && n_blocks > 0 &&
+          (dbl || Cfg::kSpareP1 ? ptx::mbar_wait(drain, 0, kWaitLimit)
+                                : ptx::mbar_wait(&pv_done[qt], (n_blocks - 1) & 1, kWaitLimit));
+      if (!ok) {
+        atomicExch(p.err, 1);
+        *fail = 1;
+      } else if (row.part >= 0 && (n_blocks == 0 || __all_sync(0xffffffffu, last_done))) {
+        // A key split: this row's unnormalised O, its maximum (log2 units) and sum.
+        if (n_blocks > 0) tc::fence_after();
+        const int64_t vec = (int64_t)row.part + (int64_t)g * n_rho + rho;
+        float4 *po = reinterpret_cast<float4 *>(p.part_o + vec * D);
 #pragma unroll 1  // one 16-column chunk of code (instruction fetch)
-      for (int c = 0; c < D / 16; ++c) {
-        float o16[16];
-        if (n_blocks > 0) {
+        for (int c = 0; c < D / 16; ++c) {
+          float o16[16];
+          if (n_blocks > 0) {
+            tc::ld16(tO + 16 * c, o16);
+            tc::wait_ld();
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) o16[i] = 0.f;
+          }
+          if (qvalid) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              po[4 * c + i] =
+                  make_float4(o16[4 * i], o16[4 * i + 1], o16[4 * i + 2], o16[4 * i + 3]);
+          }
+        }
+        if (qvalid) p.part_ml[vec] = make_float2(m_used, l_run);
+      } else if (__all_sync(0xffffffffu, last_done)) {
+        tc::fence_after();
+        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+        const int t = qvalid ? rho / p.rep : 0, h = qvalid ? rho % p.rep : 0;
+        __nv_bfloat16 *dst = p.out + (int64_t)row.call_row * p.out_row_stride +
+                             ((int64_t)t * p.Hq + g * p.rep + h) * D;
+#pragma unroll 1  // one 16-column chunk of code (instruction fetch)
+        for (int c = 0; c < D / 16; ++c) {
+          float o16[16];
           tc::ld16(tO + 16 * c, o16);
           tc::wait_ld();
-        } else {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) o16[i] = 0.f;
+          uint4 w0, w1;
+          w0.x = ptx::pack_bf16(o16[0] * inv, o16[1] * inv);
+          w0.y = ptx::pack_bf16(o16[2] * inv, o16[3] * inv);
+          w0.z = ptx::pack_bf16(o16[4] * inv, o16[5] * inv);
+          w0.w = ptx::pack_bf16(o16[6] * inv, o16[7] * inv);
+          w1.x = ptx::pack_bf16(o16[8] * inv, o16[9] * inv);
+          w1.y = ptx::pack_bf16(o16[10] * inv, o16[11] * inv);
+          w1.z = ptx::pack_bf16(o16[12] * inv, o16[13] * inv);
+          w1.w = ptx::pack_bf16(o16[14] * inv, o16[15] * inv);
+          if (qvalid) {
+            *reinterpret_cast<uint4 *>(dst + 16 * c) = w0;
+            *reinterpret_cast<uint4 *>(dst + 16 * c + 8) = w1;
+          }
         }
-        if (qvalid) {
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            po[4 * c + i] = make_float4(o16[4 * i], o16[4 * i + 1], o16[4 * i + 2], o16[4 * i + 3]);
-        }
+      } else if (n_blocks > 0) {
+        atomicExch(p.err, 1);
+        *fail = 1;
       }
-      if (qvalid) p.part_ml[vec] = make_float2(m_used, l_run);
-    } else if (__all_sync(0xffffffffu, last_done)) {
-      tc::fence_after();
-      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-      const int t = qvalid ? rho / p.rep : 0, h = qvalid ? rho % p.rep : 0;
-      __nv_bfloat16 *dst = p.out + (int64_t)row.call_row * p.out_row_stride +
-                           ((int64_t)t * p.Hq + g * p.rep + h) * D;
-#pragma unroll 1  // one 16-column chunk of code (instruction fetch)
-      for (int c = 0; c < D / 16; ++c) {
-        float o16[16];
-        tc::ld16(tO + 16 * c, o16);
-        tc::wait_ld();
-        uint4 w0, w1;
-        w0.x = ptx::pack_bf16(o16[0] * inv, o16[1] * inv);
-        w0.y = ptx::pack_bf16(o16[2] * inv, o16[3] * inv);
-        w0.z = ptx::pack_bf16(o16[4] * inv, o16[5] * inv);
-        w0.w = ptx::pack_bf16(o16[6] * inv, o16[7] * inv);
-        w1.x = ptx::pack_bf16(o16[8] * inv, o16[9] * inv);
-        w1.y = ptx::pack_bf16(o16[10] * inv, o16[11] * inv);
-        w1.z = ptx::pack_bf16(o16[12] * inv, o16[13] * inv);
-        w1.w = ptx::pack_bf16(o16[14] * inv, o16[15] * inv);
-        if (qvalid) {
-          *reinterpret_cast<uint4 *>(dst + 16 * c) = w0;
-          *reinterpret_cast<uint4 *>(dst + 16 * c + 8) = w1;
-        }
-      }
-    } else if (n_blocks > 0) {
-      atomicExch(p.err, 1);
-      *fail = 1;
     }
   }
 
