@@ -498,17 +498,19 @@ __global__ void __launch_bounds__(Roles<TQ>::kThreads, TQ == 1 ? 2 : 1)
                   (m.kb >= m.r2 && m.kb + kKeys - 1 <= m.r3);
       return m;
     };
-    // (bitwise tests: no per-element branches)
     const float scale = p.scale_log2;
-    auto masked = [&](const TileMask &m, int i, float x) {
-      const int kidx = m.kb + i;
-      const bool vis = ((kidx >= m.r0) & (kidx <= m.r1)) | ((kidx >= m.r2) & (kidx <= m.r3));
-      return vis ? x * scale : -INFINITY;
+    // Bits lo..hi of a 64-key tile (clamped to the tile; none when lo > hi).
+    auto range_bits = [](int lo, int hi) -> uint64_t {
+      lo = max(lo, 0);
+      hi = min(hi, kKeys - 1);
+      if (lo > hi) return 0ull;
+      const uint64_t upto = hi == 63 ? ~0ull : (2ull << hi) - 1ull;
+      return upto & ~((1ull << lo) - 1ull);
     };
-    // S of tile h of the block (64 columns) into v; returns its maximum in log2 units.  A
-    // tile entirely visible stays unscaled (raw = true: the scale goes into the exponent's
-    // FMA); any other is masked and scaled here.
-    bool raw = false;
+    // S of tile h of the block (64 columns) into v, unscaled (the scale goes into the
+    // exponent's FMA), keys the row does not see set to -inf through the tile's visibility
+    // bits (one bit test and one select per key); returns its maximum in log2 units
+    // (scaling by a positive number commutes with max).
     auto load_tile = [&](int j, int h, float (&v)[kKeys]) {
       const TileMask m = tile_mask(j);
 #pragma unroll
@@ -519,11 +521,17 @@ __global__ void __launch_bounds__(Roles<TQ>::kThreads, TQ == 1 ? 2 : 1)
         for (int i = 0; i < 16; ++i) v[16 * c + i] = t16[i];
       }
       tc::wait_ld();
-      raw = m.all_vis;
-      if (raw) return max64(v) * scale;  // scaling by a positive number commutes with max
+      if (!m.all_vis) {
+        const uint64_t bits =
+            range_bits(m.r0 - m.kb, m.r1 - m.kb) | range_bits(m.r2 - m.kb, m.r3 - m.kb);
+        const uint32_t b0 = (uint32_t)bits, b1 = (uint32_t)(bits >> 32);
 #pragma unroll
-      for (int i = 0; i < kKeys; ++i) v[i] = masked(m, i, v[i]);
-      return max64(v);
+        for (int i = 0; i < 32; ++i) {
+          v[i] = (b0 >> i) & 1u ? v[i] : -INFINITY;
+          v[32 + i] = (b1 >> i) & 1u ? v[32 + i] : -INFINITY;
+        }
+      }
+      return max64(v) * scale;
     };
     // P = 2^(s - m) of tile h as bf16 high + low parts over its S columns (tile 1: the
     // spare columns, when there are any): keys 2i, 2i+1 of the high part in column
@@ -533,9 +541,8 @@ __global__ void __launch_bounds__(Roles<TQ>::kThreads, TQ == 1 ? 2 : 1)
     auto store_p = [&](int h, const float (&v)[kKeys]) {
       const float base = m_used == -INFINITY ? 0.f : m_used;
       const uint64_t nb = ptx::f2_pack(-base, -base);
-      // x = s * scale - m for a raw tile, s - m for a scaled one (one packed FMA per pair)
-      const float sc = raw ? scale : 1.f;
-      const uint64_t sc2 = ptx::f2_pack(sc, sc);
+      // x = s * scale - m (one packed FMA per pair)
+      const uint64_t sc2 = ptx::f2_pack(scale, scale);
       const uint32_t tP = Cfg::kSpareP1 && h == 1 ? tmem + Cfg::kColP1 + lane_off : tS + kKeys * h;
 #pragma unroll
       for (int c = 0; c < kKeys / 32; ++c) {
