@@ -19,21 +19,26 @@
 // Warp roles (with two tiles; with one, warps 0-3, 4 and 5):
 //   warps 0-7  softmax, four per query tile: thread i of a tile owns query row i =
 //              TMEM lane i of that tile's accumulators.  They rotate the queries into
-//              shared memory, read S from TMEM, mask, run the online softmax (lazy
-//              rescaling: O in TMEM is rescaled only when a row's maximum grows by
-//              more than 2^8), write P as bf16 high and low parts back into the TMEM
-//              columns that held S, and finally read O from TMEM and normalise.
+//              shared memory (while the producer already streams K/V), read S from TMEM,
+//              mask it through a 64-bit visibility mask per 64-key tile, run the online
+//              softmax (lazy rescaling: O in TMEM is rescaled only when a row's maximum
+//              grows by more than 2^8), write P as bf16 high and low parts back into the
+//              TMEM columns that held S (with one tile, the second 64-key tile's P into
+//              the spare columns), and finally read O from TMEM and normalise.  With one
+//              tile, a warp none of whose rows is a query row only keeps the barriers.
 //   warp 8     TMA producer of the K and V blocks (128-byte swizzle).
 //   warps 9-10 MMA issuers, one thread per query tile (warp 9 also owns TMEM).  Per
 //              block: S = Q K^T (M=128, N=128) into the tile's S buffer, then, once the
 //              softmax wrote P of each 64-key tile, O += P_hi V + P_lo V (M=128, N=D)
 //              with P read from TMEM and V read in place as an MN-major operand (keys are
-//              its K).  QK(b+1) is issued right after PV(b), which reads P from the S
-//              buffer it overwrites: successive tcgen05.mma of one thread execute in
-//              issue order.  The two query tiles' chains run independently.  A two-tile
-//              CTA with a single query tile in use double-buffers S in the other tile's
-//              columns, so QK(b+1) is issued before PV(b) and runs during the softmax of
-//              block b.
+//              its K).  tcgen05.mma operations are ordered only among those with the same
+//              accumulator and shape, so QK(b+1), which overwrites the P that PV(b) reads,
+//              waits for that PV to finish: for all of it with two tiles, for PV of the
+//              first 64-key tile with one (the second tile's P sits in the spare columns),
+//              once the softmax has read S of the second tile.  The two query tiles'
+//              chains run independently.  A two-tile CTA with a single query tile in use
+//              double-buffers S in the other tile's columns, so QK(b+1) (after PV(b - 1))
+//              runs during the softmax of block b.
 // Every mbarrier wait is bounded; on a timeout the CTA records the error, lets its
 // own TMA loads and MMAs finish (bounded), frees its TMEM and returns.
 #include "kvinc_internal.h"
